@@ -1,0 +1,87 @@
+"""Seeded synthetic inputs shaped like the workloads of the NVFP4 linear
+projection (Full-Stack FP4 pages, section 4: a 3B-parameter transformer; the
+pages publish no data, so every tensor here is synthetic).
+
+This module only draws random numbers and rounds them to BF16 storage; it
+holds none of the quantization or GEMM arithmetic.  Both the CUDA path and
+the oracle take their inputs from here, as BF16 bit patterns (numpy uint16),
+so the two sides see identical bytes.
+
+Recipes (all from numpy's PCG64 with an explicit seed):
+  - activations X ~ N(0, 1), or Student-t(df=3) / sqrt(3) (unit variance);
+  - weights W ~ N(0, 0.02^2), optionally with a few columns scaled x20;
+  - gradients dY ~ N(0, (1e-3)^2) (1e-3 read as the standard deviation);
+  - quantize-sweep tensors ~ N(0, 1) with 0.1% of entries scaled x50.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+
+def to_bf16_bits(x_f32: np.ndarray) -> np.ndarray:
+    """Store float32 values as BF16 (round to nearest even); returns uint16 bits."""
+    t = torch.from_numpy(np.ascontiguousarray(x_f32, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def bits_to_torch(u16: np.ndarray, device=None) -> torch.Tensor:
+    """View BF16 bit patterns as a torch.bfloat16 tensor (optionally moved)."""
+    t = torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16)
+    return t.to(device) if device is not None else t
+
+
+def torch_to_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def normal(shape, std: float, seed: int) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    return to_bf16_bits(rng.standard_normal(shape, dtype=np.float32) * np.float32(std))
+
+
+def student_t(shape, df: float, seed: int) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    x = rng.standard_t(df, size=shape).astype(np.float32)
+    if df > 2:
+        x /= np.float32(np.sqrt(df / (df - 2.0)))
+    return to_bf16_bits(x)
+
+
+def with_outlier_entries(shape, frac: float, factor: float, seed: int) -> np.ndarray:
+    """N(0,1) with a seeded fraction of entries multiplied by `factor`."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(shape, dtype=np.float32)
+    n = x.size
+    k = max(1, int(round(frac * n)))
+    idx = rng.choice(n, size=k, replace=False)
+    x.reshape(-1)[idx] *= np.float32(factor)
+    return to_bf16_bits(x)
+
+
+def weight_with_outlier_columns(n_out: int, n_in: int, std: float, n_cols: int,
+                                factor: float, seed: int) -> np.ndarray:
+    """W (n_out x n_in) ~ N(0, std^2) with `n_cols` seeded input-feature columns x factor."""
+    rng = np.random.default_rng(seed)
+    w = rng.standard_normal((n_out, n_in), dtype=np.float32) * np.float32(std)
+    cols = rng.choice(n_in, size=n_cols, replace=False)
+    w[:, cols] *= np.float32(factor)
+    return to_bf16_bits(w)
+
+
+# Workload shapes.  Names describe what each is.
+SINGLE_FWD_256x512x512 = dict(name="single_fwd_256x512x512_r16", M=256, K=512, N=512, r=16,
+                              x="normal", seed=0)
+MLP_UP_1B = dict(name="mlp_up_T8192_d2048_f5632_r32", M=8192, K=2048, N=5632, r=32, seed=1)
+BLOCK_3B_PROJECTIONS = [
+    # (name, N out, K in) for T=16384 tokens, d_model 3072, d_ff 8192
+    ("qkv", 9216, 3072),
+    ("o", 3072, 3072),
+    ("gate_up", 16384, 3072),
+    ("down", 3072, 8192),
+]
+BLOCK_3B = dict(name="block3b_T16384_d3072_ff8192_r64", T=16384, r=64,
+                projections=BLOCK_3B_PROJECTIONS)
+QUANT_SWEEP_ELEMS = [1 << 20, 1 << 24, 1 << 26, 1 << 28]
+GEMM_SWEEP = [(2048, 2048, 2048), (4096, 4096, 4096), (8192, 8192, 8192),
+              (16384, 16384, 16384), (16384, 3072, 8192), (3072, 8192, 16384)]

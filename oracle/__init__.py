@@ -1,0 +1,364 @@
+"""NVFP4 oracle: plain, slow, obviously-correct CPU reference for the NVFP4
+linear-projection hot path of "Full-Stack FP4: Stable LLM Pretraining with
+Quantized Projections, Optimizers, and Attention".
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this package.  It
+shares no code with the CUDA library and never imports it.
+
+The quantizer is plain C (``nvfp4_oracle.c``, FP32 steps with FMA contraction
+off, brute-force rounding); the products are NumPy FP64 matmuls of the exactly
+dequantized operands.  Functions and the passages they follow:
+
+- ``quantize``: NVFP4 block quantization, "standard NVFP4" (section 3, Key
+  contributions) with SR for gradients (SR is named in section 2.2, Q-AdamW).
+  The format itself (E2M1 codes, E4M3 scale per 16 elements, FP32 tensor
+  scale) is not defined on the pages; see the C file for every reading.
+- ``lora_svd_split``: W = W_res + beta * L2 @ L1 (section 2.1, LoRA-SVD linear
+  projections, the "Mechanism" paragraph), initialised by an exact truncated
+  SVD (READING: the pages realign with a randomized SVD; for a one-off split
+  the exact SVD is the plainest choice, and Sigma goes into L2).
+- ``branch_factor``: P = bf16(X @ L^T), the BF16 low-rank branch (section 2.1:
+  the subspace L2 L1 is kept in BF16).  READING: the intermediate P is rounded
+  to BF16 once.
+- ``gemm`` / ``linear_fwd`` / ``linear_bwd``: the three products of a linear
+  layer, Y = X W^T, dX = dY W, dW = dY^T X, with the residual in NVFP4 and the
+  branch in BF16 (section 2.1).  READING: gradients (dY) use SR in both dX and
+  dW; X and W use RTN; beta = 1 unless given.
+
+Parity pins: see ``tests/test_oracle_pins.py``.  The scale layout and the SR
+bit mapping are this library's chosen conventions (parity unpinned by the
+pages; pinned by invariants and brute force).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nvfp4_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+RTN = 0
+SR = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle into ``oracle/liboracle.so`` (gcc, OpenMP)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            i64, u64, u32, f32, f64 = (ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint32,
+                                       ctypes.c_float, ctypes.c_double)
+            L.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+            L.oracle_bf16_to_f32.restype = f32
+            L.oracle_f64_to_bf16_rn.argtypes = [f64]
+            L.oracle_f64_to_bf16_rn.restype = ctypes.c_uint16
+            L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            L.oracle_e4m3_value.restype = f64
+            L.oracle_e4m3_encode_rn_sat.argtypes = [f32]
+            L.oracle_e4m3_encode_rn_sat.restype = ctypes.c_uint8
+            L.oracle_e2m1_value.argtypes = [ctypes.c_uint8]
+            L.oracle_e2m1_value.restype = f64
+            L.oracle_e2m1_rtn.argtypes = [f32]
+            L.oracle_e2m1_rtn.restype = ctypes.c_uint8
+            L.oracle_e2m1_sr.argtypes = [f32, u32]
+            L.oracle_e2m1_sr.restype = ctypes.c_uint8
+            L.oracle_philox4x32_10.argtypes = [P, P, P]
+            L.oracle_philox4x32_10.restype = None
+            L.oracle_sr_bits.argtypes = [u64, u32, u64]
+            L.oracle_sr_bits.restype = u32
+            L.oracle_amax_bf16.argtypes = [P, i64, i64, i64]
+            L.oracle_amax_bf16.restype = f32
+            L.oracle_tensor_scale.argtypes = [f32]
+            L.oracle_tensor_scale.restype = f32
+            for name in ("oracle_quantize_rows", "oracle_quantize_cols"):
+                fn = getattr(L, name)
+                fn.argtypes = [P, i64, i64, i64, ctypes.c_int, u64, u32, f32, P, P]
+                fn.restype = None
+            L.oracle_dequantize.argtypes = [P, P, f32, i64, i64, P]
+            L.oracle_dequantize.restype = None
+            L.oracle_mma_scale_offset.argtypes = [i64, i64, i64]
+            L.oracle_mma_scale_offset.restype = i64
+            L.oracle_mma_scale_bytes.argtypes = [i64, i64]
+            L.oracle_mma_scale_bytes.restype = i64
+            L.oracle_scales_to_mma.argtypes = [P, i64, i64, P]
+            L.oracle_scales_to_mma.restype = None
+            L.oracle_f64_to_bf16_rn_array.argtypes = [P, i64, P]
+            L.oracle_f64_to_bf16_rn_array.restype = None
+            L.oracle_e4m3_encode_array.argtypes = [P, i64, P]
+            L.oracle_e4m3_encode_array.restype = None
+            L.oracle_e2m1_rtn_array.argtypes = [P, i64, P]
+            L.oracle_e2m1_rtn_array.restype = None
+            L.oracle_e2m1_sr_array.argtypes = [P, P, i64, P]
+            L.oracle_e2m1_sr_array.restype = None
+            L.oracle_sr_bits_array.argtypes = [u64, u32, u64, i64, P]
+            L.oracle_sr_bits_array.restype = None
+            L.oracle_max_threads.argtypes = []
+            L.oracle_max_threads.restype = ctypes.c_int
+            L.oracle_set_threads.argtypes = [ctypes.c_int]
+            L.oracle_set_threads.restype = None
+            _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ---------------------------------------------------------------------------
+# scalar / elementwise definitions
+# ---------------------------------------------------------------------------
+
+def bf16_to_f32(u16: np.ndarray) -> np.ndarray:
+    """BF16 bit patterns -> float32 values (exact widening)."""
+    return (np.asarray(u16, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def bf16_rn(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to BF16 (nearest, ties to even); returns bit patterns."""
+    v = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    lib().oracle_f64_to_bf16_rn_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def e4m3_value(b: int) -> float:
+    return lib().oracle_e4m3_value(int(b))
+
+
+def e4m3_encode(v: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    lib().oracle_e4m3_encode_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def e2m1_value(code: int) -> float:
+    return lib().oracle_e2m1_value(int(code))
+
+
+def e2m1_rtn(y: np.ndarray) -> np.ndarray:
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    out = np.empty(y.shape, dtype=np.uint8)
+    lib().oracle_e2m1_rtn_array(_ptr(y), y.size, _ptr(out))
+    return out
+
+
+def e2m1_sr(y: np.ndarray, rnd16: np.ndarray) -> np.ndarray:
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    r = np.ascontiguousarray(rnd16, dtype=np.uint32)
+    assert r.shape == y.shape
+    out = np.empty(y.shape, dtype=np.uint8)
+    lib().oracle_e2m1_sr_array(_ptr(y), _ptr(r), y.size, _ptr(out))
+    return out
+
+
+def philox4x32_10(ctr, key) -> np.ndarray:
+    c = np.ascontiguousarray(ctr, dtype=np.uint32).reshape(4)
+    k = np.ascontiguousarray(key, dtype=np.uint32).reshape(2)
+    out = np.empty(4, dtype=np.uint32)
+    lib().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def sr_bits(seed: int, stream: int, e0: int, n: int) -> np.ndarray:
+    out = np.empty(n, dtype=np.uint32)
+    lib().oracle_sr_bits_array(seed, stream, e0, n, _ptr(out))
+    return out
+
+
+def set_threads(n: int) -> None:
+    lib().oracle_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(lib().oracle_max_threads())
+
+
+# ---------------------------------------------------------------------------
+# quantizer
+# ---------------------------------------------------------------------------
+
+def amax(x_bf16: np.ndarray) -> float:
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    R, C = x.shape
+    return float(lib().oracle_amax_bf16(_ptr(x), R, C, C))
+
+
+def tensor_scale(amax_value: float) -> float:
+    return float(lib().oracle_tensor_scale(float(amax_value)))
+
+
+class QTensor:
+    """Quantized tensor in the oracle's own (row-major) layout.
+
+    codes: uint8 [rows, cols/2], element 2i in the low nibble.
+    scales: uint8 [rows, cols/16] row-major E4M3 bytes.
+    S_t: float32 tensor (decode) scale; amax: the tensor amax it came from.
+    rows/cols describe the quantized (possibly transposed) tensor.
+    """
+
+    def __init__(self, codes, scales, S_t, amax_value, rows, cols):
+        self.codes, self.scales = codes, scales
+        self.S_t, self.amax = float(S_t), float(amax_value)
+        self.rows, self.cols = rows, cols
+
+    def mma_scales(self) -> np.ndarray:
+        return scales_to_mma(self.scales)
+
+    def dequantize(self, rows=None) -> np.ndarray:
+        if rows is None:
+            return dequantize(self.codes, self.scales, self.S_t)
+        rows = np.asarray(rows)
+        return dequantize(np.ascontiguousarray(self.codes[rows]),
+                          np.ascontiguousarray(self.scales[rows]), self.S_t)
+
+
+def quantize(x_bf16: np.ndarray, mode: int = RTN, seed: int = 0, stream: int = 0,
+             transposed: bool = False, amax_value: float | None = None) -> QTensor:
+    """Quantize a BF16 [R, C] tensor (uint16 bit patterns).
+
+    transposed=False: blocks of 16 along C, result is R x C.
+    transposed=True: blocks of 16 along R, result is the C x R tensor.
+    """
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    R, C = x.shape
+    a = amax(x) if amax_value is None else float(np.float32(amax_value))
+    S = tensor_scale(a)
+    if not transposed:
+        assert C % 16 == 0
+        codes = np.zeros((R, C // 2), dtype=np.uint8)
+        scales = np.zeros((R, C // 16), dtype=np.uint8)
+        lib().oracle_quantize_rows(_ptr(x), R, C, C, mode, seed, stream, S, _ptr(codes), _ptr(scales))
+        return QTensor(codes, scales, S, a, R, C)
+    assert R % 16 == 0
+    codes = np.zeros((C, R // 2), dtype=np.uint8)
+    scales = np.zeros((C, R // 16), dtype=np.uint8)
+    lib().oracle_quantize_cols(_ptr(x), R, C, C, mode, seed, stream, S, _ptr(codes), _ptr(scales))
+    return QTensor(codes, scales, S, a, C, R)
+
+
+def dequantize(codes: np.ndarray, scales: np.ndarray, S_t: float) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    R = codes.shape[0]
+    C = codes.shape[1] * 2
+    out = np.empty((R, C), dtype=np.float64)
+    lib().oracle_dequantize(_ptr(codes), _ptr(scales), float(S_t), R, C, _ptr(out))
+    return out
+
+
+def mma_scale_offset(r: int, k: int, kb: int) -> int:
+    return int(lib().oracle_mma_scale_offset(r, k, kb))
+
+
+def mma_scale_bytes(rows: int, kb: int) -> int:
+    return int(lib().oracle_mma_scale_bytes(rows, kb))
+
+
+def scales_to_mma(scales_rowmajor: np.ndarray) -> np.ndarray:
+    s = np.ascontiguousarray(scales_rowmajor, dtype=np.uint8)
+    R, KB = s.shape
+    out = np.empty(mma_scale_bytes(R, KB), dtype=np.uint8)
+    lib().oracle_scales_to_mma(_ptr(s), R, KB, _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# products (FP64 of exactly dequantized operands)
+# ---------------------------------------------------------------------------
+
+def gemm(deqA: np.ndarray, deqB: np.ndarray, P_bf16=None, Q_bf16=None, beta: float = 1.0) -> np.ndarray:
+    """out = A @ B^T (+ beta * P @ Q^T), FP64.  A: M x K, B: N x K, P: M x r, Q: N x r."""
+    out = deqA.astype(np.float64) @ deqB.astype(np.float64).T
+    if P_bf16 is not None and P_bf16.shape[1] > 0:
+        P = bf16_to_f32(P_bf16).astype(np.float64)
+        Q = bf16_to_f32(Q_bf16).astype(np.float64)
+        out += float(beta) * (P @ Q.T)
+    return out
+
+
+def branch_factor(x_bf16: np.ndarray, L_bf16_t: np.ndarray) -> np.ndarray:
+    """P = bf16(X @ L^T) with the product in FP64.  X: M x K, L: r x K."""
+    X = bf16_to_f32(x_bf16).astype(np.float64)
+    L = bf16_to_f32(L_bf16_t).astype(np.float64)
+    return bf16_rn(X @ L.T)
+
+
+def lora_svd_split(W_bf16: np.ndarray, r: int):
+    """Exact truncated SVD split of W (N x K): returns (W_res, L1, L2) as BF16
+    bit patterns with L2 = bf16(U_r Sigma_r) (N x r), L1 = bf16(V_r^T) (r x K),
+    W_res = bf16(W - L2 @ L1) (beta = 1)."""
+    W = bf16_to_f32(W_bf16).astype(np.float64)
+    if r == 0:
+        N, K = W.shape
+        return np.ascontiguousarray(W_bf16), np.zeros((0, K), np.uint16), np.zeros((N, 0), np.uint16)
+    U, S, Vt = np.linalg.svd(W, full_matrices=False)
+    L2 = bf16_rn(U[:, :r] * S[:r])
+    L1 = bf16_rn(Vt[:r, :])
+    low = bf16_to_f32(L2).astype(np.float64) @ bf16_to_f32(L1).astype(np.float64)
+    W_res = bf16_rn(W - low)
+    return W_res, L1, L2
+
+
+def linear_fwd(X, W_res, L1, L2, beta: float = 1.0, out_rows=None):
+    """Y = bf16( deq(Xq) deq(Wq)^T + beta * bf16(X L1^T) L2^T ), returned as FP64
+    before the final rounding (callers round with bf16_rn or compare directly).
+
+    Also returns the quantized operands.  out_rows restricts the product to a
+    subset of output rows (the quantization is always of the full tensors)."""
+    Xq = quantize(X, RTN)
+    Wq = quantize(W_res, RTN)
+    rows = slice(None) if out_rows is None else np.asarray(out_rows)
+    A = Xq.dequantize(None if out_rows is None else rows)
+    B = Wq.dequantize()
+    if L1.shape[0] > 0:
+        P = branch_factor(np.ascontiguousarray(X[rows]), L1)
+        Y = gemm(A, B, P, L2, beta)
+    else:
+        Y = gemm(A, B)
+    return Y, Xq, Wq
+
+
+def linear_bwd(dY, X, W_res, L1, L2, seed: int, beta: float = 1.0, dx_rows=None, dw_rows=None):
+    """dX = deq(SR_row(dY)) deq(RTN_col(W_res))^T + beta * bf16(dY L2) L1  (M x K)
+    dW = deq(SR_col(dY)) deq(RTN_col(X))^T                                 (N x K)
+    SR streams: 0 for the row (dX) operand, 1 for the column (dW) operand."""
+    dYq = quantize(dY, SR, seed=seed, stream=0)
+    WqT = quantize(W_res, RTN, transposed=True)        # K x N
+    dYqT = quantize(dY, SR, seed=seed, stream=1, transposed=True)  # N x M
+    XqT = quantize(X, RTN, transposed=True)             # K x M
+    xr = slice(None) if dx_rows is None else np.asarray(dx_rows)
+    A = dYq.dequantize(None if dx_rows is None else xr)
+    B = WqT.dequantize()
+    if L1.shape[0] > 0:
+        P2 = branch_factor(np.ascontiguousarray(dY[xr]), np.ascontiguousarray(L2.T))
+        dX = gemm(A, B, P2, np.ascontiguousarray(L1.T), beta)
+    else:
+        dX = gemm(A, B)
+    wr = slice(None) if dw_rows is None else np.asarray(dw_rows)
+    dW = gemm(dYqT.dequantize(None if dw_rows is None else wr), XqT.dequantize())
+    return dX, dW, dict(dYq=dYq, WqT=WqT, dYqT=dYqT, XqT=XqT)
