@@ -1,0 +1,184 @@
+/*
+ * nvfp4_gb300.h -- C ABI of the GB300 (sm_103a) NVFP4 linear-projection library.
+ *
+ * What it computes follows "Full-Stack FP4: Stable LLM Pretraining with
+ * Quantized Projections, Optimizers, and Attention" (gist.science explainer):
+ *   - section 1 (Problem statement): NVFP4 tensor-core arithmetic on Blackwell
+ *     for the linear projections of LLM pretraining;
+ *   - section 2.1 (LoRA-SVD linear projections), "Mechanism": the weight is
+ *     W = W_res + beta * L2 L1 with the rank-r subspace L2 L1 kept in BF16 and
+ *     the residual W_res in NVFP4;
+ *   - section 3 (Key contributions): "standard NVFP4" quantization; section 2.2
+ *     names stochastic rounding (SR), used here for gradients.
+ * The pages do not define the NVFP4 encoding; this library reads it as:
+ *   E2M1 element codes (grid +-{0,0.5,1,1.5,2,3,4,6}), one unsigned E4M3 scale
+ *   per 16 contiguous elements, one FP32 tensor scale S_t = amax / 2688;
+ *   s_b = E4M3_rn_satfinite(amax_b / (6 S_t)); d = s_b S_t; y = x * (1/d);
+ *   code = E2M1_rn_satfinite(y) (RTN) or stochastic rounding of y driven by
+ *   16 bits of Philox4x32-10 per element (SR).
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     allocates no device memory.  fp4_tensor and the other structs passed by
+ *     pointer live in HOST memory and are read during the call only.
+ *   - Every call is asynchronous on the caller's stream (cudaStream_t passed as
+ *     void*; NULL = legacy default stream) and returns an fp4_status at once.
+ *     Argument errors are detected on the host before anything is launched.
+ *   - Device-side timeouts (a bounded wait that expired) are recorded in a
+ *     device status word; fp4_check_status() synchronises the stream and reads
+ *     (and clears) it.
+ *   - fp4_last_error() returns a thread-local message for the last failure.
+ *   - BF16 tensors are row-major with a leading dimension (in elements);
+ *     base pointers and row pitches must be 16-byte aligned.
+ *   - Inputs must be finite (no Inf/NaN).
+ */
+#ifndef NVFP4_GB300_H
+#define NVFP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP4_OK = 0,
+    FP4_ERR_INVALID_ARG = 1,       /* null pointer, bad enum, negative size      */
+    FP4_ERR_MISALIGNED = 2,        /* pointer or pitch not 16-byte aligned       */
+    FP4_ERR_UNSUPPORTED_SHAPE = 3, /* shape outside what a kernel supports      */
+    FP4_ERR_CUDA = 4,              /* a CUDA runtime/driver call failed          */
+    FP4_ERR_TIMEOUT = 5,           /* a device-side bounded wait expired         */
+    FP4_ERR_WORKSPACE = 6          /* workspace pointer/size too small           */
+} fp4_status;
+
+typedef enum { FP4_ROUND_RTN = 0, FP4_ROUND_SR = 1 } fp4_round_mode;
+typedef enum { FP4_OUT_BF16 = 0, FP4_OUT_F32 = 1 } fp4_out_dtype;
+
+/* An NVFP4 tensor of logical shape rows x cols, blocks of 16 along cols.
+ *   codes:  rows * cols / 2 bytes, row-major; element 2i of a row sits in the
+ *           low nibble of byte i, element 2i+1 in the high nibble; a code is
+ *           sign << 3 | magnitude index (0..7 over the E2M1 grid).
+ *   scales: fp4_scale_bytes(rows, cols) bytes of UE4M3 block scales in the
+ *           layout the block-scaled tensor-core MMA reads: the [rows][cols/16]
+ *           scale matrix is cut into 128-row x 4-column atoms of 512 bytes,
+ *           atoms ordered by 128-row block then by column group; inside an atom
+ *           scale (r, k) is at byte (r % 32) * 16 + ((r % 128) / 32) * 4 + k % 4.
+ *           Padding bytes (rows or column groups beyond the tensor) are zero.
+ *   scale:  2 floats: scale[0] = S_t (FP32 decode tensor scale), scale[1] = amax.
+ * All three pointers are device pointers, 16-byte aligned. */
+typedef struct {
+    void* codes;
+    void* scales;
+    float* scale;
+    int64_t rows;
+    int64_t cols;
+} fp4_tensor;
+
+/* Bytes of the MMA-layout scale buffer for a rows x cols NVFP4 tensor. */
+int64_t fp4_scale_bytes(int64_t rows, int64_t cols);
+
+/* Tensor amax: *amax_out (device) = max |x| over x[rows][cols] (BF16, pitch ld).
+ * The value is written, not accumulated.  rows >= 1, cols % 8 == 0. */
+fp4_status fp4_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                    float* amax_out, void* stream);
+
+/* Quantize x[rows][cols] (BF16, pitch ld) row-wise: out is rows x cols with
+ * blocks of 16 along cols.  round_mode RTN, or SR with Philox key = seed and
+ * counter stream id `sr_stream`; the SR draw of element (r, c) uses element
+ * index e = r * cols + c.  amax_opt: device pointer to a precomputed amax of
+ * x (or NULL: the call computes it into out->scale[1]).  Requires
+ * cols % 16 == 0; out->rows/cols must equal rows/cols.
+ * Passage: section 3 "standard NVFP4"; section 2.2 (SR). */
+fp4_status fp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                        int round_mode, uint64_t seed, uint32_t sr_stream,
+                        const float* amax_opt, fp4_tensor* out, void* stream);
+
+/* Quantize x[rows][cols] column-wise (blocks of 16 along rows) and emit the
+ * transposed tensor: out is cols x rows, out row c holding source column c.
+ * SR element index is the SOURCE index e = r * cols + c.  Requires rows % 16
+ * == 0 and cols % 16 == 0; out->rows == cols, out->cols == rows.
+ * This is the K-major operand form of x^T needed by dX = dY W and dW = dY^T X
+ * (section 2.1, the backward pass of the projection). */
+fp4_status fp4_quantize_transposed(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                   int round_mode, uint64_t seed, uint32_t sr_stream,
+                                   const float* amax_opt, fp4_tensor* out, void* stream);
+
+/* Both orientations from one read of x: out_row as fp4_quantize (SR stream
+ * sr_stream_row), out_col as fp4_quantize_transposed (SR stream sr_stream_col).
+ * Either output may be NULL. */
+fp4_status fp4_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                             int round_mode, uint64_t seed, uint32_t sr_stream_row,
+                             uint32_t sr_stream_col, const float* amax_opt,
+                             fp4_tensor* out_row, fp4_tensor* out_col, void* stream);
+
+/* Block-scaled NVFP4 GEMM with the fused BF16 low-rank branch:
+ *   C[m][n] = S_tA * S_tB * sum_k A[m][k] B[n][k]  +  beta * sum_j P[m][j] Q[n][j]
+ * A: M x K NVFP4, B: N x K NVFP4 (both blocks along K), P: M x r BF16 (pitch r),
+ * Q: N x r BF16 (pitch r); r in {0, 16, 32, 48, 64} (r = 0: P, Q ignored).
+ * C: M x N, BF16 or FP32 (c_dtype), pitch ldc elements.
+ * Requires M % 128 == 0, N % 128 == 0, K % 64 == 0.
+ * Passage: section 2.1 "Mechanism" (residual in NVFP4, subspace in BF16,
+ * added into the same output). */
+fp4_status fp4_gemm_blockscaled(const fp4_tensor* A, const fp4_tensor* B,
+                                const void* P, const void* Q, int r, float beta,
+                                void* C, int c_dtype, int64_t ldc, void* stream);
+
+/* Low-rank branch factor: P[m][j] = bf16( sum_k X[m][k] L[j][k] ), FP32
+ * accumulation.  X: M x K BF16 (pitch ldx), L: r x K BF16 (pitch K), P: M x r
+ * BF16 (pitch r).  Requires M % 128 == 0, K % 64 == 0, r in {16,32,48,64}.
+ * Forward: P = X L1^T; backward: P' = dY L2 (pass L = L2^T). */
+fp4_status fp4_branch_factor(const void* X, int64_t M, int64_t K, int64_t ldx,
+                             const void* L, int r, void* P, void* stream);
+
+/* Workspace bytes needed by fp4_linear_fwd / fp4_linear_bwd. */
+size_t fp4_linear_fwd_workspace(int64_t M, int64_t N, int64_t K, int r);
+size_t fp4_linear_bwd_workspace(int64_t M, int64_t N, int64_t K, int r);
+
+/* Linear projection forward (section 2.1):
+ *   Y = X W^T = S_tX S_tW Xq Wq^T + beta * bf16(X L1^T) L2^T      (M x N, BF16)
+ * X: M x K BF16 (pitch ldx); Wq: N x K NVFP4 (RTN-quantized W_res, prepared by
+ * the caller, reused across micro-batches); L1: r x K, L2: N x r BF16.
+ * X is quantized RTN in both orientations from one read; the column form
+ * (K x M) is written to xqT_saved (caller-owned) for the dW product of the
+ * backward pass.  ws/ws_bytes: device workspace of at least
+ * fp4_linear_fwd_workspace(M, N, K, r) bytes, 256-byte aligned. */
+fp4_status fp4_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx,
+                          const fp4_tensor* Wq, const void* L1, const void* L2, int r,
+                          float beta, void* Y, int64_t ldy, fp4_tensor* xqT_saved,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* Linear projection backward (section 2.1, backward pass; the subspace
+ * constraint on the factor update is not part of this call):
+ *   dX = S_tdY S_tW dYq WqT^T + beta * bf16(dY L2) L1     (M x K, BF16)
+ *   dW = S_tdY' S_tX dYqT XqT^T                          (N x K, BF16 or FP32)
+ * dY: M x N BF16 (pitch lddy), quantized with SR (seed; Philox stream 0 for
+ * the row form used by dX, stream 1 for the column form used by dW).
+ * WqT: K x N NVFP4 (W_res quantized column-wise, RTN); xqT_saved: K x M from
+ * fp4_linear_fwd.  ws: at least fp4_linear_bwd_workspace(M, N, K, r) bytes. */
+fp4_status fp4_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t lddy,
+                          const fp4_tensor* WqT, const fp4_tensor* xqT_saved,
+                          const void* L1, const void* L2, int r, float beta, uint64_t seed,
+                          void* dX, int64_t lddx, void* dW, int dw_dtype, int64_t lddw,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, then read and clear the device status word.
+ * Returns FP4_ERR_TIMEOUT if any kernel recorded an expired wait. */
+fp4_status fp4_check_status(void* stream);
+
+/* Thread-local text of the last error (never NULL). */
+const char* fp4_last_error(void);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t fp4_launch_count(void);
+
+/* Diagnostic: convert n floats (device) with the quantizer's own E2M1 RTN
+ * routine (codes, one per byte) and E4M3 scale routine (bytes) so tests can
+ * check the conversion conventions against the oracle.  n % 2 == 0. */
+fp4_status fp4_debug_convert(const float* in, int64_t n, uint8_t* e2m1_out,
+                             uint8_t* e4m3_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_GB300_H */

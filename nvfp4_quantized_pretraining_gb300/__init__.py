@@ -1,0 +1,262 @@
+"""Python binding of the GB300 NVFP4 linear-projection library.
+
+Argument marshalling only: every computation runs in the CUDA kernels of
+``libnvfp4_gb300.so`` (built in-tree by ``build.py``); PyTorch provides device
+memory and streams.  Names and semantics follow ``include/nvfp4_gb300.h``.
+There is no CPU fallback: if the library is missing or cannot be loaded,
+importing a call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libnvfp4_gb300.so")
+
+FP4_OK = 0
+FP4_ERR_INVALID_ARG = 1
+FP4_ERR_MISALIGNED = 2
+FP4_ERR_UNSUPPORTED_SHAPE = 3
+FP4_ERR_CUDA = 4
+FP4_ERR_TIMEOUT = 5
+FP4_ERR_WORKSPACE = 6
+STATUS_NAMES = {0: "FP4_OK", 1: "FP4_ERR_INVALID_ARG", 2: "FP4_ERR_MISALIGNED", 3: "FP4_ERR_UNSUPPORTED_SHAPE",
+                4: "FP4_ERR_CUDA", 5: "FP4_ERR_TIMEOUT", 6: "FP4_ERR_WORKSPACE"}
+RTN = 0
+SR = 1
+OUT_BF16 = 0
+OUT_F32 = 1
+
+EXPORTS = ["fp4_scale_bytes", "fp4_amax", "fp4_quantize", "fp4_quantize_transposed", "fp4_quantize_dual",
+           "fp4_gemm_blockscaled", "fp4_branch_factor", "fp4_linear_fwd_workspace", "fp4_linear_bwd_workspace",
+           "fp4_linear_fwd", "fp4_linear_bwd", "fp4_check_status", "fp4_last_error", "fp4_launch_count",
+           "fp4_debug_convert"]
+
+
+class FP4Error(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class CTensor(ctypes.Structure):
+    """Mirror of ``fp4_tensor``."""
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"CUDA library {LIB_PATH} is missing: run nvfp4_quantized_pretraining_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i64, u64, u32, i32, f32 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint32,
+                                  ctypes.c_int, ctypes.c_float)
+    T = ctypes.POINTER(CTensor)
+    sig = {
+        "fp4_scale_bytes": (i64, [i64, i64]),
+        "fp4_amax": (i32, [P, i64, i64, i64, P, P]),
+        "fp4_quantize": (i32, [P, i64, i64, i64, i32, u64, u32, P, T, P]),
+        "fp4_quantize_transposed": (i32, [P, i64, i64, i64, i32, u64, u32, P, T, P]),
+        "fp4_quantize_dual": (i32, [P, i64, i64, i64, i32, u64, u32, u32, P, T, T, P]),
+        "fp4_gemm_blockscaled": (i32, [T, T, P, P, i32, f32, P, i32, i64, P]),
+        "fp4_branch_factor": (i32, [P, i64, i64, i64, P, i32, P, P]),
+        "fp4_linear_fwd_workspace": (ctypes.c_size_t, [i64, i64, i64, i32]),
+        "fp4_linear_bwd_workspace": (ctypes.c_size_t, [i64, i64, i64, i32]),
+        "fp4_linear_fwd": (i32, [P, i64, i64, i64, T, P, P, i32, f32, P, i64, T, P, ctypes.c_size_t, P]),
+        "fp4_linear_bwd": (i32, [P, i64, i64, i64, T, T, P, P, i32, f32, u64, P, i64, P, i32, i64, P,
+                                 ctypes.c_size_t, P]),
+        "fp4_check_status": (i32, [P]),
+        "fp4_last_error": (ctypes.c_char_p, []),
+        "fp4_launch_count": (u64, []),
+        "fp4_debug_convert": (i32, [P, i64, P, P, P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def _check(status: int) -> None:
+    if status != FP4_OK:
+        raise FP4Error(status, lib().fp4_last_error().decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _bf16_2d(x: torch.Tensor, name: str):
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or x.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D CUDA bfloat16 tensor with unit column stride")
+    return x.shape[0], x.shape[1], x.stride(0)
+
+
+def scale_bytes(rows: int, cols: int) -> int:
+    return int(lib().fp4_scale_bytes(rows, cols))
+
+
+@dataclass
+class NVFP4Tensor:
+    """Device buffers of one NVFP4 tensor (rows x cols, blocks of 16 along cols).
+
+    codes: uint8 [rows, cols/2]; scales: uint8 [fp4_scale_bytes] in the MMA
+    layout; scale: float32 [2] = (S_t, amax)."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    scale: torch.Tensor
+    rows: int
+    cols: int
+
+    @staticmethod
+    def empty(rows: int, cols: int, device="cuda") -> "NVFP4Tensor":
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=device)
+        scales = torch.empty(scale_bytes(rows, cols), dtype=torch.uint8, device=device)
+        scale = torch.zeros(2, dtype=torch.float32, device=device)
+        return NVFP4Tensor(codes, scales, scale, rows, cols)
+
+    def c(self) -> CTensor:
+        return CTensor(self.codes.data_ptr(), self.scales.data_ptr(), self.scale.data_ptr(), self.rows, self.cols)
+
+    @property
+    def tensor_scale(self) -> float:
+        return float(self.scale[0])
+
+
+def fp4_amax(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    R, C, ld = _bf16_2d(x, "x")
+    out = torch.empty(1, dtype=torch.float32, device=x.device) if out is None else out
+    _check(lib().fp4_amax(x.data_ptr(), R, C, ld, out.data_ptr(), _stream(stream)))
+    return out
+
+
+def fp4_quantize(x, round_mode=RTN, seed=0, sr_stream=0, amax=None, out=None, stream=None) -> NVFP4Tensor:
+    R, C, ld = _bf16_2d(x, "x")
+    out = NVFP4Tensor.empty(R, C, x.device) if out is None else out
+    ct = out.c()
+    _check(lib().fp4_quantize(x.data_ptr(), R, C, ld, round_mode, seed, sr_stream, _ptr(amax),
+                              ctypes.byref(ct), _stream(stream)))
+    return out
+
+
+def fp4_quantize_transposed(x, round_mode=RTN, seed=0, sr_stream=1, amax=None, out=None, stream=None) -> NVFP4Tensor:
+    R, C, ld = _bf16_2d(x, "x")
+    out = NVFP4Tensor.empty(C, R, x.device) if out is None else out
+    ct = out.c()
+    _check(lib().fp4_quantize_transposed(x.data_ptr(), R, C, ld, round_mode, seed, sr_stream, _ptr(amax),
+                                         ctypes.byref(ct), _stream(stream)))
+    return out
+
+
+def fp4_quantize_dual(x, round_mode=RTN, seed=0, sr_stream_row=0, sr_stream_col=1, amax=None,
+                      out_row=None, out_col=None, stream=None):
+    R, C, ld = _bf16_2d(x, "x")
+    out_row = NVFP4Tensor.empty(R, C, x.device) if out_row is None else out_row
+    out_col = NVFP4Tensor.empty(C, R, x.device) if out_col is None else out_col
+    cr, cc = out_row.c(), out_col.c()
+    _check(lib().fp4_quantize_dual(x.data_ptr(), R, C, ld, round_mode, seed, sr_stream_row, sr_stream_col,
+                                   _ptr(amax), ctypes.byref(cr), ctypes.byref(cc), _stream(stream)))
+    return out_row, out_col
+
+
+def fp4_gemm_blockscaled(A: NVFP4Tensor, B: NVFP4Tensor, P=None, Q=None, beta=1.0, out=None,
+                         out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+    r = 0 if P is None else P.shape[1]
+    if out is None:
+        out = torch.empty((A.rows, B.rows), dtype=out_dtype, device=A.codes.device)
+    c_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    ca, cb = A.c(), B.c()
+    _check(lib().fp4_gemm_blockscaled(ctypes.byref(ca), ctypes.byref(cb), _ptr(P), _ptr(Q), r, float(beta),
+                                      out.data_ptr(), c_dtype, out.stride(0), _stream(stream)))
+    return out
+
+
+def fp4_branch_factor(X: torch.Tensor, L: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+    M, K, ldx = _bf16_2d(X, "X")
+    r = L.shape[0]
+    out = torch.empty((M, r), dtype=torch.bfloat16, device=X.device) if out is None else out
+    _check(lib().fp4_branch_factor(X.data_ptr(), M, K, ldx, L.data_ptr(), r, out.data_ptr(), _stream(stream)))
+    return out
+
+
+def linear_fwd_workspace(M, N, K, r) -> int:
+    return int(lib().fp4_linear_fwd_workspace(M, N, K, r))
+
+
+def linear_bwd_workspace(M, N, K, r) -> int:
+    return int(lib().fp4_linear_bwd_workspace(M, N, K, r))
+
+
+def fp4_linear_fwd(X, Wq: NVFP4Tensor, L1=None, L2=None, beta=1.0, Y=None, xqT_saved=None, workspace=None,
+                   stream=None):
+    """Y = X W^T with W = W_res + beta L2 L1 (Wq = NVFP4 of W_res).  Returns (Y, xqT_saved)."""
+    M, K, ldx = _bf16_2d(X, "X")
+    N = Wq.rows
+    r = 0 if L1 is None else L1.shape[0]
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
+    xqT_saved = NVFP4Tensor.empty(K, M, X.device) if xqT_saved is None else xqT_saved
+    need = linear_fwd_workspace(M, N, K, r)
+    workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=X.device) if workspace is None else workspace
+    cw, cx = Wq.c(), xqT_saved.c()
+    _check(lib().fp4_linear_fwd(X.data_ptr(), M, K, ldx, ctypes.byref(cw), _ptr(L1), _ptr(L2), r, float(beta),
+                                Y.data_ptr(), Y.stride(0), ctypes.byref(cx), workspace.data_ptr(),
+                                workspace.numel(), _stream(stream)))
+    return Y, xqT_saved
+
+
+def fp4_linear_bwd(dY, WqT: NVFP4Tensor, xqT_saved: NVFP4Tensor, L1=None, L2=None, beta=1.0, seed=0,
+                   dX=None, dW=None, dw_dtype=torch.bfloat16, workspace=None, stream=None):
+    """dX = dY W, dW_res = dY^T X.  Returns (dX, dW)."""
+    M, N, lddy = _bf16_2d(dY, "dY")
+    K = WqT.rows
+    r = 0 if L1 is None else L1.shape[0]
+    dX = torch.empty((M, K), dtype=torch.bfloat16, device=dY.device) if dX is None else dX
+    dW = torch.empty((N, K), dtype=dw_dtype, device=dY.device) if dW is None else dW
+    need = linear_bwd_workspace(M, N, K, r)
+    workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dY.device) if workspace is None else workspace
+    cw, cx = WqT.c(), xqT_saved.c()
+    _check(lib().fp4_linear_bwd(dY.data_ptr(), M, N, lddy, ctypes.byref(cw), ctypes.byref(cx), _ptr(L1), _ptr(L2),
+                                r, float(beta), seed, dX.data_ptr(), dX.stride(0), dW.data_ptr(),
+                                OUT_F32 if dW.dtype == torch.float32 else OUT_BF16, dW.stride(0),
+                                workspace.data_ptr(), workspace.numel(), _stream(stream)))
+    return dX, dW
+
+
+def fp4_check_status(stream=None) -> None:
+    _check(lib().fp4_check_status(_stream(stream)))
+
+
+def fp4_last_error() -> str:
+    return lib().fp4_last_error().decode()
+
+
+def fp4_launch_count() -> int:
+    return int(lib().fp4_launch_count())
+
+
+def fp4_debug_convert(x: torch.Tensor, stream=None):
+    n = x.numel()
+    e2m1 = torch.empty(n, dtype=torch.uint8, device=x.device)
+    e4m3 = torch.empty(n, dtype=torch.uint8, device=x.device)
+    _check(lib().fp4_debug_convert(x.data_ptr(), n, e2m1.data_ptr(), e4m3.data_ptr(), _stream(stream)))
+    return e2m1, e4m3

@@ -1,0 +1,376 @@
+// C ABI of the NVFP4 linear-projection library: argument validation, the
+// composition of the linear forward/backward passes, and error reporting.
+// Every entry point is declared (with its contract) in include/nvfp4_gb300.h.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "kernels.h"
+#include "nvfp4_gb300.h"
+
+namespace nvfp4 {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+static thread_local std::string t_err = "no error";
+
+static fp4_status fail(fp4_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+static fp4_status fail(fp4_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return st;
+}
+
+#define CUDA_TRY(expr)                                                                      \
+  do {                                                                                      \
+    cudaError_t e_ = (expr);                                                                \
+    if (e_ != cudaSuccess)                                                                  \
+      return fail(FP4_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_));            \
+  } while (0)
+
+static int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  static std::atomic<int> cache[64];
+  if (dev >= 0 && dev < 64) {
+    int v = cache[dev].load();
+    if (v > 0) return v;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev >= 0 && dev < 64) cache[dev].store(n);
+  return n;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static int64_t scale_bytes(int64_t rows, int64_t cols) {
+  const int64_t kb = cols / 16;
+  return ((rows + 127) / 128) * 128 * ((kb + 3) / 4) * 4;
+}
+static bool scale_padded(int64_t rows, int64_t cols) { return (rows % 128) != 0 || ((cols / 16) % 4) != 0; }
+
+static fp4_status check_tensor(const fp4_tensor* t, const char* name) {
+  if (!t) return fail(FP4_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!t->codes || !t->scales || !t->scale) return fail(FP4_ERR_INVALID_ARG, "%s has a NULL buffer", name);
+  if (!aligned16(t->codes) || !aligned16(t->scales) || (reinterpret_cast<uintptr_t>(t->scale) & 7u))
+    return fail(FP4_ERR_MISALIGNED, "%s buffers must be 16-byte aligned (scale 8-byte)", name);
+  if (t->rows <= 0 || t->cols <= 0 || t->cols % 16 != 0)
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "%s shape %lld x %lld: cols must be a positive multiple of 16", name,
+                (long long)t->rows, (long long)t->cols);
+  return FP4_OK;
+}
+
+static fp4_status check_bf16_input(const void* x, int64_t rows, int64_t cols, int64_t ld, const char* name) {
+  if (!x) return fail(FP4_ERR_INVALID_ARG, "%s is NULL", name);
+  if (rows <= 0 || cols <= 0) return fail(FP4_ERR_INVALID_ARG, "%s has a non-positive size", name);
+  if (ld < cols) return fail(FP4_ERR_INVALID_ARG, "%s: ld %lld < cols %lld", name, (long long)ld, (long long)cols);
+  if (!aligned16(x) || (ld * 2) % 16 != 0)
+    return fail(FP4_ERR_MISALIGNED, "%s: base and row pitch must be 16-byte aligned", name);
+  if (rows * (cols / 8) >= (int64_t(1) << 32) || rows >= (int64_t(1) << 31))
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "%s: tensor too large (%lld x %lld)", name, (long long)rows,
+                (long long)cols);
+  return FP4_OK;
+}
+
+static QOut qout(const fp4_tensor* t) { return QOut{t->codes, t->scales, t->scale}; }
+
+// Quantize in one or both orientations.  amax: precomputed (device) or NULL.
+static fp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld, int round_mode,
+                                uint64_t seed, uint32_t sr_row, uint32_t sr_col, const float* amax_opt,
+                                const fp4_tensor* out_row, const fp4_tensor* out_col, cudaStream_t s) {
+  fp4_status st = check_bf16_input(x, rows, cols, ld, "x");
+  if (st) return st;
+  if (round_mode != FP4_ROUND_RTN && round_mode != FP4_ROUND_SR)
+    return fail(FP4_ERR_INVALID_ARG, "round_mode %d is not RTN (0) or SR (1)", round_mode);
+  if (cols % 16 != 0) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "cols %lld is not a multiple of 16", (long long)cols);
+  if (!out_row && !out_col) return fail(FP4_ERR_INVALID_ARG, "no output tensor");
+  if (out_row) {
+    if ((st = check_tensor(out_row, "out"))) return st;
+    if (out_row->rows != rows || out_row->cols != cols)
+      return fail(FP4_ERR_INVALID_ARG, "out is %lld x %lld, expected %lld x %lld", (long long)out_row->rows,
+                  (long long)out_row->cols, (long long)rows, (long long)cols);
+  }
+  if (out_col) {
+    if (rows % 16 != 0)
+      return fail(FP4_ERR_UNSUPPORTED_SHAPE, "transposed quantization needs rows %% 16 == 0 (rows = %lld)",
+                  (long long)rows);
+    if (rows / 64 >= 65535) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rows %lld too large", (long long)rows);
+    if ((st = check_tensor(out_col, "out_col"))) return st;
+    if (out_col->rows != cols || out_col->cols != rows)
+      return fail(FP4_ERR_INVALID_ARG, "transposed out is %lld x %lld, expected %lld x %lld",
+                  (long long)out_col->rows, (long long)out_col->cols, (long long)cols, (long long)rows);
+  }
+  if (amax_opt && (reinterpret_cast<uintptr_t>(amax_opt) & 3u))
+    return fail(FP4_ERR_MISALIGNED, "amax_opt must be 4-byte aligned");
+  if (out_row && scale_padded(rows, cols))
+    CUDA_TRY(cudaMemsetAsync(out_row->scales, 0, scale_bytes(rows, cols), s));
+  if (out_col && scale_padded(cols, rows))
+    CUDA_TRY(cudaMemsetAsync(out_col->scales, 0, scale_bytes(cols, rows), s));
+  const float* amax = amax_opt;
+  if (!amax) {
+    float* slot = out_row ? &out_row->scale[1] : &out_col->scale[1];
+    CUDA_TRY(launch_amax(x, rows, cols, ld, slot, sm_count(), s));
+    amax = slot;
+  }
+  const bool sr = round_mode == FP4_ROUND_SR;
+  if (out_row && !out_col) {
+    CUDA_TRY(launch_quantize_rows(x, rows, cols, ld, sr, seed, sr_row, amax, out_row->codes, out_row->scales,
+                                  out_row->scale, sm_count(), s));
+  } else {
+    QOut r{}, c{};
+    if (out_row) r = qout(out_row);
+    c = qout(out_col);
+    CUDA_TRY(launch_quantize_dual(x, rows, cols, ld, sr, seed, sr_row, sr_col, amax, out_row ? &r : nullptr, &c, s));
+  }
+  return FP4_OK;
+}
+
+static fp4_status gemm_impl(const fp4_tensor* A, const fp4_tensor* B, const void* P, const void* Q, int r,
+                            float beta, void* C, int c_dtype, int64_t ldc, cudaStream_t s) {
+  fp4_status st;
+  if ((st = check_tensor(A, "A")) || (st = check_tensor(B, "B"))) return st;
+  const int64_t M = A->rows, N = B->rows, K = A->cols;
+  if (B->cols != K) return fail(FP4_ERR_INVALID_ARG, "A is ? x %lld but B is ? x %lld", (long long)K, (long long)B->cols);
+  if (M % 128 || N % 128 || K % 64)
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "GEMM needs M %% 128 == 0, N %% 128 == 0, K %% 64 == 0 (M=%lld N=%lld K=%lld)",
+                (long long)M, (long long)N, (long long)K);
+  if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "GEMM dimension too large");
+  if (r != 0 && r != 16 && r != 32 && r != 48 && r != 64)
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rank r=%d not in {0,16,32,48,64}", r);
+  if (r > 0) {
+    if (!P || !Q) return fail(FP4_ERR_INVALID_ARG, "r > 0 needs P and Q");
+    if (!aligned16(P) || !aligned16(Q)) return fail(FP4_ERR_MISALIGNED, "P and Q must be 16-byte aligned");
+  }
+  if (!C) return fail(FP4_ERR_INVALID_ARG, "C is NULL");
+  if (c_dtype != FP4_OUT_BF16 && c_dtype != FP4_OUT_F32) return fail(FP4_ERR_INVALID_ARG, "bad c_dtype %d", c_dtype);
+  const int esz = c_dtype == FP4_OUT_F32 ? 4 : 2;
+  if (ldc < N) return fail(FP4_ERR_INVALID_ARG, "ldc %lld < N %lld", (long long)ldc, (long long)N);
+  if (!aligned16(C) || (ldc * esz) % 16) return fail(FP4_ERR_MISALIGNED, "C base and row pitch must be 16-byte aligned");
+  GemmArgs g;
+  g.a_codes = A->codes;
+  g.a_scales = A->scales;
+  g.a_scale = A->scale;
+  g.b_codes = B->codes;
+  g.b_scales = B->scales;
+  g.b_scale = B->scale;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.P = P;
+  g.Q = Q;
+  g.r = r;
+  g.beta = beta;
+  g.C = C;
+  g.c_f32 = c_dtype == FP4_OUT_F32;
+  g.ldc = ldc;
+  CUDA_TRY(launch_gemm_nvf4(g, sm_count(), s));
+  return FP4_OK;
+}
+
+static fp4_status branch_impl(const void* X, int64_t M, int64_t K, int64_t ldx, const void* L, int r, void* P,
+                              cudaStream_t s) {
+  fp4_status st = check_bf16_input(X, M, K, ldx, "X");
+  if (st) return st;
+  if (!L || !P) return fail(FP4_ERR_INVALID_ARG, "L and P must be non-NULL");
+  if (!aligned16(L) || !aligned16(P)) return fail(FP4_ERR_MISALIGNED, "L and P must be 16-byte aligned");
+  if (M % 128 || K % 16) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "branch factor needs M %% 128 == 0, K %% 16 == 0");
+  if (r != 16 && r != 32 && r != 48 && r != 64) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rank r=%d not in {16,32,48,64}", r);
+  CUDA_TRY(launch_branch_factor(X, M, K, ldx, L, r, P, sm_count(), s));
+  return FP4_OK;
+}
+
+// Carves a workspace into 256-byte-aligned regions.
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<uint8_t*>(b)) {}
+  void* take(size_t bytes) {
+    void* p = base ? base + off : nullptr;
+    off += round256(bytes);
+    return p;
+  }
+};
+
+static fp4_tensor carve_tensor(Carver& c, int64_t rows, int64_t cols) {
+  fp4_tensor t;
+  t.codes = c.take(static_cast<size_t>(rows * cols / 2));
+  t.scales = c.take(static_cast<size_t>(scale_bytes(rows, cols)));
+  t.scale = static_cast<float*>(c.take(2 * sizeof(float)));
+  t.rows = rows;
+  t.cols = cols;
+  return t;
+}
+
+static size_t fwd_ws(int64_t M, int64_t N, int64_t K, int r, Carver* c, fp4_tensor* xq, void** P) {
+  (void)N;
+  Carver local(nullptr);
+  Carver& cv = c ? *c : local;
+  fp4_tensor t = carve_tensor(cv, M, K);
+  void* p = cv.take(static_cast<size_t>(M) * (r > 0 ? r : 0) * 2);
+  if (xq) *xq = t;
+  if (P) *P = p;
+  return cv.off;
+}
+
+static size_t bwd_ws(int64_t M, int64_t N, int64_t K, int r, Carver* c, fp4_tensor* dyq, fp4_tensor* dyqT, void** P2,
+                     void** L2T, void** L1T) {
+  Carver local(nullptr);
+  Carver& cv = c ? *c : local;
+  fp4_tensor a = carve_tensor(cv, M, N);
+  fp4_tensor b = carve_tensor(cv, N, M);
+  const int rr = r > 0 ? r : 0;
+  void* p = cv.take(static_cast<size_t>(M) * rr * 2);
+  void* l2t = cv.take(static_cast<size_t>(rr) * N * 2);
+  void* l1t = cv.take(static_cast<size_t>(K) * rr * 2);
+  if (dyq) *dyq = a;
+  if (dyqT) *dyqT = b;
+  if (P2) *P2 = p;
+  if (L2T) *L2T = l2t;
+  if (L1T) *L1T = l1t;
+  return cv.off;
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+int64_t fp4_scale_bytes(int64_t rows, int64_t cols) { return scale_bytes(rows, cols); }
+
+fp4_status fp4_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float* amax_out, void* stream) {
+  fp4_status st = check_bf16_input(x, rows, cols, ld, "x");
+  if (st) return st;
+  if (cols % 8) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "amax needs cols %% 8 == 0");
+  if (!amax_out) return fail(FP4_ERR_INVALID_ARG, "amax_out is NULL");
+  CUDA_TRY(launch_amax(x, rows, cols, ld, amax_out, sm_count(), static_cast<cudaStream_t>(stream)));
+  return FP4_OK;
+}
+
+fp4_status fp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int round_mode, uint64_t seed,
+                        uint32_t sr_stream, const float* amax_opt, fp4_tensor* out, void* stream) {
+  if (!out) return fail(FP4_ERR_INVALID_ARG, "out is NULL");
+  return quantize_impl(x, rows, cols, ld, round_mode, seed, sr_stream, 0, amax_opt, out, nullptr,
+                       static_cast<cudaStream_t>(stream));
+}
+
+fp4_status fp4_quantize_transposed(const void* x, int64_t rows, int64_t cols, int64_t ld, int round_mode,
+                                   uint64_t seed, uint32_t sr_stream, const float* amax_opt, fp4_tensor* out,
+                                   void* stream) {
+  if (!out) return fail(FP4_ERR_INVALID_ARG, "out is NULL");
+  return quantize_impl(x, rows, cols, ld, round_mode, seed, 0, sr_stream, amax_opt, nullptr, out,
+                       static_cast<cudaStream_t>(stream));
+}
+
+fp4_status fp4_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, int round_mode, uint64_t seed,
+                             uint32_t sr_stream_row, uint32_t sr_stream_col, const float* amax_opt,
+                             fp4_tensor* out_row, fp4_tensor* out_col, void* stream) {
+  return quantize_impl(x, rows, cols, ld, round_mode, seed, sr_stream_row, sr_stream_col, amax_opt, out_row, out_col,
+                       static_cast<cudaStream_t>(stream));
+}
+
+fp4_status fp4_gemm_blockscaled(const fp4_tensor* A, const fp4_tensor* B, const void* P, const void* Q, int r,
+                                float beta, void* C, int c_dtype, int64_t ldc, void* stream) {
+  return gemm_impl(A, B, P, Q, r, beta, C, c_dtype, ldc, static_cast<cudaStream_t>(stream));
+}
+
+fp4_status fp4_branch_factor(const void* X, int64_t M, int64_t K, int64_t ldx, const void* L, int r, void* P,
+                             void* stream) {
+  return branch_impl(X, M, K, ldx, L, r, P, static_cast<cudaStream_t>(stream));
+}
+
+size_t fp4_linear_fwd_workspace(int64_t M, int64_t N, int64_t K, int r) {
+  return fwd_ws(M, N, K, r, nullptr, nullptr, nullptr);
+}
+
+size_t fp4_linear_bwd_workspace(int64_t M, int64_t N, int64_t K, int r) {
+  return bwd_ws(M, N, K, r, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
+}
+
+fp4_status fp4_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx, const fp4_tensor* Wq, const void* L1,
+                          const void* L2, int r, float beta, void* Y, int64_t ldy, fp4_tensor* xqT_saved, void* ws,
+                          size_t ws_bytes, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  fp4_status st;
+  if ((st = check_bf16_input(X, M, K, ldx, "X"))) return st;
+  if ((st = check_tensor(Wq, "Wq")) || (st = check_tensor(xqT_saved, "xqT_saved"))) return st;
+  if (Wq->cols != K) return fail(FP4_ERR_INVALID_ARG, "Wq has %lld columns, X has K = %lld", (long long)Wq->cols, (long long)K);
+  const int64_t N = Wq->rows;
+  if (xqT_saved->rows != K || xqT_saved->cols != M)
+    return fail(FP4_ERR_INVALID_ARG, "xqT_saved must be K x M (%lld x %lld)", (long long)K, (long long)M);
+  if (M % 128 || N % 128 || K % 64)
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "linear needs M %% 128, N %% 128 == 0 and K %% 64 == 0");
+  if (r > 0 && (!L1 || !L2)) return fail(FP4_ERR_INVALID_ARG, "r > 0 needs L1 and L2");
+  const size_t need = fp4_linear_fwd_workspace(M, N, K, r);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return fail(FP4_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
+  Carver c(ws);
+  fp4_tensor xq;
+  void* P = nullptr;
+  fwd_ws(M, N, K, r, &c, &xq, &P);
+  if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, nullptr, &xq, xqT_saved, s))) return st;
+  if (r > 0 && (st = branch_impl(X, M, K, ldx, L1, r, P, s))) return st;
+  return gemm_impl(&xq, Wq, P, L2, r, beta, Y, FP4_OUT_BF16, ldy, s);
+}
+
+fp4_status fp4_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t lddy, const fp4_tensor* WqT,
+                          const fp4_tensor* xqT_saved, const void* L1, const void* L2, int r, float beta,
+                          uint64_t seed, void* dX, int64_t lddx, void* dW, int dw_dtype, int64_t lddw, void* ws,
+                          size_t ws_bytes, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  fp4_status st;
+  if ((st = check_bf16_input(dY, M, N, lddy, "dY"))) return st;
+  if ((st = check_tensor(WqT, "WqT")) || (st = check_tensor(xqT_saved, "xqT_saved"))) return st;
+  if (WqT->cols != N) return fail(FP4_ERR_INVALID_ARG, "WqT has %lld columns, dY has N = %lld", (long long)WqT->cols, (long long)N);
+  const int64_t K = WqT->rows;
+  if (xqT_saved->rows != K || xqT_saved->cols != M)
+    return fail(FP4_ERR_INVALID_ARG, "xqT_saved must be K x M (%lld x %lld)", (long long)K, (long long)M);
+  if (M % 128 || N % 128 || K % 128)
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "linear backward needs M, N, K multiples of 128");
+  if (r > 0 && (!L1 || !L2)) return fail(FP4_ERR_INVALID_ARG, "r > 0 needs L1 and L2");
+  if (r > 0 && (!aligned16(L1) || !aligned16(L2))) return fail(FP4_ERR_MISALIGNED, "L1 and L2 must be 16-byte aligned");
+  const size_t need = fp4_linear_bwd_workspace(M, N, K, r);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return fail(FP4_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
+  Carver c(ws);
+  fp4_tensor dyq, dyqT;
+  void *P2 = nullptr, *L2T = nullptr, *L1T = nullptr;
+  bwd_ws(M, N, K, r, &c, &dyq, &dyqT, &P2, &L2T, &L1T);
+  if ((st = quantize_impl(dY, M, N, lddy, FP4_ROUND_SR, seed, 0, 1, nullptr, &dyq, &dyqT, s))) return st;
+  if (r > 0) {
+    CUDA_TRY(launch_transpose_bf16(L2, N, r, L2T, s));
+    if ((st = branch_impl(dY, M, N, lddy, L2T, r, P2, s))) return st;
+    CUDA_TRY(launch_transpose_bf16(L1, r, K, L1T, s));
+  }
+  if ((st = gemm_impl(&dyq, WqT, P2, L1T, r, beta, dX, FP4_OUT_BF16, lddx, s))) return st;
+  return gemm_impl(&dyqT, xqT_saved, nullptr, nullptr, 0, 0.0f, dW, dw_dtype, lddw, s);
+}
+
+fp4_status fp4_check_status(void* stream) {
+  unsigned int v = 0;
+  CUDA_TRY(gemm_status_read_clear(&v, static_cast<cudaStream_t>(stream)));
+  if (v & (1u << FP4_ERR_TIMEOUT)) return fail(FP4_ERR_TIMEOUT, "a device-side wait timed out");
+  return FP4_OK;
+}
+
+const char* fp4_last_error(void) { return t_err.c_str(); }
+
+uint64_t fp4_launch_count(void) { return g_launches.load(); }
+
+fp4_status fp4_debug_convert(const float* in, int64_t n, uint8_t* e2m1_out, uint8_t* e4m3_out, void* stream) {
+  if (!in || !e2m1_out || !e4m3_out || n <= 0) return fail(FP4_ERR_INVALID_ARG, "bad debug_convert arguments");
+  CUDA_TRY(launch_debug_convert(in, n, e2m1_out, e4m3_out, static_cast<cudaStream_t>(stream)));
+  return FP4_OK;
+}
+
+}  // extern "C"

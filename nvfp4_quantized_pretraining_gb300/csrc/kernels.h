@@ -1,0 +1,58 @@
+// Internal launcher declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+// Output buffers of one quantized tensor (device pointers).
+struct QOut {
+  void* codes;
+  void* scales;
+  float* scale;
+};
+
+void count_launch();
+
+cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float* out, int num_sms,
+                        cudaStream_t s);
+cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
+                                 uint32_t stream_id, const float* amax, void* codes, void* scales, float* scale_out,
+                                 int num_sms, cudaStream_t s);
+cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
+                                 uint32_t stream_r, uint32_t stream_c, const float* amax, const QOut* row_out,
+                                 const QOut* col_out, cudaStream_t s);
+cudaError_t launch_debug_convert(const float* in, int64_t n, uint8_t* e2m1, uint8_t* e4m3, cudaStream_t s);
+
+// Block-scaled NVFP4 GEMM with the fused BF16 branch.  Tensor maps are built
+// inside; `sm_count` sizes the persistent grid.
+struct GemmArgs {
+  const void* a_codes;
+  const void* a_scales;
+  const float* a_scale;  // device: S_tA
+  const void* b_codes;
+  const void* b_scales;
+  const float* b_scale;  // device: S_tB
+  int64_t M, N, K;
+  const void* P;  // M x r bf16
+  const void* Q;  // N x r bf16
+  int r;
+  float beta;
+  void* C;
+  int c_f32;
+  int64_t ldc;
+};
+cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s);
+
+// P = bf16(X L^T): X M x K (pitch ldx), L r x K, P M x r.
+cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ldx, const void* L, int r, void* P,
+                                 int num_sms, cudaStream_t s);
+
+// Read and clear the status word of the GEMM kernels (synchronous on s).
+cudaError_t gemm_status_read_clear(unsigned int* out, cudaStream_t s);
+
+// out[c][r] = in[r][c] for a BF16 rows x cols matrix (pitches = widths).
+cudaError_t launch_transpose_bf16(const void* in, int64_t rows, int64_t cols, void* out, cudaStream_t s);
+
+}  // namespace nvfp4

@@ -1,0 +1,420 @@
+// NVFP4 quantize kernels (sm_103a): tensor amax, row-wise quantization and the
+// column-wise (transposed) / dual-orientation quantization.
+//
+// All three are HBM-bound streaming kernels: 16-byte coalesced BF16 loads,
+// block amax by warp shuffle (row blocks) or in registers (column blocks),
+// packed E2M1 codes written 4 or 8 bytes at a time and UE4M3 scales written
+// straight into the layout the block-scaled MMA reads.
+//
+// Format reading (the Full-Stack FP4 pages name NVFP4, section 1, and
+// "standard NVFP4", section 3, without defining it): see block_scale() and
+// tensor_scale() in common.cuh.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nvfp4 {
+
+// Byte offset of scale (r, k) in the MMA layout of a tensor with kb scale
+// columns: 128-row x 4-column atoms of 512 bytes, row-block-major.
+__device__ __forceinline__ uint32_t sf_offset(uint32_t r, uint32_t k, uint32_t atoms_k) {
+  return (((r >> 7) * atoms_k + (k >> 2)) << 9) + ((r & 31u) << 4) + (((r >> 5) & 3u) << 2) + (k & 3u);
+}
+
+// ---------------------------------------------------------------------------
+// amax: max |x| over a BF16 tensor.  |x| ordering equals the ordering of the
+// BF16 bit patterns with the sign cleared, so the reduction is integer
+// (two elements per 32-bit word with __vmaxu2).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ x, uint32_t cpr, uint32_t nchunks,
+                                                   int64_t ld, unsigned int* __restrict__ out) {
+  uint32_t m = 0;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  uint32_t g = blockIdx.x * blockDim.x + threadIdx.x;
+  for (; g + 3 * stride < nchunks; g += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t gg = g + u * stride;
+      const uint32_t row = gg / cpr, c8 = gg - row * cpr;
+      v[u] = __ldcs(reinterpret_cast<const uint4*>(x + row * ld + c8 * 8));
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      m = __vmaxu2(m, v[u].x & 0x7FFF7FFFu);
+      m = __vmaxu2(m, v[u].y & 0x7FFF7FFFu);
+      m = __vmaxu2(m, v[u].z & 0x7FFF7FFFu);
+      m = __vmaxu2(m, v[u].w & 0x7FFF7FFFu);
+    }
+  }
+  for (; g < nchunks; g += stride) {
+    const uint32_t row = g / cpr, c8 = g - row * cpr;
+    const uint4 v = __ldcs(reinterpret_cast<const uint4*>(x + row * ld + c8 * 8));
+    m = __vmaxu2(m, v.x & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
+  }
+  m = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  __shared__ uint32_t red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t b = red[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) b = max(b, red[w]);
+    if (b != 0) atomicMax(out, b << 16);  // float bits of the BF16 amax; ordered as unsigned
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Row-wise quantization: lane pairs (2i, 2i+1) hold the two 8-element halves
+// of one 16-element block.
+// ---------------------------------------------------------------------------
+struct RowQuantArgs {
+  const uint16_t* x;
+  int64_t ld;
+  uint32_t rows, cols, cpr, nchunks, atoms_k;
+  const float* amax;
+  uint8_t* codes;
+  uint8_t* scales;
+  float* scale_out;
+  uint64_t seed;
+  uint32_t stream;
+};
+
+template <bool SR>
+__device__ __forceinline__ void quantize_chunk_row(const RowQuantArgs& a, uint32_t g, bool valid, const uint4& w,
+                                                   float S_t, bool pack4) {
+  const int lane = threadIdx.x & 31;
+  float v[8];
+  v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+  v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+  // half-block amax from the integer patterns, then the pair's max
+  uint32_t m = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu), __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+  m = max(m & 0xFFFFu, m >> 16);
+  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  const BlockScale bs = block_scale(__uint_as_float(m << 16), S_t);
+  float y[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(v[i], bs.inv);
+  if (SR) {
+    const uint4 rnd = sr_random(a.seed, a.stream, g);
+    const uint32_t rw[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = sr_round(y[i], (i & 1) ? (rw[i >> 1] >> 16) : (rw[i >> 1] & 0xFFFFu));
+  }
+  const uint32_t codes = e2m1x8(y);
+  const uint32_t row = g / a.cpr, c8 = g - row * a.cpr;
+  if (valid) *reinterpret_cast<uint32_t*>(a.codes + (size_t)row * (a.cols >> 1) + c8 * 4) = codes;
+  if (pack4) {
+    // lanes 0,2,4,6 (mod 8) hold four consecutive scales of one row: one 32-bit store
+    const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 2);
+    const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 4);
+    const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 6);
+    if (valid && (lane & 7) == 0)
+      *reinterpret_cast<uint32_t*>(a.scales + sf_offset(row, c8 >> 1, a.atoms_k)) =
+          bs.sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  } else if (valid && (lane & 1) == 0) {
+    a.scales[sf_offset(row, c8 >> 1, a.atoms_k)] = static_cast<uint8_t>(bs.sb);
+  }
+}
+
+template <bool SR>
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const RowQuantArgs a) {
+  const float amax = *a.amax;
+  const float S_t = tensor_scale(amax);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && a.scale_out) {
+    a.scale_out[0] = S_t;
+    a.scale_out[1] = amax;
+  }
+  // cols % 64 == 0: every aligned group of 8 chunks is 4 whole blocks of one row
+  const bool pack4 = (a.cols & 63u) == 0;
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  constexpr int U = 4;
+  uint32_t base = warp * 32;
+  for (; base + (U - 1) * nwarps * 32 < a.nchunks; base += U * nwarps * 32) {
+    uint4 w[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t g = base + u * nwarps * 32 + lane;
+      w[u] = make_uint4(0, 0, 0, 0);
+      if (g < a.nchunks) {
+        const uint32_t row = g / a.cpr, c8 = g - row * a.cpr;
+        w[u] = __ldcs(reinterpret_cast<const uint4*>(a.x + row * a.ld + c8 * 8));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t g = base + u * nwarps * 32 + lane;
+      quantize_chunk_row<SR>(a, g, g < a.nchunks, w[u], S_t, pack4);
+    }
+  }
+  for (; base < a.nchunks; base += nwarps * 32) {
+    const uint32_t g = base + lane;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (g < a.nchunks) {
+      const uint32_t row = g / a.cpr, c8 = g - row * a.cpr;
+      w = __ldcs(reinterpret_cast<const uint4*>(a.x + row * a.ld + c8 * 8));
+    }
+    quantize_chunk_row<SR>(a, g, g < a.nchunks, w, S_t, pack4);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Column-wise (transposed) quantization, optionally with the row-wise output
+// from the same read.  A CTA stages a 64-row x 128-column BF16 tile in shared
+// memory; the row form is produced from registers right after the load, the
+// column form from the staged tile (one thread per column, two 16-row blocks).
+// SR random bits of the column form are drawn in the row-chunk mapping (one
+// Philox call per 8 source elements) and staged beside the tile.
+// ---------------------------------------------------------------------------
+struct DualQuantArgs {
+  const uint16_t* x;
+  int64_t ld;
+  uint32_t rows, cols, cpr;
+  const float* amax;
+  // row-wise output (rows x cols)
+  uint8_t* codes_r;
+  uint8_t* scales_r;
+  float* scale_out_r;
+  uint32_t atoms_k_r;
+  // column-wise output (cols x rows)
+  uint8_t* codes_c;
+  uint8_t* scales_c;
+  float* scale_out_c;
+  uint32_t atoms_k_c;
+  uint64_t seed;
+  uint32_t stream_r, stream_c;
+};
+
+constexpr int kTileR = 64, kTileC = 128;
+
+template <bool ROW, bool COL, bool SR>
+__global__ void __launch_bounds__(256) quantize_dual_kernel(const DualQuantArgs a) {
+  __shared__ __align__(16) uint16_t tile[kTileR][kTileC];
+  __shared__ __align__(16) uint16_t rtile[SR && COL ? kTileR : 1][SR && COL ? kTileC : 8];
+  const float amax = *a.amax;
+  const float S_t = tensor_scale(amax);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    if (ROW && a.scale_out_r) { a.scale_out_r[0] = S_t; a.scale_out_r[1] = amax; }
+    if (COL && a.scale_out_c) { a.scale_out_c[0] = S_t; a.scale_out_c[1] = amax; }
+  }
+  const uint32_t r0 = blockIdx.y * kTileR, c0 = blockIdx.x * kTileC;
+  const int tid = threadIdx.x;
+
+  uint4 w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int q = tid + i * 256;
+    const uint32_t row = r0 + (q >> 4), c8 = (c0 >> 3) + (q & 15);
+    w[i] = make_uint4(0, 0, 0, 0);
+    if (row < a.rows && c8 < a.cpr) w[i] = __ldcs(reinterpret_cast<const uint4*>(a.x + row * a.ld + c8 * 8));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int q = tid + i * 256;
+    const uint32_t row = r0 + (q >> 4), c8 = (c0 >> 3) + (q & 15);
+    const bool valid = row < a.rows && c8 < a.cpr;
+    if (COL) {
+      *reinterpret_cast<uint4*>(&tile[q >> 4][(q & 15) * 8]) = w[i];
+      if (SR) {
+        const uint4 rc = sr_random(a.seed, a.stream_c, (uint64_t)row * a.cpr + c8);
+        // element i of the chunk takes word i/2, low half for even i: store the
+        // eight 16-bit draws in element order
+        uint16_t* dst = &rtile[q >> 4][(q & 15) * 8];
+        const uint32_t rw[4] = {rc.x, rc.y, rc.z, rc.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dst[e] = static_cast<uint16_t>((e & 1) ? (rw[e >> 1] >> 16) : rw[e >> 1]);
+      }
+    }
+    if (ROW) {
+      float v[8];
+      v[0] = bf16_lo(w[i].x); v[1] = bf16_hi(w[i].x); v[2] = bf16_lo(w[i].y); v[3] = bf16_hi(w[i].y);
+      v[4] = bf16_lo(w[i].z); v[5] = bf16_hi(w[i].z); v[6] = bf16_lo(w[i].w); v[7] = bf16_hi(w[i].w);
+      uint32_t m = __vmaxu2(__vmaxu2(w[i].x & 0x7FFF7FFFu, w[i].y & 0x7FFF7FFFu),
+                            __vmaxu2(w[i].z & 0x7FFF7FFFu, w[i].w & 0x7FFF7FFFu));
+      m = max(m & 0xFFFFu, m >> 16);
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      const BlockScale bs = block_scale(__uint_as_float(m << 16), S_t);
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(v[e], bs.inv);
+      if (SR) {
+        const uint4 rr = sr_random(a.seed, a.stream_r, (uint64_t)row * a.cpr + c8);
+        const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = sr_round(y[e], (e & 1) ? (rw[e >> 1] >> 16) : (rw[e >> 1] & 0xFFFFu));
+      }
+      const uint32_t codes = e2m1x8(y);
+      if (valid) {
+        *reinterpret_cast<uint32_t*>(a.codes_r + (size_t)row * (a.cols >> 1) + c8 * 4) = codes;
+        if ((q & 1) == 0) a.scales_r[sf_offset(row, c8 >> 1, a.atoms_k_r)] = static_cast<uint8_t>(bs.sb);
+      }
+    }
+  }
+  if (!COL) return;
+  __syncthreads();
+
+  const uint32_t c = tid & (kTileC - 1);
+  const uint32_t col = c0 + c;
+  if (col >= a.cols) return;
+  uint32_t sb2 = 0;
+  const uint32_t rb0 = (tid >> 7) * 2;  // this thread's first 16-row block in the tile
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t rb = rb0 + h;
+    const uint32_t rowb = r0 + rb * 16;
+    float v[16];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t bits = tile[rb * 16 + i][c];
+      m = max(m, bits & 0x7FFFu);
+      v[i] = __uint_as_float(bits << 16);
+    }
+    const BlockScale bs = block_scale(__uint_as_float(m << 16), S_t);
+    float y[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(v[i], bs.inv);
+    if (SR) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) y[i] = sr_round(y[i], rtile[rb * 16 + i][c]);
+    }
+    float lo8[8], hi8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { lo8[i] = y[i]; hi8[i] = y[8 + i]; }
+    const uint2 codes = make_uint2(e2m1x8(lo8), e2m1x8(hi8));
+    if (rowb < a.rows)
+      *reinterpret_cast<uint2*>(a.codes_c + (size_t)col * (a.rows >> 1) + (rowb >> 1)) = codes;
+    sb2 |= bs.sb << (8 * h);
+  }
+  const uint32_t kb = (r0 >> 4) + rb0;  // even, so kb and kb+1 share one 32-bit group
+  if (r0 + rb0 * 16 < a.rows) {
+    if (r0 + (rb0 + 1) * 16 < a.rows)
+      *reinterpret_cast<uint16_t*>(a.scales_c + sf_offset(col, kb, a.atoms_k_c)) = static_cast<uint16_t>(sb2);
+    else
+      a.scales_c[sf_offset(col, kb, a.atoms_k_c)] = static_cast<uint8_t>(sb2);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Diagnostic conversion kernel: the quantizer's own E2M1 and E4M3 routines.
+// ---------------------------------------------------------------------------
+__global__ void debug_convert_kernel(const float* __restrict__ in, int64_t n, uint8_t* __restrict__ e2m1,
+                                     uint8_t* __restrict__ e4m3) {
+  const int64_t i8 = (int64_t)(blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (i8 >= n) return;
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = (i8 + i < n) ? in[i8 + i] : 0.0f;
+  const uint32_t c = e2m1x8(v);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (i8 + i < n) {
+      e2m1[i8 + i] = (c >> (4 * i)) & 0xFu;
+      e4m3[i8 + i] = static_cast<uint8_t>(e4m3_rn_sat(v[i]));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Launchers
+// ---------------------------------------------------------------------------
+static int grid_for(uint64_t work_items, int per_block, int max_blocks) {
+  uint64_t b = (work_items + per_block - 1) / per_block;
+  if (b < 1) b = 1;
+  if (b > (uint64_t)max_blocks) b = max_blocks;
+  return static_cast<int>(b);
+}
+
+cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float* out, int num_sms,
+                        cudaStream_t s) {
+  const uint32_t cpr = static_cast<uint32_t>(cols / 8);
+  const uint32_t nchunks = static_cast<uint32_t>(rows) * cpr;
+  cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  const int grid = grid_for(nchunks, 256 * 4, num_sms * 8);
+  amax_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), cpr, nchunks, ld,
+                                   reinterpret_cast<unsigned int*>(out));
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
+                                 uint32_t stream_id, const float* amax, void* codes, void* scales, float* scale_out,
+                                 int num_sms, cudaStream_t s) {
+  RowQuantArgs a;
+  a.x = static_cast<const uint16_t*>(x);
+  a.ld = ld;
+  a.rows = static_cast<uint32_t>(rows);
+  a.cols = static_cast<uint32_t>(cols);
+  a.cpr = static_cast<uint32_t>(cols / 8);
+  a.nchunks = a.rows * a.cpr;
+  a.atoms_k = static_cast<uint32_t>((cols / 16 + 3) / 4);
+  a.amax = amax;
+  a.codes = static_cast<uint8_t*>(codes);
+  a.scales = static_cast<uint8_t*>(scales);
+  a.scale_out = scale_out;
+  a.seed = seed;
+  a.stream = stream_id;
+  const int grid = grid_for(a.nchunks, 256 * 4, num_sms * 8);
+  if (sr)
+    quantize_rows_kernel<true><<<grid, 256, 0, s>>>(a);
+  else
+    quantize_rows_kernel<false><<<grid, 256, 0, s>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
+                                 uint32_t stream_r, uint32_t stream_c, const float* amax, const QOut* row_out,
+                                 const QOut* col_out, cudaStream_t s) {
+  DualQuantArgs a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.ld = ld;
+  a.rows = static_cast<uint32_t>(rows);
+  a.cols = static_cast<uint32_t>(cols);
+  a.cpr = static_cast<uint32_t>(cols / 8);
+  a.amax = amax;
+  if (row_out) {
+    a.codes_r = static_cast<uint8_t*>(row_out->codes);
+    a.scales_r = static_cast<uint8_t*>(row_out->scales);
+    a.scale_out_r = row_out->scale;
+    a.atoms_k_r = static_cast<uint32_t>((cols / 16 + 3) / 4);
+  }
+  if (col_out) {
+    a.codes_c = static_cast<uint8_t*>(col_out->codes);
+    a.scales_c = static_cast<uint8_t*>(col_out->scales);
+    a.scale_out_c = col_out->scale;
+    a.atoms_k_c = static_cast<uint32_t>((rows / 16 + 3) / 4);
+  }
+  a.seed = seed;
+  a.stream_r = stream_r;
+  a.stream_c = stream_c;
+  dim3 grid(static_cast<unsigned>((cols + kTileC - 1) / kTileC), static_cast<unsigned>((rows + kTileR - 1) / kTileR));
+  const bool R = row_out != nullptr, C = col_out != nullptr;
+  if (R && C) {
+    if (sr) quantize_dual_kernel<true, true, true><<<grid, 256, 0, s>>>(a);
+    else quantize_dual_kernel<true, true, false><<<grid, 256, 0, s>>>(a);
+  } else if (C) {
+    if (sr) quantize_dual_kernel<false, true, true><<<grid, 256, 0, s>>>(a);
+    else quantize_dual_kernel<false, true, false><<<grid, 256, 0, s>>>(a);
+  } else {
+    if (sr) quantize_dual_kernel<true, false, true><<<grid, 256, 0, s>>>(a);
+    else quantize_dual_kernel<true, false, false><<<grid, 256, 0, s>>>(a);
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_convert(const float* in, int64_t n, uint8_t* e2m1, uint8_t* e4m3, cudaStream_t s) {
+  const int64_t threads = (n + 7) / 8;
+  const int grid = static_cast<int>((threads + 255) / 256);
+  debug_convert_kernel<<<grid, 256, 0, s>>>(in, n, e2m1, e4m3);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

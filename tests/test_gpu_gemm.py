@@ -1,0 +1,128 @@
+"""GPU parity of the block-scaled NVFP4 GEMM (with the fused BF16 branch) and
+of the BF16 branch-factor GEMM against the oracle's FP64 products of the same
+operands.  Tolerance: relative Frobenius error 1e-3 (FP32 output against the
+FP64 result; BF16 output against the FP64 result rounded to BF16)."""
+import numpy as np
+import pytest
+import torch
+
+from nvfp4_quantized_pretraining_gb300 import synthetic as S
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def F():
+    import __graft_entry__
+    __graft_entry__.build()
+    import nvfp4_quantized_pretraining_gb300 as F
+    return F
+
+
+def dev(u16):
+    return S.bits_to_torch(u16, DEV)
+
+
+def rel(got, want):
+    return float(np.linalg.norm(got - want) / max(np.linalg.norm(want), 1e-300))
+
+
+def quantize_both(F, oracle_mod, x, mode=0, seed=0, stream=0):
+    g = F.fp4_quantize(dev(x), round_mode=mode, seed=seed, sr_stream=stream)
+    o = oracle_mod.quantize(x, mode, seed=seed, stream=stream)
+    torch.cuda.synchronize()
+    assert np.array_equal(g.codes.cpu().numpy(), o.codes)
+    assert np.array_equal(g.scales.cpu().numpy(), oracle_mod.scales_to_mma(o.scales))
+    return g, o
+
+
+def check_gemm(F, oracle_mod, M, N, K, r, out_dtype, beta, seed, rows=None, a_kind="normal"):
+    A = S.normal((M, K), 1.0, seed) if a_kind == "normal" else S.with_outlier_entries((M, K), 0.001, 50.0, seed)
+    B = S.normal((N, K), 1.0, seed + 1)
+    ga, oa = quantize_both(F, oracle_mod, A)
+    gb, ob = quantize_both(F, oracle_mod, B)
+    P = S.normal((M, r), 1.0, seed + 2) if r else None
+    Q = S.normal((N, r), 1.0, seed + 3) if r else None
+    C = F.fp4_gemm_blockscaled(ga, gb, None if P is None else dev(P), None if Q is None else dev(Q), beta=beta,
+                               out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    F.fp4_check_status()
+    sel = slice(None) if rows is None else rows
+    ref = oracle_mod.gemm(oa.dequantize(rows), ob.dequantize(), None if P is None else np.ascontiguousarray(P[sel]),
+                          Q, beta)
+    got = C.float().cpu().numpy().astype(np.float64)[sel]
+    if out_dtype == torch.bfloat16:
+        ref = oracle_mod.bf16_to_f32(oracle_mod.bf16_rn(ref)).astype(np.float64)
+    e = rel(got, ref)
+    assert e < TOL, (M, N, K, r, e)
+    return e
+
+
+@pytest.mark.parametrize("M,N,K,r", [
+    (128, 128, 64, 0), (128, 128, 256, 0), (128, 128, 512, 16), (256, 384, 512, 16),
+    (384, 256, 320, 32),      # K not a multiple of the 256-wide stage
+    (128, 256, 1024, 48), (512, 512, 2048, 64),
+    (2048, 2560, 512, 0),     # more tiles than SMs: persistent schedule wraps
+    (256, 512, 512, 16),      # single-forward shape (X 256x512, W 512x512, rank 16)
+])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_gemm_small(F, oracle_mod, M, N, K, r, out_dtype):
+    check_gemm(F, oracle_mod, M, N, K, r, out_dtype, beta=0.75 if r else 1.0, seed=M + N + K + r)
+
+
+def test_gemm_outliers_and_rank0_equivalence(F, oracle_mod):
+    check_gemm(F, oracle_mod, 256, 256, 1024, 0, torch.float32, 1.0, seed=3, a_kind="outliers")
+    # r > 0 with a zero branch gives the same output as r = 0 (bit for bit)
+    A = S.normal((256, 512), 1.0, 4)
+    B = S.normal((128, 512), 1.0, 5)
+    ga, gb = F.fp4_quantize(dev(A)), F.fp4_quantize(dev(B))
+    c0 = F.fp4_gemm_blockscaled(ga, gb, out_dtype=torch.float32)
+    Z1 = torch.zeros((256, 32), dtype=torch.bfloat16, device=DEV)
+    Z2 = torch.zeros((128, 32), dtype=torch.bfloat16, device=DEV)
+    c1 = F.fp4_gemm_blockscaled(ga, gb, Z1, Z2, beta=3.0, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(c0, c1)
+
+
+def test_gemm_strided_output(F, oracle_mod):
+    A = S.normal((128, 256), 1.0, 6)
+    B = S.normal((256, 256), 1.0, 7)
+    ga, oa = quantize_both(F, oracle_mod, A)
+    gb, ob = quantize_both(F, oracle_mod, B)
+    big = torch.full((128, 384), 7.0, dtype=torch.float32, device=DEV)
+    F.fp4_gemm_blockscaled(ga, gb, out=big[:, 64:320])
+    torch.cuda.synchronize()
+    ref = oracle_mod.gemm(oa.dequantize(), ob.dequantize())
+    got = big.cpu().numpy().astype(np.float64)
+    assert rel(got[:, 64:320], ref) < TOL
+    assert np.all(got[:, :64] == 7.0) and np.all(got[:, 320:] == 7.0)
+
+
+@pytest.mark.parametrize("M,N,K,r", [
+    (4096, 4096, 4096, 0), (4096, 4096, 4096, 64), (16384, 3072, 8192, 64), (3072, 8192, 16384, 0),
+])
+def test_gemm_full_size_sampled_rows(F, oracle_mod, M, N, K, r):
+    rng = np.random.default_rng(M + N)
+    rows = np.sort(rng.choice(M, 48, replace=False))
+    check_gemm(F, oracle_mod, M, N, K, r, torch.bfloat16, beta=1.0, seed=17, rows=rows)
+
+
+@pytest.mark.parametrize("M,K,r", [(128, 64, 16), (256, 512, 32), (384, 320, 48), (1024, 2048, 64),
+                                   (16384, 3072, 64)])
+def test_branch_factor(F, oracle_mod, M, K, r):
+    X = S.student_t((M, K), 3.0, M + K)
+    L = S.normal((r, K), 0.05, r)
+    P = F.fp4_branch_factor(dev(X), dev(L))
+    torch.cuda.synchronize()
+    F.fp4_check_status()
+    want = oracle_mod.branch_factor(X, L)
+    got_bits = S.torch_to_bits(P)
+    g = oracle_mod.bf16_to_f32(got_bits).astype(np.float64)
+    w = oracle_mod.bf16_to_f32(want).astype(np.float64)
+    assert rel(g, w) < TOL
+    # FP32 accumulation may flip a BF16 rounding now and then, never by more than one unit
+    assert np.mean(got_bits == want) > 0.98
+    diff = np.abs(got_bits.astype(np.int32) - want.astype(np.int32))
+    assert np.all((diff <= 1) | (g == w))
