@@ -1,0 +1,466 @@
+#!/usr/bin/env python
+"""Benchmark of the NVFP4 linear-projection hot path on GB300.
+
+One step = for every projection of the workload: NVFP4 quantization of the
+residual weight W_res (both orientations, RTN), the linear forward
+(amax + dual RTN quantization of X, BF16 branch factor, block-scaled GEMM
+with the fused rank-r branch) and the linear backward (amax + dual SR
+quantization of dY, branch factor, dX GEMM with branch, dW GEMM).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload block3b|mlp_up|single]
+
+Prints one JSON line (rank 0).  `value` is NVFP4 GEMM TFLOP/s of the whole
+step (3 GEMMs x 2MNK per projection) with inputs resident in HBM; `e2e` is the
+same with the step's inputs copied from pinned host memory and its results
+copied back inside the timed region.  The reference arm (--impl reference)
+times the CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 linear fwd+bwd TFLOP/s and % dense-FP4 peak; quantize GB/s % HBM (1 GB300)"
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor rate on GB300
+
+WORKLOADS = {
+    "block3b": dict(
+        name="block3b_T16384_d3072_ff8192_r64",
+        desc="3B-class transformer block projections, T=16384 tokens: qkv 9216x3072, o 3072x3072, "
+             "gate_up 16384x3072, down 3072x8192; rank-64 LoRA-SVD; RTN fwd, SR bwd; fwd+bwd",
+        T=16384, r=64, x="student_t",
+        projections=[("qkv", 9216, 3072), ("o", 3072, 3072), ("gate_up", 16384, 3072), ("down", 3072, 8192)]),
+    "mlp_up": dict(
+        name="mlp_up_T8192_d2048_f5632_r32",
+        desc="~1B MLP up projection, T=8192, W 5632x2048, rank-32 LoRA-SVD, fwd+bwd",
+        T=8192, r=32, x="normal", projections=[("up", 5632, 2048)]),
+    "single": dict(
+        name="single_fwd_256x512x512_r16",
+        desc="single NVFP4 linear, X 256x512, W 512x512, rank 16 (fwd+bwd)",
+        T=256, r=16, x="normal", projections=[("w", 512, 512)]),
+}
+
+# ncu DRAM traffic per launch of the block-scaled GEMM on the bench workload,
+# keyed by the SHA-256 of the kernel source it was captured on (null once the
+# source changes).  Filled from the committed profile summary.
+GEMM_TRAFFIC = {}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def gemm_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "nvfp4_quantized_pretraining_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import nvfp4_quantized_pretraining_gb300 as F
+    from nvfp4_quantized_pretraining_gb300 import build as B
+    from nvfp4_quantized_pretraining_gb300 import lora
+    from nvfp4_quantized_pretraining_gb300 import synthetic as S
+
+    rank, world, local = dist_env()
+    B.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    wl = WORKLOADS[args.workload]
+    T, r = wl["T"], wl["r"]
+    stream = torch.cuda.Stream(device=dev)
+    projs = []
+    seed0 = 1000 * rank
+    for i, (name, N, K) in enumerate(wl["projections"]):
+        W = S.normal((N, K), 0.02, seed0 + 10 * i)
+        Wres, L1, L2 = lora.lora_svd_split_randomized(W, r, seed=seed0 + 10 * i + 1)
+        X = (S.student_t_device((T, K), 3, seed0 + 10 * i + 2, dev) if wl["x"] == "student_t"
+             else S.normal_device((T, K), 1.0, seed0 + 10 * i + 2, dev))
+        dY = S.normal_device((T, N), 1e-3, seed0 + 10 * i + 3, dev)
+        p = dict(name=name, N=N, K=K, X=X, dY=dY, Wres=S.bits_to_torch(Wres, dev),
+                 L1=S.bits_to_torch(L1, dev) if r else None, L2=S.bits_to_torch(L2, dev) if r else None)
+        p["Wq"] = F.NVFP4Tensor.empty(N, K, dev)
+        p["WqT"] = F.NVFP4Tensor.empty(K, N, dev)
+        p["xqT"] = F.NVFP4Tensor.empty(K, T, dev)
+        p["Y"] = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+        p["dX"] = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+        p["dW"] = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+        p["ws_f"] = torch.empty(F.linear_fwd_workspace(T, N, K, r), dtype=torch.uint8, device=dev)
+        p["ws_b"] = torch.empty(F.linear_bwd_workspace(T, N, K, r), dtype=torch.uint8, device=dev)
+        projs.append(p)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 2x the 129 MB L2
+    gemm_flops = sum(3 * 2 * T * p["N"] * p["K"] for p in projs)
+    branch_flops = sum(2 * T * p["K"] * r + 2 * T * p["N"] * r + 2 * T * p["N"] * r + 2 * T * p["K"] * r
+                       for p in projs) if r else 0
+
+    def step(seed):
+        for p in projs:
+            F.fp4_quantize_dual(p["Wres"], out_row=p["Wq"], out_col=p["WqT"], stream=stream)
+            F.fp4_linear_fwd(p["X"], p["Wq"], p["L1"], p["L2"], Y=p["Y"], xqT_saved=p["xqT"], workspace=p["ws_f"],
+                             stream=stream)
+            F.fp4_linear_bwd(p["dY"], p["WqT"], p["xqT"], p["L1"], p["L2"], seed=seed, dX=p["dX"], dW=p["dW"],
+                             workspace=p["ws_b"], stream=stream)
+
+    def timed(fn, steps, warmup):
+        with torch.cuda.stream(stream):
+            for i in range(warmup):
+                fn(i)
+            torch.cuda.synchronize(dev)
+            if world > 1:
+                dist.barrier()
+            torch.cuda.synchronize(dev)
+            times = []
+            for i in range(steps):
+                flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn(warmup + i)
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+            torch.cuda.synchronize(dev)
+            if world > 1:
+                dist.barrier()
+        return times
+
+    # ---- main timed region: device-resident inputs
+    launches0 = F.fp4_launch_count()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    with ClockSampler(gpu_id) as clk:
+        times = timed(step, args.steps, args.warmup)
+    launches = (F.fp4_launch_count() - launches0) * args.steps // (args.steps + args.warmup)
+    F.fp4_check_status(stream)
+    total_ms = sum(times)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t[0])
+    ms_per_step = total_ms / args.steps
+    value = world * gemm_flops / (ms_per_step * 1e-3) / 1e12
+
+    # ---- kernel breakdown through the public calls (same operands), for the roofline
+    bd = breakdown(F, torch, projs, T, r, stream, dev, flush, args)
+
+    # ---- end-to-end: host inputs -> device -> step -> results back to host
+    e2e = end_to_end(F, torch, projs, T, r, stream, dev, args, gemm_flops, world)
+
+    pk, pk_kind = peaks()
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
+    gemm_tf = bd["gemm_flops"] / (bd["gemm_ms"] * 1e-3) / 1e12
+    h = gemm_source_hash()
+    traffic = GEMM_TRAFFIC.get(h)
+    q_gbs = bd["quant_bytes"] / (bd["quant_ms"] * 1e-3) / 1e9
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
+        "data": "synthetic (seeded; random-init weights split by randomized SVD)",
+        "config": {"workload": wl["name"], "description": wl["desc"], "tokens": T, "rank": r,
+                   "l2": "flushed (512 MB write) before every timed step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "kernel": "gemm_nvf4_kernel", "achieved": round(gemm_tf, 1),
+                     "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(gemm_tf / fp4_peak, 4),
+                     "traffic": traffic,
+                     "peak_note": f"{pk_kind} bf16 burst {pk['bf16_tflops']} TFLOP/s x {FP4_OVER_BF16:g} "
+                                  "(nominal dense FP4:BF16 ratio); datasheet dense FP4 13500 TFLOP/s",
+                     "frac_of_datasheet": round(gemm_tf / 13500.0, 4)},
+        "quantize": {"bound": "hbm", "achieved": round(q_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(q_gbs / pk["hbm_gbs"], 4),
+                     "note": "algorithmic bytes of the dual-orientation quantize launches (2 B read + 2 x 0.5625 B "
+                             "written per element) over their event time"},
+        "breakdown_ms": {k: round(v, 4) for k, v in bd["per_kind_ms"].items()},
+        "branch_tflops_counted_separately": round(branch_flops / 1e12, 4),
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args, wl)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def breakdown(F, torch, projs, T, r, stream, dev, flush, args):
+    """Times each public call of one step separately with CUDA events on the
+    launching stream (after warm-up, L2 flushed before every step)."""
+    ev = []
+    gemm_flops = 0
+    quant_bytes = 0
+    reps = max(2, min(args.steps, 5))
+    kinds = {}
+
+    def rec(kind, fn):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        ev.append((kind, e0, e1))
+
+    with torch.cuda.stream(stream):
+        for rep in range(reps + 1):
+            flush.zero_()
+            ev.clear()
+            for p in projs:
+                N, K = p["N"], p["K"]
+                xq = F.NVFP4Tensor.empty(T, K, dev) if rep == 0 and "xq" not in p else p.get("xq")
+                p["xq"] = xq
+                dyq = p.get("dyq") or F.NVFP4Tensor.empty(T, N, dev)
+                dyqT = p.get("dyqT") or F.NVFP4Tensor.empty(N, T, dev)
+                p["dyq"], p["dyqT"] = dyq, dyqT
+                if "P" not in p:
+                    p["P"] = torch.empty((T, r), dtype=torch.bfloat16, device=dev) if r else None
+                    p["P2"] = torch.empty((T, r), dtype=torch.bfloat16, device=dev) if r else None
+                    p["L2T"] = p["L2"].t().contiguous() if r else None
+                    p["L1T"] = p["L1"].t().contiguous() if r else None
+                    p["amax"] = torch.empty(1, dtype=torch.float32, device=dev)
+                rec("quantize_w_dual", lambda: F.fp4_quantize_dual(p["Wres"], out_row=p["Wq"], out_col=p["WqT"],
+                                                                   stream=stream))
+                rec("amax", lambda: F.fp4_amax(p["X"], out=p["amax"], stream=stream))
+                rec("quantize_x_dual", lambda: F.fp4_quantize_dual(p["X"], amax=p["amax"], out_row=xq,
+                                                                   out_col=p["xqT"], stream=stream))
+                if r:
+                    rec("branch_factor", lambda: F.fp4_branch_factor(p["X"], p["L1"], out=p["P"], stream=stream))
+                rec("gemm", lambda: F.fp4_gemm_blockscaled(xq, p["Wq"], p["P"], p["L2"], out=p["Y"], stream=stream))
+                rec("amax", lambda: F.fp4_amax(p["dY"], out=p["amax"], stream=stream))
+                rec("quantize_dy_dual_sr", lambda: F.fp4_quantize_dual(p["dY"], round_mode=F.SR, seed=rep,
+                                                                       amax=p["amax"], out_row=dyq, out_col=dyqT,
+                                                                       stream=stream))
+                if r:
+                    rec("branch_factor", lambda: F.fp4_branch_factor(p["dY"], p["L2T"], out=p["P2"], stream=stream))
+                rec("gemm", lambda: F.fp4_gemm_blockscaled(dyq, p["WqT"], p["P2"], p["L1T"], out=p["dX"],
+                                                           stream=stream))
+                rec("gemm", lambda: F.fp4_gemm_blockscaled(dyqT, p["xqT"], out=p["dW"], stream=stream))
+            torch.cuda.synchronize(dev)
+            if rep == 0:
+                continue  # warm-up pass
+            for kind, e0, e1 in ev:
+                kinds.setdefault(kind, 0.0)
+                kinds[kind] += e0.elapsed_time(e1) / reps
+    for p in projs:
+        gemm_flops += 3 * 2 * T * p["N"] * p["K"]
+        quant_bytes += int(3.125 * (T * p["K"] + T * p["N"] + p["N"] * p["K"]))
+    quant_ms = kinds.get("quantize_x_dual", 0) + kinds.get("quantize_dy_dual_sr", 0) + kinds.get("quantize_w_dual", 0)
+    return dict(gemm_flops=gemm_flops, gemm_ms=kinds["gemm"], quant_bytes=quant_bytes, quant_ms=quant_ms,
+                per_kind_ms=kinds)
+
+
+def end_to_end(F, torch, projs, T, r, stream, dev, args, gemm_flops, world):
+    """Same step, with X and dY copied from pinned host memory before and Y, dX
+    and dW copied back to pinned host memory after, all inside the timed region."""
+    hosts = []
+    h2d = d2h = 0
+    for p in projs:
+        hx = torch.empty_like(p["X"], device="cpu").pin_memory()
+        hx.copy_(p["X"])
+        hdy = torch.empty_like(p["dY"], device="cpu").pin_memory()
+        hdy.copy_(p["dY"])
+        outs = [torch.empty_like(p[k], device="cpu").pin_memory() for k in ("Y", "dX", "dW")]
+        hosts.append((hx, hdy, outs))
+        h2d += hx.numel() * 2 + hdy.numel() * 2
+        d2h += sum(o.numel() * o.element_size() for o in outs)
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for p, (hx, hdy, outs) in zip(projs, hosts):
+                p["X"].copy_(hx, non_blocking=True)
+                p["dY"].copy_(hdy, non_blocking=True)
+                F.fp4_quantize_dual(p["Wres"], out_row=p["Wq"], out_col=p["WqT"], stream=stream)
+                F.fp4_linear_fwd(p["X"], p["Wq"], p["L1"], p["L2"], Y=p["Y"], xqT_saved=p["xqT"],
+                                 workspace=p["ws_f"], stream=stream)
+                F.fp4_linear_bwd(p["dY"], p["WqT"], p["xqT"], p["L1"], p["L2"], seed=i, dX=p["dX"], dW=p["dW"],
+                                 workspace=p["ws_b"], stream=stream)
+                for o, k in zip(outs, ("Y", "dX", "dW")):
+                    o.copy_(p[k], non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if i >= args.warmup:
+                times.append(e0.elapsed_time(e1))
+    ms = sum(times) / len(times)
+    return {"value": round(world * gemm_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+
+_ORACLE_CACHE = {}
+
+
+def oracle_sample(wl, tokens):
+    """One bounded sample of the workload on the CPU oracle: the smallest
+    projection's full weight quantization plus forward+backward on a slice of
+    `tokens` tokens.  Returns (flops, seconds, description, threads)."""
+    import oracle
+    from nvfp4_quantized_pretraining_gb300 import synthetic as S
+
+    oracle.build()
+    name, N, K = min(wl["projections"], key=lambda p: p[1] * p[2])
+    r = wl["r"]
+    t = min(wl["T"], tokens)
+    key = (wl["name"], t)
+    if key not in _ORACLE_CACHE:
+        W = S.normal((N, K), 0.02, 1)
+        Wres, L1, L2 = oracle.lora_svd_split(W, r)
+        X = S.student_t((t, K), 3.0, 2) if wl["x"] == "student_t" else S.normal((t, K), 1.0, 2)
+        dY = S.normal((t, N), 1e-3, 3)
+        _ORACLE_CACHE[key] = (Wres, L1, L2, X, dY)
+    Wres, L1, L2, X, dY = _ORACLE_CACHE[key]
+    t0 = time.perf_counter()
+    oracle.linear_fwd(X, Wres, L1, L2)
+    oracle.linear_bwd(dY, X, Wres, L1, L2, seed=1)
+    dt = time.perf_counter() - t0
+    flops = 3 * 2 * t * N * K
+    desc = (f"oracle (C quantizer + NumPy FP64 GEMMs) on projection '{name}' {N}x{K} with {t} of {wl['T']} tokens: "
+            f"weight quantization (row+col) and linear fwd+bwd")
+    return flops, dt, desc, oracle.max_threads()
+
+
+def cpu_baseline(args, wl):
+    flops, dt, desc, threads = oracle_sample(wl, tokens=2048)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": desc, "seconds": round(dt, 3)}
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload]
+    times, flops_all = [], 0
+    desc = threads = None
+    for i in range(args.warmup + args.steps):
+        flops, dt, desc, threads = oracle_sample(wl, tokens=512)
+        if i >= args.warmup:
+            times.append(dt)
+            flops_all = flops
+    ms = 1e3 * sum(times) / len(times)
+    value = flops_all / (ms * 1e-3) / 1e12
+    out = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+           "config": {"workload": wl["name"], "description": wl["desc"]},
+           "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                            "sample": desc},
+           "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="block3b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

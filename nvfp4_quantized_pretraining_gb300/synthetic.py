@@ -85,3 +85,27 @@ BLOCK_3B = dict(name="block3b_T16384_d3072_ff8192_r64", T=16384, r=64,
 QUANT_SWEEP_ELEMS = [1 << 20, 1 << 24, 1 << 26, 1 << 28]
 GEMM_SWEEP = [(2048, 2048, 2048), (4096, 4096, 4096), (8192, 8192, 8192),
               (16384, 16384, 16384), (16384, 3072, 8192), (3072, 8192, 16384)]
+
+
+# Device-side generators for the benchmark's large tensors (seeded torch
+# generators on the GPU; same distributions as above, not bit-identical to
+# the NumPy versions, which the parity tests use).
+def normal_device(shape, std: float, seed: int, device="cuda") -> torch.Tensor:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return (torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std).to(torch.bfloat16)
+
+
+def student_t_device(shape, df: int, seed: int, device="cuda") -> torch.Tensor:
+    """Student-t with integer df, t = z / sqrt(chi2_df / df) with chi2_df the sum
+    of df squared standard normals; scaled to unit variance."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    z = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    chi2 = torch.zeros(shape, device=device, dtype=torch.float32)
+    for _ in range(int(df)):
+        chi2 += torch.randn(shape, generator=g, device=device, dtype=torch.float32) ** 2
+    t = z / torch.sqrt(chi2 / df)
+    if df > 2:
+        t = t / (df / (df - 2.0)) ** 0.5
+    return t.to(torch.bfloat16)

@@ -122,7 +122,8 @@ def test_branch_factor(F, oracle_mod, M, K, r):
     g = oracle_mod.bf16_to_f32(got_bits).astype(np.float64)
     w = oracle_mod.bf16_to_f32(want).astype(np.float64)
     assert rel(g, w) < TOL
-    # FP32 accumulation may flip a BF16 rounding now and then, never by more than one unit
+    # FP32 accumulation may flip a BF16 rounding now and then: at most one BF16 step
+    # (2^-7 relative) away, except for results that cancel to near zero
     assert np.mean(got_bits == want) > 0.98
-    diff = np.abs(got_bits.astype(np.int32) - want.astype(np.int32))
-    assert np.all((diff <= 1) | (g == w))
+    scale = np.abs(oracle_mod.bf16_to_f32(X).astype(np.float64)) @ np.abs(oracle_mod.bf16_to_f32(L).astype(np.float64)).T
+    assert np.all(np.abs(g - w) <= 2.0 ** -7 * np.abs(w) + 2.0 ** -20 * scale)

@@ -58,9 +58,10 @@ def test_conversion_conventions(F, oracle_mod):
     assert np.array_equal(e4m3.cpu().numpy(), oracle_mod.e4m3_encode(s))
 
 
-SHAPES = [
-    (16, 16), (128, 64), (256, 512), (200, 48), (96, 1040), (1000, 4096), (512, 512),
+SHAPES = [  # rows % 16 == 0 (the transposed form needs whole 16-row blocks); ragged vs 128-row tiles
+    (16, 16), (128, 64), (256, 512), (208, 48), (96, 1040), (1008, 4096), (512, 512),
 ]
+ROW_ONLY_SHAPES = [(200, 48), (1, 16), (1000, 4096), (129, 1040)]  # any row count for the row form
 
 
 def make_input(shape, kind, seed):
@@ -77,7 +78,7 @@ def make_input(shape, kind, seed):
     raise ValueError(kind)
 
 
-@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("shape", SHAPES + ROW_ONLY_SHAPES)
 @pytest.mark.parametrize("mode", [0, 1])
 def test_quantize_rows(F, oracle_mod, shape, mode):
     x = make_input(shape, "outliers", seed=shape[0] * 7 + shape[1])
@@ -95,7 +96,7 @@ def test_quantize_transposed(F, oracle_mod, shape, mode):
     assert_same_quant(F, got, want, oracle_mod)
 
 
-@pytest.mark.parametrize("shape", [(64, 128), (256, 512), (200, 48), (1024, 2048)])
+@pytest.mark.parametrize("shape", [(64, 128), (256, 512), (208, 48), (1024, 2048)])
 @pytest.mark.parametrize("mode", [0, 1])
 def test_quantize_dual(F, oracle_mod, shape, mode):
     x = make_input(shape, "grad", seed=5)
@@ -174,3 +175,10 @@ def test_quantize_full_size(F, oracle_mod, name, shape, kind, mode):
     assert_same_quant(F, c, oracle_mod.quantize(x, mode, seed=1, stream=1, transposed=True), oracle_mod)
     r2 = F.fp4_quantize(dev(x), round_mode=mode, seed=1)
     assert torch.equal(r2.codes, r.codes) and torch.equal(r2.scales, r.scales)
+
+
+def test_transposed_rejects_partial_row_blocks(F):
+    x = make_input((200, 48), "normal", seed=1)
+    with pytest.raises(F.FP4Error) as e:
+        F.fp4_quantize_transposed(dev(x))
+    assert e.value.status == F.FP4_ERR_UNSUPPORTED_SHAPE
