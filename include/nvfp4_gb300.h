@@ -178,6 +178,14 @@ uint64_t fp4_launch_count(void);
 fp4_status fp4_debug_convert(const float* in, int64_t n, uint8_t* e2m1_out,
                              uint8_t* e4m3_out, void* stream);
 
+/* Diagnostic: dense NVFP4 tensor-core rate probe.  Launches one CTA per SM;
+ * each issues 4 * iters block-scaled MMAs of shape M=128 x N=n x K=64
+ * (n in {128, 256}) on operands resident in shared memory.  The caller times
+ * the launch (e.g. with CUDA events on `stream`); the work is
+ * num_sms * 4 * iters * 2 * 128 * n * 64 FLOP.  *num_sms_out (host, may be
+ * NULL) receives the SM count used. */
+fp4_status fp4_mma_peak_probe(int n, int iters, int* num_sms_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -34,7 +34,7 @@ OUT_F32 = 1
 EXPORTS = ["fp4_scale_bytes", "fp4_amax", "fp4_quantize", "fp4_quantize_transposed", "fp4_quantize_dual",
            "fp4_gemm_blockscaled", "fp4_branch_factor", "fp4_linear_fwd_workspace", "fp4_linear_bwd_workspace",
            "fp4_linear_fwd", "fp4_linear_bwd", "fp4_check_status", "fp4_last_error", "fp4_launch_count",
-           "fp4_debug_convert"]
+           "fp4_debug_convert", "fp4_mma_peak_probe"]
 
 
 class FP4Error(RuntimeError):
@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
         "fp4_last_error": (ctypes.c_char_p, []),
         "fp4_launch_count": (u64, []),
         "fp4_debug_convert": (i32, [P, i64, P, P, P]),
+        "fp4_mma_peak_probe": (i32, [i32, i32, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -260,3 +261,19 @@ def fp4_debug_convert(x: torch.Tensor, stream=None):
     e4m3 = torch.empty(n, dtype=torch.uint8, device=x.device)
     _check(lib().fp4_debug_convert(x.data_ptr(), n, e2m1.data_ptr(), e4m3.data_ptr(), _stream(stream)))
     return e2m1, e4m3
+
+
+def fp4_mma_peak_probe(n: int = 256, iters: int = 20000, stream=None) -> dict:
+    """Times the dense NVFP4 MMA probe with CUDA events; returns TFLOP/s."""
+    st = torch.cuda.current_stream() if stream is None else stream
+    sms = ctypes.c_int(0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _check(lib().fp4_mma_peak_probe(n, max(1, iters // 10), ctypes.byref(sms), st.cuda_stream))  # warm-up
+    e0.record(st)
+    _check(lib().fp4_mma_peak_probe(n, iters, ctypes.byref(sms), st.cuda_stream))
+    e1.record(st)
+    e1.synchronize()
+    fp4_check_status(st)
+    ms = e0.elapsed_time(e1)
+    flops = sms.value * 4 * iters * 2 * 128 * n * 64
+    return {"n": n, "iters": iters, "sms": sms.value, "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}

@@ -373,4 +373,12 @@ fp4_status fp4_debug_convert(const float* in, int64_t n, uint8_t* e2m1_out, uint
   return FP4_OK;
 }
 
+fp4_status fp4_mma_peak_probe(int n, int iters, int* num_sms_out, void* stream) {
+  if ((n != 128 && n != 256) || iters <= 0) return fail(FP4_ERR_INVALID_ARG, "probe needs n in {128, 256}, iters > 0");
+  const int sms = sm_count();
+  if (num_sms_out) *num_sms_out = sms;
+  CUDA_TRY(launch_mma_peak(n, iters, sms, static_cast<cudaStream_t>(stream)));
+  return FP4_OK;
+}
+
 }  // extern "C"

@@ -19,13 +19,8 @@ namespace nvfp4 {
 // ---------------------------------------------------------------------------
 static __device__ unsigned int g_status = 0;
 
-constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
-
-__device__ __forceinline__ unsigned long long globaltimer_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
+// Bound on one mbarrier wait, in SM clock cycles (about 2 s at 2 GHz).
+constexpr long long kWaitTimeoutCycles = 4000000000ll;
 
 __device__ __forceinline__ void record_timeout() { atomicOr(&g_status, 1u << FP4_ERR_TIMEOUT); }
 
@@ -59,14 +54,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase with the given parity to complete.  Bounded: after
-// kWaitTimeoutNs it records FP4_ERR_TIMEOUT and returns false.
+// kWaitTimeoutCycles it records FP4_ERR_TIMEOUT and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
+  const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(a, parity)) return true;
-    if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if ((i & 63u) == 0 && clock64() - t0 > kWaitTimeoutCycles) {
       record_timeout();
       return false;
     }

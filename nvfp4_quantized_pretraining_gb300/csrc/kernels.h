@@ -49,6 +49,9 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s);
 cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ldx, const void* L, int r, void* P,
                                  int num_sms, cudaStream_t s);
 
+// Dense NVFP4 MMA rate probe: every SM issues 4 * iters M=128 x N=n x K=64 MMAs.
+cudaError_t launch_mma_peak(int n, int iters, int num_sms, cudaStream_t s);
+
 // Read and clear the status word of the GEMM kernels (synchronous on s).
 cudaError_t gemm_status_read_clear(unsigned int* out, cudaStream_t s);
 
