@@ -25,17 +25,30 @@ namespace nvfp4 {
 
 // ---------------------------------------------------------------------------
 // Block-scaled NVFP4 GEMM
+//
+// Tile 128 x 128 per CTA, 256 K elements per pipeline stage.  CTAs form CM x CN
+// clusters: the CM CTAs of a cluster column share one B tile and the CN CTAs
+// of a cluster row share one A tile; each CTA loads 1/CN of its A tile and
+// 1/CM of its B tile (codes and block scales) with TMA multicast into every
+// CTA that needs it, so L2 delivers each operand byte once per cluster.
+// Block scales reach tensor memory through tcgen05.st from four "scale" warps
+// (one per TMEM lane quadrant) instead of tcgen05.cp on the tensor pipe.  For
+// output rows m in lane quadrant q = m / 32, the MMA reads the scales of A row
+// m from lane m, column (base + q), and the scales of B row n from lane
+// 32q + n % 32, column (base + n / 32); the byte is the 16-element block
+// within the 64-wide K step.  So A scales are written once (the diagonal) and
+// B scales once per quadrant.
 // ---------------------------------------------------------------------------
 namespace g4 {
-constexpr int BM = 128;             // rows of A per tile (one tcgen05 M=128 MMA)
+constexpr int BM = 128;             // rows of A per tile (tcgen05 M=128)
 constexpr int BN = 128;             // rows of B per tile (MMA N)
 constexpr int BK = 256;             // K elements per stage (128 bytes of E2M1 per row)
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK / 2;              // 16 KB
 constexpr int B_BYTES = BN * BK / 2;              // 16 KB
 constexpr int SF_ATOM = 512;                      // 128 rows x 4 scales
-constexpr int SFA_BYTES = (BM / 128) * (BK / 64) * SF_ATOM;  // 2 KB
-constexpr int SFB_BYTES = (BN / 128) * (BK / 64) * SF_ATOM;  // 2 KB
+constexpr int SFA_BYTES = (BK / 64) * SF_ATOM;    // 2 KB (4 atoms)
+constexpr int SFB_BYTES = (BK / 64) * SF_ATOM;    // 2 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 constexpr int BR_K = 64;                          // branch rank padded to 64 (128-byte BF16 rows)
 constexpr int P_BYTES = BM * BR_K * 2;            // 16 KB, fits the A slot
@@ -43,10 +56,12 @@ constexpr int Q_BYTES = BN * BR_K * 2;            // 16 KB, fits the B slot
 // tensor memory columns
 constexpr uint32_t TM_ACC = 0;                    // 2 x BN accumulators (double buffered)
 constexpr uint32_t TM_BR = 2 * BN;                // BN branch accumulator
-constexpr uint32_t TM_SF = 3 * BN;                // STAGES x (SFA 16 + SFB 16) scale columns
+constexpr uint32_t TM_SF = 3 * BN;                // per stage: SFA 16 + SFB 16 columns
+constexpr uint32_t TM_SF_STAGE = 32;
 constexpr uint32_t TM_COLS = 512;
-static_assert(TM_SF + STAGES * (4 * (BK / 64) * (BM / 128) + 4 * (BK / 64) * (BN / 128)) <= TM_COLS, "TMEM");
-constexpr int NUM_THREADS = 192;
+static_assert(TM_SF + STAGES * TM_SF_STAGE <= TM_COLS, "TMEM budget");
+// warps: 0 TMA producer, 1 MMA issuer, 2..5 scale stagers, 6..9 epilogue
+constexpr int NUM_THREADS = 320;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 }  // namespace g4
 
@@ -65,16 +80,19 @@ struct GemmParams {
   int64_t ldc;
 };
 
+template <int CM, int CN>
 __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_p, const __grid_constant__ CUtensorMap tmap_q,
                      const GemmParams p) {
   using namespace g4;
+  constexpr int CS = CM * CN;  // CTAs per cluster
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* acc_full = empty + STAGES;
+  uint64_t* sf_ready = empty + STAGES;
+  uint64_t* acc_full = sf_ready + STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* br_empty = acc_empty + 2;
   uint64_t* done_bar = br_empty + 1;
@@ -82,10 +100,18 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = CS > 1 ? cluster_ctarank() : 0;
+  const uint32_t cx = crank % CM, cy = crank / CM;  // position in the cluster (m, n)
+  uint16_t mask_a = 0, mask_b = 0;                  // CTAs sharing my A tile / my B tile
+  for (int j = 0; j < CN; ++j) mask_a |= (uint16_t)(1u << (cx + CM * j));
+  for (int i = 0; i < CM; ++i) mask_b |= (uint16_t)(1u << (i + CM * cy));
+  const uint16_t mask_all = (uint16_t)((1u << CS) - 1);
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CS);  // one commit from every CTA of the cluster
+      mbar_init(&sf_ready[s], 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -106,13 +132,17 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
   }
   if (warp == 1) tmem_alloc(tmem_slot, TM_COLS);
   tc_fence_before();
-  __syncthreads();
+  if (CS > 1) cluster_sync();  // every CTA's barriers exist before any multicast lands
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const uint32_t num_tiles = p.num_m * p.num_n;
+  // macro tiles of (CM*128) x (CN*128); the cluster walks them persistently
+  const uint32_t cluster_id = blockIdx.x / CS, num_clusters = gridDim.x / CS;
+  const uint32_t macro_m = p.num_m / CM, num_macro = macro_m * (p.num_n / CN);
   const uint32_t num_k = (p.K + BK - 1) / BK;
   const bool has_branch = p.r > 0;
+  const uint32_t n_iter = num_k + (has_branch ? 1 : 0);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -122,9 +152,8 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
       uint32_t armed_phase[STAGES];
       for (int s = 0; s < STAGES; ++s) armed[s] = 0, armed_phase[s] = 0;
       bool ok = true;
-      for (uint32_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const uint32_t mb = tile % p.num_m, nb = tile / p.num_m;
-        const uint32_t n_iter = num_k + (has_branch ? 1 : 0);
+      for (uint32_t mt = cluster_id; mt < num_macro && ok; mt += num_clusters) {
+        const uint32_t mb = (mt % macro_m) * CM + cx, nb = (mt / macro_m) * CN + cy;
         for (uint32_t it = 0; it < n_iter; ++it) {
           if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1)) {
             ok = false;
@@ -137,14 +166,40 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
           uint8_t* sSFB = sSFA + SFA_BYTES;
           if (it < num_k) {
             const uint32_t krem = p.K - it * BK;
-            const uint32_t nk = krem >= (uint32_t)BK ? BK / 64 : krem / 64;
+            const uint32_t nk = krem >= (uint32_t)BK ? BK / 64 : krem / 64;  // 64-wide K steps in this stage
             mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES + 2 * nk * SF_ATOM);
-            tma_load_2d(sA, &tmap_a, &full[stage], (int32_t)(it * (BK / 2)), (int32_t)(mb * BM));
-            tma_load_2d(sB, &tmap_b, &full[stage], (int32_t)(it * (BK / 2)), (int32_t)(nb * BN));
-            bulk_load(sSFA, p.a_scales + ((size_t)mb * p.atoms_k + it * (BK / 64)) * SF_ATOM, nk * SF_ATOM,
-                      &full[stage]);
-            bulk_load(sSFB, p.b_scales + ((size_t)nb * p.atoms_k + it * (BK / 64)) * SF_ATOM, nk * SF_ATOM,
-                      &full[stage]);
+            const int32_t kx = (int32_t)(it * (BK / 2));
+            // A: my 1/CN share of the A tile rows (and of its scale atoms), to the CTAs of my cluster row
+            const uint32_t a_rows = BM / CN, b_rows = BN / CM;
+            if (CN > 1)
+              tma_load_2d_mc(sA + cy * a_rows * 128, &tmap_a, &full[stage], kx, (int32_t)(mb * BM + cy * a_rows),
+                             mask_a);
+            else
+              tma_load_2d(sA, &tmap_a, &full[stage], kx, (int32_t)(mb * BM));
+            if (CM > 1)
+              tma_load_2d_mc(sB + cx * b_rows * 128, &tmap_b, &full[stage], kx, (int32_t)(nb * BN + cx * b_rows),
+                             mask_b);
+            else
+              tma_load_2d(sB, &tmap_b, &full[stage], kx, (int32_t)(nb * BN));
+            // scale atoms of this stage: nk atoms per operand, split between the sharing CTAs
+            const uint8_t* gA = p.a_scales + ((size_t)mb * p.atoms_k + it * (BK / 64)) * SF_ATOM;
+            const uint8_t* gB = p.b_scales + ((size_t)nb * p.atoms_k + it * (BK / 64)) * SF_ATOM;
+            {
+              const uint32_t per = (nk + CN - 1) / CN, a0 = cy * per;
+              const uint32_t cnt = a0 < nk ? min(per, nk - a0) : 0;
+              if (cnt) {
+                if (CN > 1) bulk_load_mc(sSFA + a0 * SF_ATOM, gA + a0 * SF_ATOM, cnt * SF_ATOM, &full[stage], mask_a);
+                else bulk_load(sSFA, gA, cnt * SF_ATOM, &full[stage]);
+              }
+            }
+            {
+              const uint32_t per = (nk + CM - 1) / CM, b0 = cx * per;
+              const uint32_t cnt = b0 < nk ? min(per, nk - b0) : 0;
+              if (cnt) {
+                if (CM > 1) bulk_load_mc(sSFB + b0 * SF_ATOM, gB + b0 * SF_ATOM, cnt * SF_ATOM, &full[stage], mask_b);
+                else bulk_load(sSFB, gB, cnt * SF_ATOM, &full[stage]);
+              }
+            }
           } else {
             mbar_arrive_expect_tx(&full[stage], P_BYTES + Q_BYTES);
             tma_load_2d(sA, &tmap_p, &full[stage], 0, (int32_t)(mb * BM));
@@ -170,32 +225,28 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       uint32_t t = 0;
-      for (uint32_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++t) {
+      for (uint32_t mt = cluster_id; mt < num_macro && ok; mt += num_clusters, ++t) {
         const uint32_t buf = t & 1;
         if (!mbar_wait(&acc_empty[buf], ((t >> 1) & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + TM_ACC + buf * BN;
         for (uint32_t it = 0; it < num_k; ++it) {
-          if (*abort_flag || !mbar_wait(&full[stage], phase)) { ok = false; break; }
+          if (*abort_flag || !mbar_wait(&full[stage], phase) || !mbar_wait(&sf_ready[stage], phase)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t sA = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sB = sA + A_BYTES;
-          const uint32_t sSFA = sB + B_BYTES;
-          const uint32_t sSFB = sSFA + SFA_BYTES;
           const uint32_t krem = p.K - it * BK;
           const uint32_t nk = krem >= (uint32_t)BK ? BK / 64 : krem / 64;
-          const uint32_t tsfa = tmem + TM_SF + stage * 32;
-          const uint32_t tsfb = tsfa + 16;
-          for (uint32_t kk = 0; kk < nk; ++kk) {
-            tc_cp_32x128b_warpx4(tsfa + kk * 4, smem_desc(sSFA + kk * SF_ATOM, 0, 128, kSwizzleNone));
-            tc_cp_32x128b_warpx4(tsfb + kk * 4, smem_desc(sSFB + kk * SF_ATOM, 0, 128, kSwizzleNone));
-          }
-          for (uint32_t kk = 0; kk < nk; ++kk) {
+          const uint32_t tsf = tmem + TM_SF + stage * TM_SF_STAGE;
+          for (uint32_t kk = 0; kk < nk; ++kk)
             mma_nvf4(d_tmem, smem_desc(sA + kk * 32, 16, 1024, kSwizzle128B),
-                     smem_desc(sB + kk * 32, 16, 1024, kSwizzle128B), idesc, tsfa + kk * 4, tsfb + kk * 4,
+                     smem_desc(sB + kk * 32, 16, 1024, kSwizzle128B), idesc, tsf + kk * 4, tsf + 16 + kk * 4,
                      (it | kk) != 0);
-          }
-          tc_commit(&empty[stage]);
+          if (CS > 1) tc_commit_mc(&empty[stage], mask_all);
+          else tc_commit(&empty[stage]);
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
         if (!ok) break;
@@ -209,7 +260,8 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
           for (uint32_t kk = 0; kk < nkb; ++kk)
             mma_bf16(tmem + TM_BR, smem_desc(sA + kk * 32, 16, 1024, kSwizzle128B),
                      smem_desc(sB + kk * 32, 16, 1024, kSwizzle128B), idesc_br, kk != 0);
-          tc_commit(&empty[stage]);
+          if (CS > 1) tc_commit_mc(&empty[stage], mask_all);
+          else tc_commit(&empty[stage]);
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
         tc_commit(&acc_full[buf]);
@@ -219,16 +271,72 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
       tc_commit(done_bar);
       mbar_wait(done_bar, 0);
     }
+  } else if (warp < 6) {
+    // ---------------- scale stagers (warps 2..5) ----------------
+    const uint32_t quad = warp & 3;
+    const uint32_t lane_off = (quad * 32) << 16;
+    uint32_t stage = 0, phase = 0;
+    for (uint32_t mt = cluster_id; mt < num_macro; mt += num_clusters) {
+      bool ok = true;
+      for (uint32_t it = 0; it < n_iter; ++it) {
+        // every use of a stage (scale-carrying or not) waits for its data and
+        // arrives once on sf_ready, so sf_ready's phase tracks full's
+        if (*abort_flag || !mbar_wait_warp(&full[stage], phase)) {
+          ok = false;
+          break;
+        }
+        if (it < num_k) {
+          const uint32_t krem = p.K - it * BK;
+          const uint32_t nk = krem >= (uint32_t)BK ? BK / 64 : krem / 64;
+          const uint8_t* sSFA = smem + stage * STAGE_BYTES + A_BYTES + B_BYTES;
+          const uint8_t* sSFB = sSFA + SFA_BYTES;
+          const uint32_t tsf = TM_SF + stage * TM_SF_STAGE;
+          uint32_t wa[16], wb[16];
+          // A row m = 32*quad + lane: its 4 scales of K step j sit in atom j at byte
+          // (m % 32) * 16 + (m / 32) * 4; the MMA reads them at column tsf + 4j + quad
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t v = (uint32_t)j < nk
+                                   ? *reinterpret_cast<const uint32_t*>(sSFA + j * SF_ATOM + lane * 16 + quad * 4)
+                                   : 0u;
+            wa[4 * j] = wa[4 * j + 1] = wa[4 * j + 2] = wa[4 * j + 3] = v;
+          }
+          tmem_st_32x32b_x16(tmem + lane_off + tsf, wa);
+          // B row n = lane + 32c: its scales of K step j at column tsf + 16 + 4j + c.  The MMA reads
+          // B scales for the rows of quadrant q from lanes 32q..32q+31, so every quadrant gets a copy.
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if ((uint32_t)j < nk) v = *reinterpret_cast<const uint4*>(sSFB + j * SF_ATOM + lane * 16);
+            wb[4 * j] = v.x;
+            wb[4 * j + 1] = v.y;
+            wb[4 * j + 2] = v.z;
+            wb[4 * j + 3] = v.w;
+          }
+          tmem_st_32x32b_x16(tmem + lane_off + tsf + 16, wb);
+          tmem_st_wait(wb);
+          tmem_st_wait(wa);
+          tc_fence_before();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_ready[stage]);
+        if (++stage == STAGES) stage = 0, phase ^= 1;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        break;
+      }
+    }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (warps 6..9) ----------------
     const uint32_t quad = warp & 3;  // TMEM lanes this warp may access
     const float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
     const float beta = p.beta;
     uint32_t t = 0;
-    for (uint32_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t) {
-      const uint32_t mb = tile % p.num_m, nb = tile / p.num_m;
+    for (uint32_t mt = cluster_id; mt < num_macro; mt += num_clusters, ++t) {
+      const uint32_t mb = (mt % macro_m) * CM + cx, nb = (mt / macro_m) * CN + cy;
       const uint32_t buf = t & 1;
-      if (*abort_flag || !mbar_wait(&acc_full[buf], (t >> 1) & 1)) {
+      if (*abort_flag || !mbar_wait_warp(&acc_full[buf], (t >> 1) & 1)) {
         *abort_flag = 1;
         break;
       }
@@ -240,7 +348,7 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
         uint32_t acc[32], br[32];
         tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + buf * BN + j * 32, acc);
         if (has_branch) tmem_ld_32x32b_x32(tmem + lane_off + TM_BR + j * 32, br);
-        tmem_ld_wait();
+        tmem_ld_wait(acc, br);
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -281,6 +389,8 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, TM_COLS);
   }
+  // no CTA leaves while a peer may still multicast into it or arrive on its barriers
+  if (CS > 1) cluster_sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -296,6 +406,15 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 }  // namespace bf
+
+__device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])
+               :
+               : "memory");
+}
 
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -387,13 +506,13 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
     }
   } else {
     const uint32_t quad = warp & 3;
-    if (!*abort_flag && mbar_wait(acc_full, 0)) {
+    if (!*abort_flag && mbar_wait_warp(acc_full, 0)) {
       tc_fence_after();
       const uint32_t row = m0 + quad * 32 + lane;
       for (int j = 0; j < r; j += 16) {
         uint32_t acc[16];
         tmem_ld_32x32b_x16(tmem + ((quad * 32) << 16) + j, acc);
-        tmem_ld_wait();
+        tmem_ld_wait16(acc);
         uint32_t w[8];
 #pragma unroll
         for (int h = 0; h < 8; ++h) {
@@ -467,17 +586,63 @@ static bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
+template <int CM, int CN>
+static cudaError_t launch_gemm_cluster(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tp,
+                                       const CUtensorMap& tq, const GemmParams& p, int num_sms, cudaStream_t s) {
   using namespace g4;
+  constexpr int CS = CM * CN;
+  auto kern = gemm_nvf4_kernel<CM, CN>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  static int max_clusters = 0;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (attr_err != cudaSuccess) return;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    cfg.gridDim = dim3(num_sms / CS * CS);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = CS;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (CS > 1) {
+      if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess || max_clusters <= 0)
+        max_clusters = num_sms / CS;
+    } else {
+      max_clusters = num_sms;
+    }
   });
   if (attr_err != cudaSuccess) return attr_err;
+  const uint32_t macro = (p.num_m / CM) * (p.num_n / CN);
+  const uint32_t clusters = macro < (uint32_t)max_clusters ? macro : (uint32_t)max_clusters;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  cfg.gridDim = dim3(clusters * CS);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = CS;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = CS > 1 ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tp, tq, p);
+  count_launch();
+  return e;
+}
+
+cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
+  using namespace g4;
+  const int cm = (g.M % (2 * BM) == 0) ? 2 : 1;
+  const int cn = (g.N % (2 * BN) == 0) ? 2 : 1;
   CUtensorMap ta, tb, tp, tq;
-  if (!make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_codes, g.K / 2, g.M, g.K / 2, BK / 2, BM) ||
-      !make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_codes, g.K / 2, g.N, g.K / 2, BK / 2, BN))
+  if (!make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_codes, g.K / 2, g.M, g.K / 2, BK / 2, BM / cn) ||
+      !make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_codes, g.K / 2, g.N, g.K / 2, BK / 2, BN / cm))
     return cudaErrorInvalidValue;
   if (g.r > 0) {
     if (!make_tmap(&tp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.P, g.r, g.M, (uint64_t)g.r * 2, BR_K, BM) ||
@@ -503,11 +668,10 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
   p.C = g.C;
   p.c_f32 = g.c_f32;
   p.ldc = g.ldc;
-  const uint32_t tiles = p.num_m * p.num_n;
-  const int grid = (int)(tiles < (uint32_t)num_sms ? tiles : (uint32_t)num_sms);
-  gemm_nvf4_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, tp, tq, p);
-  count_launch();
-  return cudaGetLastError();
+  if (cm == 2 && cn == 2) return launch_gemm_cluster<2, 2>(ta, tb, tp, tq, p, num_sms, s);
+  if (cm == 2) return launch_gemm_cluster<2, 1>(ta, tb, tp, tq, p, num_sms, s);
+  if (cn == 2) return launch_gemm_cluster<1, 2>(ta, tb, tp, tq, p, num_sms, s);
+  return launch_gemm_cluster<1, 1>(ta, tb, tp, tq, p, num_sms, s);
 }
 
 cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ldx, const void* L, int r, void* P,
