@@ -24,7 +24,9 @@ dequantized operands.  Functions and the passages they follow:
 - ``gemm`` / ``linear_fwd`` / ``linear_bwd``: the three products of a linear
   layer, Y = X W^T, dX = dY W, dW = dY^T X, with the residual in NVFP4 and the
   branch in BF16 (section 2.1).  READING: gradients (dY) use SR in both dX and
-  dW; X and W use RTN; beta = 1 unless given.
+  dW; X and W use RTN; beta = 1 unless given; the branch factor is stored as
+  P~ = bf16(P * beta / alpha) next to the residual's accumulator
+  (``fold_branch``).
 
 Parity pins: see ``tests/test_oracle_pins.py``.  The scale layout and the SR
 bit mapping are this library's chosen conventions (parity unpinned by the
@@ -291,13 +293,35 @@ def scales_to_mma(scales_rowmajor: np.ndarray) -> np.ndarray:
 # products (FP64 of exactly dequantized operands)
 # ---------------------------------------------------------------------------
 
-def gemm(deqA: np.ndarray, deqB: np.ndarray, P_bf16=None, Q_bf16=None, beta: float = 1.0) -> np.ndarray:
-    """out = A @ B^T (+ beta * P @ Q^T), FP64.  A: M x K, B: N x K, P: M x r, Q: N x r."""
+def fold_branch(P_bf16: np.ndarray, beta: float, S_tA: float, S_tB: float):
+    """The branch operand as stored next to the residual's accumulator.
+
+    READING (section 2.1 keeps the L2 L1 subspace in BF16 and adds it to the
+    same output): with alpha = fl32(S_tA * S_tB) (1 when that is 0) and
+    g = fl32(beta / alpha), the BF16 factor is P~ = bf16(fl32(P * g)), so that
+    alpha * (A B^T + P~ Q^T) = A_deq B_deq^T + beta P Q^T up to the one extra
+    BF16 rounding of P~.  Returns (alpha, P~ bits)."""
+    alpha = np.float32(np.float32(S_tA) * np.float32(S_tB))
+    if alpha == 0:
+        alpha = np.float32(1.0)
+    g = np.float32(np.float32(beta) / alpha)
+    prod = bf16_to_f32(P_bf16) * g  # float32 x float32 -> float32, IEEE round to nearest
+    return float(alpha), bf16_rn(prod.astype(np.float64))
+
+
+def gemm(deqA: np.ndarray, deqB: np.ndarray, P_bf16=None, Q_bf16=None, beta: float = 1.0,
+         S_tA: float | None = None, S_tB: float | None = None) -> np.ndarray:
+    """out = A @ B^T (+ alpha * P~ @ Q^T, see fold_branch), FP64.
+    A: M x K and B: N x K dequantized (tensor scales included); P: M x r, Q: N x r
+    BF16; S_tA, S_tB: the operands' tensor scales (required with a branch)."""
     out = deqA.astype(np.float64) @ deqB.astype(np.float64).T
     if P_bf16 is not None and P_bf16.shape[1] > 0:
-        P = bf16_to_f32(P_bf16).astype(np.float64)
+        if S_tA is None or S_tB is None:
+            raise ValueError("a branch needs the operands' tensor scales")
+        alpha, Pt = fold_branch(P_bf16, beta, S_tA, S_tB)
+        P = bf16_to_f32(Pt).astype(np.float64)
         Q = bf16_to_f32(Q_bf16).astype(np.float64)
-        out += float(beta) * (P @ Q.T)
+        out += alpha * (P @ Q.T)
     return out
 
 
@@ -337,7 +361,7 @@ def linear_fwd(X, W_res, L1, L2, beta: float = 1.0, out_rows=None):
     B = Wq.dequantize()
     if L1.shape[0] > 0:
         P = branch_factor(np.ascontiguousarray(X[rows]), L1)
-        Y = gemm(A, B, P, L2, beta)
+        Y = gemm(A, B, P, L2, beta, Xq.S_t, Wq.S_t)
     else:
         Y = gemm(A, B)
     return Y, Xq, Wq
@@ -356,7 +380,7 @@ def linear_bwd(dY, X, W_res, L1, L2, seed: int, beta: float = 1.0, dx_rows=None,
     B = WqT.dequantize()
     if L1.shape[0] > 0:
         P2 = branch_factor(np.ascontiguousarray(dY[xr]), np.ascontiguousarray(L2.T))
-        dX = gemm(A, B, P2, np.ascontiguousarray(L1.T), beta)
+        dX = gemm(A, B, P2, np.ascontiguousarray(L1.T), beta, dYq.S_t, WqT.S_t)
     else:
         dX = gemm(A, B)
     wr = slice(None) if dw_rows is None else np.asarray(dw_rows)

@@ -274,7 +274,8 @@ def test_gemm_exact_rational_tiny(oracle_mod):
     P = bf16_bits([1.5, -2.0, 0.5, 3.0]).reshape(2, 2)
     Q = bf16_bits([0.25, 1.0, -1.0, 2.0]).reshape(2, 2)
     A3 = np.vstack([A, np.zeros((0, 16))])
-    out = oracle_mod.gemm(A3[:2], B, P, Q, beta=0.5)
+    # tensor scales 1 and 1: alpha = 1, P~ = bf16(0.5 P) is exact for these P
+    out = oracle_mod.gemm(A3[:2], B, P, Q, beta=0.5, S_tA=1.0, S_tB=1.0)
     Pf, Qf = oracle_mod.bf16_to_f32(P), oracle_mod.bf16_to_f32(Q)
     for m in range(2):
         for n in range(2):
@@ -350,3 +351,22 @@ def test_linear_bwd_shapes_and_stream_independence(oracle_mod):
     # unbiased-ish: dW is close to the exact product
     exact = (oracle_mod.bf16_to_f32(dY).astype(np.float64).T @ oracle_mod.bf16_to_f32(X).astype(np.float64))
     assert np.linalg.norm(dW - exact) / np.linalg.norm(exact) < 0.3
+
+
+def test_branch_fold_alpha_one_is_exact_and_bounded_otherwise(oracle_mod):
+    rng = np.random.default_rng(15)
+    P = S.to_bf16_bits(rng.standard_normal((8, 16)).astype(np.float32))
+    Pf = oracle_mod.bf16_to_f32(P).astype(np.float64)
+    # alpha = 1, beta = 1: the fold is the identity
+    a, Pt = oracle_mod.fold_branch(P, 1.0, 1.0, 1.0)
+    assert a == 1.0 and np.array_equal(Pt, P)
+    # a zero tensor scale gives alpha = 1 and P~ = bf16(beta P)
+    a, Pt = oracle_mod.fold_branch(P, 0.5, 0.0, 3.0)
+    assert a == 1.0 and np.array_equal(oracle_mod.bf16_to_f32(Pt), (oracle_mod.bf16_to_f32(P) * np.float32(0.5)))
+    # general alpha: alpha * P~ is within one BF16 rounding (2^-8 relative, + FP32 steps) of beta P
+    S_tA, S_tB, beta = 0.00731, 0.0439, 0.8
+    a, Pt = oracle_mod.fold_branch(P, beta, S_tA, S_tB)
+    assert abs(a - S_tA * S_tB) <= 2e-7 * S_tA * S_tB
+    err = np.abs(a * oracle_mod.bf16_to_f32(Pt).astype(np.float64) - beta * Pf)
+    assert np.all(err <= (2.0 ** -8 + 1e-6) * beta * np.abs(Pf) + 1e-300)
+    assert np.any(err > 0)  # the rounding is real for this alpha
