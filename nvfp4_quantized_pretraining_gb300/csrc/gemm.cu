@@ -1,18 +1,19 @@
 // Tensor-core GEMMs for the NVFP4 linear projection (sm_103a, tcgen05):
 //
-//  * gemm_nvf4_kernel: C = S_tA S_tB * (A . SFA)(B . SFB)^T + beta * P Q^T.
-//    The NVFP4 residual product and the BF16 low-rank branch of the LoRA-SVD
-//    weight split (Full-Stack FP4, section 2.1, "Mechanism":
-//    W = W_res + beta L2 L1, the subspace in BF16, the residual in NVFP4) are
-//    accumulated in two tensor-memory accumulators of the same output tile and
-//    combined in the epilogue.
+//  * gemm_nvf4_pair_kernel (M, N multiples of 256) and gemm_nvf4_kernel
+//    (multiples of 128): C = alpha * (A B^T + P~ Q^T), alpha = S_tA S_tB, with
+//    A, B NVFP4 (E2M1 codes, UE4M3 scales per 16 elements) and the BF16
+//    low-rank branch of the LoRA-SVD weight split (Full-Stack FP4, section
+//    2.1, "Mechanism": W = W_res + beta L2 L1, the subspace in BF16, the
+//    residual in NVFP4) accumulated into the same tensor-memory accumulator
+//    after rescaling P~ = bf16(P * beta / alpha), so C is rounded once.
 //  * branch_factor_kernel: P = bf16(X L^T), the skinny BF16 product that
 //    feeds the branch (M x r, r <= 64).
 //
-// Both are warp-specialised: warp 0 issues TMA loads into a ring of shared
-// memory stages, warp 1 issues tcgen05.mma from one thread (accumulators in
-// TMEM), warps 2..5 drain TMEM with tcgen05.ld and write the output.  Every
-// mbarrier wait is bounded (FP4_ERR_TIMEOUT in the status word on expiry).
+// All are warp-specialised: a TMA producer warp fills a ring of shared-memory
+// stages, one thread issues tcgen05.mma (accumulators in TMEM), "scale" warps
+// stage block scales into TMEM, epilogue warps drain TMEM with tcgen05.ld.
+// Every mbarrier wait is bounded (FP4_ERR_TIMEOUT in the status word on expiry).
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
@@ -55,8 +56,7 @@ constexpr int P_BYTES = BM * BR_K * 2;            // 16 KB, fits the A slot
 constexpr int Q_BYTES = BN * BR_K * 2;            // 16 KB, fits the B slot
 // tensor memory columns
 constexpr uint32_t TM_ACC = 0;                    // 2 x BN accumulators (double buffered)
-constexpr uint32_t TM_BR = 2 * BN;                // BN branch accumulator
-constexpr uint32_t TM_SF = 3 * BN;                // per stage: SFA 16 + SFB 16 columns
+constexpr uint32_t TM_SF = 2 * BN;                // per stage: SFA 16 + SFB 16 columns
 constexpr uint32_t TM_SF_STAGE = 32;
 constexpr uint32_t TM_COLS = 512;
 static_assert(TM_SF + STAGES * TM_SF_STAGE <= TM_COLS, "TMEM budget");
@@ -94,8 +94,7 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
   uint64_t* sf_ready = empty + STAGES;
   uint64_t* acc_full = sf_ready + STAGES;
   uint64_t* acc_empty = acc_full + 2;
-  uint64_t* br_empty = acc_empty + 2;
-  uint64_t* done_bar = br_empty + 1;
+  uint64_t* done_bar = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -117,7 +116,6 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 4);
     }
-    mbar_init(br_empty, 4);
     mbar_init(done_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -143,6 +141,8 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
   const uint32_t num_k = (p.K + BK - 1) / BK;
   const bool has_branch = p.r > 0;
   const uint32_t n_iter = num_k + (has_branch ? 1 : 0);
+  float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
+  if (alpha == 0.0f) alpha = 1.0f;  // an all-zero operand contributes exact zeros
 
   if (warp == 0) {
     if (lane == 0) {
@@ -220,46 +220,54 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
+      // One thread issues every MMA, so the loop is kept lean: descriptors are
+      // a base plus a per-stage constant (the start-address field counts 16-byte
+      // units), a full 256-wide stage is four unrolled MMAs at +32-byte K
+      // offsets, and the abort flag is only consulted at tile boundaries.
       const uint32_t idesc = idesc_nvf4(BM, BN);
       const uint32_t idesc_br = idesc_bf16(BM, BN);
+      const uint64_t adesc0 = smem_desc(smem_u32(smem), 16, 1024, kSwizzle128B);
+      const uint64_t bdesc0 = adesc0 + (A_BYTES >> 4);
+      constexpr uint64_t kStageD = STAGE_BYTES >> 4;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       uint32_t t = 0;
       for (uint32_t mt = cluster_id; mt < num_macro && ok; mt += num_clusters, ++t) {
         const uint32_t buf = t & 1;
-        if (!mbar_wait(&acc_empty[buf], ((t >> 1) & 1) ^ 1)) { ok = false; break; }
+        if (*abort_flag || !mbar_wait(&acc_empty[buf], ((t >> 1) & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + TM_ACC + buf * BN;
         for (uint32_t it = 0; it < num_k; ++it) {
-          if (*abort_flag || !mbar_wait(&full[stage], phase) || !mbar_wait(&sf_ready[stage], phase)) {
+          if (!mbar_wait(&full[stage], phase) || !mbar_wait(&sf_ready[stage], phase)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sA = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t sB = sA + A_BYTES;
-          const uint32_t krem = p.K - it * BK;
-          const uint32_t nk = krem >= (uint32_t)BK ? BK / 64 : krem / 64;
+          const uint64_t ad = adesc0 + stage * kStageD, bd = bdesc0 + stage * kStageD;
           const uint32_t tsf = tmem + TM_SF + stage * TM_SF_STAGE;
-          for (uint32_t kk = 0; kk < nk; ++kk)
-            mma_nvf4(d_tmem, smem_desc(sA + kk * 32, 16, 1024, kSwizzle128B),
-                     smem_desc(sB + kk * 32, 16, 1024, kSwizzle128B), idesc, tsf + kk * 4, tsf + 16 + kk * 4,
-                     (it | kk) != 0);
+          const uint32_t krem = p.K - it * BK;
+          if (krem >= (uint32_t)BK) {
+            mma_nvf4(d_tmem, ad, bd, idesc, tsf, tsf + 16, it != 0);
+            mma_nvf4(d_tmem, ad + 2, bd + 2, idesc, tsf + 4, tsf + 20, 1);
+            mma_nvf4(d_tmem, ad + 4, bd + 4, idesc, tsf + 8, tsf + 24, 1);
+            mma_nvf4(d_tmem, ad + 6, bd + 6, idesc, tsf + 12, tsf + 28, 1);
+          } else {
+            for (uint32_t kk = 0; kk < krem / 64; ++kk)
+              mma_nvf4(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, tsf + kk * 4, tsf + 16 + kk * 4, (it | kk) != 0);
+          }
           if (CS > 1) tc_commit_mc(&empty[stage], mask_all);
           else tc_commit(&empty[stage]);
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
         if (!ok) break;
         if (has_branch) {
-          if (!mbar_wait(br_empty, (t & 1) ^ 1)) { ok = false; break; }
-          if (*abort_flag || !mbar_wait(&full[stage], phase)) { ok = false; break; }
+          // P~ Q^T (P~ rescaled in shared memory by the scale warps) accumulates onto A B^T
+          if (!mbar_wait(&full[stage], phase) || !mbar_wait(&sf_ready[stage], phase)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sA = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t sB = sA + A_BYTES;
+          const uint64_t ad = adesc0 + stage * kStageD, bd = bdesc0 + stage * kStageD;
           const uint32_t nkb = (uint32_t)(p.r + 15) / 16;
           for (uint32_t kk = 0; kk < nkb; ++kk)
-            mma_bf16(tmem + TM_BR, smem_desc(sA + kk * 32, 16, 1024, kSwizzle128B),
-                     smem_desc(sB + kk * 32, 16, 1024, kSwizzle128B), idesc_br, kk != 0);
+            mma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc_br, 1);
           if (CS > 1) tc_commit_mc(&empty[stage], mask_all);
           else tc_commit(&empty[stage]);
           if (++stage == STAGES) stage = 0, phase ^= 1;
@@ -275,6 +283,7 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
     // ---------------- scale stagers (warps 2..5) ----------------
     const uint32_t quad = warp & 3;
     const uint32_t lane_off = (quad * 32) << 16;
+    const float g = __fdiv_rn(p.beta, alpha);
     uint32_t stage = 0, phase = 0;
     for (uint32_t mt = cluster_id; mt < num_macro; mt += num_clusters) {
       bool ok = true;
@@ -317,6 +326,22 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
           tmem_st_wait(wb);
           tmem_st_wait(wa);
           tc_fence_before();
+        } else {
+          // branch stage: P~ = bf16(P * g) in place (an elementwise map, so the swizzle is irrelevant)
+          uint4* tile = reinterpret_cast<uint4*>(smem + stage * STAGE_BYTES);
+          const int tid = (warp - 2) * 32 + lane;
+#pragma unroll 4
+          for (int i = tid; i < P_BYTES / 16; i += 128) {
+            uint4 v = tile[i];
+            uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(bf16_lo(w[e]), g), __fmul_rn(bf16_hi(w[e]), g));
+              w[e] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            tile[i] = v;
+          }
+          fence_proxy_async_smem();
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sf_ready[stage]);
@@ -328,10 +353,8 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 6..9) ----------------
+    // ---------------- epilogue (warps 6..9): C = alpha * acc ----------------
     const uint32_t quad = warp & 3;  // TMEM lanes this warp may access
-    const float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
-    const float beta = p.beta;
     uint32_t t = 0;
     for (uint32_t mt = cluster_id; mt < num_macro; mt += num_clusters, ++t) {
       const uint32_t mb = (mt % macro_m) * CM + cx, nb = (mt / macro_m) * CN + cy;
@@ -345,16 +368,12 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
       const uint32_t lane_off = (quad * 32) << 16;
 #pragma unroll 1
       for (int j = 0; j < BN / 32; ++j) {
-        uint32_t acc[32], br[32];
+        uint32_t acc[32];
         tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + buf * BN + j * 32, acc);
-        if (has_branch) tmem_ld_32x32b_x32(tmem + lane_off + TM_BR + j * 32, br);
-        tmem_ld_wait(acc, br);
+        tmem_ld_wait(acc);
         float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          v[i] = __fmul_rn(alpha, __uint_as_float(acc[i]));
-          if (has_branch) v[i] = __fadd_rn(v[i], __fmul_rn(beta, __uint_as_float(br[i])));
-        }
+        for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(alpha, __uint_as_float(acc[i]));
         const size_t col = (size_t)nb * BN + j * 32;
         if (p.c_f32) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.C) + row * p.ldc + col);
@@ -376,10 +395,7 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&acc_empty[buf]);
-        if (has_branch) mbar_arrive(br_empty);
-      }
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
   }
 
@@ -391,6 +407,344 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
   }
   // no CTA leaves while a peer may still multicast into it or arrive on its barriers
   if (CS > 1) cluster_sync();
+}
+
+// ---------------------------------------------------------------------------
+// Block-scaled NVFP4 GEMM on CTA pairs (tcgen05 cta_group::2)
+//
+// A cluster of 2 CTAs on neighbouring SMs computes a 256 x 256 output tile
+// with 2-SM MMAs (M=256, N=256, K=64 per instruction).  CTA r of the pair
+// holds A rows [128r, 128r+128) and B rows [128r, 128r+128) of the tile in its
+// shared memory and receives output rows [128r, 128r+128) x 256 columns in its
+// tensor memory; the pair leader (r = 0) issues every MMA.  Each SM thus loads
+// half of the B tile and no A rows of its partner: per SM, 38 KB of operands
+// and scales per 256-wide K stage feed 16.8 MFLOP, half the bytes per FLOP of
+// a 128 x 128 single-SM tile, which is what bounds this GEMM.
+//
+// The LoRA-SVD branch (Full-Stack FP4, section 2.1: W = W_res + beta L2 L1,
+// subspace in BF16) is accumulated into the same TMEM accumulator: with
+// alpha = S_tA S_tB (1 when 0), the scale warps rewrite the P tile in shared
+// memory as P~ = bf16(P * (beta / alpha)) and BF16 MMAs add P~ Q^T, so that
+// C = alpha * (A B^T + P~ Q^T) is rounded once.
+// ---------------------------------------------------------------------------
+namespace g2 {
+constexpr int BK = 256;
+constexpr int STAGES = 5;
+constexpr int A_BYTES = 128 * BK / 2;            // 16 KB: this CTA's 128 A rows
+constexpr int B_BYTES = 128 * BK / 2;            // 16 KB: this CTA's 128 B rows
+constexpr int SF_ATOM = 512;
+constexpr int SFA_BYTES = 4 * SF_ATOM;           // 2 KB: scales of this CTA's A rows
+constexpr int SFB_BYTES = 8 * SF_ATOM;           // 4 KB: scales of all 256 B rows
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 38 KB
+constexpr int BR_K = 64;
+constexpr int P_BYTES = 128 * BR_K * 2;          // 16 KB (A slot)
+constexpr int Q_BYTES = 128 * BR_K * 2;          // 16 KB (B slot)
+constexpr uint32_t TM_ACC = 0;                   // 256 columns
+constexpr uint32_t TM_SF = 256;                  // per stage: SFA 16 + SFB 32 columns
+constexpr uint32_t TM_SF_STAGE = 48;
+constexpr uint32_t TM_COLS = 512;
+static_assert(TM_SF + STAGES * TM_SF_STAGE <= TM_COLS, "TMEM budget");
+// warps: 0 producer, 1 MMA (leader) / TMEM allocator, 2..5 scale stagers, 6..13 epilogue (2 per quadrant)
+constexpr int NUM_THREADS = 448;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+}  // namespace g2
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
+    gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                          const __grid_constant__ CUtensorMap tmap_p, const __grid_constant__ CUtensorMap tmap_q,
+                          const GemmParams p) {
+  using namespace g2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);  // leader: A/B (+Q) of both CTAs
+  uint64_t* sf_full = full + STAGES;        // each CTA: its scales (or P) landed
+  uint64_t* empty = sf_full + STAGES;       // each CTA: the stage was consumed by the MMAs
+  uint64_t* sf_ready = empty + STAGES;      // leader: scales in TMEM (and P~ in smem) in both CTAs
+  uint64_t* acc_full = sf_ready + STAGES;   // each CTA: accumulator complete
+  uint64_t* acc_empty = acc_full + 1;       // leader: both CTAs drained the accumulator
+  uint64_t* done_bar = acc_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&sf_full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&sf_ready[s], 8);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 16);  // 8 epilogue warps in each CTA of the pair
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_b);
+    if (p.r > 0) {
+      prefetch_tmap(&tmap_p);
+      prefetch_tmap(&tmap_q);
+    }
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, TM_COLS);
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const uint32_t cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
+  const uint32_t tiles_m = p.M / 256, num_tiles = tiles_m * (p.N / 256);
+  const uint32_t num_k = (p.K + BK - 1) / BK;
+  const bool has_branch = p.r > 0;
+  const uint32_t n_iter = num_k + (has_branch ? 1 : 0);
+  float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
+  if (alpha == 0.0f) alpha = 1.0f;  // an all-zero operand contributes exact zeros
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs) ----------------
+      const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);  // leader's full[] in the cluster window
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (uint32_t mt = cluster_id; mt < num_tiles && ok; mt += num_clusters) {
+        const uint32_t mb2 = mt % tiles_m, nb2 = mt / tiles_m;
+        for (uint32_t it = 0; it < n_iter; ++it) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sA = smem + stage * STAGE_BYTES;
+          uint8_t* sB = sA + A_BYTES;
+          uint8_t* sSFA = sB + B_BYTES;
+          uint8_t* sSFB = sSFA + SFA_BYTES;
+          const uint32_t full_l = full0 + stage * 8;
+          if (it < num_k) {
+            const uint32_t krem = p.K - it * BK;
+            const uint32_t nk = krem >= (uint32_t)BK ? 4 : krem / 64;
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A_BYTES + B_BYTES));
+            const int32_t kx = (int32_t)(it * (BK / 2));
+            tma_load_2d_pair(sA, &tmap_a, full_l, kx, (int32_t)(mb2 * 256 + rank * 128));
+            tma_load_2d_pair(sB, &tmap_b, full_l, kx, (int32_t)(nb2 * 256 + rank * 128));
+            mbar_arrive_expect_tx(&sf_full[stage], 3 * nk * SF_ATOM);
+            const size_t ka = (size_t)it * 4;
+            bulk_load(sSFA, p.a_scales + ((size_t)(mb2 * 2 + rank) * p.atoms_k + ka) * SF_ATOM, nk * SF_ATOM,
+                      &sf_full[stage]);
+            bulk_load(sSFB, p.b_scales + ((size_t)(nb2 * 2) * p.atoms_k + ka) * SF_ATOM, nk * SF_ATOM,
+                      &sf_full[stage]);
+            bulk_load(sSFB + 4 * SF_ATOM, p.b_scales + ((size_t)(nb2 * 2 + 1) * p.atoms_k + ka) * SF_ATOM,
+                      nk * SF_ATOM, &sf_full[stage]);
+          } else {
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * Q_BYTES);
+            tma_load_2d_pair(sB, &tmap_q, full_l, 0, (int32_t)(nb2 * 256 + rank * 128));
+            mbar_arrive_expect_tx(&sf_full[stage], P_BYTES);
+            tma_load_2d(sA, &tmap_p, &sf_full[stage], 0, (int32_t)(mb2 * 256 + rank * 128));
+          }
+          if (++stage == STAGES) stage = 0, phase ^= 1;
+        }
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (pair leader) ----------------
+      const uint32_t idesc = idesc_nvf4(256, 256);
+      const uint32_t idesc_br = idesc_bf16(256, 256);
+      const uint64_t adesc0 = smem_desc(smem_u32(smem), 16, 1024, kSwizzle128B);
+      const uint64_t bdesc0 = adesc0 + (A_BYTES >> 4);
+      constexpr uint64_t kStageD = STAGE_BYTES >> 4;
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      uint32_t t = 0;
+      for (uint32_t mt = cluster_id; mt < num_tiles && ok; mt += num_clusters, ++t) {
+        if (*abort_flag || !mbar_wait_cluster(acc_empty, (t & 1) ^ 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + TM_ACC;
+        for (uint32_t it = 0; it < num_k; ++it) {
+          if (!mbar_wait(&full[stage], phase) || !mbar_wait_cluster(&sf_ready[stage], phase)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = adesc0 + stage * kStageD, bd = bdesc0 + stage * kStageD;
+          const uint32_t tsf = tmem + TM_SF + stage * TM_SF_STAGE;
+          const uint32_t krem = p.K - it * BK;
+          if (krem >= (uint32_t)BK) {
+            mma_nvf4_pair(d_tmem, ad, bd, idesc, tsf, tsf + 16, it != 0);
+            mma_nvf4_pair(d_tmem, ad + 2, bd + 2, idesc, tsf + 4, tsf + 24, 1);
+            mma_nvf4_pair(d_tmem, ad + 4, bd + 4, idesc, tsf + 8, tsf + 32, 1);
+            mma_nvf4_pair(d_tmem, ad + 6, bd + 6, idesc, tsf + 12, tsf + 40, 1);
+          } else {
+            for (uint32_t kk = 0; kk < krem / 64; ++kk)
+              mma_nvf4_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, tsf + kk * 4, tsf + 16 + kk * 8,
+                            (it | kk) != 0);
+          }
+          tc_commit_pair_mc(&empty[stage], 3);
+          if (++stage == STAGES) stage = 0, phase ^= 1;
+        }
+        if (!ok) break;
+        if (has_branch) {
+          if (!mbar_wait(&full[stage], phase) || !mbar_wait_cluster(&sf_ready[stage], phase)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t ad = adesc0 + stage * kStageD, bd = bdesc0 + stage * kStageD;
+          const uint32_t nkb = (uint32_t)(p.r + 15) / 16;
+          for (uint32_t kk = 0; kk < nkb; ++kk) mma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc_br, 1);
+          tc_commit_pair_mc(&empty[stage], 3);
+          if (++stage == STAGES) stage = 0, phase ^= 1;
+        }
+        tc_commit_pair_mc(acc_full, 3);
+      }
+      if (!ok) *abort_flag = 1;
+      tc_commit_pair_mc(done_bar, 1);  // (a kernel may not mix cta_group::1 and ::2 forms)
+      mbar_wait(done_bar, 0);
+    }
+  } else if (warp < 6) {
+    // ---------------- scale stagers (warps 2..5, both CTAs) ----------------
+    const uint32_t quad = warp & 3;
+    const uint32_t lane_off = (quad * 32) << 16;
+    const uint32_t sf_ready0 = mapa_shared(smem_u32(&sf_ready[0]), 0);
+    const float g = __fdiv_rn(p.beta, alpha);
+    uint32_t stage = 0, phase = 0;
+    for (uint32_t mt = cluster_id; mt < num_tiles; mt += num_clusters) {
+      bool ok = true;
+      for (uint32_t it = 0; it < n_iter; ++it) {
+        if (*abort_flag || !mbar_wait_warp(&sf_full[stage], phase)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sA = smem + stage * STAGE_BYTES;
+        if (it < num_k) {
+          const uint32_t krem = p.K - it * BK;
+          const uint32_t nk = krem >= (uint32_t)BK ? 4 : krem / 64;
+          const uint8_t* sSFA = sA + A_BYTES + B_BYTES;
+          const uint8_t* sSFB = sSFA + SFA_BYTES;
+          const uint32_t tsf = TM_SF + stage * TM_SF_STAGE;
+          uint32_t wa[16], wb[32];
+          // A row m = 32*quad + lane: scales of K step j at atom j, byte (m%32)*16 + (m/32)*4;
+          // the MMA reads them at lane m, column tsf + 4j + quad
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t v = (uint32_t)j < nk
+                                   ? *reinterpret_cast<const uint32_t*>(sSFA + j * SF_ATOM + lane * 16 + quad * 4)
+                                   : 0u;
+            wa[4 * j] = wa[4 * j + 1] = wa[4 * j + 2] = wa[4 * j + 3] = v;
+          }
+          tmem_st_32x32b_x16(tmem + lane_off + tsf, wa);
+          // B row n = 32c + lane (c = 0..7): scales of K step j at column tsf + 16 + 8j + c, in every quadrant
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint4 v = make_uint4(0, 0, 0, 0);
+              if ((uint32_t)j < nk)
+                v = *reinterpret_cast<const uint4*>(sSFB + h * 4 * SF_ATOM + j * SF_ATOM + lane * 16);
+              wb[8 * j + 4 * h] = v.x;
+              wb[8 * j + 4 * h + 1] = v.y;
+              wb[8 * j + 4 * h + 2] = v.z;
+              wb[8 * j + 4 * h + 3] = v.w;
+            }
+          }
+          tmem_st_32x32b_x32(tmem + lane_off + tsf + 16, wb);
+          tmem_st_wait(wb);
+          tmem_st_wait(wa);
+          tc_fence_before();
+        } else {
+          // branch stage: P~ = bf16(P * g) in place (element order is irrelevant to an elementwise map)
+          uint4* tile = reinterpret_cast<uint4*>(sA);
+          const int tid = (warp - 2) * 32 + lane;
+#pragma unroll 4
+          for (int i = tid; i < P_BYTES / 16; i += 128) {
+            uint4 v = tile[i];
+            uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = __fmul_rn(bf16_lo(w[e]), g), hi = __fmul_rn(bf16_hi(w[e]), g);
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+              w[e] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            tile[i] = v;
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(sf_ready0 + stage * 8);
+        if (++stage == STAGES) stage = 0, phase ^= 1;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        break;
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 6..13, both CTAs): C = alpha * acc ----------------
+    const uint32_t quad = warp & 3, half = (uint32_t)(warp - 6) >> 2;
+    const uint32_t lane_off = (quad * 32) << 16;
+    const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
+    uint32_t t = 0;
+    for (uint32_t mt = cluster_id; mt < num_tiles; mt += num_clusters, ++t) {
+      const uint32_t mb2 = mt % tiles_m, nb2 = mt / tiles_m;
+      if (*abort_flag || !mbar_wait_warp(acc_full, t & 1)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const size_t row = (size_t)mb2 * 256 + rank * 128 + quad * 32 + lane;
+      const size_t col0 = (size_t)nb2 * 256 + half * 128;
+      if (!p.c_f32) {
+        // drain the accumulator into packed BF16 registers, release TMEM, then store
+        uint32_t packed[64];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t acc[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + half * 128 + j * 32, acc);
+          tmem_ld_wait(acc);
+#pragma unroll
+          for (int h = 0; h < 16; ++h) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(acc[2 * h])),
+                                                      __fmul_rn(alpha, __uint_as_float(acc[2 * h + 1])));
+            packed[16 * j + h] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty0);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + row * p.ldc + col0);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+      } else {
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          uint32_t acc[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + half * 128 + j * 32, acc);
+          tmem_ld_wait(acc);
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.C) + row * p.ldc + col0 + j * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__fmul_rn(alpha, __uint_as_float(acc[4 * i])),
+                                 __fmul_rn(alpha, __uint_as_float(acc[4 * i + 1])),
+                                 __fmul_rn(alpha, __uint_as_float(acc[4 * i + 2])),
+                                 __fmul_rn(alpha, __uint_as_float(acc[4 * i + 3])));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty0);
+      }
+    }
+  }
+
+  // the producer's copies complete before the CTA may exit: wait out every armed stage
+  __syncthreads();
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, TM_COLS);
+  }
+  cluster_sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -636,8 +990,66 @@ static cudaError_t launch_gemm_cluster(const CUtensorMap& ta, const CUtensorMap&
   return e;
 }
 
+static cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tp,
+                                    const CUtensorMap& tq, const GemmParams& p, int num_sms, cudaStream_t s) {
+  using namespace g2;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(gemm_nvf4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (attr_err != cudaSuccess) return;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms / 2 * 2);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, gemm_nvf4_pair_kernel, &cfg) != cudaSuccess ||
+        max_clusters <= 0)
+      max_clusters = num_sms / 2;
+    (void)cudaGetLastError();
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const uint32_t tiles = (p.M / 256) * (p.N / 256);
+  const uint32_t clusters = tiles < (uint32_t)max_clusters ? tiles : (uint32_t)max_clusters;
+  gemm_nvf4_pair_kernel<<<clusters * 2, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, tp, tq, p);
+  count_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
   using namespace g4;
+  if (g.M % 256 == 0 && g.N % 256 == 0) {
+    // 2-SM path: each CTA TMA-loads 128 rows of A and of B
+    CUtensorMap ta, tb, tp, tq;
+    if (!make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_codes, g.K / 2, g.M, g.K / 2, BK / 2, 128) ||
+        !make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_codes, g.K / 2, g.N, g.K / 2, BK / 2, 128))
+      return cudaErrorInvalidValue;
+    if (g.r > 0) {
+      if (!make_tmap(&tp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.P, g.r, g.M, (uint64_t)g.r * 2, BR_K, 128) ||
+          !make_tmap(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.Q, g.r, g.N, (uint64_t)g.r * 2, BR_K, 128))
+        return cudaErrorInvalidValue;
+    } else {
+      tp = ta;
+      tq = tb;
+    }
+    GemmParams p;
+    p.a_scales = static_cast<const uint8_t*>(g.a_scales);
+    p.b_scales = static_cast<const uint8_t*>(g.b_scales);
+    p.a_scale = g.a_scale;
+    p.b_scale = g.b_scale;
+    p.M = (uint32_t)g.M;
+    p.N = (uint32_t)g.N;
+    p.K = (uint32_t)g.K;
+    p.atoms_k = (uint32_t)(g.K / 64);
+    p.num_m = (uint32_t)(g.M / 128);
+    p.num_n = (uint32_t)(g.N / 128);
+    p.r = g.r;
+    p.beta = g.beta;
+    p.C = g.C;
+    p.c_f32 = g.c_f32;
+    p.ldc = g.ldc;
+    return launch_gemm_pair(ta, tb, tp, tq, p, num_sms, s);
+  }
   const int cm = (g.M % (2 * BM) == 0) ? 2 : 1;
   const int cn = (g.N % (2 * BN) == 0) ? 2 : 1;
   CUtensorMap ta, tb, tp, tq;

@@ -51,7 +51,7 @@ def check_gemm(F, oracle_mod, M, N, K, r, out_dtype, beta, seed, rows=None, a_ki
     F.fp4_check_status()
     sel = slice(None) if rows is None else rows
     ref = oracle_mod.gemm(oa.dequantize(rows), ob.dequantize(), None if P is None else np.ascontiguousarray(P[sel]),
-                          Q, beta)
+                          Q, beta, oa.S_t, ob.S_t)
     got = C.float().cpu().numpy().astype(np.float64)[sel]
     if out_dtype == torch.bfloat16:
         ref = oracle_mod.bf16_to_f32(oracle_mod.bf16_rn(ref)).astype(np.float64)
