@@ -671,7 +671,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
           fence_proxy_async_smem();
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(sf_ready0 + stage * 8);
+        if (lane == 0) {
+          if (leader) mbar_arrive(&sf_ready[stage]);
+          else if (it < num_k) mbar_arrive_cluster_relaxed(sf_ready0 + stage * 8);  // TMEM stores already complete
+          else mbar_arrive_cluster(sf_ready0 + stage * 8);  // P~ was written through the generic proxy
+        }
         if (++stage == STAGES) stage = 0, phase ^= 1;
       }
       if (!ok) {
