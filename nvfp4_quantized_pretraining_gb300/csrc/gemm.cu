@@ -715,7 +715,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(acc_empty0);
+        if (lane == 0) {
+          // the TMEM loads are complete (tcgen05.wait::ld), so only the phase flip has to travel
+          if (leader) mbar_arrive(acc_empty);
+          else mbar_arrive_cluster_relaxed(acc_empty0);
+        }
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + row * p.ldc + col0);
 #pragma unroll
         for (int i = 0; i < 16; ++i) dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
@@ -735,7 +739,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(acc_empty0);
+        if (lane == 0) {
+          // the TMEM loads are complete (tcgen05.wait::ld), so only the phase flip has to travel
+          if (leader) mbar_arrive(acc_empty);
+          else mbar_arrive_cluster_relaxed(acc_empty0);
+        }
       }
     }
   }
