@@ -429,7 +429,7 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
 // ---------------------------------------------------------------------------
 namespace g2 {
 constexpr int BK = 256;
-constexpr int STAGES = 5;
+constexpr int STAGES = 4;
 constexpr int A_BYTES = 128 * BK / 2;            // 16 KB: this CTA's 128 A rows
 constexpr int B_BYTES = 128 * BK / 2;            // 16 KB: this CTA's 128 B rows
 constexpr int SF_ATOM = 512;
@@ -439,14 +439,17 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 38 KB
 constexpr int BR_K = 64;
 constexpr int P_BYTES = 128 * BR_K * 2;          // 16 KB (A slot)
 constexpr int Q_BYTES = 128 * BR_K * 2;          // 16 KB (B slot)
+constexpr int OUT_PITCH = 256 * 2 + 16;          // BF16 staging row (padded against bank conflicts)
+constexpr int OUT_BYTES = 128 * OUT_PITCH;       // 66 KB: this CTA's 128 x 256 output tile
 constexpr uint32_t TM_ACC = 0;                   // 256 columns
 constexpr uint32_t TM_SF = 256;                  // per stage: SFA 16 + SFB 32 columns
 constexpr uint32_t TM_SF_STAGE = 48;
 constexpr uint32_t TM_COLS = 512;
 static_assert(TM_SF + STAGES * TM_SF_STAGE <= TM_COLS, "TMEM budget");
-// warps: 0 producer, 1 MMA (leader) / TMEM allocator, 2..5 scale stagers, 6..13 epilogue (2 per quadrant)
-constexpr int NUM_THREADS = 448;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+// warps: 0 A/B producer, 1 MMA (leader) + TMEM allocator, 2 scale/P producer,
+// 3..10 scale stagers (two per TMEM lane quadrant, two K steps each), 11..14 epilogue
+constexpr int NUM_THREADS = 480;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 1024 + 256;
 static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
 }  // namespace g2
 
@@ -457,9 +460,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
   using namespace g2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);  // leader: A/B (+Q) of both CTAs
+  uint8_t* sOut = smem + STAGES * STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + OUT_BYTES);  // leader: A/B (+Q) of both CTAs
   uint64_t* sf_full = full + STAGES;        // each CTA: its scales (or P) landed
-  uint64_t* empty = sf_full + STAGES;       // each CTA: the stage was consumed by the MMAs
+  uint64_t* empty = sf_full + STAGES;       // each CTA: the stage was consumed by the MMAs (both producers wait)
   uint64_t* sf_ready = empty + STAGES;      // leader: scales in TMEM (and P~ in smem) in both CTAs
   uint64_t* acc_full = sf_ready + STAGES;   // each CTA: accumulator complete
   uint64_t* acc_empty = acc_full + 1;       // leader: both CTAs drained the accumulator
@@ -475,10 +479,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
       mbar_init(&full[s], 1);
       mbar_init(&sf_full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&sf_ready[s], 8);
+      mbar_init(&sf_ready[s], 16);  // 8 stager warps in each CTA of the pair
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 16);  // 8 epilogue warps in each CTA of the pair
+    mbar_init(acc_empty, 8);  // 4 epilogue warps in each CTA
     mbar_init(done_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -505,9 +509,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
   float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
   if (alpha == 0.0f) alpha = 1.0f;  // an all-zero operand contributes exact zeros
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 2) {
     if (lane == 0) {
-      // ---------------- TMA producer (both CTAs) ----------------
+      // ---------------- producers (both CTAs): warp 0 operands (TMA), warp 2 scales / P ----------------
+      const bool ab = warp == 0;
       const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);  // leader's full[] in the cluster window
       uint32_t stage = 0, phase = 0;
       bool ok = true;
@@ -524,25 +529,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
           uint8_t* sSFB = sSFA + SFA_BYTES;
           const uint32_t full_l = full0 + stage * 8;
           if (it < num_k) {
-            const uint32_t krem = p.K - it * BK;
-            const uint32_t nk = krem >= (uint32_t)BK ? 4 : krem / 64;
-            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A_BYTES + B_BYTES));
-            const int32_t kx = (int32_t)(it * (BK / 2));
-            tma_load_2d_pair(sA, &tmap_a, full_l, kx, (int32_t)(mb2 * 256 + rank * 128));
-            tma_load_2d_pair(sB, &tmap_b, full_l, kx, (int32_t)(nb2 * 256 + rank * 128));
-            mbar_arrive_expect_tx(&sf_full[stage], 3 * nk * SF_ATOM);
-            const size_t ka = (size_t)it * 4;
-            bulk_load(sSFA, p.a_scales + ((size_t)(mb2 * 2 + rank) * p.atoms_k + ka) * SF_ATOM, nk * SF_ATOM,
-                      &sf_full[stage]);
-            bulk_load(sSFB, p.b_scales + ((size_t)(nb2 * 2) * p.atoms_k + ka) * SF_ATOM, nk * SF_ATOM,
-                      &sf_full[stage]);
-            bulk_load(sSFB + 4 * SF_ATOM, p.b_scales + ((size_t)(nb2 * 2 + 1) * p.atoms_k + ka) * SF_ATOM,
-                      nk * SF_ATOM, &sf_full[stage]);
+            if (ab) {
+              if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A_BYTES + B_BYTES));
+              const int32_t kx = (int32_t)(it * (BK / 2));
+              tma_load_2d_pair(sA, &tmap_a, full_l, kx, (int32_t)(mb2 * 256 + rank * 128));
+              tma_load_2d_pair(sB, &tmap_b, full_l, kx, (int32_t)(nb2 * 256 + rank * 128));
+            } else {
+              const uint32_t krem = p.K - it * BK;
+              const uint32_t nk = krem >= (uint32_t)BK ? 4 : krem / 64;
+              mbar_arrive_expect_tx(&sf_full[stage], 3 * nk * SF_ATOM);
+              const size_t ka = (size_t)it * 4;
+              bulk_load(sSFA, p.a_scales + ((size_t)(mb2 * 2 + rank) * p.atoms_k + ka) * SF_ATOM, nk * SF_ATOM,
+                        &sf_full[stage]);
+              bulk_load(sSFB, p.b_scales + ((size_t)(nb2 * 2) * p.atoms_k + ka) * SF_ATOM, nk * SF_ATOM,
+                        &sf_full[stage]);
+              bulk_load(sSFB + 4 * SF_ATOM, p.b_scales + ((size_t)(nb2 * 2 + 1) * p.atoms_k + ka) * SF_ATOM,
+                        nk * SF_ATOM, &sf_full[stage]);
+            }
           } else {
-            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * Q_BYTES);
-            tma_load_2d_pair(sB, &tmap_q, full_l, 0, (int32_t)(nb2 * 256 + rank * 128));
-            mbar_arrive_expect_tx(&sf_full[stage], P_BYTES);
-            tma_load_2d(sA, &tmap_p, &sf_full[stage], 0, (int32_t)(mb2 * 256 + rank * 128));
+            if (ab) {
+              if (leader) mbar_arrive_expect_tx(&full[stage], 2 * Q_BYTES);
+              tma_load_2d_pair(sB, &tmap_q, full_l, 0, (int32_t)(nb2 * 256 + rank * 128));
+            } else {
+              mbar_arrive_expect_tx(&sf_full[stage], P_BYTES);
+              tma_load_2d(sA, &tmap_p, &sf_full[stage], 0, (int32_t)(mb2 * 256 + rank * 128));
+            }
           }
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
@@ -602,9 +613,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
       tc_commit_pair_mc(done_bar, 1);  // (a kernel may not mix cta_group::1 and ::2 forms)
       mbar_wait(done_bar, 0);
     }
-  } else if (warp < 6) {
-    // ---------------- scale stagers (warps 2..5, both CTAs) ----------------
-    const uint32_t quad = warp & 3;
+  } else if (warp < 11) {
+    // ---------------- scale stagers (warps 3..10, both CTAs) ----------------
+    // warp w serves TMEM lane quadrant w % 4 and the two K steps {2h, 2h+1}, h = (w - 3) / 4
+    const uint32_t quad = warp & 3, h = (uint32_t)(warp - 3) >> 2;
     const uint32_t lane_off = (quad * 32) << 16;
     const uint32_t sf_ready0 = mapa_shared(smem_u32(&sf_ready[0]), 0);
     const float g = __fdiv_rn(p.beta, alpha);
@@ -623,41 +635,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
           const uint8_t* sSFA = sA + A_BYTES + B_BYTES;
           const uint8_t* sSFB = sSFA + SFA_BYTES;
           const uint32_t tsf = TM_SF + stage * TM_SF_STAGE;
-          uint32_t wa[16], wb[32];
+          uint32_t wa[8], wb[16];
           // A row m = 32*quad + lane: scales of K step j at atom j, byte (m%32)*16 + (m/32)*4;
           // the MMA reads them at lane m, column tsf + 4j + quad
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t v = (uint32_t)j < nk
-                                   ? *reinterpret_cast<const uint32_t*>(sSFA + j * SF_ATOM + lane * 16 + quad * 4)
-                                   : 0u;
-            wa[4 * j] = wa[4 * j + 1] = wa[4 * j + 2] = wa[4 * j + 3] = v;
+          for (int jj = 0; jj < 2; ++jj) {
+            const uint32_t j = 2 * h + jj;
+            const uint32_t v =
+                j < nk ? *reinterpret_cast<const uint32_t*>(sSFA + j * SF_ATOM + lane * 16 + quad * 4) : 0u;
+            wa[4 * jj] = wa[4 * jj + 1] = wa[4 * jj + 2] = wa[4 * jj + 3] = v;
           }
-          tmem_st_32x32b_x16(tmem + lane_off + tsf, wa);
-          // B row n = 32c + lane (c = 0..7): scales of K step j at column tsf + 16 + 8j + c, in every quadrant
+          tmem_st_32x32b_x8(tmem + lane_off + tsf + 8 * h, wa);
+          // B row n = 32c + lane (c = 0..7): scales of K step j at column tsf + 16 + 8j + c, every quadrant
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int jj = 0; jj < 2; ++jj) {
+            const uint32_t j = 2 * h + jj;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int hh = 0; hh < 2; ++hh) {
               uint4 v = make_uint4(0, 0, 0, 0);
-              if ((uint32_t)j < nk)
-                v = *reinterpret_cast<const uint4*>(sSFB + h * 4 * SF_ATOM + j * SF_ATOM + lane * 16);
-              wb[8 * j + 4 * h] = v.x;
-              wb[8 * j + 4 * h + 1] = v.y;
-              wb[8 * j + 4 * h + 2] = v.z;
-              wb[8 * j + 4 * h + 3] = v.w;
+              if (j < nk) v = *reinterpret_cast<const uint4*>(sSFB + hh * 4 * SF_ATOM + j * SF_ATOM + lane * 16);
+              wb[8 * jj + 4 * hh] = v.x;
+              wb[8 * jj + 4 * hh + 1] = v.y;
+              wb[8 * jj + 4 * hh + 2] = v.z;
+              wb[8 * jj + 4 * hh + 3] = v.w;
             }
           }
-          tmem_st_32x32b_x32(tmem + lane_off + tsf + 16, wb);
+          tmem_st_32x32b_x16(tmem + lane_off + tsf + 16 + 16 * h, wb);
           tmem_st_wait(wb);
-          tmem_st_wait(wa);
+          tmem_st_wait8(wa);
           tc_fence_before();
         } else {
-          // branch stage: P~ = bf16(P * g) in place (element order is irrelevant to an elementwise map)
+          // branch stage: P~ = bf16(P * g) in place (an elementwise map, so the swizzle is irrelevant)
           uint4* tile = reinterpret_cast<uint4*>(sA);
-          const int tid = (warp - 2) * 32 + lane;
+          const int tid = (warp - 3) * 32 + lane;
 #pragma unroll 4
-          for (int i = tid; i < P_BYTES / 16; i += 128) {
+          for (int i = tid; i < P_BYTES / 16; i += 256) {
             uint4 v = tile[i];
             uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
@@ -684,10 +696,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 6..13, both CTAs): C = alpha * acc ----------------
-    const uint32_t quad = warp & 3, half = (uint32_t)(warp - 6) >> 2;
+    // ---------------- epilogue (warps 11..14, both CTAs): C = alpha * acc ----------------
+    const uint32_t quad = warp & 3;
     const uint32_t lane_off = (quad * 32) << 16;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
+    uint8_t* stg = sOut + quad * 32 * OUT_PITCH;  // this warp's 32 staged rows
     uint32_t t = 0;
     for (uint32_t mt = cluster_id; mt < num_tiles; mt += num_clusters, ++t) {
       const uint32_t mb2 = mt % tiles_m, nb2 = mt / tiles_m;
@@ -696,22 +709,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const size_t row = (size_t)mb2 * 256 + rank * 128 + quad * 32 + lane;
-      const size_t col0 = (size_t)nb2 * 256 + half * 128;
+      const size_t row0 = (size_t)mb2 * 256 + rank * 128 + quad * 32;
+      const size_t col0 = (size_t)nb2 * 256;
       if (!p.c_f32) {
-        // drain the accumulator into packed BF16 registers, release TMEM, then store
-        uint32_t packed[64];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        // TMEM -> registers -> BF16 -> padded shared staging; release TMEM; coalesced row stores
+#pragma unroll 1
+        for (int j = 0; j < 8; ++j) {
           uint32_t acc[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + half * 128 + j * 32, acc);
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + j * 32, acc);
           tmem_ld_wait(acc);
+          uint32_t pk[16];
 #pragma unroll
-          for (int h = 0; h < 16; ++h) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(acc[2 * h])),
-                                                      __fmul_rn(alpha, __uint_as_float(acc[2 * h + 1])));
-            packed[16 * j + h] = *reinterpret_cast<uint32_t*>(&b2);
+          for (int e = 0; e < 16; ++e) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(acc[2 * e])),
+                                                      __fmul_rn(alpha, __uint_as_float(acc[2 * e + 1])));
+            pk[e] = *reinterpret_cast<uint32_t*>(&b2);
           }
+          uint4* dst = reinterpret_cast<uint4*>(stg + lane * OUT_PITCH + j * 64);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
         tc_fence_before();
         __syncwarp();
@@ -720,14 +736,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
           if (leader) mbar_arrive(acc_empty);
           else mbar_arrive_cluster_relaxed(acc_empty0);
         }
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + row * p.ldc + col0);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        // 32 rows of 512 bytes: lane i writes bytes [16i, 16i+16) of each row
+#pragma unroll 4
+        for (int r = 0; r < 32; ++r) {
+          const uint4 v = *reinterpret_cast<const uint4*>(stg + r * OUT_PITCH + lane * 16);
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + (row0 + r) * p.ldc + col0 + lane * 8) = v;
+        }
+        __syncwarp();
       } else {
+        const size_t row = row0 + lane;
 #pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 8; ++j) {
           uint32_t acc[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + half * 128 + j * 32, acc);
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + j * 32, acc);
           tmem_ld_wait(acc);
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.C) + row * p.ldc + col0 + j * 32);
 #pragma unroll
@@ -740,7 +761,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          // the TMEM loads are complete (tcgen05.wait::ld), so only the phase flip has to travel
           if (leader) mbar_arrive(acc_empty);
           else mbar_arrive_cluster_relaxed(acc_empty0);
         }
@@ -748,7 +768,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
     }
   }
 
-  // the producer's copies complete before the CTA may exit: wait out every armed stage
   __syncthreads();
   tc_fence_before();
   cluster_sync();
