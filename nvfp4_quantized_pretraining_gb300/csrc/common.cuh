@@ -479,26 +479,23 @@ __device__ __forceinline__ BlockScale block_scale(float amax_b, float S_t) {
 __device__ __forceinline__ float tensor_scale(float amax) { return amax == 0.0f ? 0.0f : __fdiv_rn(amax, 2688.0f); }
 
 // Stochastic rounding of y to the E2M1 grid with 16 random bits: returns the
-// rounded value (a grid point, sign of y kept).
+// rounded value (a grid point, sign of y kept).  With a = min(|y|, 6), lo the
+// grid point <= a and sp the gap above it, the value rounds up iff
+// rnd16 < frac * 65536, frac = (a - lo) / sp.  In the binary32 encoding of a:
+//   a >= 1        : lo keeps the top mantissa bit, frac = low 22 mantissa bits / 2^22,
+//                   so the test is (rnd16 << 6) < m22 and rounding up adds 1 << 22;
+//   0.5 <= a < 1  : lo = 0.5, sp = 0.5, frac = m23 / 2^23: (rnd16 << 7) < m23;
+//   a < 0.5       : lo = 0, sp = 0.5, frac * 65536 = a * 2^17 (exact).
+// All comparisons are exact, so this equals the arithmetic definition bit for bit.
 __device__ __forceinline__ float sr_round(float y, uint32_t rnd16) {
-  const float a = fminf(fabsf(y), 6.0f);
-  float lo, sp;
-  if (a < 2.0f) {
-    lo = floorf(a * 2.0f) * 0.5f;
-    sp = 0.5f;
-  } else if (a < 4.0f) {
-    lo = floorf(a);
-    sp = 1.0f;
-  } else if (a < 6.0f) {
-    lo = 4.0f;
-    sp = 2.0f;
-  } else {
-    lo = 6.0f;
-    sp = 0.0f;
-  }
-  const float frac = (a - lo) * (sp == 0.5f ? 2.0f : (sp == 1.0f ? 1.0f : 0.5f));
-  const float m = (static_cast<float>(rnd16) < frac * 65536.0f) ? lo + sp : lo;
-  return copysignf(m, y);
+  const uint32_t bits = __float_as_uint(y);
+  const uint32_t sign = bits & 0x80000000u;
+  const uint32_t ab = min(bits & 0x7FFFFFFFu, 0x40C00000u);  // min(|y|, 6) on the encodings
+  const uint32_t hi = (ab & 0xFFC00000u) + ((uint32_t)((rnd16 << 6) < (ab & 0x003FFFFFu)) << 22);
+  const uint32_t mid = ((rnd16 << 7) < (ab & 0x007FFFFFu)) ? 0x3F800000u : 0x3F000000u;
+  const uint32_t low = (static_cast<float>(rnd16) < __uint_as_float(ab) * 131072.0f) ? 0x3F000000u : 0u;
+  const uint32_t r = ab >= 0x3F800000u ? hi : (ab >= 0x3F000000u ? mid : low);
+  return __uint_as_float(r | sign);
 }
 
 }  // namespace nvfp4

@@ -9,6 +9,8 @@
 // Format reading (the Full-Stack FP4 pages name NVFP4, section 1, and
 // "standard NVFP4", section 3, without defining it): see block_scale() and
 // tensor_scale() in common.cuh.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -165,11 +167,13 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const RowQuantArgs a
 
 // ---------------------------------------------------------------------------
 // Column-wise (transposed) quantization, optionally with the row-wise output
-// from the same read.  A CTA stages a 64-row x 128-column BF16 tile in shared
-// memory; the row form is produced from registers right after the load, the
-// column form from the staged tile (one thread per column, two 16-row blocks).
-// SR random bits of the column form are drawn in the row-chunk mapping (one
-// Philox call per 8 source elements) and staged beside the tile.
+// from the same read.  A CTA stages a 128-row x 128-column BF16 tile in shared
+// memory (8 coalesced 16-byte loads per thread in flight); the row form is
+// produced from registers right after the load, the column form from the
+// staged tile: a thread owns two adjacent columns (one 4-byte shared load per
+// row yields both) and 32 rows, i.e. four 16-row blocks.  SR random bits of
+// the column form are drawn in the row-chunk mapping (one Philox call per 8
+// source elements) and staged beside the tile.
 // ---------------------------------------------------------------------------
 struct DualQuantArgs {
   const uint16_t* x;
@@ -190,12 +194,14 @@ struct DualQuantArgs {
   uint32_t stream_r, stream_c;
 };
 
-constexpr int kTileR = 64, kTileC = 128;
+constexpr int kTileR = 128, kTileC = 128;
+constexpr int kDualThreads = 256;
 
 template <bool ROW, bool COL, bool SR>
-__global__ void __launch_bounds__(256) quantize_dual_kernel(const DualQuantArgs a) {
-  __shared__ __align__(16) uint16_t tile[kTileR][kTileC];
-  __shared__ __align__(16) uint16_t rtile[SR && COL ? kTileR : 1][SR && COL ? kTileC : 8];
+__global__ void __launch_bounds__(kDualThreads) quantize_dual_kernel(const DualQuantArgs a) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  uint16_t(*tile)[kTileC] = reinterpret_cast<uint16_t(*)[kTileC]>(dsm);
+  uint16_t(*rtile)[kTileC] = reinterpret_cast<uint16_t(*)[kTileC]>(dsm + kTileR * kTileC * 2);
   const float amax = *a.amax;
   const float S_t = tensor_scale(amax);
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
@@ -204,30 +210,30 @@ __global__ void __launch_bounds__(256) quantize_dual_kernel(const DualQuantArgs 
   }
   const uint32_t r0 = blockIdx.y * kTileR, c0 = blockIdx.x * kTileC;
   const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const bool pack4 = (a.cols & 63u) == 0;
+  constexpr int kLoads = kTileR * (kTileC / 8) / kDualThreads;  // 8
 
-  uint4 w[4];
+  uint4 w[kLoads];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int q = tid + i * 256;
+  for (int i = 0; i < kLoads; ++i) {
+    const int q = tid + i * kDualThreads;
     const uint32_t row = r0 + (q >> 4), c8 = (c0 >> 3) + (q & 15);
     w[i] = make_uint4(0, 0, 0, 0);
     if (row < a.rows && c8 < a.cpr) w[i] = __ldcs(reinterpret_cast<const uint4*>(a.x + row * a.ld + c8 * 8));
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int q = tid + i * 256;
+  for (int i = 0; i < kLoads; ++i) {
+    const int q = tid + i * kDualThreads;
     const uint32_t row = r0 + (q >> 4), c8 = (c0 >> 3) + (q & 15);
     const bool valid = row < a.rows && c8 < a.cpr;
     if (COL) {
       *reinterpret_cast<uint4*>(&tile[q >> 4][(q & 15) * 8]) = w[i];
       if (SR) {
+        // element e of the chunk takes word e/2, low half for even e: in element order
+        // the eight 16-bit draws are exactly the four words as stored
         const uint4 rc = sr_random(a.seed, a.stream_c, (uint64_t)row * a.cpr + c8);
-        // element i of the chunk takes word i/2, low half for even i: store the
-        // eight 16-bit draws in element order
-        uint16_t* dst = &rtile[q >> 4][(q & 15) * 8];
-        const uint32_t rw[4] = {rc.x, rc.y, rc.z, rc.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) dst[e] = static_cast<uint16_t>((e & 1) ? (rw[e >> 1] >> 16) : rw[e >> 1]);
+        *reinterpret_cast<uint4*>(&rtile[q >> 4][(q & 15) * 8]) = rc;
       }
     }
     if (ROW) {
@@ -249,54 +255,97 @@ __global__ void __launch_bounds__(256) quantize_dual_kernel(const DualQuantArgs 
         for (int e = 0; e < 8; ++e) y[e] = sr_round(y[e], (e & 1) ? (rw[e >> 1] >> 16) : (rw[e >> 1] & 0xFFFFu));
       }
       const uint32_t codes = e2m1x8(y);
-      if (valid) {
-        *reinterpret_cast<uint32_t*>(a.codes_r + (size_t)row * (a.cols >> 1) + c8 * 4) = codes;
-        if ((q & 1) == 0) a.scales_r[sf_offset(row, c8 >> 1, a.atoms_k_r)] = static_cast<uint8_t>(bs.sb);
+      if (valid) *reinterpret_cast<uint32_t*>(a.codes_r + (size_t)row * (a.cols >> 1) + c8 * 4) = codes;
+      if (pack4) {
+        // lanes 8k, 8k+2, 8k+4, 8k+6 hold four consecutive scales of one row
+        const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 2);
+        const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 4);
+        const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 6);
+        if (valid && (lane & 7) == 0)
+          *reinterpret_cast<uint32_t*>(a.scales_r + sf_offset(row, c8 >> 1, a.atoms_k_r)) =
+              bs.sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+      } else if (valid && (q & 1) == 0) {
+        a.scales_r[sf_offset(row, c8 >> 1, a.atoms_k_r)] = static_cast<uint8_t>(bs.sb);
       }
     }
   }
   if (!COL) return;
   __syncthreads();
 
-  const uint32_t c = tid & (kTileC - 1);
-  const uint32_t col = c0 + c;
+  // column phase: columns c0 + 2cp, c0 + 2cp + 1; rows r0 + 32rq .. +31 (blocks 2rq .. 2rq+1 of 16)
+  const uint32_t cp = tid & 63, rq = tid >> 6;
+  const uint32_t col = c0 + 2 * cp;
   if (col >= a.cols) return;
-  uint32_t sb2 = 0;
-  const uint32_t rb0 = (tid >> 7) * 2;  // this thread's first 16-row block in the tile
+  const bool has2 = col + 1 < a.cols;
+  uint32_t sbits[2] = {0, 0};
+  uint4 cbuf[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const uint32_t rb = rb0 + h;
-    const uint32_t rowb = r0 + rb * 16;
-    float v[16];
-    uint32_t m = 0;
+    const uint32_t rb = 2 * rq + h;  // 16-row block within the tile
+    float va[16], vb[16];
+    uint32_t ma = 0, mb = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const uint32_t bits = tile[rb * 16 + i][c];
-      m = max(m, bits & 0x7FFFu);
-      v[i] = __uint_as_float(bits << 16);
+      const uint32_t pr = *reinterpret_cast<const uint32_t*>(&tile[rb * 16 + i][2 * cp]);
+      ma = max(ma, pr & 0x7FFFu);
+      mb = max(mb, (pr >> 16) & 0x7FFFu);
+      va[i] = bf16_lo(pr);
+      vb[i] = bf16_hi(pr);
     }
-    const BlockScale bs = block_scale(__uint_as_float(m << 16), S_t);
-    float y[16];
+    const BlockScale sa = block_scale(__uint_as_float(ma << 16), S_t);
+    const BlockScale sb = block_scale(__uint_as_float(mb << 16), S_t);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(v[i], bs.inv);
+    for (int i = 0; i < 16; ++i) {
+      va[i] = __fmul_rn(va[i], sa.inv);
+      vb[i] = __fmul_rn(vb[i], sb.inv);
+    }
     if (SR) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] = sr_round(y[i], rtile[rb * 16 + i][c]);
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t rp = *reinterpret_cast<const uint32_t*>(&rtile[rb * 16 + i][2 * cp]);
+        va[i] = sr_round(va[i], rp & 0xFFFFu);
+        vb[i] = sr_round(vb[i], rp >> 16);
+      }
     }
-    float lo8[8], hi8[8];
+    float t8[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) { lo8[i] = y[i]; hi8[i] = y[8 + i]; }
-    const uint2 codes = make_uint2(e2m1x8(lo8), e2m1x8(hi8));
-    if (rowb < a.rows)
-      *reinterpret_cast<uint2*>(a.codes_c + (size_t)col * (a.rows >> 1) + (rowb >> 1)) = codes;
-    sb2 |= bs.sb << (8 * h);
+    for (int i = 0; i < 8; ++i) t8[i] = va[i];
+    const uint32_t a0 = e2m1x8(t8);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t8[i] = va[8 + i];
+    const uint32_t a1 = e2m1x8(t8);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t8[i] = vb[i];
+    const uint32_t b0 = e2m1x8(t8);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t8[i] = vb[8 + i];
+    const uint32_t b1 = e2m1x8(t8);
+    if (h == 0) {
+      cbuf[0].x = a0; cbuf[0].y = a1; cbuf[1].x = b0; cbuf[1].y = b1;
+    } else {
+      cbuf[0].z = a0; cbuf[0].w = a1; cbuf[1].z = b0; cbuf[1].w = b1;
+    }
+    sbits[0] |= sa.sb << (8 * h);
+    sbits[1] |= sb.sb << (8 * h);
   }
-  const uint32_t kb = (r0 >> 4) + rb0;  // even, so kb and kb+1 share one 32-bit group
-  if (r0 + rb0 * 16 < a.rows) {
-    if (r0 + (rb0 + 1) * 16 < a.rows)
-      *reinterpret_cast<uint16_t*>(a.scales_c + sf_offset(col, kb, a.atoms_k_c)) = static_cast<uint16_t>(sb2);
-    else
-      a.scales_c[sf_offset(col, kb, a.atoms_k_c)] = static_cast<uint8_t>(sb2);
+  const uint32_t rowb = r0 + 32 * rq;  // first source row of this thread's 32
+  const uint32_t kb = rowb >> 4;       // even: kb and kb+1 share one 32-bit scale group
+  if (rowb < a.rows) {
+    const bool two = rowb + 16 < a.rows;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (j == 1 && !has2) break;
+      uint8_t* cdst = a.codes_c + (size_t)(col + j) * (a.rows >> 1) + (rowb >> 1);
+      if (two && (((a.rows >> 1) & 15u) == 0)) {
+        *reinterpret_cast<uint4*>(cdst) = cbuf[j];
+      } else {
+        *reinterpret_cast<uint2*>(cdst) = make_uint2(cbuf[j].x, cbuf[j].y);
+        if (two) *reinterpret_cast<uint2*>(cdst + 8) = make_uint2(cbuf[j].z, cbuf[j].w);
+      }
+      uint8_t* sdst = a.scales_c + sf_offset(col + j, kb, a.atoms_k_c);
+      if (two) *reinterpret_cast<uint16_t*>(sdst) = static_cast<uint16_t>(sbits[j]);
+      else *sdst = static_cast<uint8_t>(sbits[j]);
+    }
   }
 }
 
@@ -395,15 +444,26 @@ cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int6
   a.stream_c = stream_c;
   dim3 grid(static_cast<unsigned>((cols + kTileC - 1) / kTileC), static_cast<unsigned>((rows + kTileR - 1) / kTileR));
   const bool R = row_out != nullptr, C = col_out != nullptr;
+  const int smem = C ? kTileR * kTileC * 2 * (sr ? 2 : 1) : 0;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(quantize_dual_kernel<true, true, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kTileR * kTileC * 2);
+    if (attr == cudaSuccess)
+      attr = cudaFuncSetAttribute(quantize_dual_kernel<false, true, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kTileR * kTileC * 2);
+  });
+  if (attr != cudaSuccess) return attr;
   if (R && C) {
-    if (sr) quantize_dual_kernel<true, true, true><<<grid, 256, 0, s>>>(a);
-    else quantize_dual_kernel<true, true, false><<<grid, 256, 0, s>>>(a);
+    if (sr) quantize_dual_kernel<true, true, true><<<grid, kDualThreads, smem, s>>>(a);
+    else quantize_dual_kernel<true, true, false><<<grid, kDualThreads, smem, s>>>(a);
   } else if (C) {
-    if (sr) quantize_dual_kernel<false, true, true><<<grid, 256, 0, s>>>(a);
-    else quantize_dual_kernel<false, true, false><<<grid, 256, 0, s>>>(a);
+    if (sr) quantize_dual_kernel<false, true, true><<<grid, kDualThreads, smem, s>>>(a);
+    else quantize_dual_kernel<false, true, false><<<grid, kDualThreads, smem, s>>>(a);
   } else {
-    if (sr) quantize_dual_kernel<true, false, true><<<grid, 256, 0, s>>>(a);
-    else quantize_dual_kernel<true, false, false><<<grid, 256, 0, s>>>(a);
+    if (sr) quantize_dual_kernel<true, false, true><<<grid, kDualThreads, smem, s>>>(a);
+    else quantize_dual_kernel<true, false, false><<<grid, kDualThreads, smem, s>>>(a);
   }
   count_launch();
   return cudaGetLastError();
