@@ -178,6 +178,18 @@ uint64_t fp4_launch_count(void);
 fp4_status fp4_debug_convert(const float* in, int64_t n, uint8_t* e2m1_out,
                              uint8_t* e4m3_out, void* stream);
 
+/* Diagnostic: stochastically round n floats (device) to E2M1 with the
+ * quantizer's own rounding routine, element i using the 16 random bits
+ * rnd16[i] (device), so tests can drive exact ties and denormals that Philox
+ * draws reach only by chance.  Element i rounds up in magnitude iff
+ * rnd16[i] < frac * 2^16, frac its position between the two neighbouring grid
+ * points (magnitude clamped to 6 first; sign kept).  One code per byte in
+ * e2m1_out.  0 < n <= 2^34.  Stochastic rounding is the one "Full-Stack FP4"
+ * (gist.science explainer) names in section 2.2; the 16-bit comparison is this
+ * library's reading of it (see the encoding note at the top). */
+fp4_status fp4_debug_sr_round(const float* in, const uint16_t* rnd16, int64_t n,
+                              uint8_t* e2m1_out, void* stream);
+
 /* Diagnostic: dense NVFP4 tensor-core rate probe.  Launches one CTA per SM;
  * each issues 4 * iters block-scaled MMAs of shape M=128 x N=n x K=64
  * (n in {128, 256}) on operands resident in shared memory.  The caller times

@@ -34,7 +34,7 @@ OUT_F32 = 1
 EXPORTS = ["fp4_scale_bytes", "fp4_amax", "fp4_quantize", "fp4_quantize_transposed", "fp4_quantize_dual",
            "fp4_gemm_blockscaled", "fp4_branch_factor", "fp4_linear_fwd_workspace", "fp4_linear_bwd_workspace",
            "fp4_linear_fwd", "fp4_linear_bwd", "fp4_check_status", "fp4_last_error", "fp4_launch_count",
-           "fp4_debug_convert", "fp4_mma_peak_probe"]
+           "fp4_debug_convert", "fp4_debug_sr_round", "fp4_mma_peak_probe"]
 
 
 class FP4Error(RuntimeError):
@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
         "fp4_last_error": (ctypes.c_char_p, []),
         "fp4_launch_count": (u64, []),
         "fp4_debug_convert": (i32, [P, i64, P, P, P]),
+        "fp4_debug_sr_round": (i32, [P, P, i64, P, P]),
         "fp4_mma_peak_probe": (i32, [i32, i32, P, P]),
     }
     for name, (res, args) in sig.items():
@@ -261,6 +262,17 @@ def fp4_debug_convert(x: torch.Tensor, stream=None):
     e4m3 = torch.empty(n, dtype=torch.uint8, device=x.device)
     _check(lib().fp4_debug_convert(x.data_ptr(), n, e2m1.data_ptr(), e4m3.data_ptr(), _stream(stream)))
     return e2m1, e4m3
+
+
+def fp4_debug_sr_round(y: torch.Tensor, rnd16: torch.Tensor, stream=None) -> torch.Tensor:
+    """Stochastic rounding of float32 ``y`` with the given 16-bit random values
+    (int32 or uint16 tensor on the same device); E2M1 codes, one per byte."""
+    assert y.dtype == torch.float32 and y.is_contiguous() and y.numel() > 0
+    r = rnd16.to(torch.int32).to(torch.int16).contiguous()  # same bits as uint16
+    assert r.numel() == y.numel() and r.device == y.device
+    out = torch.empty(y.numel(), dtype=torch.uint8, device=y.device)
+    _check(lib().fp4_debug_sr_round(y.data_ptr(), r.data_ptr(), y.numel(), out.data_ptr(), _stream(stream)))
+    return out
 
 
 def fp4_mma_peak_probe(n: int = 256, iters: int = 20000, stream=None) -> dict:

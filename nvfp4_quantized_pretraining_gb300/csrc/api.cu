@@ -373,6 +373,13 @@ fp4_status fp4_debug_convert(const float* in, int64_t n, uint8_t* e2m1_out, uint
   return FP4_OK;
 }
 
+fp4_status fp4_debug_sr_round(const float* in, const uint16_t* rnd16, int64_t n, uint8_t* e2m1_out, void* stream) {
+  if (!in || !rnd16 || !e2m1_out || n <= 0 || n > (int64_t(1) << 34))
+    return fail(FP4_ERR_INVALID_ARG, "bad debug_sr_round arguments");
+  CUDA_TRY(launch_debug_sr_round(in, rnd16, n, e2m1_out, static_cast<cudaStream_t>(stream)));
+  return FP4_OK;
+}
+
 fp4_status fp4_mma_peak_probe(int n, int iters, int* num_sms_out, void* stream) {
   if ((n != 128 && n != 256) || iters <= 0) return fail(FP4_ERR_INVALID_ARG, "probe needs n in {128, 256}, iters > 0");
   const int sms = sm_count();

@@ -395,21 +395,48 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon et al., SC'11)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// The ten round keys of a (seed lo, seed hi) key: round r uses
+// (k0 + r * 0x9E3779B9, k1 + r * 0xBB67AE85).  Computed once per thread.
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+__device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
+  PhiloxKeys k;
+  uint32_t a = static_cast<uint32_t>(seed), b = static_cast<uint32_t>(seed >> 32);
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    if (r > 0) {
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
-    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k.k0[r] = a;
+    k.k1[r] = b;
+    a += 0x9E3779B9u;
+    b += 0xBB67AE85u;
+  }
+  return k;
+}
+// One round: 64-bit products give hi and lo of c0*M0 and c2*M1 in one multiply each.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys& k) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c.x;
+    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c.z;
+    c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k.k0[r], static_cast<uint32_t>(p1),
+                   static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k.k1[r], static_cast<uint32_t>(p0));
   }
   return c;
 }
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+  PhiloxKeys k;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    k.k0[r] = k0 + static_cast<uint32_t>(r) * 0x9E3779B9u;
+    k.k1[r] = k1 + static_cast<uint32_t>(r) * 0xBB67AE85u;
+  }
+  return philox4x32_10(c, k);
+}
 
 // The 128 random bits for element group j (elements 8j..8j+7) of a tensor.
+__device__ __forceinline__ uint4 sr_random(const PhiloxKeys& k, uint32_t stream, uint64_t j) {
+  return philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(j >> 32), stream, 0u), k);
+}
 __device__ __forceinline__ uint4 sr_random(uint64_t seed, uint32_t stream, uint64_t j) {
   return philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(j >> 32), stream, 0u),
                        static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
@@ -480,22 +507,29 @@ __device__ __forceinline__ float tensor_scale(float amax) { return amax == 0.0f 
 
 // Stochastic rounding of y to the E2M1 grid with 16 random bits: returns the
 // rounded value (a grid point, sign of y kept).  With a = min(|y|, 6), lo the
-// grid point <= a and sp the gap above it, the value rounds up iff
-// rnd16 < frac * 65536, frac = (a - lo) / sp.  In the binary32 encoding of a:
-//   a >= 1        : lo keeps the top mantissa bit, frac = low 22 mantissa bits / 2^22,
-//                   so the test is (rnd16 << 6) < m22 and rounding up adds 1 << 22;
-//   0.5 <= a < 1  : lo = 0.5, sp = 0.5, frac = m23 / 2^23: (rnd16 << 7) < m23;
-//   a < 0.5       : lo = 0, sp = 0.5, frac * 65536 = a * 2^17 (exact).
-// All comparisons are exact, so this equals the arithmetic definition bit for bit.
+// grid point <= a and sp the gap above it (0.5 below 2, 1 in [2, 4), 2 in
+// [4, 6]), the value rounds up iff rnd16 < frac * 65536, frac = (a - lo) / sp,
+// i.e. iff frac > u with u = rnd16 / 65536.  That is the same as
+//   result = sp * ceil(a / sp - u) = ceil_sp(a - u * sp),
+// which is computed on the floating-point pipe:
+//   sp from the exponent of a: max(2^(e-1), 0.5);
+//   u = (1 + rnd16 * 2^-16) - 1, exact (rnd16 fills the top 16 mantissa bits);
+//   t = a - u * sp rounded upward (one fused multiply-add);
+//   ceil_sp(t) = (t + M rounded upward) - M with M = 1.5 * 2^23 * sp, whose
+//   binade has spacing sp and holds t + M for every t in (-sp, 6].
+// Upward rounding of t to its own (finer) grid commutes with the ceiling to
+// multiples of sp, so the result equals the arithmetic definition bit for bit
+// (denormal inputs included: no flush to zero in this code).
 __device__ __forceinline__ float sr_round(float y, uint32_t rnd16) {
   const uint32_t bits = __float_as_uint(y);
-  const uint32_t sign = bits & 0x80000000u;
   const uint32_t ab = min(bits & 0x7FFFFFFFu, 0x40C00000u);  // min(|y|, 6) on the encodings
-  const uint32_t hi = (ab & 0xFFC00000u) + ((uint32_t)((rnd16 << 6) < (ab & 0x003FFFFFu)) << 22);
-  const uint32_t mid = ((rnd16 << 7) < (ab & 0x007FFFFFu)) ? 0x3F800000u : 0x3F000000u;
-  const uint32_t low = (static_cast<float>(rnd16) < __uint_as_float(ab) * 131072.0f) ? 0x3F000000u : 0u;
-  const uint32_t r = ab >= 0x3F800000u ? hi : (ab >= 0x3F000000u ? mid : low);
-  return __uint_as_float(r | sign);
+  const int32_t spb = max(static_cast<int32_t>(ab & 0x7F800000u) - 0x00800000, 0x3F000000);
+  const float sp = __int_as_float(spb);
+  const float M = __int_as_float(spb + 0x0BC00000);
+  const float u = __uint_as_float(0x3F800000u | (rnd16 << 7)) - 1.0f;
+  const float t = __fmaf_ru(-u, sp, __uint_as_float(ab));
+  const float c = __fadd_ru(t, M) - M;
+  return __uint_as_float(__float_as_uint(c) | (bits & 0x80000000u));
 }
 
 }  // namespace nvfp4

@@ -87,7 +87,7 @@ struct RowQuantArgs {
 
 template <bool SR>
 __device__ __forceinline__ void quantize_chunk_row(const RowQuantArgs& a, uint32_t g, bool valid, const uint4& w,
-                                                   float S_t, bool pack4) {
+                                                   float S_t, bool pack4, const PhiloxKeys& keys) {
   const int lane = threadIdx.x & 31;
   float v[8];
   v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
@@ -101,7 +101,7 @@ __device__ __forceinline__ void quantize_chunk_row(const RowQuantArgs& a, uint32
 #pragma unroll
   for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(v[i], bs.inv);
   if (SR) {
-    const uint4 rnd = sr_random(a.seed, a.stream, g);
+    const uint4 rnd = sr_random(keys, a.stream, g);
     const uint32_t rw[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) y[i] = sr_round(y[i], (i & 1) ? (rw[i >> 1] >> 16) : (rw[i >> 1] & 0xFFFFu));
@@ -132,6 +132,8 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const RowQuantArgs a
   }
   // cols % 64 == 0: every aligned group of 8 chunks is 4 whole blocks of one row
   const bool pack4 = (a.cols & 63u) == 0;
+  PhiloxKeys keys;
+  if (SR) keys = philox_keys(a.seed);
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const RowQuantArgs a
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const uint32_t g = base + u * nwarps * 32 + lane;
-      quantize_chunk_row<SR>(a, g, g < a.nchunks, w[u], S_t, pack4);
+      quantize_chunk_row<SR>(a, g, g < a.nchunks, w[u], S_t, pack4, keys);
     }
   }
   for (; base < a.nchunks; base += nwarps * 32) {
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const RowQuantArgs a
       const uint32_t row = g / a.cpr, c8 = g - row * a.cpr;
       w = __ldcs(reinterpret_cast<const uint4*>(a.x + row * a.ld + c8 * 8));
     }
-    quantize_chunk_row<SR>(a, g, g < a.nchunks, w, S_t, pack4);
+    quantize_chunk_row<SR>(a, g, g < a.nchunks, w, S_t, pack4, keys);
   }
 }
 
@@ -212,6 +214,8 @@ __global__ void __launch_bounds__(kDualThreads) quantize_dual_kernel(const DualQ
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const bool pack4 = (a.cols & 63u) == 0;
+  PhiloxKeys keys;
+  if (SR) keys = philox_keys(a.seed);
   constexpr int kLoads = kTileR * (kTileC / 8) / kDualThreads;  // 8
 
   uint4 w[kLoads];
@@ -232,7 +236,7 @@ __global__ void __launch_bounds__(kDualThreads) quantize_dual_kernel(const DualQ
       if (SR) {
         // element e of the chunk takes word e/2, low half for even e: in element order
         // the eight 16-bit draws are exactly the four words as stored
-        const uint4 rc = sr_random(a.seed, a.stream_c, (uint64_t)row * a.cpr + c8);
+        const uint4 rc = sr_random(keys, a.stream_c, (uint64_t)row * a.cpr + c8);
         *reinterpret_cast<uint4*>(&rtile[q >> 4][(q & 15) * 8]) = rc;
       }
     }
@@ -249,7 +253,7 @@ __global__ void __launch_bounds__(kDualThreads) quantize_dual_kernel(const DualQ
 #pragma unroll
       for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(v[e], bs.inv);
       if (SR) {
-        const uint4 rr = sr_random(a.seed, a.stream_r, (uint64_t)row * a.cpr + c8);
+        const uint4 rr = sr_random(keys, a.stream_r, (uint64_t)row * a.cpr + c8);
         const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
 #pragma unroll
         for (int e = 0; e < 8; ++e) y[e] = sr_round(y[e], (e & 1) ? (rw[e >> 1] >> 16) : (rw[e >> 1] & 0xFFFFu));
@@ -368,6 +372,20 @@ __global__ void debug_convert_kernel(const float* __restrict__ in, int64_t n, ui
     }
 }
 
+// Diagnostic stochastic rounding: the quantizer's own sr_round on given random bits.
+__global__ void debug_sr_round_kernel(const float* __restrict__ in, const uint16_t* __restrict__ rnd, int64_t n,
+                                      uint8_t* __restrict__ e2m1) {
+  const int64_t i8 = (int64_t)(blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (i8 >= n) return;
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = (i8 + i < n) ? sr_round(in[i8 + i], rnd[i8 + i]) : 0.0f;
+  const uint32_t c = e2m1x8(v);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (i8 + i < n) e2m1[i8 + i] = (c >> (4 * i)) & 0xFu;
+}
+
 // ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
@@ -473,6 +491,14 @@ cudaError_t launch_debug_convert(const float* in, int64_t n, uint8_t* e2m1, uint
   const int64_t threads = (n + 7) / 8;
   const int grid = static_cast<int>((threads + 255) / 256);
   debug_convert_kernel<<<grid, 256, 0, s>>>(in, n, e2m1, e4m3);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_sr_round(const float* in, const uint16_t* rnd, int64_t n, uint8_t* e2m1, cudaStream_t s) {
+  const int64_t threads = (n + 7) / 8;
+  const int grid = static_cast<int>((threads + 255) / 256);
+  debug_sr_round_kernel<<<grid, 256, 0, s>>>(in, rnd, n, e2m1);
   count_launch();
   return cudaGetLastError();
 }

@@ -58,6 +58,34 @@ def test_conversion_conventions(F, oracle_mod):
     assert np.array_equal(e4m3.cpu().numpy(), oracle_mod.e4m3_encode(s))
 
 
+def sr_cases(rng):
+    """Inputs and 16-bit draws that hit every branch of the SR rule: all three
+    gap sizes, saturation, signed zeros, denormals, and exact ties
+    rnd16 == frac * 2^16 (which must round down)."""
+    y = [rng.uniform(-7, 7, 200000), rng.uniform(-2, 2, 100000), rng.uniform(-1, 1, 50000) * 1e-3,
+         rng.standard_normal(20000) * 1e-39,
+         np.array([0.0, -0.0, 0.5, 1.0, 1.5, 2, 3, 4, 6, 7, -6.5, 0.25, 0.75, 5.999999, 1e-40, 0.4999999,
+                   0.9999999, 1.9999999, 3.9999999, 5.0, 4.0000005, 1e30, -1e30])]
+    y = np.concatenate(y).astype(np.float32)
+    rnd = rng.integers(0, 65536, y.size).astype(np.uint32)
+    rnd[:46] = np.array([0, 65535] * 23, np.uint32)
+    k = rng.integers(0, 6 * 131072, 100000)           # magnitudes on a 2^-17 grid
+    yt = (k / 131072.0).astype(np.float32) * rng.choice(np.array([-1, 1], np.float32), k.size)
+    a = np.abs(yt).astype(np.float64)
+    sp = np.where(a >= 4, 2.0, np.where(a >= 2, 1.0, 0.5))
+    tie = (np.round((a - np.floor(a / sp) * sp) / sp * 65536).astype(np.int64) & 0xFFFF).astype(np.uint32)
+    return np.concatenate([y, yt]), np.concatenate([rnd, tie])
+
+
+def test_sr_rounding_rule(F, oracle_mod):
+    y, rnd = sr_cases(np.random.default_rng(11))
+    got = F.fp4_debug_sr_round(torch.from_numpy(y).to(DEV), torch.from_numpy(rnd.astype(np.int32)).to(DEV))
+    want = oracle_mod.e2m1_sr(y, rnd)
+    g = got.cpu().numpy()
+    bad = np.flatnonzero(g != want)
+    assert bad.size == 0, f"{bad.size} of {y.size} differ, e.g. y={y[bad[:4]]} rnd={rnd[bad[:4]]}"
+
+
 SHAPES = [  # rows % 16 == 0 (the transposed form needs whole 16-row blocks); ragged vs 128-row tiles
     (16, 16), (128, 64), (256, 512), (208, 48), (96, 1040), (1008, 4096), (512, 512),
 ]
