@@ -148,6 +148,34 @@ fp4_status fp4_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx,
                           float beta, void* Y, int64_t ldy, fp4_tensor* xqT_saved,
                           void* ws, size_t ws_bytes, void* stream);
 
+/* fp4_linear_fwd without a caller workspace; the call allocates nothing.
+ * Same arguments, result and launches as fp4_linear_fwd minus ws/ws_bytes:
+ * the workspace lives in a 32 MiB file-scope device buffer of this library
+ * (a static __device__ array, created when the module loads).  The pages have
+ * no counterpart to this call: it is an interface variant, not part of the
+ * method.
+ * For callers that cannot allocate device memory: plain C host code linked
+ * only against this library, which has no device allocator of its own, and
+ * callers that must not call cudaMalloc/cudaFree in the middle of a step
+ * (cudaFree synchronises the device; with the rest of HBM reserved by a
+ * caching allocator, cudaMalloc fails for lack of memory).
+ * Limit: fp4_linear_fwd_workspace(M, N, K, r) <= 32 MiB (about M * K <= 50e6
+ * at r = 64, e.g. M = 16384, K = 3072); larger shapes return
+ * FP4_ERR_WORKSPACE, with the sizes in fp4_last_error(), before anything is
+ * launched.
+ * Nothing in the scratch has to start at zero: each call zeroes what it
+ * reduces into (the amax slot) before use and overwrites the rest.
+ * The first call on each device looks the buffer's address up
+ * (cudaGetSymbolAddress, which can load the module) and caches it; make that
+ * first call on each device before any stream capture begins.
+ * All calls on one device share the one buffer: calls whose executions can
+ * overlap (unordered streams, several host threads) race on it and give wrong
+ * results.  Order them (one stream, or events). */
+fp4_status fp4_linear_fwd_noalloc(const void* X, int64_t M, int64_t K, int64_t ldx,
+                                  const fp4_tensor* Wq, const void* L1, const void* L2, int r,
+                                  float beta, void* Y, int64_t ldy, fp4_tensor* xqT_saved,
+                                  void* stream);
+
 /* Linear projection backward (section 2.1, backward pass; the subspace
  * constraint on the factor update is not part of this call):
  *   dX = S_tdY S_tW dYq WqT^T + beta * bf16(dY L2) L1     (M x K, BF16)

@@ -33,7 +33,7 @@ OUT_F32 = 1
 
 EXPORTS = ["fp4_scale_bytes", "fp4_amax", "fp4_quantize", "fp4_quantize_transposed", "fp4_quantize_dual",
            "fp4_gemm_blockscaled", "fp4_branch_factor", "fp4_linear_fwd_workspace", "fp4_linear_bwd_workspace",
-           "fp4_linear_fwd", "fp4_linear_bwd", "fp4_check_status", "fp4_last_error", "fp4_launch_count",
+           "fp4_linear_fwd", "fp4_linear_fwd_noalloc", "fp4_linear_bwd", "fp4_check_status", "fp4_last_error", "fp4_launch_count",
            "fp4_debug_convert", "fp4_debug_sr_round", "fp4_mma_peak_probe"]
 
 
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
         "fp4_linear_fwd_workspace": (ctypes.c_size_t, [i64, i64, i64, i32]),
         "fp4_linear_bwd_workspace": (ctypes.c_size_t, [i64, i64, i64, i32]),
         "fp4_linear_fwd": (i32, [P, i64, i64, i64, T, P, P, i32, f32, P, i64, T, P, ctypes.c_size_t, P]),
+        "fp4_linear_fwd_noalloc": (i32, [P, i64, i64, i64, T, P, P, i32, f32, P, i64, T, P]),
         "fp4_linear_bwd": (i32, [P, i64, i64, i64, T, T, P, P, i32, f32, u64, P, i64, P, i32, i64, P,
                                  ctypes.c_size_t, P]),
         "fp4_check_status": (i32, [P]),
@@ -223,6 +224,17 @@ def fp4_linear_fwd(X, Wq: NVFP4Tensor, L1=None, L2=None, beta=1.0, Y=None, xqT_s
     _check(lib().fp4_linear_fwd(X.data_ptr(), M, K, ldx, ctypes.byref(cw), _ptr(L1), _ptr(L2), r, float(beta),
                                 Y.data_ptr(), Y.stride(0), ctypes.byref(cx), workspace.data_ptr(),
                                 workspace.numel(), _stream(stream)))
+    return Y, xqT_saved
+
+
+def fp4_linear_fwd_noalloc(X, Wq: NVFP4Tensor, L1, L2, beta, Y, xqT_saved, stream=None):
+    """fp4_linear_fwd with the library's static scratch instead of a workspace.
+    Y (M x N BF16) and xqT_saved (K x M) are caller-owned; nothing is allocated."""
+    M, K, ldx = _bf16_2d(X, "X")
+    r = 0 if L1 is None else L1.shape[0]
+    cw, cx = Wq.c(), xqT_saved.c()
+    _check(lib().fp4_linear_fwd_noalloc(X.data_ptr(), M, K, ldx, ctypes.byref(cw), _ptr(L1), _ptr(L2), r,
+                                        float(beta), Y.data_ptr(), Y.stride(0), ctypes.byref(cx), _stream(stream)))
     return Y, xqT_saved
 
 

@@ -240,6 +240,28 @@ static size_t bwd_ws(int64_t M, int64_t N, int64_t K, int r, Carver* c, fp4_tens
   return cv.off;
 }
 
+// Scratch of fp4_linear_fwd_noalloc: one file-scope device buffer, created with
+// the module, so that call needs no allocation.  32 MiB holds the forward
+// workspace up to M * K ~ 50e6 elements at r = 64 (e.g. M = 16384, K = 3072).
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up on the
+// first call per device and cached.
+static fp4_status noalloc_scratch(void** out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(FP4_ERR_INVALID_ARG, "device ordinal %d out of range", dev);
+  static std::atomic<void*> cache[64];
+  void* p = cache[dev].load(std::memory_order_acquire);
+  if (!p) {
+    CUDA_TRY(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+    cache[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return FP4_OK;
+}
+
 }  // namespace nvfp4
 
 using namespace nvfp4;
@@ -314,6 +336,37 @@ fp4_status fp4_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx, cons
   const size_t need = fp4_linear_fwd_workspace(M, N, K, r);
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
     return fail(FP4_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
+  Carver c(ws);
+  fp4_tensor xq;
+  void* P = nullptr;
+  fwd_ws(M, N, K, r, &c, &xq, &P);
+  if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, nullptr, &xq, xqT_saved, s))) return st;
+  if (r > 0 && (st = branch_impl(X, M, K, ldx, L1, r, P, s))) return st;
+  return gemm_impl(&xq, Wq, P, L2, r, beta, Y, FP4_OUT_BF16, ldy, s);
+}
+
+fp4_status fp4_linear_fwd_noalloc(const void* X, int64_t M, int64_t K, int64_t ldx, const fp4_tensor* Wq,
+                                  const void* L1, const void* L2, int r, float beta, void* Y, int64_t ldy,
+                                  fp4_tensor* xqT_saved, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  fp4_status st;
+  if ((st = check_bf16_input(X, M, K, ldx, "X"))) return st;
+  if ((st = check_tensor(Wq, "Wq")) || (st = check_tensor(xqT_saved, "xqT_saved"))) return st;
+  if (Wq->cols != K) return fail(FP4_ERR_INVALID_ARG, "Wq has %lld columns, X has K = %lld", (long long)Wq->cols, (long long)K);
+  const int64_t N = Wq->rows;
+  if (xqT_saved->rows != K || xqT_saved->cols != M)
+    return fail(FP4_ERR_INVALID_ARG, "xqT_saved must be K x M (%lld x %lld)", (long long)K, (long long)M);
+  if (M % 128 || N % 128 || K % 64)
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "linear needs M %% 128, N %% 128 == 0 and K %% 64 == 0");
+  if (r > 0 && (!L1 || !L2)) return fail(FP4_ERR_INVALID_ARG, "r > 0 needs L1 and L2");
+  const size_t need = fp4_linear_fwd_workspace(M, N, K, r);
+  if (need > kNoAllocScratchBytes)
+    return fail(FP4_ERR_WORKSPACE,
+                "fp4_linear_fwd_noalloc: M = %lld, K = %lld, r = %d needs %zu bytes of scratch but the static "
+                "scratch holds %zu; use fp4_linear_fwd with a caller workspace",
+                (long long)M, (long long)K, r, need, kNoAllocScratchBytes);
+  void* ws = nullptr;
+  if ((st = noalloc_scratch(&ws))) return st;
   Carver c(ws);
   fp4_tensor xq;
   void* P = nullptr;
