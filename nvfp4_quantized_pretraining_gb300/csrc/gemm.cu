@@ -429,7 +429,7 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
 // ---------------------------------------------------------------------------
 namespace g2 {
 constexpr int BK = 256;
-constexpr int STAGES = 4;
+constexpr int STAGES = 5;
 constexpr int A_BYTES = 128 * BK / 2;            // 16 KB: this CTA's 128 A rows
 constexpr int B_BYTES = 128 * BK / 2;            // 16 KB: this CTA's 128 B rows
 constexpr int SF_ATOM = 512;
@@ -439,24 +439,27 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 38 KB
 constexpr int BR_K = 64;
 constexpr int P_BYTES = 128 * BR_K * 2;          // 16 KB (A slot)
 constexpr int Q_BYTES = 128 * BR_K * 2;          // 16 KB (B slot)
-constexpr int OUT_PITCH = 256 * 2 + 16;          // BF16 staging row (padded against bank conflicts)
-constexpr int OUT_BYTES = 128 * OUT_PITCH;       // 66 KB: this CTA's 128 x 256 output tile
+constexpr int EPI_WARPS = 8;                     // two per TMEM lane quadrant, 128 columns each
+constexpr int CHUNK_BYTES = 32 * 64;             // 32 rows x 32 BF16 columns, 64-byte swizzled rows
+constexpr int OUT_BYTES = EPI_WARPS * 2 * CHUNK_BYTES;  // 32 KB: two chunks in flight per epilogue warp
 constexpr uint32_t TM_ACC = 0;                   // 256 columns
 constexpr uint32_t TM_SF = 256;                  // per stage: SFA 16 + SFB 32 columns
 constexpr uint32_t TM_SF_STAGE = 48;
 constexpr uint32_t TM_COLS = 512;
 static_assert(TM_SF + STAGES * TM_SF_STAGE <= TM_COLS, "TMEM budget");
 // warps: 0 A/B producer, 1 MMA (leader) + TMEM allocator, 2 scale/P producer,
-// 3..10 scale stagers (two per TMEM lane quadrant, two K steps each), 11..14 epilogue
-constexpr int NUM_THREADS = 480;
+// 3..10 scale stagers (two per TMEM lane quadrant, two K steps each), 11..18 epilogue
+constexpr int FIRST_EPI_WARP = 11;
+constexpr int NUM_THREADS = (FIRST_EPI_WARP + EPI_WARPS) * 32;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 1024 + 256;
 static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 }  // namespace g2
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                           const __grid_constant__ CUtensorMap tmap_p, const __grid_constant__ CUtensorMap tmap_q,
-                          const GemmParams p) {
+                          const __grid_constant__ CUtensorMap tmap_c, const GemmParams p) {
   using namespace g2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -482,7 +485,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
       mbar_init(&sf_ready[s], 16);  // 8 stager warps in each CTA of the pair
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 8);  // 4 epilogue warps in each CTA
+    mbar_init(acc_empty, 2 * EPI_WARPS);  // every epilogue warp of both CTAs
     mbar_init(done_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -494,6 +497,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
       prefetch_tmap(&tmap_p);
       prefetch_tmap(&tmap_q);
     }
+    if (!p.c_f32) prefetch_tmap(&tmap_c);
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, TM_COLS);
   tc_fence_before();
@@ -696,12 +700,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 11..14, both CTAs): C = alpha * acc ----------------
-    const uint32_t quad = warp & 3;
+    // ---------------- epilogue (warps 11..18, both CTAs): C = alpha * acc ----------------
+    // warp w reads TMEM lane quadrant w % 4 (rows 32q..32q+31 of this CTA's 128) and
+    // columns [128h, 128h + 128), h = (w - 11) / 4, in four 32-column chunks
+    const uint32_t quad = warp & 3, h = (uint32_t)(warp - FIRST_EPI_WARP) >> 2;
     const uint32_t lane_off = (quad * 32) << 16;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
-    uint8_t* stg = sOut + quad * 32 * OUT_PITCH;  // this warp's 32 staged rows
-    uint32_t t = 0;
+    uint8_t* stg = sOut + (warp - FIRST_EPI_WARP) * 2 * CHUNK_BYTES;  // this warp's two staging chunks
+    uint32_t t = 0, nst = 0;
     for (uint32_t mt = cluster_id; mt < num_tiles; mt += num_clusters, ++t) {
       const uint32_t mb2 = mt % tiles_m, nb2 = mt / tiles_m;
       if (*abort_flag || !mbar_wait_warp(acc_full, t & 1)) {
@@ -709,46 +715,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const size_t row0 = (size_t)mb2 * 256 + rank * 128 + quad * 32;
-      const size_t col0 = (size_t)nb2 * 256;
+      const uint32_t row0 = mb2 * 256 + rank * 128 + quad * 32;
+      const uint32_t col0 = nb2 * 256 + h * 128;
       if (!p.c_f32) {
-        // TMEM -> registers -> BF16 -> padded shared staging; release TMEM; coalesced row stores
-#pragma unroll 1
-        for (int j = 0; j < 8; ++j) {
-          uint32_t acc[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + j * 32, acc);
-          tmem_ld_wait(acc);
+        // TMEM -> registers -> BF16 -> swizzled shared chunk -> TMA store; the next chunk's TMEM
+        // load is issued before this one is converted
+        uint32_t acc[2][32];
+        tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + h * 128, acc[0]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          tmem_ld_wait(acc[j & 1]);
+          if (j < 3) tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + h * 128 + (j + 1) * 32, acc[(j + 1) & 1]);
+          if (j == 3) {
+            // every TMEM read of the accumulator is complete: release it to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (leader) mbar_arrive(acc_empty);
+              else mbar_arrive_cluster_relaxed(acc_empty0);
+            }
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(acc[2 * e])),
-                                                      __fmul_rn(alpha, __uint_as_float(acc[2 * e + 1])));
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(acc[j & 1][2 * e])),
+                                                      __fmul_rn(alpha, __uint_as_float(acc[j & 1][2 * e + 1])));
             pk[e] = *reinterpret_cast<uint32_t*>(&b2);
           }
-          uint4* dst = reinterpret_cast<uint4*>(stg + lane * OUT_PITCH + j * 64);
+          uint8_t* chunk = stg + (nst & 1) * CHUNK_BYTES;
+          // the store that last read this chunk (two stores ago) must have finished reading it
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          // row = lane, 64 bytes; 16-byte unit u lands at u ^ ((row >> 1) & 3) (64-byte swizzle)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(chunk + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmap_c, chunk, (int32_t)(col0 + j * 32), (int32_t)row0);
+            bulk_commit_group();
+          }
+          ++nst;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          // the TMEM loads are complete (tcgen05.wait::ld), so only the phase flip has to travel
-          if (leader) mbar_arrive(acc_empty);
-          else mbar_arrive_cluster_relaxed(acc_empty0);
-        }
-        // 32 rows of 512 bytes: lane i writes bytes [16i, 16i+16) of each row
-#pragma unroll 4
-        for (int r = 0; r < 32; ++r) {
-          const uint4 v = *reinterpret_cast<const uint4*>(stg + r * OUT_PITCH + lane * 16);
-          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + (row0 + r) * p.ldc + col0 + lane * 8) = v;
-        }
-        __syncwarp();
       } else {
-        const size_t row = row0 + lane;
+        const size_t row = (size_t)row0 + lane;
 #pragma unroll 1
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 4; ++j) {
           uint32_t acc[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + j * 32, acc);
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + h * 128 + j * 32, acc);
           tmem_ld_wait(acc);
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.C) + row * p.ldc + col0 + j * 32);
 #pragma unroll
@@ -766,6 +782,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
         }
       }
     }
+    if (lane == 0) bulk_wait_all();  // every TMA store of this warp has completed
+    __syncwarp();
   }
 
   __syncthreads();
@@ -959,7 +977,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 2-D row-major tensor map: inner dimension `inner` elements, `outer` rows,
 // row pitch `pitch_bytes`, box inner x outer, 128-byte swizzle.
 static bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
-                      uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
+                      uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -967,7 +986,7 @@ static bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, 
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1022,7 +1041,8 @@ static cudaError_t launch_gemm_cluster(const CUtensorMap& ta, const CUtensorMap&
 }
 
 static cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tp,
-                                    const CUtensorMap& tq, const GemmParams& p, int num_sms, cudaStream_t s) {
+                                    const CUtensorMap& tq, const CUtensorMap& tc, const GemmParams& p, int num_sms,
+                                    cudaStream_t s) {
   using namespace g2;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -1042,7 +1062,7 @@ static cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb
   if (attr_err != cudaSuccess) return attr_err;
   const uint32_t tiles = (p.M / 256) * (p.N / 256);
   const uint32_t clusters = tiles < (uint32_t)max_clusters ? tiles : (uint32_t)max_clusters;
-  gemm_nvf4_pair_kernel<<<clusters * 2, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, tp, tq, p);
+  gemm_nvf4_pair_kernel<<<clusters * 2, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, tp, tq, tc, p);
   count_launch();
   return cudaGetLastError();
 }
@@ -1079,7 +1099,12 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
     p.C = g.C;
     p.c_f32 = g.c_f32;
     p.ldc = g.ldc;
-    return launch_gemm_pair(ta, tb, tp, tq, p, num_sms, s);
+    // BF16 output leaves through TMA stores of 32 x 32 tiles (64-byte rows, 64-byte swizzle)
+    CUtensorMap tc = ta;
+    if (!g.c_f32 && !make_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.C, g.N, g.M, (uint64_t)g.ldc * 2, 32, 32,
+                               CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+    return launch_gemm_pair(ta, tb, tp, tq, tc, p, num_sms, s);
   }
   const int cm = (g.M % (2 * BM) == 0) ? 2 : 1;
   const int cn = (g.N % (2 * BN) == 0) ? 2 : 1;

@@ -100,6 +100,22 @@ def test_gemm_strided_output(F, oracle_mod):
     assert np.all(got[:, :64] == 7.0) and np.all(got[:, 320:] == 7.0)
 
 
+def test_gemm_strided_bf16_output_pair_path(F, oracle_mod):
+    # M, N multiples of 256 take the 2-SM kernel, whose BF16 tiles leave by TMA stores
+    A = S.normal((512, 512), 1.0, 8)
+    B = S.normal((512, 512), 1.0, 9)
+    ga, oa = quantize_both(F, oracle_mod, A)
+    gb, ob = quantize_both(F, oracle_mod, B)
+    big = torch.full((512, 640), 7.0, dtype=torch.bfloat16, device=DEV)
+    F.fp4_gemm_blockscaled(ga, gb, out=big[:, 64:576])
+    torch.cuda.synchronize()
+    ref = oracle_mod.gemm(oa.dequantize(), ob.dequantize())
+    ref = oracle_mod.bf16_to_f32(oracle_mod.bf16_rn(ref)).astype(np.float64)
+    got = big.float().cpu().numpy().astype(np.float64)
+    assert rel(got[:, 64:576], ref) < TOL
+    assert np.all(got[:, :64] == 7.0) and np.all(got[:, 576:] == 7.0)
+
+
 @pytest.mark.parametrize("M,N,K,r", [
     (4096, 4096, 4096, 0), (4096, 4096, 4096, 64), (16384, 3072, 8192, 64), (3072, 8192, 16384, 0),
 ])
