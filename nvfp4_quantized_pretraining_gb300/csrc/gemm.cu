@@ -464,11 +464,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sOut = smem + STAGES * STAGE_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + OUT_BYTES);  // leader: A/B (+Q) of both CTAs
+  // leader's full[s]: A/B (+Q) of both CTAs landed AND the scales are in TMEM (P~ in smem)
+  // in both CTAs -- one wait per stage for the MMA warp
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + OUT_BYTES);
   uint64_t* sf_full = full + STAGES;        // each CTA: its scales (or P) landed
   uint64_t* empty = sf_full + STAGES;       // each CTA: the stage was consumed by the MMAs (both producers wait)
-  uint64_t* sf_ready = empty + STAGES;      // leader: scales in TMEM (and P~ in smem) in both CTAs
-  uint64_t* acc_full = sf_ready + STAGES;   // each CTA: accumulator complete
+  uint64_t* acc_full = empty + STAGES;      // each CTA: accumulator complete
   uint64_t* acc_empty = acc_full + 1;       // leader: both CTAs drained the accumulator
   uint64_t* done_bar = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
@@ -479,10 +480,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
   const bool leader = rank == 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 1 + 16);  // producer (expect_tx) + 8 stager warps in each CTA
       mbar_init(&sf_full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&sf_ready[s], 16);  // 8 stager warps in each CTA of the pair
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * EPI_WARPS);  // every epilogue warp of both CTAs
@@ -580,7 +580,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem + TM_ACC;
         for (uint32_t it = 0; it < num_k; ++it) {
-          if (!mbar_wait(&full[stage], phase) || !mbar_wait_cluster(&sf_ready[stage], phase)) {
+          if (!mbar_wait_cluster(&full[stage], phase)) {
             ok = false;
             break;
           }
@@ -603,7 +603,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
         }
         if (!ok) break;
         if (has_branch) {
-          if (!mbar_wait(&full[stage], phase) || !mbar_wait_cluster(&sf_ready[stage], phase)) { ok = false; break; }
+          if (!mbar_wait_cluster(&full[stage], phase)) { ok = false; break; }
           tc_fence_after();
           const uint64_t ad = adesc0 + stage * kStageD, bd = bdesc0 + stage * kStageD;
           const uint32_t nkb = (uint32_t)(p.r + 15) / 16;
@@ -622,7 +622,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
     // warp w serves TMEM lane quadrant w % 4 and the two K steps {2h, 2h+1}, h = (w - 3) / 4
     const uint32_t quad = warp & 3, h = (uint32_t)(warp - 3) >> 2;
     const uint32_t lane_off = (quad * 32) << 16;
-    const uint32_t sf_ready0 = mapa_shared(smem_u32(&sf_ready[0]), 0);
+    const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);  // leader's full[] in the cluster window
     const float g = __fdiv_rn(p.beta, alpha);
     uint32_t stage = 0, phase = 0;
     for (uint32_t mt = cluster_id; mt < num_tiles; mt += num_clusters) {
@@ -688,9 +688,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
         }
         __syncwarp();
         if (lane == 0) {
-          if (leader) mbar_arrive(&sf_ready[stage]);
-          else if (it < num_k) mbar_arrive_cluster_relaxed(sf_ready0 + stage * 8);  // TMEM stores already complete
-          else mbar_arrive_cluster(sf_ready0 + stage * 8);  // P~ was written through the generic proxy
+          if (leader) mbar_arrive(&full[stage]);
+          else if (it < num_k) mbar_arrive_cluster_relaxed(full0 + stage * 8);  // TMEM stores already complete
+          else mbar_arrive_cluster(full0 + stage * 8);  // P~ was written through the generic proxy
         }
         if (++stage == STAGES) stage = 0, phase ^= 1;
       }
