@@ -24,6 +24,15 @@ constexpr long long kWaitTimeoutCycles = 4000000000ll;
 
 __device__ __forceinline__ void record_timeout() { atomicOr(&g_status, 1u << FP4_ERR_TIMEOUT); }
 
+// After a wait has expired, a kernel gives up on its pipeline but may still have
+// TMA copies in flight into its (or, in a cluster, its peer's) shared memory.
+// A bounded pause (about 2 ms at 2 GHz) before the teardown lets them land
+// before the shared memory is released.
+__device__ __forceinline__ void drain_pause() {
+  const long long t0 = clock64();
+  while (clock64() - t0 < 4000000ll) __nanosleep(2000);
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

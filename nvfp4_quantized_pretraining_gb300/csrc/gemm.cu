@@ -400,6 +400,10 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
   }
 
   __syncthreads();
+  if (*abort_flag) {  // a wait expired: let copies still in flight land first
+    if (threadIdx.x == 0) drain_pause();
+    __syncthreads();
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -787,6 +791,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
   }
 
   __syncthreads();
+  if (*abort_flag) {  // a wait expired: let copies still in flight land first
+    if (threadIdx.x == 0) drain_pause();
+    __syncthreads();
+  }
   tc_fence_before();
   cluster_sync();
   if (warp == 1) {
@@ -932,6 +940,10 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
     }
   }
   __syncthreads();
+  if (*abort_flag) {  // a wait expired: let copies still in flight land first
+    if (threadIdx.x == 0) drain_pause();
+    __syncthreads();
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
