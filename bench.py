@@ -311,18 +311,23 @@ def breakdown(F, torch, projs, T, r, stream, dev, flush, args):
                     p["amax"] = torch.empty(1, dtype=torch.float32, device=dev)
                 rec("quantize_w_dual", lambda: F.fp4_quantize_dual(p["Wres"], out_row=p["Wq"], out_col=p["WqT"],
                                                                    stream=stream))
-                rec("amax", lambda: F.fp4_amax(p["X"], out=p["amax"], stream=stream))
+                # as in fp4_linear_fwd/bwd: with a branch, its factor kernel also yields the amax
+                if r:
+                    rec("branch_factor_amax", lambda: F.fp4_branch_factor(p["X"], p["L1"], out=p["P"],
+                                                                          amax=p["amax"], stream=stream))
+                else:
+                    rec("amax", lambda: F.fp4_amax(p["X"], out=p["amax"], stream=stream))
                 rec("quantize_x_dual", lambda: F.fp4_quantize_dual(p["X"], amax=p["amax"], out_row=xq,
                                                                    out_col=p["xqT"], stream=stream))
-                if r:
-                    rec("branch_factor", lambda: F.fp4_branch_factor(p["X"], p["L1"], out=p["P"], stream=stream))
                 rec("gemm", lambda: F.fp4_gemm_blockscaled(xq, p["Wq"], p["P"], p["L2"], out=p["Y"], stream=stream))
-                rec("amax", lambda: F.fp4_amax(p["dY"], out=p["amax"], stream=stream))
+                if r:
+                    rec("branch_factor_amax", lambda: F.fp4_branch_factor(p["dY"], p["L2T"], out=p["P2"],
+                                                                          amax=p["amax"], stream=stream))
+                else:
+                    rec("amax", lambda: F.fp4_amax(p["dY"], out=p["amax"], stream=stream))
                 rec("quantize_dy_dual_sr", lambda: F.fp4_quantize_dual(p["dY"], round_mode=F.SR, seed=rep,
                                                                        amax=p["amax"], out_row=dyq, out_col=dyqT,
                                                                        stream=stream))
-                if r:
-                    rec("branch_factor", lambda: F.fp4_branch_factor(p["dY"], p["L2T"], out=p["P2"], stream=stream))
                 rec("gemm", lambda: F.fp4_gemm_blockscaled(dyq, p["WqT"], p["P2"], p["L1T"], out=p["dX"],
                                                            stream=stream))
                 rec("gemm", lambda: F.fp4_gemm_blockscaled(dyqT, p["xqT"], out=p["dW"], stream=stream))

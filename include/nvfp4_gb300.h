@@ -126,10 +126,14 @@ fp4_status fp4_gemm_blockscaled(const fp4_tensor* A, const fp4_tensor* B,
 
 /* Low-rank branch factor: P[m][j] = bf16( sum_k X[m][k] L[j][k] ), FP32
  * accumulation.  X: M x K BF16 (pitch ldx), L: r x K BF16 (pitch K), P: M x r
- * BF16 (pitch r).  Requires M % 128 == 0, K % 64 == 0, r in {16,32,48,64}.
- * Forward: P = X L1^T; backward: P' = dY L2 (pass L = L2^T). */
+ * BF16 (pitch r).  Requires M % 128 == 0, K % 16 == 0, r in {16,32,48,64}.
+ * Forward: P = X L1^T; backward: P' = dY L2 (pass L = L2^T).
+ * amax_out (optional, device, 4-byte aligned; NULL to skip): also receives
+ * max |X| over the whole tensor, the same value fp4_amax returns, taken from
+ * this call's own read of X; the call zeroes it first.  The linear calls use
+ * it so that X (or dY) is read once for the factor and the tensor scale. */
 fp4_status fp4_branch_factor(const void* X, int64_t M, int64_t K, int64_t ldx,
-                             const void* L, int r, void* P, void* stream);
+                             const void* L, int r, void* P, float* amax_out, void* stream);
 
 /* Workspace bytes needed by fp4_linear_fwd / fp4_linear_bwd. */
 size_t fp4_linear_fwd_workspace(int64_t M, int64_t N, int64_t K, int r);

@@ -70,7 +70,7 @@ def lib() -> ctypes.CDLL:
         "fp4_quantize_transposed": (i32, [P, i64, i64, i64, i32, u64, u32, P, T, P]),
         "fp4_quantize_dual": (i32, [P, i64, i64, i64, i32, u64, u32, u32, P, T, T, P]),
         "fp4_gemm_blockscaled": (i32, [T, T, P, P, i32, f32, P, i32, i64, P]),
-        "fp4_branch_factor": (i32, [P, i64, i64, i64, P, i32, P, P]),
+        "fp4_branch_factor": (i32, [P, i64, i64, i64, P, i32, P, P, P]),
         "fp4_linear_fwd_workspace": (ctypes.c_size_t, [i64, i64, i64, i32]),
         "fp4_linear_bwd_workspace": (ctypes.c_size_t, [i64, i64, i64, i32]),
         "fp4_linear_fwd": (i32, [P, i64, i64, i64, T, P, P, i32, f32, P, i64, T, P, ctypes.c_size_t, P]),
@@ -194,11 +194,13 @@ def fp4_gemm_blockscaled(A: NVFP4Tensor, B: NVFP4Tensor, P=None, Q=None, beta=1.
     return out
 
 
-def fp4_branch_factor(X: torch.Tensor, L: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+def fp4_branch_factor(X: torch.Tensor, L: torch.Tensor, out=None, amax=None, stream=None) -> torch.Tensor:
+    """P = bf16(X L^T); with ``amax`` (a 1-element float32 device tensor) also max |X|."""
     M, K, ldx = _bf16_2d(X, "X")
     r = L.shape[0]
     out = torch.empty((M, r), dtype=torch.bfloat16, device=X.device) if out is None else out
-    _check(lib().fp4_branch_factor(X.data_ptr(), M, K, ldx, L.data_ptr(), r, out.data_ptr(), _stream(stream)))
+    _check(lib().fp4_branch_factor(X.data_ptr(), M, K, ldx, L.data_ptr(), r, out.data_ptr(), _ptr(amax),
+                                   _stream(stream)))
     return out
 
 

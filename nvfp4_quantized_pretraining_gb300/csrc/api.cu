@@ -178,14 +178,14 @@ static fp4_status gemm_impl(const fp4_tensor* A, const fp4_tensor* B, const void
 }
 
 static fp4_status branch_impl(const void* X, int64_t M, int64_t K, int64_t ldx, const void* L, int r, void* P,
-                              cudaStream_t s) {
+                              cudaStream_t s, float* amax_out = nullptr) {
   fp4_status st = check_bf16_input(X, M, K, ldx, "X");
   if (st) return st;
   if (!L || !P) return fail(FP4_ERR_INVALID_ARG, "L and P must be non-NULL");
   if (!aligned16(L) || !aligned16(P)) return fail(FP4_ERR_MISALIGNED, "L and P must be 16-byte aligned");
   if (M % 128 || K % 16) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "branch factor needs M %% 128 == 0, K %% 16 == 0");
   if (r != 16 && r != 32 && r != 48 && r != 64) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rank r=%d not in {16,32,48,64}", r);
-  CUDA_TRY(launch_branch_factor(X, M, K, ldx, L, r, P, sm_count(), s));
+  CUDA_TRY(launch_branch_factor(X, M, K, ldx, L, r, P, amax_out, sm_count(), s));
   return FP4_OK;
 }
 
@@ -307,8 +307,10 @@ fp4_status fp4_gemm_blockscaled(const fp4_tensor* A, const fp4_tensor* B, const 
 }
 
 fp4_status fp4_branch_factor(const void* X, int64_t M, int64_t K, int64_t ldx, const void* L, int r, void* P,
-                             void* stream) {
-  return branch_impl(X, M, K, ldx, L, r, P, static_cast<cudaStream_t>(stream));
+                             float* amax_out, void* stream) {
+  if (amax_out && (reinterpret_cast<uintptr_t>(amax_out) & 3u))
+    return fail(FP4_ERR_MISALIGNED, "amax_out must be 4-byte aligned");
+  return branch_impl(X, M, K, ldx, L, r, P, static_cast<cudaStream_t>(stream), amax_out);
 }
 
 size_t fp4_linear_fwd_workspace(int64_t M, int64_t N, int64_t K, int r) {
@@ -340,8 +342,13 @@ fp4_status fp4_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx, cons
   fp4_tensor xq;
   void* P = nullptr;
   fwd_ws(M, N, K, r, &c, &xq, &P);
-  if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, nullptr, &xq, xqT_saved, s))) return st;
-  if (r > 0 && (st = branch_impl(X, M, K, ldx, L1, r, P, s))) return st;
+  if (r > 0) {
+    // the branch factor's read of X also yields max |X| for the quantizer (no separate amax pass)
+    if ((st = branch_impl(X, M, K, ldx, L1, r, P, s, &xq.scale[1]))) return st;
+    if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, &xq.scale[1], &xq, xqT_saved, s))) return st;
+  } else if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, nullptr, &xq, xqT_saved, s))) {
+    return st;
+  }
   return gemm_impl(&xq, Wq, P, L2, r, beta, Y, FP4_OUT_BF16, ldy, s);
 }
 
@@ -371,8 +378,13 @@ fp4_status fp4_linear_fwd_noalloc(const void* X, int64_t M, int64_t K, int64_t l
   fp4_tensor xq;
   void* P = nullptr;
   fwd_ws(M, N, K, r, &c, &xq, &P);
-  if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, nullptr, &xq, xqT_saved, s))) return st;
-  if (r > 0 && (st = branch_impl(X, M, K, ldx, L1, r, P, s))) return st;
+  if (r > 0) {
+    // the branch factor's read of X also yields max |X| for the quantizer (no separate amax pass)
+    if ((st = branch_impl(X, M, K, ldx, L1, r, P, s, &xq.scale[1]))) return st;
+    if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, &xq.scale[1], &xq, xqT_saved, s))) return st;
+  } else if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, nullptr, &xq, xqT_saved, s))) {
+    return st;
+  }
   return gemm_impl(&xq, Wq, P, L2, r, beta, Y, FP4_OUT_BF16, ldy, s);
 }
 
@@ -399,11 +411,14 @@ fp4_status fp4_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t lddy, co
   fp4_tensor dyq, dyqT;
   void *P2 = nullptr, *L2T = nullptr, *L1T = nullptr;
   bwd_ws(M, N, K, r, &c, &dyq, &dyqT, &P2, &L2T, &L1T);
-  if ((st = quantize_impl(dY, M, N, lddy, FP4_ROUND_SR, seed, 0, 1, nullptr, &dyq, &dyqT, s))) return st;
   if (r > 0) {
+    // the branch factor's read of dY also yields max |dY| for the quantizer (no separate amax pass)
     CUDA_TRY(launch_transpose_bf16(L2, N, r, L2T, s));
-    if ((st = branch_impl(dY, M, N, lddy, L2T, r, P2, s))) return st;
+    if ((st = branch_impl(dY, M, N, lddy, L2T, r, P2, s, &dyq.scale[1]))) return st;
     CUDA_TRY(launch_transpose_bf16(L1, r, K, L1T, s));
+    if ((st = quantize_impl(dY, M, N, lddy, FP4_ROUND_SR, seed, 0, 1, &dyq.scale[1], &dyq, &dyqT, s))) return st;
+  } else if ((st = quantize_impl(dY, M, N, lddy, FP4_ROUND_SR, seed, 0, 1, nullptr, &dyq, &dyqT, s))) {
+    return st;
   }
   if ((st = gemm_impl(&dyq, WqT, P2, L1T, r, beta, dX, FP4_OUT_BF16, lddx, s))) return st;
   return gemm_impl(&dyqT, xqT_saved, nullptr, nullptr, 0, 0.0f, dW, dw_dtype, lddw, s);

@@ -838,7 +838,7 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 
 __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
     branch_factor_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_l,
-                         uint32_t K, int r, __nv_bfloat16* __restrict__ P) {
+                         uint32_t K, int r, __nv_bfloat16* __restrict__ P, unsigned int* __restrict__ amax_out) {
   using namespace bf;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -852,7 +852,7 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], amax_out ? 1 + 4 : 1);  // the MMA commit (+ the 4 amax warps)
     }
     mbar_init(acc_full, 1);
     mbar_init(done_bar, 1);
@@ -917,6 +917,32 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
     }
   } else {
     const uint32_t quad = warp & 3;
+    if (amax_out) {
+      // warps 2..5 fold every landed X tile into max |x| while the MMAs consume it: the tensor
+      // scale of X comes out of this read of X (integer max of the |bf16| patterns, as the
+      // standalone amax kernel takes it; zero padding past K does not change it)
+      const int t = (warp - 2) * 32 + lane;
+      uint32_t m = 0, stage = 0, phase = 0;
+      for (uint32_t it = 0; it < num_k; ++it) {
+        if (*abort_flag || !mbar_wait_warp(&full[stage], phase)) {
+          *abort_flag = 1;
+          break;
+        }
+        const uint4* tile = reinterpret_cast<const uint4*>(smem + stage * STAGE_BYTES);
+#pragma unroll
+        for (int i = 0; i < A_BYTES / 16 / 128; ++i) {
+          const uint4 v = tile[t + 128 * i];
+          m = __vmaxu2(m, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                   __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+        if (++stage == STAGES) stage = 0, phase ^= 1;
+      }
+      m = max(m & 0xFFFFu, m >> 16);
+      m = __reduce_max_sync(0xFFFFFFFFu, m);
+      if (lane == 0 && m != 0) atomicMax(amax_out, m << 16);
+    }
     if (!*abort_flag && mbar_wait_warp(acc_full, 0)) {
       tc_fence_after();
       const uint32_t row = m0 + quad * 32 + lane;
@@ -1155,7 +1181,7 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
 }
 
 cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ldx, const void* L, int r, void* P,
-                                 int num_sms, cudaStream_t s) {
+                                 float* amax_out, int num_sms, cudaStream_t s) {
   using namespace bf;
   (void)num_sms;
   static std::once_flag once;
@@ -1168,9 +1194,14 @@ cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ld
   if (!make_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, (uint64_t)ldx * 2, BK, BM) ||
       !make_tmap(&tl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L, K, r, (uint64_t)K * 2, BK, (uint32_t)r))
     return cudaErrorInvalidValue;
+  if (amax_out) {
+    const cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), s);
+    if (e != cudaSuccess) return e;
+  }
   const int grid = (int)(M / BM);
   branch_factor_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tx, tl, (uint32_t)K, r,
-                                                             static_cast<__nv_bfloat16*>(P));
+                                                             static_cast<__nv_bfloat16*>(P),
+                                                             reinterpret_cast<unsigned int*>(amax_out));
   count_launch();
   return cudaGetLastError();
 }

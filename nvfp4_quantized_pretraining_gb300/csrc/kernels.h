@@ -47,8 +47,9 @@ struct GemmArgs {
 cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s);
 
 // P = bf16(X L^T): X M x K (pitch ldx), L r x K, P M x r.
+// amax_out (optional, device): also reduces max |X| into it (zeroed by the launcher).
 cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ldx, const void* L, int r, void* P,
-                                 int num_sms, cudaStream_t s);
+                                 float* amax_out, int num_sms, cudaStream_t s);
 
 // Dense NVFP4 MMA rate probe: every SM issues 4 * iters M=128 x N=n x K=64 MMAs.
 cudaError_t launch_mma_peak(int n, int iters, int num_sms, cudaStream_t s);

@@ -130,9 +130,14 @@ def test_gemm_full_size_sampled_rows(F, oracle_mod, M, N, K, r):
 def test_branch_factor(F, oracle_mod, M, K, r):
     X = S.student_t((M, K), 3.0, M + K)
     L = S.normal((r, K), 0.05, r)
-    P = F.fp4_branch_factor(dev(X), dev(L))
+    amax = torch.full((1,), -1.0, dtype=torch.float32, device=DEV)  # the call must zero it first
+    P = F.fp4_branch_factor(dev(X), dev(L), amax=amax)
     torch.cuda.synchronize()
     F.fp4_check_status()
+    assert np.float32(amax.item()) == np.float32(oracle_mod.amax(X))
+    P0 = F.fp4_branch_factor(dev(X), dev(L))  # without the amax output: the same factor
+    torch.cuda.synchronize()
+    assert torch.equal(P0.view(torch.int16), P.view(torch.int16))
     want = oracle_mod.branch_factor(X, L)
     got_bits = S.torch_to_bits(P)
     g = oracle_mod.bf16_to_f32(got_bits).astype(np.float64)
