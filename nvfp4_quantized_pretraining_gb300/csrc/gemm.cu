@@ -473,7 +473,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(sOut + OUT_BYTES);
   uint64_t* sf_full = full + STAGES;        // each CTA: its scales (or P) landed
   uint64_t* empty = sf_full + STAGES;       // each CTA: the stage was consumed by the MMAs (both producers wait)
-  uint64_t* acc_full = empty + STAGES;      // each CTA: accumulator complete
+  uint64_t* peer_ready = empty + STAGES;    // peer CTA: its 8 stager warps are done with stage s
+  uint64_t* acc_full = peer_ready + STAGES; // each CTA: accumulator complete
   uint64_t* acc_empty = acc_full + 1;       // leader: both CTAs drained the accumulator
   uint64_t* done_bar = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
@@ -484,9 +485,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
   const bool leader = rank == 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1 + 16);  // producer (expect_tx) + 8 stager warps in each CTA
+      // leader: producer (expect_tx) + its 8 stager warps + one forwarded arrival for the peer's 8
+      mbar_init(&full[s], 1 + 8 + 1);
       mbar_init(&sf_full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&peer_ready[s], 8);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * EPI_WARPS);  // every epilogue warp of both CTAs
@@ -620,13 +623,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
       if (!ok) *abort_flag = 1;
       tc_commit_pair_mc(done_bar, 1);  // (a kernel may not mix cta_group::1 and ::2 forms)
       mbar_wait(done_bar, 0);
+    } else if (lane == 0) {
+      // ---------------- peer: forward its stagers' completion as one remote arrival per stage ----------------
+      const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (uint32_t mt = cluster_id; mt < num_tiles && ok; mt += num_clusters) {
+        for (uint32_t it = 0; it < n_iter; ++it) {
+          if (*abort_flag || !mbar_wait(&peer_ready[stage], phase)) {
+            ok = false;
+            break;
+          }
+          if (it < num_k) mbar_arrive_cluster_relaxed(full0 + stage * 8);  // TMEM stores already complete
+          else mbar_arrive_cluster(full0 + stage * 8);  // P~ was written through the generic proxy
+          if (++stage == STAGES) stage = 0, phase ^= 1;
+        }
+      }
+      if (!ok) *abort_flag = 1;
     }
   } else if (warp < 11) {
     // ---------------- scale stagers (warps 3..10, both CTAs) ----------------
     // warp w serves TMEM lane quadrant w % 4 and the two K steps {2h, 2h+1}, h = (w - 3) / 4
     const uint32_t quad = warp & 3, h = (uint32_t)(warp - 3) >> 2;
     const uint32_t lane_off = (quad * 32) << 16;
-    const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);  // leader's full[] in the cluster window
     const float g = __fdiv_rn(p.beta, alpha);
     uint32_t stage = 0, phase = 0;
     for (uint32_t mt = cluster_id; mt < num_tiles; mt += num_clusters) {
@@ -691,11 +710,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
           fence_proxy_async_smem();
         }
         __syncwarp();
-        if (lane == 0) {
-          if (leader) mbar_arrive(&full[stage]);
-          else if (it < num_k) mbar_arrive_cluster_relaxed(full0 + stage * 8);  // TMEM stores already complete
-          else mbar_arrive_cluster(full0 + stage * 8);  // P~ was written through the generic proxy
-        }
+        if (lane == 0) mbar_arrive(leader ? &full[stage] : &peer_ready[stage]);
         if (++stage == STAGES) stage = 0, phase ^= 1;
       }
       if (!ok) {
