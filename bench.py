@@ -82,13 +82,14 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (monotonic time, line)
         self.thread = None
+        self.window = None  # (t0, t1) of the timed region; samples outside it are dropped
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -98,7 +99,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def wait_ready(self, timeout: float = 10.0):
+        """Block until nvidia-smi has printed its first sample (it takes a while to start)."""
+        t_end = time.monotonic() + timeout
+        while self.proc and not self.lines and time.monotonic() < t_end:
+            time.sleep(0.01)
 
     def __exit__(self, *a):
         if self.proc:
@@ -112,7 +119,9 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ts, ln in self.lines:
+            if self.window and not (self.window[0] - 0.025 <= ts <= self.window[1] + 0.025):
+                continue
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 7:
                 continue
@@ -199,6 +208,7 @@ def run_ours(args):
                 dist.barrier()
             torch.cuda.synchronize(dev)
             times = []
+            t_start = time.monotonic()
             for i in range(steps):
                 flush.zero_()
                 e0 = torch.cuda.Event(enable_timing=True)
@@ -209,9 +219,10 @@ def run_ours(args):
                 e1.synchronize()
                 times.append(e0.elapsed_time(e1))
             torch.cuda.synchronize(dev)
+            t_end = time.monotonic()
             if world > 1:
                 dist.barrier()
-        return times
+        return times, (t_start, t_end)
 
     # ---- main timed region: device-resident inputs
     launches0 = F.fp4_launch_count()
@@ -220,7 +231,8 @@ def run_ours(args):
     except Exception:
         gpu_id = str(local)
     with ClockSampler(gpu_id) as clk:
-        times = timed(step, args.steps, args.warmup)
+        clk.wait_ready()
+        times, clk.window = timed(step, args.steps, args.warmup)
     launches = (F.fp4_launch_count() - launches0) * args.steps // (args.steps + args.warmup)
     F.fp4_check_status(stream)
     total_ms = sum(times)
