@@ -230,51 +230,69 @@ __global__ void __launch_bounds__(kDualThreads) quantize_dual_kernel(const DualQ
   for (int i = 0; i < kLoads; ++i) {
     const int q = tid + i * kDualThreads;
     const uint32_t row = r0 + (q >> 4), c8 = (c0 >> 3) + (q & 15);
-    const bool valid = row < a.rows && c8 < a.cpr;
-    if (COL) {
-      *reinterpret_cast<uint4*>(&tile[q >> 4][(q & 15) * 8]) = w[i];
-      if (SR) {
-        // element e of the chunk takes word e/2, low half for even e: in element order
-        // the eight 16-bit draws are exactly the four words as stored
-        const uint4 rc = sr_random(keys, a.stream_c, (uint64_t)row * a.cpr + c8);
-        *reinterpret_cast<uint4*>(&rtile[q >> 4][(q & 15) * 8]) = rc;
-      }
+    *reinterpret_cast<uint4*>(&tile[q >> 4][(q & 15) * 8]) = w[i];
+    if (COL && SR) {
+      // element e of the chunk takes word e/2, low half for even e: in element order
+      // the eight 16-bit draws are exactly the four words as stored
+      *reinterpret_cast<uint4*>(&rtile[q >> 4][(q & 15) * 8]) =
+          sr_random(keys, a.stream_c, (uint64_t)row * a.cpr + c8);
     }
-    if (ROW) {
-      float v[8];
-      v[0] = bf16_lo(w[i].x); v[1] = bf16_hi(w[i].x); v[2] = bf16_lo(w[i].y); v[3] = bf16_hi(w[i].y);
-      v[4] = bf16_lo(w[i].z); v[5] = bf16_hi(w[i].z); v[6] = bf16_lo(w[i].w); v[7] = bf16_hi(w[i].w);
-      uint32_t m = __vmaxu2(__vmaxu2(w[i].x & 0x7FFF7FFFu, w[i].y & 0x7FFF7FFFu),
-                            __vmaxu2(w[i].z & 0x7FFF7FFFu, w[i].w & 0x7FFF7FFFu));
+  }
+  __syncthreads();
+
+  if (ROW) {
+    // row phase: one thread per 16-element block (block b = tid + 256 i: tile row b / 8, block b % 8),
+    // so each block scale is computed once.  The two 16-byte halves are read in a lane-dependent
+    // order (lanes 4..7 of every 8 first take their second half), which keeps the 128-bit shared
+    // reads of each 8-lane phase on distinct banks.
+    const int first = (lane >> 2) & 1;
+#pragma unroll 2
+    for (int i = 0; i < kTileR * (kTileC / 16) / kDualThreads; ++i) {
+      const int b = tid + i * kDualThreads;
+      const int tr = b >> 3, blk = b & 7;
+      const uint32_t row = r0 + tr, c16 = (c0 >> 4) + blk;
+      const uint4 h0 = *reinterpret_cast<const uint4*>(&tile[tr][blk * 16 + first * 8]);
+      const uint4 h1 = *reinterpret_cast<const uint4*>(&tile[tr][blk * 16 + (first ^ 1) * 8]);
+      const uint4 wl = first ? h1 : h0, wh = first ? h0 : h1;  // elements 0..7, 8..15
+      const uint32_t wd[8] = {wl.x, wl.y, wl.z, wl.w, wh.x, wh.y, wh.z, wh.w};
+      uint32_t m = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m = __vmaxu2(m, wd[e] & 0x7FFF7FFFu);
       m = max(m & 0xFFFFu, m >> 16);
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
       const BlockScale bs = block_scale(__uint_as_float(m << 16), S_t);
-      float y[8];
+      float y[2][8];  // elements 0..7 and 8..15
 #pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(v[e], bs.inv);
-      if (SR) {
-        const uint4 rr = sr_random(keys, a.stream_r, (uint64_t)row * a.cpr + c8);
-        const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = sr_round(y[e], (e & 1) ? (rw[e >> 1] >> 16) : (rw[e >> 1] & 0xFFFFu));
+      for (int e = 0; e < 8; ++e) {
+        y[e >> 2][2 * (e & 3)] = __fmul_rn(bf16_lo(wd[e]), bs.inv);
+        y[e >> 2][2 * (e & 3) + 1] = __fmul_rn(bf16_hi(wd[e]), bs.inv);
       }
-      const uint32_t codes = e2m1x8(y);
-      if (valid) *reinterpret_cast<uint32_t*>(a.codes_r + (size_t)row * (a.cols >> 1) + c8 * 4) = codes;
+      if (SR) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint4 rr = sr_random(keys, a.stream_r, (uint64_t)row * a.cpr + 2 * c16 + hh);
+          const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            y[hh][e] = sr_round(y[hh][e], (e & 1) ? (rw[e >> 1] >> 16) : (rw[e >> 1] & 0xFFFFu));
+        }
+      }
+      const uint32_t lo = e2m1x8(y[0]), hi = e2m1x8(y[1]);
+      const bool valid = row < a.rows && 16 * c16 < a.cols;
+      if (valid) *reinterpret_cast<uint2*>(a.codes_r + (size_t)row * (a.cols >> 1) + c16 * 8) = make_uint2(lo, hi);
       if (pack4) {
-        // lanes 8k, 8k+2, 8k+4, 8k+6 hold four consecutive scales of one row
-        const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 2);
-        const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 4);
-        const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 6);
-        if (valid && (lane & 7) == 0)
-          *reinterpret_cast<uint32_t*>(a.scales_r + sf_offset(row, c8 >> 1, a.atoms_k_r)) =
+        // lanes 4k .. 4k+3 hold four consecutive scales of one row
+        const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 1);
+        const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 2);
+        const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 3);
+        if (valid && (lane & 3) == 0)
+          *reinterpret_cast<uint32_t*>(a.scales_r + sf_offset(row, c16, a.atoms_k_r)) =
               bs.sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
-      } else if (valid && (q & 1) == 0) {
-        a.scales_r[sf_offset(row, c8 >> 1, a.atoms_k_r)] = static_cast<uint8_t>(bs.sb);
+      } else if (valid) {
+        a.scales_r[sf_offset(row, c16, a.atoms_k_r)] = static_cast<uint8_t>(bs.sb);
       }
     }
   }
   if (!COL) return;
-  __syncthreads();
 
   // column phase: columns c0 + 2cp, c0 + 2cp + 1; rows r0 + 32rq .. +31 (blocks 2rq .. 2rq+1 of 16)
   const uint32_t cp = tid & 63, rq = tid >> 6;
