@@ -200,7 +200,7 @@ constexpr int kTileR = 128, kTileC = 128;
 constexpr int kDualThreads = 256;
 
 template <bool ROW, bool COL, bool SR>
-__global__ void __launch_bounds__(kDualThreads) quantize_dual_kernel(const DualQuantArgs a) {
+__global__ void __launch_bounds__(kDualThreads, SR ? 3 : 5) quantize_dual_kernel(const DualQuantArgs a) {
   extern __shared__ __align__(16) uint8_t dsm[];
   uint16_t(*tile)[kTileC] = reinterpret_cast<uint16_t(*)[kTileC]>(dsm);
   uint16_t(*rtile)[kTileC] = reinterpret_cast<uint16_t(*)[kTileC]>(dsm + kTileR * kTileC * 2);
