@@ -726,7 +726,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
     const uint32_t lane_off = (quad * 32) << 16;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
     uint8_t* stg = sOut + (warp - FIRST_EPI_WARP) * 2 * CHUNK_BYTES;  // this warp's two staging chunks
-    uint32_t t = 0, nst = 0;
+    uint32_t t = 0;
     for (uint32_t mt = cluster_id; mt < num_tiles; mt += num_clusters, ++t) {
       const uint32_t mb2 = mt % tiles_m, nb2 = mt / tiles_m;
       if (*abort_flag || !mbar_wait_warp(acc_full, t & 1)) {
@@ -737,46 +737,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
       const uint32_t row0 = mb2 * 256 + rank * 128 + quad * 32;
       const uint32_t col0 = nb2 * 256 + h * 128;
       if (!p.c_f32) {
-        // TMEM -> registers -> BF16 -> swizzled shared chunk -> TMA store; the next chunk's TMEM
-        // load is issued before this one is converted
-        uint32_t acc[2][32];
-        tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + h * 128, acc[0]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          tmem_ld_wait(acc[j & 1]);
-          if (j < 3) tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + h * 128 + (j + 1) * 32, acc[(j + 1) & 1]);
-          if (j == 3) {
-            // every TMEM read of the accumulator is complete: release it to the MMA warp
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              if (leader) mbar_arrive(acc_empty);
-              else mbar_arrive_cluster_relaxed(acc_empty0);
-            }
-          }
-          uint32_t pk[16];
+        // TMEM -> registers -> BF16.  The accumulator is released as soon as all four chunks are in
+        // registers or staged: chunks 0 and 1 go to this warp's two swizzled shared chunks, 2 and 3
+        // stay packed in registers until the first two TMA stores have read their buffers.
+        auto convert = [&](const uint32_t (&a32)[32], uint32_t (&pk)[16]) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(acc[j & 1][2 * e])),
-                                                      __fmul_rn(alpha, __uint_as_float(acc[j & 1][2 * e + 1])));
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(a32[2 * e])),
+                                                      __fmul_rn(alpha, __uint_as_float(a32[2 * e + 1])));
             pk[e] = *reinterpret_cast<uint32_t*>(&b2);
           }
-          uint8_t* chunk = stg + (nst & 1) * CHUNK_BYTES;
-          // the store that last read this chunk (two stores ago) must have finished reading it
-          if (lane == 0) bulk_wait_read<1>();
-          __syncwarp();
-          // row = lane, 64 bytes; 16-byte unit u lands at u ^ ((row >> 1) & 3) (64-byte swizzle)
+        };
+        // row = lane, 64 bytes; 16-byte unit u lands at u ^ ((row >> 1) & 3) (64-byte swizzle)
+        auto stage_chunk = [&](uint8_t* chunk, const uint32_t (&pk)[16]) {
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             *reinterpret_cast<uint4*>(chunk + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4)) =
                 make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmap_c, chunk, (int32_t)(col0 + j * 32), (int32_t)row0);
-            bulk_commit_group();
-          }
-          ++nst;
+        };
+        uint8_t* buf0 = stg;
+        uint8_t* buf1 = stg + CHUNK_BYTES;
+        const uint32_t tacc = tmem + lane_off + TM_ACC + h * 128;
+        uint32_t ra[32], rb[32], pk[16], pk2[16], pk3[16];
+        // the previous tile's stores must have read both buffers before they are rewritten
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        tmem_ld_32x32b_x32(tacc, ra);
+        tmem_ld_wait(ra);
+        tmem_ld_32x32b_x32(tacc + 32, rb);
+        convert(ra, pk);
+        stage_chunk(buf0, pk);
+        tmem_ld_wait(rb);
+        tmem_ld_32x32b_x32(tacc + 64, ra);
+        convert(rb, pk);
+        stage_chunk(buf1, pk);
+        tmem_ld_wait(ra);
+        tmem_ld_32x32b_x32(tacc + 96, rb);
+        convert(ra, pk2);
+        tmem_ld_wait(rb);
+        // every TMEM read of the accumulator is complete: release it to the MMA warp
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(acc_empty);
+          else mbar_arrive_cluster_relaxed(acc_empty0);
+        }
+        convert(rb, pk3);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmap_c, buf0, (int32_t)col0, (int32_t)row0);
+          tma_store_2d(&tmap_c, buf1, (int32_t)(col0 + 32), (int32_t)row0);
+          bulk_commit_group();
+          bulk_wait_read<0>();
+        }
+        __syncwarp();
+        stage_chunk(buf0, pk2);
+        stage_chunk(buf1, pk3);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmap_c, buf0, (int32_t)(col0 + 64), (int32_t)row0);
+          tma_store_2d(&tmap_c, buf1, (int32_t)(col0 + 96), (int32_t)row0);
+          bulk_commit_group();
         }
       } else {
         const size_t row = (size_t)row0 + lane;
