@@ -874,21 +874,28 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
       : "r"(taddr));
 }
 
+// SPLIT: a cluster of two CTAs shares one 128-row block, each taking half of the K stages
+// (all 152 SMs get work when M / 128 is below the SM count; 4 stages so that two CTAs fit per
+// SM).  Rank 1 hands its FP32 partial sum to rank 0 through distributed shared memory and
+// rank 0 writes P = bf16(partial_0 + partial_1): a fixed order, so the result is deterministic.
+template <bool SPLIT>
 __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
     branch_factor_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_l,
                          uint32_t K, int r, __nv_bfloat16* __restrict__ P, unsigned int* __restrict__ amax_out) {
   using namespace bf;
+  constexpr int NST = SPLIT ? 4 : STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty = full + STAGES;
-  uint64_t* acc_full = empty + STAGES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * STAGE_BYTES);
+  uint64_t* empty = full + NST;
+  uint64_t* acc_full = empty + NST;
   uint64_t* done_bar = acc_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = SPLIT ? cluster_ctarank() : 0;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], amax_out ? 1 + 4 : 1);  // the MMA commit (+ the 4 amax warps)
     }
@@ -902,31 +909,34 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t num_k = (K + BK - 1) / BK;
-  const uint32_t m0 = blockIdx.x * BM;
+  const uint32_t num_k_all = (K + BK - 1) / BK;
+  const uint32_t kh = SPLIT ? (num_k_all + 1) / 2 : num_k_all;
+  const uint32_t k_begin = rank * kh;                 // this CTA's first K stage
+  const uint32_t num_k = SPLIT ? min(kh, num_k_all - k_begin) : num_k_all;  // >= 1: the host splits only K >= 2 stages
+  const uint32_t m0 = (SPLIT ? (blockIdx.x >> 1) : blockIdx.x) * BM;
   const uint32_t l_bytes = (uint32_t)r * BK * 2;
 
   if (warp == 0) {
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
-      int armed[STAGES];
-      uint32_t armed_phase[STAGES];
-      for (int s = 0; s < STAGES; ++s) armed[s] = 0, armed_phase[s] = 0;
+      int armed[NST];
+      uint32_t armed_phase[NST];
+      for (int s = 0; s < NST; ++s) armed[s] = 0, armed_phase[s] = 0;
       bool ok = true;
       for (uint32_t it = 0; it < num_k; ++it) {
         if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
         uint8_t* sA = smem + stage * STAGE_BYTES;
         uint8_t* sB = sA + A_BYTES;
         mbar_arrive_expect_tx(&full[stage], A_BYTES + l_bytes);
-        tma_load_2d(sA, &tmap_x, &full[stage], (int32_t)(it * BK), (int32_t)m0);
-        tma_load_2d(sB, &tmap_l, &full[stage], (int32_t)(it * BK), 0);
+        tma_load_2d(sA, &tmap_x, &full[stage], (int32_t)((k_begin + it) * BK), (int32_t)m0);
+        tma_load_2d(sB, &tmap_l, &full[stage], (int32_t)((k_begin + it) * BK), 0);
         armed[stage] = 1;
         armed_phase[stage] = phase;
-        if (++stage == STAGES) stage = 0, phase ^= 1;
+        if (++stage == NST) stage = 0, phase ^= 1;
       }
       if (!ok) {
         *abort_flag = 1;
-        for (int s = 0; s < STAGES; ++s)
+        for (int s = 0; s < NST; ++s)
           if (armed[s]) mbar_wait(&full[s], armed_phase[s]);
       }
     }
@@ -940,25 +950,28 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
         tc_fence_after();
         const uint32_t sA = smem_u32(smem + stage * STAGE_BYTES);
         const uint32_t sB = sA + A_BYTES;
-        const uint32_t krem = K - it * BK;
+        const uint32_t krem = K - (k_begin + it) * BK;
         const uint32_t nk = krem >= (uint32_t)BK ? BK / 16 : krem / 16;
         for (uint32_t kk = 0; kk < nk; ++kk)
           mma_bf16(tmem, smem_desc(sA + kk * 32, 16, 1024, kSwizzle128B),
                    smem_desc(sB + kk * 32, 16, 1024, kSwizzle128B), idesc, (it | kk) != 0);
         tc_commit(&empty[stage]);
-        if (++stage == STAGES) stage = 0, phase ^= 1;
+        if (++stage == NST) stage = 0, phase ^= 1;
       }
       if (ok) tc_commit(acc_full);
       else *abort_flag = 1;
       tc_commit(done_bar);
       mbar_wait(done_bar, 0);
     }
-  } else {
-    const uint32_t quad = warp & 3;
+  }
+  // warps 2..5: amax of the landed tiles, then the accumulator
+  uint32_t accr[4][16];  // SPLIT: this CTA's partial sum, row quad * 32 + lane, columns 16j .. 16j + 15
+  const uint32_t quad = warp & 3;
+  if (warp >= 2) {
     if (amax_out) {
-      // warps 2..5 fold every landed X tile into max |x| while the MMAs consume it: the tensor
-      // scale of X comes out of this read of X (integer max of the |bf16| patterns, as the
-      // standalone amax kernel takes it; zero padding past K does not change it)
+      // fold every landed X tile into max |x| while the MMAs consume it: the tensor scale of X
+      // comes out of this read of X (integer max of the |bf16| patterns, as the standalone
+      // amax kernel takes it; zero padding past K does not change it)
       const int t = (warp - 2) * 32 + lane;
       uint32_t m = 0, stage = 0, phase = 0;
       for (uint32_t it = 0; it < num_k; ++it) {
@@ -975,7 +988,7 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stage]);
-        if (++stage == STAGES) stage = 0, phase ^= 1;
+        if (++stage == NST) stage = 0, phase ^= 1;
       }
       m = max(m & 0xFFFFu, m >> 16);
       m = __reduce_max_sync(0xFFFFFFFFu, m);
@@ -984,26 +997,81 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
     if (!*abort_flag && mbar_wait_warp(acc_full, 0)) {
       tc_fence_after();
       const uint32_t row = m0 + quad * 32 + lane;
-      for (int j = 0; j < r; j += 16) {
-        uint32_t acc[16];
-        tmem_ld_32x32b_x16(tmem + ((quad * 32) << 16) + j, acc);
-        tmem_ld_wait16(acc);
-        uint32_t w[8];
 #pragma unroll
-        for (int h = 0; h < 8; ++h) {
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(acc[2 * h]), __uint_as_float(acc[2 * h + 1]));
-          w[h] = *reinterpret_cast<uint32_t*>(&b2);
+      for (int j = 0; j < 4; ++j) {
+        if (16 * j < r) {
+          tmem_ld_32x32b_x16(tmem + ((quad * 32) << 16) + 16 * j, accr[j]);
+          tmem_ld_wait16(accr[j]);
         }
-        uint4* dst = reinterpret_cast<uint4*>(P + (size_t)row * r + j);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
       tc_fence_before();
+      if (!SPLIT) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (16 * j >= r) break;
+          uint32_t w[8];
+#pragma unroll
+          for (int h = 0; h < 8; ++h) {
+            __nv_bfloat162 b2 =
+                __floats2bfloat162_rn(__uint_as_float(accr[j][2 * h]), __uint_as_float(accr[j][2 * h + 1]));
+            w[h] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(P + (size_t)row * r + 16 * j);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      }
     } else {
       *abort_flag = 1;
     }
   }
   __syncthreads();
+  if (SPLIT) {
+    // rank 0's stages are idle once both pipelines are done: rank 1 writes its partial there
+    // (row-major, rows padded to r + 4 floats so that 16-byte stores of 8 lanes hit distinct banks)
+    const uint32_t pitch = (uint32_t)r + 4;
+    float* partial = reinterpret_cast<float*>(smem);
+    cluster_sync();
+    if (rank == 1 && warp >= 2 && !*abort_flag) {
+      const uint32_t rl = quad * 32 + lane;
+      const uint32_t dst0 = mapa_shared(smem_u32(partial + rl * pitch), 0);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (16 * j < r) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst0 + (16 * j + 4 * q) * 4),
+                         "r"(accr[j][4 * q]), "r"(accr[j][4 * q + 1]), "r"(accr[j][4 * q + 2]),
+                         "r"(accr[j][4 * q + 3])
+                         : "memory");
+        }
+      }
+    }
+    cluster_sync();  // release / acquire: rank 1's partial is visible to rank 0
+    if (rank == 0 && warp >= 2 && !*abort_flag) {
+      const uint32_t rl = quad * 32 + lane;
+      const uint32_t row = m0 + rl;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (16 * j >= r) break;
+        uint32_t w[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 o = *reinterpret_cast<const float4*>(partial + rl * pitch + 16 * j + 4 * q);
+          const float s0 = __fadd_rn(__uint_as_float(accr[j][4 * q]), o.x);
+          const float s1 = __fadd_rn(__uint_as_float(accr[j][4 * q + 1]), o.y);
+          const float s2 = __fadd_rn(__uint_as_float(accr[j][4 * q + 2]), o.z);
+          const float s3 = __fadd_rn(__uint_as_float(accr[j][4 * q + 3]), o.w);
+          __nv_bfloat162 b0 = __floats2bfloat162_rn(s0, s1), b1 = __floats2bfloat162_rn(s2, s3);
+          w[2 * q] = *reinterpret_cast<uint32_t*>(&b0);
+          w[2 * q + 1] = *reinterpret_cast<uint32_t*>(&b1);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(P + (size_t)row * r + 16 * j);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    }
+  }
   if (*abort_flag) {  // a wait expired: let copies still in flight land first
     if (threadIdx.x == 0) drain_pause();
     __syncthreads();
@@ -1221,11 +1289,15 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
 cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ldx, const void* L, int r, void* P,
                                  float* amax_out, int num_sms, cudaStream_t s) {
   using namespace bf;
-  (void)num_sms;
+  constexpr int kSmemSplit = 4 * STAGE_BYTES + 1024 + 256;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(branch_factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    attr_err = cudaFuncSetAttribute(branch_factor_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    SMEM_BYTES);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(branch_factor_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kSmemSplit);
   });
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap tx, tl;
@@ -1236,12 +1308,32 @@ cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ld
     const cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), s);
     if (e != cudaSuccess) return e;
   }
-  const int grid = (int)(M / BM);
-  branch_factor_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tx, tl, (uint32_t)K, r,
-                                                             static_cast<__nv_bfloat16*>(P),
-                                                             reinterpret_cast<unsigned int*>(amax_out));
+  const int blocks = (int)(M / BM);
+  const int num_k = (int)((K + BK - 1) / BK);
+  __nv_bfloat16* Pb = static_cast<__nv_bfloat16*>(P);
+  unsigned int* am = reinterpret_cast<unsigned int*>(amax_out);
+  cudaError_t e;
+  if (blocks < num_sms && num_k >= 2) {
+    // fewer row blocks than SMs: two CTAs (a cluster) per row block, half of K each
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    cfg.gridDim = dim3(2 * blocks);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = kSmemSplit;
+    cfg.stream = s;
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, branch_factor_kernel<true>, tx, tl, (uint32_t)K, r, Pb, am);
+  } else {
+    branch_factor_kernel<false><<<blocks, NUM_THREADS, SMEM_BYTES, s>>>(tx, tl, (uint32_t)K, r, Pb, am);
+    e = cudaGetLastError();
+  }
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_transpose_bf16(const void* in, int64_t rows, int64_t cols, void* out, cudaStream_t s) {
