@@ -78,6 +78,9 @@ struct GemmParams {
   void* C;
   int c_f32;
   int64_t ldc;
+  // 2-SM kernel tile order: 0 walks M fastest, 1 walks N fastest.  The larger operand is walked
+  // slowest so that it streams from DRAM once while the smaller one stays resident in L2.
+  int raster_n;
 };
 
 template <int CM, int CN>
@@ -513,7 +516,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   const uint32_t cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
-  const uint32_t tiles_m = p.M / 256, num_tiles = tiles_m * (p.N / 256);
+  const uint32_t tiles_m = p.M / 256, tiles_n = p.N / 256, num_tiles = tiles_m * tiles_n;
   const uint32_t num_k = (p.K + BK - 1) / BK;
   const bool has_branch = p.r > 0;
   const uint32_t n_iter = num_k + (has_branch ? 1 : 0);
@@ -528,7 +531,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (uint32_t mt = cluster_id; mt < num_tiles && ok; mt += num_clusters) {
-        const uint32_t mb2 = mt % tiles_m, nb2 = mt / tiles_m;
+        const uint32_t mb2 = p.raster_n ? mt / tiles_n : mt % tiles_m;
+        const uint32_t nb2 = p.raster_n ? mt % tiles_n : mt / tiles_m;
         for (uint32_t it = 0; it < n_iter; ++it) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             ok = false;
@@ -728,7 +732,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
     uint8_t* stg = sOut + (warp - FIRST_EPI_WARP) * 2 * CHUNK_BYTES;  // this warp's two staging chunks
     uint32_t t = 0;
     for (uint32_t mt = cluster_id; mt < num_tiles; mt += num_clusters, ++t) {
-      const uint32_t mb2 = mt % tiles_m, nb2 = mt / tiles_m;
+      const uint32_t mb2 = p.raster_n ? mt / tiles_n : mt % tiles_m;
+      const uint32_t nb2 = p.raster_n ? mt % tiles_n : mt / tiles_m;
       if (*abort_flag || !mbar_wait_warp(acc_full, t & 1)) {
         *abort_flag = 1;
         break;
@@ -1243,6 +1248,7 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
     p.C = g.C;
     p.c_f32 = g.c_f32;
     p.ldc = g.ldc;
+    p.raster_n = g.M > g.N ? 1 : 0;  // A (M x K) is the larger operand: walk N fastest
     // BF16 output leaves through TMA stores of 32 x 32 tiles (64-byte rows, 64-byte swizzle)
     CUtensorMap tc = ta;
     if (!g.c_f32 && !make_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.C, g.N, g.M, (uint64_t)g.ldc * 2, 32, 32,
@@ -1280,6 +1286,7 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
   p.C = g.C;
   p.c_f32 = g.c_f32;
   p.ldc = g.ldc;
+  p.raster_n = 0;
   if (cm == 2 && cn == 2) return launch_gemm_cluster<2, 2>(ta, tb, tp, tq, p, num_sms, s);
   if (cm == 2) return launch_gemm_cluster<2, 1>(ta, tb, tp, tq, p, num_sms, s);
   if (cn == 2) return launch_gemm_cluster<1, 2>(ta, tb, tp, tq, p, num_sms, s);
