@@ -54,7 +54,10 @@ WORKLOADS = {
 # ncu DRAM traffic per launch of the block-scaled GEMM on the bench workload,
 # keyed by the SHA-256 of the kernel source it was captured on (null once the
 # source changes).  Filled from the committed profile summary.
-GEMM_TRAFFIC = {}
+GEMM_TRAFFIC = {
+    # profiles/gemm_nvf4_pair_block3b_dram.md: 24 launches (two steps), mean read + write per launch
+    "2546f13f98160281": 213128277,
+}
 
 
 def peaks():
