@@ -528,30 +528,37 @@ __device__ __forceinline__ BlockScale block_scale(float amax_b, float S_t) {
 // Tensor scale from amax: S_t = amax / 2688 (0 for an all-zero tensor).
 __device__ __forceinline__ float tensor_scale(float amax) { return amax == 0.0f ? 0.0f : __fdiv_rn(amax, 2688.0f); }
 
-// Stochastic rounding of y to the E2M1 grid with 16 random bits: returns the
+// The 16 random bits of one element as the float 65536 + rnd16 * 2^-7 (exponent
+// 16 above them in the high half-word): one byte permute from a Philox word,
+// whose low half feeds the even element and high half the odd one.
+__device__ __forceinline__ uint32_t sr_draw_lo(uint32_t w) { return __byte_perm(w, 0x47800000u, 0x7610); }
+__device__ __forceinline__ uint32_t sr_draw_hi(uint32_t w) { return __byte_perm(w, 0x47800000u, 0x7632); }
+
+// Stochastic rounding of y to the E2M1 grid with 16 random bits rnd16, given as
+// draw = bits of 65536 + rnd16 * 2^-7 (sr_draw_lo / sr_draw_hi): returns the
 // rounded value (a grid point, sign of y kept), for the saturating E2M1
 // conversion that follows.  With a = min(|y|, 6), lo the grid point <= a and sp
 // the gap above it (0.5 below 2, 1 in [2, 4), 2 in [4, 6]), the value rounds
 // up iff rnd16 < frac * 65536, frac = (a - lo) / sp, i.e. iff frac > u with
 // u = rnd16 / 65536.  That is the same as
 //   result = sp * ceil(a / sp - u) = ceil_sp(a - u * sp),
-// which is computed on the floating-point pipe:
-//   sp = max(2^e / 2, 0.5) from the exponent field of y (exact products);
-//   u = (1 + rnd16 * 2^-16) - 1, exact (rnd16 fills the top 16 mantissa bits);
-//   t = |y| - u * sp rounded upward (one fused multiply-add);
-//   ceil_sp(t) = (t + M rounded upward) - M with M = 1.5 * 2^23 * sp, whose
-//   binade has spacing sp and holds t + M for every t in (-sp, 8].
+// which is computed on the floating-point pipe, every product exact:
+//   s = sp * 2^-9 = max(2^e * 2^-10, 2^-10) from the exponent field of y;
+//   d = draw - 65536 = rnd16 * 2^-7, so that d * s = u * sp;
+//   t = |y| - d * s rounded upward (one fused multiply-add);
+//   ceil_sp(t) = (t + M rounded upward) - M with M = 1.5 * 2^23 * sp = 1.5 * 2^32 * s,
+//   whose binade has spacing sp and holds t + M for every t in (-sp, 8].
 // Upward rounding of t to its own (finer) grid commutes with the ceiling to
 // multiples of sp, so the result equals the arithmetic definition bit for bit
 // (denormal inputs included: no flush to zero in this code).  The clamp to 6
 // is left to the conversion: for 6 < |y| < 8 the gap is 2 and the result is 6
 // or 8, which the saturating conversion maps to 6, the clamped value's result.
-__device__ __forceinline__ float sr_round(float y, uint32_t rnd16) {
+__device__ __forceinline__ float sr_round(float y, uint32_t draw) {
   const uint32_t bits = __float_as_uint(y);
-  const float sp = fmaxf(__uint_as_float(bits & 0x7F800000u) * 0.5f, 0.5f);
-  const float M = sp * 12582912.0f;  // 1.5 * 2^23 * sp
-  const float u = __uint_as_float(0x3F800000u | (rnd16 << 7)) - 1.0f;
-  const float t = __fmaf_ru(-u, sp, fabsf(y));
+  const float sc = fmaxf(__uint_as_float(bits & 0x7F800000u) * 0x1p-10f, 0x1p-10f);
+  const float M = sc * 6442450944.0f;  // 1.5 * 2^32 * sc
+  const float d = __uint_as_float(draw) - 65536.0f;
+  const float t = __fmaf_ru(-d, sc, fabsf(y));
   const float c = __fadd_ru(t, M) - M;
   return __uint_as_float(__float_as_uint(c) | (bits & 0x80000000u));
 }

@@ -104,7 +104,7 @@ __device__ __forceinline__ void quantize_chunk_row(const RowQuantArgs& a, uint32
     const uint4 rnd = sr_random(keys, a.stream, g);
     const uint32_t rw[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = sr_round(y[i], (i & 1) ? (rw[i >> 1] >> 16) : (rw[i >> 1] & 0xFFFFu));
+    for (int i = 0; i < 8; ++i) y[i] = sr_round(y[i], (i & 1) ? sr_draw_hi(rw[i >> 1]) : sr_draw_lo(rw[i >> 1]));
   }
   const uint32_t codes = e2m1x8(y);
   const uint32_t row = g / a.cpr, c8 = g - row * a.cpr;
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 3 : 5) quantize_dual_kernel
           const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            y[hh][e] = sr_round(y[hh][e], (e & 1) ? (rw[e >> 1] >> 16) : (rw[e >> 1] & 0xFFFFu));
+            y[hh][e] = sr_round(y[hh][e], (e & 1) ? sr_draw_hi(rw[e >> 1]) : sr_draw_lo(rw[e >> 1]));
         }
       }
       const uint32_t lo = e2m1x8(y[0]), hi = e2m1x8(y[1]);
@@ -325,8 +325,8 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 3 : 5) quantize_dual_kernel
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const uint32_t rp = *reinterpret_cast<const uint32_t*>(&rtile[rb * 16 + i][2 * cp]);
-        va[i] = sr_round(va[i], rp & 0xFFFFu);
-        vb[i] = sr_round(vb[i], rp >> 16);
+        va[i] = sr_round(va[i], sr_draw_lo(rp));
+        vb[i] = sr_round(vb[i], sr_draw_hi(rp));
       }
     }
     float t8[8];
@@ -397,7 +397,7 @@ __global__ void debug_sr_round_kernel(const float* __restrict__ in, const uint16
   if (i8 >= n) return;
   float v[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = (i8 + i < n) ? sr_round(in[i8 + i], rnd[i8 + i]) : 0.0f;
+  for (int i = 0; i < 8; ++i) v[i] = (i8 + i < n) ? sr_round(in[i8 + i], 0x47800000u | rnd[i8 + i]) : 0.0f;
   const uint32_t c = e2m1x8(v);
 #pragma unroll
   for (int i = 0; i < 8; ++i)
