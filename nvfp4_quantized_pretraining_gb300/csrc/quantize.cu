@@ -170,12 +170,13 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const RowQuantArgs a
 // ---------------------------------------------------------------------------
 // Column-wise (transposed) quantization, optionally with the row-wise output
 // from the same read.  A CTA stages a 128-row x 128-column BF16 tile in shared
-// memory (8 coalesced 16-byte loads per thread in flight); the row form is
-// produced from registers right after the load, the column form from the
-// staged tile: a thread owns two adjacent columns (one 4-byte shared load per
-// row yields both) and 32 rows, i.e. four 16-row blocks.  SR random bits of
-// the column form are drawn in the row-chunk mapping (one Philox call per 8
-// source elements) and staged beside the tile.
+// memory (8 coalesced 16-byte loads per thread in flight).  Both forms are
+// then produced from the staged tile: the row form by one thread per 16-element
+// block, the column form by threads that own two adjacent columns (one 4-byte
+// shared load per row yields both, their block maxima in one packed register)
+// and 32 rows, i.e. two 16-row blocks per column.  SR random bits of the column
+// form are drawn in the row-chunk mapping (one Philox call per 8 source
+// elements) and staged beside the tile.
 // ---------------------------------------------------------------------------
 struct DualQuantArgs {
   const uint16_t* x;
@@ -305,17 +306,16 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 3 : 5) quantize_dual_kernel
   for (int h = 0; h < 2; ++h) {
     const uint32_t rb = 2 * rq + h;  // 16-row block within the tile
     float va[16], vb[16];
-    uint32_t ma = 0, mb = 0;
+    uint32_t m2 = 0;  // both columns' |bf16| maxima, one per half-word
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const uint32_t pr = *reinterpret_cast<const uint32_t*>(&tile[rb * 16 + i][2 * cp]);
-      ma = max(ma, pr & 0x7FFFu);
-      mb = max(mb, (pr >> 16) & 0x7FFFu);
+      m2 = __vmaxu2(m2, pr & 0x7FFF7FFFu);
       va[i] = bf16_lo(pr);
       vb[i] = bf16_hi(pr);
     }
-    const BlockScale sa = block_scale(__uint_as_float(ma << 16), S_t);
-    const BlockScale sb = block_scale(__uint_as_float(mb << 16), S_t);
+    const BlockScale sa = block_scale(__uint_as_float(m2 << 16), S_t);
+    const BlockScale sb = block_scale(__uint_as_float(m2 & 0xFFFF0000u), S_t);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       va[i] = __fmul_rn(va[i], sa.inv);
