@@ -374,26 +374,48 @@ def end_to_end(F, torch, projs, T, r, stream, dev, args, gemm_flops, world):
         hosts.append((hx, hdy, outs))
         h2d += hx.numel() * 2 + hdy.numel() * 2
         d2h += sum(o.numel() * o.element_size() for o in outs)
+    # Three streams, as a user of the C ABI would run it: host-to-device copies of projection i on
+    # one, its step on the compute stream once they have landed, the copies back on a third once
+    # it is done, so that transfers in both directions overlap the other projections' kernels.
+    h2d_stream = torch.cuda.Stream(device=dev)
+    d2h_stream = torch.cuda.Stream(device=dev)
     times = []
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup + args.steps):
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
+    for i in range(args.warmup + args.steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        h2d_stream.wait_event(e0)
+        landed, done = [], []
+        with torch.cuda.stream(h2d_stream):
             for p, (hx, hdy, outs) in zip(projs, hosts):
                 p["X"].copy_(hx, non_blocking=True)
                 p["dY"].copy_(hdy, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(h2d_stream)
+                landed.append(ev)
+        with torch.cuda.stream(stream):
+            for p, ev in zip(projs, landed):
+                stream.wait_event(ev)
                 F.fp4_quantize_dual(p["Wres"], out_row=p["Wq"], out_col=p["WqT"], stream=stream)
                 F.fp4_linear_fwd(p["X"], p["Wq"], p["L1"], p["L2"], Y=p["Y"], xqT_saved=p["xqT"],
                                  workspace=p["ws_f"], stream=stream)
                 F.fp4_linear_bwd(p["dY"], p["WqT"], p["xqT"], p["L1"], p["L2"], seed=i, dX=p["dX"], dW=p["dW"],
                                  workspace=p["ws_b"], stream=stream)
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                done.append(ev)
+        with torch.cuda.stream(d2h_stream):
+            for p, (hx, hdy, outs), ev in zip(projs, hosts, done):
+                d2h_stream.wait_event(ev)
                 for o, k in zip(outs, ("Y", "dX", "dW")):
                     o.copy_(p[k], non_blocking=True)
-            e1.record(stream)
-            e1.synchronize()
-            if i >= args.warmup:
-                times.append(e0.elapsed_time(e1))
+        end = torch.cuda.Event()
+        end.record(d2h_stream)
+        stream.wait_event(end)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
     ms = sum(times) / len(times)
     return {"value": round(world * gemm_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
