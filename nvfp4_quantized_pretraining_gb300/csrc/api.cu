@@ -103,12 +103,13 @@ static fp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64
     if (rows % 16 != 0)
       return fail(FP4_ERR_UNSUPPORTED_SHAPE, "transposed quantization needs rows %% 16 == 0 (rows = %lld)",
                   (long long)rows);
-    if (rows / 64 >= 65535) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rows %lld too large", (long long)rows);
     if ((st = check_tensor(out_col, "out_col"))) return st;
     if (out_col->rows != cols || out_col->cols != rows)
       return fail(FP4_ERR_INVALID_ARG, "transposed out is %lld x %lld, expected %lld x %lld",
                   (long long)out_col->rows, (long long)out_col->cols, (long long)cols, (long long)rows);
   }
+  if ((rows + 127) / 128 > 65535)  // one 128-row tile per grid row
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rows %lld too large (at most 65535 x 128)", (long long)rows);
   if (amax_opt && (reinterpret_cast<uintptr_t>(amax_opt) & 3u))
     return fail(FP4_ERR_MISALIGNED, "amax_opt must be 4-byte aligned");
   if (out_row && scale_padded(rows, cols))
@@ -122,15 +123,13 @@ static fp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64
     amax = slot;
   }
   const bool sr = round_mode == FP4_ROUND_SR;
-  if (out_row && !out_col) {
-    CUDA_TRY(launch_quantize_rows(x, rows, cols, ld, sr, seed, sr_row, amax, out_row->codes, out_row->scales,
-                                  out_row->scale, sm_count(), s));
-  } else {
-    QOut r{}, c{};
-    if (out_row) r = qout(out_row);
-    c = qout(out_col);
-    CUDA_TRY(launch_quantize_dual(x, rows, cols, ld, sr, seed, sr_row, sr_col, amax, out_row ? &r : nullptr, &c, s));
-  }
+  // one tiled kernel for every orientation request: the tile is staged once and each requested
+  // form is produced from it
+  QOut r{}, c{};
+  if (out_row) r = qout(out_row);
+  if (out_col) c = qout(out_col);
+  CUDA_TRY(launch_quantize_dual(x, rows, cols, ld, sr, seed, sr_row, sr_col, amax, out_row ? &r : nullptr,
+                                out_col ? &c : nullptr, s));
   return FP4_OK;
 }
 

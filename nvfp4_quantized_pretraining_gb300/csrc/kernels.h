@@ -17,9 +17,7 @@ void count_launch();
 
 cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float* out, int num_sms,
                         cudaStream_t s);
-cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
-                                 uint32_t stream_id, const float* amax, void* codes, void* scales, float* scale_out,
-                                 int num_sms, cudaStream_t s);
+
 cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
                                  uint32_t stream_r, uint32_t stream_c, const float* amax, const QOut* row_out,
                                  const QOut* col_out, cudaStream_t s);

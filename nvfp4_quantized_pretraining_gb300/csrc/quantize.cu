@@ -1,10 +1,10 @@
-// NVFP4 quantize kernels (sm_103a): tensor amax, row-wise quantization and the
-// column-wise (transposed) / dual-orientation quantization.
+// NVFP4 quantize kernels (sm_103a): the tensor amax and one tiled kernel that
+// produces the row-wise form, the column-wise (transposed) form, or both from
+// one read.
 //
-// All three are HBM-bound streaming kernels: 16-byte coalesced BF16 loads,
-// block amax by warp shuffle (row blocks) or in registers (column blocks),
-// packed E2M1 codes written 4 or 8 bytes at a time and UE4M3 scales written
-// straight into the layout the block-scaled MMA reads.
+// Both stream BF16 with 16-byte coalesced loads.  Block maxima are integer
+// maxima of |bf16| patterns; E2M1 codes are written 8 or 16 bytes at a time and
+// the UE4M3 scales straight into the layout the block-scaled MMA reads.
 //
 // Format reading (the Full-Stack FP4 pages name NVFP4, section 1, and
 // "standard NVFP4", section 3, without defining it): see block_scale() and
@@ -66,104 +66,6 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ 
     uint32_t b = red[0];
     for (int w = 1; w < (int)(blockDim.x >> 5); ++w) b = max(b, red[w]);
     if (b != 0) atomicMax(out, b << 16);  // float bits of the BF16 amax; ordered as unsigned
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Row-wise quantization: lane pairs (2i, 2i+1) hold the two 8-element halves
-// of one 16-element block.
-// ---------------------------------------------------------------------------
-struct RowQuantArgs {
-  const uint16_t* x;
-  int64_t ld;
-  uint32_t rows, cols, cpr, nchunks, atoms_k;
-  const float* amax;
-  uint8_t* codes;
-  uint8_t* scales;
-  float* scale_out;
-  uint64_t seed;
-  uint32_t stream;
-};
-
-template <bool SR>
-__device__ __forceinline__ void quantize_chunk_row(const RowQuantArgs& a, uint32_t g, bool valid, const uint4& w,
-                                                   float S_t, bool pack4, const PhiloxKeys& keys) {
-  const int lane = threadIdx.x & 31;
-  float v[8];
-  v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-  v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
-  // half-block amax from the integer patterns, then the pair's max
-  uint32_t m = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu), __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
-  m = max(m & 0xFFFFu, m >> 16);
-  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-  const BlockScale bs = block_scale(__uint_as_float(m << 16), S_t);
-  float y[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(v[i], bs.inv);
-  if (SR) {
-    const uint4 rnd = sr_random(keys, a.stream, g);
-    const uint32_t rw[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = sr_round(y[i], (i & 1) ? sr_draw_hi(rw[i >> 1]) : sr_draw_lo(rw[i >> 1]));
-  }
-  const uint32_t codes = e2m1x8(y);
-  const uint32_t row = g / a.cpr, c8 = g - row * a.cpr;
-  if (valid) *reinterpret_cast<uint32_t*>(a.codes + (size_t)row * (a.cols >> 1) + c8 * 4) = codes;
-  if (pack4) {
-    // lanes 0,2,4,6 (mod 8) hold four consecutive scales of one row: one 32-bit store
-    const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 2);
-    const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 4);
-    const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 6);
-    if (valid && (lane & 7) == 0)
-      *reinterpret_cast<uint32_t*>(a.scales + sf_offset(row, c8 >> 1, a.atoms_k)) =
-          bs.sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
-  } else if (valid && (lane & 1) == 0) {
-    a.scales[sf_offset(row, c8 >> 1, a.atoms_k)] = static_cast<uint8_t>(bs.sb);
-  }
-}
-
-template <bool SR>
-__global__ void __launch_bounds__(256) quantize_rows_kernel(const RowQuantArgs a) {
-  const float amax = *a.amax;
-  const float S_t = tensor_scale(amax);
-  if (blockIdx.x == 0 && threadIdx.x == 0 && a.scale_out) {
-    a.scale_out[0] = S_t;
-    a.scale_out[1] = amax;
-  }
-  // cols % 64 == 0: every aligned group of 8 chunks is 4 whole blocks of one row
-  const bool pack4 = (a.cols & 63u) == 0;
-  PhiloxKeys keys;
-  if (SR) keys = philox_keys(a.seed);
-  const uint32_t lane = threadIdx.x & 31;
-  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
-  constexpr int U = 4;
-  uint32_t base = warp * 32;
-  for (; base + (U - 1) * nwarps * 32 < a.nchunks; base += U * nwarps * 32) {
-    uint4 w[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const uint32_t g = base + u * nwarps * 32 + lane;
-      w[u] = make_uint4(0, 0, 0, 0);
-      if (g < a.nchunks) {
-        const uint32_t row = g / a.cpr, c8 = g - row * a.cpr;
-        w[u] = __ldcs(reinterpret_cast<const uint4*>(a.x + row * a.ld + c8 * 8));
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const uint32_t g = base + u * nwarps * 32 + lane;
-      quantize_chunk_row<SR>(a, g, g < a.nchunks, w[u], S_t, pack4, keys);
-    }
-  }
-  for (; base < a.nchunks; base += nwarps * 32) {
-    const uint32_t g = base + lane;
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (g < a.nchunks) {
-      const uint32_t row = g / a.cpr, c8 = g - row * a.cpr;
-      w = __ldcs(reinterpret_cast<const uint4*>(a.x + row * a.ld + c8 * 8));
-    }
-    quantize_chunk_row<SR>(a, g, g < a.nchunks, w, S_t, pack4, keys);
   }
 }
 
@@ -427,32 +329,6 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, f
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
-                                 uint32_t stream_id, const float* amax, void* codes, void* scales, float* scale_out,
-                                 int num_sms, cudaStream_t s) {
-  RowQuantArgs a;
-  a.x = static_cast<const uint16_t*>(x);
-  a.ld = ld;
-  a.rows = static_cast<uint32_t>(rows);
-  a.cols = static_cast<uint32_t>(cols);
-  a.cpr = static_cast<uint32_t>(cols / 8);
-  a.nchunks = a.rows * a.cpr;
-  a.atoms_k = static_cast<uint32_t>((cols / 16 + 3) / 4);
-  a.amax = amax;
-  a.codes = static_cast<uint8_t*>(codes);
-  a.scales = static_cast<uint8_t*>(scales);
-  a.scale_out = scale_out;
-  a.seed = seed;
-  a.stream = stream_id;
-  const int grid = grid_for(a.nchunks, 256 * 4, num_sms * 8);
-  if (sr)
-    quantize_rows_kernel<true><<<grid, 256, 0, s>>>(a);
-  else
-    quantize_rows_kernel<false><<<grid, 256, 0, s>>>(a);
-  count_launch();
-  return cudaGetLastError();
-}
-
 cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
                                  uint32_t stream_r, uint32_t stream_c, const float* amax, const QOut* row_out,
                                  const QOut* col_out, cudaStream_t s) {
@@ -480,7 +356,8 @@ cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int6
   a.stream_c = stream_c;
   dim3 grid(static_cast<unsigned>((cols + kTileC - 1) / kTileC), static_cast<unsigned>((rows + kTileR - 1) / kTileR));
   const bool R = row_out != nullptr, C = col_out != nullptr;
-  const int smem = C ? kTileR * kTileC * 2 * (sr ? 2 : 1) : 0;
+  // the BF16 tile is staged for both forms; the SR column form also stages its random bits
+  const int smem = kTileR * kTileC * 2 * ((C && sr) ? 2 : 1);
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
