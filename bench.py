@@ -56,7 +56,7 @@ WORKLOADS = {
 # source changes).  Filled from the committed profile summary.
 GEMM_TRAFFIC = {
     # profiles/gemm_nvf4_pair_block3b_dram.md: 24 launches (two steps), mean read + write per launch
-    "2546f13f98160281": 213128277,
+    "8bf1038430f07168": 213556309,
 }
 
 
