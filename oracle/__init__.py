@@ -21,6 +21,12 @@ dequantized operands.  Functions and the passages they follow:
 - ``branch_factor``: P = bf16(X @ L^T), the BF16 low-rank branch (section 2.1:
   the subspace L2 L1 is kept in BF16).  READING: the intermediate P is rounded
   to BF16 once.
+- ``lora_factor_grads``: the gradients of the branch factors, dL2 = beta dY^T P
+  and dL1 = beta P'^T X with P = bf16(X L1^T) and P' = bf16(dY L2) (section 2.1:
+  the backward pass is restricted to the subspace).  READING: straight through
+  the BF16 factors (the same rounded P and P' the forward and dX products use),
+  FP64 products, FP32 results; the Cholesky-QR constraint on the subspace is not
+  specified on the pages and is not applied here.
 - ``gemm`` / ``linear_fwd`` / ``linear_bwd``: the three products of a linear
   layer, Y = X W^T, dX = dY W, dW = dY^T X, with the residual in NVFP4 and the
   branch in BF16 (section 2.1).  READING: gradients (dY) use SR in both dX and
@@ -386,3 +392,23 @@ def linear_bwd(dY, X, W_res, L1, L2, seed: int, beta: float = 1.0, dx_rows=None,
     wr = slice(None) if dw_rows is None else np.asarray(dw_rows)
     dW = gemm(dYqT.dequantize(None if dw_rows is None else wr), XqT.dequantize())
     return dX, dW, dict(dYq=dYq, WqT=WqT, dYqT=dYqT, XqT=XqT)
+
+
+def lora_factor_grads(dY64: np.ndarray, X64: np.ndarray, P64: np.ndarray, P2_64: np.ndarray, beta: float = 1.0):
+    """Gradients of the branch factors of Y = X W_res^T + beta * P L2^T, P = X L1^T:
+        dL2 = beta * dY^T P    (N x r)      dL1 = beta * P'^T X    (r x K),  P' = dY L2.
+    All arguments FP64 (the caller decodes the BF16 tensors; P and P' are the rounded
+    factors of the BF16 branch).  FP64 products; the results are returned in FP64."""
+    dL2 = beta * (dY64.T @ P64)
+    dL1 = beta * (P2_64.T @ X64)
+    return dL1, dL2
+
+
+def lora_factor_grads_bf16(dY_bf16, X_bf16, L1_bf16, L2_bf16, beta: float = 1.0):
+    """lora_factor_grads on BF16 tensors, with P and P' formed as the branch does it."""
+    P = branch_factor(X_bf16, L1_bf16)                                  # T x r, BF16
+    P2 = branch_factor(dY_bf16, np.ascontiguousarray(L2_bf16.T))        # T x r, BF16
+    f64 = lambda u: bf16_to_f32(u).astype(np.float64)
+    dL1, dL2 = lora_factor_grads(f64(dY_bf16), f64(X_bf16), f64(P), f64(P2), beta)
+    return dL1, dL2, P, P2
+

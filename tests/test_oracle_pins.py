@@ -370,3 +370,22 @@ def test_branch_fold_alpha_one_is_exact_and_bounded_otherwise(oracle_mod):
     err = np.abs(a * oracle_mod.bf16_to_f32(Pt).astype(np.float64) - beta * Pf)
     assert np.all(err <= (2.0 ** -8 + 1e-6) * beta * np.abs(Pf) + 1e-300)
     assert np.any(err > 0)  # the rounding is real for this alpha
+
+
+def test_lora_factor_grads_match_finite_differences(oracle_mod):
+    # loss = beta * <dY, X L1^T L2^T> is linear in L1 and in L2 separately, so central differences
+    # along random directions equal <grad, E> to rounding; non-square sizes catch transpositions
+    rng = np.random.default_rng(5)
+    T, K, N, r, beta = 37, 24, 20, 5, 0.75
+    X, dY = rng.standard_normal((T, K)), rng.standard_normal((T, N))
+    L1, L2 = rng.standard_normal((r, K)), rng.standard_normal((N, r))
+    loss = lambda a1, a2: beta * np.sum(dY * (X @ a1.T @ a2.T))
+    dL1, dL2 = oracle_mod.lora_factor_grads(dY, X, X @ L1.T, dY @ L2, beta)
+    assert dL1.shape == (r, K) and dL2.shape == (N, r)
+    eps = 1e-3
+    for _ in range(4):
+        E1, E2 = rng.standard_normal((r, K)), rng.standard_normal((N, r))
+        fd1 = (loss(L1 + eps * E1, L2) - loss(L1 - eps * E1, L2)) / (2 * eps)
+        fd2 = (loss(L1, L2 + eps * E2) - loss(L1, L2 - eps * E2)) / (2 * eps)
+        assert abs(fd1 - np.sum(dL1 * E1)) <= 1e-9 * max(1.0, abs(fd1))
+        assert abs(fd2 - np.sum(dL2 * E2)) <= 1e-9 * max(1.0, abs(fd2))
