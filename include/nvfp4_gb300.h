@@ -194,6 +194,26 @@ fp4_status fp4_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t lddy,
                           void* dX, int64_t lddx, void* dW, int dw_dtype, int64_t lddw,
                           void* ws, size_t ws_bytes, void* stream);
 
+/* Gradients of the LoRA-SVD branch factors (section 2.1: W = W_res + beta L2 L1,
+ * the subspace in BF16, the backward pass restricted to the subspace), straight
+ * through the BF16 branch factors P = bf16(X L1^T) (forward) and
+ * P' = bf16(dY L2) (backward):
+ *   dL2 = beta * dY^T P   (N x r):  A = dY (T x N), B = P,  transpose_c = 0
+ *   dL1 = beta * P'^T X   (r x K):  A = X (T x K),  B = P', transpose_c = 1
+ * i.e. C = beta * A^T B with the sum over the T tokens, FP32 accumulation.
+ * A: T x M BF16, row pitch lda elements (16-byte aligned base and pitch);
+ * B: T x r BF16, pitch r; C: FP32, M x r at C[m * ldc + j] (transpose_c = 0) or
+ * r x M at C[j * ldc + m] (transpose_c = 1).  M % 128 == 0, r in {16,32,48,64},
+ * any T >= 1.  ws: at least fp4_lora_factor_grad_workspace(T, M, r) bytes,
+ * 256-byte aligned (FP32 partial sums of the token splits; the size depends on
+ * the device's SM count).  Deterministic: the partials are added in a fixed
+ * order.  The Cholesky-QR constraint the pages name is not specified there and
+ * is not applied. */
+size_t fp4_lora_factor_grad_workspace(int64_t T, int64_t M, int r);
+fp4_status fp4_lora_factor_grad(const void* A, int64_t T, int64_t M, int64_t lda,
+                                const void* B, int r, float beta, float* C, int64_t ldc,
+                                int transpose_c, void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronise `stream`, then read and clear the device status word.
  * Returns FP4_ERR_TIMEOUT if any kernel recorded an expired wait. */
 fp4_status fp4_check_status(void* stream);

@@ -33,7 +33,8 @@ OUT_F32 = 1
 
 EXPORTS = ["fp4_scale_bytes", "fp4_amax", "fp4_quantize", "fp4_quantize_transposed", "fp4_quantize_dual",
            "fp4_gemm_blockscaled", "fp4_branch_factor", "fp4_linear_fwd_workspace", "fp4_linear_bwd_workspace",
-           "fp4_linear_fwd", "fp4_linear_fwd_noalloc", "fp4_linear_bwd", "fp4_check_status", "fp4_last_error", "fp4_launch_count",
+           "fp4_linear_fwd", "fp4_linear_fwd_noalloc", "fp4_linear_bwd", "fp4_lora_factor_grad_workspace",
+           "fp4_lora_factor_grad", "fp4_check_status", "fp4_last_error", "fp4_launch_count",
            "fp4_debug_convert", "fp4_debug_sr_round", "fp4_mma_peak_probe"]
 
 
@@ -77,6 +78,8 @@ def lib() -> ctypes.CDLL:
         "fp4_linear_fwd_noalloc": (i32, [P, i64, i64, i64, T, P, P, i32, f32, P, i64, T, P]),
         "fp4_linear_bwd": (i32, [P, i64, i64, i64, T, T, P, P, i32, f32, u64, P, i64, P, i32, i64, P,
                                  ctypes.c_size_t, P]),
+        "fp4_lora_factor_grad_workspace": (ctypes.c_size_t, [i64, i64, i32]),
+        "fp4_lora_factor_grad": (i32, [P, i64, i64, i64, P, i32, f32, P, i64, i32, P, ctypes.c_size_t, P]),
         "fp4_check_status": (i32, [P]),
         "fp4_last_error": (ctypes.c_char_p, []),
         "fp4_launch_count": (u64, []),
@@ -256,6 +259,30 @@ def fp4_linear_bwd(dY, WqT: NVFP4Tensor, xqT_saved: NVFP4Tensor, L1=None, L2=Non
                                 OUT_F32 if dW.dtype == torch.float32 else OUT_BF16, dW.stride(0),
                                 workspace.data_ptr(), workspace.numel(), _stream(stream)))
     return dX, dW
+
+
+def fp4_lora_factor_grad(A: torch.Tensor, B: torch.Tensor, beta: float = 1.0, transpose: bool = False, out=None,
+                         workspace=None, stream=None) -> torch.Tensor:
+    """C = beta * A^T B (FP32) for A: T x M and B: T x r BF16; r x M when ``transpose``.
+    dL2 = fp4_lora_factor_grad(dY, P, beta); dL1 = fp4_lora_factor_grad(X, P2, beta, transpose=True)."""
+    T, M, lda = _bf16_2d(A, "A")
+    assert B.dtype == torch.bfloat16 and B.is_contiguous() and B.shape[0] == T
+    r = B.shape[1]
+    if out is None:
+        out = torch.empty((r, M) if transpose else (M, r), dtype=torch.float32, device=A.device)
+    need = lib().fp4_lora_factor_grad_workspace(T, M, r)
+    workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=A.device) if workspace is None else workspace
+    _check(lib().fp4_lora_factor_grad(A.data_ptr(), T, M, lda, B.data_ptr(), r, float(beta), out.data_ptr(),
+                                      out.stride(0), 1 if transpose else 0, workspace.data_ptr(), workspace.numel(),
+                                      _stream(stream)))
+    return out
+
+
+def lora_factor_grads(X, dY, P, P2, beta: float = 1.0, stream=None):
+    """(dL1, dL2) of the LoRA-SVD branch: dL1 = beta P2^T X (r x K), dL2 = beta dY^T P (N x r), FP32."""
+    dL2 = fp4_lora_factor_grad(dY, P, beta, stream=stream)
+    dL1 = fp4_lora_factor_grad(X, P2, beta, transpose=True, stream=stream)
+    return dL1, dL2
 
 
 def fp4_check_status(stream=None) -> None:

@@ -434,6 +434,33 @@ const char* fp4_last_error(void) { return t_err.c_str(); }
 
 uint64_t fp4_launch_count(void) { return g_launches.load(); }
 
+size_t fp4_lora_factor_grad_workspace(int64_t T, int64_t M, int r) {
+  if (T <= 0 || M <= 0 || r <= 0) return 0;
+  return round256(static_cast<size_t>(lora_grad_splits(T, M, sm_count())) * static_cast<size_t>(M) *
+                  static_cast<size_t>(r) * sizeof(float));
+}
+
+fp4_status fp4_lora_factor_grad(const void* A, int64_t T, int64_t M, int64_t lda, const void* B, int r, float beta,
+                                float* C, int64_t ldc, int transpose_c, void* ws, size_t ws_bytes, void* stream) {
+  fp4_status st;
+  if ((st = check_bf16_input(A, T, M, lda, "A"))) return st;
+  if (!B || !C) return fail(FP4_ERR_INVALID_ARG, "B and C must be non-NULL");
+  if (!aligned16(B)) return fail(FP4_ERR_MISALIGNED, "B must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(C) & 3u) return fail(FP4_ERR_MISALIGNED, "C must be 4-byte aligned");
+  if (M % 128) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "M %lld is not a multiple of 128", (long long)M);
+  if (r != 16 && r != 32 && r != 48 && r != 64) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rank r=%d not in {16,32,48,64}", r);
+  if (transpose_c != 0 && transpose_c != 1) return fail(FP4_ERR_INVALID_ARG, "transpose_c must be 0 or 1");
+  if (ldc < (transpose_c ? M : r))
+    return fail(FP4_ERR_INVALID_ARG, "ldc %lld too small for %s output", (long long)ldc, transpose_c ? "r x M" : "M x r");
+  const size_t need = fp4_lora_factor_grad_workspace(T, M, r);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return fail(FP4_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
+  const uint32_t splits = lora_grad_splits(T, M, sm_count());
+  CUDA_TRY(launch_lora_grad(A, T, M, lda, B, r, beta, C, ldc, transpose_c, static_cast<float*>(ws), splits,
+                            static_cast<cudaStream_t>(stream)));
+  return FP4_OK;
+}
+
 fp4_status fp4_debug_convert(const float* in, int64_t n, uint8_t* e2m1_out, uint8_t* e4m3_out, void* stream) {
   if (!in || !e2m1_out || !e4m3_out || n <= 0) return fail(FP4_ERR_INVALID_ARG, "bad debug_convert arguments");
   CUDA_TRY(launch_debug_convert(in, n, e2m1_out, e4m3_out, static_cast<cudaStream_t>(stream)));

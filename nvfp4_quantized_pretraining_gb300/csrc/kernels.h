@@ -58,4 +58,10 @@ cudaError_t gemm_status_read_clear(unsigned int* out, cudaStream_t s);
 // out[c][r] = in[r][c] for a BF16 rows x cols matrix (pitches = widths).
 cudaError_t launch_transpose_bf16(const void* in, int64_t rows, int64_t cols, void* out, cudaStream_t s);
 
+// LoRA factor gradients: C = beta * A^T B (A: T x M, B: T x r, row-major BF16), the token range
+// split over `splits` CTAs per 128-row block with FP32 partials in `partial` (splits x M x r).
+uint32_t lora_grad_splits(int64_t T, int64_t M, int num_sms);
+cudaError_t launch_lora_grad(const void* A, int64_t T, int64_t M, int64_t lda, const void* B, int r, float beta,
+                             float* C, int64_t ldc, int transpose_c, float* partial, uint32_t splits, cudaStream_t s);
+
 }  // namespace nvfp4
