@@ -248,6 +248,7 @@ def run_ours(args):
 
     # ---- kernel breakdown through the public calls (same operands), for the roofline
     bd = breakdown(F, torch, projs, T, r, stream, dev, flush, args)
+    lg = lora_grads(F, torch, projs, T, r, stream, dev, flush, args) if r else None
 
     # ---- end-to-end: host inputs -> device -> step -> results back to host
     e2e = end_to_end(F, torch, projs, T, r, stream, dev, args, gemm_flops, world)
@@ -277,6 +278,7 @@ def run_ours(args):
                      "note": "algorithmic bytes of the dual-orientation quantize launches (2 B read + 2 x 0.5625 B "
                              "written per element) over their event time"},
         "breakdown_ms": {k: round(v, 4) for k, v in bd["per_kind_ms"].items()},
+        "lora_factor_grads": lg,
         "branch_tflops_counted_separately": round(branch_flops / 1e12, 4),
         "e2e": e2e,
         "gpu_launches": int(launches),
@@ -358,6 +360,48 @@ def breakdown(F, torch, projs, T, r, stream, dev, flush, args):
     quant_ms = kinds.get("quantize_x_dual", 0) + kinds.get("quantize_dy_dual_sr", 0) + kinds.get("quantize_w_dual", 0)
     return dict(gemm_flops=gemm_flops, gemm_ms=kinds["gemm"], quant_bytes=quant_bytes, quant_ms=quant_ms,
                 per_kind_ms=kinds)
+
+
+def lora_grads(F, torch, projs, T, r, stream, dev, flush, args):
+    """Times the LoRA-SVD factor gradients of every projection (dL2 = beta dY^T P and
+    dL1 = beta P'^T X, with the step's own P and P'), each call after an L2 flush.
+    Not part of the timed step: a separate figure against HBM, the bound of this
+    product (it reads dY and X once; the factors and the results are small)."""
+    reps = max(2, min(args.steps, 5))
+    total = 0.0
+    nbytes = 0
+    ws = None
+    with torch.cuda.stream(stream):
+        for p in projs:
+            need = max(F.lib().fp4_lora_factor_grad_workspace(T, p["N"], r),
+                       F.lib().fp4_lora_factor_grad_workspace(T, p["K"], r))
+            if ws is None or ws.numel() < need:
+                ws = torch.empty(need, dtype=torch.uint8, device=dev)
+            dL2 = torch.empty((p["N"], r), dtype=torch.float32, device=dev)
+            dL1 = torch.empty((r, p["K"]), dtype=torch.float32, device=dev)
+            calls = [lambda: F.fp4_lora_factor_grad(p["dY"], p["P"], 1.0, out=dL2, workspace=ws, stream=stream),
+                     lambda: F.fp4_lora_factor_grad(p["X"], p["P2"], 1.0, transpose=True, out=dL1, workspace=ws,
+                                                    stream=stream)]
+            for fn, M in zip(calls, (p["N"], p["K"])):
+                fn()
+                ts = []
+                for _ in range(reps):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+                    e1.synchronize()
+                    ts.append(e0.elapsed_time(e1))
+                total += sorted(ts)[len(ts) // 2]
+                nbytes += T * M * 2 + T * r * 2 + M * r * 4
+    F.fp4_check_status(stream)
+    hbm = float(peaks()[0]["hbm_gbs"])
+    gbs = nbytes / (total * 1e-3) / 1e9
+    return {"ms_per_step": round(total, 4), "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
+            "unit": "GB/s", "frac": round(gbs / hbm, 4),
+            "note": "dL2 = dY^T P and dL1 = P'^T X of the four projections; algorithmic bytes "
+                    "(BF16 dY or X, the T x r factor, the FP32 result) over the summed median call times"}
 
 
 def end_to_end(F, torch, projs, T, r, stream, dev, args, gemm_flops, world):
