@@ -27,6 +27,18 @@ dequantized operands.  Functions and the passages they follow:
   the BF16 factors (the same rounded P and P' the forward and dX products use),
   FP64 products, FP32 results; the Cholesky-QR constraint on the subspace is not
   specified on the pages and is not applied here.
+- ``p99_clip`` / ``ns_normalize`` / ``ns_step`` / ``newton_schulz``: Q-Root,
+  Newton-Schulz iterations with every matrix product in NVFP4 (section 2.3, NVFP4
+  Root optimizer: direct NVFP4 execution; shape-dependent coefficients a, b, c and
+  p99 outlier clipping).  READINGS (the pages print neither the coefficients nor
+  the clipping rule): the quintic step X <- a X + (b A + c A^2) X with A = X X^T,
+  caller-chosen (a, b, c) (default: the cubic 1.5, -0.5, 0 for 12 steps; the
+  widely used quintic 3.4445, -4.7750, 2.0315 diverges with NVFP4 products here),
+  X_0 = G / ||G||_F, m <= n; the iterate X is clipped at the start of
+  each step to +-v, v the ceil(0.99 N)-th smallest |x| of its BF16 values (the
+  Gram matrices are not: their largest entries are the diagonal); RTN;
+  BF16 products; the two linear combinations in FP32 without contraction; with
+  c = 0 the A^2 product is skipped.
 - ``gemm`` / ``linear_fwd`` / ``linear_bwd``: the three products of a linear
   layer, Y = X W^T, dX = dY W, dW = dY^T X, with the residual in NVFP4 and the
   branch in BF16 (section 2.1).  READING: gradients (dY) use SR in both dX and
@@ -411,4 +423,76 @@ def lora_factor_grads_bf16(dY_bf16, X_bf16, L1_bf16, L2_bf16, beta: float = 1.0)
     f64 = lambda u: bf16_to_f32(u).astype(np.float64)
     dL1, dL2 = lora_factor_grads(f64(dY_bf16), f64(X_bf16), f64(P), f64(P2), beta)
     return dL1, dL2, P, P2
+
+
+# The cubic Newton-Schulz polynomial (1.5 s - 0.5 s^3, converging to 1 with zero slope there)
+# is the default: with NVFP4 products the widely used quintic (3.4445, -4.7750, 2.0315) pushes
+# singular values past its stable range and diverges in this reading (see the pins).
+NS_COEFFS = (1.5, -0.5, 0.0)
+NS_STEPS = 12
+MUON_QUINTIC = (3.4445, -4.7750, 2.0315)
+
+
+def p99_clip(x_bf16: np.ndarray, q_num: int = 99, q_den: int = 100) -> np.ndarray:
+    """Clip a BF16 tensor to +-v, v = the k-th smallest |x| with k = ceil(N q_num / q_den).
+    v is one of the tensor's own values, so the result is exactly BF16."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    mag = (x & 0x7FFF).astype(np.uint16)             # |x| patterns, ordered like |x|
+    n = mag.size
+    k = (n * q_num + q_den - 1) // q_den
+    v = np.sort(mag, axis=None)[k - 1]
+    return np.where(mag > v, (x & 0x8000) | v, x).astype(np.uint16)
+
+
+def _fl32(v):
+    return np.asarray(v, dtype=np.float32)
+
+
+def ns_lincomb(p: float, x_bf16, q: float, y_bf16) -> np.ndarray:
+    """bf16(fl32(fl32(p x) + fl32(q y))): the step's linear combinations, no FMA contraction."""
+    x = bf16_to_f32(x_bf16)
+    y = bf16_to_f32(y_bf16)
+    return bf16_rn((_fl32(np.float32(p) * x) + _fl32(np.float32(q) * y)).astype(np.float32).astype(np.float64))
+
+
+def ns_normalize(G_bf16: np.ndarray) -> np.ndarray:
+    """X_0 = bf16(G / max(||G||_F, 1e-7)), the norm and the quotient in FP64."""
+    g = bf16_to_f32(G_bf16).astype(np.float64)
+    return bf16_rn(g / max(float(np.sqrt(np.sum(g * g))), 1e-7))
+
+
+def ns_step(X_bf16: np.ndarray, a: float, b: float, c: float, clip: bool = True) -> np.ndarray:
+    """One Newton-Schulz step with NVFP4 products (section 2.3):
+    A = X X^T, B = b A + c A A, X' = a X + B X; X is m x n, m <= n.  With c = 0 (the
+    cubic) the A A product is not formed and B = bf16(fl32(b A))."""
+    X = p99_clip(X_bf16) if clip else X_bf16          # the iterate's outliers (not the Gram
+    Xq = quantize(X)                                   # matrices, whose largest entries are
+    XqT = quantize(X, transposed=True)                 # their diagonal); blocks along n / m
+    A = bf16_rn(gemm(Xq.dequantize(), Xq.dequantize()))
+    if c != 0.0:
+        Aq = quantize(A)
+        A2 = bf16_rn(gemm(Aq.dequantize(), Aq.dequantize()))   # A is symmetric: A A = A A^T
+        B = ns_lincomb(b, A, c, A2)
+    else:                                              # the cubic: B = bf16(fl32(b A))
+        B = bf16_rn(_fl32(np.float32(b) * bf16_to_f32(A)).astype(np.float64))
+    Bq = quantize(B)                                   # blocks along the contraction dim m
+    BX = bf16_rn(gemm(Bq.dequantize(), XqT.dequantize()))
+    return ns_lincomb(a, X, 1.0, BX)
+
+
+def newton_schulz(G_bf16: np.ndarray, steps: int = NS_STEPS, coeffs=NS_COEFFS, clip: bool = True) -> np.ndarray:
+    X = ns_normalize(G_bf16)
+    for _ in range(steps):
+        X = ns_step(X, *coeffs, clip=clip)
+    return X
+
+
+def newton_schulz_fp64(G: np.ndarray, steps: int = NS_STEPS, coeffs=NS_COEFFS) -> np.ndarray:
+    """The same iteration in FP64 without quantization or clipping (the exact reference)."""
+    a, b, c = coeffs
+    X = G / max(float(np.linalg.norm(G)), 1e-7)
+    for _ in range(steps):
+        A = X @ X.T
+        X = a * X + (b * A + c * (A @ A)) @ X
+    return X
 

@@ -389,3 +389,62 @@ def test_lora_factor_grads_match_finite_differences(oracle_mod):
         fd2 = (loss(L1, L2 + eps * E2) - loss(L1, L2 - eps * E2)) / (2 * eps)
         assert abs(fd1 - np.sum(dL1 * E1)) <= 1e-9 * max(1.0, abs(fd1))
         assert abs(fd2 - np.sum(dL2 * E2)) <= 1e-9 * max(1.0, abs(fd2))
+
+
+def test_newton_schulz_fp64_converges_to_polar_factor(oracle_mod):
+    # the step X <- a X + (b A + c A^2) X, A = X X^T: with the cubic (1.5, -0.5, 0) and the
+    # fifth-order (15/8, -10/8, 3/8) Newton-Schulz polynomials it converges to U V^T
+    rng = np.random.default_rng(9)
+    G = rng.standard_normal((24, 40))
+    U, _, Vt = np.linalg.svd(G, full_matrices=False)
+    polar = U @ Vt
+    for coeffs in [(1.5, -0.5, 0.0), (15 / 8, -10 / 8, 3 / 8)]:
+        X = oracle_mod.newton_schulz_fp64(G, steps=60, coeffs=coeffs)
+        assert np.abs(X - polar).max() < 1e-9, coeffs
+
+
+def test_ns_step_nvfp4_closed_form_on_scaled_identity(oracle_mod):
+    # X = s [I 0] quantizes exactly (each 16-block holds one nonzero, its own maximum), so one
+    # NVFP4 step gives the scalar recurrence a s + (b s^2 + c s^4) s on the diagonal
+    m, n, s = 32, 64, 0.5
+    X = np.zeros((m, n), np.float64)
+    X[np.arange(m), np.arange(m)] = s
+    a, b, c = oracle_mod.MUON_QUINTIC  # c != 0: the A^2 product is exercised
+    out = oracle_mod.bf16_to_f32(oracle_mod.ns_step(oracle_mod.bf16_rn(X), a, b, c, clip=False))
+    f = np.float32
+    A, A2 = f(s * s), f(s ** 4)
+    Bv = f(f(f(b) * A) + f(f(c) * A2))
+    Bv = oracle_mod.bf16_to_f32(oracle_mod.bf16_rn(np.array([Bv], np.float64)))[0]
+    BX = oracle_mod.bf16_to_f32(oracle_mod.bf16_rn(np.array([Bv * s], np.float64)))[0]
+    want = oracle_mod.bf16_to_f32(oracle_mod.bf16_rn(np.array([f(f(f(a) * f(s)) + f(BX))], np.float64)))[0]
+    assert np.all(out[np.arange(m), np.arange(m)] == want)
+    off = out.copy()
+    off[np.arange(m), np.arange(m)] = 0
+    assert np.all(off == 0)
+
+
+def test_p99_clip_matches_sorted_quantile(oracle_mod):
+    rng = np.random.default_rng(10)
+    for n in (1, 7, 100, 1000, 4097):
+        x = oracle_mod.bf16_rn(rng.standard_t(3, n) * 3.0)
+        v = np.sort(np.abs(oracle_mod.bf16_to_f32(x)))[-(-99 * n // 100) - 1]  # ceil(0.99 n)-th smallest
+        got = oracle_mod.bf16_to_f32(oracle_mod.p99_clip(x))
+        xf = oracle_mod.bf16_to_f32(x)
+        assert np.array_equal(got, np.clip(xf, -v, v))
+        assert np.mean(np.abs(xf) <= v) >= 0.99 and np.mean(np.abs(xf) < v) < 0.99 or n < 100
+
+
+def test_newton_schulz_nvfp4_stays_near_fp64_iteration(oracle_mod):
+    # the NVFP4 chain with the default cubic stays bounded and within the product noise of the
+    # FP64 iteration; the quintic diverges (the reason for the default)
+    rng = np.random.default_rng(11)
+    Gb = oracle_mod.bf16_rn(rng.standard_normal((128, 256)))
+    g = oracle_mod.bf16_to_f32(Gb).astype(np.float64)
+    X = oracle_mod.bf16_to_f32(oracle_mod.newton_schulz(Gb)).astype(np.float64)
+    ref = oracle_mod.newton_schulz_fp64(g)
+    assert np.linalg.norm(X - ref) / np.linalg.norm(ref) < 0.2
+    sv = np.linalg.svd(X, compute_uv=False)
+    assert 0.7 < sv.min() and sv.max() < 1.3
+    with np.errstate(over="ignore", invalid="ignore"):
+        Xq = oracle_mod.bf16_to_f32(oracle_mod.newton_schulz(Gb, steps=5, coeffs=oracle_mod.MUON_QUINTIC, clip=False))
+    assert not np.all(np.abs(Xq) < 10)
