@@ -249,6 +249,7 @@ def run_ours(args):
     # ---- kernel breakdown through the public calls (same operands), for the roofline
     bd = breakdown(F, torch, projs, T, r, stream, dev, flush, args)
     lg = lora_grads(F, torch, projs, T, r, stream, dev, flush, args) if r else None
+    ns = newton_schulz(F, torch, S, stream, dev, flush, args)
 
     # ---- end-to-end: host inputs -> device -> step -> results back to host
     e2e = end_to_end(F, torch, projs, T, r, stream, dev, args, gemm_flops, world)
@@ -279,6 +280,7 @@ def run_ours(args):
                              "written per element) over their event time"},
         "breakdown_ms": {k: round(v, 4) for k, v in bd["per_kind_ms"].items()},
         "lora_factor_grads": lg,
+        "newton_schulz": ns,
         "branch_tflops_counted_separately": round(branch_flops / 1e12, 4),
         "e2e": e2e,
         "gpu_launches": int(launches),
@@ -402,6 +404,43 @@ def lora_grads(F, torch, projs, T, r, stream, dev, flush, args):
             "unit": "GB/s", "frac": round(gbs / hbm, 4),
             "note": "dL2 = dY^T P and dL1 = P'^T X of the four projections; algorithmic bytes "
                     "(BF16 dY or X, the T x r factor, the FP32 result) over the summed median call times"}
+
+
+def newton_schulz(F, torch, S, stream, dev, flush, args):
+    """Times Q-Root's orthogonalisation (normalise, then 12 cubic Newton-Schulz steps with
+    NVFP4 products and the p99 clip) of one gradient of each weight shape of the block,
+    each call after an L2 flush.  Not part of the timed step (an optimizer-side figure).
+    FLOPs: 4 m^2 n per step (A = X X^T and B X)."""
+    reps = max(2, min(args.steps, 3))
+    out = {}
+    total_ms = total_flops = 0.0
+    with torch.cuda.stream(stream):
+        for i, (name, m, n) in enumerate(S.NS_SHAPES_3B):
+            G = S.normal_device((m, n), 1e-3, 500 + i, dev)
+            X = torch.empty_like(G)
+            ws = torch.empty(F.newton_schulz_workspace(m, n, F.NS_COEFFS[2]), dtype=torch.uint8, device=dev)
+            fn = lambda: F.fp4_newton_schulz(G, out=X, workspace=ws, stream=stream)
+            fn()
+            ts = []
+            for _ in range(reps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            ms = sorted(ts)[len(ts) // 2]
+            flops = F.NS_STEPS * 4.0 * m * m * n
+            out[name] = {"m": m, "n": n, "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
+            total_ms += ms
+            total_flops += flops
+            del G, X, ws
+    F.fp4_check_status(stream)
+    return {"shapes": out, "steps": F.NS_STEPS, "coeffs": list(F.NS_COEFFS), "clip": "p99 of the iterate",
+            "ms_total": round(total_ms, 4), "tflops": round(total_flops / (total_ms * 1e-3) / 1e12, 1),
+            "note": "one orthogonalisation per weight-gradient shape (m <= n); FP4 GEMM FLOPs over the "
+                    "whole call's event time (normalisation, clips, quantizations and GEMMs)"}
 
 
 def end_to_end(F, torch, projs, T, r, stream, dev, args, gemm_flops, world):

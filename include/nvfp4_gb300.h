@@ -214,6 +214,28 @@ fp4_status fp4_lora_factor_grad(const void* A, int64_t T, int64_t M, int64_t lda
                                 const void* B, int r, float beta, float* C, int64_t ldc,
                                 int transpose_c, void* ws, size_t ws_bytes, void* stream);
 
+/* Q-Root orthogonalisation: Newton-Schulz iterations with every matrix product
+ * in NVFP4 (section 2.3, NVFP4 Root optimizer: direct NVFP4 execution, shape-
+ * dependent coefficients a, b, c, p99 outlier clipping; the pages print neither
+ * the coefficients nor the clipping rule).  With normalize = 1,
+ *   X_0 = bf16(G / max(||G||_F, 1e-7))          (the norm in FP64)
+ * else X_0 = G; then `steps` times:
+ *   if clip: X <- sign(X) min(|X|, v), v = the ceil(0.99 m n)-th smallest |x|
+ *   A  = bf16(Q(X) Q(X)^T)                       (m x m; Q = NVFP4 RTN, blocks along n)
+ *   B  = bf16(fl32(b A) + fl32(c bf16(Q(A) Q(A)^T)))   (c = 0: B = bf16(fl32(b A)),
+ *                                                 the A^2 product is not formed)
+ *   X  <- bf16(fl32(a X) + bf16(Q(B) Q_T(X)))     (Q_T: blocks along m)
+ * G: m x n BF16, row pitch ldg; X: m x n BF16 output, row pitch ldx (X may be G);
+ * both 16-byte aligned with 16-byte pitches.  m % 128 == 0, n % 128 == 0,
+ * m * n < 2^34; m <= n is the efficient orientation (the caller transposes a tall
+ * matrix).  0 <= steps <= 1000.  ws: at least fp4_newton_schulz_workspace(m, n, c)
+ * bytes, 256-byte aligned.  Deterministic (the norm's partial sums and the
+ * histograms reduce in a fixed order or in integers). */
+size_t fp4_newton_schulz_workspace(int64_t m, int64_t n, float c);
+fp4_status fp4_newton_schulz(const void* G, int64_t m, int64_t n, int64_t ldg, int normalize,
+                             int steps, float a, float b, float c, int clip, void* X,
+                             int64_t ldx, void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronise `stream`, then read and clear the device status word.
  * Returns FP4_ERR_TIMEOUT if any kernel recorded an expired wait. */
 fp4_status fp4_check_status(void* stream);

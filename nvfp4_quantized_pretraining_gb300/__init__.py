@@ -34,7 +34,7 @@ OUT_F32 = 1
 EXPORTS = ["fp4_scale_bytes", "fp4_amax", "fp4_quantize", "fp4_quantize_transposed", "fp4_quantize_dual",
            "fp4_gemm_blockscaled", "fp4_branch_factor", "fp4_linear_fwd_workspace", "fp4_linear_bwd_workspace",
            "fp4_linear_fwd", "fp4_linear_fwd_noalloc", "fp4_linear_bwd", "fp4_lora_factor_grad_workspace",
-           "fp4_lora_factor_grad", "fp4_check_status", "fp4_last_error", "fp4_launch_count",
+           "fp4_lora_factor_grad", "fp4_newton_schulz_workspace", "fp4_newton_schulz", "fp4_check_status", "fp4_last_error", "fp4_launch_count",
            "fp4_debug_convert", "fp4_debug_sr_round", "fp4_mma_peak_probe"]
 
 
@@ -80,6 +80,9 @@ def lib() -> ctypes.CDLL:
                                  ctypes.c_size_t, P]),
         "fp4_lora_factor_grad_workspace": (ctypes.c_size_t, [i64, i64, i32]),
         "fp4_lora_factor_grad": (i32, [P, i64, i64, i64, P, i32, f32, P, i64, i32, P, ctypes.c_size_t, P]),
+        "fp4_newton_schulz_workspace": (ctypes.c_size_t, [i64, i64, f32]),
+        "fp4_newton_schulz": (i32, [P, i64, i64, i64, i32, i32, f32, f32, f32, i32, P, i64, P, ctypes.c_size_t,
+                                    P]),
         "fp4_check_status": (i32, [P]),
         "fp4_last_error": (ctypes.c_char_p, []),
         "fp4_launch_count": (u64, []),
@@ -283,6 +286,33 @@ def lora_factor_grads(X, dY, P, P2, beta: float = 1.0, stream=None):
     dL2 = fp4_lora_factor_grad(dY, P, beta, stream=stream)
     dL1 = fp4_lora_factor_grad(X, P2, beta, transpose=True, stream=stream)
     return dL1, dL2
+
+
+NS_COEFFS = (1.5, -0.5, 0.0)  # the cubic Newton-Schulz polynomial
+NS_STEPS = 12
+
+
+def newton_schulz_workspace(m: int, n: int, c: float = 0.0) -> int:
+    return int(lib().fp4_newton_schulz_workspace(m, n, float(c)))
+
+
+def fp4_newton_schulz(G: torch.Tensor, steps: int = NS_STEPS, coeffs=NS_COEFFS, clip: bool = True,
+                      normalize: bool = True, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """Q-Root orthogonalisation of an m x n BF16 matrix (m <= n the efficient orientation):
+    X_0 = G / ||G||_F (``normalize``), then ``steps`` Newton-Schulz steps
+    X <- a X + (b A + c A^2) X, A = X X^T, every product in NVFP4, the iterate p99-clipped
+    (``clip``) at the start of each step.  Returns the BF16 result (``out`` if given)."""
+    m, n, ldg = _bf16_2d(G, "G")
+    a, b, c = (float(v) for v in coeffs)
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=G.device)
+    _, _, ldx = _bf16_2d(out, "out")
+    need = newton_schulz_workspace(m, n, c)
+    workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=G.device) if workspace is None else workspace
+    _check(lib().fp4_newton_schulz(G.data_ptr(), m, n, ldg, 1 if normalize else 0, int(steps), a, b, c,
+                                   1 if clip else 0, out.data_ptr(), ldx, workspace.data_ptr(), workspace.numel(),
+                                   _stream(stream)))
+    return out
 
 
 def fp4_check_status(stream=None) -> None:

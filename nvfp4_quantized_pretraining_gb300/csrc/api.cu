@@ -239,6 +239,40 @@ static size_t bwd_ws(int64_t M, int64_t N, int64_t K, int r, Carver* c, fp4_tens
   return cv.off;
 }
 
+// Workspace of fp4_newton_schulz: the iterate's two NVFP4 forms, the m x m Gram
+// matrix (B overwrites it), A's NVFP4 form and A^2 when c != 0, B's NVFP4 form,
+// the m x n product B X, the magnitude histogram, the norm's partial sums and a
+// clip-value slot.
+struct NsBufs {
+  fp4_tensor xq, xqT, aq, bq;
+  void* A;
+  void* A2;
+  void* BX;
+  uint32_t* hist;
+  double* partial;
+  uint32_t* clip;
+};
+
+static size_t ns_ws(int64_t m, int64_t n, float c, Carver* c_opt, NsBufs* out) {
+  Carver local(nullptr);
+  Carver& cv = c_opt ? *c_opt : local;
+  NsBufs w{};
+  w.xq = carve_tensor(cv, m, n);
+  w.xqT = carve_tensor(cv, n, m);
+  w.A = cv.take(static_cast<size_t>(m * m * 2));
+  if (c != 0.0f) {
+    w.aq = carve_tensor(cv, m, m);
+    w.A2 = cv.take(static_cast<size_t>(m * m * 2));
+  }
+  w.bq = carve_tensor(cv, m, m);
+  w.BX = cv.take(static_cast<size_t>(m * n * 2));
+  w.hist = static_cast<uint32_t*>(cv.take(kNsHistBins * sizeof(uint32_t)));
+  w.partial = static_cast<double*>(cv.take(static_cast<size_t>(ns_sumsq_blocks(sm_count())) * sizeof(double)));
+  w.clip = static_cast<uint32_t*>(cv.take(16));
+  if (out) *out = w;
+  return cv.off;
+}
+
 // Scratch of fp4_linear_fwd_noalloc: one file-scope device buffer, created with
 // the module, so that call needs no allocation.  32 MiB holds the forward
 // workspace up to M * K ~ 50e6 elements at r = 64 (e.g. M = 16384, K = 3072).
@@ -458,6 +492,72 @@ fp4_status fp4_lora_factor_grad(const void* A, int64_t T, int64_t M, int64_t lda
   const uint32_t splits = lora_grad_splits(T, M, sm_count());
   CUDA_TRY(launch_lora_grad(A, T, M, lda, B, r, beta, C, ldc, transpose_c, static_cast<float*>(ws), splits,
                             static_cast<cudaStream_t>(stream)));
+  return FP4_OK;
+}
+
+size_t fp4_newton_schulz_workspace(int64_t m, int64_t n, float c) {
+  if (m <= 0 || n <= 0) return 0;
+  return ns_ws(m, n, c, nullptr, nullptr);
+}
+
+fp4_status fp4_newton_schulz(const void* G, int64_t m, int64_t n, int64_t ldg, int normalize, int steps, float a,
+                             float b, float c, int clip, void* X, int64_t ldx, void* ws, size_t ws_bytes,
+                             void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  fp4_status st;
+  if ((st = check_bf16_input(G, m, n, ldg, "G")) || (st = check_bf16_input(X, m, n, ldx, "X"))) return st;
+  if (m % 128 || n % 128)
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "Newton-Schulz needs m %% 128 == 0 and n %% 128 == 0 (m=%lld n=%lld)",
+                (long long)m, (long long)n);
+  if (m * n >= (int64_t(1) << 34)) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "Newton-Schulz matrix too large");
+  if (steps < 0 || steps > 1000) return fail(FP4_ERR_INVALID_ARG, "steps %d not in [0, 1000]", steps);
+  if ((normalize != 0 && normalize != 1) || (clip != 0 && clip != 1))
+    return fail(FP4_ERR_INVALID_ARG, "normalize and clip must be 0 or 1");
+  if (G != X && ldg == ldx) {
+    const uint8_t* g0 = static_cast<const uint8_t*>(G);
+    const uint8_t* x0 = static_cast<const uint8_t*>(X);
+    const int64_t span = ((m - 1) * ldx + n) * 2;
+    if (g0 < x0 + span && x0 < g0 + span) return fail(FP4_ERR_INVALID_ARG, "G and X overlap without being equal");
+  }
+  const size_t need = fp4_newton_schulz_workspace(m, n, c);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return fail(FP4_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
+  Carver cv(ws);
+  NsBufs w;
+  ns_ws(m, n, c, &cv, &w);
+  const int sms = sm_count();
+  // k-th smallest magnitude: k = ceil(0.99 m n)
+  const int64_t count = m * n;
+  const uint32_t k = static_cast<uint32_t>((count * 99 + 99) / 100);
+  uint32_t* hist = clip ? w.hist : nullptr;
+  if (clip && steps > 0) CUDA_TRY(cudaMemsetAsync(w.hist, 0, kNsHistBins * sizeof(uint32_t), s));
+  uint32_t* hist0 = steps > 0 ? hist : nullptr;
+  if (normalize) {
+    CUDA_TRY(launch_ns_normalize(G, m, n, ldg, X, ldx, w.partial, hist0, sms, s));
+  } else if (G != X || hist0) {
+    CUDA_TRY(launch_ns_lincomb(G, ldg, 1.0f, nullptr, 0, 0.0f, X, ldx, m, n, nullptr, hist0, sms, s));
+  }
+  for (int it = 0; it < steps; ++it) {
+    const float* amax_x = nullptr;
+    if (clip) {
+      CUDA_TRY(launch_ns_select_clip(w.hist, k, X, m, n, ldx, w.clip, &w.xq.scale[1], nullptr, sms, s));
+      amax_x = &w.xq.scale[1];  // the clipped iterate's max |x| is the clip value itself
+    }
+    if ((st = quantize_impl(X, m, n, ldx, FP4_ROUND_RTN, 0, 0, 0, amax_x, &w.xq, &w.xqT, s))) return st;
+    if ((st = gemm_impl(&w.xq, &w.xq, nullptr, nullptr, 0, 0.0f, w.A, FP4_OUT_BF16, m, s))) return st;
+    const void* A2 = nullptr;
+    if (c != 0.0f) {
+      if ((st = quantize_impl(w.A, m, m, m, FP4_ROUND_RTN, 0, 0, 0, nullptr, &w.aq, nullptr, s))) return st;
+      if ((st = gemm_impl(&w.aq, &w.aq, nullptr, nullptr, 0, 0.0f, w.A2, FP4_OUT_BF16, m, s))) return st;
+      A2 = w.A2;
+    }
+    // B overwrites A in place; its max |B| goes straight to the quantizer
+    CUDA_TRY(launch_ns_lincomb(w.A, m, b, A2, m, c, w.A, m, m, m, &w.bq.scale[1], nullptr, sms, s));
+    if ((st = quantize_impl(w.A, m, m, m, FP4_ROUND_RTN, 0, 0, 0, &w.bq.scale[1], &w.bq, nullptr, s))) return st;
+    if ((st = gemm_impl(&w.bq, &w.xqT, nullptr, nullptr, 0, 0.0f, w.BX, FP4_OUT_BF16, n, s))) return st;
+    CUDA_TRY(launch_ns_lincomb(X, ldx, a, w.BX, n, 1.0f, X, ldx, m, n, nullptr, it + 1 < steps ? hist : nullptr, sms,
+                               s));
+  }
   return FP4_OK;
 }
 

@@ -64,4 +64,22 @@ uint32_t lora_grad_splits(int64_t T, int64_t M, int num_sms);
 cudaError_t launch_lora_grad(const void* A, int64_t T, int64_t M, int64_t lda, const void* B, int r, float beta,
                              float* C, int64_t ldc, int transpose_c, float* partial, uint32_t splits, cudaStream_t s);
 
+// Newton-Schulz elementwise kernels (BF16 matrices, cols % 8 == 0, rows * cols / 8 < 2^32).
+// Normalisation: X = bf16(G / max(||G||_F, 1e-7)); `partial` holds ns_sumsq_blocks(num_sms)
+// doubles; hist (optional, zeroed, 32768 counters) receives the |X| histogram.
+constexpr int kNsHistBins = 32768;
+int ns_sumsq_blocks(int num_sms);
+cudaError_t launch_ns_normalize(const void* G, int64_t rows, int64_t cols, int64_t ldg, void* X, int64_t ldx,
+                                double* partial, uint32_t* hist, int num_sms, cudaStream_t s);
+// The k-th smallest |x| pattern from `hist` (then zeroed) into *clip_slot and, as a float, into
+// *amax_out; *zero_slot (optional) is zeroed; then X is clipped in place to +-that value.
+cudaError_t launch_ns_select_clip(uint32_t* hist, uint32_t k, void* X, int64_t rows, int64_t cols, int64_t ldx,
+                                  uint32_t* clip_slot, float* amax_out, unsigned int* zero_slot, int num_sms,
+                                  cudaStream_t s);
+// out = bf16(fl32(p x) + fl32(q y)) (y optional); amax_out (optional): max |out| (zeroed here);
+// hist (optional, zeroed): the |out| histogram.  out may alias x or y.
+cudaError_t launch_ns_lincomb(const void* x, int64_t ldx, float p, const void* y, int64_t ldy, float q, void* out,
+                              int64_t ldo, int64_t rows, int64_t cols, float* amax_out, uint32_t* hist, int num_sms,
+                              cudaStream_t s);
+
 }  // namespace nvfp4

@@ -11,7 +11,10 @@ Recipes (all from numpy's PCG64 with an explicit seed):
   - activations X ~ N(0, 1), or Student-t(df=3) / sqrt(3) (unit variance);
   - weights W ~ N(0, 0.02^2), optionally with a few columns scaled x20;
   - gradients dY ~ N(0, (1e-3)^2) (1e-3 read as the standard deviation);
-  - quantize-sweep tensors ~ N(0, 1) with 0.1% of entries scaled x50.
+  - quantize-sweep tensors ~ N(0, 1) with 0.1% of entries scaled x50;
+  - Newton-Schulz iterates X = U diag(s) V^T (m x n) with U, V from the QR
+    factorisation of Gaussian matrices and s ~ Uniform[s_lo, s_hi]: a matrix
+    part-way to orthogonality.
 """
 from __future__ import annotations
 
@@ -69,6 +72,15 @@ def weight_with_outlier_columns(n_out: int, n_in: int, std: float, n_cols: int,
     return to_bf16_bits(w)
 
 
+def spectrum_matrix(m: int, n: int, s_lo: float, s_hi: float, seed: int) -> np.ndarray:
+    """m x n (m <= n) with singular values ~ Uniform[s_lo, s_hi] and random singular vectors."""
+    rng = np.random.default_rng(seed)
+    U, _ = np.linalg.qr(rng.standard_normal((m, m)))
+    V, _ = np.linalg.qr(rng.standard_normal((n, m)))
+    s = rng.uniform(s_lo, s_hi, size=m)
+    return to_bf16_bits(((U * s) @ V.T).astype(np.float32))
+
+
 # Workload shapes.  Names describe what each is.
 SINGLE_FWD_256x512x512 = dict(name="single_fwd_256x512x512_r16", M=256, K=512, N=512, r=16,
                               x="normal", seed=0)
@@ -83,6 +95,8 @@ BLOCK_3B_PROJECTIONS = [
 BLOCK_3B = dict(name="block3b_T16384_d3072_ff8192_r64", T=16384, r=64,
                 projections=BLOCK_3B_PROJECTIONS)
 QUANT_SWEEP_ELEMS = [1 << 20, 1 << 24, 1 << 26, 1 << 28]
+# Q-Root Newton-Schulz: the weight-gradient shapes of the 3B block, oriented m <= n
+NS_SHAPES_3B = [("qkv", 3072, 9216), ("o", 3072, 3072), ("gate_up", 3072, 16384), ("down", 3072, 8192)]
 GEMM_SWEEP = [(2048, 2048, 2048), (4096, 4096, 4096), (8192, 8192, 8192),
               (16384, 16384, 16384), (16384, 3072, 8192), (3072, 8192, 16384)]
 
