@@ -12,6 +12,9 @@ Recipes (all from numpy's PCG64 with an explicit seed):
   - weights W ~ N(0, 0.02^2), optionally with a few columns scaled x20;
   - gradients dY ~ N(0, (1e-3)^2) (1e-3 read as the standard deviation);
   - quantize-sweep tensors ~ N(0, 1) with 0.1% of entries scaled x50;
+  - AdamW second moments v = (a_i b_j)^2 z_ij: row and column scales a, b
+    ~ lognormal(0, 0.5), z the mean of 8 squared Student-t(3) draws / 3 (a
+    heavy-tailed mean-1 factor), times 1e-6;
   - Newton-Schulz iterates X = U diag(s) V^T (m x n) with U, V from the QR
     factorisation of Gaussian matrices and s ~ Uniform[s_lo, s_hi]: a matrix
     part-way to orthogonality.
@@ -79,6 +82,15 @@ def spectrum_matrix(m: int, n: int, s_lo: float, s_hi: float, seed: int) -> np.n
     V, _ = np.linalg.qr(rng.standard_normal((n, m)))
     s = rng.uniform(s_lo, s_hi, size=m)
     return to_bf16_bits(((U * s) @ V.T).astype(np.float32))
+
+
+def adam_second_moment(rows: int, cols: int, seed: int) -> np.ndarray:
+    """FP32 [rows, cols] non-negative state shaped like AdamW's v_t (see the recipe above)."""
+    rng = np.random.default_rng(seed)
+    a = np.exp(rng.normal(0.0, 0.5, (rows, 1)))
+    b = np.exp(rng.normal(0.0, 0.5, (1, cols)))
+    z = np.mean(rng.standard_t(3, (8, rows, cols)) ** 2, axis=0) / 3.0
+    return ((a * b) ** 2 * z * 1e-6).astype(np.float32)
 
 
 # Workload shapes.  Names describe what each is.

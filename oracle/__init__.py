@@ -39,6 +39,16 @@ dequantized operands.  Functions and the passages they follow:
   Gram matrices are not: their largest entries are the diagonal); RTN;
   BF16 products; the two linear combinations in FP32 without contraction; with
   c = 0 the A^2 product is skipped.
+- ``fwht16`` / ``vt_encode`` / ``vt_decode``: the Q-AdamW second-moment codec
+  (section 2.2, Quantized-state AdamW: square root, tile mean kept in BF16,
+  Hadamard transform of the residual, NVFP4; rebuilt by inverting the transform
+  and the mean, then squaring).  READINGS (the pages give no sizes): the tile and
+  the Hadamard both span one 16-element NVFP4 block along a row; the mean is the
+  FP32 pairwise-tree sum of the 16 square roots times 1/16, rounded to BF16; the
+  transform is the Walsh-Hadamard butterfly in natural order, FP32, scaled by
+  1/4 (orthonormal, its own inverse); RTN with one tensor scale from the
+  transformed residual's amax; the decode takes each dequantized value to FP32
+  once, then inverts in FP32; every step in FP32 without contraction.
 - ``gemm`` / ``linear_fwd`` / ``linear_bwd``: the three products of a linear
   layer, Y = X W^T, dX = dY W, dW = dY^T X, with the residual in NVFP4 and the
   branch in BF16 (section 2.1).  READING: gradients (dY) use SR in both dX and
@@ -117,6 +127,8 @@ def lib():
                 fn = getattr(L, name)
                 fn.argtypes = [P, i64, i64, i64, ctypes.c_int, u64, u32, f32, P, P]
                 fn.restype = None
+            L.oracle_quantize_rows_f32.argtypes = [P, i64, i64, f32, P, P]
+            L.oracle_quantize_rows_f32.restype = None
             L.oracle_dequantize.argtypes = [P, P, f32, i64, i64, P]
             L.oracle_dequantize.restype = None
             L.oracle_mma_scale_offset.argtypes = [i64, i64, i64]
@@ -423,6 +435,78 @@ def lora_factor_grads_bf16(dY_bf16, X_bf16, L1_bf16, L2_bf16, beta: float = 1.0)
     f64 = lambda u: bf16_to_f32(u).astype(np.float64)
     dL1, dL2 = lora_factor_grads(f64(dY_bf16), f64(X_bf16), f64(P), f64(P2), beta)
     return dL1, dL2, P, P2
+
+
+# ---------------------------------------------------------------------------
+# Q-AdamW second-moment codec (section 2.2)
+# ---------------------------------------------------------------------------
+
+def fwht16(x) -> np.ndarray:
+    """Walsh-Hadamard transform (unnormalised, natural order) of each trailing
+    16-vector, FP32: four butterfly stages, stage h pairing i and i + h within
+    groups of 2h, (a, b) -> (a + b, a - b)."""
+    y = np.array(x, dtype=np.float32, copy=True)
+    for h in (1, 2, 4, 8):
+        v = y.reshape(y.shape[:-1] + (16 // (2 * h), 2, h))
+        a = v[..., 0, :].copy()
+        b = v[..., 1, :].copy()
+        v[..., 0, :] = a + b
+        v[..., 1, :] = a - b
+    return y
+
+
+def _tree_sum16(u):
+    """FP32 pairwise sum of each trailing 16-vector: adjacent pairs, then pairs of those."""
+    t = np.asarray(u, dtype=np.float32)
+    while t.shape[-1] > 1:
+        t = t[..., 0::2] + t[..., 1::2]
+    return t[..., 0]
+
+
+def vt_transform(v_f32: np.ndarray):
+    """The encoder's steps before quantization: returns (h, mean_bf16) with
+    u = sqrt(v), mean = bf16(tree_sum(u) / 16) per 16-block, r = u - mean,
+    h = fwht16(r) / 4, all FP32."""
+    v = np.ascontiguousarray(v_f32, dtype=np.float32)
+    R, C = v.shape
+    assert C % 16 == 0
+    u = np.sqrt(v).reshape(R, C // 16, 16)
+    mean = bf16_rn(_tree_sum16(u).astype(np.float64) / 16.0)
+    r = u - bf16_to_f32(mean)[..., None]
+    h = fwht16(r) * np.float32(0.25)
+    return h.reshape(R, C), mean
+
+
+def quantize_f32(x_f32: np.ndarray) -> QTensor:
+    """RTN row quantization of an FP32 [R, C] tensor (blocks of 16 along C)."""
+    x = np.ascontiguousarray(x_f32, dtype=np.float32)
+    R, C = x.shape
+    a = float(np.max(np.abs(x))) if x.size else 0.0
+    S = tensor_scale(a)
+    codes = np.zeros((R, C // 2), dtype=np.uint8)
+    scales = np.zeros((R, C // 16), dtype=np.uint8)
+    lib().oracle_quantize_rows_f32(_ptr(x), R, C, S, _ptr(codes), _ptr(scales))
+    return QTensor(codes, scales, S, np.float32(a), R, C)
+
+
+def vt_encode(v_f32: np.ndarray):
+    """Encode a non-negative FP32 second moment: (QTensor of the transformed
+    residual, BF16 tile means [R, C/16])."""
+    h, mean = vt_transform(v_f32)
+    return quantize_f32(h), mean
+
+
+def vt_inverse(h_f32: np.ndarray, mean_bf16: np.ndarray) -> np.ndarray:
+    """The decoder's steps after dequantization: u = fwht16(h) / 4 + mean, v = u * u (FP32)."""
+    h = np.asarray(h_f32, dtype=np.float32)
+    R, C = h.shape
+    r = fwht16(h.reshape(R, C // 16, 16)) * np.float32(0.25)
+    u = r + bf16_to_f32(mean_bf16)[..., None]
+    return (u * u).reshape(R, C)
+
+
+def vt_decode(q: QTensor, mean_bf16: np.ndarray) -> np.ndarray:
+    return vt_inverse(q.dequantize().astype(np.float32), mean_bf16)
 
 
 # The cubic Newton-Schulz polynomial (1.5 s - 0.5 s^3, converging to 1 with zero slope there)

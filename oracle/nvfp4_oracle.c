@@ -296,6 +296,31 @@ void oracle_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t
     }
 }
 
+/* Row orientation of an FP32 tensor (RTN only): the same block rule as
+ * oracle_quantize_rows applied to FP32 inputs (used by the optimizer-state
+ * codec, whose transformed values are FP32). */
+void oracle_quantize_rows_f32(const float* x, int64_t rows, int64_t cols, float S_t,
+                              uint8_t* codes, uint8_t* scales) {
+    int64_t kb = cols / 16;
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < kb; ++b) {
+            float v[16];
+            for (int i = 0; i < 16; ++i) v[i] = x[r * cols + b * 16 + i];
+            float inv;
+            uint8_t s_b = block_scale(v, 16, S_t, &inv);
+            scales[r * kb + b] = s_b;
+            for (int i = 0; i < 16; ++i) {
+                uint8_t q = oracle_e2m1_rtn(v[i] * inv);
+                int64_t idx = r * cols + b * 16 + i;
+                uint8_t* byte = &codes[idx / 2];
+                if (idx % 2 == 0) *byte = (uint8_t)((*byte & 0xF0) | q);
+                else *byte = (uint8_t)((*byte & 0x0F) | (q << 4));
+            }
+        }
+    }
+}
+
 /* Column orientation: blocks of 16 along rows, emitted as the transposed
  * (cols x rows) tensor, i.e. output row c holds source column c.  rows must
  * be a multiple of 16.  codes: cols x rows/2 bytes; scales: cols x rows/16.

@@ -448,3 +448,84 @@ def test_newton_schulz_nvfp4_stays_near_fp64_iteration(oracle_mod):
     with np.errstate(over="ignore", invalid="ignore"):
         Xq = oracle_mod.bf16_to_f32(oracle_mod.newton_schulz(Gb, steps=5, coeffs=oracle_mod.MUON_QUINTIC, clip=False))
     assert not np.all(np.abs(Xq) < 10)
+
+
+# ---------------------------------------------------------------------------
+# Q-AdamW second-moment codec
+# ---------------------------------------------------------------------------
+
+def _sylvester16():
+    H = np.array([[1.0]])
+    while H.shape[0] < 16:
+        H = np.block([[H, H], [H, -H]])
+    return H
+
+
+def test_fwht16_is_the_hadamard_matrix_and_its_own_inverse(oracle_mod):
+    H = _sylvester16()
+    assert np.array_equal(H @ H, 16 * np.eye(16))
+    x = np.random.default_rng(3).standard_normal((5, 16)).astype(np.float32)
+    y = oracle_mod.fwht16(x).astype(np.float64)
+    ref = x.astype(np.float64) @ H.T
+    assert np.max(np.abs(y - ref)) <= 16 * 2.0 ** -24 * np.max(np.abs(ref))
+    # integer inputs: every butterfly is exact, so the transform is exactly H x
+    xi = np.random.default_rng(4).integers(-1000, 1000, (7, 16)).astype(np.float32)
+    assert np.array_equal(oracle_mod.fwht16(xi).astype(np.float64), xi.astype(np.float64) @ H.T)
+    assert np.array_equal(oracle_mod.fwht16(oracle_mod.fwht16(xi)), 16 * xi)
+
+
+def test_vt_transform_inverts_without_quantization(oracle_mod):
+    from nvfp4_quantized_pretraining_gb300 import synthetic as S
+    v = S.adam_second_moment(32, 128, 5)
+    h, mean = oracle_mod.vt_transform(v)
+    back = oracle_mod.vt_inverse(h, mean).astype(np.float64)
+    assert np.max(np.abs(np.sqrt(back) - np.sqrt(v)) / np.sqrt(v)) < 1e-5
+    # the tile mean is the BF16 rounding of the block's mean of square roots
+    want = np.sqrt(v.astype(np.float64)).reshape(32, 8, 16).mean(-1)
+    got = oracle_mod.bf16_to_f32(mean).astype(np.float64)
+    assert np.max(np.abs(got - want) / want) <= 2.0 ** -8
+
+
+def test_vt_codec_constant_blocks_are_exact(oracle_mod):
+    # a block of equal values whose square root is a BF16 number has a zero residual
+    v = np.repeat(np.array([[4.0, 2.25, 0.0, 0.015625]], dtype=np.float32), 16, axis=1)
+    q, mean = oracle_mod.vt_encode(v)
+    assert np.array_equal(oracle_mod.bf16_to_f32(mean), np.array([[2.0, 1.5, 0.0, 0.125]], dtype=np.float32))
+    assert not q.codes.any()
+    assert np.array_equal(oracle_mod.vt_decode(q, mean), v)
+
+
+def test_vt_codec_worked_block(oracle_mod):
+    # Worked by hand: u = 1 + (21/128) * (row k of the 16-point Hadamard matrix) has mean 1
+    # (the row sums to 0 for k > 0), residual +-21/128, and transform (16/4)(21/128) e_k =
+    # 0.65625 e_k.  Then amax = 0.65625, S_t = 0.65625 / 2688 = 2^-12, the block scale is
+    # E4M3(448) = 0x7E, the spike's code is +6 (0x7) and the others 0; decoding gives
+    # 6 * 448 * 2^-12 = 0.65625 back, so v = u^2 returns exactly.
+    H = _sylvester16()
+    for k in (1, 5, 15):
+        u = 1.0 + (21.0 / 128.0) * H[k]
+        v = (u * u).astype(np.float32)[None, :]
+        assert np.array_equal(v.astype(np.float64), (u * u)[None, :])   # exact squares
+        q, mean = oracle_mod.vt_encode(v)
+        assert oracle_mod.bf16_to_f32(mean)[0, 0] == 1.0
+        assert q.S_t == np.float32(2.0 ** -12)
+        assert q.scales[0, 0] == 0x7E
+        codes = np.stack([q.codes[0] & 0xF, q.codes[0] >> 4], axis=1).reshape(-1)
+        want = np.zeros(16, dtype=np.uint8)
+        want[k] = 0x7
+        assert np.array_equal(codes, want)
+        assert np.array_equal(oracle_mod.vt_decode(q, mean), v)
+
+
+def test_vt_codec_lowers_the_error_of_plain_nvfp4(oracle_mod):
+    # section 2.2: the transformed pipeline stores v_t with a lower reconstruction error than
+    # NVFP4 of v_t itself; measured on sqrt(v), the quantity the AdamW update divides by
+    from nvfp4_quantized_pretraining_gb300 import synthetic as S
+    v = S.adam_second_moment(256, 512, 6)
+    r = lambda vh: np.linalg.norm(np.sqrt(np.maximum(vh, 0)) - np.sqrt(v)) / np.linalg.norm(np.sqrt(v))
+    plain = r(oracle_mod.quantize_f32(v).dequantize())
+    q, mean = oracle_mod.vt_encode(v)
+    codec = r(oracle_mod.vt_decode(q, mean).astype(np.float64))
+    sqrt_only = r(oracle_mod.quantize_f32(np.sqrt(v)).dequantize() ** 2)
+    assert codec < 0.4 * plain
+    assert codec < sqrt_only < plain
