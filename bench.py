@@ -250,6 +250,7 @@ def run_ours(args):
     bd = breakdown(F, torch, projs, T, r, stream, dev, flush, args)
     lg = lora_grads(F, torch, projs, T, r, stream, dev, flush, args) if r else None
     ns = newton_schulz(F, torch, S, stream, dev, flush, args)
+    vt = qadamw_codec(F, torch, projs, stream, dev, flush, args)
 
     # ---- end-to-end: host inputs -> device -> step -> results back to host
     e2e = end_to_end(F, torch, projs, T, r, stream, dev, args, gemm_flops, world)
@@ -281,6 +282,7 @@ def run_ours(args):
         "breakdown_ms": {k: round(v, 4) for k, v in bd["per_kind_ms"].items()},
         "lora_factor_grads": lg,
         "newton_schulz": ns,
+        "qadamw_v_codec": vt,
         "branch_tflops_counted_separately": round(branch_flops / 1e12, 4),
         "e2e": e2e,
         "gpu_launches": int(launches),
@@ -441,6 +443,54 @@ def newton_schulz(F, torch, S, stream, dev, flush, args):
             "ms_total": round(total_ms, 4), "tflops": round(total_flops / (total_ms * 1e-3) / 1e12, 1),
             "note": "one orthogonalisation per weight-gradient shape (m <= n); FP4 GEMM FLOPs over the "
                     "whole call's event time (normalisation, clips, quantizations and GEMMs)"}
+
+
+def qadamw_codec(F, torch, projs, stream, dev, flush, args):
+    """Times the Q-AdamW second-moment codec on the AdamW state of each weight of the block
+    (FP32 v with the weight's shape), encode and decode separately, each call after an L2
+    flush.  Not part of the timed step (an optimizer-side figure).  Algorithmic bytes per
+    element: encode reads v once (4 B) and writes codes, scales and means (0.6875 B); decode
+    the reverse.  The encoder reads v twice (max |h| first), so its ceiling is ~54% of HBM."""
+    reps = max(2, min(args.steps, 5))
+    enc = dec = 0.0
+    elems = 0
+    with torch.cuda.stream(stream):
+        for i, p in enumerate(projs):
+            R, C = p["N"], p["K"]
+            g = torch.Generator(device=dev)
+            g.manual_seed(900 + i)
+            v = (torch.randn((R, C), generator=g, device=dev) ** 2) * 1e-6
+            q = F.NVFP4Tensor.empty(R, C, dev)
+            mean = torch.empty((R, C // 16), dtype=torch.bfloat16, device=dev)
+            out = torch.empty_like(v)
+            calls = (lambda: F.fp4_qadamw_v_encode(v, out=q, mean=mean, stream=stream),
+                     lambda: F.fp4_qadamw_v_decode(q, mean, out=out, stream=stream))
+            med = []
+            for fn in calls:
+                fn()
+                ts = []
+                for _ in range(reps):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+                    e1.synchronize()
+                    ts.append(e0.elapsed_time(e1))
+                med.append(sorted(ts)[len(ts) // 2])
+            enc += med[0]
+            dec += med[1]
+            elems += R * C
+            del v, q, mean, out
+    F.fp4_check_status(stream)
+    hbm = float(peaks()[0]["hbm_gbs"])
+    nbytes = elems * (4 + 0.5 + 1 / 16 + 2 / 16)
+    ge, gd = nbytes / (enc * 1e-3) / 1e9, nbytes / (dec * 1e-3) / 1e9
+    return {"elements": elems, "encode_ms": round(enc, 4), "decode_ms": round(dec, 4), "bound": "hbm",
+            "encode_gbs": round(ge, 1), "decode_gbs": round(gd, 1), "peak": hbm, "unit": "GB/s",
+            "encode_frac": round(ge / hbm, 4), "decode_frac": round(gd / hbm, 4),
+            "note": "v_t of the four weights (FP32 state); 4.6875 algorithmic B/element each way over the "
+                    "summed median call times; the encoder reads v twice by design"}
 
 
 def end_to_end(F, torch, projs, T, r, stream, dev, args, gemm_flops, world):

@@ -236,6 +236,27 @@ fp4_status fp4_newton_schulz(const void* G, int64_t m, int64_t n, int64_t ldg, i
                              int steps, float a, float b, float c, int clip, void* X,
                              int64_t ldx, void* ws, size_t ws_bytes, void* stream);
 
+/* Q-AdamW second-moment codec (section 2.2, Quantized-state AdamW: v_t is
+ * stored in NVFP4 after a square root, a tile mean kept in BF16 and a Hadamard
+ * transform of the residual; it is rebuilt by inverting the transform and the
+ * mean, then squaring).  The pages give no tile or transform size; here both
+ * span one 16-element NVFP4 block along a row:
+ *   u = sqrt(v)                        mean = bf16((pairwise-tree sum of u) / 16)
+ *   h = WHT16(u - mean) / 4            (Walsh-Hadamard butterfly, natural order)
+ *   out = NVFP4 RTN of h               (tensor scale from max |h|)
+ * and decode: v' = (WHT16(deq) / 4 + mean)^2, deq = fl32(e2m1 * e4m3 * S_t).
+ * Every step is one FP32 operation in that order (bit-reproducible).
+ * v: rows x cols FP32, v >= 0 (a negative or NaN entry is unsupported), row
+ * pitch ldv elements (16-byte aligned base and pitch), cols % 16 == 0.
+ * out: rows x cols NVFP4 tensor (scales in the MMA layout, out->scale[0] = S_t,
+ * [1] = max |h|).  mean: rows x cols/16 BF16, row-major, pitch cols/16.
+ * Encode reads v twice (max |h|, then the codes).  Decode writes v_out
+ * (rows x cols FP32, pitch ldo, 16-byte aligned) from in and mean. */
+fp4_status fp4_qadamw_v_encode(const float* v, int64_t rows, int64_t cols, int64_t ldv,
+                               fp4_tensor* out, uint16_t* mean, void* stream);
+fp4_status fp4_qadamw_v_decode(const fp4_tensor* in, const uint16_t* mean, float* v_out,
+                               int64_t ldo, void* stream);
+
 /* Synchronise `stream`, then read and clear the device status word.
  * Returns FP4_ERR_TIMEOUT if any kernel recorded an expired wait. */
 fp4_status fp4_check_status(void* stream);

@@ -34,7 +34,8 @@ OUT_F32 = 1
 EXPORTS = ["fp4_scale_bytes", "fp4_amax", "fp4_quantize", "fp4_quantize_transposed", "fp4_quantize_dual",
            "fp4_gemm_blockscaled", "fp4_branch_factor", "fp4_linear_fwd_workspace", "fp4_linear_bwd_workspace",
            "fp4_linear_fwd", "fp4_linear_fwd_noalloc", "fp4_linear_bwd", "fp4_lora_factor_grad_workspace",
-           "fp4_lora_factor_grad", "fp4_newton_schulz_workspace", "fp4_newton_schulz", "fp4_check_status", "fp4_last_error", "fp4_launch_count",
+           "fp4_lora_factor_grad", "fp4_newton_schulz_workspace", "fp4_newton_schulz", "fp4_qadamw_v_encode",
+           "fp4_qadamw_v_decode", "fp4_check_status", "fp4_last_error", "fp4_launch_count",
            "fp4_debug_convert", "fp4_debug_sr_round", "fp4_mma_peak_probe"]
 
 
@@ -83,6 +84,8 @@ def lib() -> ctypes.CDLL:
         "fp4_newton_schulz_workspace": (ctypes.c_size_t, [i64, i64, f32]),
         "fp4_newton_schulz": (i32, [P, i64, i64, i64, i32, i32, f32, f32, f32, i32, P, i64, P, ctypes.c_size_t,
                                     P]),
+        "fp4_qadamw_v_encode": (i32, [P, i64, i64, i64, T, P, P]),
+        "fp4_qadamw_v_decode": (i32, [T, P, P, i64, P]),
         "fp4_check_status": (i32, [P]),
         "fp4_last_error": (ctypes.c_char_p, []),
         "fp4_launch_count": (u64, []),
@@ -312,6 +315,36 @@ def fp4_newton_schulz(G: torch.Tensor, steps: int = NS_STEPS, coeffs=NS_COEFFS, 
     _check(lib().fp4_newton_schulz(G.data_ptr(), m, n, ldg, 1 if normalize else 0, int(steps), a, b, c,
                                    1 if clip else 0, out.data_ptr(), ldx, workspace.data_ptr(), workspace.numel(),
                                    _stream(stream)))
+    return out
+
+
+def _f32_2d(x: torch.Tensor, name: str):
+    if x.dtype != torch.float32 or x.dim() != 2 or not x.is_cuda or x.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D CUDA float32 tensor with unit column stride")
+    return x.shape[0], x.shape[1], x.stride(0)
+
+
+def fp4_qadamw_v_encode(v: torch.Tensor, out: NVFP4Tensor | None = None, mean: torch.Tensor | None = None,
+                        stream=None):
+    """Encode AdamW's second moment v (FP32, >= 0): sqrt, BF16 mean per 16-element block,
+    16-point Hadamard of the residual, NVFP4.  Returns (NVFP4Tensor, BF16 means [R, C/16])."""
+    R, C, ldv = _f32_2d(v, "v")
+    out = NVFP4Tensor.empty(R, C, v.device) if out is None else out
+    if mean is None:
+        mean = torch.empty((R, C // 16), dtype=torch.bfloat16, device=v.device)
+    ct = out.c()
+    _check(lib().fp4_qadamw_v_encode(v.data_ptr(), R, C, ldv, ctypes.byref(ct), mean.data_ptr(), _stream(stream)))
+    return out, mean
+
+
+def fp4_qadamw_v_decode(q: NVFP4Tensor, mean: torch.Tensor, out: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """Rebuild v (FP32) from fp4_qadamw_v_encode's output."""
+    if out is None:
+        out = torch.empty((q.rows, q.cols), dtype=torch.float32, device=mean.device)
+    _, _, ldo = _f32_2d(out, "out")
+    ct = q.c()
+    _check(lib().fp4_qadamw_v_decode(ctypes.byref(ct), mean.data_ptr(), out.data_ptr(), ldo, _stream(stream)))
     return out
 
 

@@ -561,6 +561,42 @@ fp4_status fp4_newton_schulz(const void* G, int64_t m, int64_t n, int64_t ldg, i
   return FP4_OK;
 }
 
+static fp4_status check_f32_matrix(const float* p, int64_t rows, int64_t cols, int64_t ld, const char* name) {
+  if (!p) return fail(FP4_ERR_INVALID_ARG, "%s is NULL", name);
+  if (rows <= 0 || cols <= 0 || cols % 16 != 0)
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "%s is %lld x %lld: cols must be a positive multiple of 16", name,
+                (long long)rows, (long long)cols);
+  if (ld < cols) return fail(FP4_ERR_INVALID_ARG, "%s: ld %lld < cols %lld", name, (long long)ld, (long long)cols);
+  if (!aligned16(p) || ld % 4 != 0)
+    return fail(FP4_ERR_MISALIGNED, "%s: base and row pitch must be 16-byte aligned", name);
+  if (rows * (cols / 16) >= (int64_t(1) << 32)) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "%s too large", name);
+  return FP4_OK;
+}
+
+fp4_status fp4_qadamw_v_encode(const float* v, int64_t rows, int64_t cols, int64_t ldv, fp4_tensor* out,
+                               uint16_t* mean, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  fp4_status st;
+  if ((st = check_f32_matrix(v, rows, cols, ldv, "v")) || (st = check_tensor(out, "out"))) return st;
+  if (out->rows != rows || out->cols != cols)
+    return fail(FP4_ERR_INVALID_ARG, "out is %lld x %lld, expected %lld x %lld", (long long)out->rows,
+                (long long)out->cols, (long long)rows, (long long)cols);
+  if (!mean || (reinterpret_cast<uintptr_t>(mean) & 1u)) return fail(FP4_ERR_INVALID_ARG, "mean must be non-NULL and 2-byte aligned");
+  if (scale_padded(rows, cols)) CUDA_TRY(cudaMemsetAsync(out->scales, 0, scale_bytes(rows, cols), s));
+  CUDA_TRY(launch_vt_encode(v, rows, cols, ldv, qout(out), mean, sm_count(), s));
+  return FP4_OK;
+}
+
+fp4_status fp4_qadamw_v_decode(const fp4_tensor* in, const uint16_t* mean, float* v_out, int64_t ldo, void* stream) {
+  fp4_status st;
+  if ((st = check_tensor(in, "in"))) return st;
+  if ((st = check_f32_matrix(v_out, in->rows, in->cols, ldo, "v_out"))) return st;
+  if (!mean || (reinterpret_cast<uintptr_t>(mean) & 1u)) return fail(FP4_ERR_INVALID_ARG, "mean must be non-NULL and 2-byte aligned");
+  CUDA_TRY(launch_vt_decode(in->codes, in->scales, in->scale, mean, in->rows, in->cols, v_out, ldo, sm_count(),
+                            static_cast<cudaStream_t>(stream)));
+  return FP4_OK;
+}
+
 fp4_status fp4_debug_convert(const float* in, int64_t n, uint8_t* e2m1_out, uint8_t* e4m3_out, void* stream) {
   if (!in || !e2m1_out || !e4m3_out || n <= 0) return fail(FP4_ERR_INVALID_ARG, "bad debug_convert arguments");
   CUDA_TRY(launch_debug_convert(in, n, e2m1_out, e4m3_out, static_cast<cudaStream_t>(stream)));

@@ -82,4 +82,12 @@ cudaError_t launch_ns_lincomb(const void* x, int64_t ldx, float p, const void* y
                               int64_t ldo, int64_t rows, int64_t cols, float* amax_out, uint32_t* hist, int num_sms,
                               cudaStream_t s);
 
+// Q-AdamW second-moment codec: v (FP32 rows x cols, pitch ldv, cols % 16 == 0) to NVFP4
+// codes/scales/S_t (out; out.scale[1] receives the amax) and BF16 tile means (rows x cols/16);
+// and back to FP32 (pitch ldo).
+cudaError_t launch_vt_encode(const float* v, int64_t rows, int64_t cols, int64_t ldv, const QOut& out,
+                             uint16_t* mean, int num_sms, cudaStream_t s);
+cudaError_t launch_vt_decode(const void* codes, const void* scales, const float* scale, const uint16_t* mean,
+                             int64_t rows, int64_t cols, float* out, int64_t ldo, int num_sms, cudaStream_t s);
+
 }  // namespace nvfp4
