@@ -165,6 +165,9 @@ def run_ours(args):
     B.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.part != "all":
+        run_part(args, F, torch, S, dev)
+        return
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     wl = WORKLOADS[args.workload]
@@ -408,12 +411,25 @@ def lora_grads(F, torch, projs, T, r, stream, dev, flush, args):
                     "(BF16 dY or X, the T x r factor, the FP32 result) over the summed median call times"}
 
 
+def run_part(args, F, torch, S, dev):
+    """One optimizer-side measurement alone, with the same shapes as in the full line."""
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    if args.part == "newton_schulz":
+        res = newton_schulz(F, torch, S, stream, dev, flush, args)
+    else:
+        wl = WORKLOADS[args.workload]
+        projs = [dict(name=n, N=N, K=K) for n, N, K in wl["projections"]]
+        res = qadamw_codec(F, torch, projs, stream, dev, flush, args)
+    print(json.dumps({args.part: res}), flush=True)
+
+
 def newton_schulz(F, torch, S, stream, dev, flush, args):
     """Times Q-Root's orthogonalisation (normalise, then 12 cubic Newton-Schulz steps with
     NVFP4 products and the p99 clip) of one gradient of each weight shape of the block,
     each call after an L2 flush.  Not part of the timed step (an optimizer-side figure).
     FLOPs: 4 m^2 n per step (A = X X^T and B X)."""
-    reps = max(2, min(args.steps, 3))
+    reps = max(1, min(args.steps, 3))
     out = {}
     total_ms = total_flops = 0.0
     with torch.cuda.stream(stream):
@@ -451,7 +467,7 @@ def qadamw_codec(F, torch, projs, stream, dev, flush, args):
     flush.  Not part of the timed step (an optimizer-side figure).  Algorithmic bytes per
     element: encode reads v once (4 B) and writes codes, scales and means (0.6875 B); decode
     the reverse.  The encoder reads v twice (max |h| first), so its ceiling is ~54% of HBM."""
-    reps = max(2, min(args.steps, 5))
+    reps = max(1, min(args.steps, 5))
     enc = dec = 0.0
     elems = 0
     with torch.cuda.stream(stream):
@@ -628,6 +644,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="block3b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--part", choices=["all", "newton_schulz", "qadamw_v_codec"], default="all",
+                    help="run one optimizer-side measurement alone (prints its JSON object; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -227,7 +227,7 @@ fp4_status fp4_lora_factor_grad(const void* A, int64_t T, int64_t M, int64_t lda
  *   X  <- bf16(fl32(a X) + bf16(Q(B) Q_T(X)))     (Q_T: blocks along m)
  * G: m x n BF16, row pitch ldg; X: m x n BF16 output, row pitch ldx (X may be G);
  * both 16-byte aligned with 16-byte pitches.  m % 128 == 0, n % 128 == 0,
- * m * n < 2^34; m <= n is the efficient orientation (the caller transposes a tall
+ * m * n < 2^32; m <= n is the efficient orientation (the caller transposes a tall
  * matrix).  0 <= steps <= 1000.  ws: at least fp4_newton_schulz_workspace(m, n, c)
  * bytes, 256-byte aligned.  Deterministic (the norm's partial sums and the
  * histograms reduce in a fixed order or in integers). */

@@ -84,9 +84,11 @@ static fp4_status check_bf16_input(const void* x, int64_t rows, int64_t cols, in
 static QOut qout(const fp4_tensor* t) { return QOut{t->codes, t->scales, t->scale}; }
 
 // Quantize in one or both orientations.  amax: precomputed (device) or NULL.
+// clip (optional, device; both forms, RTN): |x| is clipped to that BF16 magnitude pattern first.
 static fp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld, int round_mode,
                                 uint64_t seed, uint32_t sr_row, uint32_t sr_col, const float* amax_opt,
-                                const fp4_tensor* out_row, const fp4_tensor* out_col, cudaStream_t s) {
+                                const fp4_tensor* out_row, const fp4_tensor* out_col, cudaStream_t s,
+                                const uint32_t* clip = nullptr) {
   fp4_status st = check_bf16_input(x, rows, cols, ld, "x");
   if (st) return st;
   if (round_mode != FP4_ROUND_RTN && round_mode != FP4_ROUND_SR)
@@ -129,7 +131,7 @@ static fp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64
   if (out_row) r = qout(out_row);
   if (out_col) c = qout(out_col);
   CUDA_TRY(launch_quantize_dual(x, rows, cols, ld, sr, seed, sr_row, sr_col, amax, out_row ? &r : nullptr,
-                                out_col ? &c : nullptr, s));
+                                out_col ? &c : nullptr, s, clip));
   return FP4_OK;
 }
 
@@ -509,7 +511,8 @@ fp4_status fp4_newton_schulz(const void* G, int64_t m, int64_t n, int64_t ldg, i
   if (m % 128 || n % 128)
     return fail(FP4_ERR_UNSUPPORTED_SHAPE, "Newton-Schulz needs m %% 128 == 0 and n %% 128 == 0 (m=%lld n=%lld)",
                 (long long)m, (long long)n);
-  if (m * n >= (int64_t(1) << 34)) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "Newton-Schulz matrix too large");
+  if (m * n >= (int64_t(1) << 32))  // 32-bit histogram counts
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "Newton-Schulz matrix too large (m n >= 2^32)");
   if (steps < 0 || steps > 1000) return fail(FP4_ERR_INVALID_ARG, "steps %d not in [0, 1000]", steps);
   if ((normalize != 0 && normalize != 1) || (clip != 0 && clip != 1))
     return fail(FP4_ERR_INVALID_ARG, "normalize and clip must be 0 or 1");
@@ -535,15 +538,18 @@ fp4_status fp4_newton_schulz(const void* G, int64_t m, int64_t n, int64_t ldg, i
   if (normalize) {
     CUDA_TRY(launch_ns_normalize(G, m, n, ldg, X, ldx, w.partial, hist0, sms, s));
   } else if (G != X || hist0) {
-    CUDA_TRY(launch_ns_lincomb(G, ldg, 1.0f, nullptr, 0, 0.0f, X, ldx, m, n, nullptr, hist0, sms, s));
+    CUDA_TRY(launch_ns_lincomb(G, ldg, 1.0f, nullptr, 0, 0.0f, X, ldx, m, n, nullptr, nullptr, hist0, sms, s));
   }
+  // The clip is applied by the iterate's readers (the quantizer and the update), so X stays unclipped
+  // in memory between the two.
+  const uint32_t* clip_v = clip ? w.clip : nullptr;
   for (int it = 0; it < steps; ++it) {
     const float* amax_x = nullptr;
     if (clip) {
-      CUDA_TRY(launch_ns_select_clip(w.hist, k, X, m, n, ldx, w.clip, &w.xq.scale[1], nullptr, sms, s));
+      CUDA_TRY(launch_ns_select(w.hist, k, w.clip, &w.xq.scale[1], s));
       amax_x = &w.xq.scale[1];  // the clipped iterate's max |x| is the clip value itself
     }
-    if ((st = quantize_impl(X, m, n, ldx, FP4_ROUND_RTN, 0, 0, 0, amax_x, &w.xq, &w.xqT, s))) return st;
+    if ((st = quantize_impl(X, m, n, ldx, FP4_ROUND_RTN, 0, 0, 0, amax_x, &w.xq, &w.xqT, s, clip_v))) return st;
     if ((st = gemm_impl(&w.xq, &w.xq, nullptr, nullptr, 0, 0.0f, w.A, FP4_OUT_BF16, m, s))) return st;
     const void* A2 = nullptr;
     if (c != 0.0f) {
@@ -552,11 +558,11 @@ fp4_status fp4_newton_schulz(const void* G, int64_t m, int64_t n, int64_t ldg, i
       A2 = w.A2;
     }
     // B overwrites A in place; its max |B| goes straight to the quantizer
-    CUDA_TRY(launch_ns_lincomb(w.A, m, b, A2, m, c, w.A, m, m, m, &w.bq.scale[1], nullptr, sms, s));
+    CUDA_TRY(launch_ns_lincomb(w.A, m, b, A2, m, c, w.A, m, m, m, nullptr, &w.bq.scale[1], nullptr, sms, s));
     if ((st = quantize_impl(w.A, m, m, m, FP4_ROUND_RTN, 0, 0, 0, &w.bq.scale[1], &w.bq, nullptr, s))) return st;
     if ((st = gemm_impl(&w.bq, &w.xqT, nullptr, nullptr, 0, 0.0f, w.BX, FP4_OUT_BF16, n, s))) return st;
-    CUDA_TRY(launch_ns_lincomb(X, ldx, a, w.BX, n, 1.0f, X, ldx, m, n, nullptr, it + 1 < steps ? hist : nullptr, sms,
-                               s));
+    CUDA_TRY(launch_ns_lincomb(X, ldx, a, w.BX, n, 1.0f, X, ldx, m, n, clip_v, nullptr,
+                               it + 1 < steps ? hist : nullptr, sms, s));
   }
   return FP4_OK;
 }

@@ -18,9 +18,11 @@ void count_launch();
 cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float* out, int num_sms,
                         cudaStream_t s);
 
+// clip (optional, device, both orientations with RTN only): |x| is clipped to this BF16
+// magnitude pattern before quantization.
 cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
                                  uint32_t stream_r, uint32_t stream_c, const float* amax, const QOut* row_out,
-                                 const QOut* col_out, cudaStream_t s);
+                                 const QOut* col_out, cudaStream_t s, const uint32_t* clip = nullptr);
 cudaError_t launch_debug_convert(const float* in, int64_t n, uint8_t* e2m1, uint8_t* e4m3, cudaStream_t s);
 cudaError_t launch_debug_sr_round(const float* in, const uint16_t* rnd, int64_t n, uint8_t* e2m1, cudaStream_t s);
 
@@ -72,15 +74,14 @@ int ns_sumsq_blocks(int num_sms);
 cudaError_t launch_ns_normalize(const void* G, int64_t rows, int64_t cols, int64_t ldg, void* X, int64_t ldx,
                                 double* partial, uint32_t* hist, int num_sms, cudaStream_t s);
 // The k-th smallest |x| pattern from `hist` (then zeroed) into *clip_slot and, as a float, into
-// *amax_out; *zero_slot (optional) is zeroed; then X is clipped in place to +-that value.
-cudaError_t launch_ns_select_clip(uint32_t* hist, uint32_t k, void* X, int64_t rows, int64_t cols, int64_t ldx,
-                                  uint32_t* clip_slot, float* amax_out, unsigned int* zero_slot, int num_sms,
-                                  cudaStream_t s);
-// out = bf16(fl32(p x) + fl32(q y)) (y optional); amax_out (optional): max |out| (zeroed here);
-// hist (optional, zeroed): the |out| histogram.  out may alias x or y.
+// *amax_out (the clipped tensor's max |x|).
+cudaError_t launch_ns_select(uint32_t* hist, uint32_t k, uint32_t* clip_slot, float* amax_out, cudaStream_t s);
+// out = bf16(fl32(p x') + fl32(q y)) (y optional), x' = x clipped to +-*clip_x (optional);
+// amax_out (optional): max |out| (zeroed here); hist (optional, zeroed): the |out| histogram.
+// out may alias x or y.
 cudaError_t launch_ns_lincomb(const void* x, int64_t ldx, float p, const void* y, int64_t ldy, float q, void* out,
-                              int64_t ldo, int64_t rows, int64_t cols, float* amax_out, uint32_t* hist, int num_sms,
-                              cudaStream_t s);
+                              int64_t ldo, int64_t rows, int64_t cols, const uint32_t* clip_x, float* amax_out,
+                              uint32_t* hist, int num_sms, cudaStream_t s);
 
 // Q-AdamW second-moment codec: v (FP32 rows x cols, pitch ldv, cols % 16 == 0) to NVFP4
 // codes/scales/S_t (out; out.scale[1] receives the amax) and BF16 tile means (rows x cols/16);

@@ -5,7 +5,10 @@
 //   - X_0 = bf16(G / ||G||_F): a sum of squares (fixed-order reduction), then the
 //     scaled copy, which also histograms |X_0| for the first clip;
 //   - the p99 clip: the k-th smallest |x| of the iterate read off a 32768-bin
-//     histogram of the BF16 magnitude patterns (integer, exact), then the clip;
+//     histogram of the BF16 magnitude patterns (integer, exact); the clip itself
+//     is applied by the iterate's two readers (the quantizer as it stages a
+//     tile, and the step's final linear combination), so the iterate is never
+//     rewritten;
 //   - the linear combinations out = bf16(fl32(p x) + fl32(q y)), fused either with
 //     the amax of the output (for its quantization) or with the histogram of the
 //     output (the next step's clip).
@@ -17,6 +20,7 @@
 namespace nvfp4 {
 
 constexpr int kNsThreads = 512;
+constexpr int kNsHistThreads = 1024;  // kernels with a 128 KB shared histogram: one CTA per SM
 constexpr int kHistBins = kNsHistBins;  // one bin per BF16 magnitude pattern (sign cleared)
 constexpr size_t kHistSmem = kHistBins * sizeof(uint32_t);
 
@@ -154,7 +158,7 @@ __device__ __forceinline__ double sum_partials(const double* __restrict__ partia
 // X = bf16(G / max(||G||_F, 1e-7)); HIST: also histogram |X| into `hist`.
 // G and X may be the same matrix (each element is read, then written, by one thread).
 template <bool HIST>
-__global__ void __launch_bounds__(kNsThreads) ns_normalize_kernel(const uint16_t* g, int64_t ldg,
+__global__ void __launch_bounds__(HIST ? kNsHistThreads : kNsThreads) ns_normalize_kernel(const uint16_t* g, int64_t ldg,
                                                                   uint16_t* x, int64_t ldx, uint32_t cpr,
                                                                   uint32_t nchunks, const double* __restrict__ partial,
                                                                   int npartial, uint32_t* __restrict__ hist) {
@@ -164,134 +168,148 @@ __global__ void __launch_bounds__(kNsThreads) ns_normalize_kernel(const uint16_t
   const double inv64 = 1.0 / fmax(norm, 1e-7);
   const float inv32 = __double2float_rn(inv64);
   const bool wide = inv64 < 0x1p-100;
-  for (uint32_t c = blockIdx.x * blockDim.x + threadIdx.x; c < nchunks; c += gridDim.x * blockDim.x) {
-    const uint4 v = *reinterpret_cast<const uint4*>(chunk_ptr(g, c, cpr, ldg));
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
+  // two chunks per iteration, both loads issued before either is used
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t c0 = blockIdx.x * blockDim.x + threadIdx.x; c0 < nchunks; c0 += 2 * stride) {
+    const uint32_t c1 = c0 + stride;
+    const uint4 v0 = *reinterpret_cast<const uint4*>(chunk_ptr(g, c0, cpr, ldg));
+    uint4 v1 = make_uint4(0, 0, 0, 0);
+    if (c1 < nchunks) v1 = *reinterpret_cast<const uint4*>(chunk_ptr(g, c1, cpr, ldg));
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      o[j] = scaled_bf16(w[j] & 0xFFFFu, inv32, inv64, wide) | (scaled_bf16(w[j] >> 16, inv32, inv64, wide) << 16);
-    *reinterpret_cast<uint4*>(const_cast<uint16_t*>(chunk_ptr(x, c, cpr, ldx))) = make_uint4(o[0], o[1], o[2], o[3]);
-    if (HIST) hist_add8(sh_hist, o);
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t c = u ? c1 : c0;
+      if (c >= nchunks) break;
+      const uint4 v = u ? v1 : v0;
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        o[j] = scaled_bf16(w[j] & 0xFFFFu, inv32, inv64, wide) | (scaled_bf16(w[j] >> 16, inv32, inv64, wide) << 16);
+      *reinterpret_cast<uint4*>(const_cast<uint16_t*>(chunk_ptr(x, c, cpr, ldx))) = make_uint4(o[0], o[1], o[2], o[3]);
+      if (HIST) hist_add8(sh_hist, o);
+    }
   }
   if (HIST) hist_flush(sh_hist, hist);
 }
 
 // The k-th smallest magnitude pattern (k >= 1) from the histogram: one CTA of
-// 1024 threads, 32 bins each.  Writes the pattern to clip_out[0], its binary32
-// value to amax_out (the clipped tensor's max |x|), zeroes the histogram for its
-// next use and zeroes `zero_slot`.
+// 1024 threads; warp w owns bins [1024 w, 1024 w + 1024) and reads them in 32
+// coalesced rounds (round j, lane l: bin 1024 w + 32 j + l), so each round is a
+// run of 32 consecutive bins.  The warp totals are scanned across the CTA; the
+// warp whose range holds the k-th element then scans its rounds in order.
+// Writes the pattern to clip_out[0], its binary32 value to amax_out (the
+// clipped tensor's max |x|) and zeroes the histogram for its next use.
 __global__ void __launch_bounds__(1024) ns_select_kernel(uint32_t* __restrict__ hist, uint32_t k,
-                                                         uint32_t* __restrict__ clip_out, float* __restrict__ amax_out,
-                                                         unsigned int* __restrict__ zero_slot) {
-  constexpr int kPer = kHistBins / 1024;
-  __shared__ uint32_t warp_sum[32];
+                                                         uint32_t* __restrict__ clip_out, float* __restrict__ amax_out) {
+  constexpr int kRounds = kHistBins / 1024;
+  __shared__ uint32_t warp_excl[32];
   __shared__ uint32_t found;
   const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
-  uint32_t h[kPer];
-  uint32_t local = 0;
+  uint32_t* base = hist + wid * 1024 + lane;
+  uint32_t h[kRounds];
+  uint32_t wsum = 0;
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    h[i] = hist[t * kPer + i];
-    local += h[i];
+  for (int j = 0; j < kRounds; ++j) {
+    h[j] = base[32 * j];
+    wsum += h[j];
   }
-  // inclusive scan of `local` over the block (counts fit: at most 2^32 - 1 elements)
-  uint32_t incl = local;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += n;
-  }
-  if (lane == 31) warp_sum[wid] = incl;
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, o);  // counts < 2^32
+  if (lane == 0) warp_excl[wid] = wsum;
   if (t == 0) found = 0xFFFFFFFFu;
   __syncthreads();
   if (wid == 0) {
-    uint32_t ws = warp_sum[lane], wincl = ws;
+    const uint32_t mine = warp_excl[lane];
+    uint32_t incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t n = __shfl_up_sync(0xFFFFFFFFu, wincl, o);
-      if (lane >= o) wincl += n;
+      const uint32_t n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += n;
     }
-    warp_sum[lane] = wincl - ws;  // exclusive prefix of the warps
+    warp_excl[lane] = incl - mine;
   }
   __syncthreads();
-  incl += warp_sum[wid];
-  const uint32_t excl = incl - local;
-  if (excl < k && k <= incl) {  // exactly one thread
+  const uint32_t excl = warp_excl[wid];
+  if (excl < k && k - excl <= wsum) {  // exactly one warp (uniform branch)
     uint32_t run = excl;
-    for (int i = 0; i < kPer; ++i) {
-      run += h[i];
-      if (run >= k) {
-        found = static_cast<uint32_t>(t * kPer + i);
+#pragma unroll
+    for (int j = 0; j < kRounds; ++j) {
+      uint32_t incl = h[j];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      const uint32_t hit = __ballot_sync(0xFFFFFFFFu, run + incl >= k);
+      if (hit) {
+        if (lane == 0) found = static_cast<uint32_t>(wid * 1024 + 32 * j + __ffs(hit) - 1);
         break;
       }
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
   }
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) hist[t * kPer + i] = 0;
+  for (int j = 0; j < kRounds; ++j) base[32 * j] = 0;
   __syncthreads();
   if (t == 0) {
     const uint32_t v = found == 0xFFFFFFFFu ? 0x7FFFu : found;
     clip_out[0] = v;
     *amax_out = __uint_as_float(v << 16);
-    if (zero_slot) *zero_slot = 0;
   }
 }
 
-// x <- sign(x) * min(|x|, v) in place; only 16-byte chunks with a clipped
-// element are written back.
-__global__ void __launch_bounds__(kNsThreads) ns_clip_kernel(uint16_t* __restrict__ x, int64_t ld, uint32_t cpr,
-                                                             uint32_t nchunks, const uint32_t* __restrict__ clip) {
-  const uint32_t v = *clip;
-  const uint32_t v2 = v | (v << 16);
-  for (uint32_t c = blockIdx.x * blockDim.x + threadIdx.x; c < nchunks; c += gridDim.x * blockDim.x) {
-    uint4* p = reinterpret_cast<uint4*>(const_cast<uint16_t*>(chunk_ptr(x, c, cpr, ld)));
-    const uint4 in = *p;
-    uint32_t w[4] = {in.x, in.y, in.z, in.w};
-    bool any = false;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t mag = w[j] & 0x7FFF7FFFu;
-      const uint32_t m = __vminu2(mag, v2);
-      any |= m != mag;
-      w[j] = (w[j] & 0x80008000u) | m;
-    }
-    if (any) *p = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
-// out = bf16(fl32(p x) + fl32(q y)) (no contraction); without y: bf16(fl32(p x)).
+// out = bf16(fl32(p x') + fl32(q y)) (no contraction); without y: bf16(fl32(p x')),
+// where x' is x with |x| clipped to *clip_x (when given).
 // EPI 1: max |out| into *amax (float bits, the slot zeroed beforehand);
 // EPI 2: |out| histogram into `hist`.  out may alias x or y (same index only).
 template <bool HAS_Y, int EPI>
-__global__ void __launch_bounds__(kNsThreads) ns_lincomb_kernel(const uint16_t* x, int64_t ldx, float p,
+__global__ void __launch_bounds__(EPI == 2 ? kNsHistThreads : kNsThreads) ns_lincomb_kernel(const uint16_t* x, int64_t ldx, float p,
                                                                 const uint16_t* y, int64_t ldy, float q, uint16_t* out,
                                                                 int64_t ldo, uint32_t cpr, uint32_t nchunks,
+                                                                const uint32_t* __restrict__ clip_x,
                                                                 unsigned int* __restrict__ amax,
                                                                 uint32_t* __restrict__ hist) {
   extern __shared__ uint32_t sh_hist[];
   if (EPI == 2) hist_zero(sh_hist);
+  // min with 0x7FFF leaves every magnitude pattern as it is
+  const uint32_t clip2 = clip_x ? *clip_x * 0x10001u : 0x7FFF7FFFu;
   uint32_t m2 = 0;
-  for (uint32_t c = blockIdx.x * blockDim.x + threadIdx.x; c < nchunks; c += gridDim.x * blockDim.x) {
-    const uint4 vx = *reinterpret_cast<const uint4*>(chunk_ptr(x, c, cpr, ldx));
-    uint4 vy = make_uint4(0, 0, 0, 0);
-    if (HAS_Y) vy = *reinterpret_cast<const uint4*>(chunk_ptr(y, c, cpr, ldy));
-    const uint32_t wx[4] = {vx.x, vx.y, vx.z, vx.w};
-    const uint32_t wy[4] = {vy.x, vy.y, vy.z, vy.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float lo = __fmul_rn(p, bf16_lo(wx[j]));
-      float hi = __fmul_rn(p, bf16_hi(wx[j]));
-      if (HAS_Y) {
-        lo = __fadd_rn(lo, __fmul_rn(q, bf16_lo(wy[j])));
-        hi = __fadd_rn(hi, __fmul_rn(q, bf16_hi(wy[j])));
-      }
-      o[j] = bf16_rn(lo) | (bf16_rn(hi) << 16);
-      if (EPI == 1) m2 = __vmaxu2(m2, o[j] & 0x7FFF7FFFu);
+  // two chunks per iteration, all loads issued before any is used
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t c0 = blockIdx.x * blockDim.x + threadIdx.x; c0 < nchunks; c0 += 2 * stride) {
+    const uint32_t c1 = c0 + stride;
+    const bool two = c1 < nchunks;
+    uint4 vx[2], vy[2];
+    vx[0] = *reinterpret_cast<const uint4*>(chunk_ptr(x, c0, cpr, ldx));
+    vx[1] = two ? *reinterpret_cast<const uint4*>(chunk_ptr(x, c1, cpr, ldx)) : make_uint4(0, 0, 0, 0);
+    vy[0] = vy[1] = make_uint4(0, 0, 0, 0);
+    if (HAS_Y) {
+      vy[0] = *reinterpret_cast<const uint4*>(chunk_ptr(y, c0, cpr, ldy));
+      if (two) vy[1] = *reinterpret_cast<const uint4*>(chunk_ptr(y, c1, cpr, ldy));
     }
-    *reinterpret_cast<uint4*>(const_cast<uint16_t*>(chunk_ptr(out, c, cpr, ldo))) = make_uint4(o[0], o[1], o[2], o[3]);
-    if (EPI == 2) hist_add8(sh_hist, o);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (u == 1 && !two) break;
+      uint32_t wx[4] = {vx[u].x, vx[u].y, vx[u].z, vx[u].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) wx[j] = (wx[j] & 0x80008000u) | __vminu2(wx[j] & 0x7FFF7FFFu, clip2);
+      const uint32_t wy[4] = {vy[u].x, vy[u].y, vy[u].z, vy[u].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float lo = __fmul_rn(p, bf16_lo(wx[j]));
+        float hi = __fmul_rn(p, bf16_hi(wx[j]));
+        if (HAS_Y) {
+          lo = __fadd_rn(lo, __fmul_rn(q, bf16_lo(wy[j])));
+          hi = __fadd_rn(hi, __fmul_rn(q, bf16_hi(wy[j])));
+        }
+        o[j] = bf16_rn(lo) | (bf16_rn(hi) << 16);
+        if (EPI == 1) m2 = __vmaxu2(m2, o[j] & 0x7FFF7FFFu);
+      }
+      *reinterpret_cast<uint4*>(const_cast<uint16_t*>(chunk_ptr(out, u ? c1 : c0, cpr, ldo))) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+      if (EPI == 2) hist_add8(sh_hist, o);
+    }
   }
   if (EPI == 1) {
     uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
@@ -330,7 +348,7 @@ cudaError_t launch_ns_normalize(const void* G, int64_t rows, int64_t cols, int64
   if (hist) {
     static cudaError_t attr = hist_attr(reinterpret_cast<const void*>(ns_normalize_kernel<true>));
     if (attr != cudaSuccess) return attr;
-    ns_normalize_kernel<true><<<ns_grid(nchunks, num_sms, 1), kNsThreads, kHistSmem, s>>>(
+    ns_normalize_kernel<true><<<num_sms, kNsHistThreads, kHistSmem, s>>>(
         static_cast<const uint16_t*>(G), ldg, static_cast<uint16_t*>(X), ldx, cpr, nchunks, partial, nb, hist);
   } else {
     ns_normalize_kernel<false><<<ns_grid(nchunks, num_sms, 4), kNsThreads, 0, s>>>(
@@ -340,24 +358,15 @@ cudaError_t launch_ns_normalize(const void* G, int64_t rows, int64_t cols, int64
   return cudaGetLastError();
 }
 
-cudaError_t launch_ns_select_clip(uint32_t* hist, uint32_t k, void* X, int64_t rows, int64_t cols, int64_t ldx,
-                                  uint32_t* clip_slot, float* amax_out, unsigned int* zero_slot, int num_sms,
-                                  cudaStream_t s) {
-  ns_select_kernel<<<1, 1024, 0, s>>>(hist, k, clip_slot, amax_out, zero_slot);
-  count_launch();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const uint32_t cpr = static_cast<uint32_t>(cols / 8);
-  const uint32_t nchunks = static_cast<uint32_t>(rows) * cpr;
-  ns_clip_kernel<<<ns_grid(nchunks, num_sms, 4), kNsThreads, 0, s>>>(static_cast<uint16_t*>(X), ldx, cpr, nchunks,
-                                                                     clip_slot);
+cudaError_t launch_ns_select(uint32_t* hist, uint32_t k, uint32_t* clip_slot, float* amax_out, cudaStream_t s) {
+  ns_select_kernel<<<1, 1024, 0, s>>>(hist, k, clip_slot, amax_out);
   count_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_ns_lincomb(const void* x, int64_t ldx, float p, const void* y, int64_t ldy, float q, void* out,
-                              int64_t ldo, int64_t rows, int64_t cols, float* amax_out, uint32_t* hist, int num_sms,
-                              cudaStream_t s) {
+                              int64_t ldo, int64_t rows, int64_t cols, const uint32_t* clip_x, float* amax_out,
+                              uint32_t* hist, int num_sms, cudaStream_t s) {
   const uint32_t cpr = static_cast<uint32_t>(cols / 8);
   const uint32_t nchunks = static_cast<uint32_t>(rows) * cpr;
   const uint16_t* xx = static_cast<const uint16_t*>(x);
@@ -368,32 +377,30 @@ cudaError_t launch_ns_lincomb(const void* x, int64_t ldx, float p, const void* y
     cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), s);
     if (e != cudaSuccess) return e;
   }
-  const int g4 = ns_grid(nchunks, num_sms, 4), g1 = ns_grid(nchunks, num_sms, 1);
+  const int g4 = ns_grid(nchunks, num_sms, 4), g1 = num_sms;  // the histogram kernels: one CTA per SM
+#define NS_LINCOMB_ARGS xx, ldx, p, yy, ldy, q, oo, ldo, cpr, nchunks, clip_x
   if (hist) {
     if (y) {
       static cudaError_t attr = hist_attr(reinterpret_cast<const void*>(ns_lincomb_kernel<true, 2>));
       if (attr != cudaSuccess) return attr;
-      ns_lincomb_kernel<true, 2><<<g1, kNsThreads, kHistSmem, s>>>(xx, ldx, p, yy, ldy, q, oo, ldo, cpr, nchunks,
-                                                                   nullptr, hist);
+      ns_lincomb_kernel<true, 2><<<g1, kNsHistThreads, kHistSmem, s>>>(NS_LINCOMB_ARGS, nullptr, hist);
     } else {
       static cudaError_t attr = hist_attr(reinterpret_cast<const void*>(ns_lincomb_kernel<false, 2>));
       if (attr != cudaSuccess) return attr;
-      ns_lincomb_kernel<false, 2><<<g1, kNsThreads, kHistSmem, s>>>(xx, ldx, p, yy, ldy, q, oo, ldo, cpr, nchunks,
-                                                                    nullptr, hist);
+      ns_lincomb_kernel<false, 2><<<g1, kNsHistThreads, kHistSmem, s>>>(NS_LINCOMB_ARGS, nullptr, hist);
     }
   } else if (amax_out) {
     if (y)
-      ns_lincomb_kernel<true, 1><<<g4, kNsThreads, 0, s>>>(xx, ldx, p, yy, ldy, q, oo, ldo, cpr, nchunks, am, nullptr);
+      ns_lincomb_kernel<true, 1><<<g4, kNsThreads, 0, s>>>(NS_LINCOMB_ARGS, am, nullptr);
     else
-      ns_lincomb_kernel<false, 1><<<g4, kNsThreads, 0, s>>>(xx, ldx, p, yy, ldy, q, oo, ldo, cpr, nchunks, am, nullptr);
+      ns_lincomb_kernel<false, 1><<<g4, kNsThreads, 0, s>>>(NS_LINCOMB_ARGS, am, nullptr);
   } else {
     if (y)
-      ns_lincomb_kernel<true, 0><<<g4, kNsThreads, 0, s>>>(xx, ldx, p, yy, ldy, q, oo, ldo, cpr, nchunks, nullptr,
-                                                          nullptr);
+      ns_lincomb_kernel<true, 0><<<g4, kNsThreads, 0, s>>>(NS_LINCOMB_ARGS, nullptr, nullptr);
     else
-      ns_lincomb_kernel<false, 0><<<g4, kNsThreads, 0, s>>>(xx, ldx, p, yy, ldy, q, oo, ldo, cpr, nchunks, nullptr,
-                                                           nullptr);
+      ns_lincomb_kernel<false, 0><<<g4, kNsThreads, 0, s>>>(NS_LINCOMB_ARGS, nullptr, nullptr);
   }
+#undef NS_LINCOMB_ARGS
   count_launch();
   return cudaGetLastError();
 }

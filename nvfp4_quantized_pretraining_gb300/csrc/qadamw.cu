@@ -42,12 +42,17 @@ __device__ __forceinline__ void wht16(float (&x)[16]) {
   }
 }
 
-// h (16 values) and the BF16 mean pattern of one block of v.
-__device__ __forceinline__ uint32_t vt_forward(const float* __restrict__ v, float (&h)[16]) {
+__device__ __forceinline__ void load_block(const float* __restrict__ v, float4 (&f)[4]) {
   const float4* p = reinterpret_cast<const float4*>(v);
 #pragma unroll
+  for (int q = 0; q < 4; ++q) f[q] = __ldcs(p + q);
+}
+
+// h (16 values) and the BF16 mean pattern of one block of v (loaded into f).
+__device__ __forceinline__ uint32_t vt_forward(const float4 (&fv)[4], float (&h)[16]) {
+#pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const float4 f = __ldcs(p + q);
+    const float4 f = fv[q];
     h[4 * q + 0] = __fsqrt_rn(f.x);
     h[4 * q + 1] = __fsqrt_rn(f.y);
     h[4 * q + 2] = __fsqrt_rn(f.z);
@@ -79,11 +84,20 @@ __device__ __forceinline__ const float* block_src(const float* v, uint32_t b, ui
 __global__ void __launch_bounds__(kVtThreads) vt_amax_kernel(const float* __restrict__ v, int64_t ldv, uint32_t kbpr,
                                                              uint32_t nblocks, unsigned int* __restrict__ amax) {
   uint32_t m = 0;
-  for (uint32_t b = blockIdx.x * blockDim.x + threadIdx.x; b < nblocks; b += gridDim.x * blockDim.x) {
+  // the next block's loads are issued before the current block's arithmetic
+  const uint32_t stride = gridDim.x * blockDim.x;
+  uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+  float4 cur[4];
+  if (b < nblocks) load_block(block_src(v, b, kbpr, ldv), cur);
+  for (; b < nblocks; b += stride) {
+    float4 nxt[4];
+    if (b + stride < nblocks) load_block(block_src(v, b + stride, kbpr, ldv), nxt);
     float h[16];
-    vt_forward(block_src(v, b, kbpr, ldv), h);
+    vt_forward(cur, h);
 #pragma unroll
     for (int i = 0; i < 16; ++i) m = max(m, __float_as_uint(h[i]) & 0x7FFFFFFFu);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
@@ -104,9 +118,17 @@ __global__ void __launch_bounds__(kVtThreads) vt_encode_kernel(const float* __re
     scale_out[0] = S_t;
     scale_out[1] = a;
   }
-  for (uint32_t b = blockIdx.x * blockDim.x + threadIdx.x; b < nblocks; b += gridDim.x * blockDim.x) {
+  const uint32_t stride = gridDim.x * blockDim.x;
+  uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+  float4 cur[4];
+  if (b < nblocks) load_block(block_src(v, b, kbpr, ldv), cur);
+  for (; b < nblocks; b += stride) {
+    float4 nxt[4];
+    if (b + stride < nblocks) load_block(block_src(v, b + stride, kbpr, ldv), nxt);
     float h[16];
-    const uint32_t mean = vt_forward(block_src(v, b, kbpr, ldv), h);
+    const uint32_t mean = vt_forward(cur, h);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
     float amax_b = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) amax_b = fmaxf(amax_b, fabsf(h[i]));

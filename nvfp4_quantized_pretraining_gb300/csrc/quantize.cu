@@ -92,12 +92,13 @@ struct DualQuantArgs {
   uint32_t atoms_k_c;
   uint64_t seed;
   uint32_t stream_r, stream_c;
+  const uint32_t* clip;  // CLIP: |x| is clipped to this BF16 magnitude pattern as the tile is staged
 };
 
 constexpr int kTileR = 128, kTileC = 128;
 constexpr int kDualThreads = 256;
 
-template <bool ROW, bool COL, bool SR>
+template <bool ROW, bool COL, bool SR, bool CLIP = false>
 __global__ void __launch_bounds__(kDualThreads, SR ? 3 : 5) quantize_dual_kernel(const DualQuantArgs a) {
   extern __shared__ __align__(16) uint8_t dsm[];
   uint16_t(*tile)[kTileC] = reinterpret_cast<uint16_t(*)[kTileC]>(dsm);
@@ -128,6 +129,13 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 3 : 5) quantize_dual_kernel
   for (int i = 0; i < kLoads; ++i) {
     const int q = tid + i * kDualThreads;
     const uint32_t row = r0 + (q >> 4), c8 = (c0 >> 3) + (q & 15);
+    if (CLIP) {
+      const uint32_t v2 = *a.clip * 0x10001u;
+      w[i].x = (w[i].x & 0x80008000u) | __vminu2(w[i].x & 0x7FFF7FFFu, v2);
+      w[i].y = (w[i].y & 0x80008000u) | __vminu2(w[i].y & 0x7FFF7FFFu, v2);
+      w[i].z = (w[i].z & 0x80008000u) | __vminu2(w[i].z & 0x7FFF7FFFu, v2);
+      w[i].w = (w[i].w & 0x80008000u) | __vminu2(w[i].w & 0x7FFF7FFFu, v2);
+    }
     *reinterpret_cast<uint4*>(&tile[q >> 4][(q & 15) * 8]) = w[i];
     if (COL && SR) {
       // element e of the chunk takes word e/2, low half for even e: in element order
@@ -326,8 +334,9 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, f
 
 cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
                                  uint32_t stream_r, uint32_t stream_c, const float* amax, const QOut* row_out,
-                                 const QOut* col_out, cudaStream_t s) {
+                                 const QOut* col_out, cudaStream_t s, const uint32_t* clip) {
   DualQuantArgs a{};
+  a.clip = clip;
   a.x = static_cast<const uint16_t*>(x);
   a.ld = ld;
   a.rows = static_cast<uint32_t>(rows);
@@ -363,7 +372,10 @@ cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int6
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kTileR * kTileC * 2);
   });
   if (attr != cudaSuccess) return attr;
-  if (R && C) {
+  if (clip) {  // the clipped form: both orientations, RTN
+    if (!(R && C) || sr) return cudaErrorInvalidValue;
+    quantize_dual_kernel<true, true, false, true><<<grid, kDualThreads, smem, s>>>(a);
+  } else if (R && C) {
     if (sr) quantize_dual_kernel<true, true, true><<<grid, kDualThreads, smem, s>>>(a);
     else quantize_dual_kernel<true, true, false><<<grid, kDualThreads, smem, s>>>(a);
   } else if (C) {
