@@ -27,6 +27,12 @@ dequantized operands.  Functions and the passages they follow:
   the BF16 factors (the same rounded P and P' the forward and dX products use),
   FP64 products, FP32 results; the Cholesky-QR constraint on the subspace is not
   specified on the pages and is not applied here.
+- ``cholesky_lower`` / ``lora_cholqr``: the Cholesky-QR step of the LoRA-SVD
+  backward (section 2.1: the backward pass is restricted to the subspace under a
+  Cholesky-QR constraint).  READING (no formula on the pages): the rows of L1
+  are re-orthonormalised through the Cholesky factor of their Gram matrix,
+  L1 L1^T = L L^T, L1 <- L^-1 L1, and L2 <- L2 L keeps beta L2 L1 unchanged;
+  FP64, each factor rounded to BF16 once.
 - ``p99_clip`` / ``ns_normalize`` / ``ns_step`` / ``newton_schulz``: Q-Root,
   Newton-Schulz iterations with every matrix product in NVFP4 (section 2.3, NVFP4
   Root optimizer: direct NVFP4 execution; shape-dependent coefficients a, b, c and
@@ -435,6 +441,47 @@ def lora_factor_grads_bf16(dY_bf16, X_bf16, L1_bf16, L2_bf16, beta: float = 1.0)
     f64 = lambda u: bf16_to_f32(u).astype(np.float64)
     dL1, dL2 = lora_factor_grads(f64(dY_bf16), f64(X_bf16), f64(P), f64(P2), beta)
     return dL1, dL2, P, P2
+
+
+# ---------------------------------------------------------------------------
+# Cholesky-QR of the LoRA-SVD factors (section 2.1)
+# ---------------------------------------------------------------------------
+
+def cholesky_lower(G: np.ndarray):
+    """Cholesky-Banachiewicz, row by row, FP64: G = L L^T with L lower triangular and a
+    positive diagonal.  Returns (L, info): info = 0, or j >= 1 when the leading minor of
+    order j is not positive definite (L is then only filled up to row j - 1)."""
+    G = np.asarray(G, dtype=np.float64)
+    r = G.shape[0]
+    L = np.zeros_like(G)
+    for i in range(r):
+        for j in range(i + 1):
+            s = G[i, j] - float(np.dot(L[i, :j], L[j, :j]))
+            if i == j:
+                if not s > 0.0:
+                    return L, i + 1
+                L[i, i] = np.sqrt(s)
+            else:
+                L[i, j] = s / L[j, j]
+    return L, 0
+
+
+def lora_cholqr_f64(L1_bf16: np.ndarray, L2_bf16: np.ndarray):
+    """(L1', L2', info) in FP64: L1 L1^T = L L^T, L1' = L^-1 L1, L2' = L2 L."""
+    l1 = bf16_to_f32(L1_bf16).astype(np.float64)
+    l2 = bf16_to_f32(L2_bf16).astype(np.float64)
+    L, info = cholesky_lower(l1 @ l1.T)
+    if info:
+        return None, None, info
+    return np.linalg.solve(L, l1), l2 @ L, 0
+
+
+def lora_cholqr(L1_bf16: np.ndarray, L2_bf16: np.ndarray):
+    """BF16 (L1', L2', info); L1: r x K, L2: N x r (bit patterns)."""
+    a, b, info = lora_cholqr_f64(L1_bf16, L2_bf16)
+    if info:
+        return None, None, info
+    return bf16_rn(a), bf16_rn(b), 0
 
 
 # ---------------------------------------------------------------------------

@@ -529,3 +529,51 @@ def test_vt_codec_lowers_the_error_of_plain_nvfp4(oracle_mod):
     sqrt_only = r(oracle_mod.quantize_f32(np.sqrt(v)).dequantize() ** 2)
     assert codec < 0.4 * plain
     assert codec < sqrt_only < plain
+
+
+# ---------------------------------------------------------------------------
+# Cholesky-QR of the LoRA-SVD factors
+# ---------------------------------------------------------------------------
+
+def test_cholesky_lower_matches_library_and_reports_the_failing_minor(oracle_mod):
+    rng = np.random.default_rng(12)
+    A = rng.standard_normal((24, 40))
+    G = A @ A.T
+    L, info = oracle_mod.cholesky_lower(G)
+    assert info == 0
+    assert np.allclose(L, np.linalg.cholesky(G), rtol=0, atol=1e-12 * np.abs(G).max())
+    # exact small cases: the second pivot is 1 - 1 = 0 (singular) or 1 - 4 < 0 (indefinite)
+    assert oracle_mod.cholesky_lower(np.array([[4.0, 2, 0], [2, 1, 0], [0, 0, 1]]))[1] == 2
+    assert oracle_mod.cholesky_lower(np.array([[1.0, 2], [2, 1]]))[1] == 2
+    assert oracle_mod.cholesky_lower(-np.eye(3))[1] == 1
+
+
+def test_lora_cholqr_equals_householder_qr(oracle_mod):
+    # L1^T = Q R (Householder, numpy); with the signs of R's diagonal made positive the
+    # Q factor is unique, so the Cholesky-QR rows must equal Q^T
+    from nvfp4_quantized_pretraining_gb300 import synthetic as S
+    r, K, N = 16, 96, 48
+    L1 = S.normal((r, K), 0.3, 13)
+    L2 = S.normal((N, r), 0.1, 14)
+    a, b, info = oracle_mod.lora_cholqr_f64(L1, L2)
+    assert info == 0
+    l1 = oracle_mod.bf16_to_f32(L1).astype(np.float64)
+    l2 = oracle_mod.bf16_to_f32(L2).astype(np.float64)
+    Q, R = np.linalg.qr(l1.T)
+    D = np.sign(np.diag(R))
+    assert np.allclose(a, (Q * D).T, atol=1e-10)
+    assert np.allclose(a @ a.T, np.eye(r), atol=1e-12)
+    assert np.allclose(b @ a, l2 @ l1, atol=1e-12)            # beta L2 L1 unchanged
+    assert np.allclose(b, l2 @ (R.T * D), atol=1e-10)          # L = R^T with the signs fixed
+
+
+def test_lora_cholqr_rank_one_closed_form(oracle_mod):
+    from nvfp4_quantized_pretraining_gb300 import synthetic as S
+    L1 = S.normal((1, 64), 1.0, 15)
+    L2 = S.normal((32, 1), 1.0, 16)
+    a, b, info = oracle_mod.lora_cholqr_f64(L1, L2)
+    l1 = oracle_mod.bf16_to_f32(L1).astype(np.float64)
+    n = np.linalg.norm(l1)
+    assert info == 0
+    assert np.allclose(a, l1 / n, atol=1e-15)
+    assert np.allclose(b, oracle_mod.bf16_to_f32(L2).astype(np.float64) * n, atol=1e-12)
