@@ -252,6 +252,7 @@ def run_ours(args):
     # ---- kernel breakdown through the public calls (same operands), for the roofline
     bd = breakdown(F, torch, projs, T, r, stream, dev, flush, args)
     lg = lora_grads(F, torch, projs, T, r, stream, dev, flush, args) if r else None
+    cq = lora_cholqr(F, torch, projs, r, stream, dev, flush, args) if r else None
     ns = newton_schulz(F, torch, S, stream, dev, flush, args)
     vt = qadamw_codec(F, torch, projs, stream, dev, flush, args)
 
@@ -284,6 +285,7 @@ def run_ours(args):
                              "written per element) over their event time"},
         "breakdown_ms": {k: round(v, 4) for k, v in bd["per_kind_ms"].items()},
         "lora_factor_grads": lg,
+        "lora_cholqr": cq,
         "newton_schulz": ns,
         "qadamw_v_codec": vt,
         "branch_tflops_counted_separately": round(branch_flops / 1e12, 4),
@@ -409,6 +411,37 @@ def lora_grads(F, torch, projs, T, r, stream, dev, flush, args):
             "unit": "GB/s", "frac": round(gbs / hbm, 4),
             "note": "dL2 = dY^T P and dL1 = P'^T X of the four projections; algorithmic bytes "
                     "(BF16 dY or X, the T x r factor, the FP32 result) over the summed median call times"}
+
+
+def lora_cholqr(F, torch, projs, r, stream, dev, flush, args):
+    """Times the Cholesky-QR step of each projection's LoRA factors (L1 r x K, L2 N x r),
+    out of place, each call after an L2 flush.  Not part of the timed step.  It moves
+    only the factors (a few MB), so it is latency-bound: three short launches."""
+    reps = max(1, min(args.steps, 5))
+    total = 0.0
+    with torch.cuda.stream(stream):
+        for p in projs:
+            o1, o2 = torch.empty_like(p["L1"]), torch.empty_like(p["L2"])
+            info = torch.zeros(1, dtype=torch.int32, device=dev)
+            ws = torch.empty(F.lib().fp4_lora_cholqr_workspace(p["K"], r), dtype=torch.uint8, device=dev)
+            fn = lambda: F.fp4_lora_cholqr(p["L1"], p["L2"], L1_out=o1, L2_out=o2, info=info, workspace=ws,
+                                           stream=stream)
+            fn()
+            ts = []
+            for _ in range(reps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            total += sorted(ts)[len(ts) // 2]
+            if int(info.item()) != 0:
+                raise RuntimeError(f"Cholesky-QR of {p['name']}: info = {int(info.item())}")
+    F.fp4_check_status(stream)
+    return {"ms_per_step": round(total, 4), "bound": "latency",
+            "note": "L1 <- L^-1 L1, L2 <- L2 L of the four projections (r = 64), summed median call times"}
 
 
 def run_part(args, F, torch, S, dev):

@@ -214,6 +214,23 @@ fp4_status fp4_lora_factor_grad(const void* A, int64_t T, int64_t M, int64_t lda
                                 const void* B, int r, float beta, float* C, int64_t ldc,
                                 int transpose_c, void* ws, size_t ws_bytes, void* stream);
 
+/* Cholesky-QR step of the LoRA-SVD branch (section 2.1: the backward pass is
+ * restricted to the subspace under a Cholesky-QR constraint; no formula on the
+ * pages).  Reading: the rows of L1 are re-orthonormalised through the Cholesky
+ * factor of their Gram matrix and L2 takes the factor, so beta L2 L1 is kept:
+ *   L1 L1^T = L L^T,   L1_out = bf16(L^-1 L1),   L2_out = bf16(L2 L).
+ * FP32 arithmetic (Gram partials over 128-column chunks added in a fixed order).
+ * L1: r x K BF16, row pitch ld1 elements; L2: N x r BF16, pitch r; the outputs
+ * have the same layouts and may be the inputs (in-place update).  All 16-byte
+ * aligned.  r in {16, 32, 48, 64}.  info (device int): 0 on success, else j >= 1
+ * when the leading minor of order j of L1 L1^T is not positive definite, and
+ * then the outputs are not written.  ws: fp4_lora_cholqr_workspace(K, r) bytes,
+ * 256-byte aligned. */
+size_t fp4_lora_cholqr_workspace(int64_t K, int r);
+fp4_status fp4_lora_cholqr(const void* L1, int64_t K, int64_t ld1, const void* L2, int64_t N,
+                           int r, void* L1_out, void* L2_out, int* info, void* ws,
+                           size_t ws_bytes, void* stream);
+
 /* Q-Root orthogonalisation: Newton-Schulz iterations with every matrix product
  * in NVFP4 (section 2.3, NVFP4 Root optimizer: direct NVFP4 execution, shape-
  * dependent coefficients a, b, c, p99 outlier clipping; the pages print neither

@@ -34,7 +34,7 @@ OUT_F32 = 1
 EXPORTS = ["fp4_scale_bytes", "fp4_amax", "fp4_quantize", "fp4_quantize_transposed", "fp4_quantize_dual",
            "fp4_gemm_blockscaled", "fp4_branch_factor", "fp4_linear_fwd_workspace", "fp4_linear_bwd_workspace",
            "fp4_linear_fwd", "fp4_linear_fwd_noalloc", "fp4_linear_bwd", "fp4_lora_factor_grad_workspace",
-           "fp4_lora_factor_grad", "fp4_newton_schulz_workspace", "fp4_newton_schulz", "fp4_qadamw_v_encode",
+           "fp4_lora_factor_grad", "fp4_lora_cholqr_workspace", "fp4_lora_cholqr", "fp4_newton_schulz_workspace", "fp4_newton_schulz", "fp4_qadamw_v_encode",
            "fp4_qadamw_v_decode", "fp4_check_status", "fp4_last_error", "fp4_launch_count",
            "fp4_debug_convert", "fp4_debug_sr_round", "fp4_mma_peak_probe"]
 
@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
                                  ctypes.c_size_t, P]),
         "fp4_lora_factor_grad_workspace": (ctypes.c_size_t, [i64, i64, i32]),
         "fp4_lora_factor_grad": (i32, [P, i64, i64, i64, P, i32, f32, P, i64, i32, P, ctypes.c_size_t, P]),
+        "fp4_lora_cholqr_workspace": (ctypes.c_size_t, [i64, i32]),
+        "fp4_lora_cholqr": (i32, [P, i64, i64, P, i64, i32, P, P, P, P, ctypes.c_size_t, P]),
         "fp4_newton_schulz_workspace": (ctypes.c_size_t, [i64, i64, f32]),
         "fp4_newton_schulz": (i32, [P, i64, i64, i64, i32, i32, f32, f32, f32, i32, P, i64, P, ctypes.c_size_t,
                                     P]),
@@ -289,6 +291,27 @@ def lora_factor_grads(X, dY, P, P2, beta: float = 1.0, stream=None):
     dL2 = fp4_lora_factor_grad(dY, P, beta, stream=stream)
     dL1 = fp4_lora_factor_grad(X, P2, beta, transpose=True, stream=stream)
     return dL1, dL2
+
+
+def fp4_lora_cholqr(L1: torch.Tensor, L2: torch.Tensor, L1_out=None, L2_out=None, info=None, workspace=None,
+                    stream=None):
+    """Cholesky-QR of the LoRA-SVD factors: L1 (r x K) <- L^-1 L1, L2 (N x r) <- L2 L with
+    L1 L1^T = L L^T (beta L2 L1 unchanged).  Pass L1_out=L1, L2_out=L2 to update in place.
+    Returns (L1_out, L2_out, info); info (device int32) is 0 or the order of the first
+    non-positive-definite leading minor, in which case the outputs are not written."""
+    r, K, ld1 = _bf16_2d(L1, "L1")
+    N = L2.shape[0]
+    assert L2.dtype == torch.bfloat16 and L2.is_contiguous() and L2.shape[1] == r
+    if L1_out is None:  # the C ABI writes L1_out with L1's row pitch
+        L1_out = torch.empty((r, ld1), dtype=torch.bfloat16, device=L1.device)[:, :K]
+    L2_out = torch.empty_like(L2) if L2_out is None else L2_out
+    assert L1_out.stride(0) == ld1
+    info = torch.zeros(1, dtype=torch.int32, device=L1.device) if info is None else info
+    need = lib().fp4_lora_cholqr_workspace(K, r)
+    workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=L1.device) if workspace is None else workspace
+    _check(lib().fp4_lora_cholqr(L1.data_ptr(), K, ld1, L2.data_ptr(), N, r, L1_out.data_ptr(), L2_out.data_ptr(),
+                                 info.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(stream)))
+    return L1_out, L2_out, info
 
 
 NS_COEFFS = (1.5, -0.5, 0.0)  # the cubic Newton-Schulz polynomial

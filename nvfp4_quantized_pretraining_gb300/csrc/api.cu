@@ -567,6 +567,27 @@ fp4_status fp4_newton_schulz(const void* G, int64_t m, int64_t n, int64_t ldg, i
   return FP4_OK;
 }
 
+size_t fp4_lora_cholqr_workspace(int64_t K, int r) {
+  if (K <= 0 || r <= 0) return 0;
+  return round256((static_cast<size_t>(cholqr_parts(K)) + 2) * static_cast<size_t>(r) * r * sizeof(float));
+}
+
+fp4_status fp4_lora_cholqr(const void* L1, int64_t K, int64_t ld1, const void* L2, int64_t N, int r, void* L1_out,
+                           void* L2_out, int* info, void* ws, size_t ws_bytes, void* stream) {
+  fp4_status st;
+  if (r != 16 && r != 32 && r != 48 && r != 64) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rank r=%d not in {16,32,48,64}", r);
+  if ((st = check_bf16_input(L1, r, K, ld1, "L1")) || (st = check_bf16_input(L2, N, r, r, "L2"))) return st;
+  if (!L1_out || !L2_out || !info) return fail(FP4_ERR_INVALID_ARG, "L1_out, L2_out and info must be non-NULL");
+  if (!aligned16(L1_out) || !aligned16(L2_out) || (reinterpret_cast<uintptr_t>(info) & 3u))
+    return fail(FP4_ERR_MISALIGNED, "L1_out and L2_out must be 16-byte aligned, info 4-byte aligned");
+  const size_t need = fp4_lora_cholqr_workspace(K, r);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return fail(FP4_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
+  CUDA_TRY(launch_lora_cholqr(L1, K, ld1, L2, N, r, L1_out, L2_out, info, static_cast<float*>(ws),
+                              static_cast<cudaStream_t>(stream)));
+  return FP4_OK;
+}
+
 static fp4_status check_f32_matrix(const float* p, int64_t rows, int64_t cols, int64_t ld, const char* name) {
   if (!p) return fail(FP4_ERR_INVALID_ARG, "%s is NULL", name);
   if (rows <= 0 || cols <= 0 || cols % 16 != 0)

@@ -83,6 +83,13 @@ cudaError_t launch_ns_lincomb(const void* x, int64_t ldx, float p, const void* y
                               int64_t ldo, int64_t rows, int64_t cols, const uint32_t* clip_x, float* amax_out,
                               uint32_t* hist, int num_sms, cudaStream_t s);
 
+// Cholesky-QR of the LoRA factors: L1 (r x K, pitch ld1) <- L^-1 L1 and L2 (N x r) <- L2 L with
+// L1 L1^T = L L^T; ws holds cholqr_parts(K) * r * r + 2 * r * r floats; *info (device) = 0 or the
+// order of the first non-positive-definite leading minor (then nothing is written).
+int cholqr_parts(int64_t K);
+cudaError_t launch_lora_cholqr(const void* L1, int64_t K, int64_t ld1, const void* L2, int64_t N, int r,
+                               void* L1_out, void* L2_out, int* info, float* ws, cudaStream_t s);
+
 // Q-AdamW second-moment codec: v (FP32 rows x cols, pitch ldv, cols % 16 == 0) to NVFP4
 // codes/scales/S_t (out; out.scale[1] receives the amax) and BF16 tile means (rows x cols/16);
 // and back to FP32 (pitch ldo).

@@ -1,0 +1,218 @@
+// Cholesky-QR step of the LoRA-SVD branch ("Full-Stack FP4", section 2.1: the
+// backward pass is restricted to the subspace under a Cholesky-QR constraint).
+// Reading: the rows of L1 (r x K) are re-orthonormalised through the Cholesky
+// factor of their Gram matrix, L1 L1^T = L L^T, L1 <- L^-1 L1, and L2 (N x r)
+// takes the factor, L2 <- L2 L, so beta L2 L1 is unchanged.
+//
+// Three launches, FP32 arithmetic (the BF16 products are exact in FP32):
+//   1. Gram partials: CTA s (of at most 32) sums the 128-column chunks s, s + 32,
+//      ... of L1 into an r x r FP32 partial;
+//   2. one CTA adds the partials in a fixed order, factors G = L L^T
+//      (right-looking, lower triangle) and reports a non-positive pivot in *info
+//      (LAPACK convention: the order of the failing leading minor);
+//   3. the update: one thread per column of L1 (forward substitution with L)
+//      and one per row of L2 (the row times L), BF16 results; nothing is written
+//      when *info != 0.  Each thread reads its whole column or row before writing
+//      it, so the update may be in place.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nvfp4 {
+
+constexpr int kCqrChunk = 128;   // columns of L1 per Gram step
+constexpr int kCqrMaxParts = 32; // Gram CTAs (partials)
+constexpr int kCqrThreads = 256;
+
+// r x r partial Gram matrix of the 128-column chunks blockIdx.x, blockIdx.x + gridDim.x, ...
+// Thread t owns row i = t / 4 and columns j = t % 4 + 4 u (u < r / 4) of the partial.
+template <int R>
+__global__ void __launch_bounds__(kCqrThreads) cholqr_gram_kernel(const uint16_t* __restrict__ L1, int64_t K,
+                                                                  int64_t ld, float* __restrict__ partial) {
+  __shared__ float tile[R][kCqrChunk + 1];
+  constexpr int kCols = R / 4;
+  const int i = threadIdx.x / 4, j0 = threadIdx.x % 4;
+  float acc[kCols];
+#pragma unroll
+  for (int u = 0; u < kCols; ++u) acc[u] = 0.0f;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kCqrChunk;
+  for (int64_t k0 = static_cast<int64_t>(blockIdx.x) * kCqrChunk; k0 < K; k0 += step) {
+    __syncthreads();  // the previous chunk's reads are done
+    for (int e = threadIdx.x; e < R * kCqrChunk; e += kCqrThreads) {
+      const int row = e / kCqrChunk, col = e % kCqrChunk;
+      const int64_t k = k0 + col;
+      tile[row][col] = k < K ? __uint_as_float(static_cast<uint32_t>(L1[row * ld + k]) << 16) : 0.0f;
+    }
+    __syncthreads();
+    if (i < R) {
+      for (int k = 0; k < kCqrChunk; ++k) {
+        const float a = tile[i][k];
+#pragma unroll
+        for (int u = 0; u < kCols; ++u) acc[u] = fmaf(a, tile[j0 + 4 * u][k], acc[u]);
+      }
+    }
+  }
+  if (i < R) {
+    float* out = partial + static_cast<int64_t>(blockIdx.x) * R * R + i * R;
+#pragma unroll
+    for (int u = 0; u < kCols; ++u) out[j0 + 4 * u] = acc[u];
+  }
+}
+
+// One CTA: G = sum of the partials (fixed order), G = L L^T.  Writes L (lower,
+// zeros above) and the reciprocals of its diagonal.
+template <int R>
+__global__ void __launch_bounds__(1024) cholqr_factor_kernel(const float* __restrict__ partial, int nparts,
+                                                             float* __restrict__ Lout, float* __restrict__ inv_diag,
+                                                             int* __restrict__ info) {
+  __shared__ float G[R][R + 1];
+  __shared__ int bad;
+  for (int e = threadIdx.x; e < R * R; e += blockDim.x) {
+    float v[kCqrMaxParts];
+#pragma unroll
+    for (int p = 0; p < kCqrMaxParts; ++p) v[p] = p < nparts ? partial[p * R * R + e] : 0.0f;
+    float s = 0.0f;
+#pragma unroll
+    for (int p = 0; p < kCqrMaxParts; ++p) s += v[p];
+    G[e / R][e % R] = s;
+  }
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  // right-looking factorisation in place (lower triangle of G becomes L)
+  for (int j = 0; j < R; ++j) {
+    if (threadIdx.x == 0) {
+      const float d = G[j][j];
+      if (!(d > 0.0f)) bad = j + 1;
+      else G[j][j] = sqrtf(d);
+    }
+    __syncthreads();
+    if (bad) break;
+    const float djj = G[j][j];
+    for (int i = j + 1 + threadIdx.x; i < R; i += blockDim.x) G[i][j] = G[i][j] / djj;
+    __syncthreads();
+    const int n = R - j - 1;  // trailing (n x n) lower triangle
+    for (int e = threadIdx.x; e < n * n; e += blockDim.x) {
+      const int i = j + 1 + e / n, k = j + 1 + e % n;
+      if (k <= i) G[i][k] -= G[i][j] * G[k][j];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *info = bad;
+  if (bad) return;  // uniform: every thread read `bad` after the same barrier
+  for (int e = threadIdx.x; e < R * R; e += blockDim.x) {
+    const int i = e / R, k = e % R;
+    Lout[e] = k <= i ? G[i][k] : 0.0f;
+  }
+  if (threadIdx.x < R) inv_diag[threadIdx.x] = 1.0f / G[threadIdx.x][threadIdx.x];
+}
+
+__device__ __forceinline__ uint32_t bf16_pattern(float v) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
+  return r;
+}
+
+// Blocks [0, ncolblocks): columns of L1 (L1' = L^-1 L1 by forward substitution);
+// the rest: rows of L2 (L2' = L2 L).
+template <int R>
+__global__ void __launch_bounds__(kCqrThreads) cholqr_apply_kernel(
+    const uint16_t* L1, int64_t K, int64_t ld1, uint16_t* L1_out, const uint16_t* L2, int64_t N, uint16_t* L2_out,
+    const float* __restrict__ Lmat, const float* __restrict__ inv_diag, const int* __restrict__ info,
+    int ncolblocks) {
+  __shared__ float M[R][R + 1];
+  __shared__ float dinv[R];
+  if (*info != 0) return;
+  for (int e = threadIdx.x; e < R * R; e += blockDim.x) M[e / R][e % R] = Lmat[e];
+  if (threadIdx.x < R) dinv[threadIdx.x] = inv_diag[threadIdx.x];
+  __syncthreads();
+  if (static_cast<int>(blockIdx.x) < ncolblocks) {
+    const int64_t k = static_cast<int64_t>(blockIdx.x) * kCqrThreads + threadIdx.x;
+    if (k >= K) return;
+    float x[R];
+#pragma unroll
+    for (int c = 0; c < R; ++c) x[c] = __uint_as_float(static_cast<uint32_t>(L1[c * ld1 + k]) << 16);
+    // x <- L^-1 x in place: x_i = (x_i - sum_{c < i} L_ic x_c) / L_ii
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      float s = x[i];
+#pragma unroll
+      for (int c = 0; c < i; ++c) s = fmaf(-M[i][c], x[c], s);
+      x[i] = s * dinv[i];
+      L1_out[i * ld1 + k] = static_cast<uint16_t>(bf16_pattern(x[i]));
+    }
+  } else {
+    const int64_t n = static_cast<int64_t>(blockIdx.x - ncolblocks) * kCqrThreads + threadIdx.x;
+    if (n >= N) return;
+    float x[R];
+    const uint4* row = reinterpret_cast<const uint4*>(L2 + n * R);
+#pragma unroll
+    for (int q = 0; q < R / 8; ++q) {
+      const uint4 w = row[q];
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        x[8 * q + 2 * h] = __uint_as_float(ws[h] << 16);
+        x[8 * q + 2 * h + 1] = __uint_as_float(ws[h] & 0xFFFF0000u);
+      }
+    }
+    uint4* out = reinterpret_cast<uint4*>(L2_out + n * R);
+#pragma unroll
+    for (int q = 0; q < R / 8; ++q) {
+      uint32_t packed[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        float y[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int j = 8 * q + 2 * h + t;
+          float s = 0.0f;
+#pragma unroll
+          for (int i = j; i < R; ++i) s = fmaf(x[i], M[i][j], s);
+          y[t] = s;
+        }
+        packed[h] = bf16_pattern(y[0]) | (bf16_pattern(y[1]) << 16);
+      }
+      out[q] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    }
+  }
+}
+
+int cholqr_parts(int64_t K) {
+  const int64_t chunks = (K + kCqrChunk - 1) / kCqrChunk;
+  return static_cast<int>(chunks < kCqrMaxParts ? chunks : kCqrMaxParts);
+}
+
+template <int R>
+static cudaError_t cholqr_launch(const void* L1, int64_t K, int64_t ld1, const void* L2, int64_t N, void* L1_out,
+                                 void* L2_out, int* info, float* ws, cudaStream_t s) {
+  const int parts = cholqr_parts(K);
+  float* partial = ws;
+  float* Lmat = ws + static_cast<int64_t>(parts) * R * R;
+  float* inv_diag = Lmat + R * R;
+  cholqr_gram_kernel<R><<<parts, kCqrThreads, 0, s>>>(static_cast<const uint16_t*>(L1), K, ld1, partial);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cholqr_factor_kernel<R><<<1, 1024, 0, s>>>(partial, parts, Lmat, inv_diag, info);
+  count_launch();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int colblocks = static_cast<int>((K + kCqrThreads - 1) / kCqrThreads);
+  const int rowblocks = static_cast<int>((N + kCqrThreads - 1) / kCqrThreads);
+  cholqr_apply_kernel<R><<<colblocks + rowblocks, kCqrThreads, 0, s>>>(
+      static_cast<const uint16_t*>(L1), K, ld1, static_cast<uint16_t*>(L1_out), static_cast<const uint16_t*>(L2), N,
+      static_cast<uint16_t*>(L2_out), Lmat, inv_diag, info, colblocks);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lora_cholqr(const void* L1, int64_t K, int64_t ld1, const void* L2, int64_t N, int r,
+                               void* L1_out, void* L2_out, int* info, float* ws, cudaStream_t s) {
+  switch (r) {
+    case 16: return cholqr_launch<16>(L1, K, ld1, L2, N, L1_out, L2_out, info, ws, s);
+    case 32: return cholqr_launch<32>(L1, K, ld1, L2, N, L1_out, L2_out, info, ws, s);
+    case 48: return cholqr_launch<48>(L1, K, ld1, L2, N, L1_out, L2_out, info, ws, s);
+    case 64: return cholqr_launch<64>(L1, K, ld1, L2, N, L1_out, L2_out, info, ws, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace nvfp4
