@@ -148,6 +148,22 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest `value` over all ranks (the slowest rank's time); `value` itself on one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0])
+
+
+def whole_job_tflops(flops_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: the work of every rank's step over the slowest rank's step time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -241,13 +257,9 @@ def run_ours(args):
         times, clk.window = timed(step, args.steps, args.warmup)
     launches = (F.fp4_launch_count() - launches0) * args.steps // (args.steps + args.warmup)
     F.fp4_check_status(stream)
-    total_ms = sum(times)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t[0])
+    total_ms = max_over_ranks(sum(times), dev)
     ms_per_step = total_ms / args.steps
-    value = world * gemm_flops / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(gemm_flops, world, ms_per_step)
 
     # ---- kernel breakdown through the public calls (same operands), for the roofline
     bd = breakdown(F, torch, projs, T, r, stream, dev, flush, args)
