@@ -75,6 +75,22 @@ def weight_with_outlier_columns(n_out: int, n_in: int, std: float, n_cols: int,
     return to_bf16_bits(w)
 
 
+def gapped_weight(n_out: int, n_in: int, r: int, seed: int) -> np.ndarray:
+    """N x K weight with a spectral gap after r: singular values 4..2 for the first r, then
+    0.5..0 (random singular vectors), scaled like N(0, 0.02) weights."""
+    rng = np.random.default_rng(seed)
+    m = min(n_out, n_in)
+    U, _ = np.linalg.qr(rng.standard_normal((n_out, m)))
+    V, _ = np.linalg.qr(rng.standard_normal((n_in, m)))
+    s = np.concatenate([np.linspace(4.0, 2.0, r), np.linspace(0.5, 0.0, m - r)])
+    return to_bf16_bits(((U * (s * 0.02 * np.sqrt(m) / 3.0)) @ V.T).astype(np.float32))
+
+
+def gaussian_test_matrix(n_in: int, s: int, seed: int) -> np.ndarray:
+    """The randomized SVD's test matrix Omega (K x s), N(0, 1) stored in BF16."""
+    return normal((n_in, s), 1.0, seed)
+
+
 def spectrum_matrix(m: int, n: int, s_lo: float, s_hi: float, seed: int) -> np.ndarray:
     """m x n (m <= n) with singular values ~ Uniform[s_lo, s_hi] and random singular vectors."""
     rng = np.random.default_rng(seed)

@@ -27,6 +27,14 @@ dequantized operands.  Functions and the passages they follow:
   the BF16 factors (the same rounded P and P' the forward and dX products use),
   FP64 products, FP32 results; the Cholesky-QR constraint on the subspace is not
   specified on the pages and is not applied here.
+- ``lora_realign``: the periodic realignment of the LoRA-SVD subspace by a
+  randomized SVD (section 2.1, Realignment).  READING: the randomized subspace
+  iteration and direct SVD of Halko, Martinsson and Tropp (SIAM Review 2011,
+  Algorithms 4.4 and 5.1) on W = W_res + beta L2 L1 with a caller-supplied
+  Gaussian test matrix Omega (K x s, s >= r) and q power iterations, each
+  product re-orthonormalised; then L2 = U_r Sigma_r / beta, L1 = V_r^T (each
+  row's largest-magnitude entry made positive), W_res = W - beta L2 L1 with the
+  BF16 factors; FP64, each output rounded to BF16 once.
 - ``cholesky_lower`` / ``lora_cholqr``: the Cholesky-QR step of the LoRA-SVD
   backward (section 2.1: the backward pass is restricted to the subspace under a
   Cholesky-QR constraint).  READING (no formula on the pages): the rows of L1
@@ -441,6 +449,42 @@ def lora_factor_grads_bf16(dY_bf16, X_bf16, L1_bf16, L2_bf16, beta: float = 1.0)
     f64 = lambda u: bf16_to_f32(u).astype(np.float64)
     dL1, dL2 = lora_factor_grads(f64(dY_bf16), f64(X_bf16), f64(P), f64(P2), beta)
     return dL1, dL2, P, P2
+
+
+# ---------------------------------------------------------------------------
+# Randomized-SVD realignment of the LoRA-SVD subspace (section 2.1)
+# ---------------------------------------------------------------------------
+
+def _orth(Y: np.ndarray) -> np.ndarray:
+    """An orthonormal basis of the columns of Y (Householder QR)."""
+    return np.linalg.qr(Y)[0]
+
+
+def lora_realign_f64(W_res_bf16, L1_bf16, L2_bf16, beta: float, Omega_bf16, q: int):
+    """FP64 (L2', L1', sigma_r, W) before rounding: the randomized range finder with q
+    power iterations on W = W_res + beta L2 L1 and the SVD of the small projection."""
+    f = lambda u: bf16_to_f32(u).astype(np.float64)
+    r = L1_bf16.shape[0]
+    W = f(W_res_bf16) + beta * (f(L2_bf16) @ f(L1_bf16))
+    Y = W @ f(Omega_bf16)                       # N x s sketch of the range
+    for _ in range(q):                          # subspace iteration, orthonormalising each product
+        Y = W @ _orth(W.T @ _orth(Y))
+    Q = _orth(Y)
+    B = Q.T @ W                                 # s x K
+    Ub, sig, Vt = np.linalg.svd(B, full_matrices=False)
+    U = Q @ Ub[:, :r]
+    V = Vt[:r]
+    flip = np.sign(V[np.arange(r), np.argmax(np.abs(V), axis=1)])
+    flip[flip == 0] = 1.0
+    return (U * (sig[:r] * flip)) / beta, V * flip[:, None], sig[:r], W
+
+
+def lora_realign(W_res_bf16, L1_bf16, L2_bf16, beta: float, Omega_bf16, q: int = 2):
+    """BF16 (W_res', L1', L2') with W_res' = bf16(W - beta bf16(L2') bf16(L1'))."""
+    L2n, L1n, _, W = lora_realign_f64(W_res_bf16, L1_bf16, L2_bf16, beta, Omega_bf16, q)
+    L2b, L1b = bf16_rn(L2n), bf16_rn(L1n)
+    f = lambda u: bf16_to_f32(u).astype(np.float64)
+    return bf16_rn(W - beta * (f(L2b) @ f(L1b))), L1b, L2b
 
 
 # ---------------------------------------------------------------------------

@@ -577,3 +577,44 @@ def test_lora_cholqr_rank_one_closed_form(oracle_mod):
     assert info == 0
     assert np.allclose(a, l1 / n, atol=1e-15)
     assert np.allclose(b, oracle_mod.bf16_to_f32(L2).astype(np.float64) * n, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Randomized-SVD realignment
+# ---------------------------------------------------------------------------
+
+def test_lora_realign_recovers_an_exactly_low_rank_weight(oracle_mod):
+    # W = L2 L1 of rank r and s >= r: the range finder captures the range exactly, so the
+    # realigned factors give back W (to FP64 rounding) and the residual is zero
+    from nvfp4_quantized_pretraining_gb300 import synthetic as S
+    N, K, r, s = 96, 160, 8, 16
+    L2 = S.normal((N, r), 0.5, 20)
+    L1 = S.normal((r, K), 0.5, 21)
+    W_res = np.zeros((N, K), np.uint16)
+    f = lambda u: oracle_mod.bf16_to_f32(u).astype(np.float64)
+    L2n, L1n, sig, W = oracle_mod.lora_realign_f64(W_res, L1, L2, 1.0, S.gaussian_test_matrix(K, s, 22), 0)
+    assert np.allclose(L2n @ L1n, W, atol=1e-12 * np.abs(W).max())
+    assert np.allclose(L1n @ L1n.T, np.eye(r), atol=1e-12)
+    assert np.allclose(sig, np.linalg.svd(W, compute_uv=False)[:r], rtol=1e-12)
+
+
+def test_lora_realign_matches_the_truncated_svd_on_a_gapped_spectrum(oracle_mod):
+    # with a gap sigma_{r+1} / sigma_r = 1/4 and q = 2 the subspace error is ~(1/4)^5 ~ 1e-3 of
+    # the tail; the rank-r product must match the exact truncated SVD to that order
+    from nvfp4_quantized_pretraining_gb300 import synthetic as S
+    N, K, r, s = 192, 256, 16, 32
+    W0 = S.gapped_weight(N, K, r, 23)
+    zero1, zero2 = np.zeros((r, K), np.uint16), np.zeros((N, r), np.uint16)
+    beta = 0.5
+    L2n, L1n, sig, W = oracle_mod.lora_realign_f64(W0, zero1, zero2, beta, S.gaussian_test_matrix(K, s, 24), 2)
+    U, S_, Vt = np.linalg.svd(W, full_matrices=False)
+    best = (U[:, :r] * S_[:r]) @ Vt[:r]
+    assert np.linalg.norm(beta * L2n @ L1n - best) / np.linalg.norm(best) < 1e-3
+    assert np.allclose(sig, S_[:r], rtol=1e-3)
+    # the BF16 split is W to the rounding of its parts
+    W_res, L1, L2 = oracle_mod.lora_realign(W0, zero1, zero2, beta, S.gaussian_test_matrix(K, s, 24), 2)
+    f = lambda u: oracle_mod.bf16_to_f32(u).astype(np.float64)
+    back = f(W_res) + beta * f(L2) @ f(L1)
+    assert np.abs(back - W).max() <= 2.0 ** -8 * np.abs(f(W_res)).max()
+    # the sign convention: each L1 row's largest-magnitude entry is positive
+    assert np.all(L1n[np.arange(r), np.argmax(np.abs(L1n), axis=1)] > 0)
