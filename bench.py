@@ -265,6 +265,7 @@ def run_ours(args):
     bd = breakdown(F, torch, projs, T, r, stream, dev, flush, args)
     lg = lora_grads(F, torch, projs, T, r, stream, dev, flush, args) if r else None
     cq = lora_cholqr(F, torch, projs, r, stream, dev, flush, args) if r else None
+    ra = lora_realign(F, torch, S, projs, r, stream, dev, flush, args) if r else None
     ns = newton_schulz(F, torch, S, stream, dev, flush, args)
     vt = qadamw_codec(F, torch, projs, stream, dev, flush, args)
 
@@ -298,6 +299,7 @@ def run_ours(args):
         "breakdown_ms": {k: round(v, 4) for k, v in bd["per_kind_ms"].items()},
         "lora_factor_grads": lg,
         "lora_cholqr": cq,
+        "lora_realign": ra,
         "newton_schulz": ns,
         "qadamw_v_codec": vt,
         "branch_tflops_counted_separately": round(branch_flops / 1e12, 4),
@@ -456,16 +458,68 @@ def lora_cholqr(F, torch, projs, r, stream, dev, flush, args):
             "note": "L1 <- L^-1 L1, L2 <- L2 L of the four projections (r = 64), summed median call times"}
 
 
+REALIGN_OVERSAMPLE, REALIGN_POWER_ITERS = 16, 2
+
+
+def lora_realign(F, torch, S, projs, r, stream, dev, flush, args):
+    """Times the randomized-SVD realignment of each projection's weight (W_res + L2 L1, rank r,
+    sketch width r + 16, 2 power iterations), out of place, each call after an L2 flush.  Not
+    part of the timed step (it runs every few thousand steps).  FLOPs are those of the FP32
+    products, 2 N K (2 r + s (2 + 2 q)) per weight, against the FP32 CUDA-core rate
+    (152 SMs x 128 FMA/clk x 2 FLOP x the sampled SM clock is ~80 TFLOP/s at 2.07 GHz)."""
+    s_cols, q = r + REALIGN_OVERSAMPLE, REALIGN_POWER_ITERS
+    reps = max(1, min(args.steps, 3))
+    total, flops = 0.0, 0.0
+    with torch.cuda.stream(stream):
+        for i, p in enumerate(projs):
+            N, K = p["N"], p["K"]
+            Om = S.normal_device((K, s_cols), 1.0, 700 + i, dev)
+            outs = (torch.empty_like(p["Wres"]), torch.empty_like(p["L1"]), torch.empty_like(p["L2"]))
+            info = torch.zeros(1, dtype=torch.int32, device=dev)
+            ws = torch.empty(F.lib().fp4_lora_realign_workspace(N, K, r, s_cols), dtype=torch.uint8, device=dev)
+            fn = lambda: F.fp4_lora_realign(p["Wres"], p["L1"], p["L2"], Om, q=q, out=outs, info=info,
+                                            workspace=ws, stream=stream)
+            fn()
+            ts = []
+            for _ in range(reps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            total += sorted(ts)[len(ts) // 2]
+            flops += 2.0 * N * K * (2 * r + s_cols * (2 + 2 * q))
+            if int(info.item()) != 0:
+                raise RuntimeError(f"realignment of {p['name']}: info = {int(info.item())}")
+            del outs, ws, Om
+    F.fp4_check_status(stream)
+    fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+    tf = flops / (total * 1e-3) / 1e12
+    return {"ms_total": round(total, 4), "sketch": s_cols, "power_iters": q, "fp32_tflops": round(tf, 1),
+            "bound": "alu", "peak": round(fp32_peak, 1), "unit": "TFLOP/s", "frac": round(tf / fp32_peak, 4),
+            "note": "four weights of the block; FP32 product FLOPs over the summed median call times; the peak "
+                    "is the FP32 FMA rate at the 2.07 GHz maximum SM clock"}
+
+
 def run_part(args, F, torch, S, dev):
     """One optimizer-side measurement alone, with the same shapes as in the full line."""
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    wl = WORKLOADS[args.workload]
+    projs = [dict(name=n, N=N, K=K) for n, N, K in wl["projections"]]
     if args.part == "newton_schulz":
         res = newton_schulz(F, torch, S, stream, dev, flush, args)
-    else:
-        wl = WORKLOADS[args.workload]
-        projs = [dict(name=n, N=N, K=K) for n, N, K in wl["projections"]]
+    elif args.part == "qadamw_v_codec":
         res = qadamw_codec(F, torch, projs, stream, dev, flush, args)
+    else:
+        r = wl["r"]
+        for i, p in enumerate(projs):
+            p["Wres"] = S.normal_device((p["N"], p["K"]), 0.02, 800 + i, dev)
+            p["L1"] = S.normal_device((r, p["K"]), 0.02, 810 + i, dev)
+            p["L2"] = S.normal_device((p["N"], r), 0.02, 820 + i, dev)
+        res = lora_realign(F, torch, S, projs, r, stream, dev, flush, args)
     print(json.dumps({args.part: res}), flush=True)
 
 
@@ -689,7 +743,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="block3b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--part", choices=["all", "newton_schulz", "qadamw_v_codec"], default="all",
+    ap.add_argument("--part", choices=["all", "newton_schulz", "qadamw_v_codec", "lora_realign"], default="all",
                     help="run one optimizer-side measurement alone (prints its JSON object; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

@@ -214,6 +214,31 @@ fp4_status fp4_lora_factor_grad(const void* A, int64_t T, int64_t M, int64_t lda
                                 const void* B, int r, float beta, float* C, int64_t ldc,
                                 int transpose_c, void* ws, size_t ws_bytes, void* stream);
 
+/* Realignment of the LoRA-SVD subspace by a randomized SVD (section 2.1,
+ * Realignment: the subspace is reset periodically with a randomized SVD; the
+ * pages give no parameters).  The randomized subspace iteration and direct SVD
+ * of Halko, Martinsson and Tropp (SIAM Review 2011, Algorithms 4.4 and 5.1) on
+ * W = W_res + beta L2 L1:
+ *   Y = W Omega;  q times Y = W orth(W^T orth(Y));  Q = orth(Y);  B = Q^T W;
+ *   B = Ub Sigma V^T;  L2_out = bf16(Q Ub_r Sigma_r / beta);  L1_out = bf16(V_r^T);
+ *   W_res_out = bf16(W - beta L2_out L1_out),
+ * each L1_out row's largest-magnitude entry made positive (L2_out's column
+ * follows).  FP32 arithmetic: cuBLAS SGEMM for the products, Cholesky-QR twice
+ * for orth(), a one-CTA Jacobi eigensolver for B B^T.
+ * W_res: N x K BF16, row pitch ldw (W_res_out the same); L1: r x K (pitch K);
+ * L2: N x r (pitch r); Omega: K x s BF16 test matrix (pitch s), Gaussian,
+ * supplied by the caller.  Outputs may be the inputs.  r in {16,32,48,64},
+ * s a multiple of 16 in [r, 128], N, K >= s, N K < 2^31, 0 <= q <= 8, beta > 0.
+ * W must have numerical rank >= s.  info (device int): 0, or nonzero when a
+ * Cholesky factorisation failed (then no output is written).
+ * ws: fp4_lora_realign_workspace(N, K, r, s) bytes (about 4 N K), 256-byte
+ * aligned.  Uses one cuBLAS handle per device, created on the first call. */
+size_t fp4_lora_realign_workspace(int64_t N, int64_t K, int r, int s);
+fp4_status fp4_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t ldw,
+                            const void* L1, const void* L2, int r, float beta,
+                            const void* Omega, int s, int q, void* W_res_out, void* L1_out,
+                            void* L2_out, int* info, void* ws, size_t ws_bytes, void* stream);
+
 /* Cholesky-QR step of the LoRA-SVD branch (section 2.1: the backward pass is
  * restricted to the subspace under a Cholesky-QR constraint; no formula on the
  * pages).  Reading: the rows of L1 are re-orthonormalised through the Cholesky

@@ -34,7 +34,7 @@ OUT_F32 = 1
 EXPORTS = ["fp4_scale_bytes", "fp4_amax", "fp4_quantize", "fp4_quantize_transposed", "fp4_quantize_dual",
            "fp4_gemm_blockscaled", "fp4_branch_factor", "fp4_linear_fwd_workspace", "fp4_linear_bwd_workspace",
            "fp4_linear_fwd", "fp4_linear_fwd_noalloc", "fp4_linear_bwd", "fp4_lora_factor_grad_workspace",
-           "fp4_lora_factor_grad", "fp4_lora_cholqr_workspace", "fp4_lora_cholqr", "fp4_newton_schulz_workspace", "fp4_newton_schulz", "fp4_qadamw_v_encode",
+           "fp4_lora_factor_grad", "fp4_lora_cholqr_workspace", "fp4_lora_cholqr", "fp4_lora_realign_workspace", "fp4_lora_realign", "fp4_newton_schulz_workspace", "fp4_newton_schulz", "fp4_qadamw_v_encode",
            "fp4_qadamw_v_decode", "fp4_check_status", "fp4_last_error", "fp4_launch_count",
            "fp4_debug_convert", "fp4_debug_sr_round", "fp4_mma_peak_probe"]
 
@@ -82,6 +82,9 @@ def lib() -> ctypes.CDLL:
         "fp4_lora_factor_grad_workspace": (ctypes.c_size_t, [i64, i64, i32]),
         "fp4_lora_factor_grad": (i32, [P, i64, i64, i64, P, i32, f32, P, i64, i32, P, ctypes.c_size_t, P]),
         "fp4_lora_cholqr_workspace": (ctypes.c_size_t, [i64, i32]),
+        "fp4_lora_realign_workspace": (ctypes.c_size_t, [i64, i64, i32, i32]),
+        "fp4_lora_realign": (i32, [P, i64, i64, i64, P, P, i32, f32, P, i32, i32, P, P, P, P, P, ctypes.c_size_t,
+                                   P]),
         "fp4_lora_cholqr": (i32, [P, i64, i64, P, i64, i32, P, P, P, P, ctypes.c_size_t, P]),
         "fp4_newton_schulz_workspace": (ctypes.c_size_t, [i64, i64, f32]),
         "fp4_newton_schulz": (i32, [P, i64, i64, i64, i32, i32, f32, f32, f32, i32, P, i64, P, ctypes.c_size_t,
@@ -312,6 +315,30 @@ def fp4_lora_cholqr(L1: torch.Tensor, L2: torch.Tensor, L1_out=None, L2_out=None
     _check(lib().fp4_lora_cholqr(L1.data_ptr(), K, ld1, L2.data_ptr(), N, r, L1_out.data_ptr(), L2_out.data_ptr(),
                                  info.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(stream)))
     return L1_out, L2_out, info
+
+
+def fp4_lora_realign(W_res: torch.Tensor, L1: torch.Tensor, L2: torch.Tensor, Omega: torch.Tensor,
+                     beta: float = 1.0, q: int = 2, out=None, info=None, workspace=None, stream=None):
+    """Randomized-SVD realignment of W = W_res + beta L2 L1 with the test matrix Omega (K x s, BF16)
+    and q power iterations.  Returns (W_res', L1', L2', info); pass out=(W_res, L1, L2) to update in
+    place.  info (device int32) is nonzero when a Cholesky factorisation failed (nothing written)."""
+    N, K, ldw = _bf16_2d(W_res, "W_res")
+    r = L1.shape[0]
+    s = Omega.shape[1]
+    for t, shape in ((L1, (r, K)), (L2, (N, r)), (Omega, (K, s))):
+        assert t.dtype == torch.bfloat16 and t.is_contiguous() and tuple(t.shape) == shape
+    if out is None:
+        out = (torch.empty((N, ldw), dtype=torch.bfloat16, device=W_res.device)[:, :K], torch.empty_like(L1),
+               torch.empty_like(L2))
+    Wo, L1o, L2o = out
+    assert Wo.stride(0) == ldw
+    info = torch.zeros(1, dtype=torch.int32, device=W_res.device) if info is None else info
+    need = lib().fp4_lora_realign_workspace(N, K, r, s)
+    workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=W_res.device) if workspace is None else workspace
+    _check(lib().fp4_lora_realign(W_res.data_ptr(), N, K, ldw, L1.data_ptr(), L2.data_ptr(), r, float(beta),
+                                  Omega.data_ptr(), s, int(q), Wo.data_ptr(), L1o.data_ptr(), L2o.data_ptr(),
+                                  info.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(stream)))
+    return Wo, L1o, L2o, info
 
 
 NS_COEFFS = (1.5, -0.5, 0.0)  # the cubic Newton-Schulz polynomial

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnvfp4_gb300.so")
-SOURCES = ["quantize.cu", "gemm.cu", "lora_grad.cu", "lora_cholqr.cu", "newton_schulz.cu", "qadamw.cu", "peak.cu", "api.cu"]
+SOURCES = ["quantize.cu", "gemm.cu", "lora_grad.cu", "lora_cholqr.cu", "realign.cu", "newton_schulz.cu", "qadamw.cu", "peak.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 
@@ -62,7 +62,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         msg = "\n".join(" ".join(c) + "\n" + o for c, o in failed)
         raise RuntimeError("nvcc failed:\n" + msg)
     tmp = LIB + f".tmp{os.getpid()}"
-    subprocess.run([nvcc()] + ARCH + ["-shared", "-o", tmp] + objs, check=True)
+    subprocess.run([nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcublas"], check=True)
     os.replace(tmp, LIB)
     return LIB
 

@@ -588,6 +588,37 @@ fp4_status fp4_lora_cholqr(const void* L1, int64_t K, int64_t ld1, const void* L
   return FP4_OK;
 }
 
+size_t fp4_lora_realign_workspace(int64_t N, int64_t K, int r, int s) {
+  if (N <= 0 || K <= 0 || r <= 0 || s <= 0) return 0;
+  return round256(realign_workspace_floats(N, K, r, s) * sizeof(float));
+}
+
+fp4_status fp4_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t ldw, const void* L1, const void* L2,
+                            int r, float beta, const void* Omega, int s, int q, void* W_res_out, void* L1_out,
+                            void* L2_out, int* info, void* ws, size_t ws_bytes, void* stream) {
+  fp4_status st;
+  if (r != 16 && r != 32 && r != 48 && r != 64) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rank r=%d not in {16,32,48,64}", r);
+  if (s < r || s > 128 || s % 16 != 0)
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "sketch width s=%d must be a multiple of 16 in [r, 128]", s);
+  if (q < 0 || q > 8) return fail(FP4_ERR_INVALID_ARG, "power iterations q=%d not in [0, 8]", q);
+  if (!(beta > 0.0f)) return fail(FP4_ERR_INVALID_ARG, "beta must be positive");
+  if ((st = check_bf16_input(W_res, N, K, ldw, "W_res")) || (st = check_bf16_input(L1, r, K, K, "L1")) ||
+      (st = check_bf16_input(L2, N, r, r, "L2")) || (st = check_bf16_input(Omega, K, s, s, "Omega")))
+    return st;
+  if (N < s || K < s) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "N and K must be at least s");
+  if (N * K >= (int64_t(1) << 31) || N >= (int64_t(1) << 30))
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "W too large for the 32-bit BLAS dimensions");
+  if (!W_res_out || !L1_out || !L2_out || !info) return fail(FP4_ERR_INVALID_ARG, "outputs and info must be non-NULL");
+  if (!aligned16(W_res_out) || !aligned16(L1_out) || !aligned16(L2_out) || (reinterpret_cast<uintptr_t>(info) & 3u))
+    return fail(FP4_ERR_MISALIGNED, "outputs must be 16-byte aligned, info 4-byte aligned");
+  const size_t need = fp4_lora_realign_workspace(N, K, r, s);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return fail(FP4_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
+  CUDA_TRY(launch_lora_realign(W_res, N, K, ldw, L1, L2, r, beta, Omega, s, q, W_res_out, L1_out, L2_out, info,
+                               static_cast<float*>(ws), sm_count(), static_cast<cudaStream_t>(stream)));
+  return FP4_OK;
+}
+
 static fp4_status check_f32_matrix(const float* p, int64_t rows, int64_t cols, int64_t ld, const char* name) {
   if (!p) return fail(FP4_ERR_INVALID_ARG, "%s is NULL", name);
   if (rows <= 0 || cols <= 0 || cols % 16 != 0)

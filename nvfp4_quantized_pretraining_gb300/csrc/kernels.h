@@ -90,6 +90,14 @@ int cholqr_parts(int64_t K);
 cudaError_t launch_lora_cholqr(const void* L1, int64_t K, int64_t ld1, const void* L2, int64_t N, int r,
                                void* L1_out, void* L2_out, int* info, float* ws, cudaStream_t s);
 
+// Randomized-SVD realignment of the LoRA-SVD subspace (FP32, cuBLAS SGEMM for the plain
+// products); ws holds realign_workspace_floats(N, K, r, s) floats; *info (device) = 0, or a
+// failed Cholesky (1000 * stage + pivot order), in which case no output is written.
+size_t realign_workspace_floats(int64_t N, int64_t K, int r, int s);
+cudaError_t launch_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t ldw, const void* L1, const void* L2,
+                                int r, float beta, const void* Omega, int s_cols, int q, void* W_res_out,
+                                void* L1_out, void* L2_out, int* info, float* ws, int num_sms, cudaStream_t st);
+
 // Q-AdamW second-moment codec: v (FP32 rows x cols, pitch ldv, cols % 16 == 0) to NVFP4
 // codes/scales/S_t (out; out.scale[1] receives the amax) and BF16 tile means (rows x cols/16);
 // and back to FP32 (pitch ldo).
