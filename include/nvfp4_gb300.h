@@ -232,7 +232,9 @@ fp4_status fp4_lora_factor_grad(const void* A, int64_t T, int64_t M, int64_t lda
  * W must have numerical rank >= s.  info (device int): 0, or nonzero when a
  * Cholesky factorisation failed (then no output is written).
  * ws: fp4_lora_realign_workspace(N, K, r, s) bytes (about 4 N K), 256-byte
- * aligned.  Uses one cuBLAS handle per device, created on the first call. */
+ * aligned.  Uses one cuBLAS handle per device, created on the first call and
+ * shared: calls on one device must not run concurrently from several host
+ * threads (each call sets the handle's stream). */
 size_t fp4_lora_realign_workspace(int64_t N, int64_t K, int r, int s);
 fp4_status fp4_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t ldw,
                             const void* L1, const void* L2, int r, float beta,
