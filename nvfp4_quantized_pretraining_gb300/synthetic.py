@@ -92,11 +92,12 @@ def gaussian_test_matrix(n_in: int, s: int, seed: int) -> np.ndarray:
 
 
 def spectrum_matrix(m: int, n: int, s_lo: float, s_hi: float, seed: int) -> np.ndarray:
-    """m x n (m <= n) with singular values ~ Uniform[s_lo, s_hi] and random singular vectors."""
+    """m x n with min(m, n) singular values ~ Uniform[s_lo, s_hi] and random singular vectors."""
     rng = np.random.default_rng(seed)
-    U, _ = np.linalg.qr(rng.standard_normal((m, m)))
-    V, _ = np.linalg.qr(rng.standard_normal((n, m)))
-    s = rng.uniform(s_lo, s_hi, size=m)
+    k = min(m, n)
+    U, _ = np.linalg.qr(rng.standard_normal((m, k)))
+    V, _ = np.linalg.qr(rng.standard_normal((n, k)))
+    s = rng.uniform(s_lo, s_hi, size=k)
     return to_bf16_bits(((U * s) @ V.T).astype(np.float32))
 
 

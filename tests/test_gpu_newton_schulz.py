@@ -115,6 +115,7 @@ def test_p99_clip_bit_exact(F, oracle_mod, m, n):
     (384, 768, (1.5, -0.5, 0.0), True),
     (256, 512, (15 / 8, -10 / 8, 3 / 8), True),     # quintic: the A^2 product and its lincomb
     (128, 384, (3.4445, -4.7750, 2.0315), False),
+    (384, 256, (1.5, -0.5, 0.0), True),              # m > n: a tall iterate (m x m Gram matrix of rank n)
 ])
 def test_one_step_matches_oracle(F, oracle_mod, m, n, coeffs, clip):
     X0 = S.spectrum_matrix(m, n, 0.3, 1.1, m + 7 * n)
