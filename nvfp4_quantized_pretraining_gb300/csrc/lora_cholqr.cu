@@ -14,6 +14,7 @@
 //      and one per row of L2 (the row times L), BF16 results; nothing is written
 //      when *info != 0.  Each thread reads its whole column or row before writing
 //      it, so the update may be in place.
+#include "bf16_convert.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -105,11 +106,6 @@ __global__ void __launch_bounds__(1024) cholqr_factor_kernel(const float* __rest
   if (threadIdx.x < R) inv_diag[threadIdx.x] = 1.0f / G[threadIdx.x][threadIdx.x];
 }
 
-__device__ __forceinline__ uint32_t bf16_pattern(float v) {
-  uint16_t r;
-  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
-  return r;
-}
 
 // Blocks [0, ncolblocks): columns of L1 (L1' = L^-1 L1 by forward substitution);
 // the rest: rows of L2 (L2' = L2 L).
@@ -137,7 +133,7 @@ __global__ void __launch_bounds__(kCqrThreads) cholqr_apply_kernel(
 #pragma unroll
       for (int c = 0; c < i; ++c) s = fmaf(-M[i][c], x[c], s);
       x[i] = s * dinv[i];
-      L1_out[i * ld1 + k] = static_cast<uint16_t>(bf16_pattern(x[i]));
+      L1_out[i * ld1 + k] = static_cast<uint16_t>(bf16_rn_bits(x[i]));
     }
   } else {
     const int64_t n = static_cast<int64_t>(blockIdx.x - ncolblocks) * kCqrThreads + threadIdx.x;
@@ -169,7 +165,7 @@ __global__ void __launch_bounds__(kCqrThreads) cholqr_apply_kernel(
           for (int i = j; i < R; ++i) s = fmaf(x[i], M[i][j], s);
           y[t] = s;
         }
-        packed[h] = bf16_pattern(y[0]) | (bf16_pattern(y[1]) << 16);
+        packed[h] = bf16_rn_bits(y[0]) | (bf16_rn_bits(y[1]) << 16);
       }
       out[q] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }

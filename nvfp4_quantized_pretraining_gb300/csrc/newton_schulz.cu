@@ -14,6 +14,7 @@
 //     output (the next step's clip).
 // All kernels are grid-stride loops over 16-byte chunks (8 BF16) of row-major
 // matrices with a row pitch; the grid is sized in multiples of the SM count.
+#include "bf16_convert.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -29,12 +30,6 @@ __device__ __forceinline__ const uint16_t* chunk_ptr(const uint16_t* base, uint3
   return base + static_cast<int64_t>(row) * ld + static_cast<int64_t>(c - row * cpr) * 8;
 }
 
-// binary32 -> BF16 pattern, round to nearest even (the PTX conversion).
-__device__ __forceinline__ uint32_t bf16_rn(float v) {
-  uint16_t r;
-  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
-  return r;
-}
 
 // Round a double to the nearest BF16 pattern, ties to even, directly (rounding to
 // binary32 first would round twice).  Normal range: keep the top 7 of the 52
@@ -71,7 +66,7 @@ __device__ __forceinline__ uint32_t scaled_bf16(uint32_t h, float inv32, double 
   const bool near_mid = (low > 0x8000u - 5u) && (low < 0x8000u + 5u);
   const bool tiny = (pb & 0x7F800000u) < (27u << 23) && (pb & 0x7FFFFFFFu) != 0;  // |p| < 2^-100
   if (near_mid || tiny || wide) return bf16_from_f64_rn(bf16_to_f64(h) * inv64);
-  return bf16_rn(p);
+  return bf16_rn_bits(p);
 }
 
 // ---------------------------------------------------------------------------
@@ -303,7 +298,7 @@ __global__ void __launch_bounds__(EPI == 2 ? kNsHistThreads : kNsThreads) ns_lin
           lo = __fadd_rn(lo, __fmul_rn(q, bf16_lo(wy[j])));
           hi = __fadd_rn(hi, __fmul_rn(q, bf16_hi(wy[j])));
         }
-        o[j] = bf16_rn(lo) | (bf16_rn(hi) << 16);
+        o[j] = bf16_rn_bits(lo) | (bf16_rn_bits(hi) << 16);
         if (EPI == 1) m2 = __vmaxu2(m2, o[j] & 0x7FFF7FFFu);
       }
       *reinterpret_cast<uint4*>(const_cast<uint16_t*>(chunk_ptr(out, u ? c1 : c0, cpr, ldo))) =

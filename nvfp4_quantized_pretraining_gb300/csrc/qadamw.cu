@@ -12,6 +12,7 @@
 // Every operation is a single FP32 operation in a fixed order (no contraction).
 // The encoder makes two passes over v (max |h|, then the codes), since the tensor
 // scale needs the whole tensor; both recompute h from v instead of storing it.
+#include "bf16_convert.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "scale_layout.cuh"
@@ -20,11 +21,6 @@ namespace nvfp4 {
 
 constexpr int kVtThreads = 256;
 
-__device__ __forceinline__ uint32_t bf16_bits_rn(float v) {
-  uint16_t r;
-  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
-  return r;
-}
 
 // In-place unnormalised Walsh-Hadamard transform of 16 values, natural order.
 __device__ __forceinline__ void wht16(float (&x)[16]) {
@@ -65,7 +61,7 @@ __device__ __forceinline__ uint32_t vt_forward(const float4 (&fv)[4], float (&h)
   for (int i = 0; i < 4; ++i) t[i] = __fadd_rn(t[2 * i], t[2 * i + 1]);
 #pragma unroll
   for (int i = 0; i < 2; ++i) t[i] = __fadd_rn(t[2 * i], t[2 * i + 1]);
-  const uint32_t mean = bf16_bits_rn(__fmul_rn(__fadd_rn(t[0], t[1]), 0.0625f));
+  const uint32_t mean = bf16_rn_bits(__fmul_rn(__fadd_rn(t[0], t[1]), 0.0625f));
   const float mu = __uint_as_float(mean << 16);
 #pragma unroll
   for (int i = 0; i < 16; ++i) h[i] = __fsub_rn(h[i], mu);

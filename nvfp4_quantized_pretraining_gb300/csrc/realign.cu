@@ -18,6 +18,7 @@
 
 #include <atomic>
 
+#include "bf16_convert.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -54,9 +55,7 @@ __global__ void __launch_bounds__(kRlThreads) rl_f32_to_bf16(const float* __rest
     float v = in[r * ld + c];
     if (rs) v *= rs[r];
     if (cs) v *= cs[c];
-    uint16_t b;
-    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(b) : "f"(v));
-    out[r * ldo + c] = b;
+    out[r * ldo + c] = static_cast<uint16_t>(bf16_rn_bits(v));
   }
 }
 
