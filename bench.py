@@ -181,7 +181,7 @@ def run_ours(args):
     B.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if args.part != "all":
+    if args.part not in ("all", "step"):
         run_part(args, F, torch, S, dev)
         return
     if world > 1:
@@ -263,6 +263,14 @@ def run_ours(args):
 
     # ---- kernel breakdown through the public calls (same operands), for the roofline
     bd = breakdown(F, torch, projs, T, r, stream, dev, flush, args)
+    if args.part == "step":  # the timed step and its breakdown only (for profiling)
+        if rank == 0:
+            print(json.dumps({"step": {"ms_per_step": round(ms_per_step, 4), "value": round(value, 2),
+                                       "breakdown_ms": {k: round(v, 4) for k, v in bd["per_kind_ms"].items()}}}),
+                  flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     lg = lora_grads(F, torch, projs, T, r, stream, dev, flush, args) if r else None
     cq = lora_cholqr(F, torch, projs, r, stream, dev, flush, args) if r else None
     ra = lora_realign(F, torch, S, projs, r, stream, dev, flush, args) if r else None
@@ -762,7 +770,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="block3b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--part", choices=["all", "newton_schulz", "qadamw_v_codec", "lora_realign"], default="all",
+    ap.add_argument("--part", choices=["all", "step", "newton_schulz", "qadamw_v_codec", "lora_realign"], default="all",
                     help="run one optimizer-side measurement alone (prints its JSON object; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
