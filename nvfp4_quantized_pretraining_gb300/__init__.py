@@ -359,7 +359,9 @@ def fp4_newton_schulz(G: torch.Tensor, steps: int = NS_STEPS, coeffs=NS_COEFFS, 
     a, b, c = (float(v) for v in coeffs)
     if out is None:
         out = torch.empty((m, n), dtype=torch.bfloat16, device=G.device)
-    _, _, ldx = _bf16_2d(out, "out")
+    mo, no, ldx = _bf16_2d(out, "out")
+    if (mo, no) != (m, n):
+        raise ValueError(f"out is {mo} x {no}, expected {m} x {n}")
     need = newton_schulz_workspace(m, n, c)
     workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=G.device) if workspace is None else workspace
     _check(lib().fp4_newton_schulz(G.data_ptr(), m, n, ldg, 1 if normalize else 0, int(steps), a, b, c,
@@ -374,6 +376,12 @@ def _f32_2d(x: torch.Tensor, name: str):
     return x.shape[0], x.shape[1], x.stride(0)
 
 
+def _check_means(mean: torch.Tensor, R: int, C: int) -> None:
+    if (mean.dtype != torch.bfloat16 or not mean.is_cuda or not mean.is_contiguous()
+            or tuple(mean.shape) != (R, C // 16)):
+        raise ValueError(f"mean must be a contiguous CUDA bfloat16 tensor of shape ({R}, {C // 16})")
+
+
 def fp4_qadamw_v_encode(v: torch.Tensor, out: NVFP4Tensor | None = None, mean: torch.Tensor | None = None,
                         stream=None):
     """Encode AdamW's second moment v (FP32, >= 0): sqrt, BF16 mean per 16-element block,
@@ -382,6 +390,9 @@ def fp4_qadamw_v_encode(v: torch.Tensor, out: NVFP4Tensor | None = None, mean: t
     out = NVFP4Tensor.empty(R, C, v.device) if out is None else out
     if mean is None:
         mean = torch.empty((R, C // 16), dtype=torch.bfloat16, device=v.device)
+    _check_means(mean, R, C)
+    if (out.rows, out.cols) != (R, C):
+        raise ValueError(f"out is {out.rows} x {out.cols}, expected {R} x {C}")
     ct = out.c()
     _check(lib().fp4_qadamw_v_encode(v.data_ptr(), R, C, ldv, ctypes.byref(ct), mean.data_ptr(), _stream(stream)))
     return out, mean
@@ -390,9 +401,12 @@ def fp4_qadamw_v_encode(v: torch.Tensor, out: NVFP4Tensor | None = None, mean: t
 def fp4_qadamw_v_decode(q: NVFP4Tensor, mean: torch.Tensor, out: torch.Tensor | None = None,
                         stream=None) -> torch.Tensor:
     """Rebuild v (FP32) from fp4_qadamw_v_encode's output."""
+    _check_means(mean, q.rows, q.cols)
     if out is None:
         out = torch.empty((q.rows, q.cols), dtype=torch.float32, device=mean.device)
-    _, _, ldo = _f32_2d(out, "out")
+    R, C, ldo = _f32_2d(out, "out")
+    if (R, C) != (q.rows, q.cols):
+        raise ValueError(f"out is {R} x {C}, expected {q.rows} x {q.cols}")
     ct = q.c()
     _check(lib().fp4_qadamw_v_decode(ctypes.byref(ct), mean.data_ptr(), out.data_ptr(), ldo, _stream(stream)))
     return out
