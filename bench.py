@@ -285,7 +285,8 @@ def run_ours(args):
     gemm_tf = bd["gemm_flops"] / (bd["gemm_ms"] * 1e-3) / 1e12
     h = gemm_source_hash()
     traffic = GEMM_TRAFFIC.get(h)
-    q_gbs = bd["quant_bytes"] / (bd["quant_ms"] * 1e-3) / 1e9
+    q_gbs = bd["rtn_bytes"] / (bd["rtn_ms"] * 1e-3) / 1e9
+    sr_gbs = bd["sr_bytes"] / (bd["sr_ms"] * 1e-3) / 1e9
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
@@ -300,10 +301,15 @@ def run_ours(args):
                      "peak_note": f"{pk_kind} bf16 burst {pk['bf16_tflops']} TFLOP/s x {FP4_OVER_BF16:g} "
                                   "(nominal dense FP4:BF16 ratio); datasheet dense FP4 13500 TFLOP/s",
                      "frac_of_datasheet": round(gemm_tf / 13500.0, 4)},
-        "quantize": {"bound": "hbm", "achieved": round(q_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(q_gbs / pk["hbm_gbs"], 4),
-                     "note": "algorithmic bytes of the dual-orientation quantize launches (2 B read + 2 x 0.5625 B "
-                             "written per element) over their event time"},
+        "quantize_rtn": {"bound": "hbm", "achieved": round(q_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(q_gbs / pk["hbm_gbs"], 4),
+                         "note": "X and W: algorithmic bytes of the dual-orientation RTN launches (2 B read + "
+                                 "2 x 0.5625 B written per element) over their event time"},
+        "quantize_sr": {"bound": "alu", "elements_per_s": round(bd["sr_elems"] / (bd["sr_ms"] * 1e-3), 1),
+                        "achieved_gbs": round(sr_gbs, 1), "hbm_frac": round(sr_gbs / pk["hbm_gbs"], 4),
+                        "note": "dY, both forms with SR: bound by the integer ALU pipe (two Philox4x32-10 draws "
+                                "and the SR rule per element; ncu on the 1B MLP dY: ALU pipe 64% busy, issue "
+                                "slots 74%, DRAM 14%, profiles/quantize_dual_and_branch_factor_mlp_up.md)"},
         "breakdown_ms": {k: round(v, 4) for k, v in bd["per_kind_ms"].items()},
         "lora_factor_grads": lg,
         "lora_cholqr": cq,
@@ -328,7 +334,6 @@ def breakdown(F, torch, projs, T, r, stream, dev, flush, args):
     launching stream (after warm-up, L2 flushed before every step)."""
     ev = []
     gemm_flops = 0
-    quant_bytes = 0
     reps = max(2, min(args.steps, 5))
     kinds = {}
 
@@ -385,12 +390,16 @@ def breakdown(F, torch, projs, T, r, stream, dev, flush, args):
             for kind, e0, e1 in ev:
                 kinds.setdefault(kind, 0.0)
                 kinds[kind] += e0.elapsed_time(e1) / reps
+    rtn_bytes = sr_bytes = 0
+    sr_elems = 0
     for p in projs:
         gemm_flops += 3 * 2 * T * p["N"] * p["K"]
-        quant_bytes += int(3.125 * (T * p["K"] + T * p["N"] + p["N"] * p["K"]))
-    quant_ms = kinds.get("quantize_x_dual", 0) + kinds.get("quantize_dy_dual_sr", 0) + kinds.get("quantize_w_dual", 0)
-    return dict(gemm_flops=gemm_flops, gemm_ms=kinds["gemm"], quant_bytes=quant_bytes, quant_ms=quant_ms,
-                per_kind_ms=kinds)
+        rtn_bytes += int(3.125 * (T * p["K"] + p["N"] * p["K"]))   # X and W: both forms from one read
+        sr_bytes += int(3.125 * T * p["N"])                        # dY
+        sr_elems += T * p["N"]
+    rtn_ms = kinds.get("quantize_x_dual", 0) + kinds.get("quantize_w_dual", 0)
+    return dict(gemm_flops=gemm_flops, gemm_ms=kinds["gemm"], rtn_bytes=rtn_bytes, rtn_ms=rtn_ms,
+                sr_bytes=sr_bytes, sr_elems=sr_elems, sr_ms=kinds.get("quantize_dy_dual_sr", 0), per_kind_ms=kinds)
 
 
 def lora_grads(F, torch, projs, T, r, stream, dev, flush, args):
