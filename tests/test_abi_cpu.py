@@ -135,3 +135,25 @@ def test_linear_argument_checks(F):
     xT2 = _t(rows=128, cols=128)
     assert L.fp4_linear_bwd(0x1000, 256, 256, 256, ctypes.byref(WT), ctypes.byref(xT2), None, None, 0, 1.0, 0,
                             0x2000, 128, 0x3000, 0, 128, 0x8000, 1 << 30, None) == F.FP4_ERR_INVALID_ARG
+
+
+def test_header_is_plain_c_and_a_c_host_links_the_library(F, tmp_path):
+    # The boundary is a C ABI: the header must compile as C99 (no C++), and a C program that
+    # takes the address of every declared call must link against the shared library.
+    names = header_functions()
+    src = tmp_path / "abi_host.c"
+    src.write_text('#include "nvfp4_gb300.h"\n#include <stdio.h>\n'
+                   "typedef void (*any_fn)(void);\n"
+                   "int main(void) {\n  any_fn fns[] = {\n" +
+                   "".join(f"    (any_fn)&{n},\n" for n in names) +
+                   "  };\n  printf(\"%d\\n\", (int)(sizeof(fns) / sizeof(fns[0])));\n"
+                   "  return fp4_scale_bytes(128, 64) == 2048 ? 0 : 1;\n}\n")
+    lib_dir = os.path.dirname(F.LIB_PATH)
+    exe = tmp_path / "abi_host"
+    import subprocess
+    cc = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                         str(src), "-L", lib_dir, "-lnvfp4_gb300", f"-Wl,-rpath,{lib_dir}", "-o", str(exe)],
+                        capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0 and run.stdout.strip() == str(len(names)), run.stdout + run.stderr
