@@ -147,7 +147,7 @@ def test_header_is_plain_c_and_a_c_host_links_the_library(F, tmp_path):
                    "int main(void) {\n  any_fn fns[] = {\n" +
                    "".join(f"    (any_fn)&{n},\n" for n in names) +
                    "  };\n  printf(\"%d\\n\", (int)(sizeof(fns) / sizeof(fns[0])));\n"
-                   "  return fp4_scale_bytes(128, 64) == 2048 ? 0 : 1;\n}\n")
+                   "  return fp4_scale_bytes(128, 64) == 512 ? 0 : 1;  /* 128 rows x 4 scale bytes */\n}\n")
     lib_dir = os.path.dirname(F.LIB_PATH)
     exe = tmp_path / "abi_host"
     import subprocess
