@@ -112,12 +112,22 @@ fp4_status fp4_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t 
                              uint32_t sr_stream_col, const float* amax_opt,
                              fp4_tensor* out_row, fp4_tensor* out_col, void* stream);
 
-/* Block-scaled NVFP4 GEMM with the fused BF16 low-rank branch:
- *   C[m][n] = S_tA * S_tB * sum_k A[m][k] B[n][k]  +  beta * sum_j P[m][j] Q[n][j]
+/* Block-scaled NVFP4 GEMM with the fused BF16 low-rank branch.  In exact
+ * arithmetic it is
+ *   C[m][n] = S_tA * S_tB * sum_k A[m][k] B[n][k]  +  beta * sum_j P[m][j] Q[n][j];
+ * what it computes is that sum with the branch folded into the residual's
+ * FP32 accumulator, so the output is rounded once:
+ *   alpha = fl32(S_tA * S_tB)   (alpha = 1 when that product is 0)
+ *   P~[m][j] = bf16(fl32(P[m][j] * fl32(beta / alpha)))
+ *   C[m][n] = round_c(fl32(alpha * acc)),  acc = sum_k A B + sum_j P~ Q  (FP32)
+ * with A, B their dequantized E2M1 x E4M3 values (exact products), round_c the
+ * RN-even conversion to C's type.  P~ adds one BF16 rounding to the branch
+ * beyond the BF16 P and Q themselves (relative 2^-9 at most per element of P).
  * A: M x K NVFP4, B: N x K NVFP4 (both blocks along K), P: M x r BF16 (pitch r),
  * Q: N x r BF16 (pitch r); r in {0, 16, 32, 48, 64} (r = 0: P, Q ignored).
  * C: M x N, BF16 or FP32 (c_dtype), pitch ldc elements.
- * Requires M % 128 == 0, N % 128 == 0, K % 64 == 0.
+ * Requires M % 128 == 0, N % 128 == 0, K % 64 == 0, and S_tA * S_tB not
+ * below the FP32 normal range unless one of them is 0.
  * Passage: section 2.1 "Mechanism" (residual in NVFP4, subspace in BF16,
  * added into the same output). */
 fp4_status fp4_gemm_blockscaled(const fp4_tensor* A, const fp4_tensor* B,
@@ -141,6 +151,8 @@ size_t fp4_linear_bwd_workspace(int64_t M, int64_t N, int64_t K, int r);
 
 /* Linear projection forward (section 2.1):
  *   Y = X W^T = S_tX S_tW Xq Wq^T + beta * bf16(X L1^T) L2^T      (M x N, BF16)
+ * (the GEMM of fp4_gemm_blockscaled with P = bf16(X L1^T), Q = L2: the same
+ * branch fold and single rounding of Y)
  * X: M x K BF16 (pitch ldx); Wq: N x K NVFP4 (RTN-quantized W_res, prepared by
  * the caller, reused across micro-batches); L1: r x K, L2: N x r BF16.
  * X is quantized RTN in both orientations from one read; the column form
@@ -170,8 +182,10 @@ fp4_status fp4_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx,
  * Nothing in the scratch has to start at zero: each call zeroes what it
  * reduces into (the amax slot) before use and overwrites the rest.
  * The first call on each device looks the buffer's address up
- * (cudaGetSymbolAddress, which can load the module) and caches it; make that
- * first call on each device before any stream capture begins.
+ * (cudaGetSymbolAddress, which can load the module) and caches it for the
+ * life of the process; make that first call on each device before any stream
+ * capture begins.  cudaDeviceReset unloads the module and leaves the cached
+ * address stale: do not use this call after resetting a device it has run on.
  * All calls on one device share the one buffer: calls whose executions can
  * overlap (unordered streams, several host threads) race on it and give wrong
  * results.  Order them (one stream, or events). */

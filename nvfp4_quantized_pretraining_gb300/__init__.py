@@ -130,6 +130,42 @@ def _bf16_2d(x: torch.Tensor, name: str):
     return x.shape[0], x.shape[1], x.stride(0)
 
 
+def _check_out(t: torch.Tensor, shape, dtypes, device, name: str) -> None:
+    """A caller-owned output: exact shape and dtype, on ``device``, unit column stride."""
+    if not isinstance(dtypes, tuple):
+        dtypes = (dtypes,)
+    if (t.dim() != 2 or tuple(t.shape) != tuple(shape) or t.dtype not in dtypes or t.device != device
+            or t.stride(1) != 1 or t.stride(0) < shape[1]):
+        raise ValueError(f"{name} must be a {shape[0]} x {shape[1]} {'/'.join(str(d) for d in dtypes)} tensor on "
+                         f"{device} with unit column stride (got {tuple(t.shape)} {t.dtype} on {t.device}, "
+                         f"strides {t.stride()})")
+
+
+def _check_factor(t, shape, device, name: str) -> None:
+    """A LoRA factor read by the kernels with a pitch equal to its width: contiguous BF16."""
+    if (t.dtype != torch.bfloat16 or t.device != device or not t.is_contiguous()
+            or tuple(t.shape) != tuple(shape)):
+        raise ValueError(f"{name} must be a contiguous {shape[0]} x {shape[1]} bfloat16 tensor on {device} "
+                         f"(got {tuple(t.shape)} {t.dtype} on {t.device})")
+
+
+def _check_qtensor(q, rows: int, cols: int, name: str) -> None:
+    if (q.rows, q.cols) != (rows, cols):
+        raise ValueError(f"{name} is {q.rows} x {q.cols}, expected {rows} x {cols}")
+
+
+def _branch_factors(L1, L2, N: int, K: int, device):
+    """Rank of the branch (0 without one) after checking L1 (r x K) and L2 (N x r)."""
+    if L1 is None and L2 is None:
+        return 0
+    if L1 is None or L2 is None:
+        raise ValueError("L1 and L2 must both be given or both be None")
+    r = L1.shape[0]
+    _check_factor(L1, (r, K), device, "L1")
+    _check_factor(L2, (N, r), device, "L2")
+    return r
+
+
 def scale_bytes(rows: int, cols: int) -> int:
     return int(lib().fp4_scale_bytes(rows, cols))
 
@@ -202,6 +238,10 @@ def fp4_gemm_blockscaled(A: NVFP4Tensor, B: NVFP4Tensor, P=None, Q=None, beta=1.
     r = 0 if P is None else P.shape[1]
     if out is None:
         out = torch.empty((A.rows, B.rows), dtype=out_dtype, device=A.codes.device)
+    _check_out(out, (A.rows, B.rows), (torch.bfloat16, torch.float32), A.codes.device, "out")
+    if r:
+        _check_factor(P, (A.rows, r), A.codes.device, "P")
+        _check_factor(Q, (B.rows, r), A.codes.device, "Q")
     c_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     ca, cb = A.c(), B.c()
     _check(lib().fp4_gemm_blockscaled(ctypes.byref(ca), ctypes.byref(cb), _ptr(P), _ptr(Q), r, float(beta),
@@ -213,7 +253,9 @@ def fp4_branch_factor(X: torch.Tensor, L: torch.Tensor, out=None, amax=None, str
     """P = bf16(X L^T); with ``amax`` (a 1-element float32 device tensor) also max |X|."""
     M, K, ldx = _bf16_2d(X, "X")
     r = L.shape[0]
+    _check_factor(L, (r, K), X.device, "L")
     out = torch.empty((M, r), dtype=torch.bfloat16, device=X.device) if out is None else out
+    _check_factor(out, (M, r), X.device, "out")
     _check(lib().fp4_branch_factor(X.data_ptr(), M, K, ldx, L.data_ptr(), r, out.data_ptr(), _ptr(amax),
                                    _stream(stream)))
     return out
@@ -232,9 +274,12 @@ def fp4_linear_fwd(X, Wq: NVFP4Tensor, L1=None, L2=None, beta=1.0, Y=None, xqT_s
     """Y = X W^T with W = W_res + beta L2 L1 (Wq = NVFP4 of W_res).  Returns (Y, xqT_saved)."""
     M, K, ldx = _bf16_2d(X, "X")
     N = Wq.rows
-    r = 0 if L1 is None else L1.shape[0]
+    _check_qtensor(Wq, N, K, "Wq")
+    r = _branch_factors(L1, L2, N, K, X.device)
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
+    _check_out(Y, (M, N), torch.bfloat16, X.device, "Y")
     xqT_saved = NVFP4Tensor.empty(K, M, X.device) if xqT_saved is None else xqT_saved
+    _check_qtensor(xqT_saved, K, M, "xqT_saved")
     need = linear_fwd_workspace(M, N, K, r)
     workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=X.device) if workspace is None else workspace
     cw, cx = Wq.c(), xqT_saved.c()
@@ -248,7 +293,11 @@ def fp4_linear_fwd_noalloc(X, Wq: NVFP4Tensor, L1, L2, beta, Y, xqT_saved, strea
     """fp4_linear_fwd with the library's static scratch instead of a workspace.
     Y (M x N BF16) and xqT_saved (K x M) are caller-owned; nothing is allocated."""
     M, K, ldx = _bf16_2d(X, "X")
-    r = 0 if L1 is None else L1.shape[0]
+    N = Wq.rows
+    _check_qtensor(Wq, N, K, "Wq")
+    r = _branch_factors(L1, L2, N, K, X.device)
+    _check_out(Y, (M, N), torch.bfloat16, X.device, "Y")
+    _check_qtensor(xqT_saved, K, M, "xqT_saved")
     cw, cx = Wq.c(), xqT_saved.c()
     _check(lib().fp4_linear_fwd_noalloc(X.data_ptr(), M, K, ldx, ctypes.byref(cw), _ptr(L1), _ptr(L2), r,
                                         float(beta), Y.data_ptr(), Y.stride(0), ctypes.byref(cx), _stream(stream)))
@@ -260,9 +309,13 @@ def fp4_linear_bwd(dY, WqT: NVFP4Tensor, xqT_saved: NVFP4Tensor, L1=None, L2=Non
     """dX = dY W, dW_res = dY^T X.  Returns (dX, dW)."""
     M, N, lddy = _bf16_2d(dY, "dY")
     K = WqT.rows
-    r = 0 if L1 is None else L1.shape[0]
+    _check_qtensor(WqT, K, N, "WqT")
+    _check_qtensor(xqT_saved, K, M, "xqT_saved")
+    r = _branch_factors(L1, L2, N, K, dY.device)
     dX = torch.empty((M, K), dtype=torch.bfloat16, device=dY.device) if dX is None else dX
     dW = torch.empty((N, K), dtype=dw_dtype, device=dY.device) if dW is None else dW
+    _check_out(dX, (M, K), torch.bfloat16, dY.device, "dX")
+    _check_out(dW, (N, K), (torch.bfloat16, torch.float32), dY.device, "dW")
     need = linear_bwd_workspace(M, N, K, r)
     workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dY.device) if workspace is None else workspace
     cw, cx = WqT.c(), xqT_saved.c()

@@ -241,6 +241,43 @@ static size_t bwd_ws(int64_t M, int64_t N, int64_t K, int r, Carver* c, fp4_tens
   return cv.off;
 }
 
+// Argument checks shared by the two forward entry points.
+static fp4_status check_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx, const fp4_tensor* Wq,
+                                   const void* L1, const void* L2, int r, const fp4_tensor* xqT_saved) {
+  fp4_status st;
+  if ((st = check_bf16_input(X, M, K, ldx, "X"))) return st;
+  if ((st = check_tensor(Wq, "Wq")) || (st = check_tensor(xqT_saved, "xqT_saved"))) return st;
+  if (Wq->cols != K)
+    return fail(FP4_ERR_INVALID_ARG, "Wq has %lld columns, X has K = %lld", (long long)Wq->cols, (long long)K);
+  const int64_t N = Wq->rows;
+  if (xqT_saved->rows != K || xqT_saved->cols != M)
+    return fail(FP4_ERR_INVALID_ARG, "xqT_saved must be K x M (%lld x %lld)", (long long)K, (long long)M);
+  if (M % 128 || N % 128 || K % 64)
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "linear needs M %% 128, N %% 128 == 0 and K %% 64 == 0");
+  if (r > 0 && (!L1 || !L2)) return fail(FP4_ERR_INVALID_ARG, "r > 0 needs L1 and L2");
+  return FP4_OK;
+}
+
+// The forward's launches on a workspace `ws` already checked to hold fwd_ws(M, N, K, r) bytes:
+// the branch factor of X (its read of X also yields max |X|), the dual RTN quantization of X,
+// then the block-scaled GEMM with the fused branch.  With r = 0: amax, quantize, GEMM.
+static fp4_status linear_fwd_on(void* ws, const void* X, int64_t M, int64_t K, int64_t ldx, const fp4_tensor* Wq,
+                                const void* L1, const void* L2, int r, float beta, void* Y, int64_t ldy,
+                                const fp4_tensor* xqT_saved, cudaStream_t s) {
+  fp4_status st;
+  Carver c(ws);
+  fp4_tensor xq;
+  void* P = nullptr;
+  fwd_ws(M, Wq->rows, K, r, &c, &xq, &P);
+  if (r > 0) {
+    if ((st = branch_impl(X, M, K, ldx, L1, r, P, s, &xq.scale[1]))) return st;
+    if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, &xq.scale[1], &xq, xqT_saved, s))) return st;
+  } else if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, nullptr, &xq, xqT_saved, s))) {
+    return st;
+  }
+  return gemm_impl(&xq, Wq, P, L2, r, beta, Y, FP4_OUT_BF16, ldy, s);
+}
+
 // Workspace of fp4_newton_schulz: the iterate's two NVFP4 forms, the m x m Gram
 // matrix (B overwrites it), A's NVFP4 form and A^2 when c != 0, B's NVFP4 form,
 // the m x n product B X, the magnitude histogram, the norm's partial sums and a
@@ -282,7 +319,8 @@ constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of g_noalloc_scratch on the current device, looked up on the
-// first call per device and cached.
+// first call per device and cached for the life of the process (a
+// cudaDeviceReset unloads the module, after which the cached address is stale).
 static fp4_status noalloc_scratch(void** out) {
   int dev = 0;
   CUDA_TRY(cudaGetDevice(&dev));
@@ -359,49 +397,20 @@ size_t fp4_linear_bwd_workspace(int64_t M, int64_t N, int64_t K, int r) {
 fp4_status fp4_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx, const fp4_tensor* Wq, const void* L1,
                           const void* L2, int r, float beta, void* Y, int64_t ldy, fp4_tensor* xqT_saved, void* ws,
                           size_t ws_bytes, void* stream) {
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   fp4_status st;
-  if ((st = check_bf16_input(X, M, K, ldx, "X"))) return st;
-  if ((st = check_tensor(Wq, "Wq")) || (st = check_tensor(xqT_saved, "xqT_saved"))) return st;
-  if (Wq->cols != K) return fail(FP4_ERR_INVALID_ARG, "Wq has %lld columns, X has K = %lld", (long long)Wq->cols, (long long)K);
-  const int64_t N = Wq->rows;
-  if (xqT_saved->rows != K || xqT_saved->cols != M)
-    return fail(FP4_ERR_INVALID_ARG, "xqT_saved must be K x M (%lld x %lld)", (long long)K, (long long)M);
-  if (M % 128 || N % 128 || K % 64)
-    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "linear needs M %% 128, N %% 128 == 0 and K %% 64 == 0");
-  if (r > 0 && (!L1 || !L2)) return fail(FP4_ERR_INVALID_ARG, "r > 0 needs L1 and L2");
-  const size_t need = fp4_linear_fwd_workspace(M, N, K, r);
+  if ((st = check_linear_fwd(X, M, K, ldx, Wq, L1, L2, r, xqT_saved))) return st;
+  const size_t need = fp4_linear_fwd_workspace(M, Wq->rows, K, r);
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
     return fail(FP4_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
-  Carver c(ws);
-  fp4_tensor xq;
-  void* P = nullptr;
-  fwd_ws(M, N, K, r, &c, &xq, &P);
-  if (r > 0) {
-    // the branch factor's read of X also yields max |X| for the quantizer (no separate amax pass)
-    if ((st = branch_impl(X, M, K, ldx, L1, r, P, s, &xq.scale[1]))) return st;
-    if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, &xq.scale[1], &xq, xqT_saved, s))) return st;
-  } else if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, nullptr, &xq, xqT_saved, s))) {
-    return st;
-  }
-  return gemm_impl(&xq, Wq, P, L2, r, beta, Y, FP4_OUT_BF16, ldy, s);
+  return linear_fwd_on(ws, X, M, K, ldx, Wq, L1, L2, r, beta, Y, ldy, xqT_saved, static_cast<cudaStream_t>(stream));
 }
 
 fp4_status fp4_linear_fwd_noalloc(const void* X, int64_t M, int64_t K, int64_t ldx, const fp4_tensor* Wq,
                                   const void* L1, const void* L2, int r, float beta, void* Y, int64_t ldy,
                                   fp4_tensor* xqT_saved, void* stream) {
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   fp4_status st;
-  if ((st = check_bf16_input(X, M, K, ldx, "X"))) return st;
-  if ((st = check_tensor(Wq, "Wq")) || (st = check_tensor(xqT_saved, "xqT_saved"))) return st;
-  if (Wq->cols != K) return fail(FP4_ERR_INVALID_ARG, "Wq has %lld columns, X has K = %lld", (long long)Wq->cols, (long long)K);
-  const int64_t N = Wq->rows;
-  if (xqT_saved->rows != K || xqT_saved->cols != M)
-    return fail(FP4_ERR_INVALID_ARG, "xqT_saved must be K x M (%lld x %lld)", (long long)K, (long long)M);
-  if (M % 128 || N % 128 || K % 64)
-    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "linear needs M %% 128, N %% 128 == 0 and K %% 64 == 0");
-  if (r > 0 && (!L1 || !L2)) return fail(FP4_ERR_INVALID_ARG, "r > 0 needs L1 and L2");
-  const size_t need = fp4_linear_fwd_workspace(M, N, K, r);
+  if ((st = check_linear_fwd(X, M, K, ldx, Wq, L1, L2, r, xqT_saved))) return st;
+  const size_t need = fp4_linear_fwd_workspace(M, Wq->rows, K, r);
   if (need > kNoAllocScratchBytes)
     return fail(FP4_ERR_WORKSPACE,
                 "fp4_linear_fwd_noalloc: M = %lld, K = %lld, r = %d needs %zu bytes of scratch but the static "
@@ -409,18 +418,7 @@ fp4_status fp4_linear_fwd_noalloc(const void* X, int64_t M, int64_t K, int64_t l
                 (long long)M, (long long)K, r, need, kNoAllocScratchBytes);
   void* ws = nullptr;
   if ((st = noalloc_scratch(&ws))) return st;
-  Carver c(ws);
-  fp4_tensor xq;
-  void* P = nullptr;
-  fwd_ws(M, N, K, r, &c, &xq, &P);
-  if (r > 0) {
-    // the branch factor's read of X also yields max |X| for the quantizer (no separate amax pass)
-    if ((st = branch_impl(X, M, K, ldx, L1, r, P, s, &xq.scale[1]))) return st;
-    if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, &xq.scale[1], &xq, xqT_saved, s))) return st;
-  } else if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, nullptr, &xq, xqT_saved, s))) {
-    return st;
-  }
-  return gemm_impl(&xq, Wq, P, L2, r, beta, Y, FP4_OUT_BF16, ldy, s);
+  return linear_fwd_on(ws, X, M, K, ldx, Wq, L1, L2, r, beta, Y, ldy, xqT_saved, static_cast<cudaStream_t>(stream));
 }
 
 fp4_status fp4_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t lddy, const fp4_tensor* WqT,

@@ -25,20 +25,18 @@
 namespace nvfp4 {
 
 // ---------------------------------------------------------------------------
-// Block-scaled NVFP4 GEMM
+// Block-scaled NVFP4 GEMM, one CTA per 128 x 128 tile (shapes whose M or N is
+// an odd multiple of 128; multiples of 256 take the CTA-pair kernel below)
 //
-// Tile 128 x 128 per CTA, 256 K elements per pipeline stage.  CTAs form CM x CN
-// clusters: the CM CTAs of a cluster column share one B tile and the CN CTAs
-// of a cluster row share one A tile; each CTA loads 1/CN of its A tile and
-// 1/CM of its B tile (codes and block scales) with TMA multicast into every
-// CTA that needs it, so L2 delivers each operand byte once per cluster.
-// Block scales reach tensor memory through tcgen05.st from four "scale" warps
-// (one per TMEM lane quadrant) instead of tcgen05.cp on the tensor pipe.  For
-// output rows m in lane quadrant q = m / 32, the MMA reads the scales of A row
-// m from lane m, column (base + q), and the scales of B row n from lane
-// 32q + n % 32, column (base + n / 32); the byte is the 16-element block
-// within the 64-wide K step.  So A scales are written once (the diagonal) and
-// B scales once per quadrant.
+// 256 K elements per pipeline stage; each CTA loads its own A and B tiles and
+// their block scales with plain TMA / bulk copies and walks its tiles
+// persistently.  Block scales reach tensor memory through tcgen05.st from four
+// "scale" warps (one per TMEM lane quadrant) instead of tcgen05.cp on the
+// tensor pipe.  For output rows m in lane quadrant q = m / 32, the MMA reads
+// the scales of A row m from lane m, column (base + q), and the scales of B
+// row n from lane 32q + n % 32, column (base + n / 32); the byte is the
+// 16-element block within the 64-wide K step.  So A scales are written once
+// (the diagonal) and B scales once per quadrant.
 // ---------------------------------------------------------------------------
 namespace g4 {
 constexpr int BM = 128;             // rows of A per tile (tcgen05 M=128)
@@ -83,13 +81,11 @@ struct GemmParams {
   int raster_n;
 };
 
-template <int CM, int CN>
 __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_p, const __grid_constant__ CUtensorMap tmap_q,
                      const GemmParams p) {
   using namespace g4;
-  constexpr int CS = CM * CN;  // CTAs per cluster
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
@@ -102,17 +98,11 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t crank = CS > 1 ? cluster_ctarank() : 0;
-  const uint32_t cx = crank % CM, cy = crank / CM;  // position in the cluster (m, n)
-  uint16_t mask_a = 0, mask_b = 0;                  // CTAs sharing my A tile / my B tile
-  for (int j = 0; j < CN; ++j) mask_a |= (uint16_t)(1u << (cx + CM * j));
-  for (int i = 0; i < CM; ++i) mask_b |= (uint16_t)(1u << (i + CM * cy));
-  const uint16_t mask_all = (uint16_t)((1u << CS) - 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CS);  // one commit from every CTA of the cluster
+      mbar_init(&empty[s], 1);
       mbar_init(&sf_ready[s], 4);
     }
     for (int b = 0; b < 2; ++b) {
@@ -133,14 +123,12 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
   }
   if (warp == 1) tmem_alloc(tmem_slot, TM_COLS);
   tc_fence_before();
-  if (CS > 1) cluster_sync();  // every CTA's barriers exist before any multicast lands
-  else __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // macro tiles of (CM*128) x (CN*128); the cluster walks them persistently
-  const uint32_t cluster_id = blockIdx.x / CS, num_clusters = gridDim.x / CS;
-  const uint32_t macro_m = p.num_m / CM, num_macro = macro_m * (p.num_n / CN);
+  // 128 x 128 output tiles, M fastest; the CTAs walk them persistently
+  const uint32_t num_tiles = p.num_m * p.num_n;
   const uint32_t num_k = (p.K + BK - 1) / BK;
   const bool has_branch = p.r > 0;
   const uint32_t n_iter = num_k + (has_branch ? 1 : 0);
@@ -155,8 +143,8 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
       uint32_t armed_phase[STAGES];
       for (int s = 0; s < STAGES; ++s) armed[s] = 0, armed_phase[s] = 0;
       bool ok = true;
-      for (uint32_t mt = cluster_id; mt < num_macro && ok; mt += num_clusters) {
-        const uint32_t mb = (mt % macro_m) * CM + cx, nb = (mt / macro_m) * CN + cy;
+      for (uint32_t mt = blockIdx.x; mt < num_tiles && ok; mt += gridDim.x) {
+        const uint32_t mb = mt % p.num_m, nb = mt / p.num_m;
         for (uint32_t it = 0; it < n_iter; ++it) {
           if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1)) {
             ok = false;
@@ -172,37 +160,13 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
             const uint32_t nk = krem >= (uint32_t)BK ? BK / 64 : krem / 64;  // 64-wide K steps in this stage
             mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES + 2 * nk * SF_ATOM);
             const int32_t kx = (int32_t)(it * (BK / 2));
-            // A: my 1/CN share of the A tile rows (and of its scale atoms), to the CTAs of my cluster row
-            const uint32_t a_rows = BM / CN, b_rows = BN / CM;
-            if (CN > 1)
-              tma_load_2d_mc(sA + cy * a_rows * 128, &tmap_a, &full[stage], kx, (int32_t)(mb * BM + cy * a_rows),
-                             mask_a);
-            else
-              tma_load_2d(sA, &tmap_a, &full[stage], kx, (int32_t)(mb * BM));
-            if (CM > 1)
-              tma_load_2d_mc(sB + cx * b_rows * 128, &tmap_b, &full[stage], kx, (int32_t)(nb * BN + cx * b_rows),
-                             mask_b);
-            else
-              tma_load_2d(sB, &tmap_b, &full[stage], kx, (int32_t)(nb * BN));
-            // scale atoms of this stage: nk atoms per operand, split between the sharing CTAs
-            const uint8_t* gA = p.a_scales + ((size_t)mb * p.atoms_k + it * (BK / 64)) * SF_ATOM;
-            const uint8_t* gB = p.b_scales + ((size_t)nb * p.atoms_k + it * (BK / 64)) * SF_ATOM;
-            {
-              const uint32_t per = (nk + CN - 1) / CN, a0 = cy * per;
-              const uint32_t cnt = a0 < nk ? min(per, nk - a0) : 0;
-              if (cnt) {
-                if (CN > 1) bulk_load_mc(sSFA + a0 * SF_ATOM, gA + a0 * SF_ATOM, cnt * SF_ATOM, &full[stage], mask_a);
-                else bulk_load(sSFA, gA, cnt * SF_ATOM, &full[stage]);
-              }
-            }
-            {
-              const uint32_t per = (nk + CM - 1) / CM, b0 = cx * per;
-              const uint32_t cnt = b0 < nk ? min(per, nk - b0) : 0;
-              if (cnt) {
-                if (CM > 1) bulk_load_mc(sSFB + b0 * SF_ATOM, gB + b0 * SF_ATOM, cnt * SF_ATOM, &full[stage], mask_b);
-                else bulk_load(sSFB, gB, cnt * SF_ATOM, &full[stage]);
-              }
-            }
+            tma_load_2d(sA, &tmap_a, &full[stage], kx, (int32_t)(mb * BM));
+            tma_load_2d(sB, &tmap_b, &full[stage], kx, (int32_t)(nb * BN));
+            // the scale atoms of this stage: nk consecutive 512-byte atoms per operand
+            bulk_load(sSFA, p.a_scales + ((size_t)mb * p.atoms_k + it * (BK / 64)) * SF_ATOM, nk * SF_ATOM,
+                      &full[stage]);
+            bulk_load(sSFB, p.b_scales + ((size_t)nb * p.atoms_k + it * (BK / 64)) * SF_ATOM, nk * SF_ATOM,
+                      &full[stage]);
           } else {
             mbar_arrive_expect_tx(&full[stage], P_BYTES + Q_BYTES);
             tma_load_2d(sA, &tmap_p, &full[stage], 0, (int32_t)(mb * BM));
@@ -235,7 +199,7 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       uint32_t t = 0;
-      for (uint32_t mt = cluster_id; mt < num_macro && ok; mt += num_clusters, ++t) {
+      for (uint32_t mt = blockIdx.x; mt < num_tiles && ok; mt += gridDim.x, ++t) {
         const uint32_t buf = t & 1;
         if (*abort_flag || !mbar_wait(&acc_empty[buf], ((t >> 1) & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
@@ -258,8 +222,7 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
             for (uint32_t kk = 0; kk < krem / 64; ++kk)
               mma_nvf4(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, tsf + kk * 4, tsf + 16 + kk * 4, (it | kk) != 0);
           }
-          if (CS > 1) tc_commit_mc(&empty[stage], mask_all);
-          else tc_commit(&empty[stage]);
+          tc_commit(&empty[stage]);
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
         if (!ok) break;
@@ -271,8 +234,7 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
           const uint32_t nkb = (uint32_t)(p.r + 15) / 16;
           for (uint32_t kk = 0; kk < nkb; ++kk)
             mma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc_br, 1);
-          if (CS > 1) tc_commit_mc(&empty[stage], mask_all);
-          else tc_commit(&empty[stage]);
+          tc_commit(&empty[stage]);
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
         tc_commit(&acc_full[buf]);
@@ -288,7 +250,7 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
     const uint32_t lane_off = (quad * 32) << 16;
     const float g = __fdiv_rn(p.beta, alpha);
     uint32_t stage = 0, phase = 0;
-    for (uint32_t mt = cluster_id; mt < num_macro; mt += num_clusters) {
+    for (uint32_t mt = blockIdx.x; mt < num_tiles; mt += gridDim.x) {
       bool ok = true;
       for (uint32_t it = 0; it < n_iter; ++it) {
         // every use of a stage (scale-carrying or not) waits for its data and
@@ -359,8 +321,8 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
     // ---------------- epilogue (warps 6..9): C = alpha * acc ----------------
     const uint32_t quad = warp & 3;  // TMEM lanes this warp may access
     uint32_t t = 0;
-    for (uint32_t mt = cluster_id; mt < num_macro; mt += num_clusters, ++t) {
-      const uint32_t mb = (mt % macro_m) * CM + cx, nb = (mt / macro_m) * CN + cy;
+    for (uint32_t mt = blockIdx.x; mt < num_tiles; mt += gridDim.x, ++t) {
+      const uint32_t mb = mt % p.num_m, nb = mt / p.num_m;
       const uint32_t buf = t & 1;
       if (*abort_flag || !mbar_wait_warp(&acc_full[buf], (t >> 1) & 1)) {
         *abort_flag = 1;
@@ -412,8 +374,6 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, TM_COLS);
   }
-  // no CTA leaves while a peer may still multicast into it or arrive on its barriers
-  if (CS > 1) cluster_sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -1139,54 +1099,21 @@ static bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int CM, int CN>
-static cudaError_t launch_gemm_cluster(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tp,
-                                       const CUtensorMap& tq, const GemmParams& p, int num_sms, cudaStream_t s) {
+static cudaError_t launch_gemm_single(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tp,
+                                      const CUtensorMap& tq, const GemmParams& p, int num_sms, cudaStream_t s) {
   using namespace g4;
-  constexpr int CS = CM * CN;
-  auto kern = gemm_nvf4_kernel<CM, CN>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  static int max_clusters = 0;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (attr_err != cudaSuccess) return;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
-    cfg.gridDim = dim3(num_sms / CS * CS);
-    cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = CS;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    if (CS > 1) {
-      if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess || max_clusters <= 0)
-        max_clusters = num_sms / CS;
-    } else {
-      max_clusters = num_sms;
-    }
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const uint32_t macro = (p.num_m / CM) * (p.num_n / CN);
-  const uint32_t clusters = macro < (uint32_t)max_clusters ? macro : (uint32_t)max_clusters;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[1];
-  cfg.gridDim = dim3(clusters * CS);
-  cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cfg.stream = s;
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = CS;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = CS > 1 ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tp, tq, p);
+  // one CTA per SM (its shared memory allows no more), at most one per tile
+  const uint32_t tiles = p.num_m * p.num_n;
+  const uint32_t grid = tiles < (uint32_t)num_sms ? tiles : (uint32_t)num_sms;
+  gemm_nvf4_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, tp, tq, p);
   count_launch();
-  return e;
+  return cudaGetLastError();
 }
 
 static cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tp,
@@ -1256,11 +1183,9 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
       return cudaErrorInvalidValue;
     return launch_gemm_pair(ta, tb, tp, tq, tc, p, num_sms, s);
   }
-  const int cm = (g.M % (2 * BM) == 0) ? 2 : 1;
-  const int cn = (g.N % (2 * BN) == 0) ? 2 : 1;
   CUtensorMap ta, tb, tp, tq;
-  if (!make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_codes, g.K / 2, g.M, g.K / 2, BK / 2, BM / cn) ||
-      !make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_codes, g.K / 2, g.N, g.K / 2, BK / 2, BN / cm))
+  if (!make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_codes, g.K / 2, g.M, g.K / 2, BK / 2, BM) ||
+      !make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_codes, g.K / 2, g.N, g.K / 2, BK / 2, BN))
     return cudaErrorInvalidValue;
   if (g.r > 0) {
     if (!make_tmap(&tp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.P, g.r, g.M, (uint64_t)g.r * 2, BR_K, BM) ||
@@ -1287,10 +1212,7 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
   p.c_f32 = g.c_f32;
   p.ldc = g.ldc;
   p.raster_n = 0;
-  if (cm == 2 && cn == 2) return launch_gemm_cluster<2, 2>(ta, tb, tp, tq, p, num_sms, s);
-  if (cm == 2) return launch_gemm_cluster<2, 1>(ta, tb, tp, tq, p, num_sms, s);
-  if (cn == 2) return launch_gemm_cluster<1, 2>(ta, tb, tp, tq, p, num_sms, s);
-  return launch_gemm_cluster<1, 1>(ta, tb, tp, tq, p, num_sms, s);
+  return launch_gemm_single(ta, tb, tp, tq, p, num_sms, s);
 }
 
 cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ldx, const void* L, int r, void* P,
