@@ -55,7 +55,7 @@ WORKLOADS = {
 # keyed by the SHA-256 of the kernel source it was captured on (null once the
 # source changes).  Filled from the committed profile summary.
 GEMM_TRAFFIC = {
-    # profiles/gemm_nvf4_pair_block3b_dram.md: 24 launches (two steps), mean read + write per launch
+    # ncu capture of the bench workload: mean dram read + write bytes per launch
     "8bf1038430f07168": 213556309,
 }
 
@@ -168,13 +168,26 @@ def whole_job_tflops(flops_per_rank_step: float, world: int, ms_per_step: float)
 # our arm
 # ---------------------------------------------------------------------------
 
+def lora_split(F, torch, S, W, r, seed, dev):
+    """The LoRA-SVD split W = W_res + L2 L1 of a random-init weight, made on the device by the
+    library's randomized-SVD realignment (W_res = W, zero factors in; sketch r + 16, 2 power
+    iterations).  Set-up, outside every timed region."""
+    N, K = W.shape
+    Om = S.normal_device((K, r + REALIGN_OVERSAMPLE), 1.0, seed, dev)
+    z1 = torch.zeros((r, K), dtype=torch.bfloat16, device=dev)
+    z2 = torch.zeros((N, r), dtype=torch.bfloat16, device=dev)
+    Wres, L1, L2, info = F.fp4_lora_realign(W, z1, z2, Om, q=REALIGN_POWER_ITERS)
+    if int(info.item()) != 0:
+        raise RuntimeError(f"LoRA-SVD split of a {N} x {K} weight failed: info = {int(info.item())}")
+    return Wres, L1, L2
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
 
     import nvfp4_quantized_pretraining_gb300 as F
     from nvfp4_quantized_pretraining_gb300 import build as B
-    from nvfp4_quantized_pretraining_gb300 import lora
     from nvfp4_quantized_pretraining_gb300 import synthetic as S
 
     rank, world, local = dist_env()
@@ -192,13 +205,12 @@ def run_ours(args):
     projs = []
     seed0 = 1000 * rank
     for i, (name, N, K) in enumerate(wl["projections"]):
-        W = S.normal((N, K), 0.02, seed0 + 10 * i)
-        Wres, L1, L2 = lora.lora_svd_split_randomized(W, r, seed=seed0 + 10 * i + 1)
+        W = S.normal_device((N, K), 0.02, seed0 + 10 * i, dev)
+        Wres, L1, L2 = lora_split(F, torch, S, W, r, seed0 + 10 * i + 1, dev) if r else (W, None, None)
         X = (S.student_t_device((T, K), 3, seed0 + 10 * i + 2, dev) if wl["x"] == "student_t"
              else S.normal_device((T, K), 1.0, seed0 + 10 * i + 2, dev))
         dY = S.normal_device((T, N), 1e-3, seed0 + 10 * i + 3, dev)
-        p = dict(name=name, N=N, K=K, X=X, dY=dY, Wres=S.bits_to_torch(Wres, dev),
-                 L1=S.bits_to_torch(L1, dev) if r else None, L2=S.bits_to_torch(L2, dev) if r else None)
+        p = dict(name=name, N=N, K=K, X=X, dY=dY, Wres=Wres, L1=L1, L2=L2)
         p["Wq"] = F.NVFP4Tensor.empty(N, K, dev)
         p["WqT"] = F.NVFP4Tensor.empty(K, N, dev)
         p["xqT"] = F.NVFP4Tensor.empty(K, T, dev)
@@ -276,6 +288,8 @@ def run_ours(args):
     ra = lora_realign(F, torch, S, projs, r, stream, dev, flush, args) if r else None
     ns = newton_schulz(F, torch, S, stream, dev, flush, args)
     vt = qadamw_codec(F, torch, projs, stream, dev, flush, args)
+    qsw = quantize_sweep(F, torch, S, stream, dev, flush, args)
+    gsw = gemm_sweep(F, torch, S, stream, dev, flush, args)
 
     # ---- end-to-end: host inputs -> device -> step -> results back to host
     e2e = end_to_end(F, torch, projs, T, r, stream, dev, args, gemm_flops, world)
@@ -295,7 +309,7 @@ def run_ours(args):
         "config": {"workload": wl["name"], "description": wl["desc"], "tokens": T, "rank": r,
                    "l2": "flushed (512 MB write) before every timed step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "tensor", "kernel": "gemm_nvf4_kernel", "achieved": round(gemm_tf, 1),
+        "roofline": {"bound": "tensor", "kernel": "gemm_nvf4_pair_kernel", "achieved": round(gemm_tf, 1),
                      "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(gemm_tf / fp4_peak, 4),
                      "traffic": traffic,
                      "peak_note": f"{pk_kind} bf16 burst {pk['bf16_tflops']} TFLOP/s x {FP4_OVER_BF16:g} "
@@ -309,13 +323,15 @@ def run_ours(args):
                         "achieved_gbs": round(sr_gbs, 1), "hbm_frac": round(sr_gbs / pk["hbm_gbs"], 4),
                         "note": "dY, both forms with SR: bound by the integer ALU pipe (two Philox4x32-10 draws "
                                 "and the SR rule per element; ncu on the 1B MLP dY: ALU pipe 64% busy, issue "
-                                "slots 74%, DRAM 14%, profiles/quantize_dual_and_branch_factor_mlp_up.md)"},
+                                "slots 74%, DRAM 14%)"},
         "breakdown_ms": {k: round(v, 4) for k, v in bd["per_kind_ms"].items()},
         "lora_factor_grads": lg,
         "lora_cholqr": cq,
         "lora_realign": ra,
         "newton_schulz": ns,
         "qadamw_v_codec": vt,
+        "quantize_sweep": qsw,
+        "gemm_sweep": gsw,
         "branch_tflops_counted_separately": round(branch_flops / 1e12, 4),
         "e2e": e2e,
         "gpu_launches": int(launches),
@@ -528,6 +544,10 @@ def run_part(args, F, torch, S, dev):
     projs = [dict(name=n, N=N, K=K) for n, N, K in wl["projections"]]
     if args.part == "newton_schulz":
         res = newton_schulz(F, torch, S, stream, dev, flush, args)
+    elif args.part == "quantize_sweep":
+        res = quantize_sweep(F, torch, S, stream, dev, flush, args)
+    elif args.part == "gemm_sweep":
+        res = gemm_sweep(F, torch, S, stream, dev, flush, args)
     elif args.part == "qadamw_v_codec":
         res = qadamw_codec(F, torch, projs, stream, dev, flush, args)
     else:
@@ -538,6 +558,108 @@ def run_part(args, F, torch, S, dev):
             p["L2"] = S.normal_device((p["N"], r), 0.02, 820 + i, dev)
         res = lora_realign(F, torch, S, projs, r, stream, dev, flush, args)
     print(json.dumps({args.part: res}), flush=True)
+
+
+def _median_ms(torch, stream, flush, fn, reps):
+    """Median CUDA-event time of fn() on `stream`, L2 flushed before each timed call."""
+    fn()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return sorted(ts)[len(ts) // 2]
+
+
+def quantize_sweep(F, torch, S, stream, dev, flush, args):
+    """The standalone quantize sweep: BF16 tensors of 1M, 16M, 64M and 256M elements shaped
+    rows x 4096, N(0, 1) with 0.1% of entries x50; RTN and SR (seed 0); the row form, the
+    transposed (column-block) form and both from one read.  Each call after an L2 flush, in two
+    variants: the quantize kernel alone with the tensor amax supplied, and the full call with the
+    amax pass.  Algorithmic bytes per element: 2 read + 0.5 + 1/16 written per form (2.5625 for
+    one form, 3.125 for both), + 2 for the amax pass."""
+    hbm = float(peaks()[0]["hbm_gbs"])
+    reps = max(3, min(args.steps, 7))
+    out = {}
+    worst = None
+    with torch.cuda.stream(stream):
+        for n in S.QUANT_SWEEP_ELEMS:
+            rows, cols = n // 4096, 4096
+            g = torch.Generator(device=dev)
+            g.manual_seed(600 + rows)
+            x = torch.randn((rows, cols), generator=g, device=dev, dtype=torch.float32)
+            x = torch.where(torch.rand((rows, cols), generator=g, device=dev) < 0.001, x * 50.0, x).to(torch.bfloat16)
+            amax = F.fp4_amax(x, stream=stream)
+            qr, qc = F.NVFP4Tensor.empty(rows, cols, dev), F.NVFP4Tensor.empty(cols, rows, dev)
+            label = f"{n >> 20}M"
+            out[label] = {"shape": [rows, cols]}
+            for mode, mname in ((F.RTN, "rtn"), (F.SR, "sr")):
+                forms = {
+                    "row": (2.5625, lambda a: F.fp4_quantize(x, mode, 0, 0, amax=a, out=qr, stream=stream)),
+                    "transposed": (2.5625, lambda a: F.fp4_quantize_transposed(x, mode, 0, 1, amax=a, out=qc,
+                                                                               stream=stream)),
+                    "dual": (3.125, lambda a: F.fp4_quantize_dual(x, mode, 0, 0, 1, amax=a, out_row=qr, out_col=qc,
+                                                                  stream=stream)),
+                }
+                for form, (bpe, fn) in forms.items():
+                    ms_k = _median_ms(torch, stream, flush, lambda: fn(amax), reps)
+                    ms_a = _median_ms(torch, stream, flush, lambda: fn(None), reps)
+                    gk = bpe * n / (ms_k * 1e-3) / 1e9
+                    ga = (bpe + 2.0) * n / (ms_a * 1e-3) / 1e9
+                    out[label][f"{form}_{mname}"] = {
+                        "ms": round(ms_k, 4), "gbs": round(gk, 1), "frac": round(gk / hbm, 4),
+                        "ms_with_amax": round(ms_a, 4), "gbs_with_amax": round(ga, 1),
+                        "frac_with_amax": round(ga / hbm, 4)}
+                    if n >= (1 << 24) and mode == F.RTN and (worst is None or gk / hbm < worst[0]):
+                        worst = (gk / hbm, f"{label} {form}")
+            del x, qr, qc, amax
+    F.fp4_check_status(stream)
+    return {"bound": "hbm", "peak": hbm, "unit": "GB/s", "sizes": out,
+            "min_rtn_frac_16M_up": None if worst is None else {"frac": round(worst[0], 4), "case": worst[1]},
+            "note": "kernel-only rate with the amax supplied (frac) and the full call with the amax pass "
+                    "(frac_with_amax); algorithmic bytes over the median call time, L2 flushed before each call"}
+
+
+def gemm_sweep(F, torch, S, stream, dev, flush, args):
+    """The block-scaled NVFP4 GEMM shape sweep: M = N = K in {2048, 4096, 8192, 16384}, the
+    16384 x 3072 x 8192 skinny shape and the 3072 x 8192 x 16384 dW shape; operands N(0, 1)
+    quantized RTN, rank 0 and rank 64 (P, Q ~ N(0, 1) BF16), BF16 output.  TFLOP/s counts the
+    2MNK FP4 FLOPs (the rank-64 branch's 2MNr BF16 FLOPs are extra work, not counted); torch's
+    BF16 matmul on the same shapes is reported as context."""
+    pk = peaks()[0]
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
+    reps = max(3, min(args.steps, 7))
+    out = {}
+    with torch.cuda.stream(stream):
+        for (M, N, K) in S.GEMM_SWEEP:
+            g = torch.Generator(device=dev)
+            g.manual_seed(M + 3 * N + 7 * K)
+            A = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+            B = torch.randn((N, K), generator=g, device=dev).to(torch.bfloat16)
+            qa, qb = F.fp4_quantize(A, stream=stream), F.fp4_quantize(B, stream=stream)
+            P = torch.randn((M, 64), generator=g, device=dev).to(torch.bfloat16)
+            Q = torch.randn((N, 64), generator=g, device=dev).to(torch.bfloat16)
+            C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            flops = 2.0 * M * N * K
+            row = {}
+            for r in (0, 64):
+                fn = (lambda: F.fp4_gemm_blockscaled(qa, qb, out=C, stream=stream)) if r == 0 else \
+                     (lambda: F.fp4_gemm_blockscaled(qa, qb, P, Q, out=C, stream=stream))
+                ms = _median_ms(torch, stream, flush, fn, reps)
+                tf = flops / (ms * 1e-3) / 1e12
+                row[f"r{r}"] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / fp4_peak, 4)}
+            ms = _median_ms(torch, stream, flush, lambda: torch.matmul(A, B.t(), out=C), reps)
+            row["torch_bf16_matmul"] = {"ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
+            out[f"{M}x{N}x{K}"] = row
+            del A, B, qa, qb, P, Q, C
+    F.fp4_check_status(stream)
+    return {"bound": "tensor", "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "shapes": out,
+            "note": "gemm_nvf4_pair_kernel; 2MNK FP4 FLOPs over the median call time (L2 flushed); the peak is "
+                    "the measured BF16 burst rate x 6 (nominal dense FP4:BF16 ratio)"}
 
 
 def newton_schulz(F, torch, S, stream, dev, flush, args):
@@ -735,16 +857,43 @@ def oracle_sample(wl, tokens):
 CPU_BASELINE_SECONDS = 10.0  # the oracle sample is repeated until about this much CPU work is timed
 
 
-def cpu_baseline(args, wl):
+def oracle_rate(wl, tokens: int, seconds: float):
+    """Repeats the oracle sample until about `seconds` of work is timed; (TFLOP/s, reps, desc, threads)."""
     total_flops, total_s, reps = 0.0, 0.0, 0
     desc = threads = None
-    while total_s < CPU_BASELINE_SECONDS and reps < 200:
-        flops, dt, desc, threads = oracle_sample(wl, tokens=2048)
+    while total_s < seconds and reps < 200:
+        flops, dt, desc, threads = oracle_sample(wl, tokens=tokens)
         total_flops += flops
         total_s += dt
         reps += 1
-    return {"value": round(total_flops / total_s / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{reps} repetitions of: {desc}", "seconds": round(total_s, 3)}
+    return total_flops / total_s / 1e12, reps, desc, threads, total_s
+
+
+def cpu_baseline(args, wl):
+    """The oracle on the host cores: all cores (OpenMP quantizer, threaded BLAS), then one thread
+    (a child process started with every thread pool at 1)."""
+    value, reps, desc, threads, secs = oracle_rate(wl, 2048, CPU_BASELINE_SECONDS)
+    out = {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+           "sample": f"{reps} repetitions of: {desc}", "seconds": round(secs, 3)}
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               NUMEXPR_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-single-thread", "--workload",
+                            args.workload], env=env, capture_output=True, text=True, timeout=600)
+        out["single_thread"] = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # the all-core figure stands on its own
+        out["single_thread"] = {"error": f"{type(e).__name__}: {e}"}
+    return out
+
+
+def run_oracle_single_thread(args):
+    import oracle
+    oracle.build()
+    oracle.set_threads(1)
+    wl = WORKLOADS[args.workload]
+    value, reps, desc, threads, secs = oracle_rate(wl, 512, 8.0)
+    print(json.dumps({"value": round(value, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                      "sample": f"{reps} repetitions of: {desc}", "seconds": round(secs, 3)}), flush=True)
 
 
 def run_reference(args):
@@ -779,12 +928,16 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="block3b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--part", choices=["all", "step", "newton_schulz", "qadamw_v_codec", "lora_realign"], default="all",
+    ap.add_argument("--oracle-single-thread", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--part", choices=["all", "step", "newton_schulz", "qadamw_v_codec", "lora_realign", "quantize_sweep",
+                             "gemm_sweep"], default="all",
                     help="run one optimizer-side measurement alone (prints its JSON object; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
-    if args.impl == "reference":
+    if args.oracle_single_thread:
+        run_oracle_single_thread(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

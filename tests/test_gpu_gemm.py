@@ -1,12 +1,15 @@
 """GPU parity of the block-scaled NVFP4 GEMM (with the fused BF16 branch) and
 of the BF16 branch-factor GEMM against the oracle's FP64 products of the same
 operands.  Tolerance: relative Frobenius error 1e-3 (FP32 output against the
-FP64 result; BF16 output against the FP64 result rounded to BF16)."""
+FP64 result; BF16 output against the FP64 result rounded to BF16), and every
+element within the FP32-accumulation bound of parity_util (one BF16 step plus
+(K + r) 2^-24 sum |a||b|)."""
 import numpy as np
 import pytest
 import torch
 
 from nvfp4_quantized_pretraining_gb300 import synthetic as S
+from parity_util import assert_elementwise
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -50,13 +53,19 @@ def check_gemm(F, oracle_mod, M, N, K, r, out_dtype, beta, seed, rows=None, a_ki
     torch.cuda.synchronize()
     F.fp4_check_status()
     sel = slice(None) if rows is None else rows
-    ref = oracle_mod.gemm(oa.dequantize(rows), ob.dequantize(), None if P is None else np.ascontiguousarray(P[sel]),
-                          Q, beta, oa.S_t, ob.S_t)
+    dA, dB = oa.dequantize(rows), ob.dequantize()
+    Psel = None if P is None else np.ascontiguousarray(P[sel])
+    exact = oracle_mod.gemm(dA, dB, Psel, Q, beta, oa.S_t, ob.S_t)
     got = C.float().cpu().numpy().astype(np.float64)[sel]
-    if out_dtype == torch.bfloat16:
-        ref = oracle_mod.bf16_to_f32(oracle_mod.bf16_rn(ref)).astype(np.float64)
+    bf16_out = out_dtype == torch.bfloat16
+    ref = oracle_mod.bf16_to_f32(oracle_mod.bf16_rn(exact)).astype(np.float64) if bf16_out else exact
     e = rel(got, ref)
     assert e < TOL, (M, N, K, r, e)
+    abs_sum = np.abs(dA) @ np.abs(dB).T
+    if r:
+        abs_sum += abs(beta) * (np.abs(oracle_mod.bf16_to_f32(Psel).astype(np.float64))
+                                @ np.abs(oracle_mod.bf16_to_f32(Q).astype(np.float64)).T)
+    assert_elementwise(got, exact, abs_sum, K + r, bf16_out, f"GEMM {M}x{N}x{K} r={r}")
     return e
 
 
@@ -116,11 +125,17 @@ def test_gemm_strided_bf16_output_pair_path(F, oracle_mod):
     assert np.all(got[:, :64] == 7.0) and np.all(got[:, 576:] == 7.0)
 
 
-@pytest.mark.parametrize("M,N,K,r", [
-    (4096, 4096, 4096, 0), (4096, 4096, 4096, 64), (16384, 3072, 8192, 64), (3072, 8192, 16384, 0),
-])
+# The block-scaled GEMM shape sweep at full size (M = N = K in {2048, 4096, 8192, 16384}, the
+# 16384 x 3072 x 8192 skinny shape and the 3072 x 8192 x 16384 dW shape), rank 0 and rank 64,
+# through the same launch configuration the benchmark times; 48 sampled output rows.
+GEMM_SWEEP = [(2048, 2048, 2048), (4096, 4096, 4096), (8192, 8192, 8192), (16384, 16384, 16384),
+              (16384, 3072, 8192), (3072, 8192, 16384)]
+
+
+@pytest.mark.parametrize("r", [0, 64])
+@pytest.mark.parametrize("M,N,K", GEMM_SWEEP)
 def test_gemm_full_size_sampled_rows(F, oracle_mod, M, N, K, r):
-    rng = np.random.default_rng(M + N)
+    rng = np.random.default_rng(M + N + r)
     rows = np.sort(rng.choice(M, 48, replace=False))
     check_gemm(F, oracle_mod, M, N, K, r, torch.bfloat16, beta=1.0, seed=17, rows=rows)
 

@@ -195,14 +195,24 @@ def test_strided_input(F, oracle_mod):
     ("mlp_up_dY_sr", (8192, 5632), "grad", 1),
     ("sweep_16M", (4096, 4096), "outliers", 0),
     ("sweep_16M_sr", (4096, 4096), "outliers", 1),
+    ("sweep_64M", (16384, 4096), "outliers", 0),
+    ("sweep_64M_sr", (16384, 4096), "outliers", 1),
+    ("sweep_256M", (65536, 4096), "outliers", 0),
+    ("sweep_256M_sr", (65536, 4096), "outliers", 1),
+    ("block3b_gate_up_dY_sr", (16384, 16384), "grad", 1),
 ])
 def test_quantize_full_size(F, oracle_mod, name, shape, kind, mode):
+    # every code and scale of the full tensor, in the dual form and the single-orientation forms
     x = make_input(shape, kind, seed=21)
-    r, c = F.fp4_quantize_dual(dev(x), round_mode=mode, seed=1)
+    xd = dev(x)
+    r, c = F.fp4_quantize_dual(xd, round_mode=mode, seed=1)
     assert_same_quant(F, r, oracle_mod.quantize(x, mode, seed=1, stream=0), oracle_mod)
     assert_same_quant(F, c, oracle_mod.quantize(x, mode, seed=1, stream=1, transposed=True), oracle_mod)
-    r2 = F.fp4_quantize(dev(x), round_mode=mode, seed=1)
-    assert torch.equal(r2.codes, r.codes) and torch.equal(r2.scales, r.scales)
+    r2 = F.fp4_quantize(xd, round_mode=mode, seed=1)
+    c2 = F.fp4_quantize_transposed(xd, round_mode=mode, seed=1)
+    torch.cuda.synchronize()
+    assert torch.equal(r2.codes, r.codes) and torch.equal(r2.scales, r.scales) and torch.equal(r2.scale, r.scale)
+    assert torch.equal(c2.codes, c.codes) and torch.equal(c2.scales, c.scales) and torch.equal(c2.scale, c.scale)
 
 
 def test_transposed_rejects_partial_row_blocks(F):
