@@ -2,8 +2,8 @@
 of the BF16 branch-factor GEMM against the oracle's FP64 products of the same
 operands.  Tolerance: relative Frobenius error 1e-3 (FP32 output against the
 FP64 result; BF16 output against the FP64 result rounded to BF16), and every
-element within the FP32-accumulation bound of parity_util (one BF16 step plus
-(K + r) 2^-24 sum |a||b|)."""
+element and every 32-column chunk within the bounds of parity_util (one BF16
+step plus (K + r) 2^-23 sum |a||b|; 8e-3 per chunk)."""
 import numpy as np
 import pytest
 import torch
@@ -65,7 +65,7 @@ def check_gemm(F, oracle_mod, M, N, K, r, out_dtype, beta, seed, rows=None, a_ki
     if r:
         abs_sum += abs(beta) * (np.abs(oracle_mod.bf16_to_f32(Psel).astype(np.float64))
                                 @ np.abs(oracle_mod.bf16_to_f32(Q).astype(np.float64)).T)
-    assert_elementwise(got, exact, abs_sum, K + r, bf16_out, f"GEMM {M}x{N}x{K} r={r}")
+    assert_elementwise(got, exact, abs_sum, K + r, bf16_out, f"GEMM {M}x{N}x{K} r={r}", rounded=ref)
     return e
 
 

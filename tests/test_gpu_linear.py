@@ -1,7 +1,7 @@
 """GPU parity of the composed NVFP4 linear projection (forward: Y; backward:
 dX and dW_res) with the LoRA-SVD BF16 branch, through the C ABI, against the
-oracle on the same seeded inputs: relative Frobenius error below 1e-3 and
-every compared element within the FP32-accumulation bound of parity_util."""
+oracle on the same seeded inputs: relative Frobenius error below 1e-3, and every
+compared element and 32-column chunk within the bounds of parity_util."""
 import numpy as np
 import pytest
 import torch
@@ -72,9 +72,9 @@ def run_layer(F, oracle_mod, M, K, N, r, seed, x_kind="normal", dx_rows=None, dw
         sX += abs(beta) * (a64(oracle_mod.branch_factor(np.ascontiguousarray(dY[sel_x]), np.ascontiguousarray(L2.T)))
                            @ a64(L1))
     sW = np.abs(q["dYqT"].dequantize(None if dw_rows is None else dw_rows)) @ np.abs(q["XqT"].dequantize()).T
-    assert_elementwise(got["Y"], Y_ref, sY, K + r, True, "Y")
-    assert_elementwise(got["dX"], dX_ref, sX, N + r, True, "dX")
-    assert_elementwise(got["dW"], dW_ref, sW, M, dw_bf16, "dW")
+    assert_elementwise(got["Y"], Y_ref, sY, K + r, True, "Y", rounded=bf(Y_ref))
+    assert_elementwise(got["dX"], dX_ref, sX, N + r, True, "dX", rounded=bf(dX_ref))
+    assert_elementwise(got["dW"], dW_ref, sW, M, dw_bf16, "dW", rounded=bf(dW_ref) if dw_bf16 else None)
     return errs
 
 
