@@ -3,7 +3,7 @@ of the BF16 branch-factor GEMM against the oracle's FP64 products of the same
 operands.  Tolerance: relative Frobenius error 1e-3 (FP32 output against the
 FP64 result; BF16 output against the FP64 result rounded to BF16), and every
 element and every 32-column chunk within the bounds of parity_util (one BF16
-step plus (K + r) 2^-23 sum |a||b|; 8e-3 per chunk)."""
+step plus (K + r) 2^-24 sum |a||b|; 8e-3 per chunk)."""
 import numpy as np
 import pytest
 import torch
