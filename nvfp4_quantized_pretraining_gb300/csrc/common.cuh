@@ -394,11 +394,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
 // Philox4x32-10 (Salmon et al., SC'11)
 // ---------------------------------------------------------------------------
 // The ten round keys of a (seed lo, seed hi) key: round r uses
-// (k0 + r * 0x9E3779B9, k1 + r * 0xBB67AE85).  Computed once per thread.
+// (k0 + r * 0x9E3779B9, k1 + r * 0xBB67AE85).  Computed once per thread, or once
+// on the host and passed in a kernel's parameters (constant memory, which the
+// XOR instructions read as an operand: no registers held).
 struct PhiloxKeys {
   uint32_t k0[10], k1[10];
 };
-__device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
+__host__ __device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
   PhiloxKeys k;
   uint32_t a = static_cast<uint32_t>(seed), b = static_cast<uint32_t>(seed >> 32);
 #pragma unroll
@@ -469,6 +471,12 @@ __device__ __forceinline__ uint32_t e2m1x4(float a, float b, float c, float d) {
       : "=r"(r)
       : "f"(a), "f"(b), "f"(c), "f"(d));
   return r & 0xFFFFu;
+}
+// Two E2M1 codes (round-to-nearest-even, saturating) in one byte, a in the low nibble.
+__device__ __forceinline__ uint32_t e2m1x2(float a, float b) {
+  uint16_t r;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n cvt.u16.u8 %0, t;\n}\n" : "=h"(r) : "f"(a), "f"(b));
+  return r;
 }
 // Eight E2M1 codes packed into 32 bits, element 0 in the low nibble.
 __device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {

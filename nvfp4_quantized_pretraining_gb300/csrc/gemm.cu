@@ -1099,6 +1099,11 @@ static bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  return make_tmap(m, dt, base, inner, outer, pitch_bytes, box_inner, box_outer, swizzle);
+}
+
 static cudaError_t launch_gemm_single(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tp,
                                       const CUtensorMap& tq, const GemmParams& p, int num_sms, cudaStream_t s) {
   using namespace g4;

@@ -1,10 +1,17 @@
 // Internal launcher declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace nvfp4 {
+
+// 2-D row-major tensor map over a rows x cols matrix (`inner` contiguous elements per row,
+// `outer` rows, row pitch `pitch_bytes`), box box_inner x box_outer, built with the driver's
+// cuTensorMapEncodeTiled (resolved at run time).  False if the driver rejects it.
+bool make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
 // Output buffers of one quantized tensor (device pointers).
 struct QOut {
@@ -20,9 +27,10 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, f
 
 // clip (optional, device, both orientations with RTN only): |x| is clipped to this BF16
 // magnitude pattern before quantization.
+// Persistent TMA-fed kernel over 128 x 128 tiles; `num_sms` sizes its grid.
 cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
                                  uint32_t stream_r, uint32_t stream_c, const float* amax, const QOut* row_out,
-                                 const QOut* col_out, cudaStream_t s, const uint32_t* clip = nullptr);
+                                 const QOut* col_out, cudaStream_t s, const uint32_t* clip, int num_sms);
 cudaError_t launch_debug_convert(const float* in, int64_t n, uint8_t* e2m1, uint8_t* e4m3, cudaStream_t s);
 cudaError_t launch_debug_sr_round(const float* in, const uint16_t* rnd, int64_t n, uint8_t* e2m1, cudaStream_t s);
 

@@ -190,30 +190,10 @@ __global__ void lora_grad_reduce_kernel(const float* __restrict__ partial, uint3
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 lg_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }();
-  return fn;
-}
-
 // A BF16 row-major tensor of `rows` x `cols` (pitch in elements) as 64-column x 64-row boxes.
 static bool lg_tmap(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch) {
-  auto fn = lg_encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {pitch * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)lg::BT};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, cols, rows, pitch * 2, 64, (uint32_t)lg::BT,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 uint32_t lora_grad_splits(int64_t T, int64_t M, int num_sms) {
