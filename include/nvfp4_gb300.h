@@ -237,18 +237,18 @@ fp4_status fp4_lora_factor_grad(const void* A, int64_t T, int64_t M, int64_t lda
  *   B = Ub Sigma V^T;  L2_out = bf16(Q Ub_r Sigma_r / beta);  L1_out = bf16(V_r^T);
  *   W_res_out = bf16(W - beta L2_out L1_out),
  * each L1_out row's largest-magnitude entry made positive (L2_out's column
- * follows).  FP32 arithmetic: cuBLAS SGEMM for the products, Cholesky-QR twice
- * for orth(), a one-CTA Jacobi eigensolver for B B^T.
+ * follows).  FP32 arithmetic: this library's own tiled FP32 GEMM for the
+ * products (outputs with few tiles split over K, the slices added in a fixed
+ * order: deterministic), Cholesky-QR twice for orth(), a one-CTA Jacobi
+ * eigensolver for B B^T.  Allocates nothing.
  * W_res: N x K BF16, row pitch ldw (W_res_out the same); L1: r x K (pitch K);
  * L2: N x r (pitch r); Omega: K x s BF16 test matrix (pitch s), Gaussian,
  * supplied by the caller.  Outputs may be the inputs.  r in {16,32,48,64},
- * s a multiple of 16 in [r, 128], N, K >= s, N K < 2^31, 0 <= q <= 8, beta > 0.
+ * s a multiple of 16 in [r, 128], N, K >= s, N, K < 2^31, 0 <= q <= 8, beta > 0.
  * W must have numerical rank >= s.  info (device int): 0, or nonzero when a
  * Cholesky factorisation failed (then no output is written).
- * ws: fp4_lora_realign_workspace(N, K, r, s) bytes (about 4 N K), 256-byte
- * aligned.  Uses one cuBLAS handle per device, created on the first call and
- * shared: calls on one device must not run concurrently from several host
- * threads (each call sets the handle's stream). */
+ * ws: fp4_lora_realign_workspace(N, K, r, s) bytes (about 4 N K + 8 MB),
+ * 256-byte aligned. */
 size_t fp4_lora_realign_workspace(int64_t N, int64_t K, int r, int s);
 fp4_status fp4_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t ldw,
                             const void* L1, const void* L2, int r, float beta,

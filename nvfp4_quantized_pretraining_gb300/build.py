@@ -63,7 +63,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         msg = "\n".join(" ".join(c) + "\n" + o for c, o in failed)
         raise RuntimeError("nvcc failed:\n" + msg)
     tmp = LIB + f".tmp{os.getpid()}"
-    subprocess.run([nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcublas"], check=True)
+    subprocess.run([nvcc()] + ARCH + ["-shared", "-o", tmp] + objs, check=True)
     os.replace(tmp, LIB)
     return LIB
 

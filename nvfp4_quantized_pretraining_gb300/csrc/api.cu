@@ -110,6 +110,8 @@ static fp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64
       return fail(FP4_ERR_INVALID_ARG, "transposed out is %lld x %lld, expected %lld x %lld",
                   (long long)out_col->rows, (long long)out_col->cols, (long long)cols, (long long)rows);
   }
+  if ((rows + 127) / 128 > 65535)  // one 128-row tile per grid row
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rows %lld too large (at most 65535 x 128)", (long long)rows);
   if (amax_opt && (reinterpret_cast<uintptr_t>(amax_opt) & 3u))
     return fail(FP4_ERR_MISALIGNED, "amax_opt must be 4-byte aligned");
   if (out_row && scale_padded(rows, cols))
@@ -129,7 +131,7 @@ static fp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64
   if (out_row) r = qout(out_row);
   if (out_col) c = qout(out_col);
   CUDA_TRY(launch_quantize_dual(x, rows, cols, ld, sr, seed, sr_row, sr_col, amax, out_row ? &r : nullptr,
-                                out_col ? &c : nullptr, s, clip, sm_count()));
+                                out_col ? &c : nullptr, s, clip));
   return FP4_OK;
 }
 
@@ -602,8 +604,8 @@ fp4_status fp4_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t ldw
       (st = check_bf16_input(L2, N, r, r, "L2")) || (st = check_bf16_input(Omega, K, s, s, "Omega")))
     return st;
   if (N < s || K < s) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "N and K must be at least s");
-  if (N * K >= (int64_t(1) << 31) || N >= (int64_t(1) << 30))
-    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "W too large for the 32-bit BLAS dimensions");
+  if (N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "W dimensions must be below 2^31");
   if (!W_res_out || !L1_out || !L2_out || !info) return fail(FP4_ERR_INVALID_ARG, "outputs and info must be non-NULL");
   if (!aligned16(W_res_out) || !aligned16(L1_out) || !aligned16(L2_out) || (reinterpret_cast<uintptr_t>(info) & 3u))
     return fail(FP4_ERR_MISALIGNED, "outputs must be 16-byte aligned, info 4-byte aligned");

@@ -27,10 +27,9 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, f
 
 // clip (optional, device, both orientations with RTN only): |x| is clipped to this BF16
 // magnitude pattern before quantization.
-// Persistent TMA-fed kernel over 128 x 128 tiles; `num_sms` sizes its grid.
 cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
                                  uint32_t stream_r, uint32_t stream_c, const float* amax, const QOut* row_out,
-                                 const QOut* col_out, cudaStream_t s, const uint32_t* clip, int num_sms);
+                                 const QOut* col_out, cudaStream_t s, const uint32_t* clip = nullptr);
 cudaError_t launch_debug_convert(const float* in, int64_t n, uint8_t* e2m1, uint8_t* e4m3, cudaStream_t s);
 cudaError_t launch_debug_sr_round(const float* in, const uint16_t* rnd, int64_t n, uint8_t* e2m1, cudaStream_t s);
 

@@ -65,22 +65,20 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ 
 }
 
 // ---------------------------------------------------------------------------
-// Dual quantizer: the row-wise form, the column-wise (transposed) form, or both
-// from one read of x.  Persistent CTAs walk the 128 x 128 BF16 tiles of x; a
-// producer warp streams each tile into a ring of shared-memory stages with TMA
-// (two 128-row x 64-column boxes, 128-byte swizzle: the 16-byte chunk c of
-// tile row r sits at chunk c ^ (r & 7) of its box row), so loads of the next
-// tiles overlap the work on the current one.  Eight compute warps produce
-// both forms from the staged tile:
-//   * row form: one thread per 16-element block (block scale computed once);
-//   * column form: one thread per 8-column x 8-row task, the two tasks of a
-//     16-row block in lanes l and l ^ 16 (block maxima combined by a shuffle).
-//     A task's eight columns share, in every row, one Philox counter (the 8
-//     source elements of one group j), so its SR draws are made in registers.
+// Column-wise (transposed) quantization, optionally with the row-wise output
+// from the same read.  A CTA stages a 128-row x 128-column BF16 tile in shared
+// memory (8 coalesced 16-byte loads per thread in flight).  Both forms are
+// then produced from the staged tile: the row form by one thread per 16-element
+// block, the column form by threads that own two adjacent columns (one 4-byte
+// shared load per row yields both, their block maxima in one packed register)
+// and 32 rows, i.e. two 16-row blocks per column.  SR random bits of the column
+// form are drawn in the row-chunk mapping (one Philox call per 8 source
+// elements) and staged beside the tile.
 // ---------------------------------------------------------------------------
 struct DualQuantArgs {
-  uint32_t rows, cols, cpr;  // cpr = cols / 8
-  uint32_t tiles_c, num_tiles;
+  const uint16_t* x;
+  int64_t ld;
+  uint32_t rows, cols, cpr;
   const float* amax;
   // row-wise output (rows x cols)
   uint8_t* codes_r;
@@ -92,248 +90,189 @@ struct DualQuantArgs {
   uint8_t* scales_c;
   float* scale_out_c;
   uint32_t atoms_k_c;
-  PhiloxKeys keys;  // SR: the round keys of the seed
+  uint64_t seed;
   uint32_t stream_r, stream_c;
-  const uint32_t* clip;  // CLIP: |x| is clipped to this BF16 magnitude pattern as the tile is read
+  const uint32_t* clip;  // CLIP: |x| is clipped to this BF16 magnitude pattern as the tile is staged
 };
 
-namespace qd {
-constexpr int TILE = 128;
-constexpr int BOX_C = 64;                     // TMA box: 128 rows x 64 BF16 columns (128-byte rows)
-constexpr int BOX_BYTES = TILE * BOX_C * 2;   // 16 KB
-constexpr int TILE_BYTES = 2 * BOX_BYTES;     // 32 KB
-constexpr int STAGES = 3;
-constexpr int COMPUTE_WARPS = 8;
-constexpr int COMPUTE_THREADS = COMPUTE_WARPS * 32;
-constexpr int THREADS = COMPUTE_THREADS + 32;  // + the TMA producer warp
-constexpr int CTAS_PER_SM = 2;
-constexpr int SMEM_BYTES = STAGES * TILE_BYTES + 1024 /*align*/ + 128 /*barriers*/;
-}  // namespace qd
+constexpr int kTileR = 128, kTileC = 128;
+constexpr int kDualThreads = 256;
 
-// Shared-memory byte offset of the 16-byte chunk holding tile columns 8c .. 8c + 7 (c = 0..15) of tile row r.
-__device__ __forceinline__ uint32_t qd_chunk(uint32_t r, uint32_t c) {
-  return (c >> 3) * qd::BOX_BYTES + r * 128u + ((((c & 7u) ^ (r & 7u))) << 4);
-}
-
-__device__ __forceinline__ uint32_t clip_word(uint32_t w, uint32_t v2) {
-  return (w & 0x80008000u) | __vminu2(w & 0x7FFF7FFFu, v2);
-}
-
-template <bool ROW, bool COL, bool SR, bool CLIP>
-__global__ void __launch_bounds__(qd::THREADS, qd::CTAS_PER_SM)
-    quantize_dual_kernel(const __grid_constant__ CUtensorMap tmap_x, const DualQuantArgs a) {
-  using namespace qd;
-  extern __shared__ uint8_t qsm_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsm_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * TILE_BYTES);
-  uint64_t* empty = full + STAGES;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], COMPUTE_WARPS);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
+template <bool ROW, bool COL, bool SR, bool CLIP = false>
+__global__ void __launch_bounds__(kDualThreads, SR ? 3 : 5) quantize_dual_kernel(const DualQuantArgs a) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  uint16_t(*tile)[kTileC] = reinterpret_cast<uint16_t(*)[kTileC]>(dsm);
+  uint16_t(*rtile)[kTileC] = reinterpret_cast<uint16_t(*)[kTileC]>(dsm + kTileR * kTileC * 2);
   const float amax = *a.amax;
   const float S_t = tensor_scale(amax);
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
     if (ROW && a.scale_out_r) { a.scale_out_r[0] = S_t; a.scale_out_r[1] = amax; }
     if (COL && a.scale_out_c) { a.scale_out_c[0] = S_t; a.scale_out_c[1] = amax; }
   }
+  const uint32_t r0 = blockIdx.y * kTileR, c0 = blockIdx.x * kTileC;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const bool pack4 = (a.cols & 63u) == 0;
+  PhiloxKeys keys;
+  if (SR) keys = philox_keys(a.seed);
+  constexpr int kLoads = kTileR * (kTileC / 8) / kDualThreads;  // 8
 
-  if (warp == COMPUTE_WARPS) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      prefetch_tmap(&tmap_x);
-      uint32_t stage = 0, phase = 0;
-      int armed[STAGES];
-      uint32_t armed_phase[STAGES];
-      for (int s = 0; s < STAGES; ++s) armed[s] = 0, armed_phase[s] = 0;
-      bool ok = true;
-      for (uint32_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
-        if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1)) {
-          ok = false;
-          break;
-        }
-        armed[stage] = 0;
-        const int32_t r0 = (int32_t)((t / a.tiles_c) * TILE), c0 = (int32_t)((t % a.tiles_c) * TILE);
-        uint8_t* dst = smem + stage * TILE_BYTES;
-        mbar_arrive_expect_tx(&full[stage], TILE_BYTES);  // out-of-range parts arrive zero-filled
-        tma_load_2d(dst, &tmap_x, &full[stage], c0, r0);
-        tma_load_2d(dst + BOX_BYTES, &tmap_x, &full[stage], c0 + BOX_C, r0);
-        armed[stage] = 1;
-        armed_phase[stage] = phase;
-        if (++stage == STAGES) stage = 0, phase ^= 1;
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        for (int s = 0; s < STAGES; ++s)  // copies already issued land before the CTA may exit
-          if (armed[s]) mbar_wait(&full[s], armed_phase[s]);
-      }
+  uint4 w[kLoads];
+#pragma unroll
+  for (int i = 0; i < kLoads; ++i) {
+    const int q = tid + i * kDualThreads;
+    const uint32_t row = r0 + (q >> 4), c8 = (c0 >> 3) + (q & 15);
+    w[i] = make_uint4(0, 0, 0, 0);
+    if (row < a.rows && c8 < a.cpr) w[i] = __ldcs(reinterpret_cast<const uint4*>(a.x + row * a.ld + c8 * 8));
+  }
+#pragma unroll
+  for (int i = 0; i < kLoads; ++i) {
+    const int q = tid + i * kDualThreads;
+    const uint32_t row = r0 + (q >> 4), c8 = (c0 >> 3) + (q & 15);
+    if (CLIP) {
+      const uint32_t v2 = *a.clip * 0x10001u;
+      w[i].x = (w[i].x & 0x80008000u) | __vminu2(w[i].x & 0x7FFF7FFFu, v2);
+      w[i].y = (w[i].y & 0x80008000u) | __vminu2(w[i].y & 0x7FFF7FFFu, v2);
+      w[i].z = (w[i].z & 0x80008000u) | __vminu2(w[i].z & 0x7FFF7FFFu, v2);
+      w[i].w = (w[i].w & 0x80008000u) | __vminu2(w[i].w & 0x7FFF7FFFu, v2);
     }
-  } else {
-    // ---------------- compute warps ----------------
-    const uint32_t tid = threadIdx.x;  // 0 .. COMPUTE_THREADS - 1
-    const bool pack4 = (a.cols & 63u) == 0;
-    const uint32_t clip2 = CLIP ? *a.clip * 0x10001u : 0u;
-    uint32_t stage = 0, phase = 0;
-    for (uint32_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
-      if (*abort_flag || !mbar_wait(&full[stage], phase)) {
-        *abort_flag = 1;
-        break;
-      }
-      const uint8_t* tile = smem + stage * TILE_BYTES;
-      const uint32_t r0 = (t / a.tiles_c) * TILE, c0 = (t % a.tiles_c) * TILE;
-
-      if (ROW) {
-        // row form: block b = tid + 256 i covers tile row b / 8, columns 16 (b % 8) .. + 15.  Lanes
-        // 4..7 of every 8 read their second chunk first, so each 8-lane phase of the 128-bit shared
-        // loads touches 8 distinct chunk positions (the two boxes share banks).
-        const int first = (lane >> 2) & 1;
-#pragma unroll(SR ? 1 : 2)
-        for (int i = 0; i < TILE * (TILE / 16) / COMPUTE_THREADS; ++i) {
-          const uint32_t b = tid + COMPUTE_THREADS * i;
-          const uint32_t tr = b >> 3, blk = b & 7;
-          const uint32_t row = r0 + tr, c16 = (c0 >> 4) + blk;
-          const uint4 h0 = *reinterpret_cast<const uint4*>(tile + qd_chunk(tr, 2 * blk + first));
-          const uint4 h1 = *reinterpret_cast<const uint4*>(tile + qd_chunk(tr, 2 * blk + (first ^ 1)));
-          const uint4 wl = first ? h1 : h0, wh = first ? h0 : h1;  // elements 0..7, 8..15
-          uint32_t wd[8] = {wl.x, wl.y, wl.z, wl.w, wh.x, wh.y, wh.z, wh.w};
-          if (CLIP) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) wd[e] = clip_word(wd[e], clip2);
-          }
-          uint32_t m = 0;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) m = __vmaxu2(m, wd[e] & 0x7FFF7FFFu);
-          m = max(m & 0xFFFFu, m >> 16);
-          const BlockScale bs = block_scale(__uint_as_float(m << 16), S_t);
-          float y[2][8];  // elements 0..7 and 8..15
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            y[e >> 2][2 * (e & 3)] = __fmul_rn(bf16_lo(wd[e]), bs.inv);
-            y[e >> 2][2 * (e & 3) + 1] = __fmul_rn(bf16_hi(wd[e]), bs.inv);
-          }
-          if (SR) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const uint4 rr = sr_random(a.keys, a.stream_r, (uint64_t)row * a.cpr + 2 * c16 + hh);
-              const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                y[hh][e] = sr_round(y[hh][e], (e & 1) ? sr_draw_hi(rw[e >> 1]) : sr_draw_lo(rw[e >> 1]));
-            }
-          }
-          const uint32_t lo = e2m1x8(y[0]), hi = e2m1x8(y[1]);
-          const bool valid = row < a.rows && 16 * c16 < a.cols;
-          if (valid) *reinterpret_cast<uint2*>(a.codes_r + (size_t)row * (a.cols >> 1) + c16 * 8) = make_uint2(lo, hi);
-          if (pack4) {
-            // lanes 4k .. 4k+3 hold four consecutive scales of one row
-            const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 1);
-            const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 2);
-            const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 3);
-            if (valid && (lane & 3) == 0)
-              *reinterpret_cast<uint32_t*>(a.scales_r + sf_offset(row, c16, a.atoms_k_r)) =
-                  bs.sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
-          } else if (valid) {
-            a.scales_r[sf_offset(row, c16, a.atoms_k_r)] = static_cast<uint8_t>(bs.sb);
-          }
-        }
-      }
-
-      if (COL) {
-        // column form: task (cg, rb8) = tile columns 8cg .. 8cg+7, tile rows 8rb8 .. 8rb8+7; lanes
-        // 0..15 take cg = 0..15 of one row group, so each 8-lane phase reads 8 distinct chunks of one row
-        const uint32_t cg = lane & 15, hsel = (uint32_t)lane >> 4, rb8 = 2 * warp + hsel;
-        const uint32_t col0 = c0 + 8 * cg, rowbase = r0 + 8 * rb8;
-        // pass 1: block maxima of the 8 columns over this task's 8 rows, then over the 16-row block
-        uint32_t m[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 q = *reinterpret_cast<const uint4*>(tile + qd_chunk(8 * rb8 + i, cg));
-          uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (CLIP) w[e] = clip_word(w[e], clip2);
-            m[e] = __vmaxu2(m[e], w[e] & 0x7FFF7FFFu);
-          }
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) m[e] = __vmaxu2(m[e], __shfl_xor_sync(0xFFFFFFFFu, m[e], 16));
-        // this lane scales columns 4 hsel .. 4 hsel + 3 and takes the partner's multipliers for the rest
-        float inv_mine[4];
-        uint32_t sb_mine[4];
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t mw = m[2 * hsel + (kk >> 1)];  // columns 4 hsel + kk
-          const uint32_t mb = (kk & 1) ? (mw & 0xFFFF0000u) : (mw << 16);
-          const BlockScale bs = block_scale(__uint_as_float(mb), S_t);
-          inv_mine[kk] = bs.inv;
-          sb_mine[kk] = bs.sb;
-        }
-        float inv[8];
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const float other = __shfl_xor_sync(0xFFFFFFFFu, inv_mine[kk], 16);
-          inv[kk] = hsel ? other : inv_mine[kk];
-          inv[4 + kk] = hsel ? inv_mine[kk] : other;
-        }
-        // pass 2, two rows at a time: codes of rows (2p, 2p + 1) of each column go to byte p of its word
-        uint32_t out[8];
-#pragma unroll(SR ? 1 : 4)
-        for (int p = 0; p < 4; ++p) {
-          float y[2][8];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t i = 2 * p + h;
-            const uint4 q = *reinterpret_cast<const uint4*>(tile + qd_chunk(8 * rb8 + i, cg));
-            uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              if (CLIP) w[e] = clip_word(w[e], clip2);
-              y[h][2 * e] = __fmul_rn(bf16_lo(w[e]), inv[2 * e]);
-              y[h][2 * e + 1] = __fmul_rn(bf16_hi(w[e]), inv[2 * e + 1]);
-            }
-            if (SR) {
-              // source elements (rowbase + i, col0 .. col0 + 7): one Philox group
-              const uint4 rr = sr_random(a.keys, a.stream_c, (uint64_t)(rowbase + i) * a.cpr + (col0 >> 3));
-              const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                y[h][k] = sr_round(y[h][k], (k & 1) ? sr_draw_hi(rw[k >> 1]) : sr_draw_lo(rw[k >> 1]));
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t b = e2m1x2(y[0][k], y[1][k]);  // row 2p in the low nibble
-            // byte p of the word <- byte 0 of b (selector 0x3210 with nibble p replaced by 4)
-            out[k] = p == 0 ? b : __byte_perm(out[k], b, (0x3210u & ~(0xFu << (4 * p))) | (4u << (4 * p)));
-          }
-        }
-        if (col0 < a.cols && rowbase < a.rows) {
-          uint8_t* cdst = a.codes_c + (size_t)col0 * (a.rows >> 1) + (rowbase >> 1);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) *reinterpret_cast<uint32_t*>(cdst + (size_t)k * (a.rows >> 1)) = out[k];
-          const uint32_t kb = rowbase >> 4;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            a.scales_c[sf_offset(col0 + 4 * hsel + kk, kb, a.atoms_k_c)] = static_cast<uint8_t>(sb_mine[kk]);
-        }
-      }
-
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-      if (++stage == STAGES) stage = 0, phase ^= 1;
+    *reinterpret_cast<uint4*>(&tile[q >> 4][(q & 15) * 8]) = w[i];
+    if (COL && SR) {
+      // element e of the chunk takes word e/2, low half for even e: in element order
+      // the eight 16-bit draws are exactly the four words as stored
+      *reinterpret_cast<uint4*>(&rtile[q >> 4][(q & 15) * 8]) =
+          sr_random(keys, a.stream_c, (uint64_t)row * a.cpr + c8);
     }
   }
   __syncthreads();
-  if (*abort_flag) {  // a wait expired: let copies still in flight land first
-    if (threadIdx.x == 0) drain_pause();
-    __syncthreads();
+
+  if (ROW) {
+    // row phase: one thread per 16-element block (block b = tid + 256 i: tile row b / 8, block b % 8),
+    // so each block scale is computed once.  The two 16-byte halves are read in a lane-dependent
+    // order (lanes 4..7 of every 8 first take their second half), which keeps the 128-bit shared
+    // reads of each 8-lane phase on distinct banks.
+    const int first = (lane >> 2) & 1;
+#pragma unroll 2
+    for (int i = 0; i < kTileR * (kTileC / 16) / kDualThreads; ++i) {
+      const int b = tid + i * kDualThreads;
+      const int tr = b >> 3, blk = b & 7;
+      const uint32_t row = r0 + tr, c16 = (c0 >> 4) + blk;
+      const uint4 h0 = *reinterpret_cast<const uint4*>(&tile[tr][blk * 16 + first * 8]);
+      const uint4 h1 = *reinterpret_cast<const uint4*>(&tile[tr][blk * 16 + (first ^ 1) * 8]);
+      const uint4 wl = first ? h1 : h0, wh = first ? h0 : h1;  // elements 0..7, 8..15
+      const uint32_t wd[8] = {wl.x, wl.y, wl.z, wl.w, wh.x, wh.y, wh.z, wh.w};
+      uint32_t m = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m = __vmaxu2(m, wd[e] & 0x7FFF7FFFu);
+      m = max(m & 0xFFFFu, m >> 16);
+      const BlockScale bs = block_scale(__uint_as_float(m << 16), S_t);
+      float y[2][8];  // elements 0..7 and 8..15
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        y[e >> 2][2 * (e & 3)] = __fmul_rn(bf16_lo(wd[e]), bs.inv);
+        y[e >> 2][2 * (e & 3) + 1] = __fmul_rn(bf16_hi(wd[e]), bs.inv);
+      }
+      if (SR) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint4 rr = sr_random(keys, a.stream_r, (uint64_t)row * a.cpr + 2 * c16 + hh);
+          const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            y[hh][e] = sr_round(y[hh][e], (e & 1) ? sr_draw_hi(rw[e >> 1]) : sr_draw_lo(rw[e >> 1]));
+        }
+      }
+      const uint32_t lo = e2m1x8(y[0]), hi = e2m1x8(y[1]);
+      const bool valid = row < a.rows && 16 * c16 < a.cols;
+      if (valid) *reinterpret_cast<uint2*>(a.codes_r + (size_t)row * (a.cols >> 1) + c16 * 8) = make_uint2(lo, hi);
+      if (pack4) {
+        // lanes 4k .. 4k+3 hold four consecutive scales of one row
+        const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 1);
+        const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 2);
+        const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, bs.sb, 3);
+        if (valid && (lane & 3) == 0)
+          *reinterpret_cast<uint32_t*>(a.scales_r + sf_offset(row, c16, a.atoms_k_r)) =
+              bs.sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+      } else if (valid) {
+        a.scales_r[sf_offset(row, c16, a.atoms_k_r)] = static_cast<uint8_t>(bs.sb);
+      }
+    }
+  }
+  if (!COL) return;
+
+  // column phase: columns c0 + 2cp, c0 + 2cp + 1; rows r0 + 32rq .. +31 (blocks 2rq .. 2rq+1 of 16)
+  const uint32_t cp = tid & 63, rq = tid >> 6;
+  const uint32_t col = c0 + 2 * cp;
+  if (col >= a.cols) return;
+  const bool has2 = col + 1 < a.cols;
+  uint32_t sbits[2] = {0, 0};
+  uint4 cbuf[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t rb = 2 * rq + h;  // 16-row block within the tile
+    float va[16], vb[16];
+    uint32_t m2 = 0;  // both columns' |bf16| maxima, one per half-word
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t pr = *reinterpret_cast<const uint32_t*>(&tile[rb * 16 + i][2 * cp]);
+      m2 = __vmaxu2(m2, pr & 0x7FFF7FFFu);
+      va[i] = bf16_lo(pr);
+      vb[i] = bf16_hi(pr);
+    }
+    const BlockScale sa = block_scale(__uint_as_float(m2 << 16), S_t);
+    const BlockScale sb = block_scale(__uint_as_float(m2 & 0xFFFF0000u), S_t);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      va[i] = __fmul_rn(va[i], sa.inv);
+      vb[i] = __fmul_rn(vb[i], sb.inv);
+    }
+    if (SR) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t rp = *reinterpret_cast<const uint32_t*>(&rtile[rb * 16 + i][2 * cp]);
+        va[i] = sr_round(va[i], sr_draw_lo(rp));
+        vb[i] = sr_round(vb[i], sr_draw_hi(rp));
+      }
+    }
+    float t8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t8[i] = va[i];
+    const uint32_t a0 = e2m1x8(t8);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t8[i] = va[8 + i];
+    const uint32_t a1 = e2m1x8(t8);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t8[i] = vb[i];
+    const uint32_t b0 = e2m1x8(t8);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t8[i] = vb[8 + i];
+    const uint32_t b1 = e2m1x8(t8);
+    if (h == 0) {
+      cbuf[0].x = a0; cbuf[0].y = a1; cbuf[1].x = b0; cbuf[1].y = b1;
+    } else {
+      cbuf[0].z = a0; cbuf[0].w = a1; cbuf[1].z = b0; cbuf[1].w = b1;
+    }
+    sbits[0] |= sa.sb << (8 * h);
+    sbits[1] |= sb.sb << (8 * h);
+  }
+  const uint32_t rowb = r0 + 32 * rq;  // first source row of this thread's 32
+  const uint32_t kb = rowb >> 4;       // even: kb and kb+1 share one 32-bit scale group
+  if (rowb < a.rows) {
+    const bool two = rowb + 16 < a.rows;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (j == 1 && !has2) break;
+      uint8_t* cdst = a.codes_c + (size_t)(col + j) * (a.rows >> 1) + (rowb >> 1);
+      if (two && (((a.rows >> 1) & 15u) == 0)) {
+        *reinterpret_cast<uint4*>(cdst) = cbuf[j];
+      } else {
+        *reinterpret_cast<uint2*>(cdst) = make_uint2(cbuf[j].x, cbuf[j].y);
+        if (two) *reinterpret_cast<uint2*>(cdst + 8) = make_uint2(cbuf[j].z, cbuf[j].w);
+      }
+      uint8_t* sdst = a.scales_c + sf_offset(col + j, kb, a.atoms_k_c);
+      if (two) *reinterpret_cast<uint16_t*>(sdst) = static_cast<uint16_t>(sbits[j]);
+      else *sdst = static_cast<uint8_t>(sbits[j]);
+    }
   }
 }
 
@@ -393,32 +332,16 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, f
   return cudaGetLastError();
 }
 
-template <bool ROW, bool COL, bool SR, bool CLIP>
-static cudaError_t launch_qd(const CUtensorMap& tm, const DualQuantArgs& a, int num_sms, cudaStream_t s) {
-  using namespace qd;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(quantize_dual_kernel<ROW, COL, SR, CLIP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                SMEM_BYTES);
-  });
-  if (attr != cudaSuccess) return attr;
-  const uint32_t slots = (uint32_t)num_sms * CTAS_PER_SM;
-  const uint32_t grid = a.num_tiles < slots ? a.num_tiles : slots;
-  quantize_dual_kernel<ROW, COL, SR, CLIP><<<grid, THREADS, SMEM_BYTES, s>>>(tm, a);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
                                  uint32_t stream_r, uint32_t stream_c, const float* amax, const QOut* row_out,
-                                 const QOut* col_out, cudaStream_t s, const uint32_t* clip, int num_sms) {
+                                 const QOut* col_out, cudaStream_t s, const uint32_t* clip) {
   DualQuantArgs a{};
   a.clip = clip;
+  a.x = static_cast<const uint16_t*>(x);
+  a.ld = ld;
   a.rows = static_cast<uint32_t>(rows);
   a.cols = static_cast<uint32_t>(cols);
   a.cpr = static_cast<uint32_t>(cols / 8);
-  a.tiles_c = static_cast<uint32_t>((cols + qd::TILE - 1) / qd::TILE);
-  a.num_tiles = a.tiles_c * static_cast<uint32_t>((rows + qd::TILE - 1) / qd::TILE);
   a.amax = amax;
   if (row_out) {
     a.codes_r = static_cast<uint8_t*>(row_out->codes);
@@ -432,28 +355,38 @@ cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int6
     a.scale_out_c = col_out->scale;
     a.atoms_k_c = static_cast<uint32_t>((rows / 16 + 3) / 4);
   }
-  a.keys = philox_keys(seed);
+  a.seed = seed;
   a.stream_r = stream_r;
   a.stream_c = stream_c;
-  // x as 128-row x 64-column boxes with the 128-byte swizzle
-  CUtensorMap tm;
-  if (!make_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)cols, (uint64_t)rows, (uint64_t)ld * 2,
-                    qd::BOX_C, qd::TILE, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>((cols + kTileC - 1) / kTileC), static_cast<unsigned>((rows + kTileR - 1) / kTileR));
   const bool R = row_out != nullptr, C = col_out != nullptr;
-  cudaError_t e;
+  // the BF16 tile is staged for both forms; the SR column form also stages its random bits
+  const int smem = kTileR * kTileC * 2 * ((C && sr) ? 2 : 1);
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(quantize_dual_kernel<true, true, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kTileR * kTileC * 2);
+    if (attr == cudaSuccess)
+      attr = cudaFuncSetAttribute(quantize_dual_kernel<false, true, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kTileR * kTileC * 2);
+  });
+  if (attr != cudaSuccess) return attr;
   if (clip) {  // the clipped form: both orientations, RTN
     if (!(R && C) || sr) return cudaErrorInvalidValue;
-    e = launch_qd<true, true, false, true>(tm, a, num_sms, s);
+    quantize_dual_kernel<true, true, false, true><<<grid, kDualThreads, smem, s>>>(a);
   } else if (R && C) {
-    e = sr ? launch_qd<true, true, true, false>(tm, a, num_sms, s) : launch_qd<true, true, false, false>(tm, a, num_sms, s);
+    if (sr) quantize_dual_kernel<true, true, true><<<grid, kDualThreads, smem, s>>>(a);
+    else quantize_dual_kernel<true, true, false><<<grid, kDualThreads, smem, s>>>(a);
   } else if (C) {
-    e = sr ? launch_qd<false, true, true, false>(tm, a, num_sms, s) : launch_qd<false, true, false, false>(tm, a, num_sms, s);
+    if (sr) quantize_dual_kernel<false, true, true><<<grid, kDualThreads, smem, s>>>(a);
+    else quantize_dual_kernel<false, true, false><<<grid, kDualThreads, smem, s>>>(a);
   } else {
-    e = sr ? launch_qd<true, false, true, false>(tm, a, num_sms, s) : launch_qd<true, false, false, false>(tm, a, num_sms, s);
+    if (sr) quantize_dual_kernel<true, false, true><<<grid, kDualThreads, smem, s>>>(a);
+    else quantize_dual_kernel<true, false, false><<<grid, kDualThreads, smem, s>>>(a);
   }
   count_launch();
-  return e;
+  return cudaGetLastError();
 }
 
 cudaError_t launch_debug_convert(const float* in, int64_t n, uint8_t* e2m1, uint8_t* e4m3, cudaStream_t s) {

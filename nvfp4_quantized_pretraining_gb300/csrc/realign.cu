@@ -6,16 +6,15 @@
 //   Y = W Omega;  q times: Y = W basis(W^T basis(Y));  Q = orth(Y);  B = Q^T W;
 //   B B^T = Ub Lambda Ub^T (Jacobi);  L2 = Q Ub_r Sigma_r / beta;  L1 = Ub_r^T B / Sigma_r;
 //   W_res = W - beta bf16(L2) bf16(L1).
-// FP32 throughout.  The plain products are cuBLAS SGEMMs (row-major operands
-// through the transposed column-major call); orth() is Cholesky-QR (the factor
-// and its inverse in one CTA, Y L^-T as an SGEMM): twice for the final basis,
+// FP32 throughout.  The plain products run in this file's own tiled FP32 GEMM
+// (rl_sgemm_kernel: 64 x 64 output tiles, split over K into a fixed-order sum
+// when the output has few tiles); orth() is Cholesky-QR (the factor and its
+// inverse in one CTA, Y L^-T as a product): twice for the final basis,
 // once between the products of the subspace iteration, which depend on the span
 // only.  The first pass adds a small diagonal shift: the column space is that of
 // Y whatever the triangular factor, so the shift only guards the factorisation
 // of a near-rank-deficient sketch.  The small symmetric eigenproblem is a cyclic
 // Jacobi iteration with round-robin pairs in one CTA.
-#include <cublas_v2.h>
-
 #include <atomic>
 
 #include "bf16_convert.cuh"
@@ -58,6 +57,98 @@ __global__ void __launch_bounds__(kRlThreads) rl_f32_to_bf16(const float* __rest
     out[r * ldo + c] = static_cast<uint16_t>(bf16_rn_bits(v));
   }
 }
+
+// ---------------------------------------------------------------------------
+// FP32 GEMM on row-major operands: C (m x n, ldc) = alpha op(A) op(B) + beta C, op(A) m x k
+// (A stored m x k, or k x m when ta), op(B) k x n (B stored k x n, or n x k when tb).  A CTA
+// of 256 threads computes a 64 x 64 tile, 4 x 4 outputs per thread, over the K slice of
+// blockIdx.z: with one slice it writes C; with several, each slice's sum goes to
+// partial[z] (m x n) and rl_sgemm_reduce adds the slices in order, so the result is
+// deterministic.  Tiles of op(A) and op(B), 16 deep in K, are staged in shared memory
+// k-major; the loads run along whichever dimension is contiguous in memory.
+// ---------------------------------------------------------------------------
+namespace rg {
+constexpr int BM = 64, BN = 64, BK = 16, THREADS = 256;
+}
+
+template <bool TA, bool TB>
+__global__ void __launch_bounds__(rg::THREADS) rl_sgemm_kernel(int64_t m, int64_t n, int64_t k, int64_t kslice,
+                                                              float alpha, const float* __restrict__ A, int64_t lda,
+                                                              const float* __restrict__ B, int64_t ldb, float beta,
+                                                              float* __restrict__ C, int64_t ldc,
+                                                              float* __restrict__ partial) {
+  using namespace rg;
+  __shared__ __align__(16) float As[BK][BM + 4];
+  __shared__ __align__(16) float Bs[BK][BN + 4];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * BM, n0 = static_cast<int64_t>(blockIdx.x) * BN;
+  const int64_t k0 = static_cast<int64_t>(blockIdx.z) * kslice;
+  const int64_t k1 = k0 + kslice < k ? k0 + kslice : k;
+  float acc[4][4] = {};
+  for (int64_t kt = k0; kt < k1; kt += BK) {
+    // 1024 elements of each tile, 4 per thread
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = tid + u * THREADS;
+      int mi, ki;
+      if (TA) { ki = e / BM; mi = e % BM; }  // A stored k x m: contiguous along m
+      else { mi = e / BK; ki = e % BK; }     // A stored m x k: contiguous along k
+      const int64_t gm = m0 + mi, gk = kt + ki;
+      float v = 0.0f;
+      if (gm < m && gk < k1) v = TA ? A[gk * lda + gm] : A[gm * lda + gk];
+      As[ki][mi] = v;
+      int nj, kj;
+      if (TB) { nj = e / BK; kj = e % BK; }  // B stored n x k: contiguous along k
+      else { kj = e / BN; nj = e % BN; }     // B stored k x n: contiguous along n
+      const int64_t gn = n0 + nj, gk2 = kt + kj;
+      float w = 0.0f;
+      if (gn < n && gk2 < k1) w = TB ? B[gn * ldb + gk2] : B[gk2 * ldb + gn];
+      Bs[kj][nj] = w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      const float4 a = *reinterpret_cast<const float4*>(&As[kk][4 * ty]);
+      const float4 b = *reinterpret_cast<const float4*>(&Bs[kk][4 * tx]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  float* out = partial ? partial + static_cast<int64_t>(blockIdx.z) * m * n : nullptr;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t gm = m0 + 4 * ty + i;
+    if (gm >= m) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t gn = n0 + 4 * tx + j;
+      if (gn >= n) continue;
+      if (out) out[gm * n + gn] = acc[i][j];
+      else C[gm * ldc + gn] = beta == 0.0f ? alpha * acc[i][j] : fmaf(alpha, acc[i][j], beta * C[gm * ldc + gn]);
+    }
+  }
+}
+
+// C = alpha (partial[0] + partial[1] + ... + partial[splits - 1]) + beta C, slices added in order.
+__global__ void __launch_bounds__(kRlThreads) rl_sgemm_reduce(int64_t m, int64_t n, int splits, float alpha,
+                                                              const float* __restrict__ partial, float beta,
+                                                              float* __restrict__ C, int64_t ldc) {
+  const int64_t total = m * n;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float s = 0.0f;
+    for (int z = 0; z < splits; ++z) s += partial[z * total + e];
+    const int64_t r = e / n, c = e - r * n;
+    C[r * ldc + c] = beta == 0.0f ? alpha * s : fmaf(alpha, s, beta * C[r * ldc + c]);
+  }
+}
+
+// Elements of split-K scratch the products of one realignment need at most (see Rl::gemm).
+constexpr int64_t kRlSplitFloats = int64_t(1) << 21;
 
 // ---------------------------------------------------------------------------
 // Cholesky of an S x S Gram matrix (S <= 128, a multiple of 16) in one CTA, and
@@ -321,49 +412,47 @@ __global__ void __launch_bounds__(kRlThreads) rl_sign_scale_kernel(const float* 
 // ---------------------------------------------------------------------------
 namespace {
 
-// cuBLAS handle per device, created on first use.
-cublasHandle_t rl_handle(cudaError_t* err) {
-  int dev = 0;
-  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return nullptr;
-  static std::atomic<cublasHandle_t> handles[64];
-  if (dev < 0 || dev >= 64) {
-    *err = cudaErrorInvalidDevice;
-    return nullptr;
-  }
-  cublasHandle_t h = handles[dev].load();
-  if (!h) {
-    cublasHandle_t fresh = nullptr;
-    if (cublasCreate(&fresh) != CUBLAS_STATUS_SUCCESS) {
-      *err = cudaErrorUnknown;
-      return nullptr;
-    }
-    cublasSetMathMode(fresh, CUBLAS_PEDANTIC_MATH);  // FP32 products, no reduced-precision modes
-    cublasHandle_t expected = nullptr;
-    if (!handles[dev].compare_exchange_strong(expected, fresh)) {
-      cublasDestroy(fresh);
-      h = expected;
-    } else {
-      h = fresh;
-    }
-  }
-  return h;
-}
-
 struct Rl {
-  cublasHandle_t h;
   cudaStream_t s;
   int num_sms;
+  float* split;  // kRlSplitFloats of split-K scratch
   cudaError_t err = cudaSuccess;
 
-  // Row-major C (m x n, ldc) = alpha op(A) op(B) + beta C, op(A) m x k, op(B) k x n.
+  // Row-major C (m x n, ldc) = alpha op(A) op(B) + beta C, op(A) m x k, op(B) k x n.  An output
+  // of fewer tiles than two per SM is split over K (slices of at least 512) into the scratch, as
+  // far as it holds the slices.
   void gemm(bool ta, bool tb, int64_t m, int64_t n, int64_t k, float alpha, const float* A, int64_t lda,
             const float* B, int64_t ldb, float beta, float* C, int64_t ldc) {
     if (err != cudaSuccess) return;
-    const cublasStatus_t st =
-        cublasSgemm(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N, static_cast<int>(n),
-                    static_cast<int>(m), static_cast<int>(k), &alpha, B, static_cast<int>(ldb), A,
-                    static_cast<int>(lda), &beta, C, static_cast<int>(ldc));
-    if (st != CUBLAS_STATUS_SUCCESS) err = cudaErrorUnknown;
+    const int64_t tiles = ((m + rg::BM - 1) / rg::BM) * ((n + rg::BN - 1) / rg::BN);
+    int64_t splits = 1;
+    const int64_t want = 2 * static_cast<int64_t>(num_sms);
+    if (tiles < want) {
+      splits = (want + tiles - 1) / tiles;
+      const int64_t by_k = (k + 511) / 512;
+      if (splits > by_k) splits = by_k;
+      const int64_t by_ws = kRlSplitFloats / (m * n);
+      if (splits > by_ws) splits = by_ws;
+      if (splits > 64) splits = 64;
+      if (splits < 1) splits = 1;
+    }
+    int64_t kslice = (k + splits - 1) / splits;
+    kslice = (kslice + rg::BK - 1) / rg::BK * rg::BK;
+    splits = (k + kslice - 1) / kslice;
+    const dim3 grid(static_cast<unsigned>((n + rg::BN - 1) / rg::BN), static_cast<unsigned>((m + rg::BM - 1) / rg::BM),
+                    static_cast<unsigned>(splits));
+    float* part = splits > 1 ? split : nullptr;
+    if (ta && tb) rl_sgemm_kernel<true, true><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    else if (ta) rl_sgemm_kernel<true, false><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    else if (tb) rl_sgemm_kernel<false, true><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    else rl_sgemm_kernel<false, false><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    count_launch();
+    if ((err = cudaGetLastError()) != cudaSuccess) return;
+    if (part) {
+      rl_sgemm_reduce<<<this->grid(m * n), kRlThreads, 0, s>>>(m, n, static_cast<int>(splits), alpha, part, beta, C, ldc);
+      count_launch();
+      err = cudaGetLastError();
+    }
   }
   int grid(int64_t n) const {
     const int64_t b = (n + kRlThreads - 1) / kRlThreads;
@@ -416,16 +505,14 @@ size_t realign_workspace_floats(int64_t N, int64_t K, int r, int s) {
          + static_cast<size_t>(K * s)                       // Omega
          + 5 * static_cast<size_t>(s) * s + 4 * static_cast<size_t>(s)  // G, M, C, evecs, spare; evals, rs, cs, spare
          + static_cast<size_t>(r * K) + static_cast<size_t>(N * r)      // T1, T2
-         + static_cast<size_t>(r * K) + static_cast<size_t>(N * r);     // L1, L2 (FP32)
+         + static_cast<size_t>(r * K) + static_cast<size_t>(N * r)      // L1, L2 (FP32)
+         + static_cast<size_t>(kRlSplitFloats);                         // split-K partial sums
 }
 
 cudaError_t launch_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t ldw, const void* L1, const void* L2,
                                 int r, float beta, const void* Omega, int s_cols, int q, void* W_res_out,
                                 void* L1_out, void* L2_out, int* info, float* ws, int num_sms, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
-  cublasHandle_t h = rl_handle(&e);
-  if (!h) return e;
-  if (cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
   static std::atomic<int> attr_done{0};
   if (!attr_done.load()) {
     const int jac = (2 * kRlMaxS * (kRlMaxS + 1) + 2 * kRlMaxS) * 4;
@@ -450,9 +537,10 @@ cudaError_t launch_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t
   float* T2 = T1 + static_cast<int64_t>(r) * K;
   float* L1f = T2 + N * r;
   float* L2f = L1f + static_cast<int64_t>(r) * K;
+  float* split = L2f + N * r;
 
   if ((e = cudaMemsetAsync(info, 0, sizeof(int), st)) != cudaSuccess) return e;
-  Rl rl{h, st, num_sms};
+  Rl rl{st, num_sms, split};
   // W = W_res + beta L2 L1 (FP32)
   rl.to_f32(W_res, ldw, W, K, N, K);
   rl.to_f32(L1, K, L1f, K, r, K);
