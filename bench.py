@@ -546,6 +546,8 @@ def run_part(args, F, torch, S, dev):
         res = newton_schulz(F, torch, S, stream, dev, flush, args)
     elif args.part == "quantize_sweep":
         res = quantize_sweep(F, torch, S, stream, dev, flush, args)
+    elif args.part == "quantize_one":
+        res = quantize_one(F, torch, stream, dev, flush, args)
     elif args.part == "gemm_sweep":
         res = gemm_sweep(F, torch, S, stream, dev, flush, args)
     elif args.part == "qadamw_v_codec":
@@ -622,6 +624,33 @@ def quantize_sweep(F, torch, S, stream, dev, flush, args):
             "min_rtn_frac_16M_up": None if worst is None else {"frac": round(worst[0], 4), "case": worst[1]},
             "note": "kernel-only rate with the amax supplied (frac) and the full call with the amax pass "
                     "(frac_with_amax); algorithmic bytes over the median call time, L2 flushed before each call"}
+
+
+def quantize_one(F, torch, stream, dev, flush, args):
+    """One quantize call on an N(0, 1) tensor of --qshape with 0.1% of entries x50 (--qform row,
+    transposed or dual; --qmode rtn or sr), amax supplied: `steps` warm-up calls, then one timed
+    call after an L2 flush.  For profiling a single launch of the quantizer."""
+    rows, cols = args.qshape
+    g = torch.Generator(device=dev)
+    g.manual_seed(601)
+    x = torch.randn((rows, cols), generator=g, device=dev, dtype=torch.float32)
+    x = torch.where(torch.rand((rows, cols), generator=g, device=dev) < 0.001, x * 50.0, x).to(torch.bfloat16)
+    amax = F.fp4_amax(x, stream=stream)
+    mode = F.SR if args.qmode == "sr" else F.RTN
+    qr, qc = F.NVFP4Tensor.empty(rows, cols, dev), F.NVFP4Tensor.empty(cols, rows, dev)
+    fn = {"row": lambda: F.fp4_quantize(x, mode, 0, 0, amax=amax, out=qr, stream=stream),
+          "transposed": lambda: F.fp4_quantize_transposed(x, mode, 0, 1, amax=amax, out=qc, stream=stream),
+          "dual": lambda: F.fp4_quantize_dual(x, mode, 0, 0, 1, amax=amax, out_row=qr, out_col=qc,
+                                              stream=stream)}[args.qform]
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            fn()
+        ms = _median_ms(torch, stream, flush, fn, 1)
+    F.fp4_check_status(stream)
+    bpe = 3.125 if args.qform == "dual" else 2.5625
+    gbs = bpe * rows * cols / (ms * 1e-3) / 1e9
+    return {"shape": [rows, cols], "form": args.qform, "mode": args.qmode, "ms": round(ms, 4), "gbs": round(gbs, 1),
+            "frac": round(gbs / float(peaks()[0]["hbm_gbs"]), 4)}
 
 
 def gemm_sweep(F, torch, S, stream, dev, flush, args):
@@ -929,8 +958,11 @@ def main():
     ap.add_argument("--workload", choices=list(WORKLOADS), default="block3b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-single-thread", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--qshape", type=int, nargs=2, default=[16384, 16384], help="--part quantize_one: rows cols")
+    ap.add_argument("--qform", choices=["row", "transposed", "dual"], default="dual")
+    ap.add_argument("--qmode", choices=["rtn", "sr"], default="sr")
     ap.add_argument("--part", choices=["all", "step", "newton_schulz", "qadamw_v_codec", "lora_realign", "quantize_sweep",
-                             "gemm_sweep"], default="all",
+                             "gemm_sweep", "quantize_one"], default="all",
                     help="run one optimizer-side measurement alone (prints its JSON object; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
