@@ -548,6 +548,8 @@ def run_part(args, F, torch, S, dev):
         res = quantize_sweep(F, torch, S, stream, dev, flush, args)
     elif args.part == "quantize_one":
         res = quantize_one(F, torch, stream, dev, flush, args)
+    elif args.part == "branch_one":
+        res = branch_one(F, torch, S, stream, dev, flush, args)
     elif args.part == "gemm_sweep":
         res = gemm_sweep(F, torch, S, stream, dev, flush, args)
     elif args.part == "qadamw_v_codec":
@@ -650,6 +652,28 @@ def quantize_one(F, torch, stream, dev, flush, args):
     bpe = 3.125 if args.qform == "dual" else 2.5625
     gbs = bpe * rows * cols / (ms * 1e-3) / 1e9
     return {"shape": [rows, cols], "form": args.qform, "mode": args.qmode, "ms": round(ms, 4), "gbs": round(gbs, 1),
+            "frac": round(gbs / float(peaks()[0]["hbm_gbs"]), 4)}
+
+
+def branch_one(F, torch, S, stream, dev, flush, args):
+    """One branch-factor call P = bf16(X L^T) with max |X| on X of --qshape (M x K, Student-t
+    activations) and L of rank --rank: `steps` warm-up calls, then one timed call after an L2
+    flush.  Algorithmic bytes: X read once (2 B per element), L and P.  For profiling one launch."""
+    M, K = args.qshape
+    r = args.rank
+    X = S.student_t_device((M, K), 3, 611, dev)
+    L = S.normal_device((r, K), 0.02, 612, dev)
+    P = torch.empty((M, r), dtype=torch.bfloat16, device=dev)
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
+    fn = lambda: F.fp4_branch_factor(X, L, out=P, amax=amax, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            fn()
+        ms = _median_ms(torch, stream, flush, fn, 1)
+    F.fp4_check_status(stream)
+    nbytes = 2 * M * K + 2 * r * K + 2 * M * r
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"shape": [M, K], "rank": r, "ms": round(ms, 4), "gbs": round(gbs, 1),
             "frac": round(gbs / float(peaks()[0]["hbm_gbs"]), 4)}
 
 
@@ -961,8 +985,9 @@ def main():
     ap.add_argument("--qshape", type=int, nargs=2, default=[16384, 16384], help="--part quantize_one: rows cols")
     ap.add_argument("--qform", choices=["row", "transposed", "dual"], default="dual")
     ap.add_argument("--qmode", choices=["rtn", "sr"], default="sr")
+    ap.add_argument("--rank", type=int, default=64, help="--part branch_one: the branch rank")
     ap.add_argument("--part", choices=["all", "step", "newton_schulz", "qadamw_v_codec", "lora_realign", "quantize_sweep",
-                             "gemm_sweep", "quantize_one"], default="all",
+                             "gemm_sweep", "quantize_one", "branch_one"], default="all",
                     help="run one optimizer-side measurement alone (prints its JSON object; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

@@ -61,49 +61,49 @@ __global__ void __launch_bounds__(kRlThreads) rl_f32_to_bf16(const float* __rest
 // ---------------------------------------------------------------------------
 // FP32 GEMM on row-major operands: C (m x n, ldc) = alpha op(A) op(B) + beta C, op(A) m x k
 // (A stored m x k, or k x m when ta), op(B) k x n (B stored k x n, or n x k when tb).  A CTA
-// of 256 threads computes a 64 x 64 tile, 4 x 4 outputs per thread, over the K slice of
-// blockIdx.z: with one slice it writes C; with several, each slice's sum goes to
-// partial[z] (m x n) and rl_sgemm_reduce adds the slices in order, so the result is
-// deterministic.  Tiles of op(A) and op(B), 16 deep in K, are staged in shared memory
-// k-major; the loads run along whichever dimension is contiguous in memory.
+// of 256 threads computes a BM x BN tile (128 x 32, 64 x 64 or 32 x 128, whichever pads the
+// output least), 4 x 4 outputs per thread, over the K slice of blockIdx.z: with one slice it
+// writes C; with several, each slice's sum goes to partial[z] (m x n) and rl_sgemm_reduce adds
+// the slices in order, so the result is deterministic.  Tiles of op(A) and op(B), 16 deep in K,
+// are staged in shared memory k-major; the loads run along whichever dimension is contiguous.
 // ---------------------------------------------------------------------------
 namespace rg {
-constexpr int BM = 64, BN = 64, BK = 16, THREADS = 256;
+constexpr int BK = 16, THREADS = 256;
 }
 
-template <bool TA, bool TB>
+template <bool TA, bool TB, int BM, int BN>
 __global__ void __launch_bounds__(rg::THREADS) rl_sgemm_kernel(int64_t m, int64_t n, int64_t k, int64_t kslice,
                                                               float alpha, const float* __restrict__ A, int64_t lda,
                                                               const float* __restrict__ B, int64_t ldb, float beta,
                                                               float* __restrict__ C, int64_t ldc,
                                                               float* __restrict__ partial) {
   using namespace rg;
+  static_assert(BM * BN == 16 * THREADS, "4 x 4 outputs per thread");
   __shared__ __align__(16) float As[BK][BM + 4];
   __shared__ __align__(16) float Bs[BK][BN + 4];
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int tid = threadIdx.x, tx = tid % (BN / 4), ty = tid / (BN / 4);
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * BM, n0 = static_cast<int64_t>(blockIdx.x) * BN;
   const int64_t k0 = static_cast<int64_t>(blockIdx.z) * kslice;
   const int64_t k1 = k0 + kslice < k ? k0 + kslice : k;
   float acc[4][4] = {};
   for (int64_t kt = k0; kt < k1; kt += BK) {
-    // 1024 elements of each tile, 4 per thread
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < BM * BK / THREADS; ++u) {
       const int e = tid + u * THREADS;
       int mi, ki;
       if (TA) { ki = e / BM; mi = e % BM; }  // A stored k x m: contiguous along m
       else { mi = e / BK; ki = e % BK; }     // A stored m x k: contiguous along k
       const int64_t gm = m0 + mi, gk = kt + ki;
-      float v = 0.0f;
-      if (gm < m && gk < k1) v = TA ? A[gk * lda + gm] : A[gm * lda + gk];
-      As[ki][mi] = v;
+      As[ki][mi] = (gm < m && gk < k1) ? (TA ? A[gk * lda + gm] : A[gm * lda + gk]) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < BN * BK / THREADS; ++u) {
+      const int e = tid + u * THREADS;
       int nj, kj;
       if (TB) { nj = e / BK; kj = e % BK; }  // B stored n x k: contiguous along k
       else { kj = e / BN; nj = e % BN; }     // B stored k x n: contiguous along n
-      const int64_t gn = n0 + nj, gk2 = kt + kj;
-      float w = 0.0f;
-      if (gn < n && gk2 < k1) w = TB ? B[gn * ldb + gk2] : B[gk2 * ldb + gn];
-      Bs[kj][nj] = w;
+      const int64_t gn = n0 + nj, gk = kt + kj;
+      Bs[kj][nj] = (gn < n && gk < k1) ? (TB ? B[gn * ldb + gk] : B[gk * ldb + gn]) : 0.0f;
     }
     __syncthreads();
 #pragma unroll
@@ -424,7 +424,17 @@ struct Rl {
   void gemm(bool ta, bool tb, int64_t m, int64_t n, int64_t k, float alpha, const float* A, int64_t lda,
             const float* B, int64_t ldb, float beta, float* C, int64_t ldc) {
     if (err != cudaSuccess) return;
-    const int64_t tiles = ((m + rg::BM - 1) / rg::BM) * ((n + rg::BN - 1) / rg::BN);
+    // the tile shape that pads the output least (ties: the square tile)
+    const int64_t shapes[3][2] = {{64, 64}, {128, 32}, {32, 128}};
+    int pick = 0;
+    int64_t best = -1;
+    for (int i = 0; i < 3; ++i) {
+      const int64_t bm = shapes[i][0], bn = shapes[i][1];
+      const int64_t area = ((m + bm - 1) / bm) * bm * ((n + bn - 1) / bn) * bn;
+      if (best < 0 || area < best) best = area, pick = i;
+    }
+    const int64_t BM = shapes[pick][0], BN = shapes[pick][1];
+    const int64_t tiles = ((m + BM - 1) / BM) * ((n + BN - 1) / BN);
     int64_t splits = 1;
     const int64_t want = 2 * static_cast<int64_t>(num_sms);
     if (tiles < want) {
@@ -439,13 +449,10 @@ struct Rl {
     int64_t kslice = (k + splits - 1) / splits;
     kslice = (kslice + rg::BK - 1) / rg::BK * rg::BK;
     splits = (k + kslice - 1) / kslice;
-    const dim3 grid(static_cast<unsigned>((n + rg::BN - 1) / rg::BN), static_cast<unsigned>((m + rg::BM - 1) / rg::BM),
+    const dim3 grid(static_cast<unsigned>((n + BN - 1) / BN), static_cast<unsigned>((m + BM - 1) / BM),
                     static_cast<unsigned>(splits));
     float* part = splits > 1 ? split : nullptr;
-    if (ta && tb) rl_sgemm_kernel<true, true><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
-    else if (ta) rl_sgemm_kernel<true, false><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
-    else if (tb) rl_sgemm_kernel<false, true><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
-    else rl_sgemm_kernel<false, false><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    launch_tile(pick, ta, tb, grid, m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
     count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return;
     if (part) {
@@ -453,6 +460,22 @@ struct Rl {
       count_launch();
       err = cudaGetLastError();
     }
+  }
+  template <int BM, int BN>
+  void launch_t(bool ta, bool tb, dim3 grid, int64_t m, int64_t n, int64_t k, int64_t kslice, float alpha,
+                const float* A, int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
+                float* part) {
+    if (ta && tb) rl_sgemm_kernel<true, true, BM, BN><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    else if (ta) rl_sgemm_kernel<true, false, BM, BN><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    else if (tb) rl_sgemm_kernel<false, true, BM, BN><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    else rl_sgemm_kernel<false, false, BM, BN><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+  }
+  void launch_tile(int pick, bool ta, bool tb, dim3 grid, int64_t m, int64_t n, int64_t k, int64_t kslice,
+                   float alpha, const float* A, int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                   int64_t ldc, float* part) {
+    if (pick == 1) launch_t<128, 32>(ta, tb, grid, m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    else if (pick == 2) launch_t<32, 128>(ta, tb, grid, m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    else launch_t<64, 64>(ta, tb, grid, m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
   }
   int grid(int64_t n) const {
     const int64_t b = (n + kRlThreads - 1) / kRlThreads;
