@@ -395,37 +395,32 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
 // C = alpha * (A B^T + P~ Q^T) is rounded once.
 // ---------------------------------------------------------------------------
 namespace g2 {
-constexpr int BK = 128;                          // K elements per stage: 64 bytes of E2M1 per row
-constexpr int KSTEPS = BK / 64;                  // MMAs (K = 64 each) per stage
-constexpr int STAGES = 10;
-constexpr int A_BYTES = 128 * BK / 2;            // 8 KB: this CTA's 128 A rows
-constexpr int B_BYTES = 128 * BK / 2;            // 8 KB: this CTA's 128 B rows
+constexpr int BK = 256;
+constexpr int STAGES = 5;
+constexpr int A_BYTES = 128 * BK / 2;            // 16 KB: this CTA's 128 A rows
+constexpr int B_BYTES = 128 * BK / 2;            // 16 KB: this CTA's 128 B rows
 constexpr int SF_ATOM = 512;
-constexpr int SFA_BYTES = KSTEPS * SF_ATOM;      // 1 KB: scales of this CTA's A rows
-constexpr int SFB_BYTES = 2 * KSTEPS * SF_ATOM;  // 2 KB: scales of all 256 B rows
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 19 KB
-constexpr int BR_K = 32;                         // branch columns per stage (64-byte BF16 rows)
-constexpr int P_BYTES = 128 * BR_K * 2;          // 8 KB (A slot)
-constexpr int Q_BYTES = 128 * BR_K * 2;          // 8 KB (B slot)
+constexpr int SFA_BYTES = 4 * SF_ATOM;           // 2 KB: scales of this CTA's A rows
+constexpr int SFB_BYTES = 8 * SF_ATOM;           // 4 KB: scales of all 256 B rows
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 38 KB
+constexpr int BR_K = 64;
+constexpr int P_BYTES = 128 * BR_K * 2;          // 16 KB (A slot)
+constexpr int Q_BYTES = 128 * BR_K * 2;          // 16 KB (B slot)
 constexpr int EPI_WARPS = 8;                     // two per TMEM lane quadrant, 128 columns each
 constexpr int CHUNK_BYTES = 32 * 64;             // 32 rows x 32 BF16 columns, 64-byte swizzled rows
 constexpr int OUT_BYTES = EPI_WARPS * 2 * CHUNK_BYTES;  // 32 KB: two chunks in flight per epilogue warp
 constexpr uint32_t TM_ACC = 0;                   // 256 columns
-constexpr uint32_t TM_SF = 256;                  // per stage: SFA 4 + SFB 8 columns per K step
-constexpr uint32_t TM_SFB = 4 * KSTEPS;          // SFB columns start after the stage's SFA columns
-constexpr uint32_t TM_SF_STAGE = 12 * KSTEPS;
+constexpr uint32_t TM_SF = 256;                  // per stage: SFA 16 + SFB 32 columns
+constexpr uint32_t TM_SF_STAGE = 48;
 constexpr uint32_t TM_COLS = 512;
 static_assert(TM_SF + STAGES * TM_SF_STAGE <= TM_COLS, "TMEM budget");
 // warps: 0 A/B producer, 1 MMA (leader) + TMEM allocator, 2 scale/P producer,
-// 3..10 scale stagers (two per TMEM lane quadrant, one K step each), 11..18 epilogue
+// 3..10 scale stagers (two per TMEM lane quadrant, two K steps each), 11..18 epilogue
 constexpr int FIRST_EPI_WARP = 11;
 constexpr int NUM_THREADS = (FIRST_EPI_WARP + EPI_WARPS) * 32;
-constexpr int BARRIER_BYTES = (4 * STAGES + 3) * 8 + 2 * 4;  // full, sf_full, empty, peer_ready; acc x2, done; slot, abort
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 1024 + 512;
-static_assert(BARRIER_BYTES <= 512, "barrier area");
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 1024 + 256;
 static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(KSTEPS == 2, "the stager warps cover two K steps per stage");
 }  // namespace g2
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
@@ -484,9 +479,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
   const uint32_t tiles_m = p.M / 256, tiles_n = p.N / 256, num_tiles = tiles_m * tiles_n;
   const uint32_t num_k = (p.K + BK - 1) / BK;
   const bool has_branch = p.r > 0;
-  // the branch P~ Q^T runs as ceil(r / 32) extra stages of 32 columns (one 64-byte row of BF16)
-  const uint32_t n_br = has_branch ? (uint32_t)(p.r + BR_K - 1) / BR_K : 0;
-  const uint32_t n_iter = num_k + n_br;
+  const uint32_t n_iter = num_k + (has_branch ? 1 : 0);
   float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
   if (alpha == 0.0f) alpha = 1.0f;  // an all-zero operand contributes exact zeros
 
@@ -518,23 +511,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
               tma_load_2d_pair(sB, &tmap_b, full_l, kx, (int32_t)(nb2 * 256 + rank * 128));
             } else {
               const uint32_t krem = p.K - it * BK;
-              const uint32_t nk = krem >= (uint32_t)BK ? KSTEPS : krem / 64;
+              const uint32_t nk = krem >= (uint32_t)BK ? 4 : krem / 64;
               mbar_arrive_expect_tx(&sf_full[stage], 3 * nk * SF_ATOM);
-              const size_t ka = (size_t)it * KSTEPS;
+              const size_t ka = (size_t)it * 4;
               bulk_load(sSFA, p.a_scales + ((size_t)(mb2 * 2 + rank) * p.atoms_k + ka) * SF_ATOM, nk * SF_ATOM,
                         &sf_full[stage]);
               bulk_load(sSFB, p.b_scales + ((size_t)(nb2 * 2) * p.atoms_k + ka) * SF_ATOM, nk * SF_ATOM,
                         &sf_full[stage]);
-              bulk_load(sSFB + KSTEPS * SF_ATOM, p.b_scales + ((size_t)(nb2 * 2 + 1) * p.atoms_k + ka) * SF_ATOM,
+              bulk_load(sSFB + 4 * SF_ATOM, p.b_scales + ((size_t)(nb2 * 2 + 1) * p.atoms_k + ka) * SF_ATOM,
                         nk * SF_ATOM, &sf_full[stage]);
             }
           } else {
             if (ab) {
               if (leader) mbar_arrive_expect_tx(&full[stage], 2 * Q_BYTES);
-              tma_load_2d_pair(sB, &tmap_q, full_l, (int32_t)((it - num_k) * BR_K), (int32_t)(nb2 * 256 + rank * 128));
+              tma_load_2d_pair(sB, &tmap_q, full_l, 0, (int32_t)(nb2 * 256 + rank * 128));
             } else {
               mbar_arrive_expect_tx(&sf_full[stage], P_BYTES);
-              tma_load_2d(sA, &tmap_p, &sf_full[stage], (int32_t)((it - num_k) * BR_K), (int32_t)(mb2 * 256 + rank * 128));
+              tma_load_2d(sA, &tmap_p, &sf_full[stage], 0, (int32_t)(mb2 * 256 + rank * 128));
             }
           }
           if (++stage == STAGES) stage = 0, phase ^= 1;
@@ -547,7 +540,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
       // ---------------- MMA issuer (pair leader) ----------------
       const uint32_t idesc = idesc_nvf4(256, 256);
       const uint32_t idesc_br = idesc_bf16(256, 256);
-      const uint64_t adesc0 = smem_desc(smem_u32(smem), 16, 512, kSwizzle64B);
+      const uint64_t adesc0 = smem_desc(smem_u32(smem), 16, 1024, kSwizzle128B);
       const uint64_t bdesc0 = adesc0 + (A_BYTES >> 4);
       constexpr uint64_t kStageD = STAGE_BYTES >> 4;
       uint32_t stage = 0, phase = 0;
@@ -566,28 +559,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
           const uint64_t ad = adesc0 + stage * kStageD, bd = bdesc0 + stage * kStageD;
           const uint32_t tsf = tmem + TM_SF + stage * TM_SF_STAGE;
           const uint32_t krem = p.K - it * BK;
-          // K step j: operands at +32 bytes per step (descriptor units of 16 bytes), A scales at
-          // column tsf + 4j, B scales at tsf + TM_SFB + 8j
           if (krem >= (uint32_t)BK) {
-            mma_nvf4_pair(d_tmem, ad, bd, idesc, tsf, tsf + TM_SFB, it != 0);
-            mma_nvf4_pair(d_tmem, ad + 2, bd + 2, idesc, tsf + 4, tsf + TM_SFB + 8, 1);
+            mma_nvf4_pair(d_tmem, ad, bd, idesc, tsf, tsf + 16, it != 0);
+            mma_nvf4_pair(d_tmem, ad + 2, bd + 2, idesc, tsf + 4, tsf + 24, 1);
+            mma_nvf4_pair(d_tmem, ad + 4, bd + 4, idesc, tsf + 8, tsf + 32, 1);
+            mma_nvf4_pair(d_tmem, ad + 6, bd + 6, idesc, tsf + 12, tsf + 40, 1);
           } else {
-            mma_nvf4_pair(d_tmem, ad, bd, idesc, tsf, tsf + TM_SFB, it != 0);  // K % 128 == 64: one step
+            for (uint32_t kk = 0; kk < krem / 64; ++kk)
+              mma_nvf4_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, tsf + kk * 4, tsf + 16 + kk * 8,
+                            (it | kk) != 0);
           }
           tc_commit_pair_mc(&empty[stage], 3);
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
         if (!ok) break;
-        for (uint32_t jb = 0; jb < n_br; ++jb) {
+        if (has_branch) {
           if (!mbar_wait_cluster(&full[stage], phase)) { ok = false; break; }
           tc_fence_after();
           const uint64_t ad = adesc0 + stage * kStageD, bd = bdesc0 + stage * kStageD;
-          const uint32_t cols = min((uint32_t)p.r - jb * BR_K, (uint32_t)BR_K);  // 16 or 32
-          for (uint32_t kk = 0; kk < cols / 16; ++kk) mma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc_br, 1);
+          const uint32_t nkb = (uint32_t)(p.r + 15) / 16;
+          for (uint32_t kk = 0; kk < nkb; ++kk) mma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc_br, 1);
           tc_commit_pair_mc(&empty[stage], 3);
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
-        if (!ok) break;
         tc_commit_pair_mc(acc_full, 3);
       }
       if (!ok) *abort_flag = 1;
@@ -613,7 +607,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
     }
   } else if (warp < 11) {
     // ---------------- scale stagers (warps 3..10, both CTAs) ----------------
-    // warp w serves TMEM lane quadrant w % 4 and K step h = (w - 3) / 4 of the stage
+    // warp w serves TMEM lane quadrant w % 4 and the two K steps {2h, 2h+1}, h = (w - 3) / 4
     const uint32_t quad = warp & 3, h = (uint32_t)(warp - 3) >> 2;
     const uint32_t lane_off = (quad * 32) << 16;
     const float g = __fdiv_rn(p.beta, alpha);
@@ -628,31 +622,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
         uint8_t* sA = smem + stage * STAGE_BYTES;
         if (it < num_k) {
           const uint32_t krem = p.K - it * BK;
-          const uint32_t nk = krem >= (uint32_t)BK ? KSTEPS : krem / 64;
+          const uint32_t nk = krem >= (uint32_t)BK ? 4 : krem / 64;
           const uint8_t* sSFA = sA + A_BYTES + B_BYTES;
           const uint8_t* sSFB = sSFA + SFA_BYTES;
           const uint32_t tsf = TM_SF + stage * TM_SF_STAGE;
-          const uint32_t j = h;  // this warp's K step
-          uint32_t wa[4], wb[8];
+          uint32_t wa[8], wb[16];
           // A row m = 32*quad + lane: scales of K step j at atom j, byte (m%32)*16 + (m/32)*4;
           // the MMA reads them at lane m, column tsf + 4j + quad
-          const uint32_t va =
-              j < nk ? *reinterpret_cast<const uint32_t*>(sSFA + j * SF_ATOM + lane * 16 + quad * 4) : 0u;
-          wa[0] = wa[1] = wa[2] = wa[3] = va;
-          tmem_st_32x32b_x4(tmem + lane_off + tsf + 4 * j, wa);
-          // B row n = 32c + lane (c = 0..7): scales of K step j at column tsf + TM_SFB + 8j + c, every quadrant
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (j < nk) v = *reinterpret_cast<const uint4*>(sSFB + hh * KSTEPS * SF_ATOM + j * SF_ATOM + lane * 16);
-            wb[4 * hh] = v.x;
-            wb[4 * hh + 1] = v.y;
-            wb[4 * hh + 2] = v.z;
-            wb[4 * hh + 3] = v.w;
+          for (int jj = 0; jj < 2; ++jj) {
+            const uint32_t j = 2 * h + jj;
+            const uint32_t v =
+                j < nk ? *reinterpret_cast<const uint32_t*>(sSFA + j * SF_ATOM + lane * 16 + quad * 4) : 0u;
+            wa[4 * jj] = wa[4 * jj + 1] = wa[4 * jj + 2] = wa[4 * jj + 3] = v;
           }
-          tmem_st_32x32b_x8(tmem + lane_off + tsf + TM_SFB + 8 * j, wb);
-          tmem_st_wait8(wb);
-          tmem_st_wait4(wa);
+          tmem_st_32x32b_x8(tmem + lane_off + tsf + 8 * h, wa);
+          // B row n = 32c + lane (c = 0..7): scales of K step j at column tsf + 16 + 8j + c, every quadrant
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const uint32_t j = 2 * h + jj;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              uint4 v = make_uint4(0, 0, 0, 0);
+              if (j < nk) v = *reinterpret_cast<const uint4*>(sSFB + hh * 4 * SF_ATOM + j * SF_ATOM + lane * 16);
+              wb[8 * jj + 4 * hh] = v.x;
+              wb[8 * jj + 4 * hh + 1] = v.y;
+              wb[8 * jj + 4 * hh + 2] = v.z;
+              wb[8 * jj + 4 * hh + 3] = v.w;
+            }
+          }
+          tmem_st_32x32b_x16(tmem + lane_off + tsf + 16 + 16 * h, wb);
+          tmem_st_wait(wb);
+          tmem_st_wait8(wa);
           tc_fence_before();
         } else {
           // branch stage: P~ = bf16(P * g) in place (an elementwise map, so the swizzle is irrelevant)
@@ -1151,19 +1152,13 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
   using namespace g4;
   if (g.M % 256 == 0 && g.N % 256 == 0) {
     // 2-SM path: each CTA TMA-loads 128 rows of A and of B
-    // operands as 128-row x 64-byte boxes (128 E2M1 codes per row), the branch factors as
-    // 128-row x 32-column boxes: both with 64-byte rows and the 64-byte swizzle
     CUtensorMap ta, tb, tp, tq;
-    if (!make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_codes, g.K / 2, g.M, g.K / 2, g2::BK / 2, 128,
-                   CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_codes, g.K / 2, g.N, g.K / 2, g2::BK / 2, 128,
-                   CU_TENSOR_MAP_SWIZZLE_64B))
+    if (!make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_codes, g.K / 2, g.M, g.K / 2, BK / 2, 128) ||
+        !make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b_codes, g.K / 2, g.N, g.K / 2, BK / 2, 128))
       return cudaErrorInvalidValue;
     if (g.r > 0) {
-      if (!make_tmap(&tp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.P, g.r, g.M, (uint64_t)g.r * 2, g2::BR_K, 128,
-                     CU_TENSOR_MAP_SWIZZLE_64B) ||
-          !make_tmap(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.Q, g.r, g.N, (uint64_t)g.r * 2, g2::BR_K, 128,
-                     CU_TENSOR_MAP_SWIZZLE_64B))
+      if (!make_tmap(&tp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.P, g.r, g.M, (uint64_t)g.r * 2, BR_K, 128) ||
+          !make_tmap(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.Q, g.r, g.N, (uint64_t)g.r * 2, BR_K, 128))
         return cudaErrorInvalidValue;
     } else {
       tp = ta;
