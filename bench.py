@@ -565,6 +565,8 @@ def run_part(args, F, torch, S, dev):
         res = quantize_one(F, torch, stream, dev, flush, args)
     elif args.part == "branch_one":
         res = branch_one(F, torch, S, stream, dev, flush, args)
+    elif args.part == "gemm_one":
+        res = gemm_one(F, torch, stream, dev, flush, args)
     elif args.part == "gemm_sweep":
         res = gemm_sweep(F, torch, S, stream, dev, flush, args)
     elif args.part == "qadamw_v_codec":
@@ -690,6 +692,29 @@ def branch_one(F, torch, S, stream, dev, flush, args):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"shape": [M, K], "rank": r, "ms": round(ms, 4), "gbs": round(gbs, 1),
             "frac": round(gbs / float(peaks()[0]["hbm_gbs"]), 4)}
+
+
+def gemm_one(F, torch, stream, dev, flush, args):
+    """One block-scaled GEMM of --gshape M N K (operands N(0, 1) quantized RTN, rank --rank branch with
+    P, Q ~ N(0, 1), BF16 output): `steps` warm-up calls, then one timed call after an L2 flush.
+    For profiling one launch of the GEMM."""
+    M, N, K = args.gshape
+    r = args.rank
+    g = torch.Generator(device=dev)
+    g.manual_seed(M + 3 * N + 7 * K)
+    qa = F.fp4_quantize(torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16), stream=stream)
+    qb = F.fp4_quantize(torch.randn((N, K), generator=g, device=dev).to(torch.bfloat16), stream=stream)
+    P = torch.randn((M, r), generator=g, device=dev).to(torch.bfloat16) if r else None
+    Q = torch.randn((N, r), generator=g, device=dev).to(torch.bfloat16) if r else None
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    fn = lambda: F.fp4_gemm_blockscaled(qa, qb, P, Q, out=C, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            fn()
+        ms = _median_ms(torch, stream, flush, fn, 1)
+    F.fp4_check_status(stream)
+    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    return {"shape": [M, N, K], "rank": r, "ms": round(ms, 4), "tflops": round(tf, 1)}
 
 
 def gemm_sweep(F, torch, S, stream, dev, flush, args):
@@ -1000,9 +1025,10 @@ def main():
     ap.add_argument("--qshape", type=int, nargs=2, default=[16384, 16384], help="--part quantize_one: rows cols")
     ap.add_argument("--qform", choices=["row", "transposed", "dual"], default="dual")
     ap.add_argument("--qmode", choices=["rtn", "sr"], default="sr")
-    ap.add_argument("--rank", type=int, default=64, help="--part branch_one: the branch rank")
+    ap.add_argument("--rank", type=int, default=64, help="--part branch_one / gemm_one: the branch rank")
+    ap.add_argument("--gshape", type=int, nargs=3, default=[16384, 3072, 8192], help="--part gemm_one: M N K")
     ap.add_argument("--part", choices=["all", "step", "newton_schulz", "qadamw_v_codec", "lora_realign", "quantize_sweep",
-                             "gemm_sweep", "quantize_one", "branch_one"], default="all",
+                             "gemm_sweep", "quantize_one", "branch_one", "gemm_one"], default="all",
                     help="run one optimizer-side measurement alone (prints its JSON object; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

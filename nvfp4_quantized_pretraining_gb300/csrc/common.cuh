@@ -217,14 +217,6 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint32_t (&r)[4]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
-               "r"(r[2]), "r"(r[3])
-               : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait4(const uint32_t (&r)[4]) {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::"r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]) : "memory");
-}
 __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
                "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
@@ -369,7 +361,7 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&a)[32], uint32_t (&b)[32
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
 // stride byte offsets (all >> 4), descriptor version 1, swizzle mode.
-enum : uint32_t { kSwizzleNone = 0, kSwizzle128B = 2, kSwizzle64B = 4 };
+enum : uint32_t { kSwizzleNone = 0, kSwizzle128B = 2 };
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
                                               uint32_t swizzle) {
   uint64_t d = 0;
@@ -479,12 +471,6 @@ __device__ __forceinline__ uint32_t e2m1x4(float a, float b, float c, float d) {
       : "=r"(r)
       : "f"(a), "f"(b), "f"(c), "f"(d));
   return r & 0xFFFFu;
-}
-// Two E2M1 codes (round-to-nearest-even, saturating) in one byte, a in the low nibble.
-__device__ __forceinline__ uint32_t e2m1x2(float a, float b) {
-  uint16_t r;
-  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n cvt.u16.u8 %0, t;\n}\n" : "=h"(r) : "f"(a), "f"(b));
-  return r;
 }
 // Eight E2M1 codes packed into 32 bits, element 0 in the low nibble.
 __device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
