@@ -581,6 +581,17 @@ def run_part(args, F, torch, S, dev):
     print(json.dumps({args.part: res}), flush=True)
 
 
+def _warm_clocks(torch, stream, flush, seconds=0.25):
+    """Keeps the GPU busy for `seconds` (L2 flushes) so that its clocks have ramped up before a
+    short timed call; a fresh process otherwise times its first calls at idle clocks."""
+    t0 = time.monotonic()
+    with torch.cuda.stream(stream):
+        while time.monotonic() - t0 < seconds:
+            for _ in range(20):
+                flush.zero_()
+            torch.cuda.synchronize()
+
+
 def _median_ms(torch, stream, flush, fn, reps):
     """Median CUDA-event time of fn() on `stream`, L2 flushed before each timed call."""
     fn()
@@ -647,8 +658,9 @@ def quantize_sweep(F, torch, S, stream, dev, flush, args):
 
 def quantize_one(F, torch, stream, dev, flush, args):
     """One quantize call on an N(0, 1) tensor of --qshape with 0.1% of entries x50 (--qform row,
-    transposed or dual; --qmode rtn or sr), amax supplied: `steps` warm-up calls, then one timed
-    call after an L2 flush.  For profiling a single launch of the quantizer."""
+    transposed or dual; --qmode rtn or sr), amax supplied: `steps` warm-up calls and a quarter
+    second of L2 flushes (clocks up), then the median of 9 calls, each after an L2 flush.  The first
+    timed call is launch `steps` + 1 of the kernel: the one to profile."""
     rows, cols = args.qshape
     g = torch.Generator(device=dev)
     g.manual_seed(601)
@@ -664,7 +676,9 @@ def quantize_one(F, torch, stream, dev, flush, args):
     with torch.cuda.stream(stream):
         for _ in range(args.steps):
             fn()
-        ms = _median_ms(torch, stream, flush, fn, 1)
+    _warm_clocks(torch, stream, flush)
+    with torch.cuda.stream(stream):
+        ms = _median_ms(torch, stream, flush, fn, 9)
     F.fp4_check_status(stream)
     bpe = 3.125 if args.qform == "dual" else 2.5625
     gbs = bpe * rows * cols / (ms * 1e-3) / 1e9
@@ -674,8 +688,9 @@ def quantize_one(F, torch, stream, dev, flush, args):
 
 def branch_one(F, torch, S, stream, dev, flush, args):
     """One branch-factor call P = bf16(X L^T) with max |X| on X of --qshape (M x K, Student-t
-    activations) and L of rank --rank: `steps` warm-up calls, then one timed call after an L2
-    flush.  Algorithmic bytes: X read once (2 B per element), L and P.  For profiling one launch."""
+    activations) and L of rank --rank: `steps` warm-up calls and a quarter second of L2
+    flushes (clocks up), then the median of 9 calls, each after an L2 flush.  Algorithmic bytes: X read
+    once (2 B per element), L and P.  The first timed call is launch `steps` + 1: the one to profile."""
     M, K = args.qshape
     r = args.rank
     X = S.student_t_device((M, K), 3, 611, dev)
@@ -686,7 +701,9 @@ def branch_one(F, torch, S, stream, dev, flush, args):
     with torch.cuda.stream(stream):
         for _ in range(args.steps):
             fn()
-        ms = _median_ms(torch, stream, flush, fn, 1)
+    _warm_clocks(torch, stream, flush)
+    with torch.cuda.stream(stream):
+        ms = _median_ms(torch, stream, flush, fn, 9)
     F.fp4_check_status(stream)
     nbytes = 2 * M * K + 2 * r * K + 2 * M * r
     gbs = nbytes / (ms * 1e-3) / 1e9
@@ -696,8 +713,8 @@ def branch_one(F, torch, S, stream, dev, flush, args):
 
 def gemm_one(F, torch, stream, dev, flush, args):
     """One block-scaled GEMM of --gshape M N K (operands N(0, 1) quantized RTN, rank --rank branch with
-    P, Q ~ N(0, 1), BF16 output): `steps` warm-up calls, then one timed call after an L2 flush.
-    For profiling one launch of the GEMM."""
+    P, Q ~ N(0, 1), BF16 output): `steps` warm-up calls and a quarter second of L2 flushes (clocks up), then the median of
+    9 calls, each after an L2 flush.  The first timed call is launch `steps` + 1: the one to profile."""
     M, N, K = args.gshape
     r = args.rank
     g = torch.Generator(device=dev)
@@ -711,7 +728,9 @@ def gemm_one(F, torch, stream, dev, flush, args):
     with torch.cuda.stream(stream):
         for _ in range(args.steps):
             fn()
-        ms = _median_ms(torch, stream, flush, fn, 1)
+    _warm_clocks(torch, stream, flush)
+    with torch.cuda.stream(stream):
+        ms = _median_ms(torch, stream, flush, fn, 9)
     F.fp4_check_status(stream)
     tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
     return {"shape": [M, N, K], "rank": r, "ms": round(ms, 4), "tflops": round(tf, 1)}

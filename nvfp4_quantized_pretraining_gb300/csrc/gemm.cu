@@ -17,6 +17,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -1084,19 +1085,57 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D row-major tensor map: inner dimension `inner` elements, `outer` rows,
-// row pitch `pitch_bytes`, box inner x outer, 128-byte swizzle.
+// row pitch `pitch_bytes`, box inner x outer, 128-byte swizzle by default.
+// A tensor map is a pure function of these parameters, so encoded maps are kept
+// in a small cache keyed on all of them (64 entries, replaced round-robin): a call
+// on the same buffers and shapes as an earlier one skips the driver's encoder.
+struct TmapKey {
+  int dt, swizzle;
+  const void* base;
+  uint64_t inner, outer, pitch;
+  uint32_t box_inner, box_outer;
+};
 static bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                       uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
                       CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+  constexpr int kCache = 64;
+  static std::mutex mu;
+  static TmapKey keys[kCache];
+  static CUtensorMap maps[kCache];
+  static int used = 0, next = 0;
+  TmapKey k;
+  std::memset(&k, 0, sizeof(k));  // padding included, for the byte-wise comparison
+  k.dt = static_cast<int>(dt);
+  k.swizzle = static_cast<int>(swizzle);
+  k.base = base;
+  k.inner = inner;
+  k.outer = outer;
+  k.pitch = pitch_bytes;
+  k.box_inner = box_inner;
+  k.box_outer = box_outer;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    for (int i = 0; i < used; ++i)
+      if (std::memcmp(&keys[i], &k, sizeof(k)) == 0) {
+        *m = maps[i];
+        return true;
+      }
+  }
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {pitch_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> g(mu);
+  keys[next] = k;
+  maps[next] = *m;
+  next = (next + 1) % kCache;
+  if (used < kCache) ++used;
+  return true;
 }
 
 bool make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,

@@ -163,10 +163,21 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 3 : 5) quantize_dual_kernel
     w[i] = make_uint4(0, 0, 0, 0);
     if (row < a.rows && c8 < a.cpr) w[i] = __ldcs(reinterpret_cast<const uint4*>(a.x + row * a.ld + c8 * 8));
   }
+  if (COL && SR) {
+    // the column form's random bits first: their ALU work overlaps the global loads in flight.
+    // Element e of a chunk takes word e/2, low half for even e: in element order the eight
+    // 16-bit draws are exactly the four words as stored
+#pragma unroll
+    for (int i = 0; i < kLoads; ++i) {
+      const int q = tid + i * kDualThreads;
+      const uint32_t row = r0 + (q >> 4), c8 = (c0 >> 3) + (q & 15);
+      *reinterpret_cast<uint4*>(&rtile[q >> 4][(q & 15) * 8]) =
+          sr_random(a.keys, a.stream_c, (uint64_t)row * a.cpr + c8);
+    }
+  }
 #pragma unroll
   for (int i = 0; i < kLoads; ++i) {
     const int q = tid + i * kDualThreads;
-    const uint32_t row = r0 + (q >> 4), c8 = (c0 >> 3) + (q & 15);
     if (CLIP) {
       const uint32_t v2 = *a.clip * 0x10001u;
       w[i].x = (w[i].x & 0x80008000u) | __vminu2(w[i].x & 0x7FFF7FFFu, v2);
@@ -175,12 +186,6 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 3 : 5) quantize_dual_kernel
       w[i].w = (w[i].w & 0x80008000u) | __vminu2(w[i].w & 0x7FFF7FFFu, v2);
     }
     *reinterpret_cast<uint4*>(&tile[q >> 4][swz(q & 15) * 8]) = w[i];
-    if (COL && SR) {
-      // element e of the chunk takes word e/2, low half for even e: in element order
-      // the eight 16-bit draws are exactly the four words as stored
-      *reinterpret_cast<uint4*>(&rtile[q >> 4][(q & 15) * 8]) =
-          sr_random(a.keys, a.stream_c, (uint64_t)row * a.cpr + c8);
-    }
   }
   __syncthreads();
 
