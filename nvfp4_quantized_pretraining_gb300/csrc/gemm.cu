@@ -813,11 +813,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
 // ---------------------------------------------------------------------------
 namespace bf {
 constexpr int BM = 128;
-constexpr int BK = 64;              // BF16 elements per stage (128-byte rows)
-constexpr int STAGES = 8;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = 64 * BK * 2;  // 8 KB (r <= 64 rows)
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BOX = 64;                 // BF16 columns per TMA box (128-byte rows, 128-byte swizzle)
+constexpr int BOXES = 2;                // boxes per stage, adjacent in K: 256 contiguous bytes per row
+constexpr int BK = BOX * BOXES;         // BF16 elements of K per stage
+constexpr int STAGES = 4;               // one CTA per SM
+constexpr int SPLIT_STAGES = 2;         // two CTAs per SM (K split over a CTA pair)
+constexpr int XBOX_BYTES = BM * BOX * 2;  // 16 KB
+constexpr int LBOX_BYTES = 64 * BOX * 2;  // 8 KB (r <= 64 rows)
+constexpr int A_BYTES = BOXES * XBOX_BYTES;
+constexpr int STAGE_BYTES = A_BYTES + BOXES * LBOX_BYTES;  // 48 KB
 constexpr int NUM_THREADS = 192;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 }  // namespace bf
@@ -849,7 +853,7 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
     branch_factor_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_l,
                          uint32_t K, int r, __nv_bfloat16* __restrict__ P, unsigned int* __restrict__ amax_out) {
   using namespace bf;
-  constexpr int NST = SPLIT ? 4 : STAGES;
+  constexpr int NST = SPLIT ? SPLIT_STAGES : STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * STAGE_BYTES);
@@ -880,7 +884,7 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
   const uint32_t k_begin = rank * kh;                 // this CTA's first K stage
   const uint32_t num_k = SPLIT ? min(kh, num_k_all - k_begin) : num_k_all;  // >= 1: the host splits only K >= 2 stages
   const uint32_t m0 = (SPLIT ? (blockIdx.x >> 1) : blockIdx.x) * BM;
-  const uint32_t l_bytes = (uint32_t)r * BK * 2;
+  const uint32_t l_bytes = (uint32_t)r * BOX * 2;  // one L box
 
   if (warp == 0) {
     if (lane == 0) {
@@ -893,9 +897,15 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
         if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
         uint8_t* sA = smem + stage * STAGE_BYTES;
         uint8_t* sB = sA + A_BYTES;
-        mbar_arrive_expect_tx(&full[stage], A_BYTES + l_bytes);
-        tma_load_2d(sA, &tmap_x, &full[stage], (int32_t)((k_begin + it) * BK), (int32_t)m0);
-        tma_load_2d(sB, &tmap_l, &full[stage], (int32_t)((k_begin + it) * BK), 0);
+        // both boxes of X back to back (256 contiguous bytes of each row), then both of L;
+        // a box past K arrives zero-filled
+        mbar_arrive_expect_tx(&full[stage], BOXES * (XBOX_BYTES + l_bytes));
+        const int32_t kx = (int32_t)((k_begin + it) * BK);
+#pragma unroll
+        for (int b = 0; b < BOXES; ++b)
+          tma_load_2d(sA + b * XBOX_BYTES, &tmap_x, &full[stage], kx + b * BOX, (int32_t)m0);
+#pragma unroll
+        for (int b = 0; b < BOXES; ++b) tma_load_2d(sB + b * LBOX_BYTES, &tmap_l, &full[stage], kx + b * BOX, 0);
         armed[stage] = 1;
         armed_phase[stage] = phase;
         if (++stage == NST) stage = 0, phase ^= 1;
@@ -918,9 +928,11 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
         const uint32_t sB = sA + A_BYTES;
         const uint32_t krem = K - (k_begin + it) * BK;
         const uint32_t nk = krem >= (uint32_t)BK ? BK / 16 : krem / 16;
-        for (uint32_t kk = 0; kk < nk; ++kk)
-          mma_bf16(tmem, smem_desc(sA + kk * 32, 16, 1024, kSwizzle128B),
-                   smem_desc(sB + kk * 32, 16, 1024, kSwizzle128B), idesc, (it | kk) != 0);
+        for (uint32_t kk = 0; kk < nk; ++kk) {  // K step kk: box kk / 4, +32 bytes per step inside it
+          const uint32_t b = kk >> 2, o = (kk & 3) * 32;
+          mma_bf16(tmem, smem_desc(sA + b * XBOX_BYTES + o, 16, 1024, kSwizzle128B),
+                   smem_desc(sB + b * LBOX_BYTES + o, 16, 1024, kSwizzle128B), idesc, (it | kk) != 0);
+        }
         tc_commit(&empty[stage]);
         if (++stage == NST) stage = 0, phase ^= 1;
       }
@@ -947,7 +959,7 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
         }
         const uint4* tile = reinterpret_cast<const uint4*>(smem + stage * STAGE_BYTES);
 #pragma unroll
-        for (int i = 0; i < A_BYTES / 16 / 128; ++i) {
+        for (int i = 0; i < A_BYTES / 16 / 128; ++i) {  // both X boxes
           const uint4 v = tile[t + 128 * i];
           m = __vmaxu2(m, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
                                    __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
@@ -1262,7 +1274,7 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
 cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ldx, const void* L, int r, void* P,
                                  float* amax_out, int num_sms, cudaStream_t s) {
   using namespace bf;
-  constexpr int kSmemSplit = 4 * STAGE_BYTES + 1024 + 256;
+  constexpr int kSmemSplit = SPLIT_STAGES * STAGE_BYTES + 1024 + 256;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
