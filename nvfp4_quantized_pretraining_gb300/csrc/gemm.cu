@@ -1286,8 +1286,8 @@ cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ld
   });
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap tx, tl;
-  if (!make_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, (uint64_t)ldx * 2, BK, BM) ||
-      !make_tmap(&tl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L, K, r, (uint64_t)K * 2, BK, (uint32_t)r))
+  if (!make_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, (uint64_t)ldx * 2, BOX, BM) ||
+      !make_tmap(&tl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L, K, r, (uint64_t)K * 2, BOX, (uint32_t)r))
     return cudaErrorInvalidValue;
   if (amax_out) {
     const cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), s);
