@@ -55,8 +55,9 @@ WORKLOADS = {
 # keyed by the SHA-256 of the kernel source it was captured on (null once the
 # source changes).  Filled from the committed profile summary.
 GEMM_TRAFFIC = {
-    # ncu capture of the bench workload: mean dram read + write bytes per launch
-    "8bf1038430f07168": 213556309,
+    # launch list of `--part step --steps 2 --warmup 3` with dram__bytes_read.sum and
+    # dram__bytes_write.sum (one pass): mean over the 96 GEMM launches of the 3B block
+    "e5306d3e9bdedc19": 214500000,
 }
 
 

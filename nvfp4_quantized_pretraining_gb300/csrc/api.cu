@@ -110,8 +110,8 @@ static fp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64
       return fail(FP4_ERR_INVALID_ARG, "transposed out is %lld x %lld, expected %lld x %lld",
                   (long long)out_col->rows, (long long)out_col->cols, (long long)cols, (long long)rows);
   }
-  if ((rows + 127) / 128 > 65535)  // one 128-row tile per grid row
-    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rows %lld too large (at most 65535 x 128)", (long long)rows);
+  if ((rows + 63) / 64 > 65535)  // one 64-row tile per grid row
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rows %lld too large (at most 65535 x 64)", (long long)rows);
   if (amax_opt && (reinterpret_cast<uintptr_t>(amax_opt) & 3u))
     return fail(FP4_ERR_MISALIGNED, "amax_opt must be 4-byte aligned");
   if (out_row && scale_padded(rows, cols))
