@@ -391,58 +391,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
 }
 
 // ---------------------------------------------------------------------------
-// Philox4x32-10 (Salmon et al., SC'11)
-// ---------------------------------------------------------------------------
-// The ten round keys of a (seed lo, seed hi) key: round r uses
-// (k0 + r * 0x9E3779B9, k1 + r * 0xBB67AE85).  Computed once per thread, or once
-// on the host and passed in a kernel's parameters (constant memory, which the
-// XOR instructions read as an operand: no registers held).
-struct PhiloxKeys {
-  uint32_t k0[10], k1[10];
-};
-__host__ __device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
-  PhiloxKeys k;
-  uint32_t a = static_cast<uint32_t>(seed), b = static_cast<uint32_t>(seed >> 32);
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    k.k0[r] = a;
-    k.k1[r] = b;
-    a += 0x9E3779B9u;
-    b += 0xBB67AE85u;
-  }
-  return k;
-}
-// One round: 64-bit products give hi and lo of c0*M0 and c2*M1 in one multiply each.
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys& k) {
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c.x;
-    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c.z;
-    c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k.k0[r], static_cast<uint32_t>(p1),
-                   static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k.k1[r], static_cast<uint32_t>(p0));
-  }
-  return c;
-}
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
-  PhiloxKeys k;
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    k.k0[r] = k0 + static_cast<uint32_t>(r) * 0x9E3779B9u;
-    k.k1[r] = k1 + static_cast<uint32_t>(r) * 0xBB67AE85u;
-  }
-  return philox4x32_10(c, k);
-}
-
-// The 128 random bits for element group j (elements 8j..8j+7) of a tensor.
-__device__ __forceinline__ uint4 sr_random(const PhiloxKeys& k, uint32_t stream, uint64_t j) {
-  return philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(j >> 32), stream, 0u), k);
-}
-__device__ __forceinline__ uint4 sr_random(uint64_t seed, uint32_t stream, uint64_t j) {
-  return philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(j >> 32), stream, 0u),
-                       static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
-}
-
-// ---------------------------------------------------------------------------
 // NVFP4 conversions
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -504,40 +452,5 @@ __device__ __forceinline__ BlockScale block_scale(float amax_b, float S_t) {
 
 // Tensor scale from amax: S_t = amax / 2688 (0 for an all-zero tensor).
 __device__ __forceinline__ float tensor_scale(float amax) { return amax == 0.0f ? 0.0f : __fdiv_rn(amax, 2688.0f); }
-
-// The 16 random bits of one element as the float 65536 + rnd16 * 2^-7 (exponent
-// 16 above them in the high half-word): one byte permute from a Philox word,
-// whose low half feeds the even element and high half the odd one.
-__device__ __forceinline__ uint32_t sr_draw_lo(uint32_t w) { return __byte_perm(w, 0x47800000u, 0x7610); }
-__device__ __forceinline__ uint32_t sr_draw_hi(uint32_t w) { return __byte_perm(w, 0x47800000u, 0x7632); }
-
-// Stochastic rounding of y to the E2M1 grid with 16 random bits rnd16, given as
-// draw = bits of 65536 + rnd16 * 2^-7 (sr_draw_lo / sr_draw_hi): returns the
-// rounded value (a grid point, sign of y kept), for the saturating E2M1
-// conversion that follows.  With a = min(|y|, 6), lo the grid point <= a and sp
-// the gap above it (0.5 below 2, 1 in [2, 4), 2 in [4, 6]), the value rounds
-// up iff rnd16 < frac * 65536, frac = (a - lo) / sp, i.e. iff frac > u with
-// u = rnd16 / 65536.  That is the same as
-//   result = sp * ceil(a / sp - u) = ceil_sp(a - u * sp),
-// which is computed on the floating-point pipe, every product exact:
-//   s = sp * 2^-9 = max(2^e * 2^-10, 2^-10) from the exponent field of y;
-//   d = draw - 65536 = rnd16 * 2^-7, so that d * s = u * sp;
-//   t = |y| - d * s rounded upward (one fused multiply-add);
-//   ceil_sp(t) = (t + M rounded upward) - M with M = 1.5 * 2^23 * sp = 1.5 * 2^32 * s,
-//   whose binade has spacing sp and holds t + M for every t in (-sp, 8].
-// Upward rounding of t to its own (finer) grid commutes with the ceiling to
-// multiples of sp, so the result equals the arithmetic definition bit for bit
-// (denormal inputs included: no flush to zero in this code).  The clamp to 6
-// is left to the conversion: for 6 < |y| < 8 the gap is 2 and the result is 6
-// or 8, which the saturating conversion maps to 6, the clamped value's result.
-__device__ __forceinline__ float sr_round(float y, uint32_t draw) {
-  const uint32_t bits = __float_as_uint(y);
-  const float sc = fmaxf(__uint_as_float(bits & 0x7F800000u) * 0x1p-10f, 0x1p-10f);
-  const float M = sc * 6442450944.0f;  // 1.5 * 2^32 * sc
-  const float d = __uint_as_float(draw) - 65536.0f;
-  const float t = __fmaf_ru(-d, sc, fabsf(y));
-  const float c = __fadd_ru(t, M) - M;
-  return __uint_as_float(__float_as_uint(c) | (bits & 0x80000000u));
-}
 
 }  // namespace nvfp4

@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "scale_layout.cuh"
+#include "sr.cuh"
 
 namespace nvfp4 {
 
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 6 : 10) quantize_dual_kerne
           const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            y[hh][e] = sr_round(y[hh][e], (e & 1) ? sr_draw_hi(rw[e >> 1]) : sr_draw_lo(rw[e >> 1]));
+            y[hh][e] = sr_round(y[hh][e], (e & 1) ? sr_bias_hi(rw[e >> 1]) : sr_bias_lo(rw[e >> 1]));
         }
       }
       const uint32_t lo = e2m1x8(y[0]), hi = e2m1x8(y[1]);
@@ -277,8 +278,8 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 6 : 10) quantize_dual_kerne
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const uint32_t rp = *reinterpret_cast<const uint32_t*>(&rtile[rb * 16 + i][2 * cp]);
-        va[i] = sr_round(va[i], sr_draw_lo(rp));
-        vb[i] = sr_round(vb[i], sr_draw_hi(rp));
+        va[i] = sr_round(va[i], sr_bias_lo(rp));
+        vb[i] = sr_round(vb[i], sr_bias_hi(rp));
       }
     }
     float t8[8];
@@ -349,7 +350,7 @@ __global__ void debug_sr_round_kernel(const float* __restrict__ in, const uint16
   if (i8 >= n) return;
   float v[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = (i8 + i < n) ? sr_round(in[i8 + i], 0x47800000u | rnd[i8 + i]) : 0.0f;
+  for (int i = 0; i < 8; ++i) v[i] = (i8 + i < n) ? sr_round(in[i8 + i], sr_bias_lo(rnd[i8 + i])) : 0.0f;
   const uint32_t c = e2m1x8(v);
 #pragma unroll
   for (int i = 0; i < 8; ++i)
