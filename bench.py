@@ -233,8 +233,11 @@ def run_ours(args):
         p["Y"] = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
         p["dX"] = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
         p["dW"] = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
-        p["ws_f"] = torch.empty(F.linear_fwd_workspace(T, N, K, r), dtype=torch.uint8, device=dev)
-        p["ws_b"] = torch.empty(F.linear_bwd_workspace(T, N, K, r), dtype=torch.uint8, device=dev)
+        # each with the room for the GEMMs' split tail
+        p["ws_f"] = torch.empty(F.linear_fwd_workspace(T, N, K, r) + F.gemm_split_workspace(), dtype=torch.uint8,
+                                device=dev)
+        p["ws_b"] = torch.empty(F.linear_bwd_workspace(T, N, K, r) + F.gemm_split_workspace(), dtype=torch.uint8,
+                                device=dev)
         projs.append(p)
     flush = L2Flush(torch, dev)  # > 2x the 129 MB L2, left clean
     gemm_flops = sum(3 * 2 * T * p["N"] * p["K"] for p in projs)
@@ -368,6 +371,7 @@ def breakdown(F, torch, projs, T, r, stream, dev, flush, args):
     gemm_flops = 0
     reps = max(2, min(args.steps, 5))
     kinds = {}
+    sk = torch.empty(F.gemm_split_workspace(), dtype=torch.uint8, device=dev)  # as the linear calls have
 
     def rec(kind, fn):
         e0 = torch.cuda.Event(enable_timing=True)
@@ -404,7 +408,8 @@ def breakdown(F, torch, projs, T, r, stream, dev, flush, args):
                     rec("amax", lambda: F.fp4_amax(p["X"], out=p["amax"], stream=stream))
                 rec("quantize_x_dual", lambda: F.fp4_quantize_dual(p["X"], amax=p["amax"], out_row=xq,
                                                                    out_col=p["xqT"], stream=stream))
-                rec("gemm", lambda: F.fp4_gemm_blockscaled(xq, p["Wq"], p["P"], p["L2"], out=p["Y"], stream=stream))
+                rec("gemm", lambda: F.fp4_gemm_blockscaled_ws(xq, p["Wq"], p["P"], p["L2"], out=p["Y"], workspace=sk,
+                                                              stream=stream))
                 if r:
                     rec("branch_factor_amax", lambda: F.fp4_branch_factor(p["dY"], p["L2T"], out=p["P2"],
                                                                           amax=p["amax"], stream=stream))
@@ -413,9 +418,10 @@ def breakdown(F, torch, projs, T, r, stream, dev, flush, args):
                 rec("quantize_dy_dual_sr", lambda: F.fp4_quantize_dual(p["dY"], round_mode=F.SR, seed=rep,
                                                                        amax=p["amax"], out_row=dyq, out_col=dyqT,
                                                                        stream=stream))
-                rec("gemm", lambda: F.fp4_gemm_blockscaled(dyq, p["WqT"], p["P2"], p["L1T"], out=p["dX"],
-                                                           stream=stream))
-                rec("gemm", lambda: F.fp4_gemm_blockscaled(dyqT, p["xqT"], out=p["dW"], stream=stream))
+                rec("gemm", lambda: F.fp4_gemm_blockscaled_ws(dyq, p["WqT"], p["P2"], p["L1T"], out=p["dX"],
+                                                              workspace=sk, stream=stream))
+                rec("gemm", lambda: F.fp4_gemm_blockscaled_ws(dyqT, p["xqT"], out=p["dW"], workspace=sk,
+                                                              stream=stream))
             torch.cuda.synchronize(dev)
             if rep == 0:
                 continue  # warm-up pass
@@ -725,7 +731,8 @@ def gemm_one(F, torch, stream, dev, flush, args):
     P = torch.randn((M, r), generator=g, device=dev).to(torch.bfloat16) if r else None
     Q = torch.randn((N, r), generator=g, device=dev).to(torch.bfloat16) if r else None
     C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    fn = lambda: F.fp4_gemm_blockscaled(qa, qb, P, Q, out=C, stream=stream)
+    sk = torch.empty(F.gemm_split_workspace(), dtype=torch.uint8, device=dev)
+    fn = lambda: F.fp4_gemm_blockscaled_ws(qa, qb, P, Q, out=C, workspace=sk, stream=stream)
     with torch.cuda.stream(stream):
         for _ in range(args.steps):
             fn()
@@ -747,6 +754,7 @@ def gemm_sweep(F, torch, S, stream, dev, flush, args):
     fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
     reps = max(3, min(args.steps, 7))
     out = {}
+    sk = torch.empty(F.gemm_split_workspace(), dtype=torch.uint8, device=dev)
     with torch.cuda.stream(stream):
         for (M, N, K) in S.GEMM_SWEEP:
             g = torch.Generator(device=dev)
@@ -760,8 +768,8 @@ def gemm_sweep(F, torch, S, stream, dev, flush, args):
             flops = 2.0 * M * N * K
             row = {}
             for r in (0, 64):
-                fn = (lambda: F.fp4_gemm_blockscaled(qa, qb, out=C, stream=stream)) if r == 0 else \
-                     (lambda: F.fp4_gemm_blockscaled(qa, qb, P, Q, out=C, stream=stream))
+                fn = (lambda: F.fp4_gemm_blockscaled_ws(qa, qb, out=C, workspace=sk, stream=stream)) if r == 0 else \
+                     (lambda: F.fp4_gemm_blockscaled_ws(qa, qb, P, Q, out=C, workspace=sk, stream=stream))
                 ms = _median_ms(torch, stream, flush, fn, reps)
                 tf = flops / (ms * 1e-3) / 1e12
                 row[f"r{r}"] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / fp4_peak, 4)}

@@ -134,6 +134,27 @@ fp4_status fp4_gemm_blockscaled(const fp4_tensor* A, const fp4_tensor* B,
                                 const void* P, const void* Q, int r, float beta,
                                 void* C, int c_dtype, int64_t ldc, void* stream);
 
+/* Bytes of device workspace with which a GEMM may split its last partial wave
+ * of tiles along K (one 256 x 256 FP32 partial per pair of SMs of the current
+ * device: 19 MiB on a 152-SM GPU). */
+size_t fp4_gemm_split_workspace(void);
+
+/* fp4_gemm_blockscaled with a workspace for a split tail.  When M and N are
+ * multiples of 256, K is at least 48 * 256 and the 256 x 256 tiles fill
+ * W >= 1 whole waves over the SM pairs plus R < pairs more, each of the last
+ * R tiles is cut into S = pairs / R consecutive K ranges, computed by S pairs
+ * in parallel; a second launch adds the S FP32 partial accumulators in K order
+ * (the branch is in the last range) and rounds once, as for a whole tile.  So
+ * the result equals fp4_gemm_blockscaled's up to the FP32 summation order
+ * inside those tiles, and it is the same from run to run.
+ * ws: NULL (no split: exactly fp4_gemm_blockscaled) or at least
+ * fp4_gemm_split_workspace() bytes, 256-byte aligned (else FP4_ERR_WORKSPACE);
+ * its content is scratch.  Calls that share one ws must be ordered. */
+fp4_status fp4_gemm_blockscaled_ws(const fp4_tensor* A, const fp4_tensor* B,
+                                   const void* P, const void* Q, int r, float beta,
+                                   void* C, int c_dtype, int64_t ldc,
+                                   void* ws, size_t ws_bytes, void* stream);
+
 /* Low-rank branch factor: P[m][j] = bf16( sum_k X[m][k] L[j][k] ), FP32
  * accumulation.  X: M x K BF16 (pitch ldx), L: r x K BF16 (pitch K), P: M x r
  * BF16 (pitch r).  Requires M % 128 == 0, K % 16 == 0, r in {16,32,48,64}.
@@ -158,16 +179,20 @@ size_t fp4_linear_bwd_workspace(int64_t M, int64_t N, int64_t K, int r);
  * X is quantized RTN in both orientations from one read; the column form
  * (K x M) is written to xqT_saved (caller-owned) for the dW product of the
  * backward pass.  ws/ws_bytes: device workspace of at least
- * fp4_linear_fwd_workspace(M, N, K, r) bytes, 256-byte aligned. */
+ * fp4_linear_fwd_workspace(M, N, K, r) bytes, 256-byte aligned; with
+ * fp4_gemm_split_workspace() bytes more, the GEMM may split its tail as
+ * fp4_gemm_blockscaled_ws does. */
 fp4_status fp4_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx,
                           const fp4_tensor* Wq, const void* L1, const void* L2, int r,
                           float beta, void* Y, int64_t ldy, fp4_tensor* xqT_saved,
                           void* ws, size_t ws_bytes, void* stream);
 
 /* fp4_linear_fwd without a caller workspace; the call allocates nothing.
- * Same arguments, result and launches as fp4_linear_fwd minus ws/ws_bytes:
- * the workspace lives in a 32 MiB file-scope device buffer of this library
- * (a static __device__ array, created when the module loads).  The pages have
+ * Same arguments, result and launches as fp4_linear_fwd minus ws/ws_bytes
+ * (given a workspace with the split-tail room): the workspace lives in a
+ * 32 MiB file-scope device buffer of this library, followed by 20 MiB for the
+ * GEMM's split tail (a static __device__ array, created when the module
+ * loads; on a GPU with more than 160 SMs the tail is not split).  The pages have
  * no counterpart to this call: it is an interface variant, not part of the
  * method.
  * For callers that cannot allocate device memory: plain C host code linked
@@ -201,7 +226,9 @@ fp4_status fp4_linear_fwd_noalloc(const void* X, int64_t M, int64_t K, int64_t l
  * dY: M x N BF16 (pitch lddy), quantized with SR (seed; Philox stream 0 for
  * the row form used by dX, stream 1 for the column form used by dW).
  * WqT: K x N NVFP4 (W_res quantized column-wise, RTN); xqT_saved: K x M from
- * fp4_linear_fwd.  ws: at least fp4_linear_bwd_workspace(M, N, K, r) bytes. */
+ * fp4_linear_fwd.  ws: at least fp4_linear_bwd_workspace(M, N, K, r) bytes;
+ * with fp4_gemm_split_workspace() bytes more, the dX and dW GEMMs may split
+ * their tails as fp4_gemm_blockscaled_ws does. */
 fp4_status fp4_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t lddy,
                           const fp4_tensor* WqT, const fp4_tensor* xqT_saved,
                           const void* L1, const void* L2, int r, float beta, uint64_t seed,

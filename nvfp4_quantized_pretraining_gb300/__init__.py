@@ -32,7 +32,7 @@ OUT_BF16 = 0
 OUT_F32 = 1
 
 EXPORTS = ["fp4_scale_bytes", "fp4_amax", "fp4_quantize", "fp4_quantize_transposed", "fp4_quantize_dual",
-           "fp4_gemm_blockscaled", "fp4_branch_factor", "fp4_linear_fwd_workspace", "fp4_linear_bwd_workspace",
+           "fp4_gemm_blockscaled", "fp4_gemm_split_workspace", "fp4_gemm_blockscaled_ws", "fp4_branch_factor", "fp4_linear_fwd_workspace", "fp4_linear_bwd_workspace",
            "fp4_linear_fwd", "fp4_linear_fwd_noalloc", "fp4_linear_bwd", "fp4_lora_factor_grad_workspace",
            "fp4_lora_factor_grad", "fp4_lora_cholqr_workspace", "fp4_lora_cholqr", "fp4_lora_realign_workspace",
            "fp4_lora_realign", "fp4_newton_schulz_workspace", "fp4_newton_schulz", "fp4_qadamw_v_encode",
@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
         "fp4_quantize_transposed": (i32, [P, i64, i64, i64, i32, u64, u32, P, T, P]),
         "fp4_quantize_dual": (i32, [P, i64, i64, i64, i32, u64, u32, u32, P, T, T, P]),
         "fp4_gemm_blockscaled": (i32, [T, T, P, P, i32, f32, P, i32, i64, P]),
+        "fp4_gemm_split_workspace": (ctypes.c_size_t, []),
+        "fp4_gemm_blockscaled_ws": (i32, [T, T, P, P, i32, f32, P, i32, i64, P, ctypes.c_size_t, P]),
         "fp4_branch_factor": (i32, [P, i64, i64, i64, P, i32, P, P, P]),
         "fp4_linear_fwd_workspace": (ctypes.c_size_t, [i64, i64, i64, i32]),
         "fp4_linear_bwd_workspace": (ctypes.c_size_t, [i64, i64, i64, i32]),
@@ -233,8 +235,7 @@ def fp4_quantize_dual(x, round_mode=RTN, seed=0, sr_stream_row=0, sr_stream_col=
     return out_row, out_col
 
 
-def fp4_gemm_blockscaled(A: NVFP4Tensor, B: NVFP4Tensor, P=None, Q=None, beta=1.0, out=None,
-                         out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+def _gemm_args(A, B, P, Q, out, out_dtype):
     r = 0 if P is None else P.shape[1]
     if out is None:
         out = torch.empty((A.rows, B.rows), dtype=out_dtype, device=A.codes.device)
@@ -242,10 +243,32 @@ def fp4_gemm_blockscaled(A: NVFP4Tensor, B: NVFP4Tensor, P=None, Q=None, beta=1.
     if r:
         _check_factor(P, (A.rows, r), A.codes.device, "P")
         _check_factor(Q, (B.rows, r), A.codes.device, "Q")
-    c_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    return r, out, OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+
+
+def fp4_gemm_blockscaled(A: NVFP4Tensor, B: NVFP4Tensor, P=None, Q=None, beta=1.0, out=None,
+                         out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+    r, out, c_dtype = _gemm_args(A, B, P, Q, out, out_dtype)
     ca, cb = A.c(), B.c()
     _check(lib().fp4_gemm_blockscaled(ctypes.byref(ca), ctypes.byref(cb), _ptr(P), _ptr(Q), r, float(beta),
                                       out.data_ptr(), c_dtype, out.stride(0), _stream(stream)))
+    return out
+
+
+def gemm_split_workspace() -> int:
+    return int(lib().fp4_gemm_split_workspace())
+
+
+def fp4_gemm_blockscaled_ws(A: NVFP4Tensor, B: NVFP4Tensor, P=None, Q=None, beta=1.0, out=None,
+                            out_dtype=torch.bfloat16, workspace=None, stream=None) -> torch.Tensor:
+    """fp4_gemm_blockscaled with the split-tail workspace (allocated here when not given)."""
+    r, out, c_dtype = _gemm_args(A, B, P, Q, out, out_dtype)
+    if workspace is None:
+        workspace = torch.empty(gemm_split_workspace(), dtype=torch.uint8, device=A.codes.device)
+    ca, cb = A.c(), B.c()
+    _check(lib().fp4_gemm_blockscaled_ws(ctypes.byref(ca), ctypes.byref(cb), _ptr(P), _ptr(Q), r, float(beta),
+                                         out.data_ptr(), c_dtype, out.stride(0), workspace.data_ptr(),
+                                         workspace.numel(), _stream(stream)))
     return out
 
 
@@ -280,8 +303,9 @@ def fp4_linear_fwd(X, Wq: NVFP4Tensor, L1=None, L2=None, beta=1.0, Y=None, xqT_s
     _check_out(Y, (M, N), torch.bfloat16, X.device, "Y")
     xqT_saved = NVFP4Tensor.empty(K, M, X.device) if xqT_saved is None else xqT_saved
     _check_qtensor(xqT_saved, K, M, "xqT_saved")
-    need = linear_fwd_workspace(M, N, K, r)
-    workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=X.device) if workspace is None else workspace
+    if workspace is None:  # with the room for the GEMM's split tail
+        workspace = torch.empty(linear_fwd_workspace(M, N, K, r) + gemm_split_workspace(), dtype=torch.uint8,
+                                device=X.device)
     cw, cx = Wq.c(), xqT_saved.c()
     _check(lib().fp4_linear_fwd(X.data_ptr(), M, K, ldx, ctypes.byref(cw), _ptr(L1), _ptr(L2), r, float(beta),
                                 Y.data_ptr(), Y.stride(0), ctypes.byref(cx), workspace.data_ptr(),
@@ -316,8 +340,9 @@ def fp4_linear_bwd(dY, WqT: NVFP4Tensor, xqT_saved: NVFP4Tensor, L1=None, L2=Non
     dW = torch.empty((N, K), dtype=dw_dtype, device=dY.device) if dW is None else dW
     _check_out(dX, (M, K), torch.bfloat16, dY.device, "dX")
     _check_out(dW, (N, K), (torch.bfloat16, torch.float32), dY.device, "dW")
-    need = linear_bwd_workspace(M, N, K, r)
-    workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dY.device) if workspace is None else workspace
+    if workspace is None:  # with the room for the GEMMs' split tail
+        workspace = torch.empty(linear_bwd_workspace(M, N, K, r) + gemm_split_workspace(), dtype=torch.uint8,
+                                device=dY.device)
     cw, cx = WqT.c(), xqT_saved.c()
     _check(lib().fp4_linear_bwd(dY.data_ptr(), M, N, lddy, ctypes.byref(cw), ctypes.byref(cx), _ptr(L1), _ptr(L2),
                                 r, float(beta), seed, dX.data_ptr(), dX.stride(0), dW.data_ptr(),

@@ -135,8 +135,11 @@ static fp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64
   return FP4_OK;
 }
 
+// sk_ws (optional, 256-byte aligned, sk_bytes of room): lets the GEMM split its last partial wave
+// of tiles along K (gemm_splitk_ws_bytes() bytes are enough for any shape).
 static fp4_status gemm_impl(const fp4_tensor* A, const fp4_tensor* B, const void* P, const void* Q, int r,
-                            float beta, void* C, int c_dtype, int64_t ldc, cudaStream_t s) {
+                            float beta, void* C, int c_dtype, int64_t ldc, cudaStream_t s, void* sk_ws = nullptr,
+                            size_t sk_bytes = 0) {
   fp4_status st;
   if ((st = check_tensor(A, "A")) || (st = check_tensor(B, "B"))) return st;
   const int64_t M = A->rows, N = B->rows, K = A->cols;
@@ -174,6 +177,8 @@ static fp4_status gemm_impl(const fp4_tensor* A, const fp4_tensor* B, const void
   g.C = C;
   g.c_f32 = c_dtype == FP4_OUT_F32;
   g.ldc = ldc;
+  g.sk_ws = static_cast<float*>(sk_ws);
+  g.sk_ws_bytes = sk_ws ? sk_bytes : 0;
   CUDA_TRY(launch_gemm_nvf4(g, sm_count(), s));
   return FP4_OK;
 }
@@ -258,12 +263,19 @@ static fp4_status check_linear_fwd(const void* X, int64_t M, int64_t K, int64_t 
   return FP4_OK;
 }
 
+// Room for the GEMMs' split tail after the required part of a caller workspace of ws_bytes
+// bytes, or nullptr when it does not fit.
+static void* split_region(void* ws, size_t ws_bytes, size_t need) {
+  return ws_bytes >= need + gemm_splitk_ws_bytes(sm_count()) ? static_cast<uint8_t*>(ws) + need : nullptr;
+}
+
 // The forward's launches on a workspace `ws` already checked to hold fwd_ws(M, N, K, r) bytes:
 // the branch factor of X (its read of X also yields max |X|), the dual RTN quantization of X,
 // then the block-scaled GEMM with the fused branch.  With r = 0: amax, quantize, GEMM.
-static fp4_status linear_fwd_on(void* ws, const void* X, int64_t M, int64_t K, int64_t ldx, const fp4_tensor* Wq,
-                                const void* L1, const void* L2, int r, float beta, void* Y, int64_t ldy,
-                                const fp4_tensor* xqT_saved, cudaStream_t s) {
+// sk_ws: the GEMM's split-tail room (gemm_splitk_ws_bytes() bytes) or nullptr.
+static fp4_status linear_fwd_on(void* ws, void* sk_ws, const void* X, int64_t M, int64_t K, int64_t ldx,
+                                const fp4_tensor* Wq, const void* L1, const void* L2, int r, float beta, void* Y,
+                                int64_t ldy, const fp4_tensor* xqT_saved, cudaStream_t s) {
   fp4_status st;
   Carver c(ws);
   fp4_tensor xq;
@@ -275,7 +287,7 @@ static fp4_status linear_fwd_on(void* ws, const void* X, int64_t M, int64_t K, i
   } else if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, nullptr, &xq, xqT_saved, s))) {
     return st;
   }
-  return gemm_impl(&xq, Wq, P, L2, r, beta, Y, FP4_OUT_BF16, ldy, s);
+  return gemm_impl(&xq, Wq, P, L2, r, beta, Y, FP4_OUT_BF16, ldy, s, sk_ws, gemm_splitk_ws_bytes(sm_count()));
 }
 
 // Workspace of fp4_newton_schulz: the iterate's two NVFP4 forms, the m x m Gram
@@ -316,7 +328,9 @@ static size_t ns_ws(int64_t m, int64_t n, float c, Carver* c_opt, NsBufs* out) {
 // the module, so that call needs no allocation.  32 MiB holds the forward
 // workspace up to M * K ~ 50e6 elements at r = 64 (e.g. M = 16384, K = 3072).
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
-static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+// followed by the GEMM's split-tail room: 256 KB per CTA pair, enough for 160 SMs
+constexpr size_t kNoAllocSplitBytes = size_t(20) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes + kNoAllocSplitBytes];
 
 // Device address of g_noalloc_scratch on the current device, looked up on the
 // first call per device and cached for the life of the process (a
@@ -379,6 +393,19 @@ fp4_status fp4_gemm_blockscaled(const fp4_tensor* A, const fp4_tensor* B, const 
   return gemm_impl(A, B, P, Q, r, beta, C, c_dtype, ldc, static_cast<cudaStream_t>(stream));
 }
 
+size_t fp4_gemm_split_workspace(void) { return gemm_splitk_ws_bytes(sm_count()); }
+
+fp4_status fp4_gemm_blockscaled_ws(const fp4_tensor* A, const fp4_tensor* B, const void* P, const void* Q, int r,
+                                   float beta, void* C, int c_dtype, int64_t ldc, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  if (ws) {
+    const size_t need = gemm_splitk_ws_bytes(sm_count());
+    if (ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
+      return fail(FP4_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
+  }
+  return gemm_impl(A, B, P, Q, r, beta, C, c_dtype, ldc, static_cast<cudaStream_t>(stream), ws, ws_bytes);
+}
+
 fp4_status fp4_branch_factor(const void* X, int64_t M, int64_t K, int64_t ldx, const void* L, int r, void* P,
                              float* amax_out, void* stream) {
   if (amax_out && (reinterpret_cast<uintptr_t>(amax_out) & 3u))
@@ -402,7 +429,8 @@ fp4_status fp4_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx, cons
   const size_t need = fp4_linear_fwd_workspace(M, Wq->rows, K, r);
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
     return fail(FP4_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
-  return linear_fwd_on(ws, X, M, K, ldx, Wq, L1, L2, r, beta, Y, ldy, xqT_saved, static_cast<cudaStream_t>(stream));
+  return linear_fwd_on(ws, split_region(ws, ws_bytes, need), X, M, K, ldx, Wq, L1, L2, r, beta, Y, ldy, xqT_saved,
+                       static_cast<cudaStream_t>(stream));
 }
 
 fp4_status fp4_linear_fwd_noalloc(const void* X, int64_t M, int64_t K, int64_t ldx, const fp4_tensor* Wq,
@@ -418,7 +446,9 @@ fp4_status fp4_linear_fwd_noalloc(const void* X, int64_t M, int64_t K, int64_t l
                 (long long)M, (long long)K, r, need, kNoAllocScratchBytes);
   void* ws = nullptr;
   if ((st = noalloc_scratch(&ws))) return st;
-  return linear_fwd_on(ws, X, M, K, ldx, Wq, L1, L2, r, beta, Y, ldy, xqT_saved, static_cast<cudaStream_t>(stream));
+  void* sk = gemm_splitk_ws_bytes(sm_count()) <= kNoAllocSplitBytes ? static_cast<uint8_t*>(ws) + kNoAllocScratchBytes
+                                                                     : nullptr;
+  return linear_fwd_on(ws, sk, X, M, K, ldx, Wq, L1, L2, r, beta, Y, ldy, xqT_saved, static_cast<cudaStream_t>(stream));
 }
 
 fp4_status fp4_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t lddy, const fp4_tensor* WqT,
@@ -453,8 +483,10 @@ fp4_status fp4_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t lddy, co
   } else if ((st = quantize_impl(dY, M, N, lddy, FP4_ROUND_SR, seed, 0, 1, nullptr, &dyq, &dyqT, s))) {
     return st;
   }
-  if ((st = gemm_impl(&dyq, WqT, P2, L1T, r, beta, dX, FP4_OUT_BF16, lddx, s))) return st;
-  return gemm_impl(&dyqT, xqT_saved, nullptr, nullptr, 0, 0.0f, dW, dw_dtype, lddw, s);
+  void* sk = split_region(ws, ws_bytes, need);  // one region serves both GEMMs (same stream, in order)
+  const size_t skb = gemm_splitk_ws_bytes(sm_count());
+  if ((st = gemm_impl(&dyq, WqT, P2, L1T, r, beta, dX, FP4_OUT_BF16, lddx, s, sk, skb))) return st;
+  return gemm_impl(&dyqT, xqT_saved, nullptr, nullptr, 0, 0.0f, dW, dw_dtype, lddw, s, sk, skb);
 }
 
 fp4_status fp4_check_status(void* stream) {

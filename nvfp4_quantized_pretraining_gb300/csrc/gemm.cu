@@ -80,6 +80,13 @@ struct GemmParams {
   // 2-SM kernel tile order: 0 walks M fastest, 1 walks N fastest.  The larger operand is walked
   // slowest so that it streams from DRAM once while the smaller one stays resident in L2.
   int raster_n;
+  // 2-SM kernel, split tail: tiles [0, dp_tiles) are computed whole, round-robin over the CTA
+  // pairs; when sk_split = S > 0, each of the remaining tiles is cut into S pieces along K, one
+  // per pair, whose FP32 partial accumulators go to sk_ws (256 x 256 floats per piece) for
+  // gemm_splitk_reduce_kernel to sum.  sk_split = 0: every tile whole (dp_tiles unused).
+  uint32_t dp_tiles;
+  uint32_t sk_split;
+  float* sk_ws;
 };
 
 __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
@@ -418,11 +425,59 @@ static_assert(TM_SF + STAGES * TM_SF_STAGE <= TM_COLS, "TMEM budget");
 // warps: 0 A/B producer, 1 MMA (leader) + TMEM allocator, 2 scale/P producer,
 // 3..10 scale stagers (two per TMEM lane quadrant, two K steps each), 11..18 epilogue
 constexpr int FIRST_EPI_WARP = 11;
+// Split the tail wave only when K >= 48 * 256: the last wave's few pairs run with the L2 to
+// themselves, faster than a full wave, so shorter pieces do not repay the partial stores and
+// the reduction's launch (measured on the 3B block's GEMMs: a loss at K = 8192 and 9216, a gain
+// of 2-5% at K = 16384).
+constexpr uint32_t kSplitMinStages = 48;
 constexpr int NUM_THREADS = (FIRST_EPI_WARP + EPI_WARPS) * 32;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 1024 + 256;
 static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 }  // namespace g2
+
+// One unit of a CTA pair's work: a whole 256 x 256 tile, or K stages [kb, ke) of a tile of
+// the split tail, whose FP32 partial goes to workspace slot `slot`.
+struct PairWork {
+  uint32_t mb2, nb2, kb, ke;
+  int32_t slot;  // -1: the tile's result goes to C
+  bool branch;   // this unit adds the BF16 branch stage (a split tile's last piece)
+};
+
+// Unit i of cluster cid (of ncl): the whole tiles cid, cid + ncl, ... (below dp_tiles when the
+// tail is split), then, with a split tail, tail unit cid: tile dp_tiles + cid / S, K piece cid % S.
+// Every role of the kernel walks the same sequence.
+__device__ __forceinline__ bool pair_work(const GemmParams& p, uint32_t cid, uint32_t ncl, uint32_t i,
+                                          uint32_t tiles_m, uint32_t tiles_n, uint32_t num_k, bool has_branch,
+                                          PairWork& w) {
+  const uint32_t num_tiles = tiles_m * tiles_n;
+  uint32_t mt;
+  w.kb = 0;
+  w.ke = num_k;
+  w.slot = -1;
+  w.branch = has_branch;
+  if (p.sk_split == 0) {
+    mt = cid + i * ncl;
+    if (mt >= num_tiles) return false;
+  } else {
+    const uint32_t ndp = p.dp_tiles / ncl, S = p.sk_split;
+    if (i < ndp) {
+      mt = cid + i * ncl;
+    } else if (i == ndp && cid < (num_tiles - p.dp_tiles) * S) {
+      const uint32_t piece = cid % S;
+      mt = p.dp_tiles + cid / S;
+      w.kb = piece * num_k / S;
+      w.ke = (piece + 1) * num_k / S;
+      w.slot = (int32_t)cid;
+      w.branch = has_branch && piece == S - 1;
+    } else {
+      return false;
+    }
+  }
+  w.mb2 = p.raster_n ? mt / tiles_n : mt % tiles_m;
+  w.nb2 = p.raster_n ? mt % tiles_n : mt / tiles_m;
+  return true;
+}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -477,10 +532,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   const uint32_t cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
-  const uint32_t tiles_m = p.M / 256, tiles_n = p.N / 256, num_tiles = tiles_m * tiles_n;
+  const uint32_t tiles_m = p.M / 256, tiles_n = p.N / 256;
   const uint32_t num_k = (p.K + BK - 1) / BK;
   const bool has_branch = p.r > 0;
-  const uint32_t n_iter = num_k + (has_branch ? 1 : 0);
   float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
   if (alpha == 0.0f) alpha = 1.0f;  // an all-zero operand contributes exact zeros
 
@@ -491,10 +545,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
       const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);  // leader's full[] in the cluster window
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (uint32_t mt = cluster_id; mt < num_tiles && ok; mt += num_clusters) {
-        const uint32_t mb2 = p.raster_n ? mt / tiles_n : mt % tiles_m;
-        const uint32_t nb2 = p.raster_n ? mt % tiles_n : mt / tiles_m;
-        for (uint32_t it = 0; it < n_iter; ++it) {
+      PairWork w;
+      for (uint32_t wi = 0; ok && pair_work(p, cluster_id, num_clusters, wi, tiles_m, tiles_n, num_k, has_branch, w);
+           ++wi) {
+        const uint32_t mb2 = w.mb2, nb2 = w.nb2;
+        for (uint32_t it = w.kb; it < w.ke + (w.branch ? 1u : 0u); ++it) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             ok = false;
             break;
@@ -504,7 +559,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
           uint8_t* sSFA = sB + B_BYTES;
           uint8_t* sSFB = sSFA + SFA_BYTES;
           const uint32_t full_l = full0 + stage * 8;
-          if (it < num_k) {
+          if (it < w.ke) {
             if (ab) {
               if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A_BYTES + B_BYTES));
               const int32_t kx = (int32_t)(it * (BK / 2));
@@ -547,11 +602,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       uint32_t t = 0;
-      for (uint32_t mt = cluster_id; mt < num_tiles && ok; mt += num_clusters, ++t) {
+      PairWork w;
+      for (; ok && pair_work(p, cluster_id, num_clusters, t, tiles_m, tiles_n, num_k, has_branch, w); ++t) {
         if (*abort_flag || !mbar_wait_cluster(acc_empty, (t & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + TM_ACC;
-        for (uint32_t it = 0; it < num_k; ++it) {
+        for (uint32_t it = w.kb; it < w.ke; ++it) {
           if (!mbar_wait_cluster(&full[stage], phase)) {
             ok = false;
             break;
@@ -561,20 +617,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
           const uint32_t tsf = tmem + TM_SF + stage * TM_SF_STAGE;
           const uint32_t krem = p.K - it * BK;
           if (krem >= (uint32_t)BK) {
-            mma_nvf4_pair(d_tmem, ad, bd, idesc, tsf, tsf + 16, it != 0);
+            mma_nvf4_pair(d_tmem, ad, bd, idesc, tsf, tsf + 16, it != w.kb);
             mma_nvf4_pair(d_tmem, ad + 2, bd + 2, idesc, tsf + 4, tsf + 24, 1);
             mma_nvf4_pair(d_tmem, ad + 4, bd + 4, idesc, tsf + 8, tsf + 32, 1);
             mma_nvf4_pair(d_tmem, ad + 6, bd + 6, idesc, tsf + 12, tsf + 40, 1);
           } else {
             for (uint32_t kk = 0; kk < krem / 64; ++kk)
               mma_nvf4_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, tsf + kk * 4, tsf + 16 + kk * 8,
-                            (it | kk) != 0);
+                            it != w.kb || kk != 0);
           }
           tc_commit_pair_mc(&empty[stage], 3);
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
         if (!ok) break;
-        if (has_branch) {
+        if (w.branch) {
           if (!mbar_wait_cluster(&full[stage], phase)) { ok = false; break; }
           tc_fence_after();
           const uint64_t ad = adesc0 + stage * kStageD, bd = bdesc0 + stage * kStageD;
@@ -593,13 +649,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
       const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (uint32_t mt = cluster_id; mt < num_tiles && ok; mt += num_clusters) {
-        for (uint32_t it = 0; it < n_iter; ++it) {
+      PairWork w;
+      for (uint32_t wi = 0; ok && pair_work(p, cluster_id, num_clusters, wi, tiles_m, tiles_n, num_k, has_branch, w);
+           ++wi) {
+        for (uint32_t it = w.kb; it < w.ke + (w.branch ? 1u : 0u); ++it) {
           if (*abort_flag || !mbar_wait(&peer_ready[stage], phase)) {
             ok = false;
             break;
           }
-          if (it < num_k) mbar_arrive_cluster_relaxed(full0 + stage * 8);  // TMEM stores already complete
+          if (it < w.ke) mbar_arrive_cluster_relaxed(full0 + stage * 8);  // TMEM stores already complete
           else mbar_arrive_cluster(full0 + stage * 8);  // P~ was written through the generic proxy
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
@@ -613,15 +671,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
     const uint32_t lane_off = (quad * 32) << 16;
     const float g = __fdiv_rn(p.beta, alpha);
     uint32_t stage = 0, phase = 0;
-    for (uint32_t mt = cluster_id; mt < num_tiles; mt += num_clusters) {
+    PairWork w;
+    for (uint32_t wi = 0; pair_work(p, cluster_id, num_clusters, wi, tiles_m, tiles_n, num_k, has_branch, w); ++wi) {
       bool ok = true;
-      for (uint32_t it = 0; it < n_iter; ++it) {
+      for (uint32_t it = w.kb; it < w.ke + (w.branch ? 1u : 0u); ++it) {
         if (*abort_flag || !mbar_wait_warp(&sf_full[stage], phase)) {
           ok = false;
           break;
         }
         uint8_t* sA = smem + stage * STAGE_BYTES;
-        if (it < num_k) {
+        if (it < w.ke) {
           const uint32_t krem = p.K - it * BK;
           const uint32_t nk = krem >= (uint32_t)BK ? 4 : krem / 64;
           const uint8_t* sSFA = sA + A_BYTES + B_BYTES;
@@ -692,9 +751,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
     const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
     uint8_t* stg = sOut + (warp - FIRST_EPI_WARP) * 2 * CHUNK_BYTES;  // this warp's two staging chunks
     uint32_t t = 0;
-    for (uint32_t mt = cluster_id; mt < num_tiles; mt += num_clusters, ++t) {
-      const uint32_t mb2 = p.raster_n ? mt / tiles_n : mt % tiles_m;
-      const uint32_t nb2 = p.raster_n ? mt % tiles_n : mt / tiles_m;
+    PairWork w;
+    for (; pair_work(p, cluster_id, num_clusters, t, tiles_m, tiles_n, num_k, has_branch, w); ++t) {
+      const uint32_t mb2 = w.mb2, nb2 = w.nb2;
       if (*abort_flag || !mbar_wait_warp(acc_full, t & 1)) {
         *abort_flag = 1;
         break;
@@ -702,7 +761,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
       tc_fence_after();
       const uint32_t row0 = mb2 * 256 + rank * 128 + quad * 32;
       const uint32_t col0 = nb2 * 256 + h * 128;
-      if (!p.c_f32) {
+      if (w.slot >= 0) {
+        // a piece of a split tile: the raw FP32 accumulator to its slot, 256 x 256 row-major
+        float* part = p.sk_ws + (size_t)w.slot * 65536 + (size_t)(rank * 128 + quad * 32 + lane) * 256 + h * 128;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          uint32_t acc[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_ACC + h * 128 + j * 32, acc);
+          tmem_ld_wait(acc);
+          float4* dst = reinterpret_cast<float4*>(part + j * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(acc[4 * i]), __uint_as_float(acc[4 * i + 1]),
+                                 __uint_as_float(acc[4 * i + 2]), __uint_as_float(acc[4 * i + 3]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(acc_empty);
+          else mbar_arrive_cluster_relaxed(acc_empty0);
+        }
+      } else if (!p.c_f32) {
         // TMEM -> registers -> BF16.  The accumulator is released as soon as all four chunks are in
         // registers or staged: chunks 0 and 1 go to this warp's two swizzled shared chunks, 2 and 3
         // stay packed in registers until the first two TMA stores have read their buffers.
@@ -806,6 +885,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
     tmem_dealloc_pair(tmem, TM_COLS);
   }
   cluster_sync();
+}
+
+// The split tail's result: C = round_c(fl32(alpha * acc)) with acc the FP32 sum of a tile's
+// S partial accumulators taken in piece order (so the result does not depend on which pair
+// finished first).  One thread per 4 consecutive columns of one row of one tail tile.
+__global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(const GemmParams p, uint32_t tail_tiles) {
+  const uint32_t idx = blockIdx.x * 256 + threadIdx.x;
+  const uint32_t tt = idx >> 14;  // 16384 float4 per 256 x 256 tile
+  if (tt >= tail_tiles) return;
+  const uint32_t e = idx & 16383u, row = e >> 6, c4 = e & 63u;
+  const uint32_t S = p.sk_split;
+  const float4* part = reinterpret_cast<const float4*>(p.sk_ws) + (size_t)tt * S * 16384 + e;
+  float4 acc = part[0];
+#pragma unroll 4
+  for (uint32_t q = 1; q < S; ++q) {
+    const float4 v = part[(size_t)q * 16384];
+    acc.x = __fadd_rn(acc.x, v.x);
+    acc.y = __fadd_rn(acc.y, v.y);
+    acc.z = __fadd_rn(acc.z, v.z);
+    acc.w = __fadd_rn(acc.w, v.w);
+  }
+  float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
+  if (alpha == 0.0f) alpha = 1.0f;
+  const uint32_t tiles_m = p.M / 256, tiles_n = p.N / 256, mt = p.dp_tiles + tt;
+  const uint32_t mb2 = p.raster_n ? mt / tiles_n : mt % tiles_m;
+  const uint32_t nb2 = p.raster_n ? mt % tiles_n : mt / tiles_m;
+  const size_t off = (size_t)(mb2 * 256 + row) * p.ldc + nb2 * 256 + c4 * 4;
+  const float x = __fmul_rn(alpha, acc.x), y = __fmul_rn(alpha, acc.y), z = __fmul_rn(alpha, acc.z),
+              w = __fmul_rn(alpha, acc.w);
+  if (p.c_f32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(p.C) + off) = make_float4(x, y, z, w);
+  } else {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(x, y), hi = __floats2bfloat162_rn(z, w);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.C) + off) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1174,7 +1289,7 @@ static cudaError_t launch_gemm_single(const CUtensorMap& ta, const CUtensorMap& 
 
 static cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tp,
                                     const CUtensorMap& tq, const CUtensorMap& tc, const GemmParams& p, int num_sms,
-                                    cudaStream_t s) {
+                                    float* sk_ws, size_t sk_ws_bytes, cudaStream_t s) {
   using namespace g2;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -1194,10 +1309,34 @@ static cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb
   if (attr_err != cudaSuccess) return attr_err;
   const uint32_t tiles = (p.M / 256) * (p.N / 256);
   const uint32_t clusters = tiles < (uint32_t)max_clusters ? tiles : (uint32_t)max_clusters;
-  gemm_nvf4_pair_kernel<<<clusters * 2, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, tp, tq, tc, p);
+  GemmParams q = p;
+  q.sk_split = 0;
+  q.dp_tiles = tiles;
+  // Split tail: with W full waves and R < clusters tiles left over, the last wave would keep
+  // clusters - R pairs idle for a whole tile.  Cutting each of the R tiles into S = clusters / R
+  // K pieces (one per pair) ends the wave after about 1/S of a tile, plus the reduction.  Taken
+  // when the pieces stay long enough (K of at least kSplitMinStages stages) to repay the partial
+  // stores and the extra launch.
+  const uint32_t num_k = (p.K + BK - 1) / BK, rem = tiles % clusters;
+  if (sk_ws && tiles > clusters && rem > 0 && num_k >= kSplitMinStages) {
+    uint32_t S = clusters / rem;
+    if (S > num_k) S = num_k;
+    if (S >= 2 && (size_t)rem * S * 65536 * sizeof(float) <= sk_ws_bytes) {
+      q.sk_split = S;
+      q.dp_tiles = tiles - rem;
+      q.sk_ws = sk_ws;
+    }
+  }
+  gemm_nvf4_pair_kernel<<<clusters * 2, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, tp, tq, tc, q);
   count_launch();
+  if (q.sk_split) {
+    gemm_splitk_reduce_kernel<<<rem * 64, 256, 0, s>>>(q, rem);
+    count_launch();
+  }
   return cudaGetLastError();
 }
+
+size_t gemm_splitk_ws_bytes(int num_sms) { return (size_t)(num_sms / 2) * 65536 * sizeof(float); }
 
 cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
   using namespace g4;
@@ -1215,7 +1354,7 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
       tp = ta;
       tq = tb;
     }
-    GemmParams p;
+    GemmParams p{};
     p.a_scales = static_cast<const uint8_t*>(g.a_scales);
     p.b_scales = static_cast<const uint8_t*>(g.b_scales);
     p.a_scale = g.a_scale;
@@ -1237,7 +1376,7 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
     if (!g.c_f32 && !make_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.C, g.N, g.M, (uint64_t)g.ldc * 2, 32, 32,
                                CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
-    return launch_gemm_pair(ta, tb, tp, tq, tc, p, num_sms, s);
+    return launch_gemm_pair(ta, tb, tp, tq, tc, p, num_sms, g.sk_ws, g.sk_ws_bytes, s);
   }
   CUtensorMap ta, tb, tp, tq;
   if (!make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_codes, g.K / 2, g.M, g.K / 2, BK / 2, BM) ||
@@ -1251,7 +1390,7 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
     tp = ta;
     tq = tb;
   }
-  GemmParams p;
+  GemmParams p{};
   p.a_scales = static_cast<const uint8_t*>(g.a_scales);
   p.b_scales = static_cast<const uint8_t*>(g.b_scales);
   p.a_scale = g.a_scale;

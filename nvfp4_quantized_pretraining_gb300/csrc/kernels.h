@@ -50,8 +50,14 @@ struct GemmArgs {
   void* C;
   int c_f32;
   int64_t ldc;
+  // optional (nullptr: none): room for the split tail's FP32 partials, gemm_splitk_ws_bytes() bytes
+  float* sk_ws = nullptr;
+  size_t sk_ws_bytes = 0;
 };
 cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s);
+// Workspace that lets launch_gemm_nvf4 split the K range of its last partial wave of 256 x 256
+// tiles over the idle CTA pairs: one 256 x 256 FP32 slot per pair.
+size_t gemm_splitk_ws_bytes(int num_sms);
 
 // P = bf16(X L^T): X M x K (pitch ldx), L r x K, P M x r.
 // amax_out (optional, device): also reduces max |X| into it (zeroed by the launcher).

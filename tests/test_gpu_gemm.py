@@ -41,15 +41,15 @@ def quantize_both(F, oracle_mod, x, mode=0, seed=0, stream=0):
     return g, o
 
 
-def check_gemm(F, oracle_mod, M, N, K, r, out_dtype, beta, seed, rows=None, a_kind="normal"):
+def check_gemm(F, oracle_mod, M, N, K, r, out_dtype, beta, seed, rows=None, a_kind="normal", split=False):
     A = S.normal((M, K), 1.0, seed) if a_kind == "normal" else S.with_outlier_entries((M, K), 0.001, 50.0, seed)
     B = S.normal((N, K), 1.0, seed + 1)
     ga, oa = quantize_both(F, oracle_mod, A)
     gb, ob = quantize_both(F, oracle_mod, B)
     P = S.normal((M, r), 1.0, seed + 2) if r else None
     Q = S.normal((N, r), 1.0, seed + 3) if r else None
-    C = F.fp4_gemm_blockscaled(ga, gb, None if P is None else dev(P), None if Q is None else dev(Q), beta=beta,
-                               out_dtype=out_dtype)
+    gemm = F.fp4_gemm_blockscaled_ws if split else F.fp4_gemm_blockscaled
+    C = gemm(ga, gb, None if P is None else dev(P), None if Q is None else dev(Q), beta=beta, out_dtype=out_dtype)
     torch.cuda.synchronize()
     F.fp4_check_status()
     sel = slice(None) if rows is None else rows
@@ -127,17 +127,69 @@ def test_gemm_strided_bf16_output_pair_path(F, oracle_mod):
 
 # The block-scaled GEMM shape sweep at full size (M = N = K in {2048, 4096, 8192, 16384}, the
 # 16384 x 3072 x 8192 skinny shape and the 3072 x 8192 x 16384 dW shape), rank 0 and rank 64,
-# through the same launch configuration the benchmark times; 48 sampled output rows.
+# through the same launch configuration the benchmark times (the split-tail workspace given: the
+# last shape splits its last wave); 48 sampled output rows, four of them in the last 256
+# (where the split tiles of an M > N shape lie).
 GEMM_SWEEP = [(2048, 2048, 2048), (4096, 4096, 4096), (8192, 8192, 8192), (16384, 16384, 16384),
               (16384, 3072, 8192), (3072, 8192, 16384)]
+
+
+def sample_rows(M, n, seed):
+    rng = np.random.default_rng(seed)
+    tail = np.array([M - 256, M - 150, M - 77, M - 1])
+    rest = rng.choice(M - 256, n - tail.size, replace=False)
+    return np.sort(np.concatenate([rest, tail]))
 
 
 @pytest.mark.parametrize("r", [0, 64])
 @pytest.mark.parametrize("M,N,K", GEMM_SWEEP)
 def test_gemm_full_size_sampled_rows(F, oracle_mod, M, N, K, r):
-    rng = np.random.default_rng(M + N + r)
-    rows = np.sort(rng.choice(M, 48, replace=False))
-    check_gemm(F, oracle_mod, M, N, K, r, torch.bfloat16, beta=1.0, seed=17, rows=rows)
+    check_gemm(F, oracle_mod, M, N, K, r, torch.bfloat16, beta=1.0, seed=17, rows=sample_rows(M, 48, M + N + r),
+               split=True)
+
+
+# Split tail, whole output against the oracle: more 256 x 256 tiles than SM pairs with a partial
+# last wave, and K of at least 48 stages of 256, so that the last wave's tiles are cut along K
+# (M <= N: the tail is the last tile column; M > N: the last tile row; 12352 = 48.25 stages: a
+# ragged last stage in the last piece).  The call launches the GEMM and the reduction.
+@pytest.mark.parametrize("M,N,K,r,out_dtype", [
+    (2304, 2304, 12288, 64, torch.bfloat16),
+    (2560, 2048, 12288, 0, torch.float32),
+    (2304, 2560, 12352, 48, torch.float32),
+])
+def test_gemm_split_tail_whole_output(F, oracle_mod, M, N, K, r, out_dtype):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = (M // 256) * (N // 256)
+    assert tiles > sms // 2 and tiles % (sms // 2) != 0  # a partial last wave on this GPU
+    n0 = F.fp4_launch_count()
+    check_gemm(F, oracle_mod, M, N, K, r, out_dtype, beta=0.75 if r else 1.0, seed=M + K + r, split=True)
+    quantize_launches = 2
+    assert F.fp4_launch_count() - n0 == quantize_launches * 2 + 2  # amax + quantize per operand, GEMM + reduce
+
+
+def test_gemm_split_tail_is_deterministic(F):
+    # Outlier entries spread the block scales, so that FP32 accumulation rounds and the
+    # summation order shows (with N(0, 1) operands every partial sum is exact in FP32 and the
+    # split result equals the whole-tile one bit for bit).
+    M, N, K = 2304, 2304, 12288
+    ga = F.fp4_quantize(dev(S.with_outlier_entries((M, K), 0.01, 1000.0, 31)))
+    gb = F.fp4_quantize(dev(S.with_outlier_entries((N, K), 0.01, 1000.0, 32)))
+    ws = torch.empty(F.gemm_split_workspace(), dtype=torch.uint8, device=DEV)
+    torch.cuda.synchronize()
+    n0 = F.fp4_launch_count()
+    c1 = F.fp4_gemm_blockscaled_ws(ga, gb, out_dtype=torch.float32, workspace=ws)
+    assert F.fp4_launch_count() - n0 == 2  # the GEMM and the reduction of the split tail
+    c2 = F.fp4_gemm_blockscaled_ws(ga, gb, out_dtype=torch.float32, workspace=ws)
+    c0 = F.fp4_gemm_blockscaled(ga, gb, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    F.fp4_check_status()
+    assert torch.equal(c1, c2)
+    # the split changes only the FP32 summation order inside the tail tiles
+    diff = (c1 != c0).reshape(M // 256, 256, N // 256, 256).any(dim=3).any(dim=1)
+    tiles = (M // 256) * (N // 256)
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    assert int(diff.sum()) <= tiles % pairs
+    assert float((c1 - c0).abs().max()) <= 1e-4 * float(c0.abs().max())
 
 
 @pytest.mark.parametrize("M,K,r", [(128, 64, 16), (256, 512, 32), (384, 320, 48), (1024, 2048, 64),
