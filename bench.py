@@ -371,7 +371,7 @@ def breakdown(F, torch, projs, T, r, stream, dev, flush, args):
     gemm_flops = 0
     reps = max(2, min(args.steps, 5))
     kinds = {}
-    sk = torch.empty(F.gemm_split_workspace(), dtype=torch.uint8, device=dev)  # as the linear calls have
+    sk = torch.empty(F.gemm_blockscaled_workspace(T, r), dtype=torch.uint8, device=dev)
 
     def rec(kind, fn):
         e0 = torch.cuda.Event(enable_timing=True)
@@ -731,7 +731,7 @@ def gemm_one(F, torch, stream, dev, flush, args):
     P = torch.randn((M, r), generator=g, device=dev).to(torch.bfloat16) if r else None
     Q = torch.randn((N, r), generator=g, device=dev).to(torch.bfloat16) if r else None
     C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    sk = torch.empty(F.gemm_split_workspace(), dtype=torch.uint8, device=dev)
+    sk = torch.empty(F.gemm_blockscaled_workspace(M, r), dtype=torch.uint8, device=dev)
     fn = lambda: F.fp4_gemm_blockscaled_ws(qa, qb, P, Q, out=C, workspace=sk, stream=stream)
     with torch.cuda.stream(stream):
         for _ in range(args.steps):
@@ -754,7 +754,6 @@ def gemm_sweep(F, torch, S, stream, dev, flush, args):
     fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
     reps = max(3, min(args.steps, 7))
     out = {}
-    sk = torch.empty(F.gemm_split_workspace(), dtype=torch.uint8, device=dev)
     with torch.cuda.stream(stream):
         for (M, N, K) in S.GEMM_SWEEP:
             g = torch.Generator(device=dev)
@@ -765,6 +764,7 @@ def gemm_sweep(F, torch, S, stream, dev, flush, args):
             P = torch.randn((M, 64), generator=g, device=dev).to(torch.bfloat16)
             Q = torch.randn((N, 64), generator=g, device=dev).to(torch.bfloat16)
             C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            sk = torch.empty(F.gemm_blockscaled_workspace(M, 64), dtype=torch.uint8, device=dev)
             flops = 2.0 * M * N * K
             row = {}
             for r in (0, 64):
@@ -776,7 +776,7 @@ def gemm_sweep(F, torch, S, stream, dev, flush, args):
             ms = _median_ms(torch, stream, flush, lambda: torch.matmul(A, B.t(), out=C), reps)
             row["torch_bf16_matmul"] = {"ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
             out[f"{M}x{N}x{K}"] = row
-            del A, B, qa, qb, P, Q, C
+            del A, B, qa, qb, P, Q, C, sk
     F.fp4_check_status(stream)
     return {"bound": "tensor", "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "shapes": out,
             "note": "gemm_nvf4_pair_kernel; 2MNK FP4 FLOPs over the median call time (L2 flushed); the peak is "

@@ -139,17 +139,25 @@ fp4_status fp4_gemm_blockscaled(const fp4_tensor* A, const fp4_tensor* B,
  * device: 19 MiB on a 152-SM GPU). */
 size_t fp4_gemm_split_workspace(void);
 
-/* fp4_gemm_blockscaled with a workspace for a split tail.  When M and N are
- * multiples of 256, K is at least 48 * 256 and the 256 x 256 tiles fill
+/* Bytes of workspace for fp4_gemm_blockscaled_ws with A of M rows and rank r:
+ * fp4_gemm_split_workspace(), plus M * r BF16 values for P~ when r > 0. */
+size_t fp4_gemm_blockscaled_workspace(int64_t M, int r);
+
+/* fp4_gemm_blockscaled with a workspace.  With r > 0 the call first writes
+ * P~ (the fold above) into the workspace by a launch of its own, so that the
+ * GEMM loads P~ like any operand tile instead of rewriting P in shared memory
+ * (the same values, so the same result).  And it may split its tail: when M and
+ * N are multiples of 256, K is at least 48 * 256 and the 256 x 256 tiles fill
  * W >= 1 whole waves over the SM pairs plus R < pairs more, each of the last
  * R tiles is cut into S = pairs / R consecutive K ranges, computed by S pairs
  * in parallel; a second launch adds the S FP32 partial accumulators in K order
  * (the branch is in the last range) and rounds once, as for a whole tile.  So
  * the result equals fp4_gemm_blockscaled's up to the FP32 summation order
  * inside those tiles, and it is the same from run to run.
- * ws: NULL (no split: exactly fp4_gemm_blockscaled) or at least
- * fp4_gemm_split_workspace() bytes, 256-byte aligned (else FP4_ERR_WORKSPACE);
- * its content is scratch.  Calls that share one ws must be ordered. */
+ * ws: NULL (exactly fp4_gemm_blockscaled) or at least
+ * fp4_gemm_blockscaled_workspace(M, r) bytes, 256-byte aligned (else
+ * FP4_ERR_WORKSPACE); its content is scratch.  Calls that share one ws must be
+ * ordered. */
 fp4_status fp4_gemm_blockscaled_ws(const fp4_tensor* A, const fp4_tensor* B,
                                    const void* P, const void* Q, int r, float beta,
                                    void* C, int c_dtype, int64_t ldc,
@@ -178,7 +186,9 @@ size_t fp4_linear_bwd_workspace(int64_t M, int64_t N, int64_t K, int r);
  * the caller, reused across micro-batches); L1: r x K, L2: N x r BF16.
  * X is quantized RTN in both orientations from one read; the column form
  * (K x M) is written to xqT_saved (caller-owned) for the dW product of the
- * backward pass.  ws/ws_bytes: device workspace of at least
+ * backward pass.  The quantization of X also writes the GEMM's P~ (the fold of
+ * fp4_gemm_blockscaled) over P in the workspace, so the GEMM loads it as it is.
+ * ws/ws_bytes: device workspace of at least
  * fp4_linear_fwd_workspace(M, N, K, r) bytes, 256-byte aligned; with
  * fp4_gemm_split_workspace() bytes more, the GEMM may split its tail as
  * fp4_gemm_blockscaled_ws does. */
@@ -226,7 +236,9 @@ fp4_status fp4_linear_fwd_noalloc(const void* X, int64_t M, int64_t K, int64_t l
  * dY: M x N BF16 (pitch lddy), quantized with SR (seed; Philox stream 0 for
  * the row form used by dX, stream 1 for the column form used by dW).
  * WqT: K x N NVFP4 (W_res quantized column-wise, RTN); xqT_saved: K x M from
- * fp4_linear_fwd.  ws: at least fp4_linear_bwd_workspace(M, N, K, r) bytes;
+ * fp4_linear_fwd.  The quantization of dY also folds P' = bf16(dY L2) for the
+ * dX GEMM (as the forward does).  ws: at least fp4_linear_bwd_workspace(M, N,
+ * K, r) bytes;
  * with fp4_gemm_split_workspace() bytes more, the dX and dW GEMMs may split
  * their tails as fp4_gemm_blockscaled_ws does. */
 fp4_status fp4_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t lddy,

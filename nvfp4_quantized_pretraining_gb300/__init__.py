@@ -32,7 +32,8 @@ OUT_BF16 = 0
 OUT_F32 = 1
 
 EXPORTS = ["fp4_scale_bytes", "fp4_amax", "fp4_quantize", "fp4_quantize_transposed", "fp4_quantize_dual",
-           "fp4_gemm_blockscaled", "fp4_gemm_split_workspace", "fp4_gemm_blockscaled_ws", "fp4_branch_factor", "fp4_linear_fwd_workspace", "fp4_linear_bwd_workspace",
+           "fp4_gemm_blockscaled", "fp4_gemm_split_workspace", "fp4_gemm_blockscaled_workspace",
+           "fp4_gemm_blockscaled_ws", "fp4_branch_factor", "fp4_linear_fwd_workspace", "fp4_linear_bwd_workspace",
            "fp4_linear_fwd", "fp4_linear_fwd_noalloc", "fp4_linear_bwd", "fp4_lora_factor_grad_workspace",
            "fp4_lora_factor_grad", "fp4_lora_cholqr_workspace", "fp4_lora_cholqr", "fp4_lora_realign_workspace",
            "fp4_lora_realign", "fp4_newton_schulz_workspace", "fp4_newton_schulz", "fp4_qadamw_v_encode",
@@ -74,6 +75,7 @@ def lib() -> ctypes.CDLL:
         "fp4_quantize_dual": (i32, [P, i64, i64, i64, i32, u64, u32, u32, P, T, T, P]),
         "fp4_gemm_blockscaled": (i32, [T, T, P, P, i32, f32, P, i32, i64, P]),
         "fp4_gemm_split_workspace": (ctypes.c_size_t, []),
+        "fp4_gemm_blockscaled_workspace": (ctypes.c_size_t, [i64, i32]),
         "fp4_gemm_blockscaled_ws": (i32, [T, T, P, P, i32, f32, P, i32, i64, P, ctypes.c_size_t, P]),
         "fp4_branch_factor": (i32, [P, i64, i64, i64, P, i32, P, P, P]),
         "fp4_linear_fwd_workspace": (ctypes.c_size_t, [i64, i64, i64, i32]),
@@ -259,12 +261,17 @@ def gemm_split_workspace() -> int:
     return int(lib().fp4_gemm_split_workspace())
 
 
+def gemm_blockscaled_workspace(M, r) -> int:
+    return int(lib().fp4_gemm_blockscaled_workspace(M, r))
+
+
 def fp4_gemm_blockscaled_ws(A: NVFP4Tensor, B: NVFP4Tensor, P=None, Q=None, beta=1.0, out=None,
                             out_dtype=torch.bfloat16, workspace=None, stream=None) -> torch.Tensor:
-    """fp4_gemm_blockscaled with the split-tail workspace (allocated here when not given)."""
+    """fp4_gemm_blockscaled with a workspace (allocated here when not given): the branch fold by a
+    launch of its own, and the split tail."""
     r, out, c_dtype = _gemm_args(A, B, P, Q, out, out_dtype)
     if workspace is None:
-        workspace = torch.empty(gemm_split_workspace(), dtype=torch.uint8, device=A.codes.device)
+        workspace = torch.empty(gemm_blockscaled_workspace(A.rows, r), dtype=torch.uint8, device=A.codes.device)
     ca, cb = A.c(), B.c()
     _check(lib().fp4_gemm_blockscaled_ws(ctypes.byref(ca), ctypes.byref(cb), _ptr(P), _ptr(Q), r, float(beta),
                                          out.data_ptr(), c_dtype, out.stride(0), workspace.data_ptr(),

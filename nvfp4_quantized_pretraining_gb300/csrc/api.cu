@@ -88,7 +88,7 @@ static QOut qout(const fp4_tensor* t) { return QOut{t->codes, t->scales, t->scal
 static fp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld, int round_mode,
                                 uint64_t seed, uint32_t sr_row, uint32_t sr_col, const float* amax_opt,
                                 const fp4_tensor* out_row, const fp4_tensor* out_col, cudaStream_t s,
-                                const uint32_t* clip = nullptr) {
+                                const uint32_t* clip = nullptr, const BranchFold* fold = nullptr) {
   fp4_status st = check_bf16_input(x, rows, cols, ld, "x");
   if (st) return st;
   if (round_mode != FP4_ROUND_RTN && round_mode != FP4_ROUND_SR)
@@ -131,15 +131,16 @@ static fp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64
   if (out_row) r = qout(out_row);
   if (out_col) c = qout(out_col);
   CUDA_TRY(launch_quantize_dual(x, rows, cols, ld, sr, seed, sr_row, sr_col, amax, out_row ? &r : nullptr,
-                                out_col ? &c : nullptr, s, clip));
+                                out_col ? &c : nullptr, s, clip, fold));
   return FP4_OK;
 }
 
 // sk_ws (optional, 256-byte aligned, sk_bytes of room): lets the GEMM split its last partial wave
 // of tiles along K (gemm_splitk_ws_bytes() bytes are enough for any shape).
+// p_folded: P holds P~ already (the branch fold done by the caller's launch before this one).
 static fp4_status gemm_impl(const fp4_tensor* A, const fp4_tensor* B, const void* P, const void* Q, int r,
                             float beta, void* C, int c_dtype, int64_t ldc, cudaStream_t s, void* sk_ws = nullptr,
-                            size_t sk_bytes = 0) {
+                            size_t sk_bytes = 0, bool p_folded = false) {
   fp4_status st;
   if ((st = check_tensor(A, "A")) || (st = check_tensor(B, "B"))) return st;
   const int64_t M = A->rows, N = B->rows, K = A->cols;
@@ -179,6 +180,7 @@ static fp4_status gemm_impl(const fp4_tensor* A, const fp4_tensor* B, const void
   g.ldc = ldc;
   g.sk_ws = static_cast<float*>(sk_ws);
   g.sk_ws_bytes = sk_ws ? sk_bytes : 0;
+  g.p_folded = p_folded;
   CUDA_TRY(launch_gemm_nvf4(g, sm_count(), s));
   return FP4_OK;
 }
@@ -282,12 +284,15 @@ static fp4_status linear_fwd_on(void* ws, void* sk_ws, const void* X, int64_t M,
   void* P = nullptr;
   fwd_ws(M, Wq->rows, K, r, &c, &xq, &P);
   if (r > 0) {
+    // the quantizer also folds P for the GEMM (P~ = bf16(P * beta / (S_tX S_tW)), in place)
+    const BranchFold fold{P, r, Wq->scale, beta};
     if ((st = branch_impl(X, M, K, ldx, L1, r, P, s, &xq.scale[1]))) return st;
-    if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, &xq.scale[1], &xq, xqT_saved, s))) return st;
+    if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, &xq.scale[1], &xq, xqT_saved, s, nullptr, &fold)))
+      return st;
   } else if ((st = quantize_impl(X, M, K, ldx, FP4_ROUND_RTN, 0, 0, 0, nullptr, &xq, xqT_saved, s))) {
     return st;
   }
-  return gemm_impl(&xq, Wq, P, L2, r, beta, Y, FP4_OUT_BF16, ldy, s, sk_ws, gemm_splitk_ws_bytes(sm_count()));
+  return gemm_impl(&xq, Wq, P, L2, r, beta, Y, FP4_OUT_BF16, ldy, s, sk_ws, gemm_splitk_ws_bytes(sm_count()), r > 0);
 }
 
 // Workspace of fp4_newton_schulz: the iterate's two NVFP4 forms, the m x m Gram
@@ -395,15 +400,32 @@ fp4_status fp4_gemm_blockscaled(const fp4_tensor* A, const fp4_tensor* B, const 
 
 size_t fp4_gemm_split_workspace(void) { return gemm_splitk_ws_bytes(sm_count()); }
 
+size_t fp4_gemm_blockscaled_workspace(int64_t M, int r) {
+  return gemm_splitk_ws_bytes(sm_count()) + (r > 0 && M > 0 ? round256(static_cast<size_t>(M) * r * 2) : 0);
+}
+
 fp4_status fp4_gemm_blockscaled_ws(const fp4_tensor* A, const fp4_tensor* B, const void* P, const void* Q, int r,
                                    float beta, void* C, int c_dtype, int64_t ldc, void* ws, size_t ws_bytes,
                                    void* stream) {
-  if (ws) {
-    const size_t need = gemm_splitk_ws_bytes(sm_count());
-    if (ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
-      return fail(FP4_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!ws) return gemm_impl(A, B, P, Q, r, beta, C, c_dtype, ldc, s);
+  fp4_status st;
+  if ((st = check_tensor(A, "A")) || (st = check_tensor(B, "B"))) return st;
+  if (r != 0 && r != 16 && r != 32 && r != 48 && r != 64)
+    return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rank r=%d not in {0,16,32,48,64}", r);
+  if (r > 0 && (!P || !Q)) return fail(FP4_ERR_INVALID_ARG, "r > 0 needs P and Q");
+  if (r > 0 && (!aligned16(P) || !aligned16(Q))) return fail(FP4_ERR_MISALIGNED, "P and Q must be 16-byte aligned");
+  const size_t split = gemm_splitk_ws_bytes(sm_count());
+  const size_t need = fp4_gemm_blockscaled_workspace(A->rows, r);
+  if (ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return fail(FP4_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
+  if (r > 0) {
+    // the branch fold by its own launch, into the workspace after the split-tail room
+    void* Pt = static_cast<uint8_t*>(ws) + split;
+    CUDA_TRY(launch_fold_branch(P, A->rows, r, A->scale, B->scale, beta, Pt, s));
+    return gemm_impl(A, B, Pt, Q, r, beta, C, c_dtype, ldc, s, ws, split, true);
   }
-  return gemm_impl(A, B, P, Q, r, beta, C, c_dtype, ldc, static_cast<cudaStream_t>(stream), ws, ws_bytes);
+  return gemm_impl(A, B, P, Q, r, beta, C, c_dtype, ldc, s, ws, split);
 }
 
 fp4_status fp4_branch_factor(const void* X, int64_t M, int64_t K, int64_t ldx, const void* L, int r, void* P,
@@ -479,13 +501,16 @@ fp4_status fp4_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t lddy, co
     CUDA_TRY(launch_transpose_bf16(L2, N, r, L2T, s));
     if ((st = branch_impl(dY, M, N, lddy, L2T, r, P2, s, &dyq.scale[1]))) return st;
     CUDA_TRY(launch_transpose_bf16(L1, r, K, L1T, s));
-    if ((st = quantize_impl(dY, M, N, lddy, FP4_ROUND_SR, seed, 0, 1, &dyq.scale[1], &dyq, &dyqT, s))) return st;
+    // the quantizer also folds P' for the dX GEMM (P'~ = bf16(P' * beta / (S_tdY S_tW)), in place)
+    const BranchFold fold{P2, r, WqT->scale, beta};
+    if ((st = quantize_impl(dY, M, N, lddy, FP4_ROUND_SR, seed, 0, 1, &dyq.scale[1], &dyq, &dyqT, s, nullptr, &fold)))
+      return st;
   } else if ((st = quantize_impl(dY, M, N, lddy, FP4_ROUND_SR, seed, 0, 1, nullptr, &dyq, &dyqT, s))) {
     return st;
   }
   void* sk = split_region(ws, ws_bytes, need);  // one region serves both GEMMs (same stream, in order)
   const size_t skb = gemm_splitk_ws_bytes(sm_count());
-  if ((st = gemm_impl(&dyq, WqT, P2, L1T, r, beta, dX, FP4_OUT_BF16, lddx, s, sk, skb))) return st;
+  if ((st = gemm_impl(&dyq, WqT, P2, L1T, r, beta, dX, FP4_OUT_BF16, lddx, s, sk, skb, r > 0))) return st;
   return gemm_impl(&dyqT, xqT_saved, nullptr, nullptr, 0, 0.0f, dW, dw_dtype, lddw, s, sk, skb);
 }
 

@@ -87,6 +87,10 @@ struct GemmParams {
   uint32_t dp_tiles;
   uint32_t sk_split;
   float* sk_ws;
+  // 2-SM kernel: P holds P~ already (folded before the launch), so the branch stage is loaded by
+  // TMA like any operand stage (P and Q both complete on the leader's barrier) and the scale
+  // warps leave it alone; 0: they fold P into P~ in shared memory
+  int p_folded;
 };
 
 __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
@@ -299,7 +303,7 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
           tmem_st_wait(wb);
           tmem_st_wait(wa);
           tc_fence_before();
-        } else {
+        } else if (!p.p_folded) {
           // branch stage: P~ = bf16(P * g) in place (an elementwise map, so the swizzle is irrelevant)
           uint4* tile = reinterpret_cast<uint4*>(smem + stage * STAGE_BYTES);
           const int tid = (warp - 2) * 32 + lane;
@@ -577,6 +581,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
               bulk_load(sSFB + 4 * SF_ATOM, p.b_scales + ((size_t)(nb2 * 2 + 1) * p.atoms_k + ka) * SF_ATOM,
                         nk * SF_ATOM, &sf_full[stage]);
             }
+          } else if (p.p_folded) {
+            // P~ and Q by TMA, both completing on the leader's barrier; the scale warps only pass
+            if (ab) {
+              if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (P_BYTES + Q_BYTES));
+              tma_load_2d_pair(sA, &tmap_p, full_l, 0, (int32_t)(mb2 * 256 + rank * 128));
+              tma_load_2d_pair(sB, &tmap_q, full_l, 0, (int32_t)(nb2 * 256 + rank * 128));
+            } else {
+              mbar_arrive(&sf_full[stage]);
+            }
           } else {
             if (ab) {
               if (leader) mbar_arrive_expect_tx(&full[stage], 2 * Q_BYTES);
@@ -657,7 +670,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
             ok = false;
             break;
           }
-          if (it < w.ke) mbar_arrive_cluster_relaxed(full0 + stage * 8);  // TMEM stores already complete
+          // K stage: the TMEM stores are complete; a folded branch stage: nothing was written
+          if (it < w.ke || p.p_folded) mbar_arrive_cluster_relaxed(full0 + stage * 8);
           else mbar_arrive_cluster(full0 + stage * 8);  // P~ was written through the generic proxy
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
@@ -715,7 +729,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
           tmem_st_wait(wb);
           tmem_st_wait8(wa);
           tc_fence_before();
-        } else {
+        } else if (!p.p_folded) {
           // branch stage: P~ = bf16(P * g) in place (an elementwise map, so the swizzle is irrelevant)
           uint4* tile = reinterpret_cast<uint4*>(sA);
           const int tid = (warp - 3) * 32 + lane;
@@ -921,6 +935,32 @@ __global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(const GemmParam
     *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.C) + off) =
         make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
   }
+}
+
+// The branch fold on its own (the scale warps' in-kernel form, run before the GEMM):
+// Pt = bf16(fl32(P * g)), g = fl32(beta / alpha), alpha = fl32(S_tA * S_tB) (1 when 0).
+__global__ void __launch_bounds__(256) fold_branch_kernel(const uint32_t* __restrict__ P, uint32_t nwords,
+                                                          const float* a_scale, const float* b_scale, float beta,
+                                                          uint32_t* __restrict__ Pt) {
+  float alpha = __fmul_rn(*a_scale, *b_scale);
+  if (alpha == 0.0f) alpha = 1.0f;
+  const float g = __fdiv_rn(beta, alpha);
+  for (uint32_t i = blockIdx.x * 256 + threadIdx.x; i < nwords; i += gridDim.x * 256) {
+    const uint32_t v = P[i];
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(bf16_lo(v), g), __fmul_rn(bf16_hi(v), g));
+    Pt[i] = *reinterpret_cast<uint32_t*>(&b2);
+  }
+}
+
+cudaError_t launch_fold_branch(const void* P, int64_t M, int r, const float* a_scale, const float* b_scale,
+                               float beta, void* Pt, cudaStream_t s) {
+  const uint32_t nwords = static_cast<uint32_t>(M * r / 2);
+  uint32_t blocks = (nwords + 255) / 256;
+  if (blocks > 1024) blocks = 1024;
+  fold_branch_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint32_t*>(P), nwords, a_scale, b_scale, beta,
+                                            static_cast<uint32_t*>(Pt));
+  count_launch();
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
@@ -1371,6 +1411,7 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
     p.c_f32 = g.c_f32;
     p.ldc = g.ldc;
     p.raster_n = g.M > g.N ? 1 : 0;  // A (M x K) is the larger operand: walk N fastest
+    p.p_folded = g.p_folded && g.r > 0;
     // BF16 output leaves through TMA stores of 32 x 32 tiles (64-byte rows, 64-byte swizzle)
     CUtensorMap tc = ta;
     if (!g.c_f32 && !make_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.C, g.N, g.M, (uint64_t)g.ldc * 2, 32, 32,
@@ -1407,6 +1448,7 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
   p.c_f32 = g.c_f32;
   p.ldc = g.ldc;
   p.raster_n = 0;
+  p.p_folded = g.p_folded && g.r > 0;  // the scale warps skip their fold (one CTA: a local arrive)
   return launch_gemm_single(ta, tb, tp, tq, p, num_sms, s);
 }
 

@@ -27,9 +27,21 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, f
 
 // clip (optional, device, both orientations with RTN only): |x| is clipped to this BF16
 // magnitude pattern before quantization.
+// The block-scaled GEMM's branch fold, P~ = bf16(fl32(P * fl32(beta / alpha))) in place with
+// alpha = fl32(S_tA * S_tB) (1 when 0): P rows x r BF16 (pitch r); other_scale: the S_t of the
+// GEMM's other operand (device).
+struct BranchFold {
+  void* P;
+  int r;
+  const float* other_scale;
+  float beta;
+};
+// fold (optional): the quantizer also folds P for the GEMM that consumes its row form (x's rows
+// are P's rows; S_tA is the quantizer's own tensor scale).
 cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
                                  uint32_t stream_r, uint32_t stream_c, const float* amax, const QOut* row_out,
-                                 const QOut* col_out, cudaStream_t s, const uint32_t* clip = nullptr);
+                                 const QOut* col_out, cudaStream_t s, const uint32_t* clip = nullptr,
+                                 const BranchFold* fold = nullptr);
 cudaError_t launch_debug_convert(const float* in, int64_t n, uint8_t* e2m1, uint8_t* e4m3, cudaStream_t s);
 cudaError_t launch_debug_sr_round(const float* in, const uint16_t* rnd, int64_t n, uint8_t* e2m1, cudaStream_t s);
 
@@ -53,11 +65,16 @@ struct GemmArgs {
   // optional (nullptr: none): room for the split tail's FP32 partials, gemm_splitk_ws_bytes() bytes
   float* sk_ws = nullptr;
   size_t sk_ws_bytes = 0;
+  // P already holds P~ (the branch fold done before the GEMM): the GEMM loads it as it is
+  bool p_folded = false;
 };
 cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s);
 // Workspace that lets launch_gemm_nvf4 split the K range of its last partial wave of 256 x 256
 // tiles over the idle CTA pairs: one 256 x 256 FP32 slot per pair.
 size_t gemm_splitk_ws_bytes(int num_sms);
+// The branch fold on its own: Pt = P~ for the GEMM of a_scale's and b_scale's operands.
+cudaError_t launch_fold_branch(const void* P, int64_t M, int r, const float* a_scale, const float* b_scale,
+                               float beta, void* Pt, cudaStream_t s);
 
 // P = bf16(X L^T): X M x K (pitch ldx), L r x K, P M x r.
 // amax_out (optional, device): also reduces max |X| into it (zeroed by the launcher).

@@ -11,6 +11,8 @@
 // tensor_scale() in common.cuh.
 #include <mutex>
 
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "scale_layout.cuh"
@@ -96,6 +98,15 @@ struct DualQuantArgs {
   PhiloxKeys keys;  // SR: the round keys of the seed (read from the parameter bank, no registers held)
   uint32_t stream_r, stream_c;
   const uint32_t* clip;  // CLIP: |x| is clipped to this BF16 magnitude pattern as the tile is staged
+  // Optional, for the GEMM that consumes the row form: its BF16 branch factor P (rows x fold_r,
+  // pitch fold_r) rewritten in place as P~ = bf16(fl32(P * fl32(beta / alpha))), alpha =
+  // fl32(S_t * the GEMM's other operand's S_t) (1 when 0), the branch fold of the block-scaled
+  // GEMM, done here because this kernel knows S_t.  The CTAs of the first tile column each take
+  // their tile's rows.
+  uint16_t* fold_p;
+  const float* fold_other;
+  float fold_beta;
+  uint32_t fold_r;
 };
 
 // The block-scale arithmetic of block_scale() (common.cuh) with its per-tensor parts set up
@@ -165,6 +176,18 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 6 : 10) quantize_dual_kerne
     const uint32_t row = r0 + (q >> 4), c8 = (c0 >> 3) + (q & 15);
     w[i] = make_uint4(0, 0, 0, 0);
     if (row < a.rows && c8 < a.cpr) w[i] = __ldcs(reinterpret_cast<const uint4*>(a.x + row * a.ld + c8 * 8));
+  }
+  if (a.fold_p && blockIdx.x == 0) {  // (overlaps the tile's loads in flight)
+    float alpha = __fmul_rn(S_t, *a.fold_other);
+    if (alpha == 0.0f) alpha = 1.0f;
+    const float g = __fdiv_rn(a.fold_beta, alpha);
+    const uint32_t nrow = a.rows - r0 < (uint32_t)kTileR ? a.rows - r0 : (uint32_t)kTileR;
+    uint32_t* P = reinterpret_cast<uint32_t*>(a.fold_p + (size_t)r0 * a.fold_r);
+    for (uint32_t i = tid; i < nrow * a.fold_r / 2; i += kDualThreads) {
+      const uint32_t v = P[i];
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(bf16_lo(v), g), __fmul_rn(bf16_hi(v), g));
+      P[i] = *reinterpret_cast<uint32_t*>(&b2);
+    }
   }
   if (COL && SR) {
     // the column form's random bits first: their ALU work overlaps the global loads in flight.
@@ -382,9 +405,15 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, f
 
 cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
                                  uint32_t stream_r, uint32_t stream_c, const float* amax, const QOut* row_out,
-                                 const QOut* col_out, cudaStream_t s, const uint32_t* clip) {
+                                 const QOut* col_out, cudaStream_t s, const uint32_t* clip, const BranchFold* fold) {
   DualQuantArgs a{};
   a.clip = clip;
+  if (fold) {
+    a.fold_p = static_cast<uint16_t*>(fold->P);
+    a.fold_other = fold->other_scale;
+    a.fold_beta = fold->beta;
+    a.fold_r = static_cast<uint32_t>(fold->r);
+  }
   a.x = static_cast<const uint16_t*>(x);
   a.ld = ld;
   a.rows = static_cast<uint32_t>(rows);

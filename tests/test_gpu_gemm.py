@@ -95,6 +95,26 @@ def test_gemm_outliers_and_rank0_equivalence(F, oracle_mod):
     assert torch.equal(c0, c1)
 
 
+@pytest.mark.parametrize("M,N,K,r", [(512, 512, 2048, 64), (384, 256, 512, 32), (256, 256, 320, 16)])
+def test_gemm_prefolded_branch_equals_in_kernel_fold(F, M, N, K, r):
+    # fp4_gemm_blockscaled_ws writes P~ by a launch of its own and the GEMM loads it as it is
+    # (the 2-SM kernel and, for 384 x 256, the one-CTA kernel); no split at these sizes, so the
+    # output equals the in-kernel fold's bit for bit
+    ga = F.fp4_quantize(dev(S.normal((M, K), 1.0, M + r)))
+    gb = F.fp4_quantize(dev(S.normal((N, K), 1.0, N + r)))
+    P = dev(S.normal((M, r), 1.0, 5))
+    Q = dev(S.normal((N, r), 1.0, 6))
+    for out_dtype in (torch.bfloat16, torch.float32):
+        c0 = F.fp4_gemm_blockscaled(ga, gb, P, Q, beta=0.3, out_dtype=out_dtype)
+        n0 = F.fp4_launch_count()
+        c1 = F.fp4_gemm_blockscaled_ws(ga, gb, P, Q, beta=0.3, out_dtype=out_dtype)
+        assert F.fp4_launch_count() - n0 == 2  # the fold and the GEMM
+        torch.cuda.synchronize()
+        F.fp4_check_status()
+        assert torch.equal(c0.view(torch.int16) if out_dtype == torch.bfloat16 else c0,
+                           c1.view(torch.int16) if out_dtype == torch.bfloat16 else c1)
+
+
 def test_gemm_strided_output(F, oracle_mod):
     A = S.normal((128, 256), 1.0, 6)
     B = S.normal((256, 256), 1.0, 7)
@@ -151,7 +171,8 @@ def test_gemm_full_size_sampled_rows(F, oracle_mod, M, N, K, r):
 # Split tail, whole output against the oracle: more 256 x 256 tiles than SM pairs with a partial
 # last wave, and K of at least 48 stages of 256, so that the last wave's tiles are cut along K
 # (M <= N: the tail is the last tile column; M > N: the last tile row; 12352 = 48.25 stages: a
-# ragged last stage in the last piece).  The call launches the GEMM and the reduction.
+# ragged last stage in the last piece).  The call launches the GEMM and the reduction (after the
+# branch fold when r > 0).
 @pytest.mark.parametrize("M,N,K,r,out_dtype", [
     (2304, 2304, 12288, 64, torch.bfloat16),
     (2560, 2048, 12288, 0, torch.float32),
@@ -163,8 +184,8 @@ def test_gemm_split_tail_whole_output(F, oracle_mod, M, N, K, r, out_dtype):
     assert tiles > sms // 2 and tiles % (sms // 2) != 0  # a partial last wave on this GPU
     n0 = F.fp4_launch_count()
     check_gemm(F, oracle_mod, M, N, K, r, out_dtype, beta=0.75 if r else 1.0, seed=M + K + r, split=True)
-    quantize_launches = 2
-    assert F.fp4_launch_count() - n0 == quantize_launches * 2 + 2  # amax + quantize per operand, GEMM + reduce
+    # amax + quantize per operand; the branch fold (r > 0); the GEMM and the reduction
+    assert F.fp4_launch_count() - n0 == 2 * 2 + (1 if r else 0) + 2
 
 
 def test_gemm_split_tail_is_deterministic(F):
