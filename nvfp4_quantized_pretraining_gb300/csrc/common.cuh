@@ -33,6 +33,15 @@ __device__ __forceinline__ void drain_pause() {
   while (clock64() - t0 < 4000000ll) __nanosleep(2000);
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic stream serialization
+// attribute (launch_pdl) may start while the kernel before it in the stream is still running:
+// pdl_wait() blocks until that kernel has completed and its memory operations are visible (a
+// no-op for a kernel launched normally), so nothing produced or read by it may be touched before.
+// pdl_trigger() lets the next such kernel start launching once every CTA of this grid has called
+// it or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

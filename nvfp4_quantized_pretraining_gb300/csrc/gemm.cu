@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_p, const __grid_constant__ CUtensorMap tmap_q,
                      const GemmParams p) {
+  pdl_trigger();
   using namespace g4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -138,6 +139,7 @@ __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // (the set-up above touches no global data)
 
   // 128 x 128 output tiles, M fastest; the CTAs walk them persistently
   const uint32_t num_tiles = p.num_m * p.num_n;
@@ -488,6 +490,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
                           const __grid_constant__ CUtensorMap tmap_p, const __grid_constant__ CUtensorMap tmap_q,
                           const __grid_constant__ CUtensorMap tmap_c, const GemmParams p) {
   using namespace g2;
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sOut = smem + STAGES * STAGE_BYTES;
@@ -534,6 +537,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // (the set-up above touches no global data)
 
   const uint32_t cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
   const uint32_t tiles_m = p.M / 256, tiles_n = p.N / 256;
@@ -905,6 +909,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
 // S partial accumulators taken in piece order (so the result does not depend on which pair
 // finished first).  One thread per 4 consecutive columns of one row of one tail tile.
 __global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(const GemmParams p, uint32_t tail_tiles) {
+  pdl_trigger();
+  pdl_wait();
   const uint32_t idx = blockIdx.x * 256 + threadIdx.x;
   const uint32_t tt = idx >> 14;  // 16384 float4 per 256 x 256 tile
   if (tt >= tail_tiles) return;
@@ -942,6 +948,8 @@ __global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(const GemmParam
 __global__ void __launch_bounds__(256) fold_branch_kernel(const uint32_t* __restrict__ P, uint32_t nwords,
                                                           const float* a_scale, const float* b_scale, float beta,
                                                           uint32_t* __restrict__ Pt) {
+  pdl_trigger();
+  pdl_wait();
   float alpha = __fmul_rn(*a_scale, *b_scale);
   if (alpha == 0.0f) alpha = 1.0f;
   const float g = __fdiv_rn(beta, alpha);
@@ -957,10 +965,10 @@ cudaError_t launch_fold_branch(const void* P, int64_t M, int r, const float* a_s
   const uint32_t nwords = static_cast<uint32_t>(M * r / 2);
   uint32_t blocks = (nwords + 255) / 256;
   if (blocks > 1024) blocks = 1024;
-  fold_branch_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint32_t*>(P), nwords, a_scale, b_scale, beta,
-                                            static_cast<uint32_t*>(Pt));
+  const cudaError_t e = launch_pdl(fold_branch_kernel, dim3(blocks), dim3(256), 0, s, static_cast<const uint32_t*>(P),
+                                   nwords, a_scale, b_scale, beta, static_cast<uint32_t*>(Pt));
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 // ---------------------------------------------------------------------------
@@ -1008,6 +1016,7 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
     branch_factor_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_l,
                          uint32_t K, int r, __nv_bfloat16* __restrict__ P, unsigned int* __restrict__ amax_out) {
   using namespace bf;
+  pdl_trigger();
   constexpr int NST = SPLIT ? SPLIT_STAGES : STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1034,6 +1043,7 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // (the set-up above touches no global data)
   const uint32_t num_k_all = (K + BK - 1) / BK;
   const uint32_t kh = SPLIT ? (num_k_all + 1) / 2 : num_k_all;
   const uint32_t k_begin = rank * kh;                 // this CTA's first K stage
@@ -1221,6 +1231,8 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
 // ---------------------------------------------------------------------------
 __global__ void transpose_bf16_kernel(const uint16_t* __restrict__ in, uint32_t rows, uint32_t cols,
                                       uint16_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ uint16_t t[32][33];
   const uint32_t c = blockIdx.x * 32 + threadIdx.x;
   for (uint32_t i = threadIdx.y; i < 32; i += blockDim.y) {
@@ -1322,9 +1334,9 @@ static cudaError_t launch_gemm_single(const CUtensorMap& ta, const CUtensorMap& 
   // one CTA per SM (its shared memory allows no more), at most one per tile
   const uint32_t tiles = p.num_m * p.num_n;
   const uint32_t grid = tiles < (uint32_t)num_sms ? tiles : (uint32_t)num_sms;
-  gemm_nvf4_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, tp, tq, p);
+  const cudaError_t e = launch_pdl(gemm_nvf4_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, ta, tb, tp, tq, p);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 static cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tp,
@@ -1367,13 +1379,14 @@ static cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb
       q.sk_ws = sk_ws;
     }
   }
-  gemm_nvf4_pair_kernel<<<clusters * 2, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, tp, tq, tc, q);
+  cudaError_t e =
+      launch_pdl(gemm_nvf4_pair_kernel, dim3(clusters * 2), dim3(NUM_THREADS), SMEM_BYTES, s, ta, tb, tp, tq, tc, q);
   count_launch();
-  if (q.sk_split) {
-    gemm_splitk_reduce_kernel<<<rem * 64, 256, 0, s>>>(q, rem);
+  if (e == cudaSuccess && q.sk_split) {
+    e = launch_pdl(gemm_splitk_reduce_kernel, dim3(rem * 64), dim3(256), 0, s, q, rem);
     count_launch();
   }
-  return cudaGetLastError();
+  return e;
 }
 
 size_t gemm_splitk_ws_bytes(int num_sms) { return (size_t)(num_sms / 2) * 65536 * sizeof(float); }
@@ -1482,7 +1495,7 @@ cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ld
   if (blocks < num_sms && num_k >= 2) {
     // fewer row blocks than SMs: two CTAs (a cluster) per row block, half of K each
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     cfg.gridDim = dim3(2 * blocks);
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = kSmemSplit;
@@ -1491,12 +1504,14 @@ cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ld
     at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, branch_factor_kernel<true>, tx, tl, (uint32_t)K, r, Pb, am);
   } else {
-    branch_factor_kernel<false><<<blocks, NUM_THREADS, SMEM_BYTES, s>>>(tx, tl, (uint32_t)K, r, Pb, am);
-    e = cudaGetLastError();
+    e = launch_pdl(branch_factor_kernel<false>, dim3(blocks), dim3(NUM_THREADS), SMEM_BYTES, s, tx, tl, (uint32_t)K, r,
+                   Pb, am);
   }
   count_launch();
   return e;
@@ -1505,10 +1520,10 @@ cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ld
 cudaError_t launch_transpose_bf16(const void* in, int64_t rows, int64_t cols, void* out, cudaStream_t s) {
   dim3 block(32, 8);
   dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32));
-  transpose_bf16_kernel<<<grid, block, 0, s>>>(static_cast<const uint16_t*>(in), (uint32_t)rows, (uint32_t)cols,
-                                               static_cast<uint16_t*>(out));
+  const cudaError_t e = launch_pdl(transpose_bf16_kernel, grid, block, 0, s, static_cast<const uint16_t*>(in),
+                                   (uint32_t)rows, (uint32_t)cols, static_cast<uint16_t*>(out));
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t gemm_status_read_clear(unsigned int* out, cudaStream_t s) {

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace nvfp4 {
 
 // 2-D row-major tensor map over a rows x cols matrix (`inner` contiguous elements per row,
@@ -21,6 +23,24 @@ struct QOut {
 };
 
 void count_launch();
+
+// Launches `kernel` with programmatic stream serialization: its CTAs may be scheduled while the
+// previous kernel in the stream drains (they wait in pdl_wait() before touching its data).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float* out, int num_sms,
                         cudaStream_t s);

@@ -27,6 +27,8 @@ namespace nvfp4 {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ x, uint32_t cpr, uint32_t nchunks,
                                                    int64_t ld, unsigned int* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   uint32_t m = 0;
   const uint32_t stride = gridDim.x * blockDim.x;
   uint32_t g = blockIdx.x * blockDim.x + threadIdx.x;
@@ -153,6 +155,8 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 6 : 10) quantize_dual_kerne
   extern __shared__ __align__(16) uint8_t dsm[];
   uint16_t(*tile)[kTileC] = reinterpret_cast<uint16_t(*)[kTileC]>(dsm);
   uint16_t(*rtile)[kTileC] = reinterpret_cast<uint16_t(*)[kTileC]>(dsm + kTileR * kTileC * 2);
+  pdl_trigger();
+  pdl_wait();
   const float amax = *a.amax;
   const float S_t = tensor_scale(amax);
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
@@ -397,10 +401,10 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, f
   cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), s);
   if (e != cudaSuccess) return e;
   const int grid = grid_for(nchunks, 256 * 4, num_sms * 8);
-  amax_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), cpr, nchunks, ld,
-                                   reinterpret_cast<unsigned int*>(out));
+  e = launch_pdl(amax_kernel, dim3(grid), dim3(256), 0, s, static_cast<const uint16_t*>(x), cpr, nchunks, ld,
+                 reinterpret_cast<unsigned int*>(out));
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, bool sr, uint64_t seed,
@@ -449,21 +453,22 @@ cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int6
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kTileR * kTileC * 2);
   });
   if (attr != cudaSuccess) return attr;
+  cudaError_t e = cudaSuccess;
   if (clip) {  // the clipped form: both orientations, RTN
     if (!(R && C) || sr) return cudaErrorInvalidValue;
-    quantize_dual_kernel<true, true, false, true><<<grid, kDualThreads, smem, s>>>(a);
+    e = launch_pdl(quantize_dual_kernel<true, true, false, true>, grid, dim3(kDualThreads), smem, s, a);
   } else if (R && C) {
-    if (sr) quantize_dual_kernel<true, true, true><<<grid, kDualThreads, smem, s>>>(a);
-    else quantize_dual_kernel<true, true, false><<<grid, kDualThreads, smem, s>>>(a);
+    if (sr) e = launch_pdl(quantize_dual_kernel<true, true, true>, grid, dim3(kDualThreads), smem, s, a);
+    else e = launch_pdl(quantize_dual_kernel<true, true, false>, grid, dim3(kDualThreads), smem, s, a);
   } else if (C) {
-    if (sr) quantize_dual_kernel<false, true, true><<<grid, kDualThreads, smem, s>>>(a);
-    else quantize_dual_kernel<false, true, false><<<grid, kDualThreads, smem, s>>>(a);
+    if (sr) e = launch_pdl(quantize_dual_kernel<false, true, true>, grid, dim3(kDualThreads), smem, s, a);
+    else e = launch_pdl(quantize_dual_kernel<false, true, false>, grid, dim3(kDualThreads), smem, s, a);
   } else {
-    if (sr) quantize_dual_kernel<true, false, true><<<grid, kDualThreads, smem, s>>>(a);
-    else quantize_dual_kernel<true, false, false><<<grid, kDualThreads, smem, s>>>(a);
+    if (sr) e = launch_pdl(quantize_dual_kernel<true, false, true>, grid, dim3(kDualThreads), smem, s, a);
+    else e = launch_pdl(quantize_dual_kernel<true, false, false>, grid, dim3(kDualThreads), smem, s, a);
   }
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_debug_convert(const float* in, int64_t n, uint8_t* e2m1, uint8_t* e4m3, cudaStream_t s) {
