@@ -157,29 +157,58 @@ __global__ void __launch_bounds__(kVtThreads) vt_decode_kernel(const uint8_t* __
                                                                const uint16_t* __restrict__ mean_in, uint32_t kbpr,
                                                                uint32_t nblocks, float* __restrict__ out, int64_t ldo) {
   const float S_t = scale_in[0];
-  for (uint32_t b = blockIdx.x * blockDim.x + threadIdx.x; b < nblocks; b += gridDim.x * blockDim.x) {
-    const uint2 c = __ldcs(reinterpret_cast<const uint2*>(codes + static_cast<uint64_t>(b) * 8));
-    const uint32_t row = b / kbpr, kb = b - row * kbpr;
-    const float sv = e4m3_value(scales[sf_offset(row, kb, atoms_k)]);
-    const float mu = __uint_as_float(static_cast<uint32_t>(mean_in[b]) << 16);
-    float x[16];
+  // Each warp decodes 32 consecutive blocks (one per lane), stages the 2 KB of results in shared
+  // memory and stores them lane-consecutively (512 contiguous bytes per instruction instead of 32
+  // pieces of 16 bytes at a 64-byte stride).  The next blocks' codes, scale byte and mean are
+  // loaded before the current ones' arithmetic.
+  __shared__ float4 stg[kVtThreads / 32][128];
+  const uint32_t lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+  uint2 cn = make_uint2(0, 0);
+  uint32_t sn = 0, mn = 0;
+  auto fetch = [&](uint32_t bb) {
+    const uint32_t row = bb / kbpr;
+    cn = __ldcs(reinterpret_cast<const uint2*>(codes + static_cast<uint64_t>(bb) * 8));
+    sn = scales[sf_offset(row, bb - row * kbpr, atoms_k)];
+    mn = mean_in[bb];
+  };
+  if (b < nblocks) fetch(b);
+  for (; b - lane < nblocks; b += stride) {  // while the warp's first block exists (warp-uniform)
+    long long off = 0;  // this lane's block: offset of its 16 outputs
+    if (b < nblocks) {
+      const uint2 c = cn;
+      const uint32_t row = b / kbpr, kb = b - row * kbpr;
+      off = static_cast<long long>(row) * ldo + static_cast<long long>(kb) * 16;
+      const float sv = e4m3_value(sn);
+      const float mu = __uint_as_float(mn << 16);
+      if (b + stride < nblocks) fetch(b + stride);
+      float x[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      x[i] = __fmul_rn(__fmul_rn(e2m1_value(c.x >> (4 * i)), sv), S_t);
-      x[8 + i] = __fmul_rn(__fmul_rn(e2m1_value(c.y >> (4 * i)), sv), S_t);
-    }
-    wht16(x);
-    float4* dst = reinterpret_cast<float4*>(out + static_cast<int64_t>(row) * ldo + static_cast<int64_t>(kb) * 16);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float u[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float w = __fadd_rn(__fmul_rn(x[4 * q + j], 0.25f), mu);
-        u[j] = __fmul_rn(w, w);
+      for (int i = 0; i < 8; ++i) {
+        x[i] = __fmul_rn(__fmul_rn(e2m1_value(c.x >> (4 * i)), sv), S_t);
+        x[8 + i] = __fmul_rn(__fmul_rn(e2m1_value(c.y >> (4 * i)), sv), S_t);
       }
-      __stcs(dst + q, make_float4(u[0], u[1], u[2], u[3]));
+      wht16(x);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float u[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float w = __fadd_rn(__fmul_rn(x[4 * q + j], 0.25f), mu);
+          u[j] = __fmul_rn(w, w);
+        }
+        stg[wib][lane * 4 + q] = make_float4(u[0], u[1], u[2], u[3]);
+      }
     }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t j = i * 32 + lane;  // float4 j of the warp's 128: block j / 4, quarter j % 4
+      const long long o = __shfl_sync(0xFFFFFFFFu, off, j >> 2);
+      if (b - lane + (j >> 2) < nblocks) __stcs(reinterpret_cast<float4*>(out + o) + (j & 3), stg[wib][j]);
+    }
+    __syncwarp();
   }
 }
 
