@@ -73,9 +73,9 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ 
 // Column-wise (transposed) quantization, optionally with the row-wise output
 // from the same read.  A CTA of 128 threads stages a 64-row x 128-column BF16
 // tile in shared memory (8 coalesced 16-byte loads per thread in flight; small
-// CTAs, ten per SM for RTN and six for SR, so that the load phase of some
-// overlaps the arithmetic of others).  Both forms are
-// then produced from the staged tile: the row form by one thread per 16-element
+// CTAs, nine per SM for RTN (56 registers; ten would spill) and six for SR, so
+// that the load phase of some overlaps the arithmetic of others).  Both forms
+// are then produced from the staged tile: the row form by one thread per 16-element
 // block, the column form by threads that own two adjacent columns (one 4-byte
 // shared load per row yields both, their block maxima in one packed register)
 // and 32 rows, i.e. two 16-row blocks per column.  SR random bits of the column
@@ -151,7 +151,7 @@ constexpr int kTileR = 64, kTileC = 128;  // 64 x 128 BF16 tiles: 16 KB staged p
 constexpr int kDualThreads = 128;
 
 template <bool ROW, bool COL, bool SR, bool CLIP = false>
-__global__ void __launch_bounds__(kDualThreads, SR ? 6 : 10) quantize_dual_kernel(const DualQuantArgs a) {
+__global__ void __launch_bounds__(kDualThreads, SR ? 6 : 9) quantize_dual_kernel(const DualQuantArgs a) {
   extern __shared__ __align__(16) uint8_t dsm[];
   uint16_t(*tile)[kTileC] = reinterpret_cast<uint16_t(*)[kTileC]>(dsm);
   uint16_t(*rtile)[kTileC] = reinterpret_cast<uint16_t(*)[kTileC]>(dsm + kTileR * kTileC * 2);
