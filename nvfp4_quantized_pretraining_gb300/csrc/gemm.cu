@@ -91,6 +91,8 @@ struct GemmParams {
   // TMA like any operand stage (P and Q both complete on the leader's barrier) and the scale
   // warps leave it alone; 0: they fold P into P~ in shared memory
   int p_folded;
+  // 2-SM kernel: B's scales by one TMA box per stage (tmap_sfb); 0 (K < 256): two bulk copies
+  int sfb_tma;
 };
 
 __global__ void __launch_bounds__(g4::NUM_THREADS, 1)
@@ -488,7 +490,8 @@ __device__ __forceinline__ bool pair_work(const GemmParams& p, uint32_t cid, uin
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                           const __grid_constant__ CUtensorMap tmap_p, const __grid_constant__ CUtensorMap tmap_q,
-                          const __grid_constant__ CUtensorMap tmap_c, const GemmParams p) {
+                          const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_sfb,
+                          const GemmParams p) {
   using namespace g2;
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
@@ -526,6 +529,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmap_a);
     prefetch_tmap(&tmap_b);
+    if (p.sfb_tma) prefetch_tmap(&tmap_sfb);
     if (p.r > 0) {
       prefetch_tmap(&tmap_p);
       prefetch_tmap(&tmap_q);
@@ -576,14 +580,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
             } else {
               const uint32_t krem = p.K - it * BK;
               const uint32_t nk = krem >= (uint32_t)BK ? 4 : krem / 64;
-              mbar_arrive_expect_tx(&sf_full[stage], 3 * nk * SF_ATOM);
+              // this CTA's A scale atoms by a bulk copy, the tile's two B row blocks (all 256 B rows)
+              // by one 2 x 2 KB TMA box (atoms past K arrive zero-filled)
+              mbar_arrive_expect_tx(&sf_full[stage], nk * SF_ATOM + (p.sfb_tma ? SFB_BYTES : 2 * nk * SF_ATOM));
               const size_t ka = (size_t)it * 4;
               bulk_load(sSFA, p.a_scales + ((size_t)(mb2 * 2 + rank) * p.atoms_k + ka) * SF_ATOM, nk * SF_ATOM,
                         &sf_full[stage]);
-              bulk_load(sSFB, p.b_scales + ((size_t)(nb2 * 2) * p.atoms_k + ka) * SF_ATOM, nk * SF_ATOM,
-                        &sf_full[stage]);
-              bulk_load(sSFB + 4 * SF_ATOM, p.b_scales + ((size_t)(nb2 * 2 + 1) * p.atoms_k + ka) * SF_ATOM,
-                        nk * SF_ATOM, &sf_full[stage]);
+              if (p.sfb_tma) {
+                tma_load_2d(sSFB, &tmap_sfb, &sf_full[stage], (int32_t)(ka * 64), (int32_t)(nb2 * 2));
+              } else {
+                bulk_load(sSFB, p.b_scales + ((size_t)(nb2 * 2) * p.atoms_k + ka) * SF_ATOM, nk * SF_ATOM,
+                          &sf_full[stage]);
+                bulk_load(sSFB + 4 * SF_ATOM, p.b_scales + ((size_t)(nb2 * 2 + 1) * p.atoms_k + ka) * SF_ATOM,
+                          nk * SF_ATOM, &sf_full[stage]);
+              }
             }
           } else if (p.p_folded) {
             // P~ and Q by TMA, both completing on the leader's barrier; the scale warps only pass
@@ -1340,7 +1350,8 @@ static cudaError_t launch_gemm_single(const CUtensorMap& ta, const CUtensorMap& 
 }
 
 static cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tp,
-                                    const CUtensorMap& tq, const CUtensorMap& tc, const GemmParams& p, int num_sms,
+                                    const CUtensorMap& tq, const CUtensorMap& tc, const CUtensorMap& tsfb,
+                                    const GemmParams& p, int num_sms,
                                     float* sk_ws, size_t sk_ws_bytes, cudaStream_t s) {
   using namespace g2;
   static std::once_flag once;
@@ -1380,7 +1391,7 @@ static cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb
     }
   }
   cudaError_t e =
-      launch_pdl(gemm_nvf4_pair_kernel, dim3(clusters * 2), dim3(NUM_THREADS), SMEM_BYTES, s, ta, tb, tp, tq, tc, q);
+      launch_pdl(gemm_nvf4_pair_kernel, dim3(clusters * 2), dim3(NUM_THREADS), SMEM_BYTES, s, ta, tb, tp, tq, tc, tsfb, q);
   count_launch();
   if (e == cudaSuccess && q.sk_split) {
     e = launch_pdl(gemm_splitk_reduce_kernel, dim3(rem * 64), dim3(256), 0, s, q, rem);
@@ -1430,7 +1441,14 @@ cudaError_t launch_gemm_nvf4(const GemmArgs& g, int num_sms, cudaStream_t s) {
     if (!g.c_f32 && !make_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.C, g.N, g.M, (uint64_t)g.ldc * 2, 32, 32,
                                CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
-    return launch_gemm_pair(ta, tb, tp, tq, tc, p, num_sms, g.sk_ws, g.sk_ws_bytes, s);
+    // B's scales as a 2-D tensor of 8-byte units: one row per 128-row block, K/64 atoms of 512 B each
+    // (a stage's box of four atoms needs K >= 256)
+    CUtensorMap tsfb = ta;
+    p.sfb_tma = g.K >= 256;
+    if (p.sfb_tma && !make_tmap(&tsfb, CU_TENSOR_MAP_DATA_TYPE_UINT64, g.b_scales, (uint64_t)(g.K / 64) * 64,
+                                (uint64_t)(g.N / 128), (uint64_t)(g.K / 64) * 512, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    return launch_gemm_pair(ta, tb, tp, tq, tc, tsfb, p, num_sms, g.sk_ws, g.sk_ws_bytes, s);
   }
   CUtensorMap ta, tb, tp, tq;
   if (!make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a_codes, g.K / 2, g.M, g.K / 2, BK / 2, BM) ||

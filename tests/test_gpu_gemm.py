@@ -75,6 +75,7 @@ def check_gemm(F, oracle_mod, M, N, K, r, out_dtype, beta, seed, rows=None, a_ki
     (128, 256, 1024, 48), (512, 512, 2048, 64),
     (2048, 2560, 512, 0),     # more tiles than SMs: persistent schedule wraps
     (256, 512, 512, 16),      # single-forward shape (X 256x512, W 512x512, rank 16)
+    (256, 256, 128, 16),      # 2-SM kernel with K below one 256-wide stage (B scales by bulk copies)
 ])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_gemm_small(F, oracle_mod, M, N, K, r, out_dtype):
