@@ -61,8 +61,9 @@ __global__ void __launch_bounds__(kRlThreads) rl_f32_to_bf16(const float* __rest
 // ---------------------------------------------------------------------------
 // FP32 GEMM on row-major operands: C (m x n, ldc) = alpha op(A) op(B) + beta C, op(A) m x k
 // (A stored m x k, or k x m when ta), op(B) k x n (B stored k x n, or n x k when tb).  A CTA
-// of 256 threads computes a BM x BN tile (128 x 32, 64 x 64 or 32 x 128, whichever pads the
-// output least), 4 x 4 outputs per thread, over the K slice of blockIdx.z: with one slice it
+// of 256 threads computes a BM x BN tile, TM x TN outputs per thread (128 x 32, 64 x 64 or
+// 32 x 128 with 4 x 4; 128 x 80 or 80 x 128 with 8 x 5 or 5 x 8 for the products whose one
+// side is the sketch width 80; whichever pads the output least), over the K slice of blockIdx.z: with one slice it
 // writes C; with several, each slice's sum goes to partial[z] (m x n) and rl_sgemm_reduce adds
 // the slices in order, so the result is deterministic.  Tiles of op(A) and op(B), 16 deep in K,
 // are staged in shared memory k-major; the loads run along whichever dimension is contiguous.
@@ -71,21 +72,21 @@ namespace rg {
 constexpr int BK = 16, THREADS = 256;
 }
 
-template <bool TA, bool TB, int BM, int BN>
+template <bool TA, bool TB, int BM, int BN, int TM, int TN>
 __global__ void __launch_bounds__(rg::THREADS) rl_sgemm_kernel(int64_t m, int64_t n, int64_t k, int64_t kslice,
                                                               float alpha, const float* __restrict__ A, int64_t lda,
                                                               const float* __restrict__ B, int64_t ldb, float beta,
                                                               float* __restrict__ C, int64_t ldc,
                                                               float* __restrict__ partial) {
   using namespace rg;
-  static_assert(BM * BN == 16 * THREADS, "4 x 4 outputs per thread");
+  static_assert(BM * BN == TM * TN * THREADS && BM % TM == 0 && BN % TN == 0, "TM x TN outputs per thread");
   __shared__ __align__(16) float As[BK][BM + 4];
   __shared__ __align__(16) float Bs[BK][BN + 4];
-  const int tid = threadIdx.x, tx = tid % (BN / 4), ty = tid / (BN / 4);
+  const int tid = threadIdx.x, tx = tid % (BN / TN), ty = tid / (BN / TN);
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * BM, n0 = static_cast<int64_t>(blockIdx.x) * BN;
   const int64_t k0 = static_cast<int64_t>(blockIdx.z) * kslice;
   const int64_t k1 = k0 + kslice < k ? k0 + kslice : k;
-  float acc[4][4] = {};
+  float acc[TM][TN] = {};
   for (int64_t kt = k0; kt < k1; kt += BK) {
 #pragma unroll
     for (int u = 0; u < BM * BK / THREADS; ++u) {
@@ -108,24 +109,26 @@ __global__ void __launch_bounds__(rg::THREADS) rl_sgemm_kernel(int64_t m, int64_
     __syncthreads();
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&As[kk][4 * ty]);
-      const float4 b = *reinterpret_cast<const float4*>(&Bs[kk][4 * tx]);
-      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+      float av[TM], bv[TN];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < TM; ++i) av[i] = As[kk][TM * ty + i];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+      for (int j = 0; j < TN; ++j) bv[j] = Bs[kk][TN * tx + j];
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
     __syncthreads();
   }
   float* out = partial ? partial + static_cast<int64_t>(blockIdx.z) * m * n : nullptr;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t gm = m0 + 4 * ty + i;
+  for (int i = 0; i < TM; ++i) {
+    const int64_t gm = m0 + TM * ty + i;
     if (gm >= m) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t gn = n0 + 4 * tx + j;
+    for (int j = 0; j < TN; ++j) {
+      const int64_t gn = n0 + TN * tx + j;
       if (gn >= n) continue;
       if (out) out[gm * n + gn] = acc[i][j];
       else C[gm * ldc + gn] = beta == 0.0f ? alpha * acc[i][j] : fmaf(alpha, acc[i][j], beta * C[gm * ldc + gn]);
@@ -424,11 +427,11 @@ struct Rl {
   void gemm(bool ta, bool tb, int64_t m, int64_t n, int64_t k, float alpha, const float* A, int64_t lda,
             const float* B, int64_t ldb, float beta, float* C, int64_t ldc) {
     if (err != cudaSuccess) return;
-    // the tile shape that pads the output least (ties: the square tile)
-    const int64_t shapes[3][2] = {{64, 64}, {128, 32}, {32, 128}};
+    // the tile shape that pads the output least (ties: the earlier in this list)
+    const int64_t shapes[5][2] = {{128, 80}, {80, 128}, {64, 64}, {128, 32}, {32, 128}};
     int pick = 0;
     int64_t best = -1;
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 5; ++i) {
       const int64_t bm = shapes[i][0], bn = shapes[i][1];
       const int64_t area = ((m + bm - 1) / bm) * bm * ((n + bn - 1) / bn) * bn;
       if (best < 0 || area < best) best = area, pick = i;
@@ -465,16 +468,20 @@ struct Rl {
   void launch_t(bool ta, bool tb, dim3 grid, int64_t m, int64_t n, int64_t k, int64_t kslice, float alpha,
                 const float* A, int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
                 float* part) {
-    if (ta && tb) rl_sgemm_kernel<true, true, BM, BN><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
-    else if (ta) rl_sgemm_kernel<true, false, BM, BN><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
-    else if (tb) rl_sgemm_kernel<false, true, BM, BN><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
-    else rl_sgemm_kernel<false, false, BM, BN><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    constexpr int TM = BM == 128 && BN == 80 ? 8 : BM == 80 ? 5 : 4;
+    constexpr int TN = BM == 128 && BN == 80 ? 5 : BM == 80 ? 8 : 4;
+    if (ta && tb) rl_sgemm_kernel<true, true, BM, BN, TM, TN><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    else if (ta) rl_sgemm_kernel<true, false, BM, BN, TM, TN><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    else if (tb) rl_sgemm_kernel<false, true, BM, BN, TM, TN><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    else rl_sgemm_kernel<false, false, BM, BN, TM, TN><<<grid, rg::THREADS, 0, s>>>(m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
   }
   void launch_tile(int pick, bool ta, bool tb, dim3 grid, int64_t m, int64_t n, int64_t k, int64_t kslice,
                    float alpha, const float* A, int64_t lda, const float* B, int64_t ldb, float beta, float* C,
                    int64_t ldc, float* part) {
-    if (pick == 1) launch_t<128, 32>(ta, tb, grid, m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
-    else if (pick == 2) launch_t<32, 128>(ta, tb, grid, m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    if (pick == 0) launch_t<128, 80>(ta, tb, grid, m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    else if (pick == 1) launch_t<80, 128>(ta, tb, grid, m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    else if (pick == 3) launch_t<128, 32>(ta, tb, grid, m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
+    else if (pick == 4) launch_t<32, 128>(ta, tb, grid, m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
     else launch_t<64, 64>(ta, tb, grid, m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
   }
   int grid(int64_t n) const {
