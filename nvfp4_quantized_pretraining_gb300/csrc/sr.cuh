@@ -62,10 +62,15 @@ __device__ __forceinline__ uint4 sr_random(const PhiloxKeys& k, uint32_t stream,
 // clearing the low 22 bits leaves lo or the next grid point (a carry out of the
 // mantissa steps into the next binade, which is that point).
 //
-// For a < 1 the gap is 0.5 throughout, as it is in [1, 2): the rule is applied to
-// z = a + 1 rounded upward and 1 is taken off again.  Rounding upward to the
-// 2^-23 grid of [1, 2) keeps the decision: lo and 64 rnd16 * 2^-23 are on that
-// grid, and for such a point m, ceil(a) > m iff a > m.
+// For a < 1 the gap is 0.5 throughout, as it is in [1, 2).  Both cases are handled
+// at once on z = a * 2^-126 rounded upward: for a >= 1 the product is exact (a
+// normal float with a's mantissa), and for a < 1 it lands in FP32's subnormal
+// range, whose spacing 2^-149 is uniform like E2M1's below 1: its pattern is the
+// integer ceil(a * 2^23), and bit 22 of it is the half-step.  The carry rule on
+// that pattern rounds a in units of 0.5 exactly as on [1, 2) (a grid point there,
+// scaled back by 2^126, is 0, 0.5 or 1).  Rounding upward to that grid keeps the
+// decision: lo and 64 rnd16 * 2^-23 are on it, and for such a point m,
+// ceil(a) > m iff a > m.
 //
 // bias comes from the Philox word: sr_bias_lo for the low half-word (even
 // element), sr_bias_hi for the high half-word (odd element).
@@ -76,10 +81,8 @@ __device__ __forceinline__ uint32_t sr_bias_hi(uint32_t w) { return (~(w >> 10) 
 // E2M1 conversion that follows.  Exact for every finite y below 2^127 in
 // magnitude, denormals included (no flush to zero in this code).
 __device__ __forceinline__ float sr_round(float y, uint32_t bias) {
-  const float a = fabsf(y);
-  const float k = a < 1.0f ? 1.0f : 0.0f;
-  const float z = __fadd_ru(a, k);
-  const float w = __uint_as_float((__float_as_uint(z) + bias) & 0xFFC00000u) - k;
+  const float z = __fmul_ru(fabsf(y), 0x1p-126f);  // (needs denormals kept: no -ftz in this build)
+  const float w = __fmul_rn(__uint_as_float((__float_as_uint(z) + bias) & 0xFFC00000u), 0x1p126f);
   return __uint_as_float(__float_as_uint(w) | (__float_as_uint(y) & 0x80000000u));
 }
 
