@@ -245,10 +245,13 @@ def run_ours(args):
                        for p in projs) if r else 0
 
     def step(seed):
+        # a training step's order: the forward of every projection in model order, then the
+        # backward in reverse order
         for p in projs:
             F.fp4_quantize_dual(p["Wres"], out_row=p["Wq"], out_col=p["WqT"], stream=stream)
             F.fp4_linear_fwd(p["X"], p["Wq"], p["L1"], p["L2"], Y=p["Y"], xqT_saved=p["xqT"], workspace=p["ws_f"],
                              stream=stream)
+        for p in reversed(projs):
             F.fp4_linear_bwd(p["dY"], p["WqT"], p["xqT"], p["L1"], p["L2"], seed=seed, dX=p["dX"], dW=p["dW"],
                              workspace=p["ws_b"], stream=stream)
 
@@ -883,15 +886,17 @@ def end_to_end(F, torch, projs, T, r, stream, dev, args, gemm_flops, world):
         h2d += hx.numel() * 2 + hdy.numel() * 2
         d2h += sum(o.numel() * o.element_size() for o in outs)
     # Three streams, as a user of the C ABI would run it: host-to-device copies on one, the step on the
-    # compute stream once a projection's inputs have landed, the copies back on a third.  The host link
-    # (measured 210 GB/s in, 193 GB/s out, 340 GB/s both ways at once, whatever the number of streams)
-    # bounds this measurement, the outbound channel most, so it is started as early as possible: each
-    # projection's Y goes back as soon as its forward is done (overlapping its backward), and the
-    # projections run in increasing order of input bytes (the first outputs appear soonest, and the
-    # largest projection's Y overlaps its own backward at the end).
+    # compute stream as each input lands, the copies back on a third.  The host link (measured 210 GB/s
+    # in, 193 GB/s out, 340 GB/s both ways at once, whatever the number of streams) bounds this
+    # measurement, the outbound channel most, so that channel is kept busy from as early as possible:
+    # every X is sent first, so that each forward starts as soon as its own X has landed and its Y
+    # goes back at once (the forwards' outputs, 1 GB, then stream out while the dY still come in);
+    # the dY follow in the order of the backward passes, and each dX and dW goes back as soon as its
+    # backward is done.
     h2d_stream = torch.cuda.Stream(device=dev)
     d2h_stream = torch.cuda.Stream(device=dev)
-    order = sorted(range(len(projs)), key=lambda i: hosts[i][0].numel() + hosts[i][1].numel())
+    fwd_order = list(range(len(projs)))
+    bwd_order = fwd_order[::-1]
     times = []
     for it in range(args.warmup + args.steps):
         e0 = torch.cuda.Event(enable_timing=True)
@@ -899,31 +904,37 @@ def end_to_end(F, torch, projs, T, r, stream, dev, args, gemm_flops, world):
         e0.record(stream)
         h2d_stream.wait_event(e0)
         d2h_stream.wait_event(e0)
-        landed = {}
+        x_in, dy_in = {}, {}
         with torch.cuda.stream(h2d_stream):
-            for i in order:
-                p, (hx, hdy, _) = projs[i], hosts[i]
-                p["X"].copy_(hx, non_blocking=True)
-                p["dY"].copy_(hdy, non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(h2d_stream)
-                landed[i] = ev
-        for i in order:
-            p, (_, _, outs) = projs[i], hosts[i]
+            for i in fwd_order:
+                projs[i]["X"].copy_(hosts[i][0], non_blocking=True)
+                x_in[i] = torch.cuda.Event()
+                x_in[i].record(h2d_stream)
+            for i in bwd_order:
+                projs[i]["dY"].copy_(hosts[i][1], non_blocking=True)
+                dy_in[i] = torch.cuda.Event()
+                dy_in[i].record(h2d_stream)
+        for i in fwd_order:
+            p, outs = projs[i], hosts[i][2]
             with torch.cuda.stream(stream):
-                stream.wait_event(landed[i])
+                stream.wait_event(x_in[i])
                 F.fp4_quantize_dual(p["Wres"], out_row=p["Wq"], out_col=p["WqT"], stream=stream)
                 F.fp4_linear_fwd(p["X"], p["Wq"], p["L1"], p["L2"], Y=p["Y"], xqT_saved=p["xqT"],
                                  workspace=p["ws_f"], stream=stream)
                 fwd_done = torch.cuda.Event()
                 fwd_done.record(stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(fwd_done)
+                outs[0].copy_(p["Y"], non_blocking=True)
+        for i in bwd_order:
+            p, outs = projs[i], hosts[i][2]
+            with torch.cuda.stream(stream):
+                stream.wait_event(dy_in[i])
                 F.fp4_linear_bwd(p["dY"], p["WqT"], p["xqT"], p["L1"], p["L2"], seed=it, dX=p["dX"], dW=p["dW"],
                                  workspace=p["ws_b"], stream=stream)
                 bwd_done = torch.cuda.Event()
                 bwd_done.record(stream)
             with torch.cuda.stream(d2h_stream):
-                d2h_stream.wait_event(fwd_done)
-                outs[0].copy_(p["Y"], non_blocking=True)
                 d2h_stream.wait_event(bwd_done)
                 outs[1].copy_(p["dX"], non_blocking=True)
                 outs[2].copy_(p["dW"], non_blocking=True)
