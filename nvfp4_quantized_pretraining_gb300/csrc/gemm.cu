@@ -1017,14 +1017,19 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
       : "r"(taddr));
 }
 
+// Without SPLIT, CTA i takes the h rows [i h, i h + h) of X (h <= 128; the X tensor map's box is h
+// rows high): with h = ceil(M / SMs) every SM streams the same share of X, one CTA each.  The MMA
+// still runs M = 128: rows h..127 of a stage hold whatever an earlier stage left there, and the
+// results of those rows are neither stored nor folded into max |X|.
 // SPLIT: a cluster of two CTAs shares one 128-row block, each taking half of the K stages
-// (all 152 SMs get work when M / 128 is below the SM count; 4 stages so that two CTAs fit per
-// SM).  Rank 1 hands its FP32 partial sum to rank 0 through distributed shared memory and
-// rank 0 writes P = bf16(partial_0 + partial_1): a fixed order, so the result is deterministic.
+// (for M too small for h >= 48 rows per SM; 4 stages so that two CTAs fit per SM).  Rank 1
+// hands its FP32 partial sum to rank 0 through distributed shared memory and rank 0 writes
+// P = bf16(partial_0 + partial_1): a fixed order, so the result is deterministic.
 template <bool SPLIT>
 __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
     branch_factor_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_l,
-                         uint32_t K, int r, __nv_bfloat16* __restrict__ P, unsigned int* __restrict__ amax_out) {
+                         uint32_t M, uint32_t K, uint32_t h, int r, __nv_bfloat16* __restrict__ P,
+                         unsigned int* __restrict__ amax_out) {
   using namespace bf;
   pdl_trigger();
   constexpr int NST = SPLIT ? SPLIT_STAGES : STAGES;
@@ -1058,8 +1063,9 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
   const uint32_t kh = SPLIT ? (num_k_all + 1) / 2 : num_k_all;
   const uint32_t k_begin = rank * kh;                 // this CTA's first K stage
   const uint32_t num_k = SPLIT ? min(kh, num_k_all - k_begin) : num_k_all;  // >= 1: the host splits only K >= 2 stages
-  const uint32_t m0 = (SPLIT ? (blockIdx.x >> 1) : blockIdx.x) * BM;
+  const uint32_t m0 = SPLIT ? (blockIdx.x >> 1) * BM : blockIdx.x * h;
   const uint32_t l_bytes = (uint32_t)r * BOX * 2;  // one L box
+  const uint32_t x_bytes = h * BOX * 2;            // one X box (h rows; rows past M arrive zero-filled)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1074,7 +1080,7 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
         uint8_t* sB = sA + A_BYTES;
         // both boxes of X back to back (256 contiguous bytes of each row), then both of L;
         // a box past K arrives zero-filled
-        mbar_arrive_expect_tx(&full[stage], BOXES * (XBOX_BYTES + l_bytes));
+        mbar_arrive_expect_tx(&full[stage], BOXES * (x_bytes + l_bytes));
         const int32_t kx = (int32_t)((k_begin + it) * BK);
 #pragma unroll
         for (int b = 0; b < BOXES; ++b)
@@ -1134,8 +1140,10 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
         }
         const uint4* tile = reinterpret_cast<const uint4*>(smem + stage * STAGE_BYTES);
 #pragma unroll
-        for (int i = 0; i < A_BYTES / 16 / 128; ++i) {  // both X boxes
-          const uint4 v = tile[t + 128 * i];
+        for (int i = 0; i < A_BYTES / 16 / 128; ++i) {  // both X boxes, the h rows landed in each
+          const int u = t + 128 * i;  // 16-byte unit: box u / 1024, row (u % 1024) / 8
+          if ((uint32_t)((u & 1023) >> 3) >= h) continue;
+          const uint4 v = tile[u];
           m = __vmaxu2(m, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
                                    __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
         }
@@ -1150,6 +1158,7 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
     if (!*abort_flag && mbar_wait_warp(acc_full, 0)) {
       tc_fence_after();
       const uint32_t row = m0 + quad * 32 + lane;
+      const bool mine = quad * 32 + lane < h && row < M;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (16 * j < r) {
@@ -1158,7 +1167,7 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
         }
       }
       tc_fence_before();
-      if (!SPLIT) {
+      if (!SPLIT && mine) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           if (16 * j >= r) break;
@@ -1497,20 +1506,26 @@ cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ld
                                       kSmemSplit);
   });
   if (attr_err != cudaSuccess) return attr_err;
+  const int blocks = (int)(M / BM);
+  const int num_k = (int)((K + BK - 1) / BK);
+  // rows per CTA with one CTA per SM; below 48 the re-read of L (r rows per stage, from L2) would
+  // outweigh X in each SM's intake, and the K split over CTA pairs takes over
+  const uint32_t h_rows = (uint32_t)((M + num_sms - 1) / num_sms);
+  const bool by_rows = h_rows >= 48 && h_rows <= (uint32_t)BM;
+  const bool split = !by_rows && blocks < num_sms && num_k >= 2;
+  const uint32_t h = by_rows ? h_rows : (uint32_t)BM;
   CUtensorMap tx, tl;
-  if (!make_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, (uint64_t)ldx * 2, BOX, BM) ||
+  if (!make_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, (uint64_t)ldx * 2, BOX, h) ||
       !make_tmap(&tl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L, K, r, (uint64_t)K * 2, BOX, (uint32_t)r))
     return cudaErrorInvalidValue;
   if (amax_out) {
     const cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), s);
     if (e != cudaSuccess) return e;
   }
-  const int blocks = (int)(M / BM);
-  const int num_k = (int)((K + BK - 1) / BK);
   __nv_bfloat16* Pb = static_cast<__nv_bfloat16*>(P);
   unsigned int* am = reinterpret_cast<unsigned int*>(amax_out);
   cudaError_t e;
-  if (blocks < num_sms && num_k >= 2) {
+  if (split) {
     // fewer row blocks than SMs: two CTAs (a cluster) per row block, half of K each
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[2];
@@ -1526,10 +1541,12 @@ cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ld
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, branch_factor_kernel<true>, tx, tl, (uint32_t)K, r, Pb, am);
+    e = cudaLaunchKernelEx(&cfg, branch_factor_kernel<true>, tx, tl, (uint32_t)M, (uint32_t)K, (uint32_t)BM, r, Pb,
+                           am);
   } else {
-    e = launch_pdl(branch_factor_kernel<false>, dim3(blocks), dim3(NUM_THREADS), SMEM_BYTES, s, tx, tl, (uint32_t)K, r,
-                   Pb, am);
+    const unsigned grid = (unsigned)((M + h - 1) / h);
+    e = launch_pdl(branch_factor_kernel<false>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, tx, tl, (uint32_t)M,
+                   (uint32_t)K, h, r, Pb, am);
   }
   count_launch();
   return e;
