@@ -238,21 +238,24 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 6 : 9) quantize_dual_kernel
       BlockScale bs;
       bs.sb = block_sb(__uint_as_float(m << 16), sc);
       bs.inv = inv_tab[bs.sb];
-      float y[2][8];  // elements 0..7 and 8..15
+      float2 y2[2][4];  // element pairs (2q, 2q+1) of elements 0..7 and 8..15, the two halves of word q
+      const float2 inv2 = make_float2(bs.inv, bs.inv);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        y[e >> 2][2 * (e & 3)] = __fmul_rn(bf16_lo(wd[e]), bs.inv);
-        y[e >> 2][2 * (e & 3) + 1] = __fmul_rn(bf16_hi(wd[e]), bs.inv);
-      }
+      for (int e = 0; e < 8; ++e) y2[e >> 2][e & 3] = __fmul2_rn(make_float2(bf16_lo(wd[e]), bf16_hi(wd[e])), inv2);
       if (SR) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const uint4 rr = sr_random(a.keys, a.stream_r, (uint64_t)row * a.cpr + 2 * c16 + hh);
           const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            y[hh][e] = sr_round(y[hh][e], (e & 1) ? sr_bias_hi(rw[e >> 1]) : sr_bias_lo(rw[e >> 1]));
+          for (int q = 0; q < 4; ++q) y2[hh][q] = sr_round2(y2[hh][q], sr_bias_lo(rw[q]), sr_bias_hi(rw[q]));
         }
+      }
+      float y[2][8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        y[e >> 2][2 * (e & 3)] = y2[e >> 2][e & 3].x;
+        y[e >> 2][2 * (e & 3) + 1] = y2[e >> 2][e & 3].y;
       }
       const uint32_t lo = e2m1x8(y[0]), hi = e2m1x8(y[1]);
       const bool valid = row < a.rows && 16 * c16 < a.cols;
@@ -296,18 +299,16 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 6 : 9) quantize_dual_kernel
     sa.inv = inv_tab[sa.sb];
     sb.sb = block_sb(__uint_as_float(m2 & 0xFFFF0000u), sc);
     sb.inv = inv_tab[sb.sb];
+    const float2 inv2 = make_float2(sa.inv, sb.inv);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      va[i] = __fmul_rn(va[i], sa.inv);
-      vb[i] = __fmul_rn(vb[i], sb.inv);
-    }
-    if (SR) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      float2 v = __fmul2_rn(make_float2(va[i], vb[i]), inv2);
+      if (SR) {
         const uint32_t rp = *reinterpret_cast<const uint32_t*>(&rtile[rb * 16 + i][2 * cp]);
-        va[i] = sr_round(va[i], sr_bias_lo(rp));
-        vb[i] = sr_round(vb[i], sr_bias_hi(rp));
+        v = sr_round2(v, sr_bias_lo(rp), sr_bias_hi(rp));
       }
+      va[i] = v.x;
+      vb[i] = v.y;
     }
     float t8[8];
 #pragma unroll

@@ -85,5 +85,15 @@ __device__ __forceinline__ float sr_round(float y, uint32_t bias) {
   const float w = __fmul_rn(__uint_as_float((__float_as_uint(z) + bias) & 0xFFC00000u), 0x1p126f);
   return __uint_as_float(__float_as_uint(w) | (__float_as_uint(y) & 0x80000000u));
 }
+// The same for two values, the multiply back by 2^126 done as one packed FP32x2 multiply (exact
+// either way).  The upward-rounded multiply stays scalar: it takes |y| as a free operand modifier.
+__device__ __forceinline__ float2 sr_round2(float2 y, uint32_t bias_x, uint32_t bias_y) {
+  const float zx = __fmul_ru(fabsf(y.x), 0x1p-126f), zy = __fmul_ru(fabsf(y.y), 0x1p-126f);
+  const float2 w = __fmul2_rn(make_float2(__uint_as_float((__float_as_uint(zx) + bias_x) & 0xFFC00000u),
+                                          __uint_as_float((__float_as_uint(zy) + bias_y) & 0xFFC00000u)),
+                              make_float2(0x1p126f, 0x1p126f));
+  return make_float2(__uint_as_float(__float_as_uint(w.x) | (__float_as_uint(y.x) & 0x80000000u)),
+                     __uint_as_float(__float_as_uint(w.y) | (__float_as_uint(y.y) & 0x80000000u)));
+}
 
 }  // namespace nvfp4
