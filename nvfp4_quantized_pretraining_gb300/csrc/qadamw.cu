@@ -22,20 +22,30 @@ namespace nvfp4 {
 constexpr int kVtThreads = 256;
 
 
-// In-place unnormalised Walsh-Hadamard transform of 16 values, natural order.
-__device__ __forceinline__ void wht16(float (&x)[16]) {
+// A block's 16 values are held as eight FP32 pairs p[k] = (x[k], x[k + 8]), so that most of the
+// per-block arithmetic runs as packed FP32x2 operations (each lane exactly the scalar operation).
+__device__ __forceinline__ float2 sub2_rn(float2 a, float2 b) {  // a - b: b * -1 is exact, one rounding
+  return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);
+}
+
+// In-place unnormalised Walsh-Hadamard transform of 16 values, natural order: levels h = 1, 2, 4
+// pair x[j] with x[j + h] inside each half, i.e. p[j] with p[j + h] in both lanes at once; level 8
+// pairs the two lanes of each p[k].
+__device__ __forceinline__ void wht16(float2 (&p)[8]) {
 #pragma unroll
-  for (int h = 1; h < 16; h <<= 1) {
+  for (int h = 1; h < 8; h <<= 1) {
 #pragma unroll
-    for (int i = 0; i < 16; i += 2 * h) {
+    for (int i = 0; i < 8; i += 2 * h) {
 #pragma unroll
       for (int j = i; j < i + h; ++j) {
-        const float a = x[j], b = x[j + h];
-        x[j] = __fadd_rn(a, b);
-        x[j + h] = __fsub_rn(a, b);
+        const float2 a = p[j], b = p[j + h];
+        p[j] = __fadd2_rn(a, b);
+        p[j + h] = sub2_rn(a, b);
       }
     }
   }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) p[k] = make_float2(__fadd_rn(p[k].x, p[k].y), __fsub_rn(p[k].x, p[k].y));
 }
 
 __device__ __forceinline__ void load_block(const float* __restrict__ v, float4 (&f)[4]) {
@@ -44,30 +54,27 @@ __device__ __forceinline__ void load_block(const float* __restrict__ v, float4 (
   for (int q = 0; q < 4; ++q) f[q] = __ldcs(p + q);
 }
 
-// h (16 values) and the BF16 mean pattern of one block of v (loaded into f).
-__device__ __forceinline__ uint32_t vt_forward(const float4 (&fv)[4], float (&h)[16]) {
+// h (16 values, as pairs h[k] = (h_k, h_k+8)) and the BF16 mean pattern of one block of v (loaded
+// into f).  The mean's pairwise tree adds (h_2i, h_2i+1) for i = 0..7, then neighbours twice more,
+// then the last two: in the pair layout the first three levels are packed additions of the same
+// operands, (t_i, t_i+4) = h[2i] + h[2i+1] and so on.
+__device__ __forceinline__ uint32_t vt_forward(const float4 (&fv)[4], float2 (&h)[8]) {
+  const float* f = reinterpret_cast<const float*>(fv);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float4 f = fv[q];
-    h[4 * q + 0] = __fsqrt_rn(f.x);
-    h[4 * q + 1] = __fsqrt_rn(f.y);
-    h[4 * q + 2] = __fsqrt_rn(f.z);
-    h[4 * q + 3] = __fsqrt_rn(f.w);
-  }
-  float t[8];
+  for (int k = 0; k < 8; ++k) h[k] = make_float2(__fsqrt_rn(f[k]), __fsqrt_rn(f[k + 8]));
+  float2 t[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) t[i] = __fadd_rn(h[2 * i], h[2 * i + 1]);
+  for (int i = 0; i < 4; ++i) t[i] = __fadd2_rn(h[2 * i], h[2 * i + 1]);  // (t_i, t_i+4)
 #pragma unroll
-  for (int i = 0; i < 4; ++i) t[i] = __fadd_rn(t[2 * i], t[2 * i + 1]);
-#pragma unroll
-  for (int i = 0; i < 2; ++i) t[i] = __fadd_rn(t[2 * i], t[2 * i + 1]);
-  const uint32_t mean = bf16_rn_bits(__fmul_rn(__fadd_rn(t[0], t[1]), 0.0625f));
+  for (int i = 0; i < 2; ++i) t[i] = __fadd2_rn(t[2 * i], t[2 * i + 1]);  // (t0+t1, t4+t5), (t2+t3, t6+t7)
+  t[0] = __fadd2_rn(t[0], t[1]);
+  const uint32_t mean = bf16_rn_bits(__fmul_rn(__fadd_rn(t[0].x, t[0].y), 0.0625f));
   const float mu = __uint_as_float(mean << 16);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) h[i] = __fsub_rn(h[i], mu);
+  for (int k = 0; k < 8; ++k) h[k] = __fadd2_rn(h[k], make_float2(-mu, -mu));
   wht16(h);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) h[i] = __fmul_rn(h[i], 0.25f);
+  for (int k = 0; k < 8; ++k) h[k] = __fmul2_rn(h[k], make_float2(0.25f, 0.25f));
   return mean;
 }
 
@@ -88,10 +95,11 @@ __global__ void __launch_bounds__(kVtThreads) vt_amax_kernel(const float* __rest
   for (; b < nblocks; b += stride) {
     float4 nxt[4];
     if (b + stride < nblocks) load_block(block_src(v, b + stride, kbpr, ldv), nxt);
-    float h[16];
+    float2 h[8];
     vt_forward(cur, h);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) m = max(m, __float_as_uint(h[i]) & 0x7FFFFFFFu);
+    for (int k = 0; k < 8; ++k)
+      m = max(m, max(__float_as_uint(h[k].x) & 0x7FFFFFFFu, __float_as_uint(h[k].y) & 0x7FFFFFFFu));
 #pragma unroll
     for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
   }
@@ -121,19 +129,20 @@ __global__ void __launch_bounds__(kVtThreads) vt_encode_kernel(const float* __re
   for (; b < nblocks; b += stride) {
     float4 nxt[4];
     if (b + stride < nblocks) load_block(block_src(v, b + stride, kbpr, ldv), nxt);
-    float h[16];
+    float2 h[8];
     const uint32_t mean = vt_forward(cur, h);
 #pragma unroll
     for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
     float amax_b = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) amax_b = fmaxf(amax_b, fabsf(h[i]));
+    for (int k = 0; k < 8; ++k) amax_b = fmaxf(amax_b, fmaxf(fabsf(h[k].x), fabsf(h[k].y)));
     const BlockScale bs = block_scale(amax_b, S_t);
     float y0[8], y1[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      y0[i] = __fmul_rn(h[i], bs.inv);
-      y1[i] = __fmul_rn(h[8 + i], bs.inv);
+    for (int k = 0; k < 8; ++k) {
+      const float2 y = __fmul2_rn(h[k], make_float2(bs.inv, bs.inv));
+      y0[k] = y.x;
+      y1[k] = y.y;
     }
     *reinterpret_cast<uint2*>(codes + static_cast<uint64_t>(b) * 8) = make_uint2(e2m1x8(y0), e2m1x8(y1));
     const uint32_t row = b / kbpr;
@@ -183,22 +192,23 @@ __global__ void __launch_bounds__(kVtThreads) vt_decode_kernel(const uint8_t* __
       const float sv = e4m3_value(sn);
       const float mu = __uint_as_float(mn << 16);
       if (b + stride < nblocks) fetch(b + stride);
-      float x[16];
+      float2 x[8];  // (x_k, x_k+8)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        x[i] = __fmul_rn(__fmul_rn(e2m1_value(c.x >> (4 * i)), sv), S_t);
-        x[8 + i] = __fmul_rn(__fmul_rn(e2m1_value(c.y >> (4 * i)), sv), S_t);
-      }
+      for (int k = 0; k < 8; ++k)
+        x[k] = __fmul2_rn(__fmul2_rn(make_float2(e2m1_value(c.x >> (4 * k)), e2m1_value(c.y >> (4 * k))),
+                                     make_float2(sv, sv)),
+                          make_float2(S_t, S_t));
       wht16(x);
+      float2 u[8];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float u[4];
+      for (int k = 0; k < 8; ++k) {
+        const float2 w = __fadd2_rn(__fmul2_rn(x[k], make_float2(0.25f, 0.25f)), make_float2(mu, mu));
+        u[k] = __fmul2_rn(w, w);
+      }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float w = __fadd_rn(__fmul_rn(x[4 * q + j], 0.25f), mu);
-          u[j] = __fmul_rn(w, w);
-        }
-        stg[wib][lane * 4 + q] = make_float4(u[0], u[1], u[2], u[3]);
+      for (int q = 0; q < 2; ++q) {
+        stg[wib][lane * 4 + q] = make_float4(u[4 * q].x, u[4 * q + 1].x, u[4 * q + 2].x, u[4 * q + 3].x);
+        stg[wib][lane * 4 + 2 + q] = make_float4(u[4 * q].y, u[4 * q + 1].y, u[4 * q + 2].y, u[4 * q + 3].y);
       }
     }
     __syncwarp();
