@@ -57,7 +57,7 @@ WORKLOADS = {
 GEMM_TRAFFIC = {
     # launch list of `--part step --steps 2 --warmup 3` with dram__bytes_read.sum and
     # dram__bytes_write.sum (one pass): mean over the 96 GEMM launches of the 3B block
-    "0cebaa4178678e16": 214800000,
+    "df940e31274b5f93": 215200000,
 }
 
 
