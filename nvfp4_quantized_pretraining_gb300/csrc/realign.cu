@@ -271,11 +271,9 @@ __global__ void __launch_bounds__(kRlJacThreads) rl_jacobi_kernel(const float* _
   extern __shared__ float sh[];
   const int ld = s + 1;
   float* A = sh;              // s x ld
-  float* V = sh + s * ld;     // s x ld
-  float* cs = V + s * ld;     // s / 2 cosines
-  float* sn = cs + s / 2;     // s / 2 sines
-  int* P = reinterpret_cast<int*>(sn + s / 2);  // s / 2 pair heads
-  int* Q = P + s / 2;                           // s / 2 pair tails
+  float* V = sh + s * ld;     // s x ld (2 s ld floats: a multiple of 8 bytes)
+  float2* CSN = reinterpret_cast<float2*>(V + s * ld);  // s / 2 (cosine, sine) pairs
+  int2* PQ = reinterpret_cast<int2*>(CSN + s / 2);      // s / 2 (head, tail) pairs
   __shared__ int rotated;
   __shared__ float red[kRlJacThreads / 32];
   if (*info != 0) return;
@@ -295,6 +293,23 @@ __global__ void __launch_bounds__(kRlJacThreads) rl_jacobi_kernel(const float* _
   for (int w = 0; w < kRlJacThreads / 32; ++w) fro2 += red[w];
   const float thresh = 1e-6f * sqrtf(fro2);
   const int half = s / 2;
+  // This thread's share of each round's update, the same in every round: 2 x 2 blocks (k, l) of A
+  // and entries (pair l, row i) of V, packed as k | l << 8 and l | i << 8 (s <= 128), computed once
+  // here rather than by a division per item and round.
+  constexpr int kItA = (kRlMaxS / 2) * (kRlMaxS / 2) / kRlJacThreads;
+  constexpr int kItV = (kRlMaxS / 2) * kRlMaxS / kRlJacThreads;
+  constexpr uint32_t kNone = 0xFFFFFFFFu;
+  uint32_t it_a[kItA], it_v[kItV];
+#pragma unroll
+  for (int j = 0; j < kItA; ++j) {
+    const int e = threadIdx.x + j * kRlJacThreads;
+    it_a[j] = e < half * half ? (uint32_t)(e / half) | ((uint32_t)(e % half) << 8) : kNone;
+  }
+#pragma unroll
+  for (int j = 0; j < kItV; ++j) {
+    const int f = threadIdx.x + j * kRlJacThreads;
+    it_v[j] = f < half * s ? (uint32_t)(f / s) | ((uint32_t)(f % s) << 8) : kNone;
+  }
   for (int sweep = 0; sweep < max_sweeps; ++sweep) {
     if (threadIdx.x == 0) rotated = 0;
     __syncthreads();
@@ -310,34 +325,38 @@ __global__ void __launch_bounds__(kRlJacThreads) rl_jacobi_kernel(const float* _
           c = rsqrtf(1.0f + t * t);
           rotated = 1;
         }
-        P[k] = p;
-        Q[k] = q;
-        cs[k] = c;
-        sn[k] = t * c;
+        PQ[k] = make_int2(p, q);
+        CSN[k] = make_float2(c, t * c);
       }
       __syncthreads();
       // A <- J^T A J as 2 x 2 blocks; V <- V J
-      for (int e = threadIdx.x; e < half * half + half * s; e += blockDim.x) {
-        if (e < half * half) {
-          const int k = e / half, l = e % half;
-          const int pk = P[k], qk = Q[k], pl = P[l], ql = Q[l];
-          const float ck = cs[k], sk = sn[k], cl = cs[l], sl = sn[l];
-          const float xpp = A[pk * ld + pl], xpq = A[pk * ld + ql], xqp = A[qk * ld + pl], xqq = A[qk * ld + ql];
-          const float rpp = ck * xpp - sk * xqp, rpq = ck * xpq - sk * xqq;  // rows of pair k
-          const float rqp = sk * xpp + ck * xqp, rqq = sk * xpq + ck * xqq;
-          A[pk * ld + pl] = cl * rpp - sl * rpq;  // columns of pair l
-          A[pk * ld + ql] = sl * rpp + cl * rpq;
-          A[qk * ld + pl] = cl * rqp - sl * rqq;
-          A[qk * ld + ql] = sl * rqp + cl * rqq;
-        } else {
-          const int f = e - half * half;
-          const int l = f / s, i = f % s;
-          const int pl = P[l], ql = Q[l];
-          const float cl = cs[l], sl = sn[l];
-          const float vp = V[i * ld + pl], vq = V[i * ld + ql];
-          V[i * ld + pl] = cl * vp - sl * vq;
-          V[i * ld + ql] = sl * vp + cl * vq;
-        }
+#pragma unroll
+      for (int j = 0; j < kItA; ++j) {
+        if (it_a[j] == kNone) continue;
+        const int k = it_a[j] & 0xFFu, l = it_a[j] >> 8;
+        const int2 qk2 = PQ[k], ql2 = PQ[l];
+        const float2 rk = CSN[k], rl = CSN[l];
+        const int pk = qk2.x, qk = qk2.y, pl = ql2.x, ql = ql2.y;
+        const float ck = rk.x, sk = rk.y, cl = rl.x, sl = rl.y;
+        const float xpp = A[pk * ld + pl], xpq = A[pk * ld + ql], xqp = A[qk * ld + pl], xqq = A[qk * ld + ql];
+        const float rpp = ck * xpp - sk * xqp, rpq = ck * xpq - sk * xqq;  // rows of pair k
+        const float rqp = sk * xpp + ck * xqp, rqq = sk * xpq + ck * xqq;
+        A[pk * ld + pl] = cl * rpp - sl * rpq;  // columns of pair l
+        A[pk * ld + ql] = sl * rpp + cl * rpq;
+        A[qk * ld + pl] = cl * rqp - sl * rqq;
+        A[qk * ld + ql] = sl * rqp + cl * rqq;
+      }
+#pragma unroll
+      for (int j = 0; j < kItV; ++j) {
+        if (it_v[j] == kNone) continue;
+        const int l = it_v[j] & 0xFFu, i = it_v[j] >> 8;
+        const int2 ql2 = PQ[l];
+        const float2 rl = CSN[l];
+        const int pl = ql2.x, ql = ql2.y;
+        const float cl = rl.x, sl = rl.y;
+        const float vp = V[i * ld + pl], vq = V[i * ld + ql];
+        V[i * ld + pl] = cl * vp - sl * vq;
+        V[i * ld + ql] = sl * vp + cl * vq;
       }
       __syncthreads();
     }
@@ -346,7 +365,7 @@ __global__ void __launch_bounds__(kRlJacThreads) rl_jacobi_kernel(const float* _
     if (!any) break;
   }
   // decreasing order (selection by one thread; s <= 128), then the permuted output
-  int* order = P;  // reuse: s entries fit in P and Q (s / 2 each, contiguous)
+  int* order = reinterpret_cast<int*>(PQ);  // reuse: s entries fit in the s / 2 int2
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int i = 0; i < s; ++i) order[i] = i;
