@@ -581,6 +581,12 @@ def run_part(args, F, torch, S, dev):
         res = gemm_sweep(F, torch, S, stream, dev, flush, args)
     elif args.part == "qadamw_v_codec":
         res = qadamw_codec(F, torch, projs, stream, dev, flush, args)
+    elif args.part == "lora_cholqr":
+        r = wl["r"]
+        for i, p in enumerate(projs):  # N(0, 0.02) rows: a positive definite Gram matrix (r <= K)
+            p["L1"] = S.normal_device((r, p["K"]), 0.02, 810 + i, dev)
+            p["L2"] = S.normal_device((p["N"], r), 0.02, 820 + i, dev)
+        res = lora_cholqr(F, torch, projs, r, stream, dev, flush, args)
     else:
         r = wl["r"]
         for i, p in enumerate(projs):
@@ -1066,7 +1072,7 @@ def main():
     ap.add_argument("--qmode", choices=["rtn", "sr"], default="sr")
     ap.add_argument("--rank", type=int, default=64, help="--part branch_one / gemm_one: the branch rank")
     ap.add_argument("--gshape", type=int, nargs=3, default=[16384, 3072, 8192], help="--part gemm_one: M N K")
-    ap.add_argument("--part", choices=["all", "step", "newton_schulz", "qadamw_v_codec", "lora_realign", "quantize_sweep",
+    ap.add_argument("--part", choices=["all", "step", "newton_schulz", "qadamw_v_codec", "lora_realign", "lora_cholqr", "quantize_sweep",
                              "gemm_sweep", "quantize_one", "branch_one", "gemm_one"], default="all",
                     help="run one optimizer-side measurement alone (prints its JSON object; for profiling)")
     args = ap.parse_args()

@@ -29,6 +29,8 @@ constexpr int kCqrThreads = 256;
 template <int R>
 __global__ void __launch_bounds__(kCqrThreads) cholqr_gram_kernel(const uint16_t* __restrict__ L1, int64_t K,
                                                                   int64_t ld, float* __restrict__ partial) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float tile[R][kCqrChunk + 1];
   constexpr int kCols = R / 4;
   const int i = threadIdx.x / 4, j0 = threadIdx.x % 4;
@@ -60,13 +62,19 @@ __global__ void __launch_bounds__(kCqrThreads) cholqr_gram_kernel(const uint16_t
 }
 
 // One CTA: G = sum of the partials (fixed order), G = L L^T.  Writes L (lower,
-// zeros above) and the reciprocals of its diagonal.
+// zeros above) and the reciprocals of its diagonal.  Per column j two phases: the
+// column below the pivot is divided by it; then the trailing lower triangle is
+// updated by 32 x 32 threads (row j + 1 + a, column j + 1 + b, b <= a, strided by
+// 32), and the thread that updates the next diagonal element takes its square root
+// (or reports it non-positive) at once, so one barrier closes both.
 template <int R>
 __global__ void __launch_bounds__(1024) cholqr_factor_kernel(const float* __restrict__ partial, int nparts,
                                                              float* __restrict__ Lout, float* __restrict__ inv_diag,
                                                              int* __restrict__ info) {
   __shared__ float G[R][R + 1];
   __shared__ int bad;
+  pdl_trigger();
+  pdl_wait();
   for (int e = threadIdx.x; e < R * R; e += blockDim.x) {
     float v[kCqrMaxParts];
 #pragma unroll
@@ -76,24 +84,31 @@ __global__ void __launch_bounds__(1024) cholqr_factor_kernel(const float* __rest
     for (int p = 0; p < kCqrMaxParts; ++p) s += v[p];
     G[e / R][e % R] = s;
   }
-  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const float d = G[0][0];
+    bad = d > 0.0f ? 0 : 1;
+    if (d > 0.0f) G[0][0] = sqrtf(d);
+  }
   __syncthreads();
   // right-looking factorisation in place (lower triangle of G becomes L)
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   for (int j = 0; j < R; ++j) {
-    if (threadIdx.x == 0) {
-      const float d = G[j][j];
-      if (!(d > 0.0f)) bad = j + 1;
-      else G[j][j] = sqrtf(d);
-    }
-    __syncthreads();
-    if (bad) break;
+    if (bad) break;  // uniform: read after the barrier that closed the previous column
     const float djj = G[j][j];
     for (int i = j + 1 + threadIdx.x; i < R; i += blockDim.x) G[i][j] = G[i][j] / djj;
     __syncthreads();
-    const int n = R - j - 1;  // trailing (n x n) lower triangle
-    for (int e = threadIdx.x; e < n * n; e += blockDim.x) {
-      const int i = j + 1 + e / n, k = j + 1 + e % n;
-      if (k <= i) G[i][k] -= G[i][j] * G[k][j];
+    for (int a = ty; j + 1 + a < R; a += 32) {
+      const int i = j + 1 + a;
+      for (int b = tx; b <= a; b += 32) {
+        const int k = j + 1 + b;
+        G[i][k] -= G[i][j] * G[k][j];
+        if (a == 0) {  // (then b == 0: the next pivot, now final)
+          const float d = G[i][i];
+          if (!(d > 0.0f)) bad = j + 2;
+          else G[i][i] = sqrtf(d);
+        }
+      }
     }
     __syncthreads();
   }
@@ -116,6 +131,8 @@ __global__ void __launch_bounds__(kCqrThreads) cholqr_apply_kernel(
     int ncolblocks) {
   __shared__ float M[R][R + 1];
   __shared__ float dinv[R];
+  pdl_trigger();
+  pdl_wait();
   if (*info != 0) return;
   for (int e = threadIdx.x; e < R * R; e += blockDim.x) M[e / R][e % R] = Lmat[e];
   if (threadIdx.x < R) dinv[threadIdx.x] = inv_diag[threadIdx.x];
@@ -184,20 +201,24 @@ static cudaError_t cholqr_launch(const void* L1, int64_t K, int64_t ld1, const v
   float* partial = ws;
   float* Lmat = ws + static_cast<int64_t>(parts) * R * R;
   float* inv_diag = Lmat + R * R;
-  cholqr_gram_kernel<R><<<parts, kCqrThreads, 0, s>>>(static_cast<const uint16_t*>(L1), K, ld1, partial);
+  // programmatic dependent launches: each kernel's set-up overlaps the previous one's tail, and
+  // each waits (griddepcontrol.wait) before its first global read
+  cudaError_t e = launch_pdl(cholqr_gram_kernel<R>, dim3(parts), dim3(kCqrThreads), 0, s,
+                             static_cast<const uint16_t*>(L1), K, ld1, partial);
   count_launch();
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  cholqr_factor_kernel<R><<<1, 1024, 0, s>>>(partial, parts, Lmat, inv_diag, info);
+  e = launch_pdl(cholqr_factor_kernel<R>, dim3(1), dim3(1024), 0, s, static_cast<const float*>(partial), parts, Lmat,
+                 inv_diag, info);
   count_launch();
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (e != cudaSuccess) return e;
   const int colblocks = static_cast<int>((K + kCqrThreads - 1) / kCqrThreads);
   const int rowblocks = static_cast<int>((N + kCqrThreads - 1) / kCqrThreads);
-  cholqr_apply_kernel<R><<<colblocks + rowblocks, kCqrThreads, 0, s>>>(
-      static_cast<const uint16_t*>(L1), K, ld1, static_cast<uint16_t*>(L1_out), static_cast<const uint16_t*>(L2), N,
-      static_cast<uint16_t*>(L2_out), Lmat, inv_diag, info, colblocks);
+  e = launch_pdl(cholqr_apply_kernel<R>, dim3(colblocks + rowblocks), dim3(kCqrThreads), 0, s,
+                 static_cast<const uint16_t*>(L1), K, ld1, static_cast<uint16_t*>(L1_out),
+                 static_cast<const uint16_t*>(L2), N, static_cast<uint16_t*>(L2_out), static_cast<const float*>(Lmat),
+                 static_cast<const float*>(inv_diag), static_cast<const int*>(info), colblocks);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_lora_cholqr(const void* L1, int64_t K, int64_t ld1, const void* L2, int64_t N, int r,
