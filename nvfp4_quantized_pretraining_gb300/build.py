@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnvfp4_gb300.so")
-SOURCES = ["quantize.cu", "gemm.cu", "lora_grad.cu", "lora_cholqr.cu", "realign.cu", "newton_schulz.cu", "qadamw.cu",
+SOURCES = ["quantize.cu", "gemm.cu", "branch.cu", "lora_grad.cu", "lora_cholqr.cu", "realign.cu", "newton_schulz.cu", "qadamw.cu",
            "peak.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE]
