@@ -630,11 +630,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
       uint32_t t = 0;
       PairWork w;
       for (; ok && pair_work(p, cluster_id, num_clusters, t, tiles_m, tiles_n, num_k, has_branch, w); ++t) {
-        if (*abort_flag || !mbar_wait_cluster(acc_empty, (t & 1) ^ 1)) { ok = false; break; }
+        if (*abort_flag || !mbar_wait(acc_empty, (t & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + TM_ACC;
         for (uint32_t it = w.kb; it < w.ke; ++it) {
-          if (!mbar_wait_cluster(&full[stage], phase)) {
+          if (!mbar_wait(&full[stage], phase)) {
             ok = false;
             break;
           }
@@ -657,7 +657,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::NUM_THREADS, 1)
         }
         if (!ok) break;
         if (w.branch) {
-          if (!mbar_wait_cluster(&full[stage], phase)) { ok = false; break; }
+          if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
           tc_fence_after();
           const uint64_t ad = adesc0 + stage * kStageD, bd = bdesc0 + stage * kStageD;
           const uint32_t nkb = (uint32_t)(p.r + 15) / 16;
