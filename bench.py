@@ -57,7 +57,7 @@ WORKLOADS = {
 GEMM_TRAFFIC = {
     # launch list of `--part step --steps 2 --warmup 3` with dram__bytes_read.sum and
     # dram__bytes_write.sum (one pass): mean over the 96 GEMM launches of the 3B block
-    "df940e31274b5f93": 215200000,
+    "f84333df2c748224": 214700000,
 }
 
 
@@ -633,43 +633,68 @@ def quantize_sweep(F, torch, S, stream, dev, flush, args):
     hbm = float(peaks()[0]["hbm_gbs"])
     reps = max(3, min(args.steps, 7))
     out = {}
-    worst = None
+    worst = worst_b2b = None
     with torch.cuda.stream(stream):
         for n in S.QUANT_SWEEP_ELEMS:
             rows, cols = n // 4096, 4096
-            g = torch.Generator(device=dev)
-            g.manual_seed(600 + rows)
-            x = torch.randn((rows, cols), generator=g, device=dev, dtype=torch.float32)
-            x = torch.where(torch.rand((rows, cols), generator=g, device=dev) < 0.001, x * 50.0, x).to(torch.bfloat16)
-            amax = F.fp4_amax(x, stream=stream)
+            # the tensor, plus copies for the back-to-back figure: distinct inputs of at least 256 MB
+            # together (more than L2), so that every call of the batch reads its tensor from HBM
+            nb = max(4, min(8, -(-(256 << 20) // (2 * n))))
+            xs = []
+            for c in range(nb):
+                g = torch.Generator(device=dev)
+                g.manual_seed(600 + rows + 7919 * c)
+                x = torch.randn((rows, cols), generator=g, device=dev, dtype=torch.float32)
+                xs.append(torch.where(torch.rand((rows, cols), generator=g, device=dev) < 0.001, x * 50.0,
+                                      x).to(torch.bfloat16))
+                del x
+            x = xs[0]
+            amaxs = [F.fp4_amax(xi, stream=stream) for xi in xs]
+            amax = amaxs[0]
             qr, qc = F.NVFP4Tensor.empty(rows, cols, dev), F.NVFP4Tensor.empty(cols, rows, dev)
             label = f"{n >> 20}M"
-            out[label] = {"shape": [rows, cols]}
+            out[label] = {"shape": [rows, cols], "back_to_back_calls": nb}
             for mode, mname in ((F.RTN, "rtn"), (F.SR, "sr")):
                 forms = {
-                    "row": (2.5625, lambda a: F.fp4_quantize(x, mode, 0, 0, amax=a, out=qr, stream=stream)),
-                    "transposed": (2.5625, lambda a: F.fp4_quantize_transposed(x, mode, 0, 1, amax=a, out=qc,
-                                                                               stream=stream)),
-                    "dual": (3.125, lambda a: F.fp4_quantize_dual(x, mode, 0, 0, 1, amax=a, out_row=qr, out_col=qc,
-                                                                  stream=stream)),
+                    "row": (2.5625, lambda xi, a: F.fp4_quantize(xi, mode, 0, 0, amax=a, out=qr, stream=stream)),
+                    "transposed": (2.5625, lambda xi, a: F.fp4_quantize_transposed(xi, mode, 0, 1, amax=a, out=qc,
+                                                                                   stream=stream)),
+                    "dual": (3.125, lambda xi, a: F.fp4_quantize_dual(xi, mode, 0, 0, 1, amax=a, out_row=qr,
+                                                                      out_col=qc, stream=stream)),
                 }
                 for form, (bpe, fn) in forms.items():
-                    ms_k = _median_ms(torch, stream, flush, lambda: fn(amax), reps)
-                    ms_a = _median_ms(torch, stream, flush, lambda: fn(None), reps)
+                    ms_k = _median_ms(torch, stream, flush, lambda: fn(x, amax), reps)
+                    ms_a = _median_ms(torch, stream, flush, lambda: fn(x, None), reps)
+
+                    def batch():
+                        for xi, ai in zip(xs, amaxs):
+                            fn(xi, ai)
+
+                    ms_b = _median_ms(torch, stream, flush, batch, reps) / nb
                     gk = bpe * n / (ms_k * 1e-3) / 1e9
                     ga = (bpe + 2.0) * n / (ms_a * 1e-3) / 1e9
+                    gb = bpe * n / (ms_b * 1e-3) / 1e9
                     out[label][f"{form}_{mname}"] = {
                         "ms": round(ms_k, 4), "gbs": round(gk, 1), "frac": round(gk / hbm, 4),
                         "ms_with_amax": round(ms_a, 4), "gbs_with_amax": round(ga, 1),
-                        "frac_with_amax": round(ga / hbm, 4)}
+                        "frac_with_amax": round(ga / hbm, 4),
+                        "ms_back_to_back": round(ms_b, 4), "frac_back_to_back": round(gb / hbm, 4)}
                     if n >= (1 << 24) and mode == F.RTN and (worst is None or gk / hbm < worst[0]):
                         worst = (gk / hbm, f"{label} {form}")
-            del x, qr, qc, amax
+                    if n >= (1 << 24) and mode == F.RTN and (worst_b2b is None or gb / hbm < worst_b2b[0]):
+                        worst_b2b = (gb / hbm, f"{label} {form}")
+            del x, xs, qr, qc, amax, amaxs
     F.fp4_check_status(stream)
     return {"bound": "hbm", "peak": hbm, "unit": "GB/s", "sizes": out,
             "min_rtn_frac_16M_up": None if worst is None else {"frac": round(worst[0], 4), "case": worst[1]},
+            "min_rtn_frac_back_to_back_16M_up": None if worst_b2b is None else
+            {"frac": round(worst_b2b[0], 4), "case": worst_b2b[1]},
             "note": "kernel-only rate with the amax supplied (frac) and the full call with the amax pass "
-                    "(frac_with_amax); algorithmic bytes over the median call time, L2 flushed before each call"}
+                    "(frac_with_amax); algorithmic bytes over the median time of one call, L2 flushed before "
+                    "each call, so a call's fixed launch and ramp cost (about 7 us, the whole 1M call) is in "
+                    "it. frac_back_to_back: the same calls issued back to back on back_to_back_calls distinct "
+                    "tensors (256 MB or more together, more than L2, so each reads HBM), the batch's median "
+                    "time per call"}
 
 
 def quantize_one(F, torch, stream, dev, flush, args):
