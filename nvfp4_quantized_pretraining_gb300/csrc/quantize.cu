@@ -157,22 +157,12 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 6 : 9) quantize_dual_kernel
   uint16_t(*rtile)[kTileC] = reinterpret_cast<uint16_t(*)[kTileC]>(dsm + kTileR * kTileC * 2);
   pdl_trigger();
   pdl_wait();
-  const float amax = *a.amax;
-  const float S_t = tensor_scale(amax);
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
-    if (ROW && a.scale_out_r) { a.scale_out_r[0] = S_t; a.scale_out_r[1] = amax; }
-    if (COL && a.scale_out_c) { a.scale_out_c[0] = S_t; a.scale_out_c[1] = amax; }
-  }
   const uint32_t r0 = blockIdx.y * kTileR, c0 = blockIdx.x * kTileC;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const bool pack4 = (a.cols & 63u) == 0;
-  __shared__ float inv_tab[128];
-  const ScaleCtx sc = scale_ctx(S_t);
-  if (tid < 128)
-    inv_tab[tid] = (tid == 0 || sc.zero) ? 0.0f : fminf(__frcp_rn(__fmul_rn(e4m3_value(tid), S_t)), 3.402823466e38f);
   constexpr int kLoads = kTileR * (kTileC / 8) / kDualThreads;  // 8
-
+  // the tile's loads first: the tensor amax, the scale set-up below and (SR) the column form's random
+  // bits run while they are in flight
   uint4 w[kLoads];
 #pragma unroll
   for (int i = 0; i < kLoads; ++i) {
@@ -181,6 +171,17 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 6 : 9) quantize_dual_kernel
     w[i] = make_uint4(0, 0, 0, 0);
     if (row < a.rows && c8 < a.cpr) w[i] = __ldcs(reinterpret_cast<const uint4*>(a.x + row * a.ld + c8 * 8));
   }
+  const float amax = *a.amax;
+  const float S_t = tensor_scale(amax);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    if (ROW && a.scale_out_r) { a.scale_out_r[0] = S_t; a.scale_out_r[1] = amax; }
+    if (COL && a.scale_out_c) { a.scale_out_c[0] = S_t; a.scale_out_c[1] = amax; }
+  }
+  const bool pack4 = (a.cols & 63u) == 0;
+  __shared__ float inv_tab[128];
+  const ScaleCtx sc = scale_ctx(S_t);
+  if (tid < 128)
+    inv_tab[tid] = (tid == 0 || sc.zero) ? 0.0f : fminf(__frcp_rn(__fmul_rn(e4m3_value(tid), S_t)), 3.402823466e38f);
   if (a.fold_p && blockIdx.x == 0) {  // (overlaps the tile's loads in flight)
     float alpha = __fmul_rn(S_t, *a.fold_other);
     if (alpha == 0.0f) alpha = 1.0f;
