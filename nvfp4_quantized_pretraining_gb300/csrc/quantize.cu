@@ -150,7 +150,8 @@ __device__ __forceinline__ uint32_t swz(uint32_t c) { return c ^ ((c >> 3) & 1u)
 constexpr int kTileR = 64, kTileC = 128;  // 64 x 128 BF16 tiles: 16 KB staged per CTA
 constexpr int kDualThreads = 128;
 
-template <bool ROW, bool COL, bool SR, bool CLIP = false>
+// J32: every element group index j = row * cpr + c8 of the tensor is below 2^32 (chosen by the host).
+template <bool ROW, bool COL, bool SR, bool CLIP = false, bool J32 = false>
 __global__ void __launch_bounds__(kDualThreads, SR ? 6 : 9) quantize_dual_kernel(const DualQuantArgs a) {
   extern __shared__ __align__(16) uint8_t dsm[];
   uint16_t(*tile)[kTileC] = reinterpret_cast<uint16_t(*)[kTileC]>(dsm);
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 6 : 9) quantize_dual_kernel
       const int q = tid + i * kDualThreads;
       const uint32_t row = r0 + (q >> 4), c8 = (c0 >> 3) + (q & 15);
       *reinterpret_cast<uint4*>(&rtile[q >> 4][(q & 15) * 8]) =
-          sr_random(a.keys, a.stream_c, (uint64_t)row * a.cpr + c8);
+          J32 ? sr_random32(a.keys, a.stream_c, row * a.cpr + c8) : sr_random(a.keys, a.stream_c, (uint64_t)row * a.cpr + c8);
     }
   }
 #pragma unroll
@@ -246,7 +247,8 @@ __global__ void __launch_bounds__(kDualThreads, SR ? 6 : 9) quantize_dual_kernel
       if (SR) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const uint4 rr = sr_random(a.keys, a.stream_r, (uint64_t)row * a.cpr + 2 * c16 + hh);
+          const uint4 rr = J32 ? sr_random32(a.keys, a.stream_r, row * a.cpr + 2 * c16 + hh)
+                               : sr_random(a.keys, a.stream_r, (uint64_t)row * a.cpr + 2 * c16 + hh);
           const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) y2[hh][q] = sr_round2(y2[hh][q], sr_bias_lo(rw[q]), sr_bias_hi(rw[q]));
@@ -448,25 +450,32 @@ cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int6
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(quantize_dual_kernel<true, true, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kTileR * kTileC * 2);
-    if (attr == cudaSuccess)
-      attr = cudaFuncSetAttribute(quantize_dual_kernel<false, true, true>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kTileR * kTileC * 2);
+    for (auto k : {quantize_dual_kernel<true, true, true>, quantize_dual_kernel<false, true, true>,
+                   quantize_dual_kernel<true, true, true, false, true>, quantize_dual_kernel<false, true, true, false, true>})
+      if (attr == cudaSuccess)
+        attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kTileR * kTileC * 2);
   });
+  // every element group index row * cpr + c8 below 2^32: the SR kernels' 32-bit counter form
+  const bool j32 = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols / 8) <= 0xFFFFFFFFull;
   if (attr != cudaSuccess) return attr;
   cudaError_t e = cudaSuccess;
   if (clip) {  // the clipped form: both orientations, RTN
     if (!(R && C) || sr) return cudaErrorInvalidValue;
     e = launch_pdl(quantize_dual_kernel<true, true, false, true>, grid, dim3(kDualThreads), smem, s, a);
   } else if (R && C) {
-    if (sr) e = launch_pdl(quantize_dual_kernel<true, true, true>, grid, dim3(kDualThreads), smem, s, a);
+    if (sr && j32)
+      e = launch_pdl(quantize_dual_kernel<true, true, true, false, true>, grid, dim3(kDualThreads), smem, s, a);
+    else if (sr) e = launch_pdl(quantize_dual_kernel<true, true, true>, grid, dim3(kDualThreads), smem, s, a);
     else e = launch_pdl(quantize_dual_kernel<true, true, false>, grid, dim3(kDualThreads), smem, s, a);
   } else if (C) {
-    if (sr) e = launch_pdl(quantize_dual_kernel<false, true, true>, grid, dim3(kDualThreads), smem, s, a);
+    if (sr && j32)
+      e = launch_pdl(quantize_dual_kernel<false, true, true, false, true>, grid, dim3(kDualThreads), smem, s, a);
+    else if (sr) e = launch_pdl(quantize_dual_kernel<false, true, true>, grid, dim3(kDualThreads), smem, s, a);
     else e = launch_pdl(quantize_dual_kernel<false, true, false>, grid, dim3(kDualThreads), smem, s, a);
   } else {
-    if (sr) e = launch_pdl(quantize_dual_kernel<true, false, true>, grid, dim3(kDualThreads), smem, s, a);
+    if (sr && j32)
+      e = launch_pdl(quantize_dual_kernel<true, false, true, false, true>, grid, dim3(kDualThreads), smem, s, a);
+    else if (sr) e = launch_pdl(quantize_dual_kernel<true, false, true>, grid, dim3(kDualThreads), smem, s, a);
     else e = launch_pdl(quantize_dual_kernel<true, false, false>, grid, dim3(kDualThreads), smem, s, a);
   }
   count_launch();

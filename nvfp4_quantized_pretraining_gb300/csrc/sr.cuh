@@ -46,6 +46,12 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys& k) {
 __device__ __forceinline__ uint4 sr_random(const PhiloxKeys& k, uint32_t stream, uint64_t j) {
   return philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(j >> 32), stream, 0u), k);
 }
+// The same for j < 2^32 (counter word 1 zero): with words 1 and 3 known zero and word 2 (the
+// stream) the same for every call, part of the first two rounds no longer depends on j, and the
+// compiler takes it out of the element loops.
+__device__ __forceinline__ uint4 sr_random32(const PhiloxKeys& k, uint32_t stream, uint32_t j) {
+  return philox4x32_10(make_uint4(j, 0u, stream, 0u), k);
+}
 
 // ---------------------------------------------------------------------------
 // The rounding rule
