@@ -344,7 +344,7 @@ def run_ours(args):
         "quantize_sr": {"bound": "alu", "elements_per_s": round(bd["sr_elems"] / (bd["sr_ms"] * 1e-3), 1),
                         "achieved_gbs": round(sr_gbs, 1), "hbm_frac": round(sr_gbs / pk["hbm_gbs"], 4),
                         "note": "dY, both forms with SR: bound by the integer ALU pipe (two Philox4x32-10 draws "
-                                "and the SR rule per element; ncu on 16384^2: ALU pipe 72% busy, 44 instructions "
+                                "and the SR rule per element; ncu on 16384^2: ALU pipe 72% busy, 43 instructions "
                                 "per element, DRAM 24%)"},
         "breakdown_ms": {k: round(v, 4) for k, v in bd["per_kind_ms"].items()},
         "lora_factor_grads": lg,
