@@ -382,6 +382,14 @@ fp4_status fp4_debug_convert(const float* in, int64_t n, uint8_t* e2m1_out,
 fp4_status fp4_debug_sr_round(const float* in, const uint16_t* rnd16, int64_t n,
                               uint8_t* e2m1_out, void* stream);
 
+/* Diagnostic: on != 0 makes every later SR quantization (until called with 0)
+ * take its kernels' general form, which computes the Philox counter word 1
+ * (the high half of the element group index) instead of assuming it zero.
+ * Tensors of 2^35 or more elements take that form anyway; this lets tests
+ * check it on small ones.  The results are the same either way.  Not for use
+ * while other host threads launch quantizations. */
+void fp4_debug_force_counter64(int on);
+
 /* Diagnostic: dense NVFP4 tensor-core rate probe.  Launches one CTA per SM;
  * each issues 4 * iters block-scaled MMAs of shape M=128 x N=n x K=64
  * (n in {128, 256}) on operands resident in shared memory.  The caller times

@@ -38,7 +38,7 @@ EXPORTS = ["fp4_scale_bytes", "fp4_amax", "fp4_quantize", "fp4_quantize_transpos
            "fp4_lora_factor_grad", "fp4_lora_cholqr_workspace", "fp4_lora_cholqr", "fp4_lora_realign_workspace",
            "fp4_lora_realign", "fp4_newton_schulz_workspace", "fp4_newton_schulz", "fp4_qadamw_v_encode",
            "fp4_qadamw_v_decode", "fp4_check_status", "fp4_last_error", "fp4_launch_count",
-           "fp4_debug_convert", "fp4_debug_sr_round", "fp4_mma_peak_probe"]
+           "fp4_debug_convert", "fp4_debug_sr_round", "fp4_debug_force_counter64", "fp4_mma_peak_probe"]
 
 
 class FP4Error(RuntimeError):
@@ -101,6 +101,7 @@ def lib() -> ctypes.CDLL:
         "fp4_launch_count": (u64, []),
         "fp4_debug_convert": (i32, [P, i64, P, P, P]),
         "fp4_debug_sr_round": (i32, [P, P, i64, P, P]),
+        "fp4_debug_force_counter64": (None, [i32]),
         "fp4_mma_peak_probe": (i32, [i32, i32, P, P]),
     }
     for name, (res, args) in sig.items():

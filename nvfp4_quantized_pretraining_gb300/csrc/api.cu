@@ -716,6 +716,8 @@ fp4_status fp4_debug_convert(const float* in, int64_t n, uint8_t* e2m1_out, uint
   return FP4_OK;
 }
 
+void fp4_debug_force_counter64(int on) { set_force_counter64(on != 0); }
+
 fp4_status fp4_debug_sr_round(const float* in, const uint16_t* rnd16, int64_t n, uint8_t* e2m1_out, void* stream) {
   if (!in || !rnd16 || !e2m1_out || n <= 0 || n > (int64_t(1) << 34))
     return fail(FP4_ERR_INVALID_ARG, "bad debug_sr_round arguments");

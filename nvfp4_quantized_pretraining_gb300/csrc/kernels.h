@@ -62,6 +62,7 @@ cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int6
                                  uint32_t stream_r, uint32_t stream_c, const float* amax, const QOut* row_out,
                                  const QOut* col_out, cudaStream_t s, const uint32_t* clip = nullptr,
                                  const BranchFold* fold = nullptr);
+void set_force_counter64(bool on);
 cudaError_t launch_debug_convert(const float* in, int64_t n, uint8_t* e2m1, uint8_t* e4m3, cudaStream_t s);
 cudaError_t launch_debug_sr_round(const float* in, const uint16_t* rnd, int64_t n, uint8_t* e2m1, cudaStream_t s);
 

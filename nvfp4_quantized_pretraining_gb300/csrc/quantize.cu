@@ -9,6 +9,7 @@
 // Format reading (the Full-Stack FP4 pages name NVFP4, section 1, and
 // "standard NVFP4", section 3, without defining it): see block_scale() and
 // tensor_scale() in common.cuh.
+#include <atomic>
 #include <mutex>
 
 #include <cuda_bf16.h>
@@ -391,6 +392,12 @@ __global__ void debug_sr_round_kernel(const float* __restrict__ in, const uint16
 // ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
+// Diagnostic switch (fp4_debug_force_counter64): the SR kernels take their general 64-bit counter
+// form whatever the tensor's size, so that tests reach the form that tensors of 2^35 or more
+// elements take.
+static std::atomic<int> g_force_counter64{0};
+void set_force_counter64(bool on) { g_force_counter64.store(on ? 1 : 0); }
+
 static int grid_for(uint64_t work_items, int per_block, int max_blocks) {
   uint64_t b = (work_items + per_block - 1) / per_block;
   if (b < 1) b = 1;
@@ -456,7 +463,8 @@ cudaError_t launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int6
         attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kTileR * kTileC * 2);
   });
   // every element group index row * cpr + c8 below 2^32: the SR kernels' 32-bit counter form
-  const bool j32 = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols / 8) <= 0xFFFFFFFFull;
+  const bool j32 = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols / 8) <= 0xFFFFFFFFull &&
+                   !g_force_counter64.load(std::memory_order_relaxed);
   if (attr != cudaSuccess) return attr;
   cudaError_t e = cudaSuccess;
   if (clip) {  // the clipped form: both orientations, RTN

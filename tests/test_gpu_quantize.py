@@ -133,6 +133,28 @@ def test_quantize_dual(F, oracle_mod, shape, mode):
     assert_same_quant(F, c, oracle_mod.quantize(x, mode, seed=1, stream=1, transposed=True), oracle_mod)
 
 
+@pytest.mark.parametrize("shape", [(208, 48), (1024, 2048)])
+def test_sr_counter_forms_agree(F, oracle_mod, shape):
+    # the SR kernels' 32-bit counter form (every tensor below 2^35 elements) and the general
+    # form that computes counter word 1: both bit-exact against the oracle, so equal
+    x = make_input(shape, "grad", seed=11)
+    want_r = oracle_mod.quantize(x, 1, seed=7, stream=0)
+    want_c = oracle_mod.quantize(x, 1, seed=7, stream=1, transposed=True)
+    outs = []
+    for force64 in (0, 1):
+        F.lib().fp4_debug_force_counter64(force64)
+        try:
+            r, c = F.fp4_quantize_dual(dev(x), round_mode=1, seed=7, sr_stream_row=0, sr_stream_col=1)
+            torch.cuda.synchronize()
+        finally:
+            F.lib().fp4_debug_force_counter64(0)
+        assert_same_quant(F, r, want_r, oracle_mod)
+        assert_same_quant(F, c, want_c, oracle_mod)
+        outs.append((r, c))
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales)
+
+
 @pytest.mark.parametrize("kind", ["tiny", "normal"])
 def test_quantize_edge_values(F, oracle_mod, kind):
     x = make_input((128, 256), kind, seed=9)
