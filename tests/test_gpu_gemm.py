@@ -215,9 +215,11 @@ def test_gemm_split_tail_is_deterministic(F):
 
 
 # 16384, 8320, 7168 and 19456 rows take h = ceil(M / 152) = 108, 55, 48 and 128 rows per CTA on
-# 152 SMs (last CTA 76, 15, 16 and 128 rows); 7168 x 704 also ends K on a half stage
+# 152 SMs (last CTA 76, 15, 16 and 128 rows); 7168 x 704 also ends K on a half stage; 19584 rows
+# (153 blocks of 128) take one CTA per 128-row block
 @pytest.mark.parametrize("M,K,r", [(128, 64, 16), (256, 512, 32), (384, 320, 48), (1024, 2048, 64),
-                                   (16384, 3072, 64), (8320, 1024, 32), (7168, 704, 16), (19456, 512, 48)])
+                                   (16384, 3072, 64), (8320, 1024, 32), (7168, 704, 16), (19456, 512, 48),
+                                   (19584, 256, 16)])
 def test_branch_factor(F, oracle_mod, M, K, r):
     X = S.student_t((M, K), 3.0, M + K)
     L = S.normal((r, K), 0.05, r)
