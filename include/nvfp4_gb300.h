@@ -276,8 +276,10 @@ fp4_status fp4_lora_factor_grad(const void* A, int64_t T, int64_t M, int64_t lda
  *   B = Ub Sigma V^T;  L2_out = bf16(Q Ub_r Sigma_r / beta);  L1_out = bf16(V_r^T);
  *   W_res_out = bf16(W - beta L2_out L1_out),
  * each L1_out row's largest-magnitude entry made positive (L2_out's column
- * follows).  FP32 arithmetic: this library's own tiled FP32 GEMM for the
- * products (outputs with few tiles split over K, the slices added in a fixed
+ * follows).  FP32 arithmetic: the products with W and W^T on the tensor cores
+ * as three TF32 products each (high and low parts of both operands; within a
+ * small multiple of FP32 rounding), the others in this library's own tiled
+ * FP32 GEMM (outputs with few tiles split over K, the slices added in a fixed
  * order: deterministic), Cholesky-QR twice for orth(), a one-CTA Jacobi
  * eigensolver for B B^T.  Allocates nothing.
  * W_res: N x K BF16, row pitch ldw (W_res_out the same); L1: r x K (pitch K);
@@ -286,7 +288,7 @@ fp4_status fp4_lora_factor_grad(const void* A, int64_t T, int64_t M, int64_t lda
  * s a multiple of 16 in [r, 128], N, K >= s, N, K < 2^31, 0 <= q <= 8, beta > 0.
  * W must have numerical rank >= s.  info (device int): 0, or nonzero when a
  * Cholesky factorisation failed (then no output is written).
- * ws: fp4_lora_realign_workspace(N, K, r, s) bytes (about 4 N K + 8 MB),
+ * ws: fp4_lora_realign_workspace(N, K, r, s) bytes (about 8 N K + 8 MB),
  * 256-byte aligned. */
 size_t fp4_lora_realign_workspace(int64_t N, int64_t K, int r, int s);
 fp4_status fp4_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t ldw,

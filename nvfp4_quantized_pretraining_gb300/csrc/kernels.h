@@ -141,8 +141,8 @@ int cholqr_parts(int64_t K);
 cudaError_t launch_lora_cholqr(const void* L1, int64_t K, int64_t ld1, const void* L2, int64_t N, int r,
                                void* L1_out, void* L2_out, int* info, float* ws, cudaStream_t s);
 
-// Randomized-SVD realignment of the LoRA-SVD subspace (FP32, cuBLAS SGEMM for the plain
-// products); ws holds realign_workspace_floats(N, K, r, s) floats; *info (device) = 0, or a
+// Randomized-SVD realignment of the LoRA-SVD subspace (FP32; the products with W on the tensor
+// cores as three TF32 products, the rest in the library's tiled FP32 GEMM); ws holds realign_workspace_floats(N, K, r, s) floats; *info (device) = 0, or a
 // failed Cholesky (1000 * stage + pivot order), in which case no output is written.
 size_t realign_workspace_floats(int64_t N, int64_t K, int r, int s);
 cudaError_t launch_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t ldw, const void* L1, const void* L2,

@@ -6,9 +6,11 @@
 //   Y = W Omega;  q times: Y = W basis(W^T basis(Y));  Q = orth(Y);  B = Q^T W;
 //   B B^T = Ub Lambda Ub^T (Jacobi);  L2 = Q Ub_r Sigma_r / beta;  L1 = Ub_r^T B / Sigma_r;
 //   W_res = W - beta bf16(L2) bf16(L1).
-// FP32 throughout.  The plain products run in this file's own tiled FP32 GEMM
-// (rl_sgemm_kernel: 64 x 64 output tiles, split over K into a fixed-order sum
-// when the output has few tiles); orth() is Cholesky-QR (the factor and its
+// FP32 throughout.  The sketch products with W and W^T (Y = W Omega, the power
+// iterations, B^T = W^T Q) run on the tensor cores as three TF32 products per
+// FP32 product (rl_tf32x3_kernel, FP32-class accuracy); the other products in
+// this file's own tiled FP32 GEMM (rl_sgemm_kernel); both split over K into a
+// fixed-order sum when the output has few tiles.  orth() is Cholesky-QR (the factor and its
 // inverse in one CTA, Y L^-T as a product): twice for the final basis,
 // once between the products of the subspace iteration, which depend on the span
 // only.  The first pass adds a small diagonal shift: the column space is that of
@@ -152,6 +154,243 @@ __global__ void __launch_bounds__(kRlThreads) rl_sgemm_reduce(int64_t m, int64_t
 
 // Elements of split-K scratch the products of one realignment need at most (see Rl::gemm).
 constexpr int64_t kRlSplitFloats = int64_t(1) << 21;
+
+// ---------------------------------------------------------------------------
+// FP32 products on the tensor cores: out (M x n, pitch n) = A B^T with A (M x Kc) and B (n x Kc)
+// both row-major and contiguous along Kc, n a multiple of 16 up to 128, as three TF32 products
+// (tcgen05.mma kind::tf32, FP32 accumulation in tensor memory):
+//   A B^T ~ A_hi B_hi^T + A_hi B_lo^T + A_lo B_hi^T,  x_hi = x with its 13 low mantissa bits
+//   cleared (exactly a TF32 value), x_lo = x - x_hi (exact in FP32).
+// The dropped term A_lo B_lo^T is below 2^-20 |a||b| per product, and the tensor core's
+// conversion of x_lo to TF32 loses at most 2^-21 |x|, so the result is within a small multiple of
+// FP32 rounding.  A's tiles arrive
+// by TMA in FP32 and four warps split them in shared memory (the high part in place, the low
+// part beside it); B is split once beforehand, its high and low parts stacked as the rows
+// [0, n) and [n, 2n) of one 2n x Kc matrix.  blockIdx.x takes 128 rows of A, blockIdx.y the
+// K stages [y * kss, (y + 1) * kss): with one slice it writes out directly, with several
+// out is slice y's partial sum (M x n) and rl_sgemm_reduce adds the slices in order.
+// ---------------------------------------------------------------------------
+namespace rt {
+constexpr int BM = 128;
+constexpr int BK = 32;                    // FP32 elements of K per stage: one 128-byte row
+constexpr int STAGES = 3;
+constexpr int TILE_BYTES = BM * BK * 4;   // 16 KB: 128 rows of A, or up to 128 rows of B
+constexpr int STAGE_BYTES = 4 * TILE_BYTES;  // A_hi, A_lo, B_hi, B_lo
+constexpr int NUM_THREADS = 192;          // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 split + epilogue
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+}  // namespace rt
+
+// Instruction descriptor, kind::tf32: TF32 x TF32 -> FP32, K-major A and B.
+__host__ __device__ constexpr uint32_t idesc_tf32(uint32_t M, uint32_t N) {
+  return (1u << 4)             // D format FP32
+         | (2u << 7)           // A format TF32
+         | (2u << 10)          // B format TF32
+         | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void rl_tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])
+               :
+               : "memory");
+}
+__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+
+__global__ void __launch_bounds__(rt::NUM_THREADS, 1)
+    rl_tf32x3_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                     uint32_t M, uint32_t n, uint32_t Kc, uint32_t kss, float* __restrict__ out) {
+  using namespace rt;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* ready = full + STAGES;
+  uint64_t* empty = ready + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* done_bar = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&ready[s], 4);  // the four split warps
+      mbar_init(&empty[s], 1);  // the MMA commit
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t num_k_all = (Kc + BK - 1) / BK;
+  const uint32_t k_begin = blockIdx.y * kss;
+  const uint32_t num_k = min(kss, num_k_all - k_begin);  // >= 1: the host makes no empty slice
+  const uint32_t m0 = blockIdx.x * BM;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int armed[STAGES];
+      uint32_t armed_phase[STAGES];
+      for (int s = 0; s < STAGES; ++s) armed[s] = 0, armed_phase[s] = 0;
+      bool ok = true;
+      for (uint32_t it = 0; it < num_k; ++it) {
+        if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
+        uint8_t* st = smem + stage * STAGE_BYTES;
+        // A's 128 rows (rows past M and columns past Kc arrive zero-filled), then B's high and low rows
+        mbar_arrive_expect_tx(&full[stage], TILE_BYTES + 2 * n * BK * 4);
+        const int32_t kx = (int32_t)((k_begin + it) * BK);
+        tma_load_2d(st, &tmap_a, &full[stage], kx, (int32_t)m0);
+        tma_load_2d(st + 2 * TILE_BYTES, &tmap_b, &full[stage], kx, 0);
+        tma_load_2d(st + 3 * TILE_BYTES, &tmap_b, &full[stage], kx, (int32_t)n);
+        armed[stage] = 1;
+        armed_phase[stage] = phase;
+        if (++stage == STAGES) stage = 0, phase ^= 1;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        for (int s = 0; s < STAGES; ++s)
+          if (armed[s]) mbar_wait(&full[s], armed_phase[s]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_tf32(BM, n);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (uint32_t it = 0; it < num_k; ++it) {
+        if (*abort_flag || !mbar_wait(&ready[stage], phase)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+#pragma unroll
+        for (uint32_t kk = 0; kk < BK / 8; ++kk) {  // 8 TF32 elements (32 bytes) of K per MMA
+          const uint32_t o = kk * 32;
+          const uint64_t a_hi = smem_desc(sa + o, 16, 1024, kSwizzle128B);
+          const uint64_t a_lo = smem_desc(sa + TILE_BYTES + o, 16, 1024, kSwizzle128B);
+          const uint64_t b_hi = smem_desc(sa + 2 * TILE_BYTES + o, 16, 1024, kSwizzle128B);
+          const uint64_t b_lo = smem_desc(sa + 3 * TILE_BYTES + o, 16, 1024, kSwizzle128B);
+          mma_tf32(tmem, a_lo, b_hi, idesc, (it | kk) != 0);
+          mma_tf32(tmem, a_hi, b_lo, idesc, 1);
+          mma_tf32(tmem, a_hi, b_hi, idesc, 1);
+        }
+        tc_commit(&empty[stage]);
+        if (++stage == STAGES) stage = 0, phase ^= 1;
+      }
+      if (ok) tc_commit(acc_full);
+      else *abort_flag = 1;
+      tc_commit(done_bar);
+      mbar_wait(done_bar, 0);
+    }
+  } else {
+    // warps 2..5: split each landed A tile (an elementwise map, so the swizzle does not matter),
+    // then drain the accumulator: warp w reads TMEM lanes 32 (w % 4) .. + 31, one row per lane
+    const int t = (warp - 2) * 32 + lane;
+    uint32_t stage = 0, phase = 0;
+    for (uint32_t it = 0; it < num_k; ++it) {
+      if (*abort_flag || !mbar_wait_warp(&full[stage], phase)) {
+        *abort_flag = 1;
+        break;
+      }
+      float4* hi = reinterpret_cast<float4*>(smem + stage * STAGE_BYTES);
+      float4* lo = reinterpret_cast<float4*>(smem + stage * STAGE_BYTES + TILE_BYTES);
+#pragma unroll
+      for (int i = 0; i < TILE_BYTES / 16 / 128; ++i) {
+        const int u = t + 128 * i;
+        const float4 v = hi[u];
+        const float4 h = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
+        hi[u] = h;
+        lo[u] = make_float4(__fsub_rn(v.x, h.x), __fsub_rn(v.y, h.y), __fsub_rn(v.z, h.z), __fsub_rn(v.w, h.w));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ready[stage]);
+      if (++stage == STAGES) stage = 0, phase ^= 1;
+    }
+    const uint32_t quad = warp & 3;
+    if (!*abort_flag && mbar_wait_warp(acc_full, 0)) {
+      tc_fence_after();
+      const uint32_t row = m0 + quad * 32 + lane;
+      for (uint32_t j = 0; j < n / 16; ++j) {
+        uint32_t v[16];
+        rl_tmem_ld16(tmem + ((quad * 32) << 16) + 16 * j, v);
+        if (row < M) {
+          float* dst = out + (size_t)blockIdx.y * M * n + (size_t)row * n + 16 * j;
+          if ((reinterpret_cast<uintptr_t>(out) & 15u) == 0) {  // n % 16 == 0: every row starts aligned
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              reinterpret_cast<float4*>(dst)[q] =
+                  make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                              __uint_as_float(v[4 * q + 3]));
+          } else {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) dst[q] = __uint_as_float(v[q]);
+          }
+        }
+      }
+      tc_fence_before();
+    } else {
+      *abort_flag = 1;
+    }
+  }
+  __syncthreads();
+  if (*abort_flag) {  // a wait expired: let copies still in flight land first
+    if (threadIdx.x == 0) drain_pause();
+    __syncthreads();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+// Transpose of an FP32 matrix (rows x cols, pitch cols) into out (cols x rows, pitch rows); with
+// SPLIT, the TF32 high part goes to out's rows [0, cols) and the low part to rows [cols, 2 cols).
+template <bool SPLIT>
+__global__ void rl_transpose_kernel(const float* __restrict__ in, int64_t rows, int64_t cols,
+                                    float* __restrict__ out) {
+  __shared__ float t[32][33];
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + threadIdx.x;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int64_t r = static_cast<int64_t>(blockIdx.y) * 32 + i;
+    if (r < rows && c < cols) t[i][threadIdx.x] = in[r * cols + c];
+  }
+  __syncthreads();
+  const int64_t r2 = static_cast<int64_t>(blockIdx.y) * 32 + threadIdx.x;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int64_t c2 = static_cast<int64_t>(blockIdx.x) * 32 + i;
+    if (r2 < rows && c2 < cols) {
+      const float v = t[threadIdx.x][i];
+      if (SPLIT) {
+        const float h = tf32_hi(v);
+        out[c2 * rows + r2] = h;
+        out[(cols + c2) * rows + r2] = __fsub_rn(v, h);
+      } else {
+        out[c2 * rows + r2] = v;
+      }
+    }
+  }
+}
 
 // ---------------------------------------------------------------------------
 // Cholesky of an S x S Gram matrix (S <= 128, a multiple of 16) in one CTA, and
@@ -503,6 +742,56 @@ struct Rl {
     else if (pick == 4) launch_t<32, 128>(ta, tb, grid, m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
     else launch_t<64, 64>(ta, tb, grid, m, n, k, kslice, alpha, A, lda, B, ldb, beta, C, ldc, part);
   }
+  // out (m x n, pitch n) = A X with A m x kc (pitch kc) and X kc x n (pitch n), on the tensor
+  // cores (rl_tf32x3_kernel) when the shapes suit its tiles and TMA (m >= 128, kc >= 32 and a
+  // multiple of 4, n a multiple of 16 up to 128), else on the tiled FP32 GEMM.  bsplit: 2 n x kc
+  // floats of scratch for X^T split into its TF32 high and low parts.  Outputs with fewer
+  // 128-row tiles than SMs are split over K, as far as the split-K scratch holds the slices.
+  void tc(const float* A, int64_t m, int64_t kc, const float* X, int n, float* bsplit, float* out) {
+    if (err != cudaSuccess) return;
+    if (m < rt::BM || kc < rt::BK || kc % 4 != 0 || n % 16 != 0 || n > 128) {
+      gemm(false, false, m, n, kc, 1.0f, A, kc, X, n, 0.0f, out, n);
+      return;
+    }
+    rl_transpose_kernel<true><<<dim3(static_cast<unsigned>((n + 31) / 32), static_cast<unsigned>((kc + 31) / 32)),
+                                dim3(32, 8), 0, s>>>(X, kc, n, bsplit);
+    count_launch();
+    if ((err = cudaGetLastError()) != cudaSuccess) return;
+    CUtensorMap ta, tb;
+    if (!make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, kc, m, kc * 4, rt::BK, rt::BM,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, bsplit, kc, 2 * n, kc * 4, rt::BK, n,
+                      CU_TENSOR_MAP_SWIZZLE_128B)) {
+      err = cudaErrorInvalidValue;
+      return;
+    }
+    const int64_t tiles = (m + rt::BM - 1) / rt::BM, stages = (kc + rt::BK - 1) / rt::BK;
+    int64_t splits = tiles < num_sms ? num_sms / tiles : 1;  // one CTA per SM: at most one wave
+    if (splits > stages / 8) splits = stages / 8;             // slices of at least 8 stages
+    if (splits > kRlSplitFloats / (m * n)) splits = kRlSplitFloats / (m * n);
+    if (splits < 1) splits = 1;
+    const int64_t kss = (stages + splits - 1) / splits;
+    splits = (stages + kss - 1) / kss;
+    rl_tf32x3_kernel<<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(splits)), rt::NUM_THREADS,
+                       rt::SMEM_BYTES, s>>>(ta, tb, static_cast<uint32_t>(m), static_cast<uint32_t>(n),
+                                            static_cast<uint32_t>(kc), static_cast<uint32_t>(kss),
+                                            splits > 1 ? split : out);
+    count_launch();
+    if ((err = cudaGetLastError()) != cudaSuccess) return;
+    if (splits > 1) {
+      rl_sgemm_reduce<<<grid(m * n), kRlThreads, 0, s>>>(m, n, static_cast<int>(splits), 1.0f, split, 0.0f, out, n);
+      count_launch();
+      err = cudaGetLastError();
+    }
+  }
+  // out (cols x rows, pitch rows) = in^T, in rows x cols (pitch cols)
+  void transpose(const float* in, int64_t rows, int64_t cols, float* out) {
+    if (err != cudaSuccess) return;
+    rl_transpose_kernel<false><<<dim3(static_cast<unsigned>((cols + 31) / 32), static_cast<unsigned>((rows + 31) / 32)),
+                                 dim3(32, 8), 0, s>>>(in, rows, cols, out);
+    count_launch();
+    err = cudaGetLastError();
+  }
   int grid(int64_t n) const {
     const int64_t b = (n + kRlThreads - 1) / kRlThreads;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
@@ -555,7 +844,9 @@ size_t realign_workspace_floats(int64_t N, int64_t K, int r, int s) {
          + 5 * static_cast<size_t>(s) * s + 4 * static_cast<size_t>(s)  // G, M, C, evecs, spare; evals, rs, cs, spare
          + static_cast<size_t>(r * K) + static_cast<size_t>(N * r)      // T1, T2
          + static_cast<size_t>(r * K) + static_cast<size_t>(N * r)      // L1, L2 (FP32)
-         + static_cast<size_t>(kRlSplitFloats);                         // split-K partial sums
+         + static_cast<size_t>(kRlSplitFloats)                          // split-K partial sums
+         + 64 + static_cast<size_t>(N * K)                              // W^T (64: alignment)
+         + 64 + 2 * static_cast<size_t>(s) * static_cast<size_t>(N > K ? N : K);  // split small operand
 }
 
 cudaError_t launch_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t ldw, const void* L1, const void* L2,
@@ -566,6 +857,8 @@ cudaError_t launch_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t
   if (!attr_done.load()) {
     const int jac = (2 * kRlMaxS * (kRlMaxS + 1) + 2 * kRlMaxS) * 4;
     if ((e = cudaFuncSetAttribute(rl_jacobi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, jac))) return e;
+    if ((e = cudaFuncSetAttribute(rl_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, rt::SMEM_BYTES)))
+      return e;
     attr_done.store(1);
   }
   const int sc = s_cols;
@@ -587,6 +880,11 @@ cudaError_t launch_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t
   float* L1f = T2 + N * r;
   float* L2f = L1f + static_cast<int64_t>(r) * K;
   float* split = L2f + N * r;
+  const auto aligned = [](float* p) {  // 256-byte aligned (TMA wants 16)
+    return reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(p) + 255) & ~uintptr_t(255));
+  };
+  float* Wt = aligned(split + kRlSplitFloats);  // K x N
+  float* Bs = aligned(Wt + N * K);             // 2 sc x max(N, K)
 
   if ((e = cudaMemsetAsync(info, 0, sizeof(int), st)) != cudaSuccess) return e;
   Rl rl{st, num_sms, split};
@@ -595,19 +893,20 @@ cudaError_t launch_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t
   rl.to_f32(L1, K, L1f, K, r, K);
   rl.to_f32(L2, r, L2f, r, N, r);
   rl.gemm(false, false, N, K, r, beta, L2f, r, L1f, K, 1.0f, W, K);
-  // range finder with q power iterations
+  rl.transpose(W, N, K, Wt);
+  // range finder with q power iterations (the products with W and W^T on the tensor cores)
   rl.to_f32(Omega, sc, Om, sc, K, sc);
-  rl.gemm(false, false, N, sc, K, 1.0f, W, K, Om, sc, 0.0f, Y, sc);
+  rl.tc(W, N, K, Om, sc, Bs, Y);
   for (int it = 0; it < q; ++it) {
     const float* Yb = rl.orth(Y, T, N, sc, G, L, info, 2 * it, 1);
-    rl.gemm(true, false, K, sc, N, 1.0f, W, K, Yb, sc, 0.0f, Z, sc);
+    rl.tc(Wt, K, N, Yb, sc, Bs, Z);
     const float* Zb = rl.orth(Z, T, K, sc, G, L, info, 2 * it + 1, 1);
-    rl.gemm(false, false, N, sc, K, 1.0f, W, K, Zb, sc, 0.0f, Y, sc);
+    rl.tc(W, N, K, Zb, sc, Bs, Y);
   }
   rl.orth(Y, T, N, sc, G, L, info, 2 * q, 2);  // the final basis, orthonormal, back in Y
-  // B = Q^T W, C = B B^T = Ub Lambda Ub^T
-  rl.gemm(true, false, sc, K, N, 1.0f, Y, sc, W, K, 0.0f, B, K);
-  rl.gemm(false, true, sc, sc, K, 1.0f, B, K, B, K, 0.0f, C, sc);
+  // B^T = W^T Q (K x sc, in B's place), C = B B^T = Ub Lambda Ub^T
+  rl.tc(Wt, K, N, Y, sc, Bs, B);
+  rl.gemm(true, false, sc, sc, K, 1.0f, B, sc, B, sc, 0.0f, C, sc);
   if (rl.err != cudaSuccess) return rl.err;
   {
     const size_t smem = (2 * static_cast<size_t>(sc) * (sc + 1) + 2 * sc) * sizeof(float);
@@ -616,7 +915,7 @@ cudaError_t launch_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   // T1 = Ub_r^T B (r x K), T2 = Q Ub_r (N x r); signs and scales; BF16 factors
-  rl.gemm(true, false, r, K, sc, 1.0f, Ub, sc, B, K, 0.0f, T1, K);
+  rl.gemm(true, true, r, K, sc, 1.0f, Ub, sc, B, sc, 0.0f, T1, K);
   rl.gemm(false, false, N, r, sc, 1.0f, Y, sc, Ub, sc, 0.0f, T2, r);
   if (rl.err != cudaSuccess) return rl.err;
   rl_sign_scale_kernel<<<r, kRlThreads, 0, st>>>(T1, K, evals, beta, rs, cs, info);
