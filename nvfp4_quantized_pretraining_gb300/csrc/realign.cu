@@ -173,12 +173,19 @@ constexpr int64_t kRlSplitFloats = int64_t(1) << 21;
 namespace rt {
 constexpr int BM = 128;
 constexpr int BK = 32;                    // FP32 elements of K per stage: one 128-byte row
-constexpr int STAGES = 3;
-constexpr int TILE_BYTES = BM * BK * 4;   // 16 KB: 128 rows of A, or up to 128 rows of B
-constexpr int STAGE_BYTES = 4 * TILE_BYTES;  // A_hi, A_lo, B_hi, B_lo
+constexpr int MAX_STAGES = 4;
+constexpr int TILE_BYTES = BM * BK * 4;   // 16 KB: 128 rows of A
 constexpr int NUM_THREADS = 192;          // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 split + epilogue
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+constexpr int SMEM_MAX = 232448;
+// A stage holds A_hi, A_lo (16 KB each), then B_hi and B_lo (n rows of 128 bytes each: a
+// multiple of 1024 bytes for n % 8 == 0); as many stages as fit, up to four.
+__host__ __device__ constexpr uint32_t stage_bytes(uint32_t n) { return 2 * TILE_BYTES + 2 * n * BK * 4; }
+__host__ __device__ constexpr uint32_t num_stages(uint32_t n) {
+  return (SMEM_MAX - 1024 - 256) / stage_bytes(n) < MAX_STAGES ? (SMEM_MAX - 1024 - 256) / stage_bytes(n)
+                                                                : MAX_STAGES;
+}
+__host__ __device__ constexpr uint32_t smem_bytes(uint32_t n) { return num_stages(n) * stage_bytes(n) + 1024 + 256; }
+static_assert(num_stages(128) >= 3 && num_stages(80) == 4 && smem_bytes(96) <= SMEM_MAX, "stages");
 }  // namespace rt
 
 // Instruction descriptor, kind::tf32: TF32 x TF32 -> FP32, K-major A and B.
@@ -218,6 +225,7 @@ __global__ void __launch_bounds__(rt::NUM_THREADS, 1)
   using namespace rt;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t STAGES = num_stages(n), STAGE_BYTES = stage_bytes(n), B_BYTES = n * BK * 4;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint64_t* ready = full + STAGES;
   uint64_t* empty = ready + STAGES;
@@ -227,7 +235,7 @@ __global__ void __launch_bounds__(rt::NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (uint32_t s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&ready[s], 4);  // the four split warps
       mbar_init(&empty[s], 1);  // the MMA commit
@@ -250,26 +258,26 @@ __global__ void __launch_bounds__(rt::NUM_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
-      int armed[STAGES];
-      uint32_t armed_phase[STAGES];
-      for (int s = 0; s < STAGES; ++s) armed[s] = 0, armed_phase[s] = 0;
+      int armed[MAX_STAGES];
+      uint32_t armed_phase[MAX_STAGES];
+      for (int s = 0; s < MAX_STAGES; ++s) armed[s] = 0, armed_phase[s] = 0;
       bool ok = true;
       for (uint32_t it = 0; it < num_k; ++it) {
         if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
         uint8_t* st = smem + stage * STAGE_BYTES;
         // A's 128 rows (rows past M and columns past Kc arrive zero-filled), then B's high and low rows
-        mbar_arrive_expect_tx(&full[stage], TILE_BYTES + 2 * n * BK * 4);
+        mbar_arrive_expect_tx(&full[stage], TILE_BYTES + 2 * B_BYTES);
         const int32_t kx = (int32_t)((k_begin + it) * BK);
         tma_load_2d(st, &tmap_a, &full[stage], kx, (int32_t)m0);
         tma_load_2d(st + 2 * TILE_BYTES, &tmap_b, &full[stage], kx, 0);
-        tma_load_2d(st + 3 * TILE_BYTES, &tmap_b, &full[stage], kx, (int32_t)n);
+        tma_load_2d(st + 2 * TILE_BYTES + B_BYTES, &tmap_b, &full[stage], kx, (int32_t)n);
         armed[stage] = 1;
         armed_phase[stage] = phase;
         if (++stage == STAGES) stage = 0, phase ^= 1;
       }
       if (!ok) {
         *abort_flag = 1;
-        for (int s = 0; s < STAGES; ++s)
+        for (uint32_t s = 0; s < STAGES; ++s)
           if (armed[s]) mbar_wait(&full[s], armed_phase[s]);
       }
     }
@@ -288,7 +296,7 @@ __global__ void __launch_bounds__(rt::NUM_THREADS, 1)
           const uint64_t a_hi = smem_desc(sa + o, 16, 1024, kSwizzle128B);
           const uint64_t a_lo = smem_desc(sa + TILE_BYTES + o, 16, 1024, kSwizzle128B);
           const uint64_t b_hi = smem_desc(sa + 2 * TILE_BYTES + o, 16, 1024, kSwizzle128B);
-          const uint64_t b_lo = smem_desc(sa + 3 * TILE_BYTES + o, 16, 1024, kSwizzle128B);
+          const uint64_t b_lo = smem_desc(sa + 2 * TILE_BYTES + B_BYTES + o, 16, 1024, kSwizzle128B);
           mma_tf32(tmem, a_lo, b_hi, idesc, (it | kk) != 0);
           mma_tf32(tmem, a_hi, b_lo, idesc, 1);
           mma_tf32(tmem, a_hi, b_hi, idesc, 1);
@@ -680,7 +688,7 @@ struct Rl {
   cudaError_t err = cudaSuccess;
 
   // Row-major C (m x n, ldc) = alpha op(A) op(B) + beta C, op(A) m x k, op(B) k x n.  An output
-  // of fewer tiles than two per SM is split over K (slices of at least 512) into the scratch, as
+  // of fewer tiles than two per SM is split over K (slices of at least 128) into the scratch, as
   // far as it holds the slices.
   void gemm(bool ta, bool tb, int64_t m, int64_t n, int64_t k, float alpha, const float* A, int64_t lda,
             const float* B, int64_t ldb, float beta, float* C, int64_t ldc) {
@@ -700,11 +708,11 @@ struct Rl {
     const int64_t want = 2 * static_cast<int64_t>(num_sms);
     if (tiles < want) {
       splits = (want + tiles - 1) / tiles;
-      const int64_t by_k = (k + 511) / 512;
+      const int64_t by_k = (k + 127) / 128;
       if (splits > by_k) splits = by_k;
       const int64_t by_ws = kRlSplitFloats / (m * n);
       if (splits > by_ws) splits = by_ws;
-      if (splits > 64) splits = 64;
+      if (splits > 256) splits = 256;
       if (splits < 1) splits = 1;
     }
     int64_t kslice = (k + splits - 1) / splits;
@@ -773,7 +781,7 @@ struct Rl {
     const int64_t kss = (stages + splits - 1) / splits;
     splits = (stages + kss - 1) / kss;
     rl_tf32x3_kernel<<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(splits)), rt::NUM_THREADS,
-                       rt::SMEM_BYTES, s>>>(ta, tb, static_cast<uint32_t>(m), static_cast<uint32_t>(n),
+                       rt::smem_bytes(static_cast<uint32_t>(n)), s>>>(ta, tb, static_cast<uint32_t>(m), static_cast<uint32_t>(n),
                                             static_cast<uint32_t>(kc), static_cast<uint32_t>(kss),
                                             splits > 1 ? split : out);
     count_launch();
@@ -857,7 +865,7 @@ cudaError_t launch_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t
   if (!attr_done.load()) {
     const int jac = (2 * kRlMaxS * (kRlMaxS + 1) + 2 * kRlMaxS) * 4;
     if ((e = cudaFuncSetAttribute(rl_jacobi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, jac))) return e;
-    if ((e = cudaFuncSetAttribute(rl_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, rt::SMEM_BYTES)))
+    if ((e = cudaFuncSetAttribute(rl_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, rt::SMEM_MAX)))
       return e;
     attr_done.store(1);
   }
