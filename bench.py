@@ -523,8 +523,10 @@ def lora_realign(F, torch, S, projs, r, stream, dev, flush, args):
     """Times the randomized-SVD realignment of each projection's weight (W_res + L2 L1, rank r,
     sketch width r + 16, 2 power iterations), out of place, each call after an L2 flush.  Not
     part of the timed step (it runs every few thousand steps).  FLOPs are those of the FP32
-    products, 2 N K (2 r + s (2 + 2 q)) per weight, against the FP32 CUDA-core rate
-    (152 SMs x 128 FMA/clk x 2 FLOP x the sampled SM clock is ~80 TFLOP/s at 2.07 GHz)."""
+    products, 2 N K (2 r + s (2 + 2 q)) per weight (the sketch products run on the tensor cores
+    as three TF32 products each, the rest on the CUDA cores), shown against the FP32 CUDA-core
+    rate (152 SMs x 128 FMA/clk x 2 FLOP x 2.07 GHz, ~80 TFLOP/s) for scale; most of the call's
+    time is now in its one-CTA Jacobi and Cholesky kernels, so it is latency-bound."""
     s_cols, q = r + REALIGN_OVERSAMPLE, REALIGN_POWER_ITERS
     reps = max(1, min(args.steps, 3))
     total, flops = 0.0, 0.0
@@ -556,9 +558,11 @@ def lora_realign(F, torch, S, projs, r, stream, dev, flush, args):
     fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12
     tf = flops / (total * 1e-3) / 1e12
     return {"ms_total": round(total, 4), "sketch": s_cols, "power_iters": q, "fp32_tflops": round(tf, 1),
-            "bound": "alu", "peak": round(fp32_peak, 1), "unit": "TFLOP/s", "frac": round(tf / fp32_peak, 4),
-            "note": "four weights of the block; FP32 product FLOPs over the summed median call times; the peak "
-                    "is the FP32 FMA rate at the 2.07 GHz maximum SM clock"}
+            "bound": "latency", "peak": round(fp32_peak, 1), "unit": "TFLOP/s", "frac": round(tf / fp32_peak, 4),
+            "note": "four weights of the block; FP32 product FLOPs over the summed median call times (the "
+                    "products with W and W^T on the tensor cores as three TF32 products each, the others on the "
+                    "CUDA cores; the one-CTA Jacobi eigensolver and Cholesky factorisations take most of the "
+                    "time); the peak is the FP32 FMA rate at the 2.07 GHz maximum SM clock, for scale"}
 
 
 def run_part(args, F, torch, S, dev):

@@ -522,6 +522,7 @@ __global__ void __launch_bounds__(kRlJacThreads) rl_jacobi_kernel(const float* _
   float2* CSN = reinterpret_cast<float2*>(V + s * ld);  // s / 2 (cosine, sine) pairs
   int2* PQ = reinterpret_cast<int2*>(CSN + s / 2);      // s / 2 (head, tail) pairs
   __shared__ int rotated;
+  __shared__ int round_rotated[2];  // round t's flag in [t & 1]
   __shared__ float red[kRlJacThreads / 32];
   if (*info != 0) return;
   float sq = 0.0f;
@@ -558,24 +559,33 @@ __global__ void __launch_bounds__(kRlJacThreads) rl_jacobi_kernel(const float* _
     it_v[j] = f < half * s ? (uint32_t)(f / s) | ((uint32_t)(f % s) << 8) : kNone;
   }
   for (int sweep = 0; sweep < max_sweeps; ++sweep) {
-    if (threadIdx.x == 0) rotated = 0;
+    if (threadIdx.x == 0) rotated = round_rotated[0] = round_rotated[1] = 0;
     __syncthreads();
     for (int round = 0; round < s - 1; ++round) {
       for (int k = threadIdx.x; k < half; k += blockDim.x) {
-        const int p = k == 0 ? s - 1 : (round + k) % (s - 1);
-        const int q = k == 0 ? round : (round - k + (s - 1)) % (s - 1);
+        // round-robin pairs: (s - 1, round) and ((round + k) mod (s - 1), (round - k) mod (s - 1))
+        int p = round + k, q = round - k;
+        if (p >= s - 1) p -= s - 1;
+        if (q < 0) q += s - 1;
+        if (k == 0) p = s - 1;
         const float apq = A[p * ld + q], app = A[p * ld + p], aqq = A[q * ld + q];
         float c = 1.0f, t = 0.0f;
         if (fabsf(apq) > thresh) {
           const float tau = (aqq - app) / (2.0f * apq);
           t = (tau >= 0.0f ? 1.0f : -1.0f) / (fabsf(tau) + sqrtf(1.0f + tau * tau));
           c = rsqrtf(1.0f + t * t);
+          round_rotated[round & 1] = 1;
           rotated = 1;
         }
         PQ[k] = make_int2(p, q);
         CSN[k] = make_float2(c, t * c);
       }
+      // the next round's flag: every read of it (last round) came before this round's first barrier
+      if (threadIdx.x == 0) round_rotated[(round + 1) & 1] = 0;
       __syncthreads();
+      // a round without a rotation changes nothing: no update, and no second barrier (its pairs and
+      // rotations are not read, and A is not written)
+      if (!round_rotated[round & 1]) continue;
       // A <- J^T A J as 2 x 2 blocks; V <- V J
 #pragma unroll
       for (int j = 0; j < kItA; ++j) {
