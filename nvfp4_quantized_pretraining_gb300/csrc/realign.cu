@@ -403,76 +403,131 @@ __global__ void rl_transpose_kernel(const float* __restrict__ in, int64_t rows, 
 // ---------------------------------------------------------------------------
 // Cholesky of an S x S Gram matrix (S <= 128, a multiple of 16) in one CTA, and
 // the inverse of the factor: G + shift * mean(diag) I = L L^T (right-looking on
-// the unscaled columns, one barrier per column: with d_j the pivot,
-// G_ik -= G_ij G_kj / d_j, and L_ij = G_ij / sqrt(d_j) at the end), then
-// M = L^-1 with thread c holding column c in registers: x_i = (delta_ic -
-// sum_{k < i} L_ik x_k) / L_ii, every lane reading the same L_ik (a shared-memory
-// broadcast).  Writes M (lower, row-major S x S); a non-positive pivot sets *info
-// (if still 0) to 1000 * stage + its order.
+// the unscaled columns: with d_j the pivot, G_ik -= (G_ij / d_j) G_kj, and
+// L_ij = G_ij / sqrt(d_j) at the end), then M = L^-1 with thread c computing
+// column c by forward substitution: x_i = (delta_ic - sum_{k < i} L_ik x_k) / L_ii.
+// The 256 threads hold G as a 16 x 16 grid of (S/16) x (S/16) register blocks
+// (thread (ty, tx) has rows ty + 16a and columns tx + 16b), so each step's update
+// is local: the owners of column j publish it in shared memory, one barrier, and
+// every thread updates its own elements.  The substitution runs right-looking
+// (once x_i is known, every later row's partial sum takes its term), which adds
+// each row's terms in the same order as the left-looking form but leaves the
+// multiply-adds of a step independent of each other.  The partial sums of rows
+// i, i + 1, .. sit in registers r[0], r[1], .. and shift down by one each step
+// (r[t] <- r[t + 1] - L_{i+1+t,i} x_i), so that every index is a compile-time
+// one; step i's coefficients L_{i+1+t,i} are stored from the start of a padded
+// row of shared memory (zeros past the end), read 16 bytes at a time.  Writes M
+// (lower, row-major S x S); a non-positive pivot sets *info (if still 0) to
+// 1000 * stage + its order.
 // ---------------------------------------------------------------------------
 constexpr int kRlCholThreads = 256;
+
+template <int S>
+constexpr int chol_smem_floats() {
+  return S * (S + 4) + 4 * S;  // sub-diagonal coefficients (rows padded), two column buffers, pivots, diagonal
+}
 
 template <int S>
 __global__ void __launch_bounds__(kRlCholThreads) rl_cholesky_kernel(const float* __restrict__ Gin, float shift,
                                                                      float* __restrict__ Mout, int* __restrict__ info,
                                                                      int stage) {
-  constexpr int ld = S + 1;
-  extern __shared__ float G[];  // S x ld: G, then L
+  constexpr int B = S / 16;
+  constexpr int ld = S + 4;
+  extern __shared__ float sh[];
+  float* LS = sh;             // LS[k * ld + t] = L_{k+1+t, k} for t < S - 1 - k, 0 beyond
+  float* col = sh + S * ld;   // column j of the partly factored matrix, in col[(j & 1) * S + i]
+  float* piv = col + 2 * S;   // the pivots d_j
+  float* diag = piv + S;      // L_kk
   __shared__ float mean_diag;
-  for (int e = threadIdx.x; e < S * S; e += blockDim.x) G[(e / S) * ld + e % S] = Gin[e];
-  __syncthreads();
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float g[B][B];
+#pragma unroll
+  for (int a = 0; a < B; ++a)
+#pragma unroll
+    for (int b = 0; b < B; ++b) g[a][b] = Gin[(ty + 16 * a) * S + tx + 16 * b];
   if (threadIdx.x == 0) {
     float t = 0.0f;
-    for (int i = 0; i < S; ++i) t += G[i * ld + i];
+    for (int i = 0; i < S; ++i) t += Gin[i * S + i];
     mean_diag = t / S;
   }
+  // zero the coefficient rows (their tails past each step's last row stay zero; the barriers of the
+  // factorization order this before the coefficients are written)
+  for (int e = threadIdx.x; e < S * ld; e += kRlCholThreads) LS[e] = 0.0f;
   __syncthreads();
-  for (int i = threadIdx.x; i < S; i += blockDim.x) G[i * ld + i] += shift * mean_diag;
-  __syncthreads();
+  if (tx == ty) {
+    const float add = shift * mean_diag;
+#pragma unroll
+    for (int a = 0; a < B; ++a) g[a][a] += add;
+  }
   int bad = 0;
-  for (int j = 0; j < S; ++j) {
-    const float d = G[j * ld + j];  // every thread reads the same pivot: the test is uniform
-    if (!(d > 0.0f)) {
-      bad = j + 1;
-      break;
+#pragma unroll
+  for (int bj = 0; bj < B; ++bj) {
+    for (int jj = 0; jj < 16 && !bad; ++jj) {
+      const int j = 16 * bj + jj;
+      float* cj = col + (j & 1) * S;
+      if (tx == jj) {  // this thread column owns column j: publish rows j.. of it
+#pragma unroll
+        for (int a = 0; a < B; ++a)
+          if (ty + 16 * a >= j) cj[ty + 16 * a] = g[a][bj];
+      }
+      __syncthreads();  // column j visible; every read of column j - 2's buffer is done
+      const float d = cj[j];  // every thread reads the same pivot: the test is uniform
+      if (!(d > 0.0f)) {
+        bad = j + 1;
+        break;
+      }
+      if (threadIdx.x == 0) piv[j] = d;
+      const float inv = 1.0f / d;
+      float li[B], lk[B];
+#pragma unroll
+      for (int a = 0; a < B; ++a) li[a] = ty + 16 * a > j ? cj[ty + 16 * a] * inv : 0.0f;
+#pragma unroll
+      for (int b = 0; b < B; ++b) lk[b] = tx + 16 * b > j ? cj[tx + 16 * b] : 0.0f;
+#pragma unroll
+      for (int a = 0; a < B; ++a)
+#pragma unroll
+        for (int b = 0; b < B; ++b)
+          if (tx + 16 * b > j && tx + 16 * b <= ty + 16 * a) g[a][b] = fmaf(-li[a], lk[b], g[a][b]);
     }
-    const float inv = 1.0f / d;
-    // lower triangle of the trailing block: warp w takes rows j + 1 + w, j + 1 + w + 8, ...
-    for (int i = j + 1 + (threadIdx.x >> 5); i < S; i += blockDim.x >> 5) {
-      const float gij = G[i * ld + j] * inv;
-      for (int k = j + 1 + (threadIdx.x & 31); k <= i; k += 32) G[i * ld + k] -= gij * G[k * ld + j];
-    }
-    __syncthreads();
   }
   if (bad) {
     if (threadIdx.x == 0) atomicCAS(info, 0, 1000 * stage + bad);
     return;
   }
-  for (int e = threadIdx.x; e < S * S; e += blockDim.x) {
-    const int i = e / S, k = e % S;
-    if (k < i) G[i * ld + k] *= rsqrtf(G[k * ld + k]);
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < S; i += blockDim.x) G[i * ld + i] = sqrtf(G[i * ld + i]);
+  __syncthreads();  // every pivot written
+#pragma unroll
+  for (int a = 0; a < B; ++a)
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int i = ty + 16 * a, k = tx + 16 * b;
+      if (k < i) LS[k * ld + (i - k - 1)] = g[a][b] * rsqrtf(piv[k]);
+      else if (k == i) diag[k] = sqrtf(piv[k]);
+    }
   __syncthreads();
   if (threadIdx.x < S) {
     const int c = threadIdx.x;
-    float x[S];
+    float r[S];
 #pragma unroll
+    for (int t = 0; t < S; ++t) r[t] = t == c ? 1.0f : 0.0f;
     for (int i = 0; i < S; ++i) {
-      float acc = i == c ? 1.0f : 0.0f;
+      const float x = i < c ? 0.0f : r[0] / diag[i];
+      Mout[i * S + c] = x;
+      const float4* row = reinterpret_cast<const float4*>(LS + i * ld);
 #pragma unroll
-      for (int k = 0; k < i; ++k) acc = fmaf(-G[i * ld + k], x[k], acc);  // x_k = 0 for k < c
-      x[i] = i < c ? 0.0f : acc / G[i * ld + i];
+      for (int q = 0; q < S / 4; ++q) {
+        const float4 l = row[q];
+        r[4 * q] = fmaf(-l.x, x, r[4 * q + 1]);
+        r[4 * q + 1] = fmaf(-l.y, x, r[4 * q + 2]);
+        r[4 * q + 2] = fmaf(-l.z, x, r[4 * q + 3]);
+        if (4 * q + 4 < S) r[4 * q + 3] = fmaf(-l.w, x, r[4 * q + 4]);
+      }
     }
-#pragma unroll
-    for (int i = 0; i < S; ++i) Mout[i * S + c] = x[i];
   }
 }
 
 template <int S>
 static cudaError_t cholesky_launch(const float* G, float shift, float* M, int* info, int stage, cudaStream_t st) {
-  const int smem = S * (S + 1) * static_cast<int>(sizeof(float));
+  const int smem = chol_smem_floats<S>() * static_cast<int>(sizeof(float));
   static const cudaError_t attr =
       cudaFuncSetAttribute(rl_cholesky_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (attr != cudaSuccess) return attr;
