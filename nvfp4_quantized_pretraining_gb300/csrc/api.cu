@@ -114,10 +114,14 @@ static fp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64
     return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rows %lld too large (at most 65535 x 64)", (long long)rows);
   if (amax_opt && (reinterpret_cast<uintptr_t>(amax_opt) & 3u))
     return fail(FP4_ERR_MISALIGNED, "amax_opt must be 4-byte aligned");
-  if (out_row && scale_padded(rows, cols))
+  if (out_row && scale_padded(rows, cols)) {
     CUDA_TRY(cudaMemsetAsync(out_row->scales, 0, scale_bytes(rows, cols), s));
-  if (out_col && scale_padded(cols, rows))
+    pdl_chain_break();
+  }
+  if (out_col && scale_padded(cols, rows)) {
     CUDA_TRY(cudaMemsetAsync(out_col->scales, 0, scale_bytes(cols, rows), s));
+    pdl_chain_break();
+  }
   const float* amax = amax_opt;
   if (!amax) {
     float* slot = out_row ? &out_row->scale[1] : &out_col->scale[1];
@@ -363,6 +367,7 @@ extern "C" {
 int64_t fp4_scale_bytes(int64_t rows, int64_t cols) { return scale_bytes(rows, cols); }
 
 fp4_status fp4_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float* amax_out, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   fp4_status st = check_bf16_input(x, rows, cols, ld, "x");
   if (st) return st;
   if (cols % 8) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "amax needs cols %% 8 == 0");
@@ -373,6 +378,7 @@ fp4_status fp4_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float
 
 fp4_status fp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int round_mode, uint64_t seed,
                         uint32_t sr_stream, const float* amax_opt, fp4_tensor* out, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   if (!out) return fail(FP4_ERR_INVALID_ARG, "out is NULL");
   return quantize_impl(x, rows, cols, ld, round_mode, seed, sr_stream, 0, amax_opt, out, nullptr,
                        static_cast<cudaStream_t>(stream));
@@ -381,6 +387,7 @@ fp4_status fp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, i
 fp4_status fp4_quantize_transposed(const void* x, int64_t rows, int64_t cols, int64_t ld, int round_mode,
                                    uint64_t seed, uint32_t sr_stream, const float* amax_opt, fp4_tensor* out,
                                    void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   if (!out) return fail(FP4_ERR_INVALID_ARG, "out is NULL");
   return quantize_impl(x, rows, cols, ld, round_mode, seed, 0, sr_stream, amax_opt, nullptr, out,
                        static_cast<cudaStream_t>(stream));
@@ -389,12 +396,14 @@ fp4_status fp4_quantize_transposed(const void* x, int64_t rows, int64_t cols, in
 fp4_status fp4_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, int round_mode, uint64_t seed,
                              uint32_t sr_stream_row, uint32_t sr_stream_col, const float* amax_opt,
                              fp4_tensor* out_row, fp4_tensor* out_col, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   return quantize_impl(x, rows, cols, ld, round_mode, seed, sr_stream_row, sr_stream_col, amax_opt, out_row, out_col,
                        static_cast<cudaStream_t>(stream));
 }
 
 fp4_status fp4_gemm_blockscaled(const fp4_tensor* A, const fp4_tensor* B, const void* P, const void* Q, int r,
                                 float beta, void* C, int c_dtype, int64_t ldc, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   return gemm_impl(A, B, P, Q, r, beta, C, c_dtype, ldc, static_cast<cudaStream_t>(stream));
 }
 
@@ -407,6 +416,7 @@ size_t fp4_gemm_blockscaled_workspace(int64_t M, int r) {
 fp4_status fp4_gemm_blockscaled_ws(const fp4_tensor* A, const fp4_tensor* B, const void* P, const void* Q, int r,
                                    float beta, void* C, int c_dtype, int64_t ldc, void* ws, size_t ws_bytes,
                                    void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (!ws) return gemm_impl(A, B, P, Q, r, beta, C, c_dtype, ldc, s);
   fp4_status st;
@@ -430,6 +440,7 @@ fp4_status fp4_gemm_blockscaled_ws(const fp4_tensor* A, const fp4_tensor* B, con
 
 fp4_status fp4_branch_factor(const void* X, int64_t M, int64_t K, int64_t ldx, const void* L, int r, void* P,
                              float* amax_out, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   if (amax_out && (reinterpret_cast<uintptr_t>(amax_out) & 3u))
     return fail(FP4_ERR_MISALIGNED, "amax_out must be 4-byte aligned");
   return branch_impl(X, M, K, ldx, L, r, P, static_cast<cudaStream_t>(stream), amax_out);
@@ -446,6 +457,7 @@ size_t fp4_linear_bwd_workspace(int64_t M, int64_t N, int64_t K, int r) {
 fp4_status fp4_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx, const fp4_tensor* Wq, const void* L1,
                           const void* L2, int r, float beta, void* Y, int64_t ldy, fp4_tensor* xqT_saved, void* ws,
                           size_t ws_bytes, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   fp4_status st;
   if ((st = check_linear_fwd(X, M, K, ldx, Wq, L1, L2, r, xqT_saved))) return st;
   const size_t need = fp4_linear_fwd_workspace(M, Wq->rows, K, r);
@@ -458,6 +470,7 @@ fp4_status fp4_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx, cons
 fp4_status fp4_linear_fwd_noalloc(const void* X, int64_t M, int64_t K, int64_t ldx, const fp4_tensor* Wq,
                                   const void* L1, const void* L2, int r, float beta, void* Y, int64_t ldy,
                                   fp4_tensor* xqT_saved, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   fp4_status st;
   if ((st = check_linear_fwd(X, M, K, ldx, Wq, L1, L2, r, xqT_saved))) return st;
   const size_t need = fp4_linear_fwd_workspace(M, Wq->rows, K, r);
@@ -477,6 +490,7 @@ fp4_status fp4_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t lddy, co
                           const fp4_tensor* xqT_saved, const void* L1, const void* L2, int r, float beta,
                           uint64_t seed, void* dX, int64_t lddx, void* dW, int dw_dtype, int64_t lddw, void* ws,
                           size_t ws_bytes, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   fp4_status st;
   if ((st = check_bf16_input(dY, M, N, lddy, "dY"))) return st;
@@ -533,6 +547,7 @@ size_t fp4_lora_factor_grad_workspace(int64_t T, int64_t M, int r) {
 
 fp4_status fp4_lora_factor_grad(const void* A, int64_t T, int64_t M, int64_t lda, const void* B, int r, float beta,
                                 float* C, int64_t ldc, int transpose_c, void* ws, size_t ws_bytes, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   fp4_status st;
   if ((st = check_bf16_input(A, T, M, lda, "A"))) return st;
   if (!B || !C) return fail(FP4_ERR_INVALID_ARG, "B and C must be non-NULL");
@@ -560,6 +575,7 @@ size_t fp4_newton_schulz_workspace(int64_t m, int64_t n, float c) {
 fp4_status fp4_newton_schulz(const void* G, int64_t m, int64_t n, int64_t ldg, int normalize, int steps, float a,
                              float b, float c, int clip, void* X, int64_t ldx, void* ws, size_t ws_bytes,
                              void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   fp4_status st;
   if ((st = check_bf16_input(G, m, n, ldg, "G")) || (st = check_bf16_input(X, m, n, ldx, "X"))) return st;
@@ -588,7 +604,10 @@ fp4_status fp4_newton_schulz(const void* G, int64_t m, int64_t n, int64_t ldg, i
   const int64_t count = m * n;
   const uint32_t k = static_cast<uint32_t>((count * 99 + 99) / 100);
   uint32_t* hist = clip ? w.hist : nullptr;
-  if (clip && steps > 0) CUDA_TRY(cudaMemsetAsync(w.hist, 0, kNsHistBins * sizeof(uint32_t), s));
+  if (clip && steps > 0) {
+    CUDA_TRY(cudaMemsetAsync(w.hist, 0, kNsHistBins * sizeof(uint32_t), s));
+    pdl_chain_break();
+  }
   uint32_t* hist0 = steps > 0 ? hist : nullptr;
   if (normalize) {
     CUDA_TRY(launch_ns_normalize(G, m, n, ldg, X, ldx, w.partial, hist0, sms, s));
@@ -629,6 +648,7 @@ size_t fp4_lora_cholqr_workspace(int64_t K, int r) {
 
 fp4_status fp4_lora_cholqr(const void* L1, int64_t K, int64_t ld1, const void* L2, int64_t N, int r, void* L1_out,
                            void* L2_out, int* info, void* ws, size_t ws_bytes, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   fp4_status st;
   if (r != 16 && r != 32 && r != 48 && r != 64) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rank r=%d not in {16,32,48,64}", r);
   if ((st = check_bf16_input(L1, r, K, ld1, "L1")) || (st = check_bf16_input(L2, N, r, r, "L2"))) return st;
@@ -651,6 +671,7 @@ size_t fp4_lora_realign_workspace(int64_t N, int64_t K, int r, int s) {
 fp4_status fp4_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t ldw, const void* L1, const void* L2,
                             int r, float beta, const void* Omega, int s, int q, void* W_res_out, void* L1_out,
                             void* L2_out, int* info, void* ws, size_t ws_bytes, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   fp4_status st;
   if (r != 16 && r != 32 && r != 48 && r != 64) return fail(FP4_ERR_UNSUPPORTED_SHAPE, "rank r=%d not in {16,32,48,64}", r);
   if (s < r || s > 128 || s % 16 != 0)
@@ -688,6 +709,7 @@ static fp4_status check_f32_matrix(const float* p, int64_t rows, int64_t cols, i
 
 fp4_status fp4_qadamw_v_encode(const float* v, int64_t rows, int64_t cols, int64_t ldv, fp4_tensor* out,
                                uint16_t* mean, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   fp4_status st;
   if ((st = check_f32_matrix(v, rows, cols, ldv, "v")) || (st = check_tensor(out, "out"))) return st;
@@ -695,12 +717,16 @@ fp4_status fp4_qadamw_v_encode(const float* v, int64_t rows, int64_t cols, int64
     return fail(FP4_ERR_INVALID_ARG, "out is %lld x %lld, expected %lld x %lld", (long long)out->rows,
                 (long long)out->cols, (long long)rows, (long long)cols);
   if (!mean || (reinterpret_cast<uintptr_t>(mean) & 1u)) return fail(FP4_ERR_INVALID_ARG, "mean must be non-NULL and 2-byte aligned");
-  if (scale_padded(rows, cols)) CUDA_TRY(cudaMemsetAsync(out->scales, 0, scale_bytes(rows, cols), s));
+  if (scale_padded(rows, cols)) {
+    CUDA_TRY(cudaMemsetAsync(out->scales, 0, scale_bytes(rows, cols), s));
+    pdl_chain_break();
+  }
   CUDA_TRY(launch_vt_encode(v, rows, cols, ldv, qout(out), mean, sm_count(), s));
   return FP4_OK;
 }
 
 fp4_status fp4_qadamw_v_decode(const fp4_tensor* in, const uint16_t* mean, float* v_out, int64_t ldo, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   fp4_status st;
   if ((st = check_tensor(in, "in"))) return st;
   if ((st = check_f32_matrix(v_out, in->rows, in->cols, ldo, "v_out"))) return st;
@@ -711,6 +737,7 @@ fp4_status fp4_qadamw_v_decode(const fp4_tensor* in, const uint16_t* mean, float
 }
 
 fp4_status fp4_debug_convert(const float* in, int64_t n, uint8_t* e2m1_out, uint8_t* e4m3_out, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   if (!in || !e2m1_out || !e4m3_out || n <= 0) return fail(FP4_ERR_INVALID_ARG, "bad debug_convert arguments");
   CUDA_TRY(launch_debug_convert(in, n, e2m1_out, e4m3_out, static_cast<cudaStream_t>(stream)));
   return FP4_OK;
@@ -719,6 +746,7 @@ fp4_status fp4_debug_convert(const float* in, int64_t n, uint8_t* e2m1_out, uint
 void fp4_debug_force_counter64(int on) { set_force_counter64(on != 0); }
 
 fp4_status fp4_debug_sr_round(const float* in, const uint16_t* rnd16, int64_t n, uint8_t* e2m1_out, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   if (!in || !rnd16 || !e2m1_out || n <= 0 || n > (int64_t(1) << 34))
     return fail(FP4_ERR_INVALID_ARG, "bad debug_sr_round arguments");
   CUDA_TRY(launch_debug_sr_round(in, rnd16, n, e2m1_out, static_cast<cudaStream_t>(stream)));
@@ -726,6 +754,7 @@ fp4_status fp4_debug_sr_round(const float* in, const uint16_t* rnd16, int64_t n,
 }
 
 fp4_status fp4_mma_peak_probe(int n, int iters, int* num_sms_out, void* stream) {
+  pdl_chain_break();  // the call's first kernel is ordered after all earlier stream work
   if ((n != 128 && n != 256) || iters <= 0) return fail(FP4_ERR_INVALID_ARG, "probe needs n in {128, 256}, iters > 0");
   const int sms = sm_count();
   if (num_sms_out) *num_sms_out = sms;

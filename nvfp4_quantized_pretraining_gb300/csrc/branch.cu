@@ -64,8 +64,8 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 template <bool SPLIT>
 __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
     branch_factor_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_l,
-                         uint32_t M, uint32_t K, uint32_t h, int r, __nv_bfloat16* __restrict__ P,
-                         unsigned int* __restrict__ amax_out) {
+                         uint32_t M, uint32_t K, uint32_t h, int r, __nv_bfloat16* P,
+                         unsigned int* amax_out) {
   using namespace bf;
   pdl_trigger();
   constexpr int NST = SPLIT ? SPLIT_STAGES : STAGES;
@@ -284,8 +284,8 @@ __global__ void __launch_bounds__(bf::NUM_THREADS, 1)
 // ---------------------------------------------------------------------------
 // BF16 transpose (small factor matrices)
 // ---------------------------------------------------------------------------
-__global__ void transpose_bf16_kernel(const uint16_t* __restrict__ in, uint32_t rows, uint32_t cols,
-                                      uint16_t* __restrict__ out) {
+__global__ void transpose_bf16_kernel(const uint16_t* in, uint32_t rows, uint32_t cols,
+                                      uint16_t* out) {
   pdl_trigger();
   pdl_wait();
   __shared__ uint16_t t[32][33];
@@ -332,6 +332,7 @@ cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ld
     return cudaErrorInvalidValue;
   if (amax_out) {
     const cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), s);
+    pdl_chain_break();
     if (e != cudaSuccess) return e;
   }
   __nv_bfloat16* Pb = static_cast<__nv_bfloat16*>(P);
@@ -352,9 +353,10 @@ cudaError_t launch_branch_factor(const void* X, int64_t M, int64_t K, int64_t ld
     at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = g_pdl_chain ? 2 : 1;  // programmatic launch only after one of the library's kernels
     e = cudaLaunchKernelEx(&cfg, branch_factor_kernel<true>, tx, tl, (uint32_t)M, (uint32_t)K, (uint32_t)BM, r, Pb,
                            am);
+    g_pdl_chain = e == cudaSuccess;
   } else {
     const unsigned grid = (unsigned)((M + h - 1) / h);
     e = launch_pdl(branch_factor_kernel<false>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, tx, tl, (uint32_t)M,

@@ -38,7 +38,9 @@ __device__ __forceinline__ void drain_pause() {
 // pdl_wait() blocks until that kernel has completed and its memory operations are visible (a
 // no-op for a kernel launched normally), so nothing produced or read by it may be touched before.
 // pdl_trigger() lets the next such kernel start launching once every CTA of this grid has called
-// it or exited.
+// it or exited.  The wait orders memory accesses only through pointers the compiler cannot assume
+// private: a kernel that calls it takes no __restrict__ pointer, whose loads the compiler may move
+// above the wait (it may assume nothing else, the wait included, changes the data behind one).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -954,9 +954,9 @@ __global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(const GemmParam
 
 // The branch fold on its own (the scale warps' in-kernel form, run before the GEMM):
 // Pt = bf16(fl32(P * g)), g = fl32(beta / alpha), alpha = fl32(S_tA * S_tB) (1 when 0).
-__global__ void __launch_bounds__(256) fold_branch_kernel(const uint32_t* __restrict__ P, uint32_t nwords,
+__global__ void __launch_bounds__(256) fold_branch_kernel(const uint32_t* P, uint32_t nwords,
                                                           const float* a_scale, const float* b_scale, float beta,
-                                                          uint32_t* __restrict__ Pt) {
+                                                          uint32_t* Pt) {
   pdl_trigger();
   pdl_wait();
   float alpha = __fmul_rn(*a_scale, *b_scale);

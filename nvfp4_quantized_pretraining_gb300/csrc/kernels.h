@@ -24,8 +24,19 @@ struct QOut {
 
 void count_launch();
 
-// Launches `kernel` with programmatic stream serialization: its CTAs may be scheduled while the
-// previous kernel in the stream drains (they wait in pdl_wait() before touching its data).
+// Programmatic dependent launch is safe only from one of this library's kernels to the next: a
+// kernel launched with it may start as soon as the previous kernel in the stream lets it, and its
+// griddepcontrol.wait waits for prerequisite kernels only, so a copy, memset or event wait queued
+// between the two would not be ordered before it.  g_pdl_chain is true while the last operation
+// this thread queued was one of the library's kernels; every C-ABI call clears it on entry, and so
+// does every memset the library queues, so the first kernel after either is launched normally
+// (ordered after everything before it in the stream).
+inline thread_local bool g_pdl_chain = false;
+inline void pdl_chain_break() { g_pdl_chain = false; }
+
+// Launches `kernel` with programmatic stream serialization when the previous operation in the stream
+// is one of this library's kernels (its CTAs may then be scheduled while that kernel drains, and
+// they wait in pdl_wait() before touching its data), else with a normal launch.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                        Args&&... args) {
@@ -38,8 +49,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  cfg.numAttrs = g_pdl_chain ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  g_pdl_chain = e == cudaSuccess;
+  return e;
 }
 
 cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float* out, int num_sms,

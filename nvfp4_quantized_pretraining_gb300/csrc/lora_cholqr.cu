@@ -27,8 +27,8 @@ constexpr int kCqrThreads = 256;
 // r x r partial Gram matrix of the 128-column chunks blockIdx.x, blockIdx.x + gridDim.x, ...
 // Thread t owns row i = t / 4 and columns j = t % 4 + 4 u (u < r / 4) of the partial.
 template <int R>
-__global__ void __launch_bounds__(kCqrThreads) cholqr_gram_kernel(const uint16_t* __restrict__ L1, int64_t K,
-                                                                  int64_t ld, float* __restrict__ partial) {
+__global__ void __launch_bounds__(kCqrThreads) cholqr_gram_kernel(const uint16_t* L1, int64_t K,
+                                                                  int64_t ld, float* partial) {
   pdl_trigger();
   pdl_wait();
   __shared__ float tile[R][kCqrChunk + 1];
@@ -61,75 +61,91 @@ __global__ void __launch_bounds__(kCqrThreads) cholqr_gram_kernel(const uint16_t
   }
 }
 
-// One CTA: G = sum of the partials (fixed order), G = L L^T.  Writes L (lower,
-// zeros above) and the reciprocals of its diagonal.  Per column j two phases: the
-// column below the pivot is divided by it; then the trailing lower triangle is
-// updated by 32 x 32 threads (row j + 1 + a, column j + 1 + b, b <= a, strided by
-// 32), and the thread that updates the next diagonal element takes its square root
-// (or reports it non-positive) at once, so one barrier closes both.
+// One CTA of 256 threads: G = sum of the partials (fixed order), G = L L^T (right-looking).  The
+// threads hold G as a 16 x 16 grid of (R/16) x (R/16) register blocks (thread (ty, tx) has rows
+// ty + 16a and columns tx + 16b).  Step j: the owners of column j publish it in shared memory,
+// one barrier, then every thread reads the pivot d_j, scales the column, l_i = G_ij / sqrt(d_j),
+// and updates its own trailing elements, G_ik -= l_i l_k (k <= i).  A non-positive pivot is seen
+// by every thread at once.  Writes L (lower, zeros above) and the reciprocals of its diagonal.
 template <int R>
-__global__ void __launch_bounds__(1024) cholqr_factor_kernel(const float* __restrict__ partial, int nparts,
-                                                             float* __restrict__ Lout, float* __restrict__ inv_diag,
-                                                             int* __restrict__ info) {
-  __shared__ float G[R][R + 1];
-  __shared__ int bad;
+__global__ void __launch_bounds__(kCqrThreads) cholqr_factor_kernel(const float* partial, int nparts,
+                                                                    float* Lout, float* inv_diag,
+                                                                    int* info) {
+  constexpr int B = R / 16;
+  __shared__ float col[2][R];
+  __shared__ float piv[R];
   pdl_trigger();
   pdl_wait();
-  for (int e = threadIdx.x; e < R * R; e += blockDim.x) {
-    float v[kCqrMaxParts];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float g[B][B];
 #pragma unroll
-    for (int p = 0; p < kCqrMaxParts; ++p) v[p] = p < nparts ? partial[p * R * R + e] : 0.0f;
-    float s = 0.0f;
+  for (int a = 0; a < B; ++a)
 #pragma unroll
-    for (int p = 0; p < kCqrMaxParts; ++p) s += v[p];
-    G[e / R][e % R] = s;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const float d = G[0][0];
-    bad = d > 0.0f ? 0 : 1;
-    if (d > 0.0f) G[0][0] = sqrtf(d);
-  }
-  __syncthreads();
-  // right-looking factorisation in place (lower triangle of G becomes L)
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  for (int j = 0; j < R; ++j) {
-    if (bad) break;  // uniform: read after the barrier that closed the previous column
-    const float djj = G[j][j];
-    for (int i = j + 1 + threadIdx.x; i < R; i += blockDim.x) G[i][j] = G[i][j] / djj;
-    __syncthreads();
-    for (int a = ty; j + 1 + a < R; a += 32) {
-      const int i = j + 1 + a;
-      for (int b = tx; b <= a; b += 32) {
-        const int k = j + 1 + b;
-        G[i][k] -= G[i][j] * G[k][j];
-        if (a == 0) {  // (then b == 0: the next pivot, now final)
-          const float d = G[i][i];
-          if (!(d > 0.0f)) bad = j + 2;
-          else G[i][i] = sqrtf(d);
-        }
-      }
+    for (int b = 0; b < B; ++b) {
+      const int e = (ty + 16 * a) * R + tx + 16 * b;
+      float v[kCqrMaxParts];
+#pragma unroll
+      for (int p = 0; p < kCqrMaxParts; ++p) v[p] = p < nparts ? partial[p * R * R + e] : 0.0f;
+      float s = 0.0f;
+#pragma unroll
+      for (int p = 0; p < kCqrMaxParts; ++p) s += v[p];
+      g[a][b] = s;
     }
-    __syncthreads();
+  int bad = 0;
+#pragma unroll
+  for (int bj = 0; bj < B; ++bj) {
+    for (int jj = 0; jj < 16 && !bad; ++jj) {
+      const int j = 16 * bj + jj;
+      float* cj = col[j & 1];
+      if (tx == jj) {  // the owners of column j publish rows j.. of it
+#pragma unroll
+        for (int a = 0; a < B; ++a)
+          if (ty + 16 * a >= j) cj[ty + 16 * a] = g[a][bj];
+      }
+      __syncthreads();  // column j visible; every read of column j - 2's buffer is done
+      const float d = cj[j];  // the same pivot for every thread: the test is uniform
+      if (!(d > 0.0f)) {
+        bad = j + 1;
+        break;
+      }
+      if (threadIdx.x == 0) piv[j] = d;
+      const float djj = sqrtf(d);
+      float li[B], lk[B];
+#pragma unroll
+      for (int a = 0; a < B; ++a) li[a] = ty + 16 * a > j ? cj[ty + 16 * a] / djj : 0.0f;
+#pragma unroll
+      for (int b = 0; b < B; ++b) lk[b] = tx + 16 * b > j ? cj[tx + 16 * b] / djj : 0.0f;
+#pragma unroll
+      for (int a = 0; a < B; ++a)
+#pragma unroll
+        for (int b = 0; b < B; ++b)
+          if (tx + 16 * b > j && tx + 16 * b <= ty + 16 * a) g[a][b] = fmaf(-li[a], lk[b], g[a][b]);
+    }
   }
   if (threadIdx.x == 0) *info = bad;
-  if (bad) return;  // uniform: every thread read `bad` after the same barrier
-  for (int e = threadIdx.x; e < R * R; e += blockDim.x) {
-    const int i = e / R, k = e % R;
-    Lout[e] = k <= i ? G[i][k] : 0.0f;
-  }
-  if (threadIdx.x < R) inv_diag[threadIdx.x] = 1.0f / G[threadIdx.x][threadIdx.x];
+  if (bad) return;  // uniform
+  __syncthreads();  // every pivot written
+#pragma unroll
+  for (int a = 0; a < B; ++a)
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int i = ty + 16 * a, k = tx + 16 * b;
+      Lout[i * R + k] = k < i ? g[a][b] / sqrtf(piv[k]) : k == i ? sqrtf(piv[k]) : 0.0f;
+    }
+  if (threadIdx.x < R) inv_diag[threadIdx.x] = 1.0f / sqrtf(piv[threadIdx.x]);
 }
 
 
-// Blocks [0, ncolblocks): columns of L1 (L1' = L^-1 L1 by forward substitution);
-// the rest: rows of L2 (L2' = L2 L).
+// Blocks [0, ncolblocks): columns of L1 (L1' = L^-1 L1 by forward substitution, right-looking:
+// once x_i is known every later row takes its term, in the same order per row as the
+// left-looking sum but with the multiply-adds of a step independent of each other); the rest:
+// rows of L2 (L2' = L2 L, accumulated row of L by row of L, each output's terms in increasing i).
 template <int R>
 __global__ void __launch_bounds__(kCqrThreads) cholqr_apply_kernel(
     const uint16_t* L1, int64_t K, int64_t ld1, uint16_t* L1_out, const uint16_t* L2, int64_t N, uint16_t* L2_out,
-    const float* __restrict__ Lmat, const float* __restrict__ inv_diag, const int* __restrict__ info,
+    const float* Lmat, const float* inv_diag, const int* info,
     int ncolblocks) {
-  __shared__ float M[R][R + 1];
+  __shared__ __align__(16) float M[R][R + 4];
   __shared__ float dinv[R];
   pdl_trigger();
   pdl_wait();
@@ -146,11 +162,10 @@ __global__ void __launch_bounds__(kCqrThreads) cholqr_apply_kernel(
     // x <- L^-1 x in place: x_i = (x_i - sum_{c < i} L_ic x_c) / L_ii
 #pragma unroll
     for (int i = 0; i < R; ++i) {
-      float s = x[i];
-#pragma unroll
-      for (int c = 0; c < i; ++c) s = fmaf(-M[i][c], x[c], s);
-      x[i] = s * dinv[i];
+      x[i] = x[i] * dinv[i];
       L1_out[i * ld1 + k] = static_cast<uint16_t>(bf16_rn_bits(x[i]));
+#pragma unroll
+      for (int t = i + 1; t < R; ++t) x[t] = fmaf(-M[t][i], x[i], x[t]);
     }
   } else {
     const int64_t n = static_cast<int64_t>(blockIdx.x - ncolblocks) * kCqrThreads + threadIdx.x;
@@ -167,23 +182,21 @@ __global__ void __launch_bounds__(kCqrThreads) cholqr_apply_kernel(
         x[8 * q + 2 * h + 1] = __uint_as_float(ws[h] & 0xFFFF0000u);
       }
     }
+    // y_j = sum_{i >= j} x_i L_ij, the terms added in increasing i
+    float y[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) y[j] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+#pragma unroll
+      for (int j = 0; j <= i; ++j) y[j] = fmaf(x[i], M[i][j], y[j]);
+    }
     uint4* out = reinterpret_cast<uint4*>(L2_out + n * R);
 #pragma unroll
     for (int q = 0; q < R / 8; ++q) {
       uint32_t packed[4];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        float y[2];
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int j = 8 * q + 2 * h + t;
-          float s = 0.0f;
-#pragma unroll
-          for (int i = j; i < R; ++i) s = fmaf(x[i], M[i][j], s);
-          y[t] = s;
-        }
-        packed[h] = bf16_rn_bits(y[0]) | (bf16_rn_bits(y[1]) << 16);
-      }
+      for (int h = 0; h < 4; ++h) packed[h] = bf16_rn_bits(y[8 * q + 2 * h]) | (bf16_rn_bits(y[8 * q + 2 * h + 1]) << 16);
       out[q] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
   }
@@ -207,8 +220,8 @@ static cudaError_t cholqr_launch(const void* L1, int64_t K, int64_t ld1, const v
                              static_cast<const uint16_t*>(L1), K, ld1, partial);
   count_launch();
   if (e != cudaSuccess) return e;
-  e = launch_pdl(cholqr_factor_kernel<R>, dim3(1), dim3(1024), 0, s, static_cast<const float*>(partial), parts, Lmat,
-                 inv_diag, info);
+  e = launch_pdl(cholqr_factor_kernel<R>, dim3(1), dim3(kCqrThreads), 0, s, static_cast<const float*>(partial), parts,
+                 Lmat, inv_diag, info);
   count_launch();
   if (e != cudaSuccess) return e;
   const int colblocks = static_cast<int>((K + kCqrThreads - 1) / kCqrThreads);

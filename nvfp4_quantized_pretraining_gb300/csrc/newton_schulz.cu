@@ -370,6 +370,7 @@ cudaError_t launch_ns_lincomb(const void* x, int64_t ldx, float p, const void* y
   unsigned int* am = reinterpret_cast<unsigned int*>(amax_out);
   if (amax_out) {
     cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), s);
+    pdl_chain_break();
     if (e != cudaSuccess) return e;
   }
   const int g4 = ns_grid(nchunks, num_sms, 4), g1 = num_sms;  // the histogram kernels: one CTA per SM

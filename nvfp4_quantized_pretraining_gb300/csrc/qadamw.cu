@@ -235,6 +235,7 @@ cudaError_t launch_vt_encode(const float* v, int64_t rows, int64_t cols, int64_t
   const uint32_t atoms_k = (kbpr + 3) / 4;
   float* amax = &out.scale[1];
   cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), s);
+  pdl_chain_break();
   if (e != cudaSuccess) return e;
   const int grid = vt_grid(nblocks, num_sms);
   vt_amax_kernel<<<grid, kVtThreads, 0, s>>>(v, ldv, kbpr, nblocks, reinterpret_cast<unsigned int*>(amax));

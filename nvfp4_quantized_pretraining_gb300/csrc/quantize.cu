@@ -26,8 +26,8 @@ namespace nvfp4 {
 // BF16 bit patterns with the sign cleared, so the reduction is integer
 // (two elements per 32-bit word with __vmaxu2).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ x, uint32_t cpr, uint32_t nchunks,
-                                                   int64_t ld, unsigned int* __restrict__ out) {
+__global__ void __launch_bounds__(256) amax_kernel(const uint16_t* x, uint32_t cpr, uint32_t nchunks,
+                                                   int64_t ld, unsigned int* out) {
   pdl_trigger();
   pdl_wait();
   uint32_t m = 0;
@@ -410,6 +410,7 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, f
   const uint32_t cpr = static_cast<uint32_t>(cols / 8);
   const uint32_t nchunks = static_cast<uint32_t>(rows) * cpr;
   cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), s);
+  pdl_chain_break();
   if (e != cudaSuccess) return e;
   const int grid = grid_for(nchunks, 256 * 4, num_sms * 8);
   e = launch_pdl(amax_kernel, dim3(grid), dim3(256), 0, s, static_cast<const uint16_t*>(x), cpr, nchunks, ld,

@@ -960,6 +960,7 @@ cudaError_t launch_lora_realign(const void* W_res, int64_t N, int64_t K, int64_t
   float* Bs = aligned(Wt + N * K);             // 2 sc x max(N, K)
 
   if ((e = cudaMemsetAsync(info, 0, sizeof(int), st)) != cudaSuccess) return e;
+  pdl_chain_break();
   Rl rl{st, num_sms, split};
   // W = W_res + beta L2 L1 (FP32)
   rl.to_f32(W_res, ldw, W, K, N, K);

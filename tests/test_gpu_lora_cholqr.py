@@ -110,3 +110,22 @@ def test_lora_cholqr_reports_a_singular_gram_and_writes_nothing(F, oracle_mod):
     torch.cuda.synchronize()
     assert int(info.item()) == 6 == oracle_mod.lora_cholqr(L1, L2)[2]
     assert bool((out1 == 7.0).all()) and bool((out2 == 7.0).all())
+
+
+@pytest.mark.gpu
+def test_lora_cholqr_waits_for_a_copy_queued_after_the_previous_call(F, oracle_mod):
+    # Calls queued back to back with a copy between them: the second call's first kernel must be
+    # ordered after the copy (which is not a kernel), not only after the first call's kernels.
+    r, K, N = 16, 256, 128
+    L1, L2 = factors(oracle_mod, r, K, N, "svd", r + K)
+    L1d, L2d = S.bits_to_torch(L1, DEV), S.bits_to_torch(L2, DEV)
+    a, b, _ = F.fp4_lora_cholqr(L1d, L2d)
+    torch.cuda.synchronize()
+    for _ in range(4):
+        F.fp4_lora_cholqr(L1d, L2d)
+        F.fp4_lora_cholqr(L1d, L2d)
+        L1i, L2i = L1d.clone(), L2d.clone()
+        _, _, info = F.fp4_lora_cholqr(L1i, L2i, L1_out=L1i, L2_out=L2i)
+        torch.cuda.synchronize()
+        assert int(info.item()) == 0
+        assert torch.equal(L1i, a) and torch.equal(L2i, b)

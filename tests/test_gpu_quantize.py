@@ -242,3 +242,22 @@ def test_transposed_rejects_partial_row_blocks(F):
     with pytest.raises(F.FP4Error) as e:
         F.fp4_quantize_transposed(dev(x))
     assert e.value.status == F.FP4_ERR_UNSUPPORTED_SHAPE
+
+
+@pytest.mark.gpu
+def test_quantize_waits_for_a_copy_queued_after_the_previous_call(F, oracle_mod):
+    # A quantization queued right behind another call and a device copy into its input: the copy
+    # (not a kernel) must land before the quantizer reads the tensor.
+    big = S.bits_to_torch(S.normal((8192, 4096), 1.0, 90), DEV)
+    src = S.bits_to_torch(S.normal((256, 4096), 1.0, 91), DEV)
+    want = F.fp4_quantize(src)
+    torch.cuda.synchronize()
+    want_codes, want_scales = want.codes.clone(), want.scales.clone()
+    for i in range(4):
+        x = torch.full_like(src, float(i + 3))
+        torch.cuda.synchronize()
+        F.fp4_quantize_dual(big)
+        x.copy_(src)
+        got = F.fp4_quantize(x)
+        torch.cuda.synchronize()
+        assert torch.equal(got.codes, want_codes) and torch.equal(got.scales, want_scales)
