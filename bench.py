@@ -57,7 +57,7 @@ WORKLOADS = {
 GEMM_TRAFFIC = {
     # launch list of `--part step --steps 2 --warmup 3` with dram__bytes_read.sum and
     # dram__bytes_write.sum (one pass): mean over the 96 GEMM launches of the 3B block
-    "f84333df2c748224": 214700000,
+    "537b552b4b8b0248": 215260000,
 }
 
 

@@ -23,6 +23,9 @@
  *     pointer live in HOST memory and are read during the call only.
  *   - Every call is asynchronous on the caller's stream (cudaStream_t passed as
  *     void*; NULL = legacy default stream) and returns an fp4_status at once.
+ *     Its work is ordered after everything queued earlier on that stream
+ *     (kernels, copies, memsets, event waits): only the kernels inside one call
+ *     overlap one another (programmatic dependent launch).
  *     Argument errors are detected on the host before anything is launched.
  *   - Device-side timeouts (a bounded wait that expired) are recorded in a
  *     device status word; fp4_check_status() synchronises the stream and reads
