@@ -24,13 +24,13 @@ struct QOut {
 
 void count_launch();
 
-// Programmatic dependent launch is safe only from one of this library's kernels to the next: a
+// Programmatic dependent launch is used only from one of this library's kernels to the next: a
 // kernel launched with it may start as soon as the previous kernel in the stream lets it, and its
-// griddepcontrol.wait waits for prerequisite kernels only, so a copy, memset or event wait queued
-// between the two would not be ordered before it.  g_pdl_chain is true while the last operation
-// this thread queued was one of the library's kernels; every C-ABI call clears it on entry, and so
-// does every memset the library queues, so the first kernel after either is launched normally
-// (ordered after everything before it in the stream).
+// griddepcontrol.wait is defined to wait for prerequisite kernels, so the library does not rely on
+// it to order a copy, memset or event wait queued between the two.  g_pdl_chain is true while the
+// last operation this thread queued was one of the library's kernels; every C-ABI call clears it on
+// entry, and so does every memset the library queues, so the first kernel after either is launched
+// normally (ordered after everything before it in the stream).
 inline thread_local bool g_pdl_chain = false;
 inline void pdl_chain_break() { g_pdl_chain = false; }
 
