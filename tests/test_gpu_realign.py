@@ -85,6 +85,8 @@ def inputs(oracle_mod, N, K, r, s, kind, seed):
 @pytest.mark.parametrize("N,K,r,s,q,beta", [
     (384, 512, 16, 32, 2, 1.0), (1024, 768, 32, 48, 2, 0.5), (640, 1280, 48, 64, 1, 1.0), (768, 512, 64, 128, 3, 2.0),
     (648, 392, 32, 48, 2, 1.0),  # ragged 128-row tiles and 32-wide K stages in the tensor-core products
+    (512, 256, 16, 16, 2, 1.0),  # sketch width 16: the narrowest tensor-core product (N = 16)
+    (514, 384, 16, 32, 2, 1.0),  # N not a multiple of 4: the W^T products fall back to the FP32 GEMM
 ])
 def test_realign_gapped_matches_oracle(F, oracle_mod, N, K, r, s, q, beta):
     W_res, L1, L2, Om = inputs(oracle_mod, N, K, r, s, "gapped", N + K + r)
