@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kCqrThreads) cholqr_gram_kernel(const uint16_t
 // One CTA of 256 threads: G = sum of the partials (fixed order), G = L L^T (right-looking).  The
 // threads hold G as a 16 x 16 grid of (R/16) x (R/16) register blocks (thread (ty, tx) has rows
 // ty + 16a and columns tx + 16b).  Step j: the owners of column j publish it in shared memory,
-// one barrier, then every thread reads the pivot d_j, scales the column, l_i = G_ij / sqrt(d_j),
+// one barrier, then every thread reads the pivot d_j, scales the column, l_i = G_ij (1 / sqrt(d_j)),
 // and updates its own trailing elements, G_ik -= l_i l_k (k <= i).  A non-positive pivot is seen
 // by every thread at once.  Writes L (lower, zeros above) and the reciprocals of its diagonal.
 template <int R>
@@ -109,12 +109,12 @@ __global__ void __launch_bounds__(kCqrThreads) cholqr_factor_kernel(const float*
         break;
       }
       if (threadIdx.x == 0) piv[j] = d;
-      const float djj = sqrtf(d);
+      const float rdjj = 1.0f / sqrtf(d);  // one reciprocal per column; the column is scaled by it
       float li[B], lk[B];
 #pragma unroll
-      for (int a = 0; a < B; ++a) li[a] = ty + 16 * a > j ? cj[ty + 16 * a] / djj : 0.0f;
+      for (int a = 0; a < B; ++a) li[a] = ty + 16 * a > j ? cj[ty + 16 * a] * rdjj : 0.0f;
 #pragma unroll
-      for (int b = 0; b < B; ++b) lk[b] = tx + 16 * b > j ? cj[tx + 16 * b] / djj : 0.0f;
+      for (int b = 0; b < B; ++b) lk[b] = tx + 16 * b > j ? cj[tx + 16 * b] * rdjj : 0.0f;
 #pragma unroll
       for (int a = 0; a < B; ++a)
 #pragma unroll
@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kCqrThreads) cholqr_factor_kernel(const float*
 #pragma unroll
     for (int b = 0; b < B; ++b) {
       const int i = ty + 16 * a, k = tx + 16 * b;
-      Lout[i * R + k] = k < i ? g[a][b] / sqrtf(piv[k]) : k == i ? sqrtf(piv[k]) : 0.0f;
+      Lout[i * R + k] = k < i ? g[a][b] * (1.0f / sqrtf(piv[k])) : k == i ? sqrtf(piv[k]) : 0.0f;
     }
   if (threadIdx.x < R) inv_diag[threadIdx.x] = 1.0f / sqrtf(piv[threadIdx.x]);
 }
