@@ -557,7 +557,9 @@ static cudaError_t launch_cholesky(int s, const float* G, float shift, float* M,
 // Schur rotation), each round rotating s / 2 disjoint pairs chosen by the
 // round-robin schedule (pair 0 is (s - 1, r), pair k is ((r + k) mod (s - 1),
 // (r - k) mod (s - 1))).  A round is two phases: the rotations, then A <- J^T A J
-// as disjoint 2 x 2 blocks (rows of pair k, columns of pair l) and V <- V J.  A
+// as disjoint 2 x 2 blocks (rows of pair k, columns of pair l; only blocks with
+// k <= l are computed, each writing its mirror too, so A stays exactly symmetric)
+// and V <- V J; a round in which no pair rotates skips its update.  A
 // pair is rotated when |a_pq| > 1e-6 ||A||_F (the Frobenius norm is invariant
 // under the rotations; FP32 rounding leaves off-diagonal noise near 6e-8 ||A||,
 // so a threshold relative to the diagonal would never be met); a sweep that
@@ -573,9 +575,8 @@ __global__ void __launch_bounds__(kRlJacThreads) rl_jacobi_kernel(const float* _
   extern __shared__ float sh[];
   const int ld = s + 1;
   float* A = sh;              // s x ld
-  float* V = sh + s * ld;     // s x ld (2 s ld floats: a multiple of 8 bytes)
-  float2* CSN = reinterpret_cast<float2*>(V + s * ld);  // s / 2 (cosine, sine) pairs
-  int2* PQ = reinterpret_cast<int2*>(CSN + s / 2);      // s / 2 (head, tail) pairs
+  float* V = sh + s * ld;     // s x ld (2 s ld floats: a multiple of 16 bytes for even s)
+  float4* ROT = reinterpret_cast<float4*>(V + s * ld);  // s / 2 pairs: (head, tail) as int bits, (cos, sin)
   __shared__ int rotated;
   __shared__ int round_rotated[2];  // round t's flag in [t & 1]
   __shared__ float red[kRlJacThreads / 32];
@@ -596,17 +597,23 @@ __global__ void __launch_bounds__(kRlJacThreads) rl_jacobi_kernel(const float* _
   for (int w = 0; w < kRlJacThreads / 32; ++w) fro2 += red[w];
   const float thresh = 1e-6f * sqrtf(fro2);
   const int half = s / 2;
-  // This thread's share of each round's update, the same in every round: 2 x 2 blocks (k, l) of A
-  // and entries (pair l, row i) of V, packed as k | l << 8 and l | i << 8 (s <= 128), computed once
-  // here rather than by a division per item and round.
-  constexpr int kItA = (kRlMaxS / 2) * (kRlMaxS / 2) / kRlJacThreads;
+  // This thread's share of each round's update, the same in every round: 2 x 2 blocks (k, l), k <= l,
+  // of A (A stays exactly symmetric: block (k, l) also writes its mirror, block (l, k)) and entries
+  // (pair l, row i) of V, packed as k | l << 8 and l | i << 8 (s <= 128), computed once here rather
+  // than by a division per item and round.
+  constexpr int kItA = ((kRlMaxS / 2) * (kRlMaxS / 2 + 1) / 2 + kRlJacThreads - 1) / kRlJacThreads;
   constexpr int kItV = (kRlMaxS / 2) * kRlMaxS / kRlJacThreads;
   constexpr uint32_t kNone = 0xFFFFFFFFu;
   uint32_t it_a[kItA], it_v[kItV];
 #pragma unroll
   for (int j = 0; j < kItA; ++j) {
-    const int e = threadIdx.x + j * kRlJacThreads;
-    it_a[j] = e < half * half ? (uint32_t)(e / half) | ((uint32_t)(e % half) << 8) : kNone;
+    int e = threadIdx.x + j * kRlJacThreads;
+    it_a[j] = kNone;
+    if (e < half * (half + 1) / 2) {  // row k of the upper triangle holds half - k blocks
+      int k = 0;
+      while (e >= half - k) e -= half - k, ++k;
+      it_a[j] = (uint32_t)k | ((uint32_t)(k + e) << 8);
+    }
   }
 #pragma unroll
   for (int j = 0; j < kItV; ++j) {
@@ -632,8 +639,7 @@ __global__ void __launch_bounds__(kRlJacThreads) rl_jacobi_kernel(const float* _
           round_rotated[round & 1] = 1;
           rotated = 1;
         }
-        PQ[k] = make_int2(p, q);
-        CSN[k] = make_float2(c, t * c);
+        ROT[k] = make_float4(__int_as_float(p), __int_as_float(q), c, t * c);
       }
       // the next round's flag: every read of it (last round) came before this round's first barrier
       if (threadIdx.x == 0) round_rotated[(round + 1) & 1] = 0;
@@ -641,31 +647,43 @@ __global__ void __launch_bounds__(kRlJacThreads) rl_jacobi_kernel(const float* _
       // a round without a rotation changes nothing: no update, and no second barrier (its pairs and
       // rotations are not read, and A is not written)
       if (!round_rotated[round & 1]) continue;
-      // A <- J^T A J as 2 x 2 blocks; V <- V J
+      // A <- J^T A J as 2 x 2 blocks (k <= l, each written with its mirror); V <- V J
 #pragma unroll
       for (int j = 0; j < kItA; ++j) {
         if (it_a[j] == kNone) continue;
         const int k = it_a[j] & 0xFFu, l = it_a[j] >> 8;
-        const int2 qk2 = PQ[k], ql2 = PQ[l];
-        const float2 rk = CSN[k], rl = CSN[l];
-        const int pk = qk2.x, qk = qk2.y, pl = ql2.x, ql = ql2.y;
-        const float ck = rk.x, sk = rk.y, cl = rl.x, sl = rl.y;
+        const float4 rk = ROT[k], rl = ROT[l];
+        const int pk = __float_as_int(rk.x), qk = __float_as_int(rk.y), pl = __float_as_int(rl.x),
+                  ql = __float_as_int(rl.y);
+        const float ck = rk.z, sk = rk.w, cl = rl.z, sl = rl.w;
         const float xpp = A[pk * ld + pl], xpq = A[pk * ld + ql], xqp = A[qk * ld + pl], xqq = A[qk * ld + ql];
         const float rpp = ck * xpp - sk * xqp, rpq = ck * xpq - sk * xqq;  // rows of pair k
         const float rqp = sk * xpp + ck * xqp, rqq = sk * xpq + ck * xqq;
-        A[pk * ld + pl] = cl * rpp - sl * rpq;  // columns of pair l
-        A[pk * ld + ql] = sl * rpp + cl * rpq;
-        A[qk * ld + pl] = cl * rqp - sl * rqq;
-        A[qk * ld + ql] = sl * rqp + cl * rqq;
+        const float npp = cl * rpp - sl * rpq, npq = sl * rpp + cl * rpq;  // columns of pair l
+        const float nqp = cl * rqp - sl * rqq, nqq = sl * rqp + cl * rqq;
+        if (k == l) {  // a diagonal block: its two off-diagonal entries are one value
+          A[pk * ld + pk] = npp;
+          A[pk * ld + qk] = npq;
+          A[qk * ld + pk] = npq;
+          A[qk * ld + qk] = nqq;
+        } else {
+          A[pk * ld + pl] = npp;
+          A[pk * ld + ql] = npq;
+          A[qk * ld + pl] = nqp;
+          A[qk * ld + ql] = nqq;
+          A[pl * ld + pk] = npp;
+          A[ql * ld + pk] = npq;
+          A[pl * ld + qk] = nqp;
+          A[ql * ld + qk] = nqq;
+        }
       }
 #pragma unroll
       for (int j = 0; j < kItV; ++j) {
         if (it_v[j] == kNone) continue;
         const int l = it_v[j] & 0xFFu, i = it_v[j] >> 8;
-        const int2 ql2 = PQ[l];
-        const float2 rl = CSN[l];
-        const int pl = ql2.x, ql = ql2.y;
-        const float cl = rl.x, sl = rl.y;
+        const float4 rl = ROT[l];
+        const int pl = __float_as_int(rl.x), ql = __float_as_int(rl.y);
+        const float cl = rl.z, sl = rl.w;
         const float vp = V[i * ld + pl], vq = V[i * ld + ql];
         V[i * ld + pl] = cl * vp - sl * vq;
         V[i * ld + ql] = sl * vp + cl * vq;
@@ -677,7 +695,7 @@ __global__ void __launch_bounds__(kRlJacThreads) rl_jacobi_kernel(const float* _
     if (!any) break;
   }
   // decreasing order (selection by one thread; s <= 128), then the permuted output
-  int* order = reinterpret_cast<int*>(PQ);  // reuse: s entries fit in the s / 2 int2
+  int* order = reinterpret_cast<int*>(ROT);  // reuse: s entries fit in the s / 2 pairs
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int i = 0; i < s; ++i) order[i] = i;
