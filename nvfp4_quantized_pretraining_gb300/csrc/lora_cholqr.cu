@@ -138,58 +138,93 @@ __global__ void __launch_bounds__(kCqrThreads) cholqr_factor_kernel(const float*
 
 // Blocks [0, ncolblocks): columns of L1 (L1' = L^-1 L1 by forward substitution, right-looking:
 // once x_i is known every later row takes its term, in the same order per row as the
-// left-looking sum but with the multiply-adds of a step independent of each other); the rest:
-// rows of L2 (L2' = L2 L, accumulated row of L by row of L, each output's terms in increasing i).
+// left-looking sum); the rest: rows of L2 (L2' = L2 L, y_j = sum_{i >= j} x_i L_ij with the
+// terms added in increasing i).  Both run a runtime loop over the R steps with the per-thread
+// values in registers that shift down by one each step (so every register index is a
+// compile-time one and the loop body stays small: a fully unrolled triangle of R^2 / 2
+// multiply-adds outgrew the instruction cache), reading each step's coefficients from a
+// zero-padded shared-memory row, 16 bytes at a time.
+constexpr int kCqrApplyThreads = 128;
+
 template <int R>
-__global__ void __launch_bounds__(kCqrThreads) cholqr_apply_kernel(
+__global__ void __launch_bounds__(kCqrApplyThreads) cholqr_apply_kernel(
     const uint16_t* L1, int64_t K, int64_t ld1, uint16_t* L1_out, const uint16_t* L2, int64_t N, uint16_t* L2_out,
-    const float* Lmat, const float* inv_diag, const int* info,
-    int ncolblocks) {
-  __shared__ __align__(16) float M[R][R + 4];
+    const float* Lmat, const float* inv_diag, const int* info, int ncolblocks) {
+  constexpr int ldl = R + 4;
+  __shared__ __align__(16) float LS[R][ldl];   // LS[i][t] = L_{i+1+t, i} (below the diagonal), 0 past R - 2 - i
+  __shared__ __align__(16) float LR[R][ldl];   // LR[i][j] = L_ij, 0 above the diagonal
   __shared__ float dinv[R];
   pdl_trigger();
   pdl_wait();
   if (*info != 0) return;
-  for (int e = threadIdx.x; e < R * R; e += blockDim.x) M[e / R][e % R] = Lmat[e];
+  for (int e = threadIdx.x; e < R * ldl; e += blockDim.x) {
+    (&LS[0][0])[e] = 0.0f;
+    (&LR[0][0])[e] = 0.0f;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < R * R; e += blockDim.x) {
+    const int i = e / R, k = e % R;
+    if (k <= i) {
+      const float v = Lmat[e];
+      LR[i][k] = v;
+      if (k < i) LS[k][i - k - 1] = v;
+    }
+  }
   if (threadIdx.x < R) dinv[threadIdx.x] = inv_diag[threadIdx.x];
   __syncthreads();
   if (static_cast<int>(blockIdx.x) < ncolblocks) {
-    const int64_t k = static_cast<int64_t>(blockIdx.x) * kCqrThreads + threadIdx.x;
+    const int64_t k = static_cast<int64_t>(blockIdx.x) * kCqrApplyThreads + threadIdx.x;
     if (k >= K) return;
-    float x[R];
+    // r[t]: the partial sum of row i + t at step i
+    float r[R];
 #pragma unroll
-    for (int c = 0; c < R; ++c) x[c] = __uint_as_float(static_cast<uint32_t>(L1[c * ld1 + k]) << 16);
-    // x <- L^-1 x in place: x_i = (x_i - sum_{c < i} L_ic x_c) / L_ii
-#pragma unroll
+    for (int c = 0; c < R; ++c) r[c] = __uint_as_float(static_cast<uint32_t>(L1[c * ld1 + k]) << 16);
     for (int i = 0; i < R; ++i) {
-      x[i] = x[i] * dinv[i];
-      L1_out[i * ld1 + k] = static_cast<uint16_t>(bf16_rn_bits(x[i]));
+      const float x = r[0] * dinv[i];
+      L1_out[i * ld1 + k] = static_cast<uint16_t>(bf16_rn_bits(x));
+      const float4* row = reinterpret_cast<const float4*>(&LS[i][0]);
 #pragma unroll
-      for (int t = i + 1; t < R; ++t) x[t] = fmaf(-M[t][i], x[i], x[t]);
+      for (int q = 0; q < R / 4; ++q) {
+        const float4 l = row[q];
+        r[4 * q] = fmaf(-l.x, x, r[4 * q + 1]);
+        r[4 * q + 1] = fmaf(-l.y, x, r[4 * q + 2]);
+        r[4 * q + 2] = fmaf(-l.z, x, r[4 * q + 3]);
+        if (4 * q + 4 < R) r[4 * q + 3] = fmaf(-l.w, x, r[4 * q + 4]);
+      }
     }
   } else {
-    const int64_t n = static_cast<int64_t>(blockIdx.x - ncolblocks) * kCqrThreads + threadIdx.x;
+    const int64_t n = static_cast<int64_t>(blockIdx.x - ncolblocks) * kCqrApplyThreads + threadIdx.x;
     if (n >= N) return;
-    float x[R];
-    const uint4* row = reinterpret_cast<const uint4*>(L2 + n * R);
+    // xr[t] = x_{i + t} at step i
+    float xr[R];
+    const uint4* src = reinterpret_cast<const uint4*>(L2 + n * R);
 #pragma unroll
     for (int q = 0; q < R / 8; ++q) {
-      const uint4 w = row[q];
+      const uint4 w = src[q];
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        x[8 * q + 2 * h] = __uint_as_float(ws[h] << 16);
-        x[8 * q + 2 * h + 1] = __uint_as_float(ws[h] & 0xFFFF0000u);
+        xr[8 * q + 2 * h] = __uint_as_float(ws[h] << 16);
+        xr[8 * q + 2 * h + 1] = __uint_as_float(ws[h] & 0xFFFF0000u);
       }
     }
-    // y_j = sum_{i >= j} x_i L_ij, the terms added in increasing i
     float y[R];
 #pragma unroll
     for (int j = 0; j < R; ++j) y[j] = 0.0f;
-#pragma unroll
     for (int i = 0; i < R; ++i) {
+      const float xi = xr[0];
+      const float4* row = reinterpret_cast<const float4*>(&LR[i][0]);
+      // L_ij = 0 for j > i: those y_j stay +0 until their first term (i = j)
 #pragma unroll
-      for (int j = 0; j <= i; ++j) y[j] = fmaf(x[i], M[i][j], y[j]);
+      for (int q = 0; q < R / 4; ++q) {
+        const float4 l = row[q];
+        y[4 * q] = fmaf(xi, l.x, y[4 * q]);
+        y[4 * q + 1] = fmaf(xi, l.y, y[4 * q + 1]);
+        y[4 * q + 2] = fmaf(xi, l.z, y[4 * q + 2]);
+        y[4 * q + 3] = fmaf(xi, l.w, y[4 * q + 3]);
+      }
+#pragma unroll
+      for (int t = 0; t + 1 < R; ++t) xr[t] = xr[t + 1];
     }
     uint4* out = reinterpret_cast<uint4*>(L2_out + n * R);
 #pragma unroll
@@ -224,9 +259,9 @@ static cudaError_t cholqr_launch(const void* L1, int64_t K, int64_t ld1, const v
                  Lmat, inv_diag, info);
   count_launch();
   if (e != cudaSuccess) return e;
-  const int colblocks = static_cast<int>((K + kCqrThreads - 1) / kCqrThreads);
-  const int rowblocks = static_cast<int>((N + kCqrThreads - 1) / kCqrThreads);
-  e = launch_pdl(cholqr_apply_kernel<R>, dim3(colblocks + rowblocks), dim3(kCqrThreads), 0, s,
+  const int colblocks = static_cast<int>((K + kCqrApplyThreads - 1) / kCqrApplyThreads);
+  const int rowblocks = static_cast<int>((N + kCqrApplyThreads - 1) / kCqrApplyThreads);
+  e = launch_pdl(cholqr_apply_kernel<R>, dim3(colblocks + rowblocks), dim3(kCqrApplyThreads), 0, s,
                  static_cast<const uint16_t*>(L1), K, ld1, static_cast<uint16_t*>(L1_out),
                  static_cast<const uint16_t*>(L2), N, static_cast<uint16_t*>(L2_out), static_cast<const float*>(Lmat),
                  static_cast<const float*>(inv_diag), static_cast<const int*>(info), colblocks);
