@@ -221,9 +221,9 @@ fp4_status fp4_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx,
  * reduces into (the amax slot) before use and overwrites the rest.
  * The first call on each device looks the buffer's address up
  * (cudaGetSymbolAddress, which can load the module) and caches it for the
- * life of the process; make that first call on each device before any stream
- * capture begins.  cudaDeviceReset unloads the module and leaves the cached
- * address stale: do not use this call after resetting a device it has run on.
+ * life of the process.  cudaDeviceReset unloads the module and leaves the
+ * cached address stale: do not use this call after resetting a device it has
+ * run on.
  * All calls on one device share the one buffer: calls whose executions can
  * overlap (unordered streams, several host threads) race on it and give wrong
  * results.  Order them (one stream, or events). */
