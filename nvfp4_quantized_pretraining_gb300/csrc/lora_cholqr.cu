@@ -40,10 +40,19 @@ __global__ void __launch_bounds__(kCqrThreads) cholqr_gram_kernel(const uint16_t
   const int64_t step = static_cast<int64_t>(gridDim.x) * kCqrChunk;
   for (int64_t k0 = static_cast<int64_t>(blockIdx.x) * kCqrChunk; k0 < K; k0 += step) {
     __syncthreads();  // the previous chunk's reads are done
-    for (int e = threadIdx.x; e < R * kCqrChunk; e += kCqrThreads) {
-      const int row = e / kCqrChunk, col = e % kCqrChunk;
-      const int64_t k = k0 + col;
-      tile[row][col] = k < K ? __uint_as_float(static_cast<uint32_t>(L1[row * ld + k]) << 16) : 0.0f;
+    // a fixed trip count, unrolled: every load of the chunk is in flight before the first store
+    static_assert(R * kCqrChunk % kCqrThreads == 0, "whole loads per thread");
+    uint16_t v[R * kCqrChunk / kCqrThreads];
+#pragma unroll
+    for (int u = 0; u < R * kCqrChunk / kCqrThreads; ++u) {
+      const int e = threadIdx.x + u * kCqrThreads;
+      const int64_t k = k0 + e % kCqrChunk;
+      v[u] = k < K ? L1[(e / kCqrChunk) * ld + k] : static_cast<uint16_t>(0);
+    }
+#pragma unroll
+    for (int u = 0; u < R * kCqrChunk / kCqrThreads; ++u) {
+      const int e = threadIdx.x + u * kCqrThreads;
+      tile[e / kCqrChunk][e % kCqrChunk] = __uint_as_float(static_cast<uint32_t>(v[u]) << 16);
     }
     __syncthreads();
     if (i < R) {
